@@ -1,0 +1,375 @@
+"""Benchmark of the sparse MXFP4 decode step on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl smx|reference] [--config 2]
+
+One step = the whole hot path (insert, q pack, index score of every page, top-k, split-K
+attention, merge) on the fixed 7-draft verify workload (B=4 rows x Q=8 query tokens, 16 query
+heads on 1 KV head, 16384-token contexts = 128 pages, top-k 16) by default. The metric is
+achieved HBM GB/s of the algorithmic bytes (every index page of each row + the K and V pages
+of the selected set) per step; microseconds per step are reported too.
+
+The timed K steps are replayed from one CUDA graph; every step reads a different copy of the
+three page pools, with enough copies that their bytes exceed 3x the L2 cache, so each step reads
+from HBM. N > 1 (torchrun) runs N independent replicas (the path has no exchange step); value is
+the bytes of all ranks over the slowest rank's time.
+
+The reference arm (--impl reference) is the CPU oracle timed on this host's cores on a bounded
+sample of the same workload (one batch row per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from sparse_attention_decode_mxfp4_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "sparse MXFP4 decode step: µs/step and achieved HBM GB/s vs GB300 peak"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="smx", choices=["smx", "reference"])
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--splits", type=int, default=0, help="partitions of the split stage (0 = workload's)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    return ap.parse_args()
+
+
+def algorithmic_bytes(w, ctx_len):
+    n_pages = [(int(c) + 127) // 128 for c in ctx_len]
+    idx = sum(n * wl.MXFP4_PAGE_BYTES for n in n_pages)
+    kv = sum(min(w.topk, n) * 2 * w.Hkv * w.kv_page_bytes for n in n_pages)
+    return idx, kv
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_sources_sha():
+    h = hashlib.sha256()
+    for f in ("smx_index.cu", "smx_device.cuh"):
+        h.update(open(os.path.join(ROOT, "sparse_attention_decode_mxfp4_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name):
+    """DRAM bytes per launch of the index scorer from a committed ncu summary, if it was taken
+    on the current kernel source and this workload; else None."""
+    p = os.path.join(ROOT, "profiles", "index_score_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    if d.get("kernel_sources_sha") != kernel_sources_sha() or d.get("workload") != workload_name:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = None
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        self.gpu = vis.split(",")[device_index] if vis else str(device_index)
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", self.gpu], stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------------------------
+def run_reference(args):
+    """The CPU oracle as it stands, one batch row of the workload per step, all host cores."""
+    import oracle
+    w = wl.config(args.config)
+    data = wl.generate(w)
+    rows = [wl.shrink(w, B=1, ctx_lens=(int(data["ctx_len"][b]),), name=w.name + f"_row{b}") for b in range(w.B)]
+    samples = []
+    for b, wb in enumerate(rows):
+        db = {k: (v[b:b + 1] if isinstance(v, np.ndarray) and v.ndim >= 1 and v.shape[0] == w.B else v)
+              for k, v in data.items()}
+        db["page_table"] = np.arange(wb.max_pages, dtype=np.int32)[None]
+        pools = wl.empty_pools(wb)
+        sh = oracle.shape_of(wb)
+        oracle.kv_fill(sh, db["k"], db["v"], db["kidx"], db["page_table"], db["n_hist"], *pools)
+        samples.append((wb, sh, db, pools))
+    idx_b, kv_b = algorithmic_bytes(w, data["ctx_len"])
+    per_row = (idx_b + kv_b) / w.B
+
+    def one(i):
+        wb, sh, db, pools = samples[i % len(samples)]
+        oracle.decode_step(sh, q_f32=db["q"], q_bf16=db["q_bf16"], qidx_bf16=db["qidx_bf16"], k_new=db["k_new"],
+                           v_new=db["v_new"], kidx_new=db["kidx_new"], page_table=db["page_table"],
+                           ctx_len=db["ctx_len"], k_pool=pools[0], v_pool=pools[1], idx_pool=pools[2])
+
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one(i)
+    dt = time.perf_counter() - t0
+    value = per_row * args.steps / dt / 1e9
+    cores = oracle.max_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": dict(w.describe(), sample="one batch row per step (rows cycled)", parallelism="replicas"),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": "one batch row of the workload per step, rows cycled"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w, data, step_bytes):
+    """Oracle on this host's cores: whole steps of the same workload, repeated for ~10 s."""
+    import oracle
+    from oracle import shape_of
+    pools = wl.empty_pools(w)
+    sh = shape_of(w)
+    oracle.kv_fill(sh, data["k"], data["v"], data["kidx"], data["page_table"], data["n_hist"], *pools)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode_step(sh, q_f32=data["q"], q_bf16=data["q_bf16"], qidx_bf16=data["qidx_bf16"],
+                           k_new=data["k_new"], v_new=data["v_new"], kidx_new=data["kidx_new"],
+                           page_table=data["page_table"], ctx_len=data["ctx_len"], k_pool=pools[0],
+                           v_pool=pools[1], idx_pool=pools[2])
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt > 10.0 or reps >= 20:
+            break
+    return {"value": step_bytes * reps / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
+            "kind": "oracle", "sample": f"{reps} whole steps of the workload ({dt:.1f} s)",
+            "us_per_step": dt / reps * 1e6}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+    import torch.distributed as dist
+    from sparse_attention_decode_mxfp4_gb300 import build as smx_build
+    from sparse_attention_decode_mxfp4_gb300 import ops
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    smx_build.build()
+    w = wl.config(args.config)
+    shape = ops.Shape.of(w, args.splits or None)
+    data = wl.generate(w)
+    idx_b, kv_b = algorithmic_bytes(w, data["ctx_len"])
+    step_bytes = idx_b + kv_b
+
+    def T(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    page_table, ctx_len = T(data["page_table"]), T(data["ctx_len"])
+    base = tuple(torch.zeros(p.shape, dtype=torch.uint8, device=dev) for p in wl.empty_pools(w))
+    ops.kv_prefill(shape, T(data["k"]), T(data["v"]), T(data["kidx"]), page_table, T(data["n_hist"]), *base)
+    torch.cuda.synchronize()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    pool_bytes = sum(p.numel() for p in base)
+    R = max(2, math.ceil(3 * l2 / step_bytes))
+    copies = [tuple(p.clone() for p in base) for _ in range(R)]
+    del base
+    inp = dict(q_f32=T(data["q"]) if w.kv_format == wl.KV_MXFP4 else None,
+               q_bf16=T(data["q_bf16"].view(np.int16)) if w.kv_format == wl.KV_E4M3_ROWSCALE else None,
+               qidx_bf16=T(data["qidx_bf16"].view(np.int16)), k_new=T(data["k_new"]), v_new=T(data["v_new"]),
+               kidx_new=T(data["kidx_new"]))
+    out = torch.empty((w.B, w.Q, w.Hq, 128), dtype=torch.float32, device=dev)
+    topk_pages = torch.empty((w.B, w.topk), dtype=torch.int32, device=dev)
+    topk_count = torch.empty((w.B,), dtype=torch.int32, device=dev)
+    workspace = ops.alloc_workspace(shape, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(i, pt=page_table, cl=ctx_len, io=inp, o=out):
+        kp, vp, ip = copies[i % R]
+        ops.decode_step(shape, **io, page_table=pt, ctx_len=cl, k_pool=kp, v_pool=vp, idx_pool=ip,
+                        topk_pages=topk_pages, topk_count=topk_count, out=o, workspace=workspace,
+                        dev_status=status)
+
+    step(0)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    g_warm, g_timed = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g_warm, stream=s):
+            for i in range(max(3, args.warmup)):
+                step(i)
+        with torch.cuda.graph(g_timed, stream=s):
+            for i in range(args.steps):
+                step(i)
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps from one graph replay ----
+    g_warm.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    g_timed.replay()
+    e1.record(cur)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    assert status.item() == 0, f"device status {status.item()}"
+    us_step = ms * 1e3 / args.steps
+    value = step_bytes * world * args.steps / (ms * 1e-3) / 1e9
+
+    # ---- dominant kernel (index scorer) alone, same rotation, CUDA events on its stream ----
+    scores = torch.empty((w.B, w.max_pages), dtype=torch.float32, device=dev)
+    g_idx = torch.cuda.CUDAGraph()
+    n_idx = args.steps
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g_idx, stream=s):
+            for i in range(n_idx):
+                ops.index_score(shape, inp["qidx_bf16"], copies[i % R][2], page_table, ctx_len, scores)
+    g_idx.replay()
+    torch.cuda.synchronize()
+    e0.record(cur)
+    g_idx.replay()
+    e1.record(cur)
+    e1.synchronize()
+    idx_us = e0.elapsed_time(e1) * 1e3 / n_idx
+    peak, peak_kind = peaks()
+    achieved = idx_b / (idx_us * 1e-6) / 1e9
+
+    # ---- end to end through the public API: pinned host inputs in, output back, every step ----
+    host_in = {k: v.cpu().pin_memory() for k, v in inp.items() if v is not None}
+    host_in["page_table"], host_in["ctx_len"] = page_table.cpu().pin_memory(), ctx_len.cpu().pin_memory()
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step(i):
+        for k in dev_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        io = {k: (dev_in[k] if v is not None else None) for k, v in inp.items()}
+        step(i, pt=dev_in["page_table"], cl=dev_in["ctx_len"], io=io)
+        host_out.copy_(out, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.e2e_steps):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / args.e2e_steps
+    e2e_val = step_bytes * world / e2e_s / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, data, step_bytes)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": us_step / 1e3, "us_per_step": us_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded N(0,1) rows quantised on the GPU; BASELINE workload shapes)",
+            "config": dict(w.describe(), num_splits=shape.num_splits, bytes_per_step=step_bytes,
+                           index_bytes=idx_b, kv_bytes=kv_b, parallelism="replicas" if world > 1 else "single",
+                           l2=f"rotating {R} pool copies ({R * pool_bytes / 1e6:.0f} MB, reads "
+                              f"{R * step_bytes / 1e6:.0f} MB per rotation > 3x L2 {l2 / 1e6:.0f} MB)"),
+            "roofline": {"bound": "hbm", "kernel": "index_score_kernel", "achieved": achieved, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": recorded_traffic(w.name), "us_per_launch": idx_us,
+                         "algorithmic_bytes_per_launch": idx_b},
+            "step_roofline_frac": value / world / peak,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": "GB/s", "us_per_step": e2e_s * 1e6, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": ops.decode_step_launches(shape) * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

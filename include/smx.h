@@ -1,0 +1,174 @@
+/*
+ * smx.h -- C ABI of libsmx: the sparse MXFP4 attention decode step on GB300 (sm_103a).
+ *
+ * One decode step over a paged, block-scaled KV cache, as described on
+ *   [ATOM-2812] ROCm/ATOM PR 2812 "Mono decode over the MXFP4 KV and index caches"
+ *               (commit messages "--index-cache-dtype mxfp4", "MXFP4 main KV",
+ *               "e4m3 q_out convention", "pack_q_e4m3");
+ *   [ATOM-2686] ROCm/ATOM PR 2686 "Enable Mono decode with fixed DSpark verify" (Summary:
+ *               fixed 7-draft verify = 8 query tokens per row, FP8 KV cache).
+ * The step: insert the new tokens' index-K, K and V rows into their pages (a1); pack q to
+ * saturating e4m3 (a2); score every page of each row with the index query (a3); select the
+ * top-k pages (a4); split-K attention over the selected pages (a5); merge the partials (a6).
+ *
+ * Conventions for every entry point
+ *  - All array pointers are DEVICE pointers owned by the caller; nothing is allocated, freed
+ *    or synchronised. Work is enqueued on `stream` (NULL = the legacy default stream) and
+ *    runs asynchronously; the return code reports argument checks and launch errors only.
+ *  - Return 0 (SMX_OK) or a negative SMX_ERR_* code; nothing is launched when an argument
+ *    check fails. Host-side checks never read device memory.
+ *  - `dev_status` (nullable) is a device int32 that kernels OR SMX_DEV_* bits into when
+ *    device-resident indices are out of range; the offending page/row is skipped (an index
+ *    page scores -inf, an attention page contributes nothing), so a bad table can never make
+ *    a kernel read or write outside the pools. The caller clears it.
+ *  - D (head dim) = Di (index dim) = 128 and page_tokens = 128 are the only supported values.
+ *
+ * Shapes and layouts (row-major, C order):
+ *   q_f32     [B][Q][Hq][128] float        q_bf16   [B][Q][Hq][128] bf16 bits (uint16)
+ *   qidx_bf16 [B][Q][128] bf16 bits        k_new, v_new [B][Q][Hkv][128] float
+ *   kidx_new  [B][Q][128] float            page_table [B][max_pages_per_row] int32 (physical ids)
+ *   ctx_len   [B] int32: tokens of the row INCLUDING the Q new ones; query token t sits at
+ *             position pos_t = ctx_len - Q + t (causal within the Q draft tokens).
+ *   k_pool, v_pool [n_pool_pages][Hkv][kv_page_bytes] uint8; idx_pool [n_pool_pages][8704] uint8
+ *   MXFP4 page (8704 B): bytes [0,8192) = 128 token rows x 64 B of E2M1 nibbles (element 2i
+ *             in the low nibble of byte i); bytes [8192,8704) = 128 rows x 4 E8M0 group scales
+ *             (group g of slot s at 8192 + 4s + g), one scale per 32 elements.
+ *   E4M3 row-scale page (16896 B): 128 rows x 128 e4m3 codes, then 128 fp32 row scales.
+ *   topk_pages [B][topk] int32: selected LOGICAL page ids, ascending, padded with -1;
+ *   topk_count [B] int32: k_eff = min(topk, ceil(ctx_len/128)).
+ *   part_o [B][S][Q][Hq][128] float (unnormalised), part_m, part_l [B][S][Q][Hq] float;
+ *   m is a maximum of z*log2(e) (log2 domain), z = q.k / sqrt(128).
+ *   out [B][Q][Hq][128] float.
+ */
+#ifndef SMX_H
+#define SMX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* smx_stream_t; /* the same type as cudaStream_t */
+
+enum {
+    SMX_OK = 0,
+    SMX_ERR_INVALID_ARG = -1,  /* null pointer, non-positive size, Hq % Hkv != 0, ... */
+    SMX_ERR_UNSUPPORTED = -2,  /* D, Di or page_tokens != 128, Q > 16, unknown kv_format */
+    SMX_ERR_CUDA = -3,         /* a kernel launch failed (cudaGetLastError) */
+    SMX_ERR_WORKSPACE = -4     /* workspace pointer null or smaller than smx_workspace_bytes */
+};
+
+enum { SMX_KV_MXFP4 = 0, SMX_KV_E4M3_ROWSCALE = 1 };
+
+/* device status bits */
+enum {
+    SMX_DEV_BAD_PAGE_ID = 1,   /* a page-table entry outside [0, n_pool_pages) was met */
+    SMX_DEV_BAD_CTX = 2,       /* ctx_len outside [Q, max_pages_per_row * 128] (row clamped) */
+    SMX_DEV_BAD_TOPK = 4       /* a selected page id outside [0, ceil(ctx_len/128)) */
+};
+
+#define SMX_MXFP4_PAGE_BYTES 8704
+#define SMX_E4M3RS_PAGE_BYTES 16896
+#define SMX_MAX_Q 16
+#define SMX_MAX_TOPK 4096
+#define SMX_MAX_PAGES_PER_ROW (1 << 20)
+
+typedef struct {
+    int32_t B;                  /* rows (sequences) in the step */
+    int32_t Q;                  /* query (draft) tokens per row, 1..16 ([ATOM-2812]: 16-token limit) */
+    int32_t Hq;                 /* query heads */
+    int32_t Hkv;                /* KV heads, Hq % Hkv == 0 */
+    int32_t D;                  /* head dim, must be 128 */
+    int32_t Di;                 /* index dim (one index head), must be 128 */
+    int32_t page_tokens;        /* must be 128 (one selected block = one page) */
+    int32_t max_pages_per_row;  /* page-table width */
+    int64_t n_pool_pages;       /* physical pages in each pool */
+    int32_t topk;               /* k pages selected per row */
+    int32_t num_splits;         /* S partitions of the selected list for the split stage */
+    int32_t kv_format;          /* SMX_KV_*: K/V page format; the index pool is always MXFP4 */
+} smx_shape_t;
+
+/* Bytes of device workspace smx_decode_step needs for this shape (page scores, packed q,
+ * split partials, alignment padding). */
+size_t smx_workspace_bytes(const smx_shape_t* shape);
+
+/* a1 -- [ATOM-2812] "--index-cache-dtype mxfp4" (index-K row store: E8M0 group scale =
+ * 2^(floor(log2 amax) - 2), E2M1 round-to-nearest-even, saturating at 6, sign kept on zero;
+ * a group holding NaN/Inf gets scale 0xFF and zero nibbles) and "MXFP4 main KV" (K and V with
+ * the same row store). With kv_format == SMX_KV_E4M3_ROWSCALE, K and V rows are written as
+ * e4m3 codes of x / s with s = fl32(amax / 448) (s = 1 when amax = 0) and the index row stays
+ * MXFP4. Writes the Q new tokens of every row at positions ctx_len - Q + t. */
+int smx_kv_insert(const smx_shape_t* shape, const float* k_new, const float* v_new,
+                  const float* kidx_new, const int32_t* page_table, const int32_t* ctx_len,
+                  uint8_t* k_pool, uint8_t* v_pool, uint8_t* idx_pool, int32_t* dev_status,
+                  smx_stream_t stream);
+
+/* Bulk form of smx_kv_insert for prompts: positions [0, n_fill[b]) of row b, read from dense
+ * k, v [B][T][Hkv][128] and kidx [B][T][128] (T = token stride, n_fill[b] <= T). Same row
+ * store as smx_kv_insert. shape->Q is ignored. */
+int smx_kv_prefill(const smx_shape_t* shape, const float* k, const float* v, const float* kidx,
+                   int64_t T, const int32_t* page_table, const int32_t* n_fill,
+                   uint8_t* k_pool, uint8_t* v_pool, uint8_t* idx_pool, int32_t* dev_status,
+                   smx_stream_t stream);
+
+/* a2 -- [ATOM-2812] "e4m3 q_out convention" / "pack_q_e4m3": n floats to e4m3 bytes at unit
+ * scale; in range = round to nearest even (torch's e4m3 cast), |x| > 448 and +-inf saturate to
+ * +-448, NaN gives 0x7F. */
+int smx_pack_q_e4m3(const float* q, uint8_t* q_e4m3, int64_t n, smx_stream_t stream);
+
+/* a3 alone -- the page scores of smx_index_score_topk without the selection. */
+int smx_index_score(const smx_shape_t* shape, const uint16_t* qidx_bf16, const uint8_t* idx_pool,
+                    const int32_t* page_table, const int32_t* ctx_len, float* page_scores,
+                    int32_t* dev_status, smx_stream_t stream);
+
+/* a3 + a4 -- [ATOM-2812] "--index-cache-dtype mxfp4" (the scorer reads the MXFP4 index pages
+ * with the bf16 index query) and "MXFP4 main KV" (the selected blocks fill the sparse table).
+ * page_scores[b][p] = max over query tokens t and tokens j of page p with j <= pos_t of
+ * qidx[b][t] . kidx[j] (fp32 accumulation; -inf for p >= ceil(ctx_len/128); NaN token scores
+ * are left out). Then the k_eff largest pages per row, ties to the lower page id, NaN last.
+ * page_scores [B][max_pages_per_row] float is an output the caller provides. */
+int smx_index_score_topk(const smx_shape_t* shape, const uint16_t* qidx_bf16,
+                         const uint8_t* idx_pool, const int32_t* page_table,
+                         const int32_t* ctx_len, float* page_scores, int32_t* topk_pages,
+                         int32_t* topk_count, int32_t* dev_status, smx_stream_t stream);
+
+/* a5 -- [ATOM-2812] "MXFP4 main KV": split stage. Partition s of S covers positions
+ * [floor(s k_eff / S), floor((s+1) k_eff / S)) of the ascending selected list; for each query
+ * (b, t, h) with KV head h / (Hq / Hkv) it keeps m = max z log2(e), l = sum 2^(z log2 e - m)
+ * and o = sum 2^(z log2 e - m) V_j over tokens j of its pages with j <= pos_t. An empty
+ * partition writes m = -inf, l = 0, o = 0. q is the packed e4m3 bytes (MXFP4 K/V) or bf16
+ * bits (E4M3 row-scale K/V, [ATOM-2812] "e4m3 q_out convention": fp8-KV keeps bf16 q). */
+int smx_sparse_attn_split(const smx_shape_t* shape, const void* q, const uint8_t* k_pool,
+                          const uint8_t* v_pool, const int32_t* page_table,
+                          const int32_t* ctx_len, const int32_t* topk_pages,
+                          const int32_t* topk_count, float* part_o, float* part_m,
+                          float* part_l, int32_t* dev_status, smx_stream_t stream);
+
+/* a6 -- [ATOM-2812] "MXFP4 main KV": merge. out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s
+ * with M = max_s m_s; out = 0 when every partition is empty. */
+int smx_sparse_attn_merge(const smx_shape_t* shape, const float* part_o, const float* part_m,
+                          const float* part_l, float* out, smx_stream_t stream);
+
+/* The whole step (a1..a6) on `stream`. q_f32 is required for MXFP4 K/V, q_bf16 for E4M3
+ * row-scale K/V (the other may be NULL). Pools are updated in place (the Q new rows).
+ * topk_pages/topk_count are outputs; workspace holds ws_bytes >= smx_workspace_bytes(shape)
+ * bytes of scratch (256-byte aligned). */
+int smx_decode_step(const smx_shape_t* shape, const float* q_f32, const uint16_t* q_bf16,
+                    const uint16_t* qidx_bf16, const float* k_new, const float* v_new,
+                    const float* kidx_new, const int32_t* page_table, const int32_t* ctx_len,
+                    uint8_t* k_pool, uint8_t* v_pool, uint8_t* idx_pool, int32_t* topk_pages,
+                    int32_t* topk_count, float* out, void* workspace, size_t ws_bytes,
+                    int32_t* dev_status, smx_stream_t stream);
+
+/* Static text for a status code. */
+const char* smx_status_string(int status);
+
+/* Number of kernel launches smx_decode_step enqueues for this shape. */
+int smx_decode_step_launches(const smx_shape_t* shape);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SMX_H */

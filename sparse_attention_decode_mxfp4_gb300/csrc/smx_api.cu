@@ -1,0 +1,242 @@
+// smx_api.cu -- the C ABI of libsmx (declared in include/smx.h): argument checks, workspace
+// layout and the order of launches. No device memory is read, allocated or synchronised here.
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "smx_internal.h"
+
+namespace smx {
+
+cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
+    constexpr int kMaxDev = 64, kMaxKernels = 8;
+    static std::mutex mu;
+    static const void* seen_kernel[kMaxKernels] = {};
+    static int seen_bytes[kMaxKernels][kMaxDev] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    std::lock_guard<std::mutex> lock(mu);
+    int slot = -1;
+    for (int i = 0; i < kMaxKernels; ++i) {
+        if (seen_kernel[i] == kernel || seen_kernel[i] == nullptr) {
+            slot = i;
+            break;
+        }
+    }
+    if (slot < 0) return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    seen_kernel[slot] = kernel;
+    if (seen_bytes[slot][dev] >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) seen_bytes[slot][dev] = bytes;
+    return e;
+}
+
+}  // namespace smx
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(const smx_shape_t* s) {
+    if (!s) return SMX_ERR_INVALID_ARG;
+    if (s->B < 1 || s->Q < 1 || s->Hq < 1 || s->Hkv < 1 || s->max_pages_per_row < 1 ||
+        s->n_pool_pages < 1 || s->topk < 1 || s->num_splits < 1)
+        return SMX_ERR_INVALID_ARG;
+    if (s->Hq % s->Hkv != 0) return SMX_ERR_INVALID_ARG;
+    if (s->D != 128 || s->Di != 128 || s->page_tokens != 128) return SMX_ERR_UNSUPPORTED;
+    if (s->Q > SMX_MAX_Q) return SMX_ERR_UNSUPPORTED;
+    if (s->kv_format != SMX_KV_MXFP4 && s->kv_format != SMX_KV_E4M3_ROWSCALE) return SMX_ERR_UNSUPPORTED;
+    if (s->topk > SMX_MAX_TOPK || s->max_pages_per_row > SMX_MAX_PAGES_PER_ROW) return SMX_ERR_UNSUPPORTED;
+    if (s->B > 65535 || s->num_splits > 65535 || (int64_t)s->Hkv * s->Hq * s->Q > 65535)
+        return SMX_ERR_UNSUPPORTED;
+    return SMX_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? SMX_OK : SMX_ERR_CUDA; }
+
+struct Workspace {
+    float* scores;
+    uint8_t* q8;
+    float* part_o;
+    float* part_m;
+    float* part_l;
+    size_t bytes;
+};
+
+Workspace layout(const smx_shape_t* s, void* base) {
+    Workspace w;
+    uint8_t* p = reinterpret_cast<uint8_t*>(base);
+    size_t off = 0;
+    const size_t rows = (size_t)s->B * s->num_splits * s->Q * s->Hq;
+    w.scores = reinterpret_cast<float*>(p + off);
+    off = align_up(off + (size_t)s->B * s->max_pages_per_row * sizeof(float));
+    w.q8 = p + off;
+    off = align_up(off + (size_t)s->B * s->Q * s->Hq * 128);
+    w.part_o = reinterpret_cast<float*>(p + off);
+    off = align_up(off + rows * 128 * sizeof(float));
+    w.part_m = reinterpret_cast<float*>(p + off);
+    off = align_up(off + rows * sizeof(float));
+    w.part_l = reinterpret_cast<float*>(p + off);
+    off = align_up(off + rows * sizeof(float));
+    w.bytes = off;
+    return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t smx_workspace_bytes(const smx_shape_t* shape) {
+    if (check_shape(shape) != SMX_OK) return 0;
+    return layout(shape, nullptr).bytes;
+}
+
+int smx_kv_insert(const smx_shape_t* s, const float* k_new, const float* v_new, const float* kidx_new,
+                  const int32_t* page_table, const int32_t* ctx_len, uint8_t* k_pool, uint8_t* v_pool,
+                  uint8_t* idx_pool, int32_t* dev_status, smx_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (!k_new || !v_new || !kidx_new || !page_table || !ctx_len || !k_pool || !v_pool || !idx_pool)
+        return SMX_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(kidx_new) || !aligned16(k_pool) ||
+        !aligned16(v_pool) || !aligned16(idx_pool))
+        return SMX_ERR_INVALID_ARG;
+    return cuda_status(smx::launch_kv_insert(*s, k_new, v_new, kidx_new, s->Q, page_table, ctx_len, nullptr,
+                                             k_pool, v_pool, idx_pool, dev_status, false, (cudaStream_t)stream));
+}
+
+int smx_kv_prefill(const smx_shape_t* s, const float* k, const float* v, const float* kidx, int64_t T,
+                   const int32_t* page_table, const int32_t* n_fill, uint8_t* k_pool, uint8_t* v_pool,
+                   uint8_t* idx_pool, int32_t* dev_status, smx_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (!k || !v || !kidx || !page_table || !n_fill || !k_pool || !v_pool || !idx_pool || T < 1)
+        return SMX_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(kidx) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        !aligned16(idx_pool))
+        return SMX_ERR_INVALID_ARG;
+    return cuda_status(smx::launch_kv_insert(*s, k, v, kidx, T, page_table, nullptr, n_fill, k_pool, v_pool,
+                                             idx_pool, dev_status, true, (cudaStream_t)stream));
+}
+
+int smx_pack_q_e4m3(const float* q, uint8_t* q_e4m3, int64_t n, smx_stream_t stream) {
+    if (!q || !q_e4m3 || n < 1) return SMX_ERR_INVALID_ARG;
+    if (!aligned16(q) || (reinterpret_cast<uintptr_t>(q_e4m3) & 3u)) return SMX_ERR_INVALID_ARG;
+    return cuda_status(smx::launch_pack_q(q, q_e4m3, n, (cudaStream_t)stream));
+}
+
+int smx_index_score(const smx_shape_t* s, const uint16_t* qidx_bf16, const uint8_t* idx_pool,
+                    const int32_t* page_table, const int32_t* ctx_len, float* page_scores, int32_t* dev_status,
+                    smx_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (!qidx_bf16 || !idx_pool || !page_table || !ctx_len || !page_scores) return SMX_ERR_INVALID_ARG;
+    if (!aligned16(qidx_bf16) || !aligned16(idx_pool)) return SMX_ERR_INVALID_ARG;
+    return cuda_status(smx::launch_index_scores(*s, qidx_bf16, idx_pool, page_table, ctx_len, page_scores,
+                                                dev_status, (cudaStream_t)stream));
+}
+
+int smx_index_score_topk(const smx_shape_t* s, const uint16_t* qidx_bf16, const uint8_t* idx_pool,
+                         const int32_t* page_table, const int32_t* ctx_len, float* page_scores,
+                         int32_t* topk_pages, int32_t* topk_count, int32_t* dev_status, smx_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (!qidx_bf16 || !idx_pool || !page_table || !ctx_len || !page_scores || !topk_pages || !topk_count)
+        return SMX_ERR_INVALID_ARG;
+    if (!aligned16(qidx_bf16) || !aligned16(idx_pool)) return SMX_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = smx::launch_index_scores(*s, qidx_bf16, idx_pool, page_table, ctx_len, page_scores,
+                                             dev_status, st);
+    if (e != cudaSuccess) return SMX_ERR_CUDA;
+    return cuda_status(smx::launch_topk(*s, page_scores, ctx_len, topk_pages, topk_count, st));
+}
+
+int smx_sparse_attn_split(const smx_shape_t* s, const void* q, const uint8_t* k_pool, const uint8_t* v_pool,
+                          const int32_t* page_table, const int32_t* ctx_len, const int32_t* topk_pages,
+                          const int32_t* topk_count, float* part_o, float* part_m, float* part_l,
+                          int32_t* dev_status, smx_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (!q || !k_pool || !v_pool || !page_table || !ctx_len || !topk_pages || !topk_count || !part_o ||
+        !part_m || !part_l)
+        return SMX_ERR_INVALID_ARG;
+    if (!aligned16(k_pool) || !aligned16(v_pool) || (reinterpret_cast<uintptr_t>(q) & 3u) ||
+        (reinterpret_cast<uintptr_t>(part_o) & 7u))
+        return SMX_ERR_INVALID_ARG;
+    return cuda_status(smx::launch_attn_split(*s, q, k_pool, v_pool, page_table, ctx_len, topk_pages, topk_count,
+                                              part_o, part_m, part_l, dev_status, (cudaStream_t)stream));
+}
+
+int smx_sparse_attn_merge(const smx_shape_t* s, const float* part_o, const float* part_m, const float* part_l,
+                          float* out, smx_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (!part_o || !part_m || !part_l || !out) return SMX_ERR_INVALID_ARG;
+    return cuda_status(smx::launch_attn_merge(*s, part_o, part_m, part_l, out, (cudaStream_t)stream));
+}
+
+int smx_decode_step(const smx_shape_t* s, const float* q_f32, const uint16_t* q_bf16, const uint16_t* qidx_bf16,
+                    const float* k_new, const float* v_new, const float* kidx_new, const int32_t* page_table,
+                    const int32_t* ctx_len, uint8_t* k_pool, uint8_t* v_pool, uint8_t* idx_pool,
+                    int32_t* topk_pages, int32_t* topk_count, float* out, void* workspace, size_t ws_bytes,
+                    int32_t* dev_status, smx_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    const bool rs = s->kv_format == SMX_KV_E4M3_ROWSCALE;
+    if ((rs ? (const void*)q_bf16 : (const void*)q_f32) == nullptr) return SMX_ERR_INVALID_ARG;
+    if (!qidx_bf16 || !k_new || !v_new || !kidx_new || !page_table || !ctx_len || !k_pool || !v_pool ||
+        !idx_pool || !topk_pages || !topk_count || !out)
+        return SMX_ERR_INVALID_ARG;
+    if (!rs && !aligned16(q_f32)) return SMX_ERR_INVALID_ARG;
+    if (rs && (reinterpret_cast<uintptr_t>(q_bf16) & 3u)) return SMX_ERR_INVALID_ARG;
+    if (!aligned16(qidx_bf16) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(kidx_new) ||
+        !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(idx_pool))
+        return SMX_ERR_INVALID_ARG;
+    const size_t need = layout(s, nullptr).bytes;
+    if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+        return SMX_ERR_WORKSPACE;
+    const Workspace w = layout(s, workspace);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (smx::launch_kv_insert(*s, k_new, v_new, kidx_new, s->Q, page_table, ctx_len, nullptr, k_pool, v_pool,
+                              idx_pool, dev_status, false, st) != cudaSuccess)
+        return SMX_ERR_CUDA;
+    const void* qa = q_bf16;
+    if (!rs) {
+        if (smx::launch_pack_q(q_f32, w.q8, (int64_t)s->B * s->Q * s->Hq * 128, st) != cudaSuccess)
+            return SMX_ERR_CUDA;
+        qa = w.q8;
+    }
+    if (smx::launch_index_scores(*s, qidx_bf16, idx_pool, page_table, ctx_len, w.scores, dev_status, st) !=
+        cudaSuccess)
+        return SMX_ERR_CUDA;
+    if (smx::launch_topk(*s, w.scores, ctx_len, topk_pages, topk_count, st) != cudaSuccess) return SMX_ERR_CUDA;
+    if (smx::launch_attn_split(*s, qa, k_pool, v_pool, page_table, ctx_len, topk_pages, topk_count, w.part_o,
+                               w.part_m, w.part_l, dev_status, st) != cudaSuccess)
+        return SMX_ERR_CUDA;
+    return cuda_status(smx::launch_attn_merge(*s, w.part_o, w.part_m, w.part_l, out, st));
+}
+
+int smx_decode_step_launches(const smx_shape_t* s) {
+    if (check_shape(s) != SMX_OK) return 0;
+    return s->kv_format == SMX_KV_E4M3_ROWSCALE ? 5 : 6;
+}
+
+const char* smx_status_string(int status) {
+    switch (status) {
+        case SMX_OK: return "ok";
+        case SMX_ERR_INVALID_ARG: return "invalid argument";
+        case SMX_ERR_UNSUPPORTED: return "unsupported shape or format";
+        case SMX_ERR_CUDA: return "CUDA launch error";
+        case SMX_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

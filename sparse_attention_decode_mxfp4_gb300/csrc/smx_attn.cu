@@ -1,0 +1,352 @@
+// smx_attn.cu -- a5 (split-K attention over the selected pages) and a6 (merge).
+//
+// [ATOM-2812] "Mono decode over the MXFP4 KV and index caches", commit "MXFP4 main KV": the
+// split stage runs QK against the K page (fp4 with E8M0 group scales) and the e4m3 q, softmax
+// with P in bf16 registers, PV against V widened to bf16 in on-chip memory, and writes
+// (sp_o, sp_m, sp_l) per partition; the merge combines the partitions.
+//
+// GB300 form: one CTA per (row b, partition s, KV head, group of up to 128 query rows); rows
+// are (draft token t, head of the KV group) pairs, so QK and PV are dense 16-row tiles for
+// the m16n8k16 bf16 MMA. Per selected page the CTA widens K and V to bf16 in shared memory
+// (E2M1 x 2^e and e4m3 are exact in bf16; the e4m3 row-scale V is scaled and rounded once),
+// zeroing token rows past the context so poisoned slots never reach an MMA, with a 16-byte
+// XOR swizzle that keeps ldmatrix conflict-free. Each warp owns 16 rows: QK (16 x 128 tokens,
+// fp32), mask, online softmax in the log2 domain, P rounded to bf16 in registers (the
+// accumulator layout of QK is the A layout of PV), PV into 16 x 128 fp32.
+#include <math.h>
+
+#include "smx_device.cuh"
+#include "smx_internal.h"
+
+namespace smx {
+
+struct AttnArgs {
+    const void* q;            // e4m3 bytes or bf16 bits, [B][Q][Hq][128]
+    const uint8_t* k_pool;
+    const uint8_t* v_pool;
+    const int32_t* page_table;
+    const int32_t* ctx_len;
+    const int32_t* topk_pages;
+    const int32_t* topk_count;
+    float* part_o;
+    float* part_m;
+    float* part_l;
+    int32_t* status;
+    int64_t n_pool;
+    int B, Q, Hq, Hkv, G, max_pages, topk, S, kv_format, rows_per_cta, n_row_groups;
+};
+
+constexpr int kAttnMaxWarps = 8;
+constexpr float kLog2eOverSqrtD = (float)(1.4426950408889634 / 11.313708498984761);
+
+// bf16 tile [128 tokens][128 dims], 256 B rows, 16-B chunk c of row r stored at c ^ (r & 7).
+__device__ __forceinline__ uint32_t swz(int row, int chunk) { return row * 256 + ((chunk ^ (row & 7)) << 4); }
+
+// Widen one page (K or V of one KV head) to bf16 in shared memory. For the e4m3 row-scale K
+// the codes are widened unscaled and the row scales go to rscale[] (applied to the scores).
+template <bool IS_V>
+__device__ __forceinline__ void widen_page(const AttnArgs& a, const uint8_t* page, int valid_rows,
+                                           uint8_t* tile, float* rscale) {
+    if (a.kv_format == SMX_KV_E4M3_ROWSCALE) {
+        // 128 rows x 8 chunks of 16 codes
+        for (int it = threadIdx.x; it < 128 * 8; it += blockDim.x) {
+            const int r = it >> 3, c = it & 7;
+            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+            if (r < valid_rows) {
+                const uint4 w = ldg_nc_v4(page + r * 128 + c * 16);
+                const float sc = __ldg(reinterpret_cast<const float*>(page + kRsScaleOff) + r);
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                uint32_t ob[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float2 lo = f16x2_to_f32x2(e4m3x2_to_f16x2(ws[i] & 0xFFFF));
+                    float2 hi = f16x2_to_f32x2(e4m3x2_to_f16x2(ws[i] >> 16));
+                    if (IS_V) {
+                        ob[2 * i] = f32x2_to_bf16x2(lo.x * sc, lo.y * sc);
+                        ob[2 * i + 1] = f32x2_to_bf16x2(hi.x * sc, hi.y * sc);
+                    } else {
+                        ob[2 * i] = f32x2_to_bf16x2(lo.x, lo.y);
+                        ob[2 * i + 1] = f32x2_to_bf16x2(hi.x, hi.y);
+                    }
+                }
+                o0 = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+                o1 = make_uint4(ob[4], ob[5], ob[6], ob[7]);
+                if (!IS_V && c == 0) rscale[r] = sc;
+            } else if (!IS_V && c == 0) {
+                rscale[r] = 0.0f;
+            }
+            *reinterpret_cast<uint4*>(tile + swz(r, 2 * c)) = o0;
+            *reinterpret_cast<uint4*>(tile + swz(r, 2 * c + 1)) = o1;
+        }
+        return;
+    }
+    // MXFP4: 128 rows x 4 chunks of 16 nibble bytes (32 elements = one scale group)
+    for (int it = threadIdx.x; it < 128 * 4; it += blockDim.x) {
+        const int r = it >> 2, c = it & 3;
+        uint32_t ob[16];
+        if (r < valid_rows) {
+            const uint4 w = ldg_nc_v4(page + r * 64 + c * 16);
+            const float sc = e8m0_to_f32(page[kMxScaleOff + r * 4 + c]);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t h0, h1, h2, h3;
+                e2m1x8_to_f16x2(ws[i], h0, h1, h2, h3);
+                const float2 f0 = f16x2_to_f32x2(h0), f1 = f16x2_to_f32x2(h1);
+                const float2 f2 = f16x2_to_f32x2(h2), f3 = f16x2_to_f32x2(h3);
+                ob[4 * i + 0] = f32x2_to_bf16x2(f0.x * sc, f0.y * sc);
+                ob[4 * i + 1] = f32x2_to_bf16x2(f1.x * sc, f1.y * sc);
+                ob[4 * i + 2] = f32x2_to_bf16x2(f2.x * sc, f2.y * sc);
+                ob[4 * i + 3] = f32x2_to_bf16x2(f3.x * sc, f3.y * sc);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ob[i] = 0;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<uint4*>(tile + swz(r, 4 * c + k)) =
+                make_uint4(ob[4 * k], ob[4 * k + 1], ob[4 * k + 2], ob[4 * k + 3]);
+    }
+}
+
+__global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* Ks = smem;                  // 32 KB
+    uint8_t* Vs = smem + 32768;          // 32 KB
+    float* kscale = reinterpret_cast<float*>(smem + 65536);   // 128 floats
+
+    const int s = blockIdx.x, b = blockIdx.y;
+    const int kvh = blockIdx.z / a.n_row_groups, rg = blockIdx.z % a.n_row_groups;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int M = a.G * a.Q;
+
+    const int ctx = clamp_ctx(a.ctx_len[b], a.Q, a.max_pages, nullptr);
+    const int n_pages = (ctx + kPage - 1) / kPage;
+    const int k_eff = min(a.topk_count[b], min(a.topk, n_pages));
+    const int lo = (int)(((int64_t)s * k_eff) / a.S), hi = (int)(((int64_t)(s + 1) * k_eff) / a.S);
+
+    // this lane's two rows
+    const int m0 = rg * a.rows_per_cta + warp * 16 + g, m1 = m0 + 8;
+    const bool v0 = m0 < M, v1 = m1 < M;
+    const int t0 = v0 ? m0 / a.G : 0, t1 = v1 ? m1 / a.G : 0;
+    const int pos0 = ctx - a.Q + t0, pos1 = ctx - a.Q + t1;
+
+    // q A fragments (bf16) for 8 k-steps: a0/a2 row m0, a1/a3 row m1
+    uint32_t qa[8][4];
+    {
+        const int h0 = kvh * a.G + (v0 ? m0 % a.G : 0), h1 = kvh * a.G + (v1 ? m1 % a.G : 0);
+        const int64_t base0 = (((int64_t)b * a.Q + t0) * a.Hq + h0) * kD;
+        const int64_t base1 = (((int64_t)b * a.Q + t1) * a.Hq + h1) * kD;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int d = ks * 16 + half * 8 + 2 * t;
+                uint32_t r0 = 0, r1 = 0;
+                if (a.kv_format == SMX_KV_E4M3_ROWSCALE) {
+                    const uint16_t* qb = reinterpret_cast<const uint16_t*>(a.q);
+                    if (v0) r0 = *reinterpret_cast<const uint32_t*>(qb + base0 + d);
+                    if (v1) r1 = *reinterpret_cast<const uint32_t*>(qb + base1 + d);
+                } else {
+                    const uint8_t* q8 = reinterpret_cast<const uint8_t*>(a.q);
+                    if (v0) {
+                        float2 f = f16x2_to_f32x2(e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(q8 + base0 + d)));
+                        r0 = f32x2_to_bf16x2(f.x, f.y);
+                    }
+                    if (v1) {
+                        float2 f = f16x2_to_f32x2(e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(q8 + base1 + d)));
+                        r1 = f32x2_to_bf16x2(f.x, f.y);
+                    }
+                }
+                qa[ks][half * 2 + 0] = r0;
+                qa[ks][half * 2 + 1] = r1;
+            }
+        }
+    }
+
+    float o[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+    float mrow0 = -INFINITY, mrow1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+    const int64_t kv_bytes = a.kv_format == SMX_KV_E4M3_ROWSCALE ? kRsPageBytes : kMxPageBytes;
+    const bool rs = a.kv_format == SMX_KV_E4M3_ROWSCALE;
+
+#pragma unroll 1
+    for (int i = lo; i < hi; ++i) {
+        const int p = a.topk_pages[(int64_t)b * a.topk + i];
+        if (p < 0 || p >= n_pages) {
+            if (threadIdx.x == 0) flag_status(a.status, SMX_DEV_BAD_TOPK);
+            continue;
+        }
+        const int64_t phys = a.page_table[(int64_t)b * a.max_pages + p];
+        if (phys < 0 || phys >= a.n_pool) {
+            if (threadIdx.x == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+            continue;
+        }
+        const int valid_rows = min(kPage, ctx - p * kPage);
+        __syncthreads();
+        widen_page<false>(a, a.k_pool + (phys * a.Hkv + kvh) * kv_bytes, valid_rows, Ks, kscale);
+        widen_page<true>(a, a.v_pool + (phys * a.Hkv + kvh) * kv_bytes, valid_rows, Vs, nullptr);
+        __syncthreads();
+        if (rg * a.rows_per_cta + warp * 16 >= M) continue;   // warp has no real rows
+
+        // ---- S = q K^T : 16 rows x 128 tokens ----
+        float sc[16][4];
+#pragma unroll
+        for (int nb = 0; nb < 16; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.0f;
+#pragma unroll
+        for (int nb = 0; nb < 16; ++nb) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ks += 2) {
+                uint32_t b0, b1, b2, b3;
+                const int row = nb * 8 + (lane & 7);
+                const int chunk = 2 * ks + (lane >> 3);
+                ldmatrix_x4(b0, b1, b2, b3, Ks + swz(row, chunk));
+                mma_bf16_16816(sc[nb], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+                mma_bf16_16816(sc[nb], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2, b3);
+            }
+        }
+        // ---- scale, mask, row max ----
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+        const int jbase = p * kPage;
+#pragma unroll
+        for (int nb = 0; nb < 16; ++nb) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int tok = nb * 8 + 2 * t + (c & 1);
+                const int j = jbase + tok;
+                float z = sc[nb][c] * kLog2eOverSqrtD;
+                if (rs) z *= kscale[tok];
+                const bool ok = (c < 2) ? (v0 && j <= pos0 && tok < valid_rows) : (v1 && j <= pos1 && tok < valid_rows);
+                z = ok ? z : -INFINITY;
+                sc[nb][c] = z;
+                if (c < 2) mx0 = fmaxf(mx0, z);
+                else mx1 = fmaxf(mx1, z);
+            }
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
+        const float mn0 = fmaxf(mrow0, mx0), mn1 = fmaxf(mrow1, mx1);
+        const float al0 = (mn0 == -INFINITY) ? 1.0f : exp2f(mrow0 - mn0);
+        const float al1 = (mn1 == -INFINITY) ? 1.0f : exp2f(mrow1 - mn1);
+        mrow0 = mn0;
+        mrow1 = mn1;
+        // ---- P (bf16) and row sums of the rounded weights ----
+        uint32_t pa[16][2];
+        float ps0 = 0.0f, ps1 = 0.0f;
+#pragma unroll
+        for (int nb = 0; nb < 16; ++nb) {
+            const float e0 = (mn0 == -INFINITY) ? 0.0f : exp2f(sc[nb][0] - mn0);
+            const float e1 = (mn0 == -INFINITY) ? 0.0f : exp2f(sc[nb][1] - mn0);
+            const float e2 = (mn1 == -INFINITY) ? 0.0f : exp2f(sc[nb][2] - mn1);
+            const float e3 = (mn1 == -INFINITY) ? 0.0f : exp2f(sc[nb][3] - mn1);
+            const __nv_bfloat162 p01 = __floats2bfloat162_rn(e0, e1), p23 = __floats2bfloat162_rn(e2, e3);
+            pa[nb][0] = *reinterpret_cast<const uint32_t*>(&p01);
+            pa[nb][1] = *reinterpret_cast<const uint32_t*>(&p23);
+            const float2 r01 = __bfloat1622float2(p01), r23 = __bfloat1622float2(p23);
+            ps0 += r01.x + r01.y;
+            ps1 += r23.x + r23.y;
+        }
+        ps0 += __shfl_xor_sync(0xFFFFFFFFu, ps0, 1);
+        ps0 += __shfl_xor_sync(0xFFFFFFFFu, ps0, 2);
+        ps1 += __shfl_xor_sync(0xFFFFFFFFu, ps1, 1);
+        ps1 += __shfl_xor_sync(0xFFFFFFFFu, ps1, 2);
+        l0 = l0 * al0 + ps0;
+        l1 = l1 * al1 + ps1;
+#pragma unroll
+        for (int db = 0; db < 16; ++db) {
+            o[db][0] *= al0; o[db][1] *= al0;
+            o[db][2] *= al1; o[db][3] *= al1;
+        }
+        // ---- O += P V ----
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t a0 = pa[2 * kk][0], a1 = pa[2 * kk][1], a2 = pa[2 * kk + 1][0], a3 = pa[2 * kk + 1][1];
+#pragma unroll
+            for (int db = 0; db < 16; db += 2) {
+                uint32_t b0, b1, b2, b3;
+                const int row = kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                const int chunk = db + (lane >> 4);
+                ldmatrix_x4_trans(b0, b1, b2, b3, Vs + swz(row, chunk));
+                mma_bf16_16816(o[db], a0, a1, a2, a3, b0, b1);
+                mma_bf16_16816(o[db + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+    }
+
+    // ---- write the partials of real rows ----
+    if (v0 || v1) {
+        const int h0 = kvh * a.G + m0 % a.G, h1 = kvh * a.G + m1 % a.G;
+        const int64_t r0 = (((int64_t)b * a.S + s) * a.Q + t0) * a.Hq + h0;
+        const int64_t r1 = (((int64_t)b * a.S + s) * a.Q + t1) * a.Hq + h1;
+#pragma unroll
+        for (int db = 0; db < 16; ++db) {
+            const int d = db * 8 + 2 * t;
+            if (v0) *reinterpret_cast<float2*>(a.part_o + r0 * kD + d) = make_float2(o[db][0], o[db][1]);
+            if (v1) *reinterpret_cast<float2*>(a.part_o + r1 * kD + d) = make_float2(o[db][2], o[db][3]);
+        }
+        if (t == 0) {
+            if (v0) { a.part_m[r0] = mrow0; a.part_l[r0] = l0; }
+            if (v1) { a.part_m[r1] = mrow1; a.part_l[r1] = l1; }
+        }
+    }
+}
+
+// ---- a6 merge: one CTA of 128 threads per (b, t, h), thread d owns one output dim ----
+__global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_m,
+                                                         const float* __restrict__ part_l, float* __restrict__ out,
+                                                         int S, int QH) {
+    const int row = blockIdx.x;          // b * Q * Hq + t * Hq + h
+    const int b = row / QH, r = row % QH;
+    const int d = threadIdx.x;
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, part_m[((int64_t)b * S + s) * QH + r]);
+    float acc = 0.0f, L = 0.0f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < S; ++s) {
+            const int64_t pi = ((int64_t)b * S + s) * QH + r;
+            const float m = part_m[pi];
+            if (m == -INFINITY) continue;
+            const float w = exp2f(m - M);
+            L += w * part_l[pi];
+            acc += w * part_o[pi * kD + d];
+        }
+        acc = acc / L;
+    }
+    out[(int64_t)row * kD + d] = acc;
+}
+
+cudaError_t launch_attn_split(const smx_shape_t& s, const void* q, const uint8_t* k_pool,
+                              const uint8_t* v_pool, const int32_t* page_table, const int32_t* ctx_len,
+                              const int32_t* topk_pages, const int32_t* topk_count, float* part_o,
+                              float* part_m, float* part_l, int32_t* status, cudaStream_t st) {
+    AttnArgs a;
+    a.q = q; a.k_pool = k_pool; a.v_pool = v_pool; a.page_table = page_table; a.ctx_len = ctx_len;
+    a.topk_pages = topk_pages; a.topk_count = topk_count; a.part_o = part_o; a.part_m = part_m;
+    a.part_l = part_l; a.status = status; a.n_pool = s.n_pool_pages; a.B = s.B; a.Q = s.Q; a.Hq = s.Hq;
+    a.Hkv = s.Hkv; a.G = s.Hq / s.Hkv; a.max_pages = s.max_pages_per_row; a.topk = s.topk; a.S = s.num_splits;
+    a.kv_format = s.kv_format;
+    const int M = a.G * a.Q;
+    const int warps = min(kAttnMaxWarps, (M + 15) / 16);
+    a.rows_per_cta = warps * 16;
+    a.n_row_groups = (M + a.rows_per_cta - 1) / a.rows_per_cta;
+    const size_t smem = 65536 + 512;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(attn_split_kernel), (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(s.num_splits, s.B, s.Hkv * a.n_row_groups);
+    attn_split_kernel<<<grid, warps * 32, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attn_merge(const smx_shape_t& s, const float* part_o, const float* part_m,
+                              const float* part_l, float* out, cudaStream_t st) {
+    const int rows = s.B * s.Q * s.Hq;
+    attn_merge_kernel<<<rows, 128, 0, st>>>(part_o, part_m, part_l, out, s.num_splits, s.Q * s.Hq);
+    return cudaGetLastError();
+}
+
+}  // namespace smx

@@ -1,0 +1,242 @@
+// smx_device.cuh -- device helpers shared by the libsmx kernels (sm_103a).
+//
+// Element formats: E2M1 / E8M0 from the OCP Microscaling Formats v1.0 spec, E4M3 from the
+// OCP 8-bit Floating Point spec; conversions use the sm_100-family PTX cvt forms
+// (cvt.rn.satfinite.e2m1x2.f32, cvt.rn.f16x2.e2m1x2, cvt.rn.satfinite.e4m3x2.f32,
+// cvt.rn.f16x2.e4m3x2). Tensor-core work uses mma.sync m16n8k16 (f16 / bf16, fp32 accum).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/smx.h"
+
+namespace smx {
+
+constexpr int kD = 128;
+constexpr int kPage = 128;
+constexpr int kMxPageBytes = SMX_MXFP4_PAGE_BYTES;   // 8704
+constexpr int kMxScaleOff = 8192;
+constexpr int kRsPageBytes = SMX_E4M3RS_PAGE_BYTES;  // 16896
+constexpr int kRsScaleOff = 16384;
+
+__device__ __forceinline__ void flag_status(int32_t* st, int bit) {
+    if (st) atomicOr(st, bit);
+}
+
+// ---- ordering, bit helpers ---------------------------------------------------------------
+// Order-preserving key of an fp32 score for descending selection: larger key = better.
+// NaN ranks below every number (key 0); -0 and +0 compare equal.
+__device__ __forceinline__ uint32_t score_key(float s) {
+    if (s != s) return 0u;
+    s = s + 0.0f;  // -0 -> +0
+    uint32_t u = __float_as_uint(s);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// 2^e as fp32 for an E8M0 byte: 2^(b-127); b = 0 is the subnormal 2^-127; 0xFF is NaN.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
+    if (b == 0xFFu) return __uint_as_float(0x7FC00000u);
+    if (b == 0u) return __uint_as_float(0x00400000u);
+    return __uint_as_float(b << 23);
+}
+
+// ---- quantisation (a1 / a2) ----------------------------------------------------------------
+// Two non-negative floats to one byte of E2M1 codes, lo in bits 0..3, hi in bits 4..7
+// (round to nearest even, saturating at 6).
+__device__ __forceinline__ uint32_t e2m1x2_rn_sat(float lo, float hi) {
+    uint16_t r;
+    asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n mov.b16 %0, {t, 0};\n}"
+        : "=h"(r) : "f"(hi), "f"(lo));
+    return (uint32_t)r & 0xFFu;
+}
+
+// Two non-negative floats (|x| <= 448) to two e4m3 bytes, lo in bits 0..7.
+__device__ __forceinline__ uint32_t e4m3x2_rn_sat(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return (uint32_t)r;
+}
+
+// floor(log2 a) of a finite positive float (exact, subnormals included).
+__device__ __forceinline__ int floor_log2_pos(float a) {
+    uint32_t u = __float_as_uint(a);
+    int e = (int)((u >> 23) & 0xFF);
+    if (e != 0) return e - 127;
+    return -149 + (31 - __clz(u & 0x7FFFFF));
+}
+
+// 2^k as fp32 for k in [-126, 127].
+__device__ __forceinline__ float exp2i_normal(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
+
+// q packing rule: NaN -> 0x7F; otherwise clamp to [-448, 448], round to nearest even; the sign
+// bit is the input's sign.
+__device__ __forceinline__ uint32_t pack_q4(float4 x) {
+    float v[4] = {x.x, x.y, x.z, x.w};
+    uint32_t code[4];
+#pragma unroll
+    for (int i = 0; i < 4; i += 2) {
+        float a0 = fminf(fabsf(v[i]), 448.0f), a1 = fminf(fabsf(v[i + 1]), 448.0f);
+        uint32_t c = e4m3x2_rn_sat(a0, a1);
+        code[i] = c & 0xFF;
+        code[i + 1] = c >> 8;
+    }
+    uint32_t out = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t c = code[i] | ((__float_as_uint(v[i]) >> 24) & 0x80u);
+        if (v[i] != v[i]) c = 0x7Fu;
+        out |= c << (8 * i);
+    }
+    return out;
+}
+
+// One 128-element row to MXFP4, warp-cooperative: lane l holds elements 4l..4l+3 (group
+// l / 8). Writes 64 nibble bytes at `nib` and 4 scale bytes at `sc`.
+__device__ __forceinline__ void quant_row_mxfp4_warp(float4 x, uint8_t* nib, uint8_t* sc, int lane) {
+    const float v[4] = {x.x, x.y, x.z, x.w};
+    bool nonfinite = false;
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (!isfinite(v[i])) nonfinite = true;
+        else amax = fmaxf(amax, fabsf(v[i]));
+    }
+    const unsigned grp_mask = 0xFFu << (lane & ~7);
+    const bool grp_nonfinite = (__ballot_sync(0xFFFFFFFFu, nonfinite) & grp_mask) != 0;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    int se = 0;
+    if (amax > 0.0f) {
+        se = floor_log2_pos(amax) - 2;
+        se = max(-127, min(127, se));
+    }
+    uint32_t sbyte = grp_nonfinite ? 0xFFu : (uint32_t)(se + 127);
+    const float inv = exp2i_normal(-se);  // -se in [-125, 127]
+    uint32_t codes = 0;
+#pragma unroll
+    for (int i = 0; i < 4; i += 2) {
+        uint32_t c = e2m1x2_rn_sat(fabsf(v[i]) * inv, fabsf(v[i + 1]) * inv);
+        c |= ((__float_as_uint(v[i]) >> 28) & 0x8u) | ((__float_as_uint(v[i + 1]) >> 24) & 0x80u);
+        codes |= c << (4 * i);
+    }
+    if (grp_nonfinite) codes = 0;
+    reinterpret_cast<uint16_t*>(nib)[lane] = (uint16_t)codes;
+    // lane 0 gathers the four group scale bytes
+    uint32_t s0 = __shfl_sync(0xFFFFFFFFu, sbyte, 0), s1 = __shfl_sync(0xFFFFFFFFu, sbyte, 8);
+    uint32_t s2 = __shfl_sync(0xFFFFFFFFu, sbyte, 16), s3 = __shfl_sync(0xFFFFFFFFu, sbyte, 24);
+    if (lane == 0) *reinterpret_cast<uint32_t*>(sc) = s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+}
+
+// One 128-element row to e4m3 codes with one fp32 scale s = fl32(amax / 448) (1 if amax = 0;
+// NaN and all codes 0x7F if the row holds NaN/Inf), warp-cooperative like above.
+__device__ __forceinline__ void quant_row_e4m3rs_warp(float4 x, uint8_t* codes, float* scale, int lane) {
+    const float v[4] = {x.x, x.y, x.z, x.w};
+    bool nonfinite = false;
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (!isfinite(v[i])) nonfinite = true;
+        else amax = fmaxf(amax, fabsf(v[i]));
+    }
+    const bool any_nf = __any_sync(0xFFFFFFFFu, nonfinite);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    uint32_t out = 0;
+#pragma unroll
+    for (int i = 0; i < 4; i += 2) {
+        float y0 = fminf(fabsf(__fdiv_rn(v[i], s)), 448.0f);
+        float y1 = fminf(fabsf(__fdiv_rn(v[i + 1], s)), 448.0f);
+        uint32_t c = e4m3x2_rn_sat(y0, y1);
+        c |= ((__float_as_uint(v[i]) >> 24) & 0x80u) | ((__float_as_uint(v[i + 1]) >> 16) & 0x8000u);
+        out |= c << (8 * i);
+    }
+    if (any_nf) out = 0x7F7F7F7Fu;
+    reinterpret_cast<uint32_t*>(codes)[lane] = out;
+    if (lane == 0) *scale = any_nf ? __uint_as_float(0x7FC00000u) : s;
+}
+
+// ---- dequantisation to f16 / bf16 ------------------------------------------------------------
+// Four bytes of E2M1 nibbles to four f16x2 (exact values in {0, +-0.5, ..., +-6}); register i
+// holds (element 2i in the low half, element 2i+1 in the high half).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t& h0, uint32_t& h1, uint32_t& h2, uint32_t& h3) {
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3) : "r"(w));
+}
+
+// Two e4m3 bytes (low 16 bits) to f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w16) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)w16));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h) {
+    __half2 v = *reinterpret_cast<__half2*>(&h);
+    return __half22float2(v);
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+    __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// ---- tensor cores ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_f16_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
+    uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
+    uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+// ---- shape helpers -----------------------------------------------------------------------------
+__device__ __forceinline__ int clamp_ctx(int ctx, int Q, int max_pages, int32_t* st) {
+    const int cap = max_pages * kPage;
+    if (ctx < Q || ctx > cap) {
+        flag_status(st, SMX_DEV_BAD_CTX);
+        ctx = max(0, min(ctx, cap));
+    }
+    return ctx;
+}
+
+}  // namespace smx

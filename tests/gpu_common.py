@@ -1,0 +1,100 @@
+"""Shared pieces of the GPU parity tests: device copies of the seeded inputs, the GPU step
+through the C ABI, and the comparison rules (bit-exact bytes, the top-k swap rule, the
+attention tolerance max|err| <= 2e-3 + 1e-2 |ref|)."""
+import numpy as np
+import torch
+
+import oracle
+from sparse_attention_decode_mxfp4_gb300 import ops
+from sparse_attention_decode_mxfp4_gb300 import workloads as wl
+from tests import helpers as H
+
+ATOL, RTOL = 2e-3, 1e-2
+SWAP_REL = 1e-5
+
+
+def dev_t(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def gpu_inputs(w, data, pools):
+    d = dict(
+        q_f32=dev_t(data["q"]), q_bf16=dev_t(data["q_bf16"].view(np.int16)),
+        qidx_bf16=dev_t(data["qidx_bf16"].view(np.int16)),
+        k_new=dev_t(data["k_new"]), v_new=dev_t(data["v_new"]), kidx_new=dev_t(data["kidx_new"]),
+        page_table=dev_t(data["page_table"]), ctx_len=dev_t(data["ctx_len"]),
+        k_pool=dev_t(pools[0]), v_pool=dev_t(pools[1]), idx_pool=dev_t(pools[2]),
+    )
+    return d
+
+
+def gpu_step(w, data, pools, num_splits=None):
+    shape = ops.Shape.of(w, num_splits)
+    g = gpu_inputs(w, data, pools)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, pages, count = ops.decode_step(
+        shape, q_f32=g["q_f32"] if w.kv_format == wl.KV_MXFP4 else None,
+        q_bf16=g["q_bf16"] if w.kv_format == wl.KV_E4M3_ROWSCALE else None,
+        qidx_bf16=g["qidx_bf16"], k_new=g["k_new"], v_new=g["v_new"], kidx_new=g["kidx_new"],
+        page_table=g["page_table"], ctx_len=g["ctx_len"], k_pool=g["k_pool"], v_pool=g["v_pool"],
+        idx_pool=g["idx_pool"], dev_status=status)
+    torch.cuda.synchronize()
+    return dict(out=out.cpu().numpy(), topk_pages=pages.cpu().numpy(), topk_count=count.cpu().numpy(),
+                pools=tuple(g[k].cpu().numpy() for k in ("k_pool", "v_pool", "idx_pool")),
+                status=int(status.item()))
+
+
+def check_topk_sets(ref_scores, ref_pages, ref_count, gpu_pages, gpu_count):
+    """Sets must be equal except for swaps between pages whose oracle scores differ by less
+    than 1e-5 relative. Returns the number of swapped pages."""
+    swaps = 0
+    assert np.array_equal(ref_count, gpu_count)
+    for b in range(len(ref_count)):
+        k = int(ref_count[b])
+        r = set(int(x) for x in ref_pages[b, :k])
+        g = [int(x) for x in gpu_pages[b, :k]]
+        assert g == sorted(g) and len(set(g)) == k, "GPU list must be ascending and distinct"
+        assert np.all(gpu_pages[b, k:] == -1)
+        go, ro = sorted(set(g) - r), sorted(r - set(g))
+        assert len(go) == len(ro)
+        for p in go:
+            for q in ro:
+                sp, sq = ref_scores[b, p], ref_scores[b, q]
+                assert abs(sp - sq) <= SWAP_REL * max(abs(sp), abs(sq)), (b, p, q, sp, sq)
+        swaps += len(go)
+    return swaps
+
+
+def attn_close(gpu, ref):
+    err = np.abs(gpu.astype(np.float64) - ref)
+    ok = err <= ATOL + RTOL * np.abs(ref)
+    return bool(np.all(ok)), float(err.max()) if err.size else 0.0
+
+
+def oracle_out_for_set(w, data, res, pools_after, pages, count, num_splits=None):
+    """The oracle's attention recomputed with a given selected set."""
+    sh = oracle.shape_of(w, num_splits)
+    q = data["q_bf16"] if w.kv_format == wl.KV_E4M3_ROWSCALE else res["q_e4m3"]
+    po, pm, pl = oracle.sparse_attn_split(sh, q, pools_after[0], pools_after[1], data["page_table"],
+                                          data["ctx_len"], pages, count)
+    return oracle.sparse_attn_merge(sh, po, pm, pl)
+
+
+def full_step_parity(w, num_splits=None, data=None):
+    """Whole-step parity on one workload: pool bytes, top-k sets, attention output."""
+    data = data if data is not None else wl.generate(w)
+    pools = H.oracle_pools(w, data)
+    ref, ref_pools = H.oracle_step(w, data, pools, num_splits=num_splits)
+    got = gpu_step(w, data, pools, num_splits=num_splits)
+    assert got["status"] == 0
+    for a, b in zip(got["pools"], ref_pools):
+        assert np.array_equal(a, b), "inserted page bytes differ"
+    swaps = check_topk_sets(ref["scores"], ref["topk_pages"], ref["topk_count"], got["topk_pages"],
+                            got["topk_count"])
+    ref_out = ref["out"]
+    if swaps:
+        ref_out = oracle_out_for_set(w, data, ref, ref_pools, got["topk_pages"], got["topk_count"], num_splits)
+    ok, err = attn_close(got["out"], ref_out)
+    assert np.all(np.isfinite(got["out"]))
+    assert ok, f"max err {err}"
+    return dict(swaps=swaps, err=err)

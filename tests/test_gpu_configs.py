@@ -1,0 +1,77 @@
+"""Whole-step GPU parity (pool bytes bit-exact, top-k sets under the swap rule, attention within
+max|err| <= 2e-3 + 1e-2 |ref|) on the four fixed workloads at full size, a stratified subset
+of the 216-case sweep (all of it with --full-sweep), and edge cases."""
+import numpy as np
+import pytest
+import torch
+
+from sparse_attention_decode_mxfp4_gb300 import ops
+from sparse_attention_decode_mxfp4_gb300 import workloads as wl
+from tests import gpu_common as C
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from sparse_attention_decode_mxfp4_gb300 import build
+    build.build()
+    ops.lib()
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4])
+def test_fixed_workload(n):
+    w = wl.config(n)
+    C.full_step_parity(w)
+
+
+def sweep_subset():
+    """Every 7th case plus the largest one: covers each value of every axis, ragged lengths and
+    cases with more partitions than selected pages."""
+    cases = wl.sweep_cases()
+    sub = [c for i, c in enumerate(cases) if i % 7 == 0] + [cases[-1]]
+    for axis, vals in (("B", wl.SWEEP_B), ("Q", wl.SWEEP_Q), ("max_ctx", wl.SWEEP_CTX),
+                       ("topk", wl.SWEEP_K), ("Hq", wl.SWEEP_HQ)):
+        assert {getattr(c, axis) for c in sub} == set(vals), axis
+    assert any(c.num_splits > c.topk for c in sub)
+    return sub
+
+
+SUB = sweep_subset()
+
+
+@pytest.mark.parametrize("case", SUB, ids=[c.name for c in SUB])
+def test_sweep_subset(case):
+    C.full_step_parity(case)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("case", wl.sweep_cases(), ids=[c.name for c in wl.sweep_cases()])
+def test_sweep_full(case, full_sweep):
+    if not full_sweep:
+        pytest.skip("run with --full-sweep")
+    C.full_step_parity(case)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(Q=16, Hq=8, max_ctx=3000, topk=6, num_splits=4),          # two n-tiles in the scorer
+    dict(Q=2, Hq=8, Hkv=2, max_ctx=1500, topk=3, num_splits=2),    # GQA
+    dict(Q=4, Hq=4, max_ctx=700, topk=50, num_splits=3),            # k >= pages: full attention
+    dict(Q=8, Hq=16, max_ctx=8, ctx_lens=(8, 8), topk=2, num_splits=5, B=2),   # ctx == Q
+    dict(Q=1, Hq=8, max_ctx=129, ctx_lens=(129,), topk=1, num_splits=1, B=1),  # one token on page 2
+    dict(Q=8, Hq=16, max_ctx=4096, topk=4, num_splits=12),          # empty partitions
+    dict(Q=8, Hq=32, max_ctx=2048, topk=4, num_splits=2),           # 256 rows: two row groups
+])
+def test_edge_cases(kw):
+    base = dict(name="edge", B=3, Hkv=1, seed=4242, ragged=True)
+    base.update(kw)
+    if "ctx_lens" in base:
+        base["ragged"] = False
+    C.full_step_parity(wl.Workload(**base))
+
+
+def test_fp8kv_ragged_small():
+    w = wl.Workload("fp8kv_small", B=3, Q=8, Hq=16, Hkv=1, max_ctx=6000, topk=6, num_splits=4,
+                    kv_format=wl.KV_E4M3_ROWSCALE, seed=99, ragged=True, big_row_frac=0.01)
+    C.full_step_parity(w)
