@@ -47,7 +47,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="smx", choices=["smx", "reference"])
     ap.add_argument("--config", type=int, default=2)
-    ap.add_argument("--splits", type=int, default=0, help="partitions of the split stage (0 = workload's)")
+    ap.add_argument("--splits", type=int, default=0,
+                    help="partitions of the split stage (0 = one selected page per partition, at most 16)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=100)
     return ap.parse_args()
@@ -225,7 +226,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     smx_build.build()
     w = wl.config(args.config)
-    shape = ops.Shape.of(w, args.splits or None)
+    shape = ops.Shape.of(w, args.splits or min(w.topk, 16))
     data = wl.generate(w)
     idx_b, kv_b = algorithmic_bytes(w, data["ctx_len"])
     step_bytes = idx_b + kv_b

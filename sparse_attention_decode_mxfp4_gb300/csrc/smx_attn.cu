@@ -8,11 +8,12 @@
 // GB300 form: one CTA per (row b, partition s, KV head, group of up to 128 query rows); rows
 // are (draft token t, head of the KV group) pairs, so QK and PV are dense 16-row tiles for
 // the m16n8k16 bf16 MMA. Per selected page the CTA widens K and V to bf16 in shared memory
-// (E2M1 x 2^e and e4m3 are exact in bf16; the e4m3 row-scale V is scaled and rounded once),
-// zeroing token rows past the context so poisoned slots never reach an MMA, with a 16-byte
-// XOR swizzle that keeps ldmatrix conflict-free. Each warp owns 16 rows: QK (16 x 128 tokens,
-// fp32), mask, online softmax in the log2 domain, P rounded to bf16 in registers (the
-// accumulator layout of QK is the A layout of PV), PV into 16 x 128 fp32.
+// (E2M1 x 2^e and e4m3 codes are exact in bf16), zeroing token rows past the context so
+// poisoned slots never reach an MMA, with a 16-byte XOR swizzle that keeps ldmatrix
+// conflict-free. Each warp owns 16 rows and walks the page in two 64-token chunks: QK (fp32),
+// mask, online softmax in the log2 domain, then the weights (times the V row scale for the
+// FP8-KV format) split into a bf16 high part and a bf16 low part, both multiplied into V, so the
+// weights keep ~16 significant bits (the accumulator layout of QK is the A layout of PV).
 #include <math.h>
 
 #include "smx_device.cuh"
@@ -42,9 +43,9 @@ constexpr float kLog2eOverSqrtD = (float)(1.4426950408889634 / 11.31370849898476
 // bf16 tile [128 tokens][128 dims], 256 B rows, 16-B chunk c of row r stored at c ^ (r & 7).
 __device__ __forceinline__ uint32_t swz(int row, int chunk) { return row * 256 + ((chunk ^ (row & 7)) << 4); }
 
-// Widen one page (K or V of one KV head) to bf16 in shared memory. For the e4m3 row-scale K
-// the codes are widened unscaled and the row scales go to rscale[] (applied to the scores).
-template <bool IS_V>
+// Widen one page (K or V of one KV head) to bf16 in shared memory (exact in both formats). For
+// the e4m3 row-scale pages the codes are widened unscaled and the row scales go to rscale[]:
+// K's scale multiplies the scores, V's multiplies the softmax weights.
 __device__ __forceinline__ void widen_page(const AttnArgs& a, const uint8_t* page, int valid_rows,
                                            uint8_t* tile, float* rscale) {
     if (a.kv_format == SMX_KV_E4M3_ROWSCALE) {
@@ -61,18 +62,13 @@ __device__ __forceinline__ void widen_page(const AttnArgs& a, const uint8_t* pag
                 for (int i = 0; i < 4; ++i) {
                     float2 lo = f16x2_to_f32x2(e4m3x2_to_f16x2(ws[i] & 0xFFFF));
                     float2 hi = f16x2_to_f32x2(e4m3x2_to_f16x2(ws[i] >> 16));
-                    if (IS_V) {
-                        ob[2 * i] = f32x2_to_bf16x2(lo.x * sc, lo.y * sc);
-                        ob[2 * i + 1] = f32x2_to_bf16x2(hi.x * sc, hi.y * sc);
-                    } else {
-                        ob[2 * i] = f32x2_to_bf16x2(lo.x, lo.y);
-                        ob[2 * i + 1] = f32x2_to_bf16x2(hi.x, hi.y);
-                    }
+                    ob[2 * i] = f32x2_to_bf16x2(lo.x, lo.y);
+                    ob[2 * i + 1] = f32x2_to_bf16x2(hi.x, hi.y);
                 }
                 o0 = make_uint4(ob[0], ob[1], ob[2], ob[3]);
                 o1 = make_uint4(ob[4], ob[5], ob[6], ob[7]);
-                if (!IS_V && c == 0) rscale[r] = sc;
-            } else if (!IS_V && c == 0) {
+                if (c == 0) rscale[r] = sc;
+            } else if (c == 0) {
                 rscale[r] = 0.0f;
             }
             *reinterpret_cast<uint4*>(tile + swz(r, 2 * c)) = o0;
@@ -114,13 +110,15 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* Ks = smem;                  // 32 KB
     uint8_t* Vs = smem + 32768;          // 32 KB
-    float* kscale = reinterpret_cast<float*>(smem + 65536);   // 128 floats
+    float* kscale = reinterpret_cast<float*>(smem + 65536);         // 128 floats (FP8-KV K)
+    float* vscale = reinterpret_cast<float*>(smem + 65536 + 512);   // 128 floats (FP8-KV V)
 
     const int s = blockIdx.x, b = blockIdx.y;
     const int kvh = blockIdx.z / a.n_row_groups, rg = blockIdx.z % a.n_row_groups;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int M = a.G * a.Q;
+    const bool rs = a.kv_format == SMX_KV_E4M3_ROWSCALE;
 
     const int ctx = clamp_ctx(a.ctx_len[b], a.Q, a.max_pages, nullptr);
     const int n_pages = (ctx + kPage - 1) / kPage;
@@ -133,7 +131,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
     const int t0 = v0 ? m0 / a.G : 0, t1 = v1 ? m1 / a.G : 0;
     const int pos0 = ctx - a.Q + t0, pos1 = ctx - a.Q + t1;
 
-    // q A fragments (bf16) for 8 k-steps: a0/a2 row m0, a1/a3 row m1
+    // q A fragments (bf16, exact) for 8 k-steps: a0/a2 row m0, a1/a3 row m1
     uint32_t qa[8][4];
     {
         const int h0 = kvh * a.G + (v0 ? m0 % a.G : 0), h1 = kvh * a.G + (v1 ? m1 % a.G : 0);
@@ -145,7 +143,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
             for (int half = 0; half < 2; ++half) {
                 const int d = ks * 16 + half * 8 + 2 * t;
                 uint32_t r0 = 0, r1 = 0;
-                if (a.kv_format == SMX_KV_E4M3_ROWSCALE) {
+                if (rs) {
                     const uint16_t* qb = reinterpret_cast<const uint16_t*>(a.q);
                     if (v0) r0 = *reinterpret_cast<const uint32_t*>(qb + base0 + d);
                     if (v1) r1 = *reinterpret_cast<const uint32_t*>(qb + base1 + d);
@@ -170,8 +168,8 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
 #pragma unroll
     for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
     float mrow0 = -INFINITY, mrow1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-    const int64_t kv_bytes = a.kv_format == SMX_KV_E4M3_ROWSCALE ? kRsPageBytes : kMxPageBytes;
-    const bool rs = a.kv_format == SMX_KV_E4M3_ROWSCALE;
+    const int64_t kv_bytes = rs ? kRsPageBytes : kMxPageBytes;
+    const bool warp_active = rg * a.rows_per_cta + warp * 16 < M;
 
 #pragma unroll 1
     for (int i = lo; i < hi; ++i) {
@@ -187,93 +185,110 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
         }
         const int valid_rows = min(kPage, ctx - p * kPage);
         __syncthreads();
-        widen_page<false>(a, a.k_pool + (phys * a.Hkv + kvh) * kv_bytes, valid_rows, Ks, kscale);
-        widen_page<true>(a, a.v_pool + (phys * a.Hkv + kvh) * kv_bytes, valid_rows, Vs, nullptr);
+        widen_page(a, a.k_pool + (phys * a.Hkv + kvh) * kv_bytes, valid_rows, Ks, kscale);
+        widen_page(a, a.v_pool + (phys * a.Hkv + kvh) * kv_bytes, valid_rows, Vs, vscale);
         __syncthreads();
-        if (rg * a.rows_per_cta + warp * 16 >= M) continue;   // warp has no real rows
-
-        // ---- S = q K^T : 16 rows x 128 tokens ----
-        float sc[16][4];
-#pragma unroll
-        for (int nb = 0; nb < 16; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.0f;
-#pragma unroll
-        for (int nb = 0; nb < 16; ++nb) {
-#pragma unroll
-            for (int ks = 0; ks < 8; ks += 2) {
-                uint32_t b0, b1, b2, b3;
-                const int row = nb * 8 + (lane & 7);
-                const int chunk = 2 * ks + (lane >> 3);
-                ldmatrix_x4(b0, b1, b2, b3, Ks + swz(row, chunk));
-                mma_bf16_16816(sc[nb], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-                mma_bf16_16816(sc[nb], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2, b3);
-            }
-        }
-        // ---- scale, mask, row max ----
-        float mx0 = -INFINITY, mx1 = -INFINITY;
+        if (!warp_active) continue;
         const int jbase = p * kPage;
+
+#pragma unroll 1
+        for (int ch = 0; ch < 2; ++ch) {          // two chunks of 64 tokens
+            // ---- S = q K^T : 16 rows x 64 tokens ----
+            float sc[8][4];
 #pragma unroll
-        for (int nb = 0; nb < 16; ++nb) {
+            for (int nb = 0; nb < 8; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.0f;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int tok = nb * 8 + 2 * t + (c & 1);
-                const int j = jbase + tok;
-                float z = sc[nb][c] * kLog2eOverSqrtD;
-                if (rs) z *= kscale[tok];
-                const bool ok = (c < 2) ? (v0 && j <= pos0 && tok < valid_rows) : (v1 && j <= pos1 && tok < valid_rows);
-                z = ok ? z : -INFINITY;
-                sc[nb][c] = z;
-                if (c < 2) mx0 = fmaxf(mx0, z);
-                else mx1 = fmaxf(mx1, z);
+            for (int nb = 0; nb < 8; ++nb) {
+#pragma unroll
+                for (int ks = 0; ks < 8; ks += 2) {
+                    uint32_t b0, b1, b2, b3;
+                    const int row = ch * 64 + nb * 8 + (lane & 7);
+                    const int chunk = 2 * ks + (lane >> 3);
+                    ldmatrix_x4(b0, b1, b2, b3, Ks + swz(row, chunk));
+                    mma_bf16_16816(sc[nb], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+                    mma_bf16_16816(sc[nb], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2, b3);
+                }
             }
-        }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
-        const float mn0 = fmaxf(mrow0, mx0), mn1 = fmaxf(mrow1, mx1);
-        const float al0 = (mn0 == -INFINITY) ? 1.0f : exp2f(mrow0 - mn0);
-        const float al1 = (mn1 == -INFINITY) ? 1.0f : exp2f(mrow1 - mn1);
-        mrow0 = mn0;
-        mrow1 = mn1;
-        // ---- P (bf16) and row sums of the rounded weights ----
-        uint32_t pa[16][2];
-        float ps0 = 0.0f, ps1 = 0.0f;
+            // ---- scale, mask, row max ----
+            float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-        for (int nb = 0; nb < 16; ++nb) {
-            const float e0 = (mn0 == -INFINITY) ? 0.0f : exp2f(sc[nb][0] - mn0);
-            const float e1 = (mn0 == -INFINITY) ? 0.0f : exp2f(sc[nb][1] - mn0);
-            const float e2 = (mn1 == -INFINITY) ? 0.0f : exp2f(sc[nb][2] - mn1);
-            const float e3 = (mn1 == -INFINITY) ? 0.0f : exp2f(sc[nb][3] - mn1);
-            const __nv_bfloat162 p01 = __floats2bfloat162_rn(e0, e1), p23 = __floats2bfloat162_rn(e2, e3);
-            pa[nb][0] = *reinterpret_cast<const uint32_t*>(&p01);
-            pa[nb][1] = *reinterpret_cast<const uint32_t*>(&p23);
-            const float2 r01 = __bfloat1622float2(p01), r23 = __bfloat1622float2(p23);
-            ps0 += r01.x + r01.y;
-            ps1 += r23.x + r23.y;
-        }
-        ps0 += __shfl_xor_sync(0xFFFFFFFFu, ps0, 1);
-        ps0 += __shfl_xor_sync(0xFFFFFFFFu, ps0, 2);
-        ps1 += __shfl_xor_sync(0xFFFFFFFFu, ps1, 1);
-        ps1 += __shfl_xor_sync(0xFFFFFFFFu, ps1, 2);
-        l0 = l0 * al0 + ps0;
-        l1 = l1 * al1 + ps1;
+            for (int nb = 0; nb < 8; ++nb) {
 #pragma unroll
-        for (int db = 0; db < 16; ++db) {
-            o[db][0] *= al0; o[db][1] *= al0;
-            o[db][2] *= al1; o[db][3] *= al1;
-        }
-        // ---- O += P V ----
+                for (int c = 0; c < 4; ++c) {
+                    const int tok = ch * 64 + nb * 8 + 2 * t + (c & 1);
+                    const int j = jbase + tok;
+                    float z = sc[nb][c] * kLog2eOverSqrtD;
+                    if (rs) z *= kscale[tok];
+                    const bool ok = (c < 2) ? (v0 && j <= pos0) : (v1 && j <= pos1);
+                    z = ok ? z : -INFINITY;
+                    sc[nb][c] = z;
+                    if (c < 2) mx0 = fmaxf(mx0, z);
+                    else mx1 = fmaxf(mx1, z);
+                }
+            }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
+            const float mn0 = fmaxf(mrow0, mx0), mn1 = fmaxf(mrow1, mx1);
+            const float al0 = (mn0 == -INFINITY) ? 1.0f : exp2f(mrow0 - mn0);
+            const float al1 = (mn1 == -INFINITY) ? 1.0f : exp2f(mrow1 - mn1);
+            mrow0 = mn0;
+            mrow1 = mn1;
+            // ---- weights: P' = p (x V row scale) as bf16 hi + lo; l sums p in fp32 ----
+            uint32_t ph[8][2], pl[8][2];
+            float ps0 = 0.0f, ps1 = 0.0f;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t a0 = pa[2 * kk][0], a1 = pa[2 * kk][1], a2 = pa[2 * kk + 1][0], a3 = pa[2 * kk + 1][1];
+            for (int nb = 0; nb < 8; ++nb) {
+                float e[4];
 #pragma unroll
-            for (int db = 0; db < 16; db += 2) {
-                uint32_t b0, b1, b2, b3;
-                const int row = kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-                const int chunk = db + (lane >> 4);
-                ldmatrix_x4_trans(b0, b1, b2, b3, Vs + swz(row, chunk));
-                mma_bf16_16816(o[db], a0, a1, a2, a3, b0, b1);
-                mma_bf16_16816(o[db + 1], a0, a1, a2, a3, b2, b3);
+                for (int c = 0; c < 4; ++c) {
+                    const float mn = (c < 2) ? mn0 : mn1;
+                    e[c] = (mn == -INFINITY) ? 0.0f : exp2f(sc[nb][c] - mn);
+                }
+                ps0 += e[0] + e[1];
+                ps1 += e[2] + e[3];
+                if (rs) {
+                    const int tok = ch * 64 + nb * 8 + 2 * t;
+                    const float s0 = vscale[tok], s1 = vscale[tok + 1];
+                    e[0] *= s0; e[1] *= s1; e[2] *= s0; e[3] *= s1;
+                }
+                const __nv_bfloat162 h01 = __floats2bfloat162_rn(e[0], e[1]), h23 = __floats2bfloat162_rn(e[2], e[3]);
+                const float2 r01 = __bfloat1622float2(h01), r23 = __bfloat1622float2(h23);
+                const __nv_bfloat162 l01 = __floats2bfloat162_rn(e[0] - r01.x, e[1] - r01.y);
+                const __nv_bfloat162 l23 = __floats2bfloat162_rn(e[2] - r23.x, e[3] - r23.y);
+                ph[nb][0] = *reinterpret_cast<const uint32_t*>(&h01);
+                ph[nb][1] = *reinterpret_cast<const uint32_t*>(&h23);
+                pl[nb][0] = *reinterpret_cast<const uint32_t*>(&l01);
+                pl[nb][1] = *reinterpret_cast<const uint32_t*>(&l23);
+            }
+            ps0 += __shfl_xor_sync(0xFFFFFFFFu, ps0, 1);
+            ps0 += __shfl_xor_sync(0xFFFFFFFFu, ps0, 2);
+            ps1 += __shfl_xor_sync(0xFFFFFFFFu, ps1, 1);
+            ps1 += __shfl_xor_sync(0xFFFFFFFFu, ps1, 2);
+            l0 = l0 * al0 + ps0;
+            l1 = l1 * al1 + ps1;
+#pragma unroll
+            for (int db = 0; db < 16; ++db) {
+                o[db][0] *= al0; o[db][1] *= al0;
+                o[db][2] *= al1; o[db][3] *= al1;
+            }
+            // ---- O += (P_hi + P_lo) V ----
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t a0 = ph[2 * kk][0], a1 = ph[2 * kk][1], a2 = ph[2 * kk + 1][0], a3 = ph[2 * kk + 1][1];
+                const uint32_t c0 = pl[2 * kk][0], c1 = pl[2 * kk][1], c2 = pl[2 * kk + 1][0], c3 = pl[2 * kk + 1][1];
+#pragma unroll
+                for (int db = 0; db < 16; db += 2) {
+                    uint32_t b0, b1, b2, b3;
+                    const int row = ch * 64 + kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                    const int chunk = db + (lane >> 4);
+                    ldmatrix_x4_trans(b0, b1, b2, b3, Vs + swz(row, chunk));
+                    mma_bf16_16816(o[db], a0, a1, a2, a3, b0, b1);
+                    mma_bf16_16816(o[db + 1], a0, a1, a2, a3, b2, b3);
+                    mma_bf16_16816(o[db], c0, c1, c2, c3, b0, b1);
+                    mma_bf16_16816(o[db + 1], c0, c1, c2, c3, b2, b3);
+                }
             }
         }
     }
@@ -331,10 +346,13 @@ cudaError_t launch_attn_split(const smx_shape_t& s, const void* q, const uint8_t
     a.Hkv = s.Hkv; a.G = s.Hq / s.Hkv; a.max_pages = s.max_pages_per_row; a.topk = s.topk; a.S = s.num_splits;
     a.kv_format = s.kv_format;
     const int M = a.G * a.Q;
-    const int warps = min(kAttnMaxWarps, (M + 15) / 16);
+    int warps = min(kAttnMaxWarps, (M + 15) / 16);
+    // split the query rows of a KV head over two CTAs when one CTA per (row, partition, head)
+    // would leave most SMs idle
+    if (warps > 4 && (int64_t)s.num_splits * s.B * s.Hkv * ((M + 127) / 128) < 148) warps = 4;
     a.rows_per_cta = warps * 16;
     a.n_row_groups = (M + a.rows_per_cta - 1) / a.rows_per_cta;
-    const size_t smem = 65536 + 512;
+    const size_t smem = 65536 + 1024;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(attn_split_kernel), (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(s.num_splits, s.B, s.Hkv * a.n_row_groups);

@@ -38,7 +38,7 @@ constexpr int kIdxWarps = 4;
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h16) { return __uint_as_float(h16 << 16); }
 
 template <int NT>
-__global__ void __launch_bounds__(kIdxWarps * 32, 4) index_score_kernel(IndexArgs a) {
+__global__ void __launch_bounds__(kIdxWarps * 32, (NT == 1 ? 4 : 3)) index_score_kernel(IndexArgs a) {
     const int b = blockIdx.y;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
@@ -104,20 +104,29 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 4) index_score_kernel(IndexArg
     const int lim = ctx - a.Q;  // token j counts for query n iff j <= lim + n
     float best = -INFINITY;
 
-#pragma unroll 1
+    // the whole page in flight at once: 16 x 16 B of nibbles and 16 scale words per lane
+    uint4 c0[8], c1[8];
+    uint32_t sw0[8], sw1[8];
+#pragma unroll
     for (int tile = 0; tile < 8; ++tile) {
         const int r0 = tile * 16 + g, r1 = r0 + 8;
-        const uint4 c0 = ldg_nc_v4(page + r0 * 64 + 16 * t);
-        const uint4 c1 = ldg_nc_v4(page + r1 * 64 + 16 * t);
-        const uint32_t sw0 = __ldg(reinterpret_cast<const uint32_t*>(page + kMxScaleOff) + r0);
-        const uint32_t sw1 = __ldg(reinterpret_cast<const uint32_t*>(page + kMxScaleOff) + r1);
+        c0[tile] = ldg_nc_v4(page + r0 * 64 + 16 * t);
+        c1[tile] = ldg_nc_v4(page + r1 * 64 + 16 * t);
+        sw0[tile] = __ldg(reinterpret_cast<const uint32_t*>(page + kMxScaleOff) + r0);
+        sw1[tile] = __ldg(reinterpret_cast<const uint32_t*>(page + kMxScaleOff) + r1);
+    }
+
+#pragma unroll
+    for (int tile = 0; tile < 8; ++tile) {
+        const int r0 = tile * 16 + g, r1 = r0 + 8;
         uint32_t f0, f1;   // f16x2 of 2^(s_t - max s) per row
         int e0, e1;        // max scale byte per row (0xFF marks a NaN scale)
         {
-            uint32_t m0 = max(max(sw0 & 0xFF, (sw0 >> 8) & 0xFF), max((sw0 >> 16) & 0xFF, sw0 >> 24));
-            uint32_t m1 = max(max(sw1 & 0xFF, (sw1 >> 8) & 0xFF), max((sw1 >> 16) & 0xFF, sw1 >> 24));
-            int rel0 = (int)((sw0 >> (8 * t)) & 0xFF) - (int)m0;
-            int rel1 = (int)((sw1 >> (8 * t)) & 0xFF) - (int)m1;
+            const uint32_t a0 = sw0[tile], a1 = sw1[tile];
+            uint32_t m0 = max(max(a0 & 0xFF, (a0 >> 8) & 0xFF), max((a0 >> 16) & 0xFF, a0 >> 24));
+            uint32_t m1 = max(max(a1 & 0xFF, (a1 >> 8) & 0xFF), max((a1 >> 16) & 0xFF, a1 >> 24));
+            int rel0 = (int)((a0 >> (8 * t)) & 0xFF) - (int)m0;
+            int rel1 = (int)((a1 >> (8 * t)) & 0xFF) - (int)m1;
             __half h0 = rel0 >= -22 ? __float2half_rn(exp2i_normal(rel0)) : __float2half_rn(0.0f);
             __half h1 = rel1 >= -22 ? __float2half_rn(exp2i_normal(rel1)) : __float2half_rn(0.0f);
             __half2 hh0 = __halves2half2(h0, h0), hh1 = __halves2half2(h1, h1);
@@ -129,8 +138,8 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 4) index_score_kernel(IndexArg
         float acc[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
-        const uint32_t w0[4] = {c0.x, c0.y, c0.z, c0.w};
-        const uint32_t w1[4] = {c1.x, c1.y, c1.z, c1.w};
+        const uint32_t w0[4] = {c0[tile].x, c0[tile].y, c0[tile].z, c0[tile].w};
+        const uint32_t w1[4] = {c1[tile].x, c1[tile].y, c1[tile].z, c1[tile].w};
 #pragma unroll
         for (int wi = 0; wi < 4; ++wi) {
             uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
