@@ -73,7 +73,7 @@ enum {
 #define SMX_E4M3RS_PAGE_BYTES 16896
 #define SMX_MAX_Q 16
 #define SMX_MAX_TOPK 4096
-#define SMX_MAX_PAGES_PER_ROW (1 << 20)
+#define SMX_MAX_PAGES_PER_ROW 32768
 
 typedef struct {
     int32_t B;                  /* rows (sequences) in the step */

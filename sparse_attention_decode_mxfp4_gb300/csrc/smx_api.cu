@@ -179,7 +179,7 @@ int smx_sparse_attn_merge(const smx_shape_t* s, const float* part_o, const float
     int rc = check_shape(s);
     if (rc) return rc;
     if (!part_o || !part_m || !part_l || !out) return SMX_ERR_INVALID_ARG;
-    return cuda_status(smx::launch_attn_merge(*s, part_o, part_m, part_l, out, (cudaStream_t)stream));
+    return cuda_status(smx::launch_attn_merge(*s, part_o, part_m, part_l, out, false, (cudaStream_t)stream));
 }
 
 int smx_decode_step(const smx_shape_t* s, const float* q_f32, const uint16_t* q_bf16, const uint16_t* qidx_bf16,
@@ -204,28 +204,21 @@ int smx_decode_step(const smx_shape_t* s, const float* q_f32, const uint16_t* q_
         return SMX_ERR_WORKSPACE;
     const Workspace w = layout(s, workspace);
     cudaStream_t st = (cudaStream_t)stream;
-    if (smx::launch_kv_insert(*s, k_new, v_new, kidx_new, s->Q, page_table, ctx_len, nullptr, k_pool, v_pool,
-                              idx_pool, dev_status, false, st) != cudaSuccess)
+    // 1) insert + index scores, 2) q packing + top-k + split stage, 3) merge; each kernel is a
+    //    programmatic dependent of the one before it and waits for it before reading its output.
+    if (smx::launch_index(*s, qidx_bf16, idx_pool, page_table, ctx_len, w.scores, dev_status, k_new, v_new,
+                          kidx_new, k_pool, v_pool, true, st) != cudaSuccess)
         return SMX_ERR_CUDA;
-    const void* qa = q_bf16;
-    if (!rs) {
-        if (smx::launch_pack_q(q_f32, w.q8, (int64_t)s->B * s->Q * s->Hq * 128, st) != cudaSuccess)
-            return SMX_ERR_CUDA;
-        qa = w.q8;
-    }
-    if (smx::launch_index_scores(*s, qidx_bf16, idx_pool, page_table, ctx_len, w.scores, dev_status, st) !=
-        cudaSuccess)
+    if (smx::launch_attn_select_split(*s, q_f32, q_bf16, k_pool, v_pool, page_table, ctx_len, w.scores,
+                                      topk_pages, topk_count, w.part_o, w.part_m, w.part_l, dev_status,
+                                      st) != cudaSuccess)
         return SMX_ERR_CUDA;
-    if (smx::launch_topk(*s, w.scores, ctx_len, topk_pages, topk_count, st) != cudaSuccess) return SMX_ERR_CUDA;
-    if (smx::launch_attn_split(*s, qa, k_pool, v_pool, page_table, ctx_len, topk_pages, topk_count, w.part_o,
-                               w.part_m, w.part_l, dev_status, st) != cudaSuccess)
-        return SMX_ERR_CUDA;
-    return cuda_status(smx::launch_attn_merge(*s, w.part_o, w.part_m, w.part_l, out, st));
+    return cuda_status(smx::launch_attn_merge(*s, w.part_o, w.part_m, w.part_l, out, true, st));
 }
 
 int smx_decode_step_launches(const smx_shape_t* s) {
     if (check_shape(s) != SMX_OK) return 0;
-    return s->kv_format == SMX_KV_E4M3_ROWSCALE ? 5 : 6;
+    return 3;
 }
 
 const char* smx_status_string(int status) {

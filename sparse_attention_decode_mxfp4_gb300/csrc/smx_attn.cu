@@ -18,6 +18,7 @@
 
 #include "smx_device.cuh"
 #include "smx_internal.h"
+#include "smx_select.cuh"
 
 namespace smx {
 
@@ -35,6 +36,13 @@ struct AttnArgs {
     int32_t* status;
     int64_t n_pool;
     int B, Q, Hq, Hkv, G, max_pages, topk, S, kv_format, rows_per_cta, n_row_groups;
+    // fused step: q from f32 with the packing rule, the selection from the page scores
+    const float* q_f32;       // MXFP4 K/V: q before packing (else nullptr: q is packed bytes)
+    const float* scores;      // [B][max_pages] (else nullptr: topk_pages/topk_count are inputs)
+    int32_t* topk_out;        // with scores: the selection is written here by one CTA per row
+    int32_t* count_out;
+    int region_bytes;         // shared bytes of the K/V tiles (also holds the selection keys)
+    int pdl;
 };
 
 constexpr int kAttnMaxWarps = 8;
@@ -108,10 +116,13 @@ __device__ __forceinline__ void widen_page(const AttnArgs& a, const uint8_t* pag
 
 __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ SelectSmem selsm;
     uint8_t* Ks = smem;                  // 32 KB
     uint8_t* Vs = smem + 32768;          // 32 KB
-    float* kscale = reinterpret_cast<float*>(smem + 65536);         // 128 floats (FP8-KV K)
-    float* vscale = reinterpret_cast<float*>(smem + 65536 + 512);   // 128 floats (FP8-KV V)
+    uint32_t* keys = reinterpret_cast<uint32_t*>(smem);                          // before the tiles
+    float* kscale = reinterpret_cast<float*>(smem + a.region_bytes);             // 128 floats (FP8-KV K)
+    float* vscale = reinterpret_cast<float*>(smem + a.region_bytes + 512);       // 128 floats (FP8-KV V)
+    int* sel = reinterpret_cast<int*>(smem + a.region_bytes + 1024);             // selected pages
 
     const int s = blockIdx.x, b = blockIdx.y;
     const int kvh = blockIdx.z / a.n_row_groups, rg = blockIdx.z % a.n_row_groups;
@@ -120,18 +131,13 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
     const int M = a.G * a.Q;
     const bool rs = a.kv_format == SMX_KV_E4M3_ROWSCALE;
 
-    const int ctx = clamp_ctx(a.ctx_len[b], a.Q, a.max_pages, nullptr);
-    const int n_pages = (ctx + kPage - 1) / kPage;
-    const int k_eff = min(a.topk_count[b], min(a.topk, n_pages));
-    const int lo = (int)(((int64_t)s * k_eff) / a.S), hi = (int)(((int64_t)(s + 1) * k_eff) / a.S);
-
     // this lane's two rows
     const int m0 = rg * a.rows_per_cta + warp * 16 + g, m1 = m0 + 8;
     const bool v0 = m0 < M, v1 = m1 < M;
     const int t0 = v0 ? m0 / a.G : 0, t1 = v1 ? m1 / a.G : 0;
-    const int pos0 = ctx - a.Q + t0, pos1 = ctx - a.Q + t1;
 
-    // q A fragments (bf16, exact) for 8 k-steps: a0/a2 row m0, a1/a3 row m1
+    // q A fragments (bf16, exact) for 8 k-steps: a0/a2 row m0, a1/a3 row m1. The fused step packs
+    // q from f32 here with the q packing rule (these inputs do not depend on the earlier kernels).
     uint32_t qa[8][4];
     {
         const int h0 = kvh * a.G + (v0 ? m0 % a.G : 0), h1 = kvh * a.G + (v1 ? m1 % a.G : 0);
@@ -148,21 +154,46 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
                     if (v0) r0 = *reinterpret_cast<const uint32_t*>(qb + base0 + d);
                     if (v1) r1 = *reinterpret_cast<const uint32_t*>(qb + base1 + d);
                 } else {
-                    const uint8_t* q8 = reinterpret_cast<const uint8_t*>(a.q);
-                    if (v0) {
-                        float2 f = f16x2_to_f32x2(e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(q8 + base0 + d)));
-                        r0 = f32x2_to_bf16x2(f.x, f.y);
+                    uint32_t w0 = 0, w1 = 0;
+                    if (a.q_f32) {
+                        if (v0) { const float2 f = *reinterpret_cast<const float2*>(a.q_f32 + base0 + d); w0 = pack_q2(f.x, f.y); }
+                        if (v1) { const float2 f = *reinterpret_cast<const float2*>(a.q_f32 + base1 + d); w1 = pack_q2(f.x, f.y); }
+                    } else {
+                        const uint8_t* q8 = reinterpret_cast<const uint8_t*>(a.q);
+                        if (v0) w0 = *reinterpret_cast<const uint16_t*>(q8 + base0 + d);
+                        if (v1) w1 = *reinterpret_cast<const uint16_t*>(q8 + base1 + d);
                     }
-                    if (v1) {
-                        float2 f = f16x2_to_f32x2(e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(q8 + base1 + d)));
-                        r1 = f32x2_to_bf16x2(f.x, f.y);
-                    }
+                    if (v0) { const float2 f = f16x2_to_f32x2(e4m3x2_to_f16x2(w0)); r0 = f32x2_to_bf16x2(f.x, f.y); }
+                    if (v1) { const float2 f = f16x2_to_f32x2(e4m3x2_to_f16x2(w1)); r1 = f32x2_to_bf16x2(f.x, f.y); }
                 }
                 qa[ks][half * 2 + 0] = r0;
                 qa[ks][half * 2 + 1] = r1;
             }
         }
     }
+    if (a.pdl) pdl_wait();
+    pdl_trigger();
+
+    const int ctx = clamp_ctx(a.ctx_len[b], a.Q, a.max_pages, nullptr);
+    const int n_pages = (ctx + kPage - 1) / kPage;
+    const int pos0 = ctx - a.Q + t0, pos1 = ctx - a.Q + t1;
+    int k_eff;
+    if (a.scores) {
+        const float* sc_row = a.scores + (int64_t)b * a.max_pages;
+        for (int i = threadIdx.x; i < n_pages; i += blockDim.x) keys[i] = score_key(sc_row[i]);
+        __syncthreads();
+        k_eff = block_select(keys, n_pages, a.topk, sel, selsm);
+        if (s == 0 && blockIdx.z == 0) {
+            for (int i = threadIdx.x; i < a.topk; i += blockDim.x)
+                a.topk_out[(int64_t)b * a.topk + i] = i < k_eff ? sel[i] : -1;
+            if (threadIdx.x == 0) a.count_out[b] = k_eff;
+        }
+    } else {
+        k_eff = min(a.topk_count[b], min(a.topk, n_pages));
+        for (int i = threadIdx.x; i < k_eff; i += blockDim.x) sel[i] = a.topk_pages[(int64_t)b * a.topk + i];
+    }
+    __syncthreads();
+    const int lo = (int)(((int64_t)s * k_eff) / a.S), hi = (int)(((int64_t)(s + 1) * k_eff) / a.S);
 
     float o[16][4];
 #pragma unroll
@@ -173,7 +204,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
 
 #pragma unroll 1
     for (int i = lo; i < hi; ++i) {
-        const int p = a.topk_pages[(int64_t)b * a.topk + i];
+        const int p = sel[i];
         if (p < 0 || p >= n_pages) {
             if (threadIdx.x == 0) flag_status(a.status, SMX_DEV_BAD_TOPK);
             continue;
@@ -314,7 +345,9 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
 // ---- a6 merge: one CTA of 128 threads per (b, t, h), thread d owns one output dim ----
 __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_m,
                                                          const float* __restrict__ part_l, float* __restrict__ out,
-                                                         int S, int QH) {
+                                                         int S, int QH, int pdl) {
+    if (pdl) pdl_wait();
+    pdl_trigger();
     const int row = blockIdx.x;          // b * Q * Hq + t * Hq + h
     const int b = row / QH, r = row % QH;
     const int d = threadIdx.x;
@@ -335,16 +368,10 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict
     out[(int64_t)row * kD + d] = acc;
 }
 
-cudaError_t launch_attn_split(const smx_shape_t& s, const void* q, const uint8_t* k_pool,
-                              const uint8_t* v_pool, const int32_t* page_table, const int32_t* ctx_len,
-                              const int32_t* topk_pages, const int32_t* topk_count, float* part_o,
-                              float* part_m, float* part_l, int32_t* status, cudaStream_t st) {
-    AttnArgs a;
-    a.q = q; a.k_pool = k_pool; a.v_pool = v_pool; a.page_table = page_table; a.ctx_len = ctx_len;
-    a.topk_pages = topk_pages; a.topk_count = topk_count; a.part_o = part_o; a.part_m = part_m;
-    a.part_l = part_l; a.status = status; a.n_pool = s.n_pool_pages; a.B = s.B; a.Q = s.Q; a.Hq = s.Hq;
+static cudaError_t launch_split_impl(const smx_shape_t& s, AttnArgs& a, bool pdl, cudaStream_t st) {
+    a.n_pool = s.n_pool_pages; a.B = s.B; a.Q = s.Q; a.Hq = s.Hq;
     a.Hkv = s.Hkv; a.G = s.Hq / s.Hkv; a.max_pages = s.max_pages_per_row; a.topk = s.topk; a.S = s.num_splits;
-    a.kv_format = s.kv_format;
+    a.kv_format = s.kv_format; a.pdl = pdl ? 1 : 0;
     const int M = a.G * a.Q;
     int warps = min(kAttnMaxWarps, (M + 15) / 16);
     // split the query rows of a KV head over two CTAs when one CTA per (row, partition, head)
@@ -352,19 +379,60 @@ cudaError_t launch_attn_split(const smx_shape_t& s, const void* q, const uint8_t
     if (warps > 4 && (int64_t)s.num_splits * s.B * s.Hkv * ((M + 127) / 128) < 148) warps = 4;
     a.rows_per_cta = warps * 16;
     a.n_row_groups = (M + a.rows_per_cta - 1) / a.rows_per_cta;
-    const size_t smem = 65536 + 1024;
+    a.region_bytes = max(65536, 4 * s.max_pages_per_row);
+    const size_t smem = (size_t)a.region_bytes + 1024 + 4 * (size_t)s.topk;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(attn_split_kernel), (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(s.num_splits, s.B, s.Hkv * a.n_row_groups);
-    attn_split_kernel<<<grid, warps * 32, smem, st>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(s.num_splits, s.B, s.Hkv * a.n_row_groups);
+    cfg.blockDim = dim3(warps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, attn_split_kernel, a);
+}
+
+cudaError_t launch_attn_split(const smx_shape_t& s, const void* q, const uint8_t* k_pool,
+                              const uint8_t* v_pool, const int32_t* page_table, const int32_t* ctx_len,
+                              const int32_t* topk_pages, const int32_t* topk_count, float* part_o,
+                              float* part_m, float* part_l, int32_t* status, cudaStream_t st) {
+    AttnArgs a = {};
+    a.q = q; a.k_pool = k_pool; a.v_pool = v_pool; a.page_table = page_table; a.ctx_len = ctx_len;
+    a.topk_pages = topk_pages; a.topk_count = topk_count; a.part_o = part_o; a.part_m = part_m;
+    a.part_l = part_l; a.status = status;
+    return launch_split_impl(s, a, false, st);
+}
+
+cudaError_t launch_attn_select_split(const smx_shape_t& s, const float* q_f32, const void* q_bf16,
+                                     const uint8_t* k_pool, const uint8_t* v_pool, const int32_t* page_table,
+                                     const int32_t* ctx_len, const float* scores, int32_t* topk_pages,
+                                     int32_t* topk_count, float* part_o, float* part_m, float* part_l,
+                                     int32_t* status, cudaStream_t st) {
+    AttnArgs a = {};
+    a.q = q_bf16; a.q_f32 = s.kv_format == SMX_KV_E4M3_ROWSCALE ? nullptr : q_f32;
+    a.k_pool = k_pool; a.v_pool = v_pool; a.page_table = page_table; a.ctx_len = ctx_len;
+    a.scores = scores; a.topk_out = topk_pages; a.count_out = topk_count;
+    a.part_o = part_o; a.part_m = part_m; a.part_l = part_l; a.status = status;
+    return launch_split_impl(s, a, true, st);
 }
 
 cudaError_t launch_attn_merge(const smx_shape_t& s, const float* part_o, const float* part_m,
-                              const float* part_l, float* out, cudaStream_t st) {
-    const int rows = s.B * s.Q * s.Hq;
-    attn_merge_kernel<<<rows, 128, 0, st>>>(part_o, part_m, part_l, out, s.num_splits, s.Q * s.Hq);
-    return cudaGetLastError();
+                              const float* part_l, float* out, bool pdl, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(s.B * s.Q * s.Hq);
+    cfg.blockDim = dim3(128);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, attn_merge_kernel, part_o, part_m, part_l, out, s.num_splits, s.Q * s.Hq,
+                              pdl ? 1 : 0);
 }
 
 }  // namespace smx

@@ -229,6 +229,39 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
     return r;
 }
 
+__device__ __forceinline__ uint4 ldg_cg_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ldg_cg_u32(const void* p) {
+    uint32_t r;
+    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float ldg_cg_f32(const float* p) {
+    float r;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(r) : "l"(p));
+    return r;
+}
+
+// Programmatic dependent launch: wait for the preceding grid's completion and memory; let the
+// next grid in the stream begin launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// The q packing rule for two floats: returns the two e4m3 bytes (lo in bits 0..7).
+__device__ __forceinline__ uint32_t pack_q2(float x0, float x1) {
+    const uint32_t c = e4m3x2_rn_sat(fminf(fabsf(x0), 448.0f), fminf(fabsf(x1), 448.0f));
+    uint32_t b0 = (c & 0xFF) | ((__float_as_uint(x0) >> 24) & 0x80u);
+    uint32_t b1 = (c >> 8) | ((__float_as_uint(x1) >> 24) & 0x80u);
+    if (x0 != x0) b0 = 0x7F;
+    if (x1 != x1) b1 = 0x7F;
+    return b0 | (b1 << 8);
+}
+
 // ---- shape helpers -----------------------------------------------------------------------------
 __device__ __forceinline__ int clamp_ctx(int ctx, int Q, int max_pages, int32_t* st) {
     const int cap = max_pages * kPage;

@@ -32,6 +32,20 @@ cudaError_t launch_attn_split(const smx_shape_t& s, const void* q, const uint8_t
                               float* part_m, float* part_l, int32_t* status, cudaStream_t st);
 
 cudaError_t launch_attn_merge(const smx_shape_t& s, const float* part_o, const float* part_m,
-                              const float* part_l, float* out, cudaStream_t st);
+                              const float* part_l, float* out, bool pdl, cudaStream_t st);
+
+// The fused step's kernels: a1 + a3 in one launch (index scorer with the insert), a2 + a4 + a5 in
+// one launch (q packing, selection from the page scores, split stage); both may be launched as
+// programmatic dependents of the preceding kernel in the stream.
+cudaError_t launch_index(const smx_shape_t& s, const uint16_t* qidx, uint8_t* idx_pool,
+                         const int32_t* page_table, const int32_t* ctx_len, float* scores, int32_t* status,
+                         const float* k_new, const float* v_new, const float* kidx_new, uint8_t* k_pool,
+                         uint8_t* v_pool, bool pdl, cudaStream_t st);
+
+cudaError_t launch_attn_select_split(const smx_shape_t& s, const float* q_f32, const void* q_bf16,
+                                     const uint8_t* k_pool, const uint8_t* v_pool, const int32_t* page_table,
+                                     const int32_t* ctx_len, const float* scores, int32_t* topk_pages,
+                                     int32_t* topk_count, float* part_o, float* part_m, float* part_l,
+                                     int32_t* status, cudaStream_t st);
 
 }  // namespace smx
