@@ -66,7 +66,8 @@ enum { SMX_KV_MXFP4 = 0, SMX_KV_E4M3_ROWSCALE = 1 };
 enum {
     SMX_DEV_BAD_PAGE_ID = 1,   /* a page-table entry outside [0, n_pool_pages) was met */
     SMX_DEV_BAD_CTX = 2,       /* ctx_len outside [Q, max_pages_per_row * 128] (row clamped) */
-    SMX_DEV_BAD_TOPK = 4       /* a selected page id outside [0, ceil(ctx_len/128)) */
+    SMX_DEV_BAD_TOPK = 4,      /* a selected page id outside [0, ceil(ctx_len/128)) */
+    SMX_DEV_TIMEOUT = 8        /* a bounded wait for a page copy gave up (the CTA stopped early) */
 };
 
 #define SMX_MXFP4_PAGE_BYTES 8704

@@ -42,6 +42,7 @@ struct AttnArgs {
     int32_t* topk_out;        // with scores: the selection is written here by one CTA per row
     int32_t* count_out;
     int region_bytes;         // shared bytes of the K/V tiles (also holds the selection keys)
+    int page_bytes;           // bytes of one K or V page (one KV head)
     int pdl;
 };
 
@@ -51,34 +52,32 @@ constexpr float kLog2eOverSqrtD = (float)(1.4426950408889634 / 11.31370849898476
 // bf16 tile [128 tokens][128 dims], 256 B rows, 16-B chunk c of row r stored at c ^ (r & 7).
 __device__ __forceinline__ uint32_t swz(int row, int chunk) { return row * 256 + ((chunk ^ (row & 7)) << 4); }
 
-// Widen one page (K or V of one KV head) to bf16 in shared memory (exact in both formats). For
-// the e4m3 row-scale pages the codes are widened unscaled and the row scales go to rscale[]:
-// K's scale multiplies the scores, V's multiplies the softmax weights.
-__device__ __forceinline__ void widen_page(const AttnArgs& a, const uint8_t* page, int valid_rows,
-                                           uint8_t* tile, float* rscale) {
-    if (a.kv_format == SMX_KV_E4M3_ROWSCALE) {
+// Widen one staged page (K or V of one KV head, raw bytes in shared memory) to bf16 tiles in
+// shared memory (exact in both formats). For the e4m3 row-scale pages the codes are widened
+// unscaled and the row scales go to rscale[]: K's scale multiplies the scores, V's multiplies
+// the softmax weights. Token rows at or past valid_rows are zero.
+__device__ __forceinline__ void widen_page(bool rs, const uint8_t* raw, int valid_rows, uint8_t* tile,
+                                           float* rscale) {
+    if (rs) {
         // 128 rows x 8 chunks of 16 codes
         for (int it = threadIdx.x; it < 128 * 8; it += blockDim.x) {
             const int r = it >> 3, c = it & 7;
             uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
             if (r < valid_rows) {
-                const uint4 w = ldg_nc_v4(page + r * 128 + c * 16);
-                const float sc = __ldg(reinterpret_cast<const float*>(page + kRsScaleOff) + r);
+                const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 128 + c * 16);
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
                 uint32_t ob[8];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    float2 lo = f16x2_to_f32x2(e4m3x2_to_f16x2(ws[i] & 0xFFFF));
-                    float2 hi = f16x2_to_f32x2(e4m3x2_to_f16x2(ws[i] >> 16));
+                    const float2 lo = f16x2_to_f32x2(e4m3x2_to_f16x2(ws[i] & 0xFFFF));
+                    const float2 hi = f16x2_to_f32x2(e4m3x2_to_f16x2(ws[i] >> 16));
                     ob[2 * i] = f32x2_to_bf16x2(lo.x, lo.y);
                     ob[2 * i + 1] = f32x2_to_bf16x2(hi.x, hi.y);
                 }
                 o0 = make_uint4(ob[0], ob[1], ob[2], ob[3]);
                 o1 = make_uint4(ob[4], ob[5], ob[6], ob[7]);
-                if (c == 0) rscale[r] = sc;
-            } else if (c == 0) {
-                rscale[r] = 0.0f;
             }
+            if (c == 0) rscale[r] = r < valid_rows ? reinterpret_cast<const float*>(raw + kRsScaleOff)[r] : 0.0f;
             *reinterpret_cast<uint4*>(tile + swz(r, 2 * c)) = o0;
             *reinterpret_cast<uint4*>(tile + swz(r, 2 * c + 1)) = o1;
         }
@@ -89,8 +88,8 @@ __device__ __forceinline__ void widen_page(const AttnArgs& a, const uint8_t* pag
         const int r = it >> 2, c = it & 3;
         uint32_t ob[16];
         if (r < valid_rows) {
-            const uint4 w = ldg_nc_v4(page + r * 64 + c * 16);
-            const float sc = e8m0_to_f32(page[kMxScaleOff + r * 4 + c]);
+            const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 64 + c * 16);
+            const float sc = e8m0_to_f32(raw[kMxScaleOff + r * 4 + c]);
             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -122,7 +121,10 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem);                          // before the tiles
     float* kscale = reinterpret_cast<float*>(smem + a.region_bytes);             // 128 floats (FP8-KV K)
     float* vscale = reinterpret_cast<float*>(smem + a.region_bytes + 512);       // 128 floats (FP8-KV V)
-    int* sel = reinterpret_cast<int*>(smem + a.region_bytes + 1024);             // selected pages
+    uint8_t* raw = smem + a.region_bytes + 1024;                                 // 2 stages x (K, V) page
+    int* sel = reinterpret_cast<int*>(raw + 4 * a.page_bytes);                  // selected pages
+    __shared__ __align__(8) uint64_t mbar[2];
+    __shared__ int stage_page[2];
 
     const int s = blockIdx.x, b = blockIdx.y;
     const int kvh = blockIdx.z / a.n_row_groups, rg = blockIdx.z % a.n_row_groups;
@@ -199,31 +201,73 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
 #pragma unroll
     for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
     float mrow0 = -INFINITY, mrow1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-    const int64_t kv_bytes = rs ? kRsPageBytes : kMxPageBytes;
     const bool warp_active = rg * a.rows_per_cta + warp * 16 < M;
+    const int page_bytes = a.page_bytes;
 
+    // ---- selected K/V pages staged by 1-D bulk copies, two pages in flight ----
+    if (threadIdx.x == 0) {
+        mbar_init(&mbar[0], 1);
+        mbar_init(&mbar[1], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    auto issue = [&](int st, int i) {  // thread 0 only
+        const int p = sel[i];
+        int64_t phys = -1;
+        if (p < 0 || p >= n_pages) {
+            flag_status(a.status, SMX_DEV_BAD_TOPK);
+        } else {
+            phys = a.page_table[(int64_t)b * a.max_pages + p];
+            if (phys < 0 || phys >= a.n_pool) {
+                flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                phys = -1;
+            }
+        }
+        if (phys < 0) {
+            stage_page[st] = -1;
+            mbar_arrive(&mbar[st]);
+            return;
+        }
+        stage_page[st] = p;
+        const int64_t off = (phys * a.Hkv + kvh) * (int64_t)page_bytes;
+        mbar_arrive_expect_tx(&mbar[st], 2u * page_bytes);
+        bulk_g2s(raw + st * 2 * page_bytes, a.k_pool + off, page_bytes, &mbar[st]);
+        bulk_g2s(raw + st * 2 * page_bytes + page_bytes, a.v_pool + off, page_bytes, &mbar[st]);
+    };
+    if (threadIdx.x == 0)
+        for (int st = 0; st < 2 && lo + st < hi; ++st) issue(st, lo + st);
+
+    bool timed_out = false;
+    int to_stage = 0;
+    uint32_t to_parity = 0;
 #pragma unroll 1
     for (int i = lo; i < hi; ++i) {
-        const int p = sel[i];
-        if (p < 0 || p >= n_pages) {
-            if (threadIdx.x == 0) flag_status(a.status, SMX_DEV_BAD_TOPK);
-            continue;
+        const int st = (i - lo) & 1;
+        const uint32_t parity = ((i - lo) >> 1) & 1;
+        const bool ok = mbar_wait_bounded(&mbar[st], parity);
+        if (__syncthreads_or(!ok)) {
+            timed_out = true;
+            to_stage = st;
+            to_parity = parity;
+            break;
         }
-        const int64_t phys = a.page_table[(int64_t)b * a.max_pages + p];
-        if (phys < 0 || phys >= a.n_pool) {
-            if (threadIdx.x == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
-            continue;
+        const int p = stage_page[st];
+        const int valid_rows = p >= 0 ? min(kPage, ctx - p * kPage) : 0;
+        if (p >= 0) {
+            const uint8_t* rk = raw + st * 2 * page_bytes;
+            widen_page(rs, rk, valid_rows, Ks, kscale);
+            widen_page(rs, rk + page_bytes, valid_rows, Vs, vscale);
         }
-        const int valid_rows = min(kPage, ctx - p * kPage);
-        __syncthreads();
-        widen_page(a, a.k_pool + (phys * a.Hkv + kvh) * kv_bytes, valid_rows, Ks, kscale);
-        widen_page(a, a.v_pool + (phys * a.Hkv + kvh) * kv_bytes, valid_rows, Vs, vscale);
-        __syncthreads();
-        if (!warp_active) continue;
+        __syncthreads();   // tiles ready; this stage's raw bytes are consumed
+        if (threadIdx.x == 0 && i + 2 < hi) {
+            fence_proxy_async_smem();
+            issue(st, i + 2);
+        }
         const int jbase = p * kPage;
+        const int n_chunks = (p >= 0 && warp_active) ? 2 : 0;
 
 #pragma unroll 1
-        for (int ch = 0; ch < 2; ++ch) {          // two chunks of 64 tokens
+        for (int ch = 0; ch < n_chunks; ++ch) {   // two chunks of 64 tokens
             // ---- S = q K^T : 16 rows x 64 tokens ----
             float sc[8][4];
 #pragma unroll
@@ -322,6 +366,15 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
                 }
             }
         }
+        __syncthreads();   // before the next page overwrites the tiles
+    }
+    if (timed_out) {
+        // give the copies still in flight a bounded chance to land before the CTA exits
+        if (threadIdx.x == 0) {
+            flag_status(a.status, SMX_DEV_TIMEOUT);
+            mbar_wait_bounded(&mbar[to_stage], to_parity);
+        }
+        __syncthreads();
     }
 
     // ---- write the partials of real rows ----
@@ -379,8 +432,9 @@ static cudaError_t launch_split_impl(const smx_shape_t& s, AttnArgs& a, bool pdl
     if (warps > 4 && (int64_t)s.num_splits * s.B * s.Hkv * ((M + 127) / 128) < 148) warps = 4;
     a.rows_per_cta = warps * 16;
     a.n_row_groups = (M + a.rows_per_cta - 1) / a.rows_per_cta;
-    a.region_bytes = max(65536, 4 * s.max_pages_per_row);
-    const size_t smem = (size_t)a.region_bytes + 1024 + 4 * (size_t)s.topk;
+    a.region_bytes = (max(65536, 4 * s.max_pages_per_row) + 127) & ~127;  // keeps the stages 128-B aligned
+    a.page_bytes = s.kv_format == SMX_KV_E4M3_ROWSCALE ? kRsPageBytes : kMxPageBytes;
+    const size_t smem = (size_t)a.region_bytes + 1024 + 4 * (size_t)a.page_bytes + 4 * (size_t)s.topk;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(attn_split_kernel), (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
