@@ -46,7 +46,7 @@ struct AttnArgs {
     int pdl;
 };
 
-constexpr int kAttnMaxWarps = 8;
+constexpr int kAttnMaxWarps = 8;   // 2 token halves x 4 row groups
 constexpr float kLog2eOverSqrtD = (float)(1.4426950408889634 / 11.313708498984761);
 
 // bf16 tile [128 tokens][128 dims], 256 B rows, 16-B chunk c of row r stored at c ^ (r & 7).
@@ -116,27 +116,32 @@ __device__ __forceinline__ void widen_page(bool rs, const uint8_t* raw, int vali
 __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ SelectSmem selsm;
+    __shared__ __align__(8) uint64_t mbar[2];
+    __shared__ int stage_page[2];
     uint8_t* Ks = smem;                  // 32 KB
     uint8_t* Vs = smem + 32768;          // 32 KB
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem);                          // before the tiles
+    float* xch = reinterpret_cast<float*>(smem);                                 // after the pages
     float* kscale = reinterpret_cast<float*>(smem + a.region_bytes);             // 128 floats (FP8-KV K)
     float* vscale = reinterpret_cast<float*>(smem + a.region_bytes + 512);       // 128 floats (FP8-KV V)
     uint8_t* raw = smem + a.region_bytes + 1024;                                 // 2 stages x (K, V) page
     int* sel = reinterpret_cast<int*>(raw + 4 * a.page_bytes);                  // selected pages
-    __shared__ __align__(8) uint64_t mbar[2];
-    __shared__ int stage_page[2];
 
     const int s = blockIdx.x, b = blockIdx.y;
     const int kvh = blockIdx.z / a.n_row_groups, rg = blockIdx.z % a.n_row_groups;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
+    const int row_warps = (blockDim.x >> 5) >> 1;   // warps per token half
+    const int wr = warp % row_warps;                // this warp's 16-row group
+    const int th = warp / row_warps;                // this warp's 64-token half of every page
     const int M = a.G * a.Q;
     const bool rs = a.kv_format == SMX_KV_E4M3_ROWSCALE;
 
     // this lane's two rows
-    const int m0 = rg * a.rows_per_cta + warp * 16 + g, m1 = m0 + 8;
+    const int m0 = rg * a.rows_per_cta + wr * 16 + g, m1 = m0 + 8;
     const bool v0 = m0 < M, v1 = m1 < M;
     const int t0 = v0 ? m0 / a.G : 0, t1 = v1 ? m1 / a.G : 0;
+    const bool warp_active = rg * a.rows_per_cta + wr * 16 < M;
 
     // q A fragments (bf16, exact) for 8 k-steps: a0/a2 row m0, a1/a3 row m1. The fused step packs
     // q from f32 here with the q packing rule (these inputs do not depend on the earlier kernels).
@@ -201,7 +206,6 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
 #pragma unroll
     for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
     float mrow0 = -INFINITY, mrow1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-    const bool warp_active = rg * a.rows_per_cta + warp * 16 < M;
     const int page_bytes = a.page_bytes;
 
     // ---- selected K/V pages staged by 1-D bulk copies, two pages in flight ----
@@ -263,11 +267,9 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
             fence_proxy_async_smem();
             issue(st, i + 2);
         }
-        const int jbase = p * kPage;
-        const int n_chunks = (p >= 0 && warp_active) ? 2 : 0;
-
-#pragma unroll 1
-        for (int ch = 0; ch < n_chunks; ++ch) {   // two chunks of 64 tokens
+        if (p >= 0 && warp_active && th * 64 < valid_rows) {
+            const int tb = th * 64;              // first token of this warp's half
+            const int jbase = p * kPage + tb;
             // ---- S = q K^T : 16 rows x 64 tokens ----
             float sc[8][4];
 #pragma unroll
@@ -277,7 +279,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
 #pragma unroll
                 for (int ks = 0; ks < 8; ks += 2) {
                     uint32_t b0, b1, b2, b3;
-                    const int row = ch * 64 + nb * 8 + (lane & 7);
+                    const int row = tb + nb * 8 + (lane & 7);
                     const int chunk = 2 * ks + (lane >> 3);
                     ldmatrix_x4(b0, b1, b2, b3, Ks + swz(row, chunk));
                     mma_bf16_16816(sc[nb], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
@@ -290,12 +292,12 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
             for (int nb = 0; nb < 8; ++nb) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const int tok = ch * 64 + nb * 8 + 2 * t + (c & 1);
-                    const int j = jbase + tok;
+                    const int tok = tb + nb * 8 + 2 * t + (c & 1);
+                    const int j = jbase + nb * 8 + 2 * t + (c & 1);
                     float z = sc[nb][c] * kLog2eOverSqrtD;
                     if (rs) z *= kscale[tok];
-                    const bool ok = (c < 2) ? (v0 && j <= pos0) : (v1 && j <= pos1);
-                    z = ok ? z : -INFINITY;
+                    const bool ok2 = (c < 2) ? (v0 && j <= pos0) : (v1 && j <= pos1);
+                    z = ok2 ? z : -INFINITY;
                     sc[nb][c] = z;
                     if (c < 2) mx0 = fmaxf(mx0, z);
                     else mx1 = fmaxf(mx1, z);
@@ -310,7 +312,8 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
             const float al1 = (mn1 == -INFINITY) ? 1.0f : exp2f(mrow1 - mn1);
             mrow0 = mn0;
             mrow1 = mn1;
-            // ---- weights: P' = p (x V row scale) as bf16 hi + lo; l sums p in fp32 ----
+            // ---- weights. MXFP4: P in bf16 (as the pages do). FP8-KV: P' = p x V row scale as a
+            // bf16 high part plus a bf16 low part (its x50 rows need ~16 bits). l sums p in fp32 ----
             uint32_t ph[8][2], pl[8][2];
             float ps0 = 0.0f, ps1 = 0.0f;
 #pragma unroll
@@ -321,21 +324,27 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
                     const float mn = (c < 2) ? mn0 : mn1;
                     e[c] = (mn == -INFINITY) ? 0.0f : exp2f(sc[nb][c] - mn);
                 }
-                ps0 += e[0] + e[1];
-                ps1 += e[2] + e[3];
                 if (rs) {
-                    const int tok = ch * 64 + nb * 8 + 2 * t;
+                    ps0 += e[0] + e[1];
+                    ps1 += e[2] + e[3];
+                    const int tok = tb + nb * 8 + 2 * t;
                     const float s0 = vscale[tok], s1 = vscale[tok + 1];
                     e[0] *= s0; e[1] *= s1; e[2] *= s0; e[3] *= s1;
                 }
                 const __nv_bfloat162 h01 = __floats2bfloat162_rn(e[0], e[1]), h23 = __floats2bfloat162_rn(e[2], e[3]);
                 const float2 r01 = __bfloat1622float2(h01), r23 = __bfloat1622float2(h23);
-                const __nv_bfloat162 l01 = __floats2bfloat162_rn(e[0] - r01.x, e[1] - r01.y);
-                const __nv_bfloat162 l23 = __floats2bfloat162_rn(e[2] - r23.x, e[3] - r23.y);
+                if (!rs) {
+                    ps0 += r01.x + r01.y;
+                    ps1 += r23.x + r23.y;
+                }
                 ph[nb][0] = *reinterpret_cast<const uint32_t*>(&h01);
                 ph[nb][1] = *reinterpret_cast<const uint32_t*>(&h23);
-                pl[nb][0] = *reinterpret_cast<const uint32_t*>(&l01);
-                pl[nb][1] = *reinterpret_cast<const uint32_t*>(&l23);
+                if (rs) {
+                    const __nv_bfloat162 l01 = __floats2bfloat162_rn(e[0] - r01.x, e[1] - r01.y);
+                    const __nv_bfloat162 l23 = __floats2bfloat162_rn(e[2] - r23.x, e[3] - r23.y);
+                    pl[nb][0] = *reinterpret_cast<const uint32_t*>(&l01);
+                    pl[nb][1] = *reinterpret_cast<const uint32_t*>(&l23);
+                }
             }
             ps0 += __shfl_xor_sync(0xFFFFFFFFu, ps0, 1);
             ps0 += __shfl_xor_sync(0xFFFFFFFFu, ps0, 2);
@@ -348,21 +357,24 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
                 o[db][0] *= al0; o[db][1] *= al0;
                 o[db][2] *= al1; o[db][3] *= al1;
             }
-            // ---- O += (P_hi + P_lo) V ----
+            // ---- O += P V ----
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint32_t a0 = ph[2 * kk][0], a1 = ph[2 * kk][1], a2 = ph[2 * kk + 1][0], a3 = ph[2 * kk + 1][1];
-                const uint32_t c0 = pl[2 * kk][0], c1 = pl[2 * kk][1], c2 = pl[2 * kk + 1][0], c3 = pl[2 * kk + 1][1];
 #pragma unroll
                 for (int db = 0; db < 16; db += 2) {
                     uint32_t b0, b1, b2, b3;
-                    const int row = ch * 64 + kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                    const int row = tb + kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
                     const int chunk = db + (lane >> 4);
                     ldmatrix_x4_trans(b0, b1, b2, b3, Vs + swz(row, chunk));
                     mma_bf16_16816(o[db], a0, a1, a2, a3, b0, b1);
                     mma_bf16_16816(o[db + 1], a0, a1, a2, a3, b2, b3);
-                    mma_bf16_16816(o[db], c0, c1, c2, c3, b0, b1);
-                    mma_bf16_16816(o[db + 1], c0, c1, c2, c3, b2, b3);
+                    if (rs) {
+                        const uint32_t c0 = pl[2 * kk][0], c1 = pl[2 * kk][1], c2 = pl[2 * kk + 1][0],
+                                       c3 = pl[2 * kk + 1][1];
+                        mma_bf16_16816(o[db], c0, c1, c2, c3, b0, b1);
+                        mma_bf16_16816(o[db + 1], c0, c1, c2, c3, b2, b3);
+                    }
                 }
             }
         }
@@ -377,8 +389,42 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
         __syncthreads();
     }
 
+    // ---- combine the two token halves: warps of half 1 hand (m, l, O) to half 0 ----
+    __syncthreads();
+    {
+        float* slot = xch + wr * (32 * 68);     // per row group: 32 lanes x (64 O + m0, m1, l0, l1)
+        if (th == 1) {
+            float* me = slot + lane * 68;
+#pragma unroll
+            for (int db = 0; db < 16; ++db) {
+                me[4 * db + 0] = o[db][0]; me[4 * db + 1] = o[db][1];
+                me[4 * db + 2] = o[db][2]; me[4 * db + 3] = o[db][3];
+            }
+            me[64] = mrow0; me[65] = mrow1; me[66] = l0; me[67] = l1;
+        }
+        __syncthreads();
+        if (th == 0) {
+            const float* ot = slot + lane * 68;
+            const float mo0 = ot[64], mo1 = ot[65], lo0 = ot[66], lo1 = ot[67];
+            const float n0 = fmaxf(mrow0, mo0), n1 = fmaxf(mrow1, mo1);
+            const float wa0 = n0 == -INFINITY ? 0.0f : exp2f(mrow0 - n0), wb0 = n0 == -INFINITY ? 0.0f : exp2f(mo0 - n0);
+            const float wa1 = n1 == -INFINITY ? 0.0f : exp2f(mrow1 - n1), wb1 = n1 == -INFINITY ? 0.0f : exp2f(mo1 - n1);
+#pragma unroll
+            for (int db = 0; db < 16; ++db) {
+                o[db][0] = o[db][0] * wa0 + ot[4 * db + 0] * wb0;
+                o[db][1] = o[db][1] * wa0 + ot[4 * db + 1] * wb0;
+                o[db][2] = o[db][2] * wa1 + ot[4 * db + 2] * wb1;
+                o[db][3] = o[db][3] * wa1 + ot[4 * db + 3] * wb1;
+            }
+            l0 = l0 * wa0 + lo0 * wb0;
+            l1 = l1 * wa1 + lo1 * wb1;
+            mrow0 = n0;
+            mrow1 = n1;
+        }
+    }
+
     // ---- write the partials of real rows ----
-    if (v0 || v1) {
+    if (th == 0 && (v0 || v1)) {
         const int h0 = kvh * a.G + m0 % a.G, h1 = kvh * a.G + m1 % a.G;
         const int64_t r0 = (((int64_t)b * a.S + s) * a.Q + t0) * a.Hq + h0;
         const int64_t r1 = (((int64_t)b * a.S + s) * a.Q + t1) * a.Hq + h1;
@@ -426,11 +472,10 @@ static cudaError_t launch_split_impl(const smx_shape_t& s, AttnArgs& a, bool pdl
     a.Hkv = s.Hkv; a.G = s.Hq / s.Hkv; a.max_pages = s.max_pages_per_row; a.topk = s.topk; a.S = s.num_splits;
     a.kv_format = s.kv_format; a.pdl = pdl ? 1 : 0;
     const int M = a.G * a.Q;
-    int warps = min(kAttnMaxWarps, (M + 15) / 16);
-    // split the query rows of a KV head over two CTAs when one CTA per (row, partition, head)
-    // would leave most SMs idle
-    if (warps > 4 && (int64_t)s.num_splits * s.B * s.Hkv * ((M + 127) / 128) < 148) warps = 4;
-    a.rows_per_cta = warps * 16;
+    // warps = 2 token halves x up to 4 groups of 16 query rows
+    const int row_warps = min(kAttnMaxWarps / 2, (M + 15) / 16);
+    const int warps = 2 * row_warps;
+    a.rows_per_cta = row_warps * 16;
     a.n_row_groups = (M + a.rows_per_cta - 1) / a.rows_per_cta;
     a.region_bytes = (max(65536, 4 * s.max_pages_per_row) + 127) & ~127;  // keeps the stages 128-B aligned
     a.page_bytes = s.kv_format == SMX_KV_E4M3_ROWSCALE ? kRsPageBytes : kMxPageBytes;

@@ -60,33 +60,138 @@ __device__ __forceinline__ float mul_exp2(float x, int k) {
     return x * exp2i_normal(k1) * exp2i_normal(k2);
 }
 
+// One lane's share of one page: 16 B of nibbles of token rows g and g+8 of the warp's two tiles,
+// and the rows' scale words.
+struct PageFrag {
+    uint4 c0[2], c1[2];
+    uint32_t sw0[2], sw1[2];
+};
+
+__device__ __forceinline__ void load_frag(PageFrag& f, const uint8_t* page, int tile0, int g, int t, bool coherent) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int r0 = (tile0 + k) * 16 + g, r1 = r0 + 8;
+        if (coherent) {   // the page was written by this kernel: read through L2
+            f.c0[k] = ldg_cg_v4(page + r0 * 64 + 16 * t);
+            f.c1[k] = ldg_cg_v4(page + r1 * 64 + 16 * t);
+            f.sw0[k] = ldg_cg_u32(page + kMxScaleOff + 4 * r0);
+            f.sw1[k] = ldg_cg_u32(page + kMxScaleOff + 4 * r1);
+        } else {
+            f.c0[k] = ldg_nc_v4(page + r0 * 64 + 16 * t);
+            f.c1[k] = ldg_nc_v4(page + r1 * 64 + 16 * t);
+            f.sw0[k] = __ldg(reinterpret_cast<const uint32_t*>(page + kMxScaleOff) + r0);
+            f.sw1[k] = __ldg(reinterpret_cast<const uint32_t*>(page + kMxScaleOff) + r1);
+        }
+    }
+}
+
+template <int NT>
+__device__ __forceinline__ float score_frag(const PageFrag& f, const uint32_t (&qf)[NT][16], const int (&sig_c)[NT][2],
+                                            int p, int tile0, int g, int t, int lim, int Q) {
+    float best = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int r0 = (tile0 + k) * 16 + g, r1 = r0 + 8;
+        uint32_t f0, f1;   // f16x2 of 2^(s_t - max s) per row
+        int e0, e1;        // max scale byte per row (0xFF marks a NaN scale)
+        {
+            const uint32_t a0 = f.sw0[k], a1 = f.sw1[k];
+            const uint32_t m0 = max(max(a0 & 0xFF, (a0 >> 8) & 0xFF), max((a0 >> 16) & 0xFF, a0 >> 24));
+            const uint32_t m1 = max(max(a1 & 0xFF, (a1 >> 8) & 0xFF), max((a1 >> 16) & 0xFF, a1 >> 24));
+            const int rel0 = (int)((a0 >> (8 * t)) & 0xFF) - (int)m0;
+            const int rel1 = (int)((a1 >> (8 * t)) & 0xFF) - (int)m1;
+            const __half h0 = rel0 >= -22 ? __float2half_rn(exp2i_normal(rel0)) : __float2half_rn(0.0f);
+            const __half h1 = rel1 >= -22 ? __float2half_rn(exp2i_normal(rel1)) : __float2half_rn(0.0f);
+            const __half2 hh0 = __halves2half2(h0, h0), hh1 = __halves2half2(h1, h1);
+            f0 = *reinterpret_cast<const uint32_t*>(&hh0);
+            f1 = *reinterpret_cast<const uint32_t*>(&hh1);
+            e0 = (int)m0;
+            e1 = (int)m1;
+        }
+        // two accumulator chains per n-tile (even and odd k-steps) for more parallel MMAs
+        float acc[NT][2][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) acc[nt][h][0] = acc[nt][h][1] = acc[nt][h][2] = acc[nt][h][3] = 0.0f;
+        const uint32_t w0[4] = {f.c0[k].x, f.c0[k].y, f.c0[k].z, f.c0[k].w};
+        const uint32_t w1[4] = {f.c1[k].x, f.c1[k].y, f.c1[k].z, f.c1[k].w};
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+            uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+            e2m1x8_to_f16x2(w0[wi], x0, x1, x2, x3);
+            e2m1x8_to_f16x2(w1[wi], y0, y1, y2, y3);
+            x0 = hmul2_u32(x0, f0); x1 = hmul2_u32(x1, f0); x2 = hmul2_u32(x2, f0); x3 = hmul2_u32(x3, f0);
+            y0 = hmul2_u32(y0, f1); y1 = hmul2_u32(y1, f1); y2 = hmul2_u32(y2, f1); y3 = hmul2_u32(y3, f1);
+            const int s0 = 2 * wi, s1 = 2 * wi + 1;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                mma_f16_16816(acc[nt][0], x0, y0, x1, y1, qf[nt][2 * s0], qf[nt][2 * s0 + 1]);
+                mma_f16_16816(acc[nt][1], x2, y2, x3, y3, qf[nt][2 * s1], qf[nt][2 * s1 + 1]);
+            }
+        }
+        const int j0 = p * kPage + r0, j1 = p * kPage + r1;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int col = c & 1;
+                const int n = nt * 8 + 2 * t + col;
+                const int j = (c < 2) ? j0 : j1;
+                const int e = (c < 2) ? e0 : e1;
+                const bool valid = (n < Q) && (j <= lim + n) && (e != 0xFF);
+                const float v = mul_exp2(acc[nt][0][c] + acc[nt][1][c], (e - 127) - sig_c[nt][col]);
+                best = valid ? fmaxf(best, v) : best;
+            }
+        }
+    }
+    return best;
+}
+
+constexpr int kIdxMaxPpc = 64;   // page-table entries of one CTA staged in shared memory
+
 template <int NT>
 __global__ void __launch_bounds__(kIdxWarps * 32, 2) index_score_kernel(IndexArgs a) {
     __shared__ __align__(16) uint32_t qh[16][64];  // f16x2 of q' per query, natural dim order
     __shared__ int sig[16];
     __shared__ float red[2][kIdxWarps];
+    __shared__ int64_t phys_s[kIdxMaxPpc];
 
     const int b = blockIdx.y;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
     if (a.pdl) pdl_wait();
-    const int ctx = clamp_ctx(a.ctx_len[b], a.Q, a.max_pages,
-                              (blockIdx.x == 0 && threadIdx.x == 0) ? a.status : nullptr);
-    const int n_pages = (ctx + kPage - 1) / kPage;
     const int p_begin = blockIdx.x * a.pages_per_cta;
     const int p_end_all = min(p_begin + a.pages_per_cta, a.max_pages);
+    // independent loads first: the row's length and this CTA's page-table entries
+    const int ctx_raw = a.ctx_len[b];
+    for (int i = threadIdx.x; i < p_end_all - p_begin; i += blockDim.x) {
+        const int64_t ph = a.page_table[(int64_t)b * a.max_pages + p_begin + i];
+        phys_s[i] = (ph < 0 || ph >= a.n_pool) ? -1 : ph;
+    }
+    const int ctx = clamp_ctx(ctx_raw, a.Q, a.max_pages, (blockIdx.x == 0 && threadIdx.x == 0) ? a.status : nullptr);
+    const int n_pages = (ctx + kPage - 1) / kPage;
     const int p_end = min(p_end_all, n_pages);
     for (int p = max(p_begin, n_pages) + threadIdx.x; p < p_end_all; p += blockDim.x)
         a.scores[(int64_t)b * a.max_pages + p] = -INFINITY;
 
     // ---- fused insert of the new tokens whose page lies in this CTA's range ----
-    bool wrote = false;
-    if (a.k_new != nullptr && p_begin < p_end) {
-        const int first_new = ctx - a.Q;
-        if (first_new / kPage < p_end && (ctx - 1) / kPage >= p_begin) {
-            wrote = true;
-            const int kinds = 1 + 2 * a.Hkv;
-            for (int r = warp; r < a.Q * kinds; r += kIdxWarps) {
+    const int first_new = ctx - a.Q;
+    const bool wrote = a.k_new != nullptr && p_begin < p_end && first_new / kPage < p_end &&
+                       (ctx - 1) / kPage >= p_begin;
+    if (wrote) {
+        const int kinds = 1 + 2 * a.Hkv;
+        const int rows = a.Q * kinds;
+        constexpr int kBatch = 8;
+        for (int r0 = warp; r0 < rows; r0 += kIdxWarps * kBatch) {
+            float4 x[kBatch];
+            int64_t dst_phys[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {   // every load of the batch in flight at once
+                const int r = r0 + u * kIdxWarps;
+                dst_phys[u] = -1;
+                x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (r >= rows) continue;
                 const int tq = r / kinds, kind = r % kinds;
                 const int pos = first_new + tq;
                 const int pg = pos / kPage;
@@ -96,29 +201,48 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 2) index_score_kernel(IndexArg
                     if (lane == 0 && kind == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
                     continue;
                 }
-                const int slot = pos % kPage;
                 const int64_t tok = (int64_t)b * a.Q + tq;
+                const float* src = kind == 0 ? a.kidx_new + tok * kD
+                                             : (kind <= a.Hkv ? a.k_new : a.v_new) + (tok * a.Hkv + (kind - 1) % a.Hkv) * kD;
+                x[u] = reinterpret_cast<const float4*>(src)[lane];
+                dst_phys[u] = phys;
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                if (dst_phys[u] < 0) continue;
+                const int r = r0 + u * kIdxWarps;
+                const int tq = r / kinds, kind = r % kinds;
+                const int slot = (first_new + tq) % kPage;
+                const int64_t phys = dst_phys[u];
                 if (kind == 0) {
-                    const float4 x = reinterpret_cast<const float4*>(a.kidx_new + tok * kD)[lane];
                     uint8_t* page = a.pool + phys * kMxPageBytes;
-                    quant_row_mxfp4_warp(x, page + slot * 64, page + kMxScaleOff + slot * 4, lane);
+                    quant_row_mxfp4_warp(x[u], page + slot * 64, page + kMxScaleOff + slot * 4, lane);
                 } else {
                     const int h = (kind - 1) % a.Hkv;
-                    const float* src = (kind <= a.Hkv ? a.k_new : a.v_new) + (tok * a.Hkv + h) * kD;
                     uint8_t* pool = kind <= a.Hkv ? a.k_pool : a.v_pool;
-                    const float4 x = reinterpret_cast<const float4*>(src)[lane];
                     if (a.kv_format == SMX_KV_E4M3_ROWSCALE) {
                         uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kRsPageBytes;
-                        quant_row_e4m3rs_warp(x, page + slot * 128,
+                        quant_row_e4m3rs_warp(x[u], page + slot * 128,
                                               reinterpret_cast<float*>(page + kRsScaleOff) + slot, lane);
                     } else {
                         uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kMxPageBytes;
-                        quant_row_mxfp4_warp(x, page + slot * 64, page + kMxScaleOff + slot * 4, lane);
+                        quant_row_mxfp4_warp(x[u], page + slot * 64, page + kMxScaleOff + slot * 4, lane);
                     }
                 }
             }
-            __threadfence();
         }
+        __threadfence();
+    }
+    __syncthreads();   // page-table entries staged; inserted rows written and fenced
+
+    const int half = warp >> 2;          // which of the two pages of an iteration
+    const int tile0 = (warp & 3) * 2;    // first of this warp's two tiles
+    // first page's loads go out before the query set-up
+    PageFrag cur;
+    {
+        const int p = p_begin + half;
+        const int64_t ph = p < p_end ? phys_s[p - p_begin] : -1;
+        if (ph >= 0) load_frag(cur, a.pool + ph * kMxPageBytes, tile0, g, t, wrote);
     }
 
     // ---- index query: f16 with a per-query power-of-two factor 2^sigma, staged in smem ----
@@ -163,94 +287,20 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 2) index_score_kernel(IndexArg
     }
 
     const int lim = ctx - a.Q;  // token j counts for query n iff j <= lim + n
-    const int half = warp >> 2;          // which of the two pages of an iteration
-    const int tile0 = (warp & 3) * 2;    // first of this warp's two tiles
     int it = 0;
 #pragma unroll 1
     for (int base = p_begin; base < p_end; base += 2, ++it) {
         const int p = base + half;
+        const int64_t ph = p < p_end ? phys_s[p - p_begin] : -1;
+        // next iteration's page in flight while this one is scored
+        PageFrag nxt;
+        const int pn = p + 2;
+        const int64_t phn = pn < p_end ? phys_s[pn - p_begin] : -1;
+        if (phn >= 0) load_frag(nxt, a.pool + phn * kMxPageBytes, tile0, g, t, wrote);
         float best = -INFINITY;
-        int64_t phys = -1;
-        if (p < p_end) {
-            phys = a.page_table[(int64_t)b * a.max_pages + p];
-            if (phys < 0 || phys >= a.n_pool) {
-                if (lane == 0 && (warp & 3) == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
-                phys = -1;
-            }
-        }
-        if (phys >= 0) {
-            const uint8_t* page = a.pool + phys * kMxPageBytes;
-            uint4 c0[2], c1[2];
-            uint32_t sw0[2], sw1[2];
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int r0 = (tile0 + k) * 16 + g, r1 = r0 + 8;
-                if (wrote) {
-                    c0[k] = ldg_cg_v4(page + r0 * 64 + 16 * t);
-                    c1[k] = ldg_cg_v4(page + r1 * 64 + 16 * t);
-                    sw0[k] = ldg_cg_u32(page + kMxScaleOff + 4 * r0);
-                    sw1[k] = ldg_cg_u32(page + kMxScaleOff + 4 * r1);
-                } else {
-                    c0[k] = ldg_nc_v4(page + r0 * 64 + 16 * t);
-                    c1[k] = ldg_nc_v4(page + r1 * 64 + 16 * t);
-                    sw0[k] = __ldg(reinterpret_cast<const uint32_t*>(page + kMxScaleOff) + r0);
-                    sw1[k] = __ldg(reinterpret_cast<const uint32_t*>(page + kMxScaleOff) + r1);
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int r0 = (tile0 + k) * 16 + g, r1 = r0 + 8;
-                uint32_t f0, f1;   // f16x2 of 2^(s_t - max s) per row
-                int e0, e1;        // max scale byte per row (0xFF marks a NaN scale)
-                {
-                    const uint32_t a0 = sw0[k], a1 = sw1[k];
-                    const uint32_t m0 = max(max(a0 & 0xFF, (a0 >> 8) & 0xFF), max((a0 >> 16) & 0xFF, a0 >> 24));
-                    const uint32_t m1 = max(max(a1 & 0xFF, (a1 >> 8) & 0xFF), max((a1 >> 16) & 0xFF, a1 >> 24));
-                    const int rel0 = (int)((a0 >> (8 * t)) & 0xFF) - (int)m0;
-                    const int rel1 = (int)((a1 >> (8 * t)) & 0xFF) - (int)m1;
-                    const __half h0 = rel0 >= -22 ? __float2half_rn(exp2i_normal(rel0)) : __float2half_rn(0.0f);
-                    const __half h1 = rel1 >= -22 ? __float2half_rn(exp2i_normal(rel1)) : __float2half_rn(0.0f);
-                    const __half2 hh0 = __halves2half2(h0, h0), hh1 = __halves2half2(h1, h1);
-                    f0 = *reinterpret_cast<const uint32_t*>(&hh0);
-                    f1 = *reinterpret_cast<const uint32_t*>(&hh1);
-                    e0 = (int)m0;
-                    e1 = (int)m1;
-                }
-                float acc[NT][4];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
-                const uint32_t w0[4] = {c0[k].x, c0[k].y, c0[k].z, c0[k].w};
-                const uint32_t w1[4] = {c1[k].x, c1[k].y, c1[k].z, c1[k].w};
-#pragma unroll
-                for (int wi = 0; wi < 4; ++wi) {
-                    uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
-                    e2m1x8_to_f16x2(w0[wi], x0, x1, x2, x3);
-                    e2m1x8_to_f16x2(w1[wi], y0, y1, y2, y3);
-                    x0 = hmul2_u32(x0, f0); x1 = hmul2_u32(x1, f0); x2 = hmul2_u32(x2, f0); x3 = hmul2_u32(x3, f0);
-                    y0 = hmul2_u32(y0, f1); y1 = hmul2_u32(y1, f1); y2 = hmul2_u32(y2, f1); y3 = hmul2_u32(y3, f1);
-                    const int s0 = 2 * wi, s1 = 2 * wi + 1;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        mma_f16_16816(acc[nt], x0, y0, x1, y1, qf[nt][2 * s0], qf[nt][2 * s0 + 1]);
-                        mma_f16_16816(acc[nt], x2, y2, x3, y3, qf[nt][2 * s1], qf[nt][2 * s1 + 1]);
-                    }
-                }
-                const int j0 = p * kPage + r0, j1 = p * kPage + r1;
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int col = c & 1;
-                        const int n = nt * 8 + 2 * t + col;
-                        const int j = (c < 2) ? j0 : j1;
-                        const int e = (c < 2) ? e0 : e1;
-                        const bool valid = (n < a.Q) && (j <= lim + n) && (e != 0xFF);
-                        const float v = mul_exp2(acc[nt][c], (e - 127) - sig_c[nt][col]);
-                        best = valid ? fmaxf(best, v) : best;
-                    }
-                }
-            }
-        }
+        if (ph >= 0) best = score_frag<NT>(cur, qf, sig_c, p, tile0, g, t, lim, a.Q);
+        else if (p < p_end && lane == 0 && (warp & 3) == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+        cur = nxt;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
         if (lane == 0) red[it & 1][warp] = best;
@@ -259,10 +309,7 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 2) index_score_kernel(IndexArg
             const int pp = base + threadIdx.x;
             if (pp < p_end) {
                 const float* r = red[it & 1] + 4 * threadIdx.x;
-                float v = fmaxf(fmaxf(r[0], r[1]), fmaxf(r[2], r[3]));
-                int64_t ph = a.page_table[(int64_t)b * a.max_pages + pp];
-                if (ph < 0 || ph >= a.n_pool) v = -INFINITY;
-                a.scores[(int64_t)b * a.max_pages + pp] = v;
+                a.scores[(int64_t)b * a.max_pages + pp] = fmaxf(fmaxf(r[0], r[1]), fmaxf(r[2], r[3]));
             }
         }
     }
@@ -296,6 +343,7 @@ static int index_pages_per_cta(const smx_shape_t& s) {
     const int64_t target = 152 * 4;
     int64_t ppc = ((int64_t)s.max_pages_per_row * s.B + target - 1) / target;
     ppc = (ppc + 1) & ~1LL;
+    if (ppc > kIdxMaxPpc) ppc = kIdxMaxPpc;
     return (int)(ppc < 2 ? 2 : ppc);
 }
 
