@@ -56,9 +56,9 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) { return row * 256 +
 // shared memory (exact in both formats). For the e4m3 row-scale pages the codes are widened
 // unscaled and the row scales go to rscale[]: K's scale multiplies the scores, V's multiplies
 // the softmax weights. Token rows at or past valid_rows are zero.
-__device__ __forceinline__ void widen_page(bool rs, const uint8_t* raw, int valid_rows, uint8_t* tile,
-                                           float* rscale) {
-    if (rs) {
+template <bool RS>
+__device__ __forceinline__ void widen_page(const uint8_t* raw, int valid_rows, uint8_t* tile, float* rscale) {
+    if (RS) {
         // 128 rows x 8 chunks of 16 codes
         for (int it = threadIdx.x; it < 128 * 8; it += blockDim.x) {
             const int r = it >> 3, c = it & 7;
@@ -113,6 +113,7 @@ __device__ __forceinline__ void widen_page(bool rs, const uint8_t* raw, int vali
     }
 }
 
+template <bool RS>
 __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ SelectSmem selsm;
@@ -135,7 +136,6 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
     const int wr = warp % row_warps;                // this warp's 16-row group
     const int th = warp / row_warps;                // this warp's 64-token half of every page
     const int M = a.G * a.Q;
-    const bool rs = a.kv_format == SMX_KV_E4M3_ROWSCALE;
 
     // this lane's two rows
     const int m0 = rg * a.rows_per_cta + wr * 16 + g, m1 = m0 + 8;
@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
             for (int half = 0; half < 2; ++half) {
                 const int d = ks * 16 + half * 8 + 2 * t;
                 uint32_t r0 = 0, r1 = 0;
-                if (rs) {
+                if (RS) {
                     const uint16_t* qb = reinterpret_cast<const uint16_t*>(a.q);
                     if (v0) r0 = *reinterpret_cast<const uint32_t*>(qb + base0 + d);
                     if (v1) r1 = *reinterpret_cast<const uint32_t*>(qb + base1 + d);
@@ -170,8 +170,9 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
                         if (v0) w0 = *reinterpret_cast<const uint16_t*>(q8 + base0 + d);
                         if (v1) w1 = *reinterpret_cast<const uint16_t*>(q8 + base1 + d);
                     }
-                    if (v0) { const float2 f = f16x2_to_f32x2(e4m3x2_to_f16x2(w0)); r0 = f32x2_to_bf16x2(f.x, f.y); }
-                    if (v1) { const float2 f = f16x2_to_f32x2(e4m3x2_to_f16x2(w1)); r1 = f32x2_to_bf16x2(f.x, f.y); }
+                    const float2 f0 = f16x2_to_f32x2(e4m3x2_to_f16x2(w0)), f1 = f16x2_to_f32x2(e4m3x2_to_f16x2(w1));
+                    r0 = f32x2_to_bf16x2(f0.x, f0.y);
+                    r1 = f32x2_to_bf16x2(f1.x, f1.y);
                 }
                 qa[ks][half * 2 + 0] = r0;
                 qa[ks][half * 2 + 1] = r1;
@@ -259,43 +260,42 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
         const int valid_rows = p >= 0 ? min(kPage, ctx - p * kPage) : 0;
         if (p >= 0) {
             const uint8_t* rk = raw + st * 2 * page_bytes;
-            widen_page(rs, rk, valid_rows, Ks, kscale);
-            widen_page(rs, rk + page_bytes, valid_rows, Vs, vscale);
+            widen_page<RS>(rk, valid_rows, Ks, kscale);
+            widen_page<RS>(rk + page_bytes, valid_rows, Vs, vscale);
         }
         __syncthreads();   // tiles ready; this stage's raw bytes are consumed
         if (threadIdx.x == 0 && i + 2 < hi) {
             fence_proxy_async_smem();
             issue(st, i + 2);
         }
-        if (p >= 0 && warp_active && th * 64 < valid_rows) {
-            const int tb = th * 64;              // first token of this warp's half
-            const int jbase = p * kPage + tb;
-            // ---- S = q K^T : 16 rows x 64 tokens ----
-            float sc[8][4];
+        // this warp's half of the page in 16-token units: QK, online softmax, one PV k-step
+        const int units = (p >= 0 && warp_active) ? max(0, min(4, (valid_rows - th * 64 + 15) / 16)) : 0;
+        const int jpage = p * kPage;
+#pragma unroll 1
+        for (int u = 0; u < units; ++u) {
+            const int tok0 = th * 64 + u * 16;
+            float sc[2][4];
 #pragma unroll
-            for (int nb = 0; nb < 8; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.0f;
-#pragma unroll
-            for (int nb = 0; nb < 8; ++nb) {
+            for (int nb = 0; nb < 2; ++nb) {
+                sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.0f;
 #pragma unroll
                 for (int ks = 0; ks < 8; ks += 2) {
                     uint32_t b0, b1, b2, b3;
-                    const int row = tb + nb * 8 + (lane & 7);
-                    const int chunk = 2 * ks + (lane >> 3);
-                    ldmatrix_x4(b0, b1, b2, b3, Ks + swz(row, chunk));
+                    ldmatrix_x4(b0, b1, b2, b3, Ks + swz(tok0 + nb * 8 + (lane & 7), 2 * ks + (lane >> 3)));
                     mma_bf16_16816(sc[nb], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
                     mma_bf16_16816(sc[nb], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2, b3);
                 }
             }
-            // ---- scale, mask, row max ----
+            // scale, mask, row max (a query token sees tokens j <= pos_t)
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int nb = 0; nb < 8; ++nb) {
+            for (int nb = 0; nb < 2; ++nb) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const int tok = tb + nb * 8 + 2 * t + (c & 1);
-                    const int j = jbase + nb * 8 + 2 * t + (c & 1);
+                    const int tok = tok0 + nb * 8 + 2 * t + (c & 1);
+                    const int j = jpage + tok;
                     float z = sc[nb][c] * kLog2eOverSqrtD;
-                    if (rs) z *= kscale[tok];
+                    if (RS) z *= kscale[tok];
                     const bool ok2 = (c < 2) ? (v0 && j <= pos0) : (v1 && j <= pos1);
                     z = ok2 ? z : -INFINITY;
                     sc[nb][c] = z;
@@ -308,73 +308,63 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
             const float mn0 = fmaxf(mrow0, mx0), mn1 = fmaxf(mrow1, mx1);
-            const float al0 = (mn0 == -INFINITY) ? 1.0f : exp2f(mrow0 - mn0);
-            const float al1 = (mn1 == -INFINITY) ? 1.0f : exp2f(mrow1 - mn1);
-            mrow0 = mn0;
-            mrow1 = mn1;
-            // ---- weights. MXFP4: P in bf16 (as the pages do). FP8-KV: P' = p x V row scale as a
-            // bf16 high part plus a bf16 low part (its x50 rows need ~16 bits). l sums p in fp32 ----
-            uint32_t ph[8][2], pl[8][2];
-            float ps0 = 0.0f, ps1 = 0.0f;
+            if (__any_sync(0xFFFFFFFFu, mn0 > mrow0 || mn1 > mrow1)) {   // a row's maximum grew
+                const float al0 = (mn0 == -INFINITY) ? 1.0f : exp2f(mrow0 - mn0);
+                const float al1 = (mn1 == -INFINITY) ? 1.0f : exp2f(mrow1 - mn1);
+                l0 *= al0;
+                l1 *= al1;
 #pragma unroll
-            for (int nb = 0; nb < 8; ++nb) {
+                for (int db = 0; db < 16; ++db) {
+                    o[db][0] *= al0; o[db][1] *= al0;
+                    o[db][2] *= al1; o[db][3] *= al1;
+                }
+                mrow0 = mn0;
+                mrow1 = mn1;
+            }
+            // weights. MXFP4: P in bf16 (as the pages do). FP8-KV: P' = p x V row scale as a bf16
+            // high part plus a bf16 low part (its x50 rows need ~16 bits). l (per lane, reduced at
+            // the end) sums the weights the PV product uses.
+            uint32_t ph[2][2], pl[2][2];
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb) {
                 float e[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const float mn = (c < 2) ? mn0 : mn1;
+                    const float mn = (c < 2) ? mrow0 : mrow1;
                     e[c] = (mn == -INFINITY) ? 0.0f : exp2f(sc[nb][c] - mn);
                 }
-                if (rs) {
-                    ps0 += e[0] + e[1];
-                    ps1 += e[2] + e[3];
-                    const int tok = tb + nb * 8 + 2 * t;
+                if (RS) {
+                    l0 += e[0] + e[1];
+                    l1 += e[2] + e[3];
+                    const int tok = tok0 + nb * 8 + 2 * t;
                     const float s0 = vscale[tok], s1 = vscale[tok + 1];
                     e[0] *= s0; e[1] *= s1; e[2] *= s0; e[3] *= s1;
                 }
                 const __nv_bfloat162 h01 = __floats2bfloat162_rn(e[0], e[1]), h23 = __floats2bfloat162_rn(e[2], e[3]);
                 const float2 r01 = __bfloat1622float2(h01), r23 = __bfloat1622float2(h23);
-                if (!rs) {
-                    ps0 += r01.x + r01.y;
-                    ps1 += r23.x + r23.y;
+                if (!RS) {
+                    l0 += r01.x + r01.y;
+                    l1 += r23.x + r23.y;
                 }
                 ph[nb][0] = *reinterpret_cast<const uint32_t*>(&h01);
                 ph[nb][1] = *reinterpret_cast<const uint32_t*>(&h23);
-                if (rs) {
+                if (RS) {
                     const __nv_bfloat162 l01 = __floats2bfloat162_rn(e[0] - r01.x, e[1] - r01.y);
                     const __nv_bfloat162 l23 = __floats2bfloat162_rn(e[2] - r23.x, e[3] - r23.y);
                     pl[nb][0] = *reinterpret_cast<const uint32_t*>(&l01);
                     pl[nb][1] = *reinterpret_cast<const uint32_t*>(&l23);
                 }
             }
-            ps0 += __shfl_xor_sync(0xFFFFFFFFu, ps0, 1);
-            ps0 += __shfl_xor_sync(0xFFFFFFFFu, ps0, 2);
-            ps1 += __shfl_xor_sync(0xFFFFFFFFu, ps1, 1);
-            ps1 += __shfl_xor_sync(0xFFFFFFFFu, ps1, 2);
-            l0 = l0 * al0 + ps0;
-            l1 = l1 * al1 + ps1;
+            // O += P V for these 16 tokens (the QK accumulator layout is PV's A layout)
 #pragma unroll
-            for (int db = 0; db < 16; ++db) {
-                o[db][0] *= al0; o[db][1] *= al0;
-                o[db][2] *= al1; o[db][3] *= al1;
-            }
-            // ---- O += P V ----
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t a0 = ph[2 * kk][0], a1 = ph[2 * kk][1], a2 = ph[2 * kk + 1][0], a3 = ph[2 * kk + 1][1];
-#pragma unroll
-                for (int db = 0; db < 16; db += 2) {
-                    uint32_t b0, b1, b2, b3;
-                    const int row = tb + kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-                    const int chunk = db + (lane >> 4);
-                    ldmatrix_x4_trans(b0, b1, b2, b3, Vs + swz(row, chunk));
-                    mma_bf16_16816(o[db], a0, a1, a2, a3, b0, b1);
-                    mma_bf16_16816(o[db + 1], a0, a1, a2, a3, b2, b3);
-                    if (rs) {
-                        const uint32_t c0 = pl[2 * kk][0], c1 = pl[2 * kk][1], c2 = pl[2 * kk + 1][0],
-                                       c3 = pl[2 * kk + 1][1];
-                        mma_bf16_16816(o[db], c0, c1, c2, c3, b0, b1);
-                        mma_bf16_16816(o[db + 1], c0, c1, c2, c3, b2, b3);
-                    }
+            for (int db = 0; db < 16; db += 2) {
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4_trans(b0, b1, b2, b3, Vs + swz(tok0 + ((lane >> 3) & 1) * 8 + (lane & 7), db + (lane >> 4)));
+                mma_bf16_16816(o[db], ph[0][0], ph[0][1], ph[1][0], ph[1][1], b0, b1);
+                mma_bf16_16816(o[db + 1], ph[0][0], ph[0][1], ph[1][0], ph[1][1], b2, b3);
+                if (RS) {
+                    mma_bf16_16816(o[db], pl[0][0], pl[0][1], pl[1][0], pl[1][1], b0, b1);
+                    mma_bf16_16816(o[db + 1], pl[0][0], pl[0][1], pl[1][0], pl[1][1], b2, b3);
                 }
             }
         }
@@ -388,6 +378,10 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
         }
         __syncthreads();
     }
+    l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
+    l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
+    l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 1);
+    l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 2);
 
     // ---- combine the two token halves: warps of half 1 hand (m, l, O) to half 0 ----
     __syncthreads();
@@ -441,30 +435,50 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
     }
 }
 
-// ---- a6 merge: one CTA of 128 threads per (b, t, h), thread d owns one output dim ----
-__global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_m,
-                                                         const float* __restrict__ part_l, float* __restrict__ out,
-                                                         int S, int QH, int pdl) {
+// ---- a6 merge: one warp per (b, t, h) row; lane l owns dims 4l..4l+3 and partitions l, l+32, ...
+constexpr int kMergeWarps = 4;
+
+__global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const float* __restrict__ part_o,
+                                                                      const float* __restrict__ part_m,
+                                                                      const float* __restrict__ part_l,
+                                                                      float* __restrict__ out, int S, int QH,
+                                                                      int rows, int pdl) {
     if (pdl) pdl_wait();
     pdl_trigger();
-    const int row = blockIdx.x;          // b * Q * Hq + t * Hq + h
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);   // b * Q * Hq + t * Hq + h
+    if (row >= rows) return;
     const int b = row / QH, r = row % QH;
-    const int d = threadIdx.x;
+    // the partitions' maxima and sums, 32 partitions per pass, all loads in flight
     float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, part_m[((int64_t)b * S + s) * QH + r]);
-    float acc = 0.0f, L = 0.0f;
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, part_m[((int64_t)b * S + s) * QH + r]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
-        for (int s = 0; s < S; ++s) {
-            const int64_t pi = ((int64_t)b * S + s) * QH + r;
-            const float m = part_m[pi];
-            if (m == -INFINITY) continue;
-            const float w = exp2f(m - M);
-            L += w * part_l[pi];
-            acc += w * part_o[pi * kD + d];
+        float L = 0.0f;
+        for (int s0 = 0; s0 < S; s0 += 32) {
+            const int s = s0 + lane;
+            float w = 0.0f;
+            if (s < S) {
+                const int64_t pi = ((int64_t)b * S + s) * QH + r;
+                const float m = part_m[pi];
+                w = (m == -INFINITY) ? 0.0f : exp2f(m - M);
+                L += w * part_l[pi];
+            }
+            const int n = min(32, S - s0);
+#pragma unroll 8
+            for (int k = 0; k < n; ++k) {
+                const float wk = __shfl_sync(0xFFFFFFFFu, w, k);
+                const float4 v = reinterpret_cast<const float4*>(part_o + (((int64_t)b * S + s0 + k) * QH + r) * kD)[lane];
+                acc.x += wk * v.x; acc.y += wk * v.y; acc.z += wk * v.z; acc.w += wk * v.w;
+            }
         }
-        acc = acc / L;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
+        acc.x /= L; acc.y /= L; acc.z /= L; acc.w /= L;
     }
-    out[(int64_t)row * kD + d] = acc;
+    reinterpret_cast<float4*>(out + (int64_t)row * kD)[lane] = acc;
 }
 
 static cudaError_t launch_split_impl(const smx_shape_t& s, AttnArgs& a, bool pdl, cudaStream_t st) {
@@ -480,7 +494,9 @@ static cudaError_t launch_split_impl(const smx_shape_t& s, AttnArgs& a, bool pdl
     a.region_bytes = (max(65536, 4 * s.max_pages_per_row) + 127) & ~127;  // keeps the stages 128-B aligned
     a.page_bytes = s.kv_format == SMX_KV_E4M3_ROWSCALE ? kRsPageBytes : kMxPageBytes;
     const size_t smem = (size_t)a.region_bytes + 1024 + 4 * (size_t)a.page_bytes + 4 * (size_t)s.topk;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(attn_split_kernel), (int)smem);
+    const void* kfn = s.kv_format == SMX_KV_E4M3_ROWSCALE ? reinterpret_cast<const void*>(attn_split_kernel<true>)
+                                                          : reinterpret_cast<const void*>(attn_split_kernel<false>);
+    cudaError_t e = ensure_smem_attr(kfn, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(s.num_splits, s.B, s.Hkv * a.n_row_groups);
@@ -492,7 +508,8 @@ static cudaError_t launch_split_impl(const smx_shape_t& s, AttnArgs& a, bool pdl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, attn_split_kernel, a);
+    if (s.kv_format == SMX_KV_E4M3_ROWSCALE) return cudaLaunchKernelEx(&cfg, attn_split_kernel<true>, a);
+    return cudaLaunchKernelEx(&cfg, attn_split_kernel<false>, a);
 }
 
 cudaError_t launch_attn_split(const smx_shape_t& s, const void* q, const uint8_t* k_pool,
@@ -522,15 +539,16 @@ cudaError_t launch_attn_select_split(const smx_shape_t& s, const float* q_f32, c
 cudaError_t launch_attn_merge(const smx_shape_t& s, const float* part_o, const float* part_m,
                               const float* part_l, float* out, bool pdl, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(s.B * s.Q * s.Hq);
-    cfg.blockDim = dim3(128);
+    const int rows = s.B * s.Q * s.Hq;
+    cfg.gridDim = dim3((rows + kMergeWarps - 1) / kMergeWarps);
+    cfg.blockDim = dim3(kMergeWarps * 32);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, attn_merge_kernel, part_o, part_m, part_l, out, s.num_splits, s.Q * s.Hq,
+    return cudaLaunchKernelEx(&cfg, attn_merge_kernel, part_o, part_m, part_l, out, s.num_splits, s.Q * s.Hq, rows,
                               pdl ? 1 : 0);
 }
 

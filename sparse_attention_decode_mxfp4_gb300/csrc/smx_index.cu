@@ -60,89 +60,77 @@ __device__ __forceinline__ float mul_exp2(float x, int k) {
     return x * exp2i_normal(k1) * exp2i_normal(k2);
 }
 
-// One lane's share of one page: 16 B of nibbles of token rows g and g+8 of the warp's two tiles,
-// and the rows' scale words.
-struct PageFrag {
-    uint4 c0[2], c1[2];
-    uint32_t sw0[2], sw1[2];
+// One lane's share of one 16-token tile: 16 B of nibbles of token rows g and g+8 and the rows'
+// scale words. Pages are read through L2 (a CTA that inserted rows must see its own writes).
+struct TileFrag {
+    uint4 c0, c1;
+    uint32_t sw0, sw1;
 };
 
-__device__ __forceinline__ void load_frag(PageFrag& f, const uint8_t* page, int tile0, int g, int t, bool coherent) {
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int r0 = (tile0 + k) * 16 + g, r1 = r0 + 8;
-        if (coherent) {   // the page was written by this kernel: read through L2
-            f.c0[k] = ldg_cg_v4(page + r0 * 64 + 16 * t);
-            f.c1[k] = ldg_cg_v4(page + r1 * 64 + 16 * t);
-            f.sw0[k] = ldg_cg_u32(page + kMxScaleOff + 4 * r0);
-            f.sw1[k] = ldg_cg_u32(page + kMxScaleOff + 4 * r1);
-        } else {
-            f.c0[k] = ldg_nc_v4(page + r0 * 64 + 16 * t);
-            f.c1[k] = ldg_nc_v4(page + r1 * 64 + 16 * t);
-            f.sw0[k] = __ldg(reinterpret_cast<const uint32_t*>(page + kMxScaleOff) + r0);
-            f.sw1[k] = __ldg(reinterpret_cast<const uint32_t*>(page + kMxScaleOff) + r1);
-        }
-    }
+__device__ __forceinline__ void load_tile(TileFrag& f, const uint8_t* page, int tile, int g, int t) {
+    const int r0 = tile * 16 + g, r1 = r0 + 8;
+    f.c0 = ldg_cg_v4(page + r0 * 64 + 16 * t);
+    f.c1 = ldg_cg_v4(page + r1 * 64 + 16 * t);
+    f.sw0 = ldg_cg_u32(page + kMxScaleOff + 4 * r0);
+    f.sw1 = ldg_cg_u32(page + kMxScaleOff + 4 * r1);
 }
 
+// Max over this lane's scores of one tile (two token rows x its query columns).
 template <int NT>
-__device__ __forceinline__ float score_frag(const PageFrag& f, const uint32_t (&qf)[NT][16], const int (&sig_c)[NT][2],
-                                            int p, int tile0, int g, int t, int lim, int Q) {
-    float best = -INFINITY;
+__device__ __forceinline__ float score_tile(const TileFrag& f, const uint32_t (&qf)[NT][16], const int (&sig_c)[NT][2],
+                                            int p, int tile, int g, int t, int lim, int Q) {
+    const int r0 = tile * 16 + g, r1 = r0 + 8;
+    uint32_t f0, f1;   // f16x2 of 2^(s_t - max s) per row
+    int e0, e1;        // max scale byte per row (0xFF marks a NaN scale)
+    {
+        const uint32_t a0 = f.sw0, a1 = f.sw1;
+        const uint32_t m0 = max(max(a0 & 0xFF, (a0 >> 8) & 0xFF), max((a0 >> 16) & 0xFF, a0 >> 24));
+        const uint32_t m1 = max(max(a1 & 0xFF, (a1 >> 8) & 0xFF), max((a1 >> 16) & 0xFF, a1 >> 24));
+        const int rel0 = (int)((a0 >> (8 * t)) & 0xFF) - (int)m0;
+        const int rel1 = (int)((a1 >> (8 * t)) & 0xFF) - (int)m1;
+        const __half h0 = rel0 >= -22 ? __float2half_rn(exp2i_normal(rel0)) : __float2half_rn(0.0f);
+        const __half h1 = rel1 >= -22 ? __float2half_rn(exp2i_normal(rel1)) : __float2half_rn(0.0f);
+        const __half2 hh0 = __halves2half2(h0, h0), hh1 = __halves2half2(h1, h1);
+        f0 = *reinterpret_cast<const uint32_t*>(&hh0);
+        f1 = *reinterpret_cast<const uint32_t*>(&hh1);
+        e0 = (int)m0;
+        e1 = (int)m1;
+    }
+    // two accumulator chains per n-tile (even and odd k-steps) for more parallel MMAs
+    float acc[NT][2][4];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int r0 = (tile0 + k) * 16 + g, r1 = r0 + 8;
-        uint32_t f0, f1;   // f16x2 of 2^(s_t - max s) per row
-        int e0, e1;        // max scale byte per row (0xFF marks a NaN scale)
-        {
-            const uint32_t a0 = f.sw0[k], a1 = f.sw1[k];
-            const uint32_t m0 = max(max(a0 & 0xFF, (a0 >> 8) & 0xFF), max((a0 >> 16) & 0xFF, a0 >> 24));
-            const uint32_t m1 = max(max(a1 & 0xFF, (a1 >> 8) & 0xFF), max((a1 >> 16) & 0xFF, a1 >> 24));
-            const int rel0 = (int)((a0 >> (8 * t)) & 0xFF) - (int)m0;
-            const int rel1 = (int)((a1 >> (8 * t)) & 0xFF) - (int)m1;
-            const __half h0 = rel0 >= -22 ? __float2half_rn(exp2i_normal(rel0)) : __float2half_rn(0.0f);
-            const __half h1 = rel1 >= -22 ? __float2half_rn(exp2i_normal(rel1)) : __float2half_rn(0.0f);
-            const __half2 hh0 = __halves2half2(h0, h0), hh1 = __halves2half2(h1, h1);
-            f0 = *reinterpret_cast<const uint32_t*>(&hh0);
-            f1 = *reinterpret_cast<const uint32_t*>(&hh1);
-            e0 = (int)m0;
-            e1 = (int)m1;
-        }
-        // two accumulator chains per n-tile (even and odd k-steps) for more parallel MMAs
-        float acc[NT][2][4];
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int h = 0; h < 2; ++h) acc[nt][h][0] = acc[nt][h][1] = acc[nt][h][2] = acc[nt][h][3] = 0.0f;
+    const uint32_t w0[4] = {f.c0.x, f.c0.y, f.c0.z, f.c0.w};
+    const uint32_t w1[4] = {f.c1.x, f.c1.y, f.c1.z, f.c1.w};
 #pragma unroll
-            for (int h = 0; h < 2; ++h) acc[nt][h][0] = acc[nt][h][1] = acc[nt][h][2] = acc[nt][h][3] = 0.0f;
-        const uint32_t w0[4] = {f.c0[k].x, f.c0[k].y, f.c0[k].z, f.c0[k].w};
-        const uint32_t w1[4] = {f.c1[k].x, f.c1[k].y, f.c1[k].z, f.c1[k].w};
-#pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
-            uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
-            e2m1x8_to_f16x2(w0[wi], x0, x1, x2, x3);
-            e2m1x8_to_f16x2(w1[wi], y0, y1, y2, y3);
-            x0 = hmul2_u32(x0, f0); x1 = hmul2_u32(x1, f0); x2 = hmul2_u32(x2, f0); x3 = hmul2_u32(x3, f0);
-            y0 = hmul2_u32(y0, f1); y1 = hmul2_u32(y1, f1); y2 = hmul2_u32(y2, f1); y3 = hmul2_u32(y3, f1);
-            const int s0 = 2 * wi, s1 = 2 * wi + 1;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                mma_f16_16816(acc[nt][0], x0, y0, x1, y1, qf[nt][2 * s0], qf[nt][2 * s0 + 1]);
-                mma_f16_16816(acc[nt][1], x2, y2, x3, y3, qf[nt][2 * s1], qf[nt][2 * s1 + 1]);
-            }
-        }
-        const int j0 = p * kPage + r0, j1 = p * kPage + r1;
+    for (int wi = 0; wi < 4; ++wi) {
+        uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+        e2m1x8_to_f16x2(w0[wi], x0, x1, x2, x3);
+        e2m1x8_to_f16x2(w1[wi], y0, y1, y2, y3);
+        x0 = hmul2_u32(x0, f0); x1 = hmul2_u32(x1, f0); x2 = hmul2_u32(x2, f0); x3 = hmul2_u32(x3, f0);
+        y0 = hmul2_u32(y0, f1); y1 = hmul2_u32(y1, f1); y2 = hmul2_u32(y2, f1); y3 = hmul2_u32(y3, f1);
+        const int s0 = 2 * wi, s1 = 2 * wi + 1;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
+            mma_f16_16816(acc[nt][0], x0, y0, x1, y1, qf[nt][2 * s0], qf[nt][2 * s0 + 1]);
+            mma_f16_16816(acc[nt][1], x2, y2, x3, y3, qf[nt][2 * s1], qf[nt][2 * s1 + 1]);
+        }
+    }
+    const int j0 = p * kPage + r0, j1 = p * kPage + r1;
+    float best = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int col = c & 1;
-                const int n = nt * 8 + 2 * t + col;
-                const int j = (c < 2) ? j0 : j1;
-                const int e = (c < 2) ? e0 : e1;
-                const bool valid = (n < Q) && (j <= lim + n) && (e != 0xFF);
-                const float v = mul_exp2(acc[nt][0][c] + acc[nt][1][c], (e - 127) - sig_c[nt][col]);
-                best = valid ? fmaxf(best, v) : best;
-            }
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int col = c & 1;
+            const int n = nt * 8 + 2 * t + col;
+            const int j = (c < 2) ? j0 : j1;
+            const int e = (c < 2) ? e0 : e1;
+            const bool valid = (n < Q) && (j <= lim + n) && (e != 0xFF);
+            const float v = mul_exp2(acc[nt][0][c] + acc[nt][1][c], (e - 127) - sig_c[nt][col]);
+            best = valid ? fmaxf(best, v) : best;
         }
     }
     return best;
@@ -237,12 +225,18 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 2) index_score_kernel(IndexArg
 
     const int half = warp >> 2;          // which of the two pages of an iteration
     const int tile0 = (warp & 3) * 2;    // first of this warp's two tiles
-    // first page's loads go out before the query set-up
-    PageFrag cur;
-    {
-        const int p = p_begin + half;
-        const int64_t ph = p < p_end ? phys_s[p - p_begin] : -1;
-        if (ph >= 0) load_frag(cur, a.pool + ph * kMxPageBytes, tile0, g, t, wrote);
+    // tasks of this warp: (iteration it, tile k) -> page p_begin + 2 it + half, tile tile0 + k
+    const int n_tasks = 2 * ((p_end - p_begin + 1) / 2);
+    auto task_page = [&](int q) { return p_begin + 2 * (q >> 1) + half; };
+    auto task_phys = [&](int q) {
+        const int p = task_page(q);
+        return p < p_end ? phys_s[p - p_begin] : (int64_t)-1;
+    };
+    // the first tile's loads go out before the query set-up
+    TileFrag cur;
+    if (n_tasks > 0) {
+        const int64_t ph = task_phys(0);
+        if (ph >= 0) load_tile(cur, a.pool + ph * kMxPageBytes, tile0, g, t);
     }
 
     // ---- index query: f16 with a per-query power-of-two factor 2^sigma, staged in smem ----
@@ -287,29 +281,33 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 2) index_score_kernel(IndexArg
     }
 
     const int lim = ctx - a.Q;  // token j counts for query n iff j <= lim + n
-    int it = 0;
+    float best = -INFINITY;
 #pragma unroll 1
-    for (int base = p_begin; base < p_end; base += 2, ++it) {
-        const int p = base + half;
-        const int64_t ph = p < p_end ? phys_s[p - p_begin] : -1;
-        // next iteration's page in flight while this one is scored
-        PageFrag nxt;
-        const int pn = p + 2;
-        const int64_t phn = pn < p_end ? phys_s[pn - p_begin] : -1;
-        if (phn >= 0) load_frag(nxt, a.pool + phn * kMxPageBytes, tile0, g, t, wrote);
-        float best = -INFINITY;
-        if (ph >= 0) best = score_frag<NT>(cur, qf, sig_c, p, tile0, g, t, lim, a.Q);
-        else if (p < p_end && lane == 0 && (warp & 3) == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+    for (int q = 0; q < n_tasks; ++q) {
+        const int p = task_page(q);
+        const int64_t ph = task_phys(q);
+        // next tile in flight while this one is scored
+        TileFrag nxt;
+        if (q + 1 < n_tasks) {
+            const int64_t phn = task_phys(q + 1);
+            if (phn >= 0) load_tile(nxt, a.pool + phn * kMxPageBytes, tile0 + ((q + 1) & 1), g, t);
+        }
+        if (ph >= 0) best = fmaxf(best, score_tile<NT>(cur, qf, sig_c, p, tile0 + (q & 1), g, t, lim, a.Q));
+        else if (p < p_end && (q & 1) == 0 && lane == 0 && (warp & 3) == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
         cur = nxt;
+        if (q & 1) {   // both tiles of this iteration's page scored: combine the page's 4 warps
+            const int it = q >> 1;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
-        if (lane == 0) red[it & 1][warp] = best;
-        __syncthreads();
-        if (threadIdx.x < 2) {
-            const int pp = base + threadIdx.x;
-            if (pp < p_end) {
-                const float* r = red[it & 1] + 4 * threadIdx.x;
-                a.scores[(int64_t)b * a.max_pages + pp] = fmaxf(fmaxf(r[0], r[1]), fmaxf(r[2], r[3]));
+            for (int o = 16; o > 0; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
+            if (lane == 0) red[it & 1][warp] = best;
+            best = -INFINITY;
+            __syncthreads();
+            if (threadIdx.x < 2) {
+                const int pp = p_begin + 2 * it + threadIdx.x;
+                if (pp < p_end) {
+                    const float* r = red[it & 1] + 4 * threadIdx.x;
+                    a.scores[(int64_t)b * a.max_pages + pp] = fmaxf(fmaxf(r[0], r[1]), fmaxf(r[2], r[3]));
+                }
             }
         }
     }
