@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--impl", default="smx", choices=["smx", "reference"])
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--splits", type=int, default=0,
-                    help="partitions of the split stage (0 = one selected page per partition, at most 16)")
+                    help="partitions of the split stage (0 = about two CTAs per SM, at most one page each)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=100)
     return ap.parse_args()
@@ -59,6 +59,15 @@ def algorithmic_bytes(w, ctx_len):
     idx = sum(n * wl.MXFP4_PAGE_BYTES for n in n_pages)
     kv = sum(min(w.topk, n) * 2 * w.Hkv * w.kv_page_bytes for n in n_pages)
     return idx, kv
+
+
+def default_splits(w):
+    """Partitions of the split stage: enough CTAs for about two per SM (a CTA covers up to 64 query
+    rows of one KV head), at most one selected page per partition."""
+    M = (w.Hq // w.Hkv) * w.Q
+    rows_per_cta = 16 * min(4, (M + 15) // 16)
+    ctas_per_split = w.B * w.Hkv * ((M + rows_per_cta - 1) // rows_per_cta)
+    return max(1, min(w.topk, 296 // ctas_per_split))
 
 
 def peaks():
@@ -226,7 +235,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     smx_build.build()
     w = wl.config(args.config)
-    shape = ops.Shape.of(w, args.splits or min(w.topk, 16))
+    shape = ops.Shape.of(w, args.splits or default_splits(w))
     data = wl.generate(w)
     idx_b, kv_b = algorithmic_bytes(w, data["ctx_len"])
     step_bytes = idx_b + kv_b

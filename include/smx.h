@@ -74,7 +74,7 @@ enum {
 #define SMX_E4M3RS_PAGE_BYTES 16896
 #define SMX_MAX_Q 16
 #define SMX_MAX_TOPK 4096
-#define SMX_MAX_PAGES_PER_ROW 32768
+#define SMX_MAX_PAGES_PER_ROW 16384  /* 2M tokens per row */
 
 typedef struct {
     int32_t B;                  /* rows (sequences) in the step */

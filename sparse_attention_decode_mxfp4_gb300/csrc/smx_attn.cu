@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
     float* vscale = reinterpret_cast<float*>(smem + a.region_bytes + 512);       // 128 floats (FP8-KV V)
     uint8_t* raw = smem + a.region_bytes + 1024;                                 // 2 stages x (K, V) page
     int* sel = reinterpret_cast<int*>(raw + 4 * a.page_bytes);                  // selected pages
+    int* pts = sel + a.topk;                                                     // the row's page table
 
     const int s = blockIdx.x, b = blockIdx.y;
     const int kvh = blockIdx.z / a.n_row_groups, rg = blockIdx.z % a.n_row_groups;
@@ -186,9 +187,15 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
     const int n_pages = (ctx + kPage - 1) / kPage;
     const int pos0 = ctx - a.Q + t0, pos1 = ctx - a.Q + t1;
     int k_eff;
+    // the row's page table comes in with the scores (one round trip), so page copies can be
+    // issued as soon as the selection is known
+    const int32_t* pt_row = a.page_table + (int64_t)b * a.max_pages;
     if (a.scores) {
         const float* sc_row = a.scores + (int64_t)b * a.max_pages;
-        for (int i = threadIdx.x; i < n_pages; i += blockDim.x) keys[i] = score_key(sc_row[i]);
+        for (int i = threadIdx.x; i < n_pages; i += blockDim.x) {
+            keys[i] = score_key(sc_row[i]);
+            pts[i] = pt_row[i];
+        }
         __syncthreads();
         k_eff = block_select(keys, n_pages, a.topk, sel, selsm);
         if (s == 0 && blockIdx.z == 0) {
@@ -197,6 +204,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
             if (threadIdx.x == 0) a.count_out[b] = k_eff;
         }
     } else {
+        for (int i = threadIdx.x; i < n_pages; i += blockDim.x) pts[i] = pt_row[i];
         k_eff = min(a.topk_count[b], min(a.topk, n_pages));
         for (int i = threadIdx.x; i < k_eff; i += blockDim.x) sel[i] = a.topk_pages[(int64_t)b * a.topk + i];
     }
@@ -222,7 +230,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
         if (p < 0 || p >= n_pages) {
             flag_status(a.status, SMX_DEV_BAD_TOPK);
         } else {
-            phys = a.page_table[(int64_t)b * a.max_pages + p];
+            phys = pts[p];
             if (phys < 0 || phys >= a.n_pool) {
                 flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
                 phys = -1;
@@ -449,33 +457,46 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const floa
     const int row = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);   // b * Q * Hq + t * Hq + h
     if (row >= rows) return;
     const int b = row / QH, r = row % QH;
-    // the partitions' maxima and sums, 32 partitions per pass, all loads in flight
-    float M = -INFINITY;
-    for (int s = lane; s < S; s += 32) M = fmaxf(M, part_m[((int64_t)b * S + s) * QH + r]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
-        float L = 0.0f;
-        for (int s0 = 0; s0 < S; s0 += 32) {
-            const int s = s0 + lane;
-            float w = 0.0f;
-            if (s < S) {
-                const int64_t pi = ((int64_t)b * S + s) * QH + r;
-                const float m = part_m[pi];
-                w = (m == -INFINITY) ? 0.0f : exp2f(m - M);
-                L += w * part_l[pi];
-            }
-            const int n = min(32, S - s0);
-#pragma unroll 8
-            for (int k = 0; k < n; ++k) {
-                const float wk = __shfl_sync(0xFFFFFFFFu, w, k);
-                const float4 v = reinterpret_cast<const float4*>(part_o + (((int64_t)b * S + s0 + k) * QH + r) * kD)[lane];
-                acc.x += wk * v.x; acc.y += wk * v.y; acc.z += wk * v.z; acc.w += wk * v.w;
-            }
+    float M = -INFINITY, L = 0.0f;
+    // 16 partitions per pass: lane l reads m, l of partition s0 + (l & 15) and dims 4l..4l+3 of all
+    // 16 partial outputs, every load of the pass in flight together
+    for (int s0 = 0; s0 < S; s0 += 16) {
+        const int n = min(16, S - s0);
+        const int sl = s0 + (lane & 15);
+        float m = -INFINITY, lv = 0.0f;
+        if ((lane & 15) < n) {
+            const int64_t pi = ((int64_t)b * S + sl) * QH + r;
+            m = part_m[pi];
+            lv = part_l[pi];
         }
+        float4 v[16];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
+        for (int k = 0; k < 16; ++k)
+            v[k] = k < n ? reinterpret_cast<const float4*>(part_o + (((int64_t)b * S + s0 + k) * QH + r) * kD)[lane]
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        float mp = m;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) mp = fmaxf(mp, __shfl_xor_sync(0xFFFFFFFFu, mp, o));
+        const float Mn = fmaxf(M, mp);
+        if (Mn != -INFINITY) {
+            const float al = (M == -INFINITY) ? 0.0f : exp2f(M - Mn);
+            acc.x *= al; acc.y *= al; acc.z *= al; acc.w *= al;
+            L *= al;
+            const float w = (m == -INFINITY) ? 0.0f : exp2f(m - Mn);
+            float lw = (lane < 16) ? w * lv : 0.0f;
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) lw += __shfl_xor_sync(0xFFFFFFFFu, lw, o);
+            L += lw;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float wk = __shfl_sync(0xFFFFFFFFu, w, k);
+                acc.x += wk * v[k].x; acc.y += wk * v[k].y; acc.z += wk * v[k].z; acc.w += wk * v[k].w;
+            }
+            M = Mn;
+        }
+    }
+    if (M != -INFINITY) {
         acc.x /= L; acc.y /= L; acc.z /= L; acc.w /= L;
     }
     reinterpret_cast<float4*>(out + (int64_t)row * kD)[lane] = acc;
@@ -493,7 +514,8 @@ static cudaError_t launch_split_impl(const smx_shape_t& s, AttnArgs& a, bool pdl
     a.n_row_groups = (M + a.rows_per_cta - 1) / a.rows_per_cta;
     a.region_bytes = (max(65536, 4 * s.max_pages_per_row) + 127) & ~127;  // keeps the stages 128-B aligned
     a.page_bytes = s.kv_format == SMX_KV_E4M3_ROWSCALE ? kRsPageBytes : kMxPageBytes;
-    const size_t smem = (size_t)a.region_bytes + 1024 + 4 * (size_t)a.page_bytes + 4 * (size_t)s.topk;
+    const size_t smem = (size_t)a.region_bytes + 1024 + 4 * (size_t)a.page_bytes + 4 * (size_t)s.topk +
+                        4 * (size_t)s.max_pages_per_row;
     const void* kfn = s.kv_format == SMX_KV_E4M3_ROWSCALE ? reinterpret_cast<const void*>(attn_split_kernel<true>)
                                                           : reinterpret_cast<const void*>(attn_split_kernel<false>);
     cudaError_t e = ensure_smem_attr(kfn, (int)smem);

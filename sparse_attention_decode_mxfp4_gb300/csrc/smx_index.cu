@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
                                                             int32_t* __restrict__ topk_pages,
                                                             int32_t* __restrict__ topk_count, int max_pages,
                                                             int topk) {
-    extern __shared__ uint32_t keys[];
+    extern __shared__ __align__(16) uint32_t keys[];
     __shared__ SelectSmem sm;
     const int b = blockIdx.x;
     const int ctx = max(0, min(ctx_len[b], max_pages * kPage));

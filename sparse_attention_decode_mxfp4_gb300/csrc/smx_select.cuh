@@ -47,8 +47,8 @@ __device__ __forceinline__ int block_excl_scan(int v, int& total, int* sm) {
     return ex;
 }
 
-// keys[0..n) (score_key values) -> out[0..k_eff) ascending page ids. out may be shared or
-// global memory. Returns k_eff. Every thread of the block must call it.
+// keys[0..n) (score_key values, 16-byte aligned shared memory) -> out[0..k_eff) ascending page
+// ids. out may be shared or global memory. Returns k_eff. Every thread of the block must call it.
 static __device__ __noinline__ int block_select(const uint32_t* keys, int n, int k, int* out, SelectSmem& sm) {
     const int k_eff = min(k, n);
     const int nthr = blockDim.x;
@@ -59,82 +59,112 @@ static __device__ __noinline__ int block_select(const uint32_t* keys, int n, int
         return k_eff;
     }
     const bool ranks = n <= 2 * nthr;
-    uint32_t T = 0;
-    int k_rem = 0;
-    if (!ranks) {
-        uint32_t prefix = 0, mask = 0;
-        k_rem = k_eff;
-#pragma unroll 1
-        for (int pass = 0; pass < 4; ++pass) {
-            const int shift = 24 - 8 * pass;
-            for (int i = threadIdx.x; i < 256; i += nthr) sm.hist[i] = 0;
-            __syncthreads();
-            for (int i = threadIdx.x; i < n; i += nthr) {
-                const uint32_t key = keys[i];
-                if ((key & mask) == prefix) atomicAdd(&sm.hist[(key >> shift) & 0xFF], 1u);
+    if (ranks) {
+        // rank of every page against all others (ties to the lower id); selected iff rank < k_eff
+        const int i0 = threadIdx.x, i1 = threadIdx.x + nthr;
+        const uint32_t k0 = i0 < n ? keys[i0] : 0u, k1 = i1 < n ? keys[i1] : 0u;
+        int r0 = 0, r1 = 0;
+        const int n4 = n & ~3;
+        const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+#pragma unroll 4
+        for (int j = 0; j < n4; j += 4) {
+            const uint4 v = k4[j >> 2];
+            const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                r0 += (kv[u] > k0) || (kv[u] == k0 && j + u < i0);
+                r1 += (kv[u] > k1) || (kv[u] == k1 && j + u < i1);
             }
-            __syncthreads();
-            if (threadIdx.x < 32) {
-                const int lane = threadIdx.x;
-                uint32_t c[8], lsum = 0;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) { c[i] = sm.hist[255 - 8 * lane - i]; lsum += c[i]; }
-                uint32_t incl = lsum;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                    if (lane >= o) incl += x;
-                }
-                const uint32_t excl = incl - lsum;
-                if (excl < (uint32_t)k_rem && incl >= (uint32_t)k_rem) {
-                    uint32_t run = excl;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        if (run + c[i] >= (uint32_t)k_rem) {
-                            sm.digit = 255 - 8 * lane - i;
-                            sm.above = run;
-                            break;
-                        }
-                        run += c[i];
-                    }
-                }
-            }
-            __syncthreads();
-            prefix |= sm.digit << shift;
-            mask |= 0xFFu << shift;
-            k_rem -= (int)sm.above;
-            __syncthreads();
         }
-        T = prefix;
+        for (int j = n4; j < n; ++j) {
+            const uint32_t kv = keys[j];
+            r0 += (kv > k0) || (kv == k0 && j < i0);
+            r1 += (kv > k1) || (kv == k1 && j < i1);
+        }
+        const int s0 = i0 < n && r0 < k_eff, s1 = i1 < n && r1 < k_eff;
+        // ids in order: i0 < nthr <= i1, so the second key's position counts all first keys
+        int tot0, tot1;
+        const int e0 = block_excl_scan(s0, tot0, sm.scan);
+        const int e1 = block_excl_scan(s1, tot1, sm.scan);
+        if (s0) out[e0] = i0;
+        if (s1) out[tot0 + e1] = i1;
+        __syncthreads();
+        return k_eff;
     }
-    int base_sel = 0, base_eq = 0;
-    for (int start = 0; start < n; start += nthr) {
-        const int i = start + threadIdx.x;
-        int sel = 0, eq = 0;
-        if (i < n) {
-            const uint32_t ki = keys[i];
-            if (ranks) {
-                int rank = 0;
-                for (int j = 0; j < n; ++j) {
-                    const uint32_t kj = keys[j];
-                    rank += (kj > ki) || (kj == ki && j < i);
+    // 4-pass 8-bit radix select of the k_eff-th key T; k_rem = how many keys equal to T to take
+    uint32_t prefix = 0, mask = 0;
+    int k_rem = k_eff;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int i = threadIdx.x; i < 256; i += nthr) sm.hist[i] = 0;
+        __syncthreads();
+        for (int i = threadIdx.x; i < n; i += nthr) {
+            const uint32_t key = keys[i];
+            if ((key & mask) == prefix) atomicAdd(&sm.hist[(key >> shift) & 0xFF], 1u);
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            const int lane = threadIdx.x;
+            uint32_t c[8], lsum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { c[i] = sm.hist[255 - 8 * lane - i]; lsum += c[i]; }
+            uint32_t incl = lsum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += x;
+            }
+            const uint32_t excl = incl - lsum;
+            if (excl < (uint32_t)k_rem && incl >= (uint32_t)k_rem) {
+                uint32_t run = excl;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (run + c[i] >= (uint32_t)k_rem) {
+                        sm.digit = 255 - 8 * lane - i;
+                        sm.above = run;
+                        break;
+                    }
+                    run += c[i];
                 }
-                sel = rank < k_eff;
-            } else {
-                sel = ki > T;
-                eq = ki == T;
             }
         }
-        if (!ranks) {
-            int t_eq;
-            const int e_eq = block_excl_scan(eq, t_eq, sm.scan);
-            sel = sel || (eq && (base_eq + e_eq) < k_rem);
-            base_eq += t_eq;
+        __syncthreads();
+        prefix |= sm.digit << shift;
+        mask |= 0xFFu << shift;
+        k_rem -= (int)sm.above;
+        __syncthreads();
+    }
+    const uint32_t T = prefix;
+    // compaction in page-id order: thread u owns up to 32 consecutive ids of a chunk
+    int base_sel = 0, base_eq = 0;
+    const int chunk = nthr * 32;
+    for (int c0 = 0; c0 < n; c0 += chunk) {
+        const int per = (min(chunk, n - c0) + nthr - 1) / nthr;
+        const int i0 = c0 + threadIdx.x * per;
+        const int i1 = min(i0 + per, n);
+        uint32_t gt_bits = 0, eq_bits = 0;
+        for (int i = i0; i < i1; ++i) {
+            const uint32_t key = keys[i];
+            gt_bits |= (uint32_t)(key > T) << (i - i0);
+            eq_bits |= (uint32_t)(key == T) << (i - i0);
+        }
+        int t_eq;
+        const int e_eq = block_excl_scan(__popc(eq_bits), t_eq, sm.scan);
+        int taken = 0;
+        uint32_t sel_bits = gt_bits;
+        for (int i = i0; i < i1; ++i) {
+            if ((eq_bits >> (i - i0)) & 1u) {
+                if (base_eq + e_eq + taken < k_rem) sel_bits |= 1u << (i - i0);
+                ++taken;
+            }
         }
         int t_sel;
-        const int e_sel = block_excl_scan(sel, t_sel, sm.scan);
-        if (sel) out[base_sel + e_sel] = i;
+        int pos = base_sel + block_excl_scan(__popc(sel_bits), t_sel, sm.scan);
+        for (int i = i0; i < i1; ++i)
+            if ((sel_bits >> (i - i0)) & 1u) out[pos++] = i;
         base_sel += t_sel;
+        base_eq += t_eq;
     }
     __syncthreads();
     return k_eff;
