@@ -55,7 +55,7 @@ typedef struct CUstream_st* smx_stream_t; /* the same type as cudaStream_t */
 enum {
     SMX_OK = 0,
     SMX_ERR_INVALID_ARG = -1,  /* null pointer, non-positive size, Hq % Hkv != 0, ... */
-    SMX_ERR_UNSUPPORTED = -2,  /* D, Di or page_tokens != 128, Q > 16, unknown kv_format */
+    SMX_ERR_UNSUPPORTED = -2,  /* D, Di or page_tokens != 128, Q > 16, unknown kv_format, limits */
     SMX_ERR_CUDA = -3,         /* a kernel launch failed (cudaGetLastError) */
     SMX_ERR_WORKSPACE = -4     /* workspace pointer null or smaller than smx_workspace_bytes */
 };
@@ -91,8 +91,11 @@ typedef struct {
     int32_t kv_format;          /* SMX_KV_*: K/V page format; the index pool is always MXFP4 */
 } smx_shape_t;
 
-/* Bytes of device workspace smx_decode_step needs for this shape (page scores, packed q,
- * split partials, alignment padding). */
+/* Bytes of device workspace smx_decode_step needs for this shape (per-row arrival counters, page
+ * scores, packed q, the selection, split partials, alignment padding). Zero the workspace once
+ * before its first use: the arrival counters it holds must start at zero, and every call leaves
+ * them at zero again. One workspace serves one shape; calls that share a workspace must not
+ * overlap on the GPU. */
 size_t smx_workspace_bytes(const smx_shape_t* shape);
 
 /* a1 -- [ATOM-2812] "--index-cache-dtype mxfp4" (index-K row store: E8M0 group scale =
@@ -155,7 +158,9 @@ int smx_sparse_attn_merge(const smx_shape_t* shape, const float* part_o, const f
 /* The whole step (a1..a6) on `stream`. q_f32 is required for MXFP4 K/V, q_bf16 for E4M3
  * row-scale K/V (the other may be NULL). Pools are updated in place (the Q new rows).
  * topk_pages/topk_count are outputs; workspace holds ws_bytes >= smx_workspace_bytes(shape)
- * bytes of scratch (256-byte aligned). */
+ * bytes of scratch (256-byte aligned, zeroed before its first use). Three kernels: the scorer
+ * (insert, q packing, page scores, and the selection in the last CTA of each row to finish),
+ * the split stage and the merge, each a programmatic dependent of the one before. */
 int smx_decode_step(const smx_shape_t* shape, const float* q_f32, const uint16_t* q_bf16,
                     const uint16_t* qidx_bf16, const float* k_new, const float* v_new,
                     const float* kidx_new, const int32_t* page_table, const int32_t* ctx_len,

@@ -54,6 +54,7 @@ int check_shape(const smx_shape_t* s) {
     if (s->Q > SMX_MAX_Q) return SMX_ERR_UNSUPPORTED;
     if (s->kv_format != SMX_KV_MXFP4 && s->kv_format != SMX_KV_E4M3_ROWSCALE) return SMX_ERR_UNSUPPORTED;
     if (s->topk > SMX_MAX_TOPK || s->max_pages_per_row > SMX_MAX_PAGES_PER_ROW) return SMX_ERR_UNSUPPORTED;
+    if (s->n_pool_pages > 0x7FFFFFFF) return SMX_ERR_UNSUPPORTED;
     if (s->B > 65535 || s->num_splits > 65535 || (int64_t)s->Hkv * s->Hq * s->Q > 65535)
         return SMX_ERR_UNSUPPORTED;
     return SMX_OK;
@@ -62,8 +63,12 @@ int check_shape(const smx_shape_t* s) {
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? SMX_OK : SMX_ERR_CUDA; }
 
 struct Workspace {
-    float* scores;
-    uint8_t* q8;
+    float* scores;        // [B][max_pages]
+    uint16_t* qbf;        // [B][Q][Hq][128] packed q as bf16 (MXFP4 K/V)
+    int32_t* arrivals;    // [B] per-row arrival counters of the scorer (zero between calls)
+    int32_t* sel_pages;   // [B][topk]
+    int32_t* sel_phys;    // [B][topk]
+    int32_t* sel_count;   // [B]
     float* part_o;
     float* part_m;
     float* part_l;
@@ -72,19 +77,24 @@ struct Workspace {
 
 Workspace layout(const smx_shape_t* s, void* base) {
     Workspace w;
-    uint8_t* p = reinterpret_cast<uint8_t*>(base);
+    const uintptr_t p = reinterpret_cast<uintptr_t>(base);
     size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const uintptr_t at = p + off;
+        off = align_up(off + bytes);
+        return at;
+    };
     const size_t rows = (size_t)s->B * s->num_splits * s->Q * s->Hq;
-    w.scores = reinterpret_cast<float*>(p + off);
-    off = align_up(off + (size_t)s->B * s->max_pages_per_row * sizeof(float));
-    w.q8 = p + off;
-    off = align_up(off + (size_t)s->B * s->Q * s->Hq * 128);
-    w.part_o = reinterpret_cast<float*>(p + off);
-    off = align_up(off + rows * 128 * sizeof(float));
-    w.part_m = reinterpret_cast<float*>(p + off);
-    off = align_up(off + rows * sizeof(float));
-    w.part_l = reinterpret_cast<float*>(p + off);
-    off = align_up(off + rows * sizeof(float));
+    // the arrival counters come first so that a zeroed prefix is easy to keep
+    w.arrivals = reinterpret_cast<int32_t*>(take((size_t)s->B * sizeof(int32_t)));
+    w.scores = reinterpret_cast<float*>(take((size_t)s->B * s->max_pages_per_row * sizeof(float)));
+    w.qbf = reinterpret_cast<uint16_t*>(take((size_t)s->B * s->Q * s->Hq * 128 * sizeof(uint16_t)));
+    w.sel_pages = reinterpret_cast<int32_t*>(take((size_t)s->B * s->topk * sizeof(int32_t)));
+    w.sel_phys = reinterpret_cast<int32_t*>(take((size_t)s->B * s->topk * sizeof(int32_t)));
+    w.sel_count = reinterpret_cast<int32_t*>(take((size_t)s->B * sizeof(int32_t)));
+    w.part_o = reinterpret_cast<float*>(take(rows * 128 * sizeof(float)));
+    w.part_m = reinterpret_cast<float*>(take(rows * sizeof(float)));
+    w.part_l = reinterpret_cast<float*>(take(rows * sizeof(float)));
     w.bytes = off;
     return w;
 }
@@ -204,14 +214,23 @@ int smx_decode_step(const smx_shape_t* s, const float* q_f32, const uint16_t* q_
         return SMX_ERR_WORKSPACE;
     const Workspace w = layout(s, workspace);
     cudaStream_t st = (cudaStream_t)stream;
-    // 1) insert + index scores, 2) q packing + top-k + split stage, 3) merge; each kernel is a
-    //    programmatic dependent of the one before it and waits for it before reading its output.
+    // 1) insert, q packing, index scores and (last CTA of each row) the selection; 2) split stage;
+    // 3) merge. Each kernel is a programmatic dependent of the one before it and waits for it
+    //    before reading its output.
+    smx::FusedSelect fs;
+    fs.q_f32 = rs ? nullptr : q_f32;
+    fs.qbf = w.qbf;
+    fs.arrivals = w.arrivals;
+    fs.sel_pages = w.sel_pages;
+    fs.sel_phys = w.sel_phys;
+    fs.sel_count = w.sel_count;
+    fs.topk_out = topk_pages;
+    fs.count_out = topk_count;
     if (smx::launch_index(*s, qidx_bf16, idx_pool, page_table, ctx_len, w.scores, dev_status, k_new, v_new,
-                          kidx_new, k_pool, v_pool, true, st) != cudaSuccess)
+                          kidx_new, k_pool, v_pool, true, st, &fs) != cudaSuccess)
         return SMX_ERR_CUDA;
-    if (smx::launch_attn_select_split(*s, q_f32, q_bf16, k_pool, v_pool, page_table, ctx_len, w.scores,
-                                      topk_pages, topk_count, w.part_o, w.part_m, w.part_l, dev_status,
-                                      st) != cudaSuccess)
+    if (smx::launch_attn_fused_split(*s, rs ? q_bf16 : w.qbf, k_pool, v_pool, ctx_len, w.sel_pages, w.sel_phys,
+                                     w.sel_count, w.part_o, w.part_m, w.part_l, dev_status, st) != cudaSuccess)
         return SMX_ERR_CUDA;
     return cuda_status(smx::launch_attn_merge(*s, w.part_o, w.part_m, w.part_l, out, true, st));
 }

@@ -36,11 +36,12 @@ struct AttnArgs {
     int32_t* status;
     int64_t n_pool;
     int B, Q, Hq, Hkv, G, max_pages, topk, S, kv_format, rows_per_cta, n_row_groups;
-    // fused step: q from f32 with the packing rule, the selection from the page scores
-    const float* q_f32;       // MXFP4 K/V: q before packing (else nullptr: q is packed bytes)
-    const float* scores;      // [B][max_pages] (else nullptr: topk_pages/topk_count are inputs)
-    int32_t* topk_out;        // with scores: the selection is written here by one CTA per row
-    int32_t* count_out;
+    // fused step: q as bf16 (packed by the scorer for MXFP4, the caller's for FP8-KV) and the
+    // row's selection staged by the scorer's last CTA
+    const uint16_t* qbf;      // [B][Q][Hq][128]
+    const int32_t* sel_pages; // [B][topk]
+    const int32_t* sel_phys;  // [B][topk]
+    const int32_t* sel_count; // [B]
     int region_bytes;         // shared bytes of the K/V tiles (also holds the selection keys)
     int page_bytes;           // bytes of one K or V page (one KV head)
     int pdl;
@@ -113,7 +114,7 @@ __device__ __forceinline__ void widen_page(const uint8_t* raw, int valid_rows, u
     }
 }
 
-template <bool RS>
+template <bool RS, bool FUSED>
 __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ SelectSmem selsm;
@@ -121,13 +122,12 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
     __shared__ int stage_page[2];
     uint8_t* Ks = smem;                  // 32 KB
     uint8_t* Vs = smem + 32768;          // 32 KB
-    uint32_t* keys = reinterpret_cast<uint32_t*>(smem);                          // before the tiles
     float* xch = reinterpret_cast<float*>(smem);                                 // after the pages
     float* kscale = reinterpret_cast<float*>(smem + a.region_bytes);             // 128 floats (FP8-KV K)
     float* vscale = reinterpret_cast<float*>(smem + a.region_bytes + 512);       // 128 floats (FP8-KV V)
     uint8_t* raw = smem + a.region_bytes + 1024;                                 // 2 stages x (K, V) page
-    int* sel = reinterpret_cast<int*>(raw + 4 * a.page_bytes);                  // selected pages
-    int* pts = sel + a.topk;                                                     // the row's page table
+    int* sel = reinterpret_cast<int*>(raw + 4 * a.page_bytes);                  // this partition's pages
+    int* selph = sel + a.topk;                                                   // and their physical ids
 
     const int s = blockIdx.x, b = blockIdx.y;
     const int kvh = blockIdx.z / a.n_row_groups, rg = blockIdx.z % a.n_row_groups;
@@ -144,72 +144,67 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
     const int t0 = v0 ? m0 / a.G : 0, t1 = v1 ? m1 / a.G : 0;
     const bool warp_active = rg * a.rows_per_cta + wr * 16 < M;
 
-    // q A fragments (bf16, exact) for 8 k-steps: a0/a2 row m0, a1/a3 row m1. The fused step packs
-    // q from f32 here with the q packing rule (these inputs do not depend on the earlier kernels).
-    uint32_t qa[8][4];
-    {
-        const int h0 = kvh * a.G + (v0 ? m0 % a.G : 0), h1 = kvh * a.G + (v1 ? m1 % a.G : 0);
-        const int64_t base0 = (((int64_t)b * a.Q + t0) * a.Hq + h0) * kD;
-        const int64_t base1 = (((int64_t)b * a.Q + t1) * a.Hq + h1) * kD;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int d = ks * 16 + half * 8 + 2 * t;
-                uint32_t r0 = 0, r1 = 0;
-                if (RS) {
-                    const uint16_t* qb = reinterpret_cast<const uint16_t*>(a.q);
-                    if (v0) r0 = *reinterpret_cast<const uint32_t*>(qb + base0 + d);
-                    if (v1) r1 = *reinterpret_cast<const uint32_t*>(qb + base1 + d);
-                } else {
-                    uint32_t w0 = 0, w1 = 0;
-                    if (a.q_f32) {
-                        if (v0) { const float2 f = *reinterpret_cast<const float2*>(a.q_f32 + base0 + d); w0 = pack_q2(f.x, f.y); }
-                        if (v1) { const float2 f = *reinterpret_cast<const float2*>(a.q_f32 + base1 + d); w1 = pack_q2(f.x, f.y); }
-                    } else {
-                        const uint8_t* q8 = reinterpret_cast<const uint8_t*>(a.q);
-                        if (v0) w0 = *reinterpret_cast<const uint16_t*>(q8 + base0 + d);
-                        if (v1) w1 = *reinterpret_cast<const uint16_t*>(q8 + base1 + d);
-                    }
-                    const float2 f0 = f16x2_to_f32x2(e4m3x2_to_f16x2(w0)), f1 = f16x2_to_f32x2(e4m3x2_to_f16x2(w1));
-                    r0 = f32x2_to_bf16x2(f0.x, f0.y);
-                    r1 = f32x2_to_bf16x2(f1.x, f1.y);
-                }
-                qa[ks][half * 2 + 0] = r0;
-                qa[ks][half * 2 + 1] = r1;
-            }
-        }
-    }
-    if (a.pdl) pdl_wait();
-    pdl_trigger();
-
     const int ctx = clamp_ctx(a.ctx_len[b], a.Q, a.max_pages, nullptr);
     const int n_pages = (ctx + kPage - 1) / kPage;
     const int pos0 = ctx - a.Q + t0, pos1 = ctx - a.Q + t1;
-    int k_eff;
-    // the row's page table comes in with the scores (one round trip), so page copies can be
-    // issued as soon as the selection is known
-    const int32_t* pt_row = a.page_table + (int64_t)b * a.max_pages;
-    if (a.scores) {
-        const float* sc_row = a.scores + (int64_t)b * a.max_pages;
-        for (int i = threadIdx.x; i < n_pages; i += blockDim.x) {
-            keys[i] = score_key(sc_row[i]);
-            pts[i] = pt_row[i];
+    if (FUSED && a.pdl) pdl_wait();
+    pdl_trigger();
+    // q A fragments (bf16, exact) for 8 k-steps: a0/a2 row m0, a1/a3 row m1; lane (g, t) holds
+    // dims 16 ks + 8 h + 2t, +1. All loads in flight together.
+    uint32_t qa[8][4];
+    {
+        const int mc0 = v0 ? m0 : 0, mc1 = v1 ? m1 : 0;   // padding rows read row 0, then zero it
+        const int64_t base0 = (((int64_t)b * a.Q + mc0 / a.G) * a.Hq + kvh * a.G + mc0 % a.G) * kD + 2 * t;
+        const int64_t base1 = (((int64_t)b * a.Q + mc1 / a.G) * a.Hq + kvh * a.G + mc1 % a.G) * kD + 2 * t;
+        if (RS || FUSED) {
+            const uint16_t* qb = FUSED && !RS ? a.qbf : reinterpret_cast<const uint16_t*>(a.q);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                qa[k >> 1][(k & 1) * 2 + 0] = *reinterpret_cast<const uint32_t*>(qb + base0 + 8 * k);
+                qa[k >> 1][(k & 1) * 2 + 1] = *reinterpret_cast<const uint32_t*>(qb + base1 + 8 * k);
+            }
+        } else {
+            const uint8_t* q8 = reinterpret_cast<const uint8_t*>(a.q);
+            uint32_t w0[16], w1[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                w0[k] = *reinterpret_cast<const uint16_t*>(q8 + base0 + 8 * k);
+                w1[k] = *reinterpret_cast<const uint16_t*>(q8 + base1 + 8 * k);
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float2 g0 = f16x2_to_f32x2(e4m3x2_to_f16x2(w0[k])), g1 = f16x2_to_f32x2(e4m3x2_to_f16x2(w1[k]));
+                qa[k >> 1][(k & 1) * 2 + 0] = f32x2_to_bf16x2(g0.x, g0.y);
+                qa[k >> 1][(k & 1) * 2 + 1] = f32x2_to_bf16x2(g1.x, g1.y);
+            }
         }
-        __syncthreads();
-        k_eff = block_select(keys, n_pages, a.topk, sel, selsm);
-        if (s == 0 && blockIdx.z == 0) {
-            for (int i = threadIdx.x; i < a.topk; i += blockDim.x)
-                a.topk_out[(int64_t)b * a.topk + i] = i < k_eff ? sel[i] : -1;
-            if (threadIdx.x == 0) a.count_out[b] = k_eff;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (!v0) qa[k][0] = qa[k][2] = 0;
+            if (!v1) qa[k][1] = qa[k][3] = 0;
         }
-    } else {
-        for (int i = threadIdx.x; i < n_pages; i += blockDim.x) pts[i] = pt_row[i];
-        k_eff = min(a.topk_count[b], min(a.topk, n_pages));
-        for (int i = threadIdx.x; i < k_eff; i += blockDim.x) sel[i] = a.topk_pages[(int64_t)b * a.topk + i];
+    }
+    // this partition's pages and their physical ids
+    const int k_eff = FUSED ? max(0, min(a.sel_count[b], min(a.topk, n_pages)))
+                            : max(0, min(a.topk_count[b], min(a.topk, n_pages)));
+    const int lo = (int)(((int64_t)s * k_eff) / a.S), hi = (int)(((int64_t)(s + 1) * k_eff) / a.S);
+    for (int i = threadIdx.x; i < hi - lo; i += blockDim.x) {
+        const int64_t at = (int64_t)b * a.topk + lo + i;
+        const int p = FUSED ? a.sel_pages[at] : a.topk_pages[at];
+        int ph = -1;
+        if (p < 0 || p >= n_pages) {
+            flag_status(a.status, SMX_DEV_BAD_TOPK);
+        } else if (FUSED) {
+            ph = a.sel_phys[at];
+        } else {
+            const int64_t v = a.page_table[(int64_t)b * a.max_pages + p];
+            if (v >= 0 && v < a.n_pool) ph = (int)v;
+            else flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+        }
+        sel[i] = p;
+        selph[i] = ph;
     }
     __syncthreads();
-    const int lo = (int)(((int64_t)s * k_eff) / a.S), hi = (int)(((int64_t)(s + 1) * k_eff) / a.S);
 
     float o[16][4];
 #pragma unroll
@@ -225,17 +220,8 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
     }
     __syncthreads();
     auto issue = [&](int st, int i) {  // thread 0 only
-        const int p = sel[i];
-        int64_t phys = -1;
-        if (p < 0 || p >= n_pages) {
-            flag_status(a.status, SMX_DEV_BAD_TOPK);
-        } else {
-            phys = pts[p];
-            if (phys < 0 || phys >= a.n_pool) {
-                flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
-                phys = -1;
-            }
-        }
+        const int p = sel[i - lo];
+        const int64_t phys = selph[i - lo];
         if (phys < 0) {
             stage_page[st] = -1;
             mbar_arrive(&mbar[st]);
@@ -284,15 +270,16 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
             const int tok0 = th * 64 + u * 16;
             float sc[2][4];
 #pragma unroll
-            for (int nb = 0; nb < 2; ++nb) {
-                sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.0f;
+            for (int nb = 0; nb < 2; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.0f;
 #pragma unroll
-                for (int ks = 0; ks < 8; ks += 2) {
-                    uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4(b0, b1, b2, b3, Ks + swz(tok0 + nb * 8 + (lane & 7), 2 * ks + (lane >> 3)));
-                    mma_bf16_16816(sc[nb], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-                    mma_bf16_16816(sc[nb], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2, b3);
-                }
+            for (int ks = 0; ks < 8; ks += 2) {
+                uint32_t b0, b1, b2, b3, c0, c1, c2, c3;
+                ldmatrix_x4(b0, b1, b2, b3, Ks + swz(tok0 + (lane & 7), 2 * ks + (lane >> 3)));
+                ldmatrix_x4(c0, c1, c2, c3, Ks + swz(tok0 + 8 + (lane & 7), 2 * ks + (lane >> 3)));
+                mma_bf16_16816(sc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+                mma_bf16_16816(sc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], c0, c1);
+                mma_bf16_16816(sc[0], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2, b3);
+                mma_bf16_16816(sc[1], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], c2, c3);
             }
             // scale, mask, row max (a query token sees tokens j <= pos_t)
             float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -502,22 +489,24 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const floa
     reinterpret_cast<float4*>(out + (int64_t)row * kD)[lane] = acc;
 }
 
-static cudaError_t launch_split_impl(const smx_shape_t& s, AttnArgs& a, bool pdl, cudaStream_t st) {
+static cudaError_t launch_split_impl(const smx_shape_t& s, AttnArgs& a, bool fused, cudaStream_t st) {
     a.n_pool = s.n_pool_pages; a.B = s.B; a.Q = s.Q; a.Hq = s.Hq;
     a.Hkv = s.Hkv; a.G = s.Hq / s.Hkv; a.max_pages = s.max_pages_per_row; a.topk = s.topk; a.S = s.num_splits;
-    a.kv_format = s.kv_format; a.pdl = pdl ? 1 : 0;
+    a.kv_format = s.kv_format; a.pdl = fused ? 1 : 0;
     const int M = a.G * a.Q;
     // warps = 2 token halves x up to 4 groups of 16 query rows
     const int row_warps = min(kAttnMaxWarps / 2, (M + 15) / 16);
     const int warps = 2 * row_warps;
     a.rows_per_cta = row_warps * 16;
     a.n_row_groups = (M + a.rows_per_cta - 1) / a.rows_per_cta;
-    a.region_bytes = (max(65536, 4 * s.max_pages_per_row) + 127) & ~127;  // keeps the stages 128-B aligned
+    a.region_bytes = 65536;
     a.page_bytes = s.kv_format == SMX_KV_E4M3_ROWSCALE ? kRsPageBytes : kMxPageBytes;
-    const size_t smem = (size_t)a.region_bytes + 1024 + 4 * (size_t)a.page_bytes + 4 * (size_t)s.topk +
-                        4 * (size_t)s.max_pages_per_row;
-    const void* kfn = s.kv_format == SMX_KV_E4M3_ROWSCALE ? reinterpret_cast<const void*>(attn_split_kernel<true>)
-                                                          : reinterpret_cast<const void*>(attn_split_kernel<false>);
+    const size_t smem = (size_t)a.region_bytes + 1024 + 4 * (size_t)a.page_bytes + 8 * (size_t)s.topk;
+    const bool rs = s.kv_format == SMX_KV_E4M3_ROWSCALE;
+    const void* kfn = rs ? (fused ? reinterpret_cast<const void*>(attn_split_kernel<true, true>)
+                                  : reinterpret_cast<const void*>(attn_split_kernel<true, false>))
+                         : (fused ? reinterpret_cast<const void*>(attn_split_kernel<false, true>)
+                                  : reinterpret_cast<const void*>(attn_split_kernel<false, false>));
     cudaError_t e = ensure_smem_attr(kfn, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -529,9 +518,11 @@ static cudaError_t launch_split_impl(const smx_shape_t& s, AttnArgs& a, bool pdl
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    if (s.kv_format == SMX_KV_E4M3_ROWSCALE) return cudaLaunchKernelEx(&cfg, attn_split_kernel<true>, a);
-    return cudaLaunchKernelEx(&cfg, attn_split_kernel<false>, a);
+    cfg.numAttrs = fused ? 1 : 0;
+    if (rs) return fused ? cudaLaunchKernelEx(&cfg, attn_split_kernel<true, true>, a)
+                         : cudaLaunchKernelEx(&cfg, attn_split_kernel<true, false>, a);
+    return fused ? cudaLaunchKernelEx(&cfg, attn_split_kernel<false, true>, a)
+                 : cudaLaunchKernelEx(&cfg, attn_split_kernel<false, false>, a);
 }
 
 cudaError_t launch_attn_split(const smx_shape_t& s, const void* q, const uint8_t* k_pool,
@@ -545,15 +536,13 @@ cudaError_t launch_attn_split(const smx_shape_t& s, const void* q, const uint8_t
     return launch_split_impl(s, a, false, st);
 }
 
-cudaError_t launch_attn_select_split(const smx_shape_t& s, const float* q_f32, const void* q_bf16,
-                                     const uint8_t* k_pool, const uint8_t* v_pool, const int32_t* page_table,
-                                     const int32_t* ctx_len, const float* scores, int32_t* topk_pages,
-                                     int32_t* topk_count, float* part_o, float* part_m, float* part_l,
-                                     int32_t* status, cudaStream_t st) {
+cudaError_t launch_attn_fused_split(const smx_shape_t& s, const uint16_t* qbf, const uint8_t* k_pool,
+                                    const uint8_t* v_pool, const int32_t* ctx_len, const int32_t* sel_pages,
+                                    const int32_t* sel_phys, const int32_t* sel_count, float* part_o,
+                                    float* part_m, float* part_l, int32_t* status, cudaStream_t st) {
     AttnArgs a = {};
-    a.q = q_bf16; a.q_f32 = s.kv_format == SMX_KV_E4M3_ROWSCALE ? nullptr : q_f32;
-    a.k_pool = k_pool; a.v_pool = v_pool; a.page_table = page_table; a.ctx_len = ctx_len;
-    a.scores = scores; a.topk_out = topk_pages; a.count_out = topk_count;
+    a.q = qbf; a.qbf = qbf; a.k_pool = k_pool; a.v_pool = v_pool; a.ctx_len = ctx_len;
+    a.sel_pages = sel_pages; a.sel_phys = sel_phys; a.sel_count = sel_count;
     a.part_o = part_o; a.part_m = part_m; a.part_l = part_l; a.status = status;
     return launch_split_impl(s, a, true, st);
 }

@@ -47,6 +47,18 @@ struct IndexArgs {
     uint8_t* v_pool;
     int Hkv, kv_format;
     int pdl;                  // wait for the preceding grid before touching memory
+    // fused step: q packed once for the split stage, and the row's selection made once by the
+    // last CTA of the row to finish (sel_pages == nullptr: none)
+    const float* q_f32;       // MXFP4 K/V: [B][Q][Hq][128] to pack (nullptr: nothing to pack)
+    uint16_t* qbf;            // [B][Q][Hq][128] bf16 of the packed q (exact)
+    int q_row_elems;          // Q * Hq * 128
+    int32_t* arrivals;        // [B] CTAs of the row that have finished; the last one resets it to 0
+    int32_t* sel_pages;       // [B][topk] selected logical page ids, ascending, -1 padded
+    int32_t* sel_phys;        // [B][topk] their physical ids (-1: none or out of range)
+    int32_t* sel_count;       // [B] k_eff
+    int32_t* topk_out;        // [B][topk] (the caller's output)
+    int32_t* count_out;       // [B]
+    int topk;
 };
 
 constexpr int kIdxWarps = 8;
@@ -280,6 +292,21 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 2) index_score_kernel(IndexArg
         sig_c[nt][1] = sig[nt * 8 + 2 * t + 1];
     }
 
+    // fused step: this CTA's slice of q[b] packed to e4m3 and stored as (exact) bf16
+    if (a.q_f32 != nullptr) {
+        const int n4 = a.q_row_elems / 4;
+        const int per = (n4 + gridDim.x - 1) / gridDim.x;
+        const int i_end = min(n4, (int)(blockIdx.x + 1) * per);
+        const float4* src = reinterpret_cast<const float4*>(a.q_f32 + (int64_t)b * a.q_row_elems);
+        uint2* dst = reinterpret_cast<uint2*>(a.qbf + (int64_t)b * a.q_row_elems);
+        for (int i = blockIdx.x * per + threadIdx.x; i < i_end; i += blockDim.x) {
+            const uint32_t w = pack_q4(src[i]);
+            const float2 lo = f16x2_to_f32x2(e4m3x2_to_f16x2(w & 0xFFFF));
+            const float2 hi = f16x2_to_f32x2(e4m3x2_to_f16x2(w >> 16));
+            dst[i] = make_uint2(f32x2_to_bf16x2(lo.x, lo.y), f32x2_to_bf16x2(hi.x, hi.y));
+        }
+    }
+
     const int lim = ctx - a.Q;  // token j counts for query n iff j <= lim + n
     float best = -INFINITY;
 #pragma unroll 1
@@ -308,6 +335,44 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 2) index_score_kernel(IndexArg
                     const float* r = red[it & 1] + 4 * threadIdx.x;
                     a.scores[(int64_t)b * a.max_pages + pp] = fmaxf(fmaxf(r[0], r[1]), fmaxf(r[2], r[3]));
                 }
+            }
+        }
+    }
+    if (a.sel_pages != nullptr) {
+        __shared__ int is_last;
+        __threadfence();   // this thread's page scores are visible device-wide
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            is_last = atomicAdd(&a.arrivals[b], 1) == (int)gridDim.x - 1;
+        }
+        __syncthreads();
+        if (is_last) {
+            // every CTA of the row fenced its scores before arriving: read them through L2
+            __threadfence();
+            extern __shared__ __align__(16) uint32_t dyn[];
+            uint32_t* keys = dyn;
+            int* sel = reinterpret_cast<int*>(dyn + a.max_pages);
+            __shared__ SelectSmem selsm;
+            const float* srow = a.scores + (int64_t)b * a.max_pages;
+            for (int i = threadIdx.x; i < n_pages; i += blockDim.x) keys[i] = score_key(ldg_cg_f32(srow + i));
+            __syncthreads();
+            const int k_eff = block_select(keys, n_pages, a.topk, sel, selsm);
+            for (int i = threadIdx.x; i < a.topk; i += blockDim.x) {
+                const int pg = i < k_eff ? sel[i] : -1;
+                int32_t ph = -1;
+                if (pg >= 0) {
+                    const int64_t v = a.page_table[(int64_t)b * a.max_pages + pg];
+                    if (v >= 0 && v < a.n_pool) ph = (int32_t)v;
+                    else flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                }
+                a.sel_pages[(int64_t)b * a.topk + i] = pg;
+                a.sel_phys[(int64_t)b * a.topk + i] = ph;
+                a.topk_out[(int64_t)b * a.topk + i] = pg;
+            }
+            if (threadIdx.x == 0) {
+                a.sel_count[b] = k_eff;
+                a.count_out[b] = k_eff;
+                a.arrivals[b] = 0;
             }
         }
     }
@@ -348,8 +413,14 @@ static int index_pages_per_cta(const smx_shape_t& s) {
 cudaError_t launch_index(const smx_shape_t& s, const uint16_t* qidx, uint8_t* idx_pool,
                          const int32_t* page_table, const int32_t* ctx_len, float* scores, int32_t* status,
                          const float* k_new, const float* v_new, const float* kidx_new, uint8_t* k_pool,
-                         uint8_t* v_pool, bool pdl, cudaStream_t st) {
-    IndexArgs a;
+                         uint8_t* v_pool, bool pdl, cudaStream_t st, const FusedSelect* fs) {
+    IndexArgs a = {};
+    if (fs) {
+        a.q_f32 = fs->q_f32; a.qbf = fs->qbf; a.q_row_elems = s.Q * s.Hq * 128; a.arrivals = fs->arrivals;
+        a.sel_pages = fs->sel_pages; a.sel_phys = fs->sel_phys; a.sel_count = fs->sel_count;
+        a.topk_out = fs->topk_out; a.count_out = fs->count_out;
+    }
+    a.topk = s.topk;
     a.qidx = qidx; a.pool = idx_pool; a.page_table = page_table; a.ctx_len = ctx_len; a.scores = scores;
     a.status = status; a.n_pool = s.n_pool_pages; a.Q = s.Q; a.max_pages = s.max_pages_per_row;
     a.pages_per_cta = index_pages_per_cta(s);
@@ -359,8 +430,14 @@ cudaError_t launch_index(const smx_shape_t& s, const uint16_t* qidx, uint8_t* id
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kIdxWarps * 32);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = fs ? 4 * ((size_t)s.max_pages_per_row + s.topk) : 0;
     cfg.stream = st;
+    if (fs) {
+        const void* kfn = s.Q <= 8 ? reinterpret_cast<const void*>(index_score_kernel<1>)
+                                   : reinterpret_cast<const void*>(index_score_kernel<2>);
+        cudaError_t e = ensure_smem_attr(kfn, (int)cfg.dynamicSmemBytes);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -374,7 +451,7 @@ cudaError_t launch_index_scores(const smx_shape_t& s, const uint16_t* qidx, cons
                                 const int32_t* page_table, const int32_t* ctx_len, float* scores,
                                 int32_t* status, cudaStream_t st) {
     return launch_index(s, qidx, const_cast<uint8_t*>(idx_pool), page_table, ctx_len, scores, status, nullptr,
-                        nullptr, nullptr, nullptr, nullptr, false, st);
+                        nullptr, nullptr, nullptr, nullptr, false, st, nullptr);
 }
 
 cudaError_t launch_topk(const smx_shape_t& s, const float* scores, const int32_t* ctx_len,

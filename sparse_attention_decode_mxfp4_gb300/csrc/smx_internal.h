@@ -34,18 +34,30 @@ cudaError_t launch_attn_split(const smx_shape_t& s, const void* q, const uint8_t
 cudaError_t launch_attn_merge(const smx_shape_t& s, const float* part_o, const float* part_m,
                               const float* part_l, float* out, bool pdl, cudaStream_t st);
 
-// The fused step's kernels: a1 + a3 in one launch (index scorer with the insert), a2 + a4 + a5 in
-// one launch (q packing, selection from the page scores, split stage); both may be launched as
-// programmatic dependents of the preceding kernel in the stream.
+// The fused step's kernels: a1 + a2 + a3 + a4 in one launch (the scorer with the insert, the q
+// packing and, in the last CTA of each row, the selection), then a5 (split stage from the staged
+// selection); each may be launched as a programmatic dependent of the preceding kernel.
+// Workspace pieces through which the fused scorer hands the split stage the packed q and the
+// row's selection.
+struct FusedSelect {
+    const float* q_f32;   // MXFP4 K/V: q to pack (nullptr for the e4m3 row-scale format)
+    uint16_t* qbf;
+    int32_t* arrivals;
+    int32_t* sel_pages;
+    int32_t* sel_phys;
+    int32_t* sel_count;
+    int32_t* topk_out;
+    int32_t* count_out;
+};
+
 cudaError_t launch_index(const smx_shape_t& s, const uint16_t* qidx, uint8_t* idx_pool,
                          const int32_t* page_table, const int32_t* ctx_len, float* scores, int32_t* status,
                          const float* k_new, const float* v_new, const float* kidx_new, uint8_t* k_pool,
-                         uint8_t* v_pool, bool pdl, cudaStream_t st);
+                         uint8_t* v_pool, bool pdl, cudaStream_t st, const FusedSelect* fs);
 
-cudaError_t launch_attn_select_split(const smx_shape_t& s, const float* q_f32, const void* q_bf16,
-                                     const uint8_t* k_pool, const uint8_t* v_pool, const int32_t* page_table,
-                                     const int32_t* ctx_len, const float* scores, int32_t* topk_pages,
-                                     int32_t* topk_count, float* part_o, float* part_m, float* part_l,
-                                     int32_t* status, cudaStream_t st);
+cudaError_t launch_attn_fused_split(const smx_shape_t& s, const uint16_t* qbf, const uint8_t* k_pool,
+                                    const uint8_t* v_pool, const int32_t* ctx_len, const int32_t* sel_pages,
+                                    const int32_t* sel_phys, const int32_t* sel_count, float* part_o,
+                                    float* part_m, float* part_l, int32_t* status, cudaStream_t st);
 
 }  // namespace smx

@@ -49,7 +49,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int& total, int* sm) {
 
 // keys[0..n) (score_key values, 16-byte aligned shared memory) -> out[0..k_eff) ascending page
 // ids. out may be shared or global memory. Returns k_eff. Every thread of the block must call it.
-static __device__ __noinline__ int block_select(const uint32_t* keys, int n, int k, int* out, SelectSmem& sm) {
+static __device__ __forceinline__ int block_select(const uint32_t* keys, int n, int k, int* out, SelectSmem& sm) {
     const int k_eff = min(k, n);
     const int nthr = blockDim.x;
     if (k_eff <= 0) return 0;

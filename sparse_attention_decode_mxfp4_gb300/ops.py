@@ -221,7 +221,8 @@ def sparse_attn_merge(shape, part_o, part_m, part_l, out=None, stream=None):
 
 
 def alloc_workspace(shape, device=None) -> torch.Tensor:
-    return torch.empty(max(256, workspace_bytes(shape)), dtype=torch.uint8, device=device or "cuda")
+    """Zeroed workspace for decode_step (its per-row counters must start at zero)."""
+    return torch.zeros(max(256, workspace_bytes(shape)), dtype=torch.uint8, device=device or "cuda")
 
 
 def decode_step(shape, *, q_f32=None, q_bf16=None, qidx_bf16, k_new, v_new, kidx_new, page_table,
