@@ -471,7 +471,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const floa
             acc.x *= al; acc.y *= al; acc.z *= al; acc.w *= al;
             L *= al;
             const float w = (m == -INFINITY) ? 0.0f : exp2f(m - Mn);
-            float lw = (lane < 16) ? w * lv : 0.0f;
+            // both 16-lane halves hold the same partitions: each half sums its own copy
+            float lw = w * lv;
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) lw += __shfl_xor_sync(0xFFFFFFFFu, lw, o);
             L += lw;
