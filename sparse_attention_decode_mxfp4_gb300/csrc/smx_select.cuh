@@ -15,7 +15,7 @@ namespace smx {
 struct SelectSmem {
     uint32_t hist[256];
     int scan[136];
-    uint32_t digit, above;
+    uint32_t digit, above, in_bin;
 };
 
 // Block-wide exclusive scan of one counter; returns the block total. All threads call.
@@ -47,8 +47,11 @@ __device__ __forceinline__ int block_excl_scan(int v, int& total, int* sm) {
     return ex;
 }
 
-// keys[0..n) (score_key values, 16-byte aligned shared memory) -> out[0..k_eff) ascending page
-// ids. out may be shared or global memory. Returns k_eff. Every thread of the block must call it.
+// keys[0..n) (score_key values in shared memory) -> out[0..k_eff) ascending page ids. out may be
+// shared or global memory. Returns k_eff. Every thread of the block must call it.
+// An 8-bit radix select walks the key bits from the top: each pass histograms the keys that share
+// the bits decided so far, finds the bin holding the k_eff-th key, and stops early once that bin
+// is taken whole. Selected = keys above the decided prefix, plus the lowest-id keys equal to it.
 static __device__ __forceinline__ int block_select(const uint32_t* keys, int n, int k, int* out, SelectSmem& sm) {
     const int k_eff = min(k, n);
     const int nthr = blockDim.x;
@@ -58,40 +61,6 @@ static __device__ __forceinline__ int block_select(const uint32_t* keys, int n, 
         __syncthreads();
         return k_eff;
     }
-    const bool ranks = n <= 2 * nthr;
-    if (ranks) {
-        // rank of every page against all others (ties to the lower id); selected iff rank < k_eff
-        const int i0 = threadIdx.x, i1 = threadIdx.x + nthr;
-        const uint32_t k0 = i0 < n ? keys[i0] : 0u, k1 = i1 < n ? keys[i1] : 0u;
-        int r0 = 0, r1 = 0;
-        const int n4 = n & ~3;
-        const uint4* k4 = reinterpret_cast<const uint4*>(keys);
-#pragma unroll 4
-        for (int j = 0; j < n4; j += 4) {
-            const uint4 v = k4[j >> 2];
-            const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                r0 += (kv[u] > k0) || (kv[u] == k0 && j + u < i0);
-                r1 += (kv[u] > k1) || (kv[u] == k1 && j + u < i1);
-            }
-        }
-        for (int j = n4; j < n; ++j) {
-            const uint32_t kv = keys[j];
-            r0 += (kv > k0) || (kv == k0 && j < i0);
-            r1 += (kv > k1) || (kv == k1 && j < i1);
-        }
-        const int s0 = i0 < n && r0 < k_eff, s1 = i1 < n && r1 < k_eff;
-        // ids in order: i0 < nthr <= i1, so the second key's position counts all first keys
-        int tot0, tot1;
-        const int e0 = block_excl_scan(s0, tot0, sm.scan);
-        const int e1 = block_excl_scan(s1, tot1, sm.scan);
-        if (s0) out[e0] = i0;
-        if (s1) out[tot0 + e1] = i1;
-        __syncthreads();
-        return k_eff;
-    }
-    // 4-pass 8-bit radix select of the k_eff-th key T; k_rem = how many keys equal to T to take
     uint32_t prefix = 0, mask = 0;
     int k_rem = k_eff;
 #pragma unroll 1
@@ -123,6 +92,7 @@ static __device__ __forceinline__ int block_select(const uint32_t* keys, int n, 
                     if (run + c[i] >= (uint32_t)k_rem) {
                         sm.digit = 255 - 8 * lane - i;
                         sm.above = run;
+                        sm.in_bin = c[i];
                         break;
                     }
                     run += c[i];
@@ -133,9 +103,10 @@ static __device__ __forceinline__ int block_select(const uint32_t* keys, int n, 
         prefix |= sm.digit << shift;
         mask |= 0xFFu << shift;
         k_rem -= (int)sm.above;
+        const bool whole_bin = (int)sm.in_bin == k_rem;
         __syncthreads();
+        if (whole_bin) break;
     }
-    const uint32_t T = prefix;
     // compaction in page-id order: thread u owns up to 32 consecutive ids of a chunk
     int base_sel = 0, base_eq = 0;
     const int chunk = nthr * 32;
@@ -145,9 +116,9 @@ static __device__ __forceinline__ int block_select(const uint32_t* keys, int n, 
         const int i1 = min(i0 + per, n);
         uint32_t gt_bits = 0, eq_bits = 0;
         for (int i = i0; i < i1; ++i) {
-            const uint32_t key = keys[i];
-            gt_bits |= (uint32_t)(key > T) << (i - i0);
-            eq_bits |= (uint32_t)(key == T) << (i - i0);
+            const uint32_t key = keys[i] & mask;
+            gt_bits |= (uint32_t)(key > prefix) << (i - i0);
+            eq_bits |= (uint32_t)(key == prefix) << (i - i0);
         }
         int t_eq;
         const int e_eq = block_excl_scan(__popc(eq_bits), t_eq, sm.scan);
