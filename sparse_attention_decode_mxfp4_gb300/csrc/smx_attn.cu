@@ -149,6 +149,50 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
     const int pos0 = ctx - a.Q + t0, pos1 = ctx - a.Q + t1;
     if (FUSED && a.pdl) pdl_wait();
     pdl_trigger();
+    // this partition's pages; the first two page copies go out before anything else
+    const int k_eff = FUSED ? max(0, min(a.sel_count[b], min(a.topk, n_pages)))
+                            : max(0, min(a.topk_count[b], min(a.topk, n_pages)));
+    const int lo = (int)(((int64_t)s * k_eff) / a.S), hi = (int)(((int64_t)(s + 1) * k_eff) / a.S);
+    const int page_bytes = a.page_bytes;
+    auto resolve = [&](int i, int& p, int& ph) {   // entry i of the row's selection
+        const int64_t at = (int64_t)b * a.topk + i;
+        p = FUSED ? a.sel_pages[at] : a.topk_pages[at];
+        ph = -1;
+        if (p < 0 || p >= n_pages) {
+            flag_status(a.status, SMX_DEV_BAD_TOPK);
+        } else if (FUSED) {
+            ph = a.sel_phys[at];
+        } else {
+            const int64_t v = a.page_table[(int64_t)b * a.max_pages + p];
+            if (v >= 0 && v < a.n_pool) ph = (int)v;
+            else flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+        }
+    };
+    auto issue = [&](int st, int p, int64_t phys) {  // thread 0 only
+        if (phys < 0) {
+            stage_page[st] = -1;
+            mbar_arrive(&mbar[st]);
+            return;
+        }
+        stage_page[st] = p;
+        const int64_t off = (phys * a.Hkv + kvh) * (int64_t)page_bytes;
+        mbar_arrive_expect_tx(&mbar[st], 2u * page_bytes);
+        bulk_g2s(raw + st * 2 * page_bytes, a.k_pool + off, page_bytes, &mbar[st]);
+        bulk_g2s(raw + st * 2 * page_bytes + page_bytes, a.v_pool + off, page_bytes, &mbar[st]);
+    };
+    if (threadIdx.x == 0) {
+        mbar_init(&mbar[0], 1);
+        mbar_init(&mbar[1], 1);
+        mbar_fence_init();
+        for (int st = 0; st < 2 && lo + st < hi; ++st) {
+            int p, ph;
+            resolve(lo + st, p, ph);
+            issue(st, p, ph);
+        }
+    }
+    // entries of the later pages, for their copies
+    for (int i = threadIdx.x + 2; i < hi - lo; i += blockDim.x) resolve(lo + i, sel[i], selph[i]);
+
     // q A fragments (bf16, exact) for 8 k-steps: a0/a2 row m0, a1/a3 row m1; lane (g, t) holds
     // dims 16 ks + 8 h + 2t, +1. All loads in flight together.
     uint32_t qa[8][4];
@@ -184,57 +228,12 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
             if (!v1) qa[k][1] = qa[k][3] = 0;
         }
     }
-    // this partition's pages and their physical ids
-    const int k_eff = FUSED ? max(0, min(a.sel_count[b], min(a.topk, n_pages)))
-                            : max(0, min(a.topk_count[b], min(a.topk, n_pages)));
-    const int lo = (int)(((int64_t)s * k_eff) / a.S), hi = (int)(((int64_t)(s + 1) * k_eff) / a.S);
-    for (int i = threadIdx.x; i < hi - lo; i += blockDim.x) {
-        const int64_t at = (int64_t)b * a.topk + lo + i;
-        const int p = FUSED ? a.sel_pages[at] : a.topk_pages[at];
-        int ph = -1;
-        if (p < 0 || p >= n_pages) {
-            flag_status(a.status, SMX_DEV_BAD_TOPK);
-        } else if (FUSED) {
-            ph = a.sel_phys[at];
-        } else {
-            const int64_t v = a.page_table[(int64_t)b * a.max_pages + p];
-            if (v >= 0 && v < a.n_pool) ph = (int)v;
-            else flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
-        }
-        sel[i] = p;
-        selph[i] = ph;
-    }
     __syncthreads();
 
     float o[16][4];
 #pragma unroll
     for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
     float mrow0 = -INFINITY, mrow1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-    const int page_bytes = a.page_bytes;
-
-    // ---- selected K/V pages staged by 1-D bulk copies, two pages in flight ----
-    if (threadIdx.x == 0) {
-        mbar_init(&mbar[0], 1);
-        mbar_init(&mbar[1], 1);
-        mbar_fence_init();
-    }
-    __syncthreads();
-    auto issue = [&](int st, int i) {  // thread 0 only
-        const int p = sel[i - lo];
-        const int64_t phys = selph[i - lo];
-        if (phys < 0) {
-            stage_page[st] = -1;
-            mbar_arrive(&mbar[st]);
-            return;
-        }
-        stage_page[st] = p;
-        const int64_t off = (phys * a.Hkv + kvh) * (int64_t)page_bytes;
-        mbar_arrive_expect_tx(&mbar[st], 2u * page_bytes);
-        bulk_g2s(raw + st * 2 * page_bytes, a.k_pool + off, page_bytes, &mbar[st]);
-        bulk_g2s(raw + st * 2 * page_bytes + page_bytes, a.v_pool + off, page_bytes, &mbar[st]);
-    };
-    if (threadIdx.x == 0)
-        for (int st = 0; st < 2 && lo + st < hi; ++st) issue(st, lo + st);
 
     bool timed_out = false;
     int to_stage = 0;
@@ -260,7 +259,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
         __syncthreads();   // tiles ready; this stage's raw bytes are consumed
         if (threadIdx.x == 0 && i + 2 < hi) {
             fence_proxy_async_smem();
-            issue(st, i + 2);
+            issue(st, sel[i + 2 - lo], selph[i + 2 - lo]);
         }
         // this warp's half of the page in 16-token units: QK, online softmax, one PV k-step
         const int units = (p >= 0 && warp_active) ? max(0, min(4, (valid_rows - th * 64 + 15) / 16)) : 0;

@@ -175,63 +175,52 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 2) index_score_kernel(IndexArg
     for (int p = max(p_begin, n_pages) + threadIdx.x; p < p_end_all; p += blockDim.x)
         a.scores[(int64_t)b * a.max_pages + p] = -INFINITY;
 
-    // ---- fused insert of the new tokens whose page lies in this CTA's range ----
+    // ---- fused insert. The index-K rows of the new tokens are written by the CTA that scores
+    // their page (before it reads the page); the K and V rows, read only by the split stage, are
+    // spread over all CTAs of the row.
     const int first_new = ctx - a.Q;
     const bool wrote = a.k_new != nullptr && p_begin < p_end && first_new / kPage < p_end &&
                        (ctx - 1) / kPage >= p_begin;
-    if (wrote) {
-        const int kinds = 1 + 2 * a.Hkv;
-        const int rows = a.Q * kinds;
-        constexpr int kBatch = 8;
-        for (int r0 = warp; r0 < rows; r0 += kIdxWarps * kBatch) {
-            float4 x[kBatch];
-            int64_t dst_phys[kBatch];
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {   // every load of the batch in flight at once
-                const int r = r0 + u * kIdxWarps;
-                dst_phys[u] = -1;
-                x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (r >= rows) continue;
-                const int tq = r / kinds, kind = r % kinds;
-                const int pos = first_new + tq;
-                const int pg = pos / kPage;
+    if (a.k_new != nullptr) {
+        const int kv_rows = a.Q * 2 * a.Hkv;
+        // index-K rows of this CTA's pages: one warp per row
+        if (wrote && warp < a.Q) {
+            for (int tq = warp; tq < a.Q; tq += kIdxWarps) {
+                const int pos = first_new + tq, pg = pos / kPage;
                 if (pos < 0 || pg < p_begin || pg >= p_end) continue;
                 const int64_t phys = a.page_table[(int64_t)b * a.max_pages + pg];
                 if (phys < 0 || phys >= a.n_pool) {
-                    if (lane == 0 && kind == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                    if (lane == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
                     continue;
                 }
-                const int64_t tok = (int64_t)b * a.Q + tq;
-                const float* src = kind == 0 ? a.kidx_new + tok * kD
-                                             : (kind <= a.Hkv ? a.k_new : a.v_new) + (tok * a.Hkv + (kind - 1) % a.Hkv) * kD;
-                x[u] = reinterpret_cast<const float4*>(src)[lane];
-                dst_phys[u] = phys;
-            }
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                if (dst_phys[u] < 0) continue;
-                const int r = r0 + u * kIdxWarps;
-                const int tq = r / kinds, kind = r % kinds;
-                const int slot = (first_new + tq) % kPage;
-                const int64_t phys = dst_phys[u];
-                if (kind == 0) {
-                    uint8_t* page = a.pool + phys * kMxPageBytes;
-                    quant_row_mxfp4_warp(x[u], page + slot * 64, page + kMxScaleOff + slot * 4, lane);
-                } else {
-                    const int h = (kind - 1) % a.Hkv;
-                    uint8_t* pool = kind <= a.Hkv ? a.k_pool : a.v_pool;
-                    if (a.kv_format == SMX_KV_E4M3_ROWSCALE) {
-                        uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kRsPageBytes;
-                        quant_row_e4m3rs_warp(x[u], page + slot * 128,
-                                              reinterpret_cast<float*>(page + kRsScaleOff) + slot, lane);
-                    } else {
-                        uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kMxPageBytes;
-                        quant_row_mxfp4_warp(x[u], page + slot * 64, page + kMxScaleOff + slot * 4, lane);
-                    }
-                }
+                const float4 x = reinterpret_cast<const float4*>(a.kidx_new + ((int64_t)b * a.Q + tq) * kD)[lane];
+                uint8_t* page = a.pool + phys * kMxPageBytes;
+                quant_row_mxfp4_warp(x, page + (pos % kPage) * 64, page + kMxScaleOff + (pos % kPage) * 4, lane);
             }
         }
-        __threadfence();
+                // K/V rows: row r of the row's Q x 2 x Hkv goes to CTA r % gridDim.x, warp (r / gridDim.x) % 8
+        for (int r = blockIdx.x + gridDim.x * warp; r < kv_rows; r += gridDim.x * kIdxWarps) {
+            const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);   // kind < Hkv: K head, else V head
+            const int pos = first_new + tq;
+            if (pos < 0) continue;
+            const int64_t phys = a.page_table[(int64_t)b * a.max_pages + pos / kPage];
+            if (phys < 0 || phys >= a.n_pool) {
+                if (lane == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                continue;
+            }
+            const int h = kind % a.Hkv, slot = pos % kPage;
+            const int64_t tok = (int64_t)b * a.Q + tq;
+            const float4 x = reinterpret_cast<const float4*>((kind < a.Hkv ? a.k_new : a.v_new) + (tok * a.Hkv + h) * kD)[lane];
+            uint8_t* pool = kind < a.Hkv ? a.k_pool : a.v_pool;
+            if (a.kv_format == SMX_KV_E4M3_ROWSCALE) {
+                uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kRsPageBytes;
+                quant_row_e4m3rs_warp(x, page + slot * 128, reinterpret_cast<float*>(page + kRsScaleOff) + slot, lane);
+            } else {
+                uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kMxPageBytes;
+                quant_row_mxfp4_warp(x, page + slot * 64, page + kMxScaleOff + slot * 4, lane);
+            }
+        }
+        if (wrote) __threadfence();
     }
     __syncthreads();   // page-table entries staged; inserted rows written and fenced
 
@@ -401,9 +390,21 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     if (threadIdx.x == 0) topk_count[b] = k_eff;
 }
 
+static int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cached[dev] == 0) {
+        int n = 0;
+        cached[dev] = (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) ? n : 148;
+    }
+    return cached[dev];
+}
+
 static int index_pages_per_cta(const smx_shape_t& s) {
-    // about four CTAs of 8 warps per SM over all rows, an even number of pages each
-    const int64_t target = 152 * 4;
+    // one wave: two CTAs of 8 warps per SM (their registers allow two) over all rows, an even
+    // number of pages each
+    const int64_t target = 2 * (int64_t)sm_count();
     int64_t ppc = ((int64_t)s.max_pages_per_row * s.B + target - 1) / target;
     ppc = (ppc + 1) & ~1LL;
     if (ppc > kIdxMaxPpc) ppc = kIdxMaxPpc;

@@ -68,9 +68,14 @@ static __device__ __forceinline__ int block_select(const uint32_t* keys, int n, 
         const int shift = 24 - 8 * pass;
         for (int i = threadIdx.x; i < 256; i += nthr) sm.hist[i] = 0;
         __syncthreads();
-        for (int i = threadIdx.x; i < n; i += nthr) {
-            const uint32_t key = keys[i];
-            if ((key & mask) == prefix) atomicAdd(&sm.hist[(key >> shift) & 0xFF], 1u);
+        // warp-aggregated: lanes that fall in the same bin add once (scores crowd a few bins)
+        const int n_warp = (n + 31) & ~31;
+        for (int i = threadIdx.x; i < n_warp; i += nthr) {
+            const uint32_t key = i < n ? keys[i] : 0u;
+            const bool in = i < n && (key & mask) == prefix;
+            const uint32_t bin = in ? (key >> shift) & 0xFF : 0x100u;
+            const unsigned peers = __match_any_sync(0xFFFFFFFFu, bin);
+            if (in && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&sm.hist[bin], (uint32_t)__popc(peers));
         }
         __syncthreads();
         if (threadIdx.x < 32) {
