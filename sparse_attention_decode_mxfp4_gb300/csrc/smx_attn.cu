@@ -149,6 +149,38 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
     const int pos0 = ctx - a.Q + t0, pos1 = ctx - a.Q + t1;
     if (FUSED && a.pdl) pdl_wait();
     pdl_trigger();
+    // q A fragments (bf16, exact) for 8 k-steps: a0/a2 row m0, a1/a3 row m1; lane (g, t) holds
+    // dims 16 ks + 8 h + 2t, +1. All loads in flight together.
+    uint32_t qa[8][4];
+    {
+        // padding rows (past the KV group's rows) read row 0: their scores are masked and their
+        // outputs never written
+        const int mc0 = v0 ? m0 : 0, mc1 = v1 ? m1 : 0;
+        const int64_t base0 = (((int64_t)b * a.Q + mc0 / a.G) * a.Hq + kvh * a.G + mc0 % a.G) * kD + 2 * t;
+        const int64_t base1 = (((int64_t)b * a.Q + mc1 / a.G) * a.Hq + kvh * a.G + mc1 % a.G) * kD + 2 * t;
+        if (RS || FUSED) {
+            const uint16_t* qb = FUSED && !RS ? a.qbf : reinterpret_cast<const uint16_t*>(a.q);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                qa[k >> 1][(k & 1) * 2 + 0] = *reinterpret_cast<const uint32_t*>(qb + base0 + 8 * k);
+                qa[k >> 1][(k & 1) * 2 + 1] = *reinterpret_cast<const uint32_t*>(qb + base1 + 8 * k);
+            }
+        } else {
+            const uint8_t* q8 = reinterpret_cast<const uint8_t*>(a.q);
+            uint32_t w0[16], w1[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                w0[k] = *reinterpret_cast<const uint16_t*>(q8 + base0 + 8 * k);
+                w1[k] = *reinterpret_cast<const uint16_t*>(q8 + base1 + 8 * k);
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float2 g0 = f16x2_to_f32x2(e4m3x2_to_f16x2(w0[k])), g1 = f16x2_to_f32x2(e4m3x2_to_f16x2(w1[k]));
+                qa[k >> 1][(k & 1) * 2 + 0] = f32x2_to_bf16x2(g0.x, g0.y);
+                qa[k >> 1][(k & 1) * 2 + 1] = f32x2_to_bf16x2(g1.x, g1.y);
+            }
+        }
+    }
     // this partition's pages; the first two page copies go out before anything else
     const int k_eff = FUSED ? max(0, min(a.sel_count[b], min(a.topk, n_pages)))
                             : max(0, min(a.topk_count[b], min(a.topk, n_pages)));
@@ -193,41 +225,6 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
     // entries of the later pages, for their copies
     for (int i = threadIdx.x + 2; i < hi - lo; i += blockDim.x) resolve(lo + i, sel[i], selph[i]);
 
-    // q A fragments (bf16, exact) for 8 k-steps: a0/a2 row m0, a1/a3 row m1; lane (g, t) holds
-    // dims 16 ks + 8 h + 2t, +1. All loads in flight together.
-    uint32_t qa[8][4];
-    {
-        const int mc0 = v0 ? m0 : 0, mc1 = v1 ? m1 : 0;   // padding rows read row 0, then zero it
-        const int64_t base0 = (((int64_t)b * a.Q + mc0 / a.G) * a.Hq + kvh * a.G + mc0 % a.G) * kD + 2 * t;
-        const int64_t base1 = (((int64_t)b * a.Q + mc1 / a.G) * a.Hq + kvh * a.G + mc1 % a.G) * kD + 2 * t;
-        if (RS || FUSED) {
-            const uint16_t* qb = FUSED && !RS ? a.qbf : reinterpret_cast<const uint16_t*>(a.q);
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                qa[k >> 1][(k & 1) * 2 + 0] = *reinterpret_cast<const uint32_t*>(qb + base0 + 8 * k);
-                qa[k >> 1][(k & 1) * 2 + 1] = *reinterpret_cast<const uint32_t*>(qb + base1 + 8 * k);
-            }
-        } else {
-            const uint8_t* q8 = reinterpret_cast<const uint8_t*>(a.q);
-            uint32_t w0[16], w1[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                w0[k] = *reinterpret_cast<const uint16_t*>(q8 + base0 + 8 * k);
-                w1[k] = *reinterpret_cast<const uint16_t*>(q8 + base1 + 8 * k);
-            }
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float2 g0 = f16x2_to_f32x2(e4m3x2_to_f16x2(w0[k])), g1 = f16x2_to_f32x2(e4m3x2_to_f16x2(w1[k]));
-                qa[k >> 1][(k & 1) * 2 + 0] = f32x2_to_bf16x2(g0.x, g0.y);
-                qa[k >> 1][(k & 1) * 2 + 1] = f32x2_to_bf16x2(g1.x, g1.y);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            if (!v0) qa[k][0] = qa[k][2] = 0;
-            if (!v1) qa[k][1] = qa[k][3] = 0;
-        }
-    }
     __syncthreads();
 
     float o[16][4];

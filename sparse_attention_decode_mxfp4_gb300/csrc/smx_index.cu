@@ -327,6 +327,9 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 2) index_score_kernel(IndexArg
             }
         }
     }
+    // the split stage's CTAs may launch now onto the SMs this grid leaves idle; they still wait
+    // for this whole grid (the selection included) before reading anything it writes
+    pdl_trigger();
     if (a.sel_pages != nullptr) {
         __shared__ int is_last;
         __threadfence();   // this thread's page scores are visible device-wide
@@ -365,7 +368,6 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 2) index_score_kernel(IndexArg
             }
         }
     }
-    pdl_trigger();
 }
 
 // ---- standalone a4: one block per row ------------------------------------------------------------

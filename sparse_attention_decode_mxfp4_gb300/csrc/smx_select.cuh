@@ -12,7 +12,10 @@
 
 namespace smx {
 
+constexpr int kRankMax = 512;   // rows up to this many pages select by counting
+
 struct SelectSmem {
+    int rank[kRankMax];
     uint32_t hist[256];
     int scan[136];
     uint32_t digit, above, in_bin;
@@ -58,6 +61,38 @@ static __device__ __forceinline__ int block_select(const uint32_t* keys, int n, 
     if (k_eff <= 0) return 0;
     if (k_eff >= n) {
         for (int i = threadIdx.x; i < n; i += nthr) out[i] = i;
+        __syncthreads();
+        return k_eff;
+    }
+    if (n <= kRankMax) {
+        // small rows: rank of each page = pages with a larger (key, lower id) pair; the comparisons
+        // of a page are split in `parts` slices over the threads and added in shared memory
+        const int parts = max(1, nthr / n);
+        for (int q = threadIdx.x; q < n; q += nthr) sm.rank[q] = 0;
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < n * parts; idx += nthr) {
+            const int i = idx % n, part = idx / n;
+            const uint64_t ki = ((uint64_t)keys[i] << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)i);
+            const int j0 = part * n / parts, j1 = (part + 1) * n / parts;
+            int r = 0;
+#pragma unroll 8
+            for (int j = j0; j < j1; ++j) {
+                const uint64_t kj = ((uint64_t)keys[j] << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)j);
+                r += kj > ki;
+            }
+            if (parts > 1) atomicAdd(&sm.rank[i], r);
+            else sm.rank[i] = r;
+        }
+        __syncthreads();
+        // compaction in id order: thread u owns ids [u * per, (u + 1) * per)
+        const int per = (n + nthr - 1) / nthr;
+        const int i0 = threadIdx.x * per, i1 = min(i0 + per, n);
+        int cnt = 0;
+        for (int q = i0; q < i1; ++q) cnt += sm.rank[q] < k_eff;
+        int total;
+        int pos = block_excl_scan(cnt, total, sm.scan);
+        for (int q = i0; q < i1; ++q)
+            if (sm.rank[q] < k_eff) out[pos++] = q;
         __syncthreads();
         return k_eff;
     }
