@@ -62,12 +62,9 @@ def algorithmic_bytes(w, ctx_len):
 
 
 def default_splits(w):
-    """Partitions of the split stage: enough CTAs for about two per SM (a CTA covers up to 64 query
-    rows of one KV head), at most one selected page per partition."""
-    M = (w.Hq // w.Hkv) * w.Q
-    rows_per_cta = 16 * min(4, (M + 15) // 16)
-    ctas_per_split = w.B * w.Hkv * ((M + rows_per_cta - 1) // rows_per_cta)
-    return max(1, min(w.topk, 296 // ctas_per_split))
+    """Partitions of the split stage, as the library suggests for this device: one wave of split
+    CTAs, the same number of selected pages in every partition."""
+    return ops.suggest_num_splits(ops.Shape.of(w, 1))
 
 
 def peaks():

@@ -174,6 +174,14 @@ const char* smx_status_string(int status);
 /* Number of kernel launches smx_decode_step enqueues for this shape. */
 int smx_decode_step_launches(const smx_shape_t* shape);
 
+/* A partition count S for this shape on the CURRENT device (the pages leave S to the
+ * implementation: any S >= 1 gives the same attention up to rounding). It is the largest S
+ * whose split CTAs (B x Hkv x row groups per partition) fill at most one wave of the device's
+ * SMs at the split kernel's occupancy, lowered so every partition holds the same number of
+ * selected pages. shape->num_splits is ignored. Returns S >= 1, or 0 when the other fields of
+ * the shape are invalid or a CUDA query fails. Reads device attributes; launches nothing. */
+int smx_suggest_num_splits(const smx_shape_t* shape);
+
 #ifdef __cplusplus
 }
 #endif

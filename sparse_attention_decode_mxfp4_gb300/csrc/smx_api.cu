@@ -10,7 +10,7 @@
 namespace smx {
 
 cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
-    constexpr int kMaxDev = 64, kMaxKernels = 8;
+    constexpr int kMaxDev = 64, kMaxKernels = 16;
     static std::mutex mu;
     static const void* seen_kernel[kMaxKernels] = {};
     static int seen_bytes[kMaxKernels][kMaxDev] = {};
@@ -238,6 +238,14 @@ int smx_decode_step(const smx_shape_t* s, const float* q_f32, const uint16_t* q_
 int smx_decode_step_launches(const smx_shape_t* s) {
     if (check_shape(s) != SMX_OK) return 0;
     return 3;
+}
+
+int smx_suggest_num_splits(const smx_shape_t* s) {
+    if (s == nullptr) return 0;
+    smx_shape_t t = *s;
+    t.num_splits = 1;
+    if (check_shape(&t) != SMX_OK) return 0;
+    return smx::suggest_num_splits(t);
 }
 
 const char* smx_status_string(int status) {

@@ -18,7 +18,6 @@
 
 #include "smx_device.cuh"
 #include "smx_internal.h"
-#include "smx_select.cuh"
 
 namespace smx {
 
@@ -59,7 +58,7 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) { return row * 256 +
 // the softmax weights. Token rows at or past valid_rows are zero.
 template <bool RS>
 __device__ __forceinline__ void widen_page(const uint8_t* raw, int valid_rows, uint8_t* tile, float* rscale) {
-    if (RS) {
+    if constexpr (RS) {
         // 128 rows x 8 chunks of 16 codes
         for (int it = threadIdx.x; it < 128 * 8; it += blockDim.x) {
             const int r = it >> 3, c = it & 7;
@@ -117,7 +116,6 @@ __device__ __forceinline__ void widen_page(const uint8_t* raw, int valid_rows, u
 template <bool RS, bool FUSED>
 __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ SelectSmem selsm;
     __shared__ __align__(8) uint64_t mbar[2];
     __shared__ int stage_page[2];
     uint8_t* Ks = smem;                  // 32 KB
@@ -484,6 +482,28 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const floa
         acc.x /= L; acc.y /= L; acc.z /= L; acc.w /= L;
     }
     reinterpret_cast<float4*>(out + (int64_t)row * kD)[lane] = acc;
+}
+
+int suggest_num_splits(const smx_shape_t& s) {
+    const int M = (s.Hq / s.Hkv) * s.Q;
+    const int row_warps = min(kAttnMaxWarps / 2, (M + 15) / 16);
+    const int rows_per_cta = row_warps * 16;
+    const int ctas_per_split = s.B * s.Hkv * ((M + rows_per_cta - 1) / rows_per_cta);
+    const int page_bytes = s.kv_format == SMX_KV_E4M3_ROWSCALE ? kRsPageBytes : kMxPageBytes;
+    const size_t smem = (size_t)65536 + 1024 + 4 * (size_t)page_bytes + 8 * (size_t)s.topk;
+    const void* kfn = s.kv_format == SMX_KV_E4M3_ROWSCALE ? reinterpret_cast<const void*>(attn_split_kernel<true, true>)
+                                                          : reinterpret_cast<const void*>(attn_split_kernel<false, true>);
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        ensure_smem_attr(kfn, (int)smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, 2 * row_warps * 32, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    // one wave of split CTAs, then equal page counts per partition
+    const int s_max = max(1, (sms * max(1, per_sm)) / max(1, ctas_per_split));
+    const int pages_per_split = (s.topk + s_max - 1) / s_max;
+    return max(1, (s.topk + pages_per_split - 1) / pages_per_split);
 }
 
 static cudaError_t launch_split_impl(const smx_shape_t& s, AttnArgs& a, bool fused, cudaStream_t st) {

@@ -55,6 +55,8 @@ cudaError_t launch_index(const smx_shape_t& s, const uint16_t* qidx, uint8_t* id
                          const float* k_new, const float* v_new, const float* kidx_new, uint8_t* k_pool,
                          uint8_t* v_pool, bool pdl, cudaStream_t st, const FusedSelect* fs);
 
+// Partition count that fills one wave of the device's SMs with split CTAs (0 on a CUDA error).
+int suggest_num_splits(const smx_shape_t& s);
 cudaError_t launch_attn_fused_split(const smx_shape_t& s, const uint16_t* qbf, const uint8_t* k_pool,
                                     const uint8_t* v_pool, const int32_t* ctx_len, const int32_t* sel_pages,
                                     const int32_t* sel_phys, const int32_t* sel_count, float* part_o,

@@ -26,7 +26,8 @@ DEV_BAD_PAGE_ID, DEV_BAD_CTX, DEV_BAD_TOPK = 1, 2, 4
 # every symbol include/smx.h declares
 SYMBOLS = ("smx_workspace_bytes", "smx_kv_insert", "smx_kv_prefill", "smx_pack_q_e4m3",
            "smx_index_score", "smx_index_score_topk", "smx_sparse_attn_split", "smx_sparse_attn_merge",
-           "smx_decode_step", "smx_status_string", "smx_decode_step_launches")
+           "smx_decode_step", "smx_status_string", "smx_decode_step_launches",
+           "smx_suggest_num_splits")
 
 
 class SmxError(RuntimeError):
@@ -95,6 +96,7 @@ def lib() -> ctypes.CDLL:
             "smx_decode_step": (ctypes.c_int, [S] + [P] * 15 + [ctypes.c_size_t, P, ST]),
             "smx_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "smx_decode_step_launches": (ctypes.c_int, [S]),
+            "smx_suggest_num_splits": (ctypes.c_int, [S]),
         }
         for name, (res, args) in sigs.items():
             f = getattr(L, name)
@@ -139,6 +141,15 @@ def workspace_bytes(shape: Shape) -> int:
 def decode_step_launches(shape: Shape) -> int:
     cs = shape.c()
     return int(lib().smx_decode_step_launches(ctypes.byref(cs)))
+
+
+def suggest_num_splits(shape: Shape) -> int:
+    """Partition count for `shape` on the current device (one wave of split CTAs, equal pages)."""
+    cs = shape.c()
+    n = int(lib().smx_suggest_num_splits(ctypes.byref(cs)))
+    if n < 1:
+        raise SmxError("smx_suggest_num_splits: invalid shape or CUDA query failed")
+    return n
 
 
 def kv_insert(shape, k_new, v_new, kidx_new, page_table, ctx_len, k_pool, v_pool, idx_pool,

@@ -83,3 +83,10 @@ def test_status_strings(L):
     for rc in (0, -1, -2, -3, -4, -99):
         assert L.smx_status_string(rc)
     assert L.smx_decode_step_launches(ctypes.byref(good_shape().c())) >= 1
+
+
+def test_split_suggestion_refuses_bad_shapes(L):
+    bad = good_shape()
+    bad.Hq = 3   # not a multiple of Hkv
+    assert L.smx_suggest_num_splits(ctypes.byref(bad.c())) == 0
+    assert L.smx_suggest_num_splits(None) == 0

@@ -152,3 +152,17 @@ def test_bad_page_ids_are_flagged_and_skipped():
     got = C.gpu_step(w, bad, pools)
     assert got["status"] & ops.DEV_BAD_PAGE_ID
     assert np.all(np.isfinite(got["out"]))
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4])
+def test_split_suggestion_fills_at_most_one_wave(cfg):
+    w = wl.config(cfg)
+    S = ops.suggest_num_splits(ops.Shape.of(w, 1))
+    assert 1 <= S <= w.topk
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M = (w.Hq // w.Hkv) * w.Q
+    rows = 16 * min(4, (M + 15) // 16)
+    ctas = S * w.B * w.Hkv * ((M + rows - 1) // rows)
+    assert S == 1 or ctas <= 2 * sms
+    pages = -(-w.topk // S)
+    assert S == -(-w.topk // pages)   # no partition count with the same longest partition is smaller
