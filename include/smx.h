@@ -182,6 +182,35 @@ int smx_decode_step_launches(const smx_shape_t* shape);
  * the shape are invalid or a CUDA query fails. Reads device attributes; launches nothing. */
 int smx_suggest_num_splits(const smx_shape_t* shape);
 
+/* Bytes of the static device scratch smx_decode_step_noalloc works in (16 MiB). */
+#define SMX_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* smx_decode_step without a caller-provided workspace and without any device allocation. The
+ * pages have no counterpart: it is an interface variant of the whole step above, with the same
+ * arguments, results, launches and errors, minus workspace/ws_bytes.
+ *
+ * Its scratch is one module-scope device array of SMX_NOALLOC_SCRATCH_BYTES per device, placed
+ * by the driver when the library's module is loaded. The call never calls cudaMalloc, cudaFree or
+ * any other allocating routine. It is meant for callers that cannot allocate: a serving process
+ * that reserves nearly all device memory for its KV pools at start-up (a later allocation could
+ * fail, or fragment the reservation); code in a decode loop that must not run cudaFree, which can
+ * synchronise the whole device; and plain C callers that have no device allocator of their own.
+ *
+ * The first call on each device (with that device current) looks up the array's address with
+ * cudaGetSymbolAddress, which may load the module on that device, and clears the per-row arrival
+ * counters at its head on `stream`. Make that first call before any stream capture. Later calls
+ * only launch kernels; the kernels leave the counters at zero.
+ *
+ * Returns SMX_ERR_WORKSPACE, before touching the device, when smx_workspace_bytes(shape) exceeds
+ * SMX_NOALLOC_SCRATCH_BYTES; SMX_ERR_CUDA if the address lookup fails. All calls on one device
+ * share the one array: calls that overlap on the GPU (other streams, other host threads) race
+ * on it and give undefined results. */
+int smx_decode_step_noalloc(const smx_shape_t* shape, const float* q_f32, const uint16_t* q_bf16,
+                            const uint16_t* qidx_bf16, const float* k_new, const float* v_new,
+                            const float* kidx_new, const int32_t* page_table, const int32_t* ctx_len,
+                            uint8_t* k_pool, uint8_t* v_pool, uint8_t* idx_pool, int32_t* topk_pages,
+                            int32_t* topk_count, float* out, int32_t* dev_status, smx_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -27,7 +27,7 @@ DEV_BAD_PAGE_ID, DEV_BAD_CTX, DEV_BAD_TOPK = 1, 2, 4
 SYMBOLS = ("smx_workspace_bytes", "smx_kv_insert", "smx_kv_prefill", "smx_pack_q_e4m3",
            "smx_index_score", "smx_index_score_topk", "smx_sparse_attn_split", "smx_sparse_attn_merge",
            "smx_decode_step", "smx_status_string", "smx_decode_step_launches",
-           "smx_suggest_num_splits")
+           "smx_suggest_num_splits", "smx_decode_step_noalloc")
 
 
 class SmxError(RuntimeError):
@@ -97,6 +97,7 @@ def lib() -> ctypes.CDLL:
             "smx_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "smx_decode_step_launches": (ctypes.c_int, [S]),
             "smx_suggest_num_splits": (ctypes.c_int, [S]),
+            "smx_decode_step_noalloc": (ctypes.c_int, [S] + [P] * 15 + [ST]),
         }
         for name, (res, args) in sigs.items():
             f = getattr(L, name)
@@ -254,4 +255,22 @@ def decode_step(shape, *, q_f32=None, q_bf16=None, qidx_bf16, k_new, v_new, kidx
                                  _p(v_pool), _p(idx_pool), _p(topk_pages), _p(topk_count), _p(out),
                                  _p(workspace), workspace.numel(), _p(dev_status), _st(stream)),
            "smx_decode_step")
+    return out, topk_pages, topk_count
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def decode_step_noalloc(shape, *, q_f32=None, q_bf16=None, qidx_bf16, k_new, v_new, kidx_new, page_table,
+                        ctx_len, k_pool, v_pool, idx_pool, topk_pages, topk_count, out, dev_status=None,
+                        stream=None):
+    """smx_decode_step_noalloc: the whole step in the library's static device scratch. Every
+    output buffer is the caller's; the call allocates nothing (first call per device: before any
+    stream capture). Calls that overlap on one device race on the shared scratch."""
+    cs = shape.c()
+    _check(lib().smx_decode_step_noalloc(ctypes.byref(cs), _p(q_f32), _p(q_bf16), _p(qidx_bf16), _p(k_new),
+                                         _p(v_new), _p(kidx_new), _p(page_table), _p(ctx_len), _p(k_pool),
+                                         _p(v_pool), _p(idx_pool), _p(topk_pages), _p(topk_count), _p(out),
+                                         _p(dev_status), _st(stream)),
+           "smx_decode_step_noalloc")
     return out, topk_pages, topk_count
