@@ -64,6 +64,7 @@ def algorithmic_bytes(w, ctx_len):
 def default_splits(w):
     """Partitions of the split stage, as the library suggests for this device: one wave of split
     CTAs, the same number of selected pages in every partition."""
+    from sparse_attention_decode_mxfp4_gb300 import ops
     return ops.suggest_num_splits(ops.Shape.of(w, 1))
 
 
@@ -206,7 +207,7 @@ def cpu_baseline(w, data, step_bytes):
                            v_pool=pools[1], idx_pool=pools[2])
         reps += 1
         dt = time.perf_counter() - t0
-        if dt > 10.0 or reps >= 20:
+        if dt > 10.0:
             break
     return {"value": step_bytes * reps / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
             "kind": "oracle", "sample": f"{reps} whole steps of the workload ({dt:.1f} s)",
