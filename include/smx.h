@@ -91,11 +91,10 @@ typedef struct {
     int32_t kv_format;          /* SMX_KV_*: K/V page format; the index pool is always MXFP4 */
 } smx_shape_t;
 
-/* Bytes of device workspace smx_decode_step needs for this shape (per-row arrival counters, page
- * scores, packed q, the selection, split partials, alignment padding). Zero the workspace once
- * before its first use: the arrival counters it holds must start at zero, and every call leaves
- * them at zero again. One workspace serves one shape; calls that share a workspace must not
- * overlap on the GPU. */
+/* Bytes of device workspace smx_decode_step needs for this shape (step counters, page scores,
+ * packed q, split partials, alignment padding). Zero the workspace once before its first use: the
+ * counters it holds must start at zero, and every call leaves them at zero again. One workspace
+ * serves one shape; calls that share a workspace must not overlap on the GPU. */
 size_t smx_workspace_bytes(const smx_shape_t* shape);
 
 /* a1 -- [ATOM-2812] "--index-cache-dtype mxfp4" (index-K row store: E8M0 group scale =
@@ -158,9 +157,11 @@ int smx_sparse_attn_merge(const smx_shape_t* shape, const float* part_o, const f
 /* The whole step (a1..a6) on `stream`. q_f32 is required for MXFP4 K/V, q_bf16 for E4M3
  * row-scale K/V (the other may be NULL). Pools are updated in place (the Q new rows).
  * topk_pages/topk_count are outputs; workspace holds ws_bytes >= smx_workspace_bytes(shape)
- * bytes of scratch (256-byte aligned, zeroed before its first use). Three kernels: the scorer
- * (insert, q packing, page scores, and the selection in the last CTA of each row to finish),
- * the split stage and the merge, each a programmatic dependent of the one before. */
+ * bytes of scratch (256-byte aligned, zeroed before its first use). One cooperative kernel of at
+ * most one CTA per SM: inserts, q packing and page scores; then per attention unit the row's
+ * selection, the split stage over one partition and the merge of a slice of rows, the phases
+ * ordered by counters in the workspace (bounded waits: SMX_DEV_TIMEOUT in dev_status if one gives
+ * up). Calls that share a workspace must not overlap on the GPU. */
 int smx_decode_step(const smx_shape_t* shape, const float* q_f32, const uint16_t* q_bf16,
                     const uint16_t* qidx_bf16, const float* k_new, const float* v_new,
                     const float* kidx_new, const int32_t* page_table, const int32_t* ctx_len,
@@ -197,9 +198,10 @@ int smx_suggest_num_splits(const smx_shape_t* shape);
  * synchronise the whole device; and plain C callers that have no device allocator of their own.
  *
  * The first call on each device (with that device current) looks up the array's address with
- * cudaGetSymbolAddress, which may load the module on that device, and clears the per-row arrival
- * counters at its head on `stream`. Make that first call before any stream capture. Later calls
- * only launch kernels; the kernels leave the counters at zero.
+ * cudaGetSymbolAddress, which may load the module on that device, and clears the step counters at
+ * its head on `stream`. Make that first call before any stream capture. Later calls launch the
+ * step; the step leaves its counters at zero, and a call whose shape needs more counter bytes than
+ * the previous call's also clears them first (one memset on `stream`).
  *
  * Returns SMX_ERR_WORKSPACE, before touching the device, when smx_workspace_bytes(shape) exceeds
  * SMX_NOALLOC_SCRATCH_BYTES; SMX_ERR_CUDA if the address lookup fails. All calls on one device

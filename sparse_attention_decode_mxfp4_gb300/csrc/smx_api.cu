@@ -34,6 +34,8 @@ cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
     return e;
 }
 
+size_t workspace_counter_bytes(const smx_shape_t& s) { return step_geom(s).n_counters * sizeof(uint32_t); }
+
 }  // namespace smx
 
 namespace {
@@ -63,12 +65,8 @@ int check_shape(const smx_shape_t* s) {
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? SMX_OK : SMX_ERR_CUDA; }
 
 struct Workspace {
+    uint32_t* counters;   // step counters (zero between calls)
     float* scores;        // [B][max_pages]
-    uint16_t* qbf;        // [B][Q][Hq][128] packed q as bf16 (MXFP4 K/V)
-    int32_t* arrivals;    // [B] per-row arrival counters of the scorer (zero between calls)
-    int32_t* sel_pages;   // [B][topk]
-    int32_t* sel_phys;    // [B][topk]
-    int32_t* sel_count;   // [B]
     float* part_o;
     float* part_m;
     float* part_l;
@@ -85,13 +83,9 @@ Workspace layout(const smx_shape_t* s, void* base) {
         return at;
     };
     const size_t rows = (size_t)s->B * s->num_splits * s->Q * s->Hq;
-    // the arrival counters come first so that a zeroed prefix is easy to keep
-    w.arrivals = reinterpret_cast<int32_t*>(take((size_t)s->B * sizeof(int32_t)));
+    // the counters come first so that a zeroed prefix is easy to keep
+    w.counters = reinterpret_cast<uint32_t*>(take(smx::step_geom(*s).n_counters * sizeof(uint32_t)));
     w.scores = reinterpret_cast<float*>(take((size_t)s->B * s->max_pages_per_row * sizeof(float)));
-    w.qbf = reinterpret_cast<uint16_t*>(take((size_t)s->B * s->Q * s->Hq * 128 * sizeof(uint16_t)));
-    w.sel_pages = reinterpret_cast<int32_t*>(take((size_t)s->B * s->topk * sizeof(int32_t)));
-    w.sel_phys = reinterpret_cast<int32_t*>(take((size_t)s->B * s->topk * sizeof(int32_t)));
-    w.sel_count = reinterpret_cast<int32_t*>(take((size_t)s->B * sizeof(int32_t)));
     w.part_o = reinterpret_cast<float*>(take(rows * 128 * sizeof(float)));
     w.part_m = reinterpret_cast<float*>(take(rows * sizeof(float)));
     w.part_l = reinterpret_cast<float*>(take(rows * sizeof(float)));
@@ -189,7 +183,7 @@ int smx_sparse_attn_merge(const smx_shape_t* s, const float* part_o, const float
     int rc = check_shape(s);
     if (rc) return rc;
     if (!part_o || !part_m || !part_l || !out) return SMX_ERR_INVALID_ARG;
-    return cuda_status(smx::launch_attn_merge(*s, part_o, part_m, part_l, out, false, (cudaStream_t)stream));
+    return cuda_status(smx::launch_attn_merge(*s, part_o, part_m, part_l, out, (cudaStream_t)stream));
 }
 
 int smx_decode_step(const smx_shape_t* s, const float* q_f32, const uint16_t* q_bf16, const uint16_t* qidx_bf16,
@@ -213,31 +207,22 @@ int smx_decode_step(const smx_shape_t* s, const float* q_f32, const uint16_t* q_
     if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
         return SMX_ERR_WORKSPACE;
     const Workspace w = layout(s, workspace);
-    cudaStream_t st = (cudaStream_t)stream;
-    // 1) insert, q packing, index scores and (last CTA of each row) the selection; 2) split stage;
-    // 3) merge. Each kernel is a programmatic dependent of the one before it and waits for it
-    //    before reading its output.
-    smx::FusedSelect fs;
-    fs.q_f32 = rs ? nullptr : q_f32;
-    fs.qbf = w.qbf;
-    fs.arrivals = w.arrivals;
-    fs.sel_pages = w.sel_pages;
-    fs.sel_phys = w.sel_phys;
-    fs.sel_count = w.sel_count;
-    fs.topk_out = topk_pages;
-    fs.count_out = topk_count;
-    if (smx::launch_index(*s, qidx_bf16, idx_pool, page_table, ctx_len, w.scores, dev_status, k_new, v_new,
-                          kidx_new, k_pool, v_pool, true, st, &fs) != cudaSuccess)
-        return SMX_ERR_CUDA;
-    if (smx::launch_attn_fused_split(*s, rs ? q_bf16 : w.qbf, k_pool, v_pool, ctx_len, w.sel_pages, w.sel_phys,
-                                     w.sel_count, w.part_o, w.part_m, w.part_l, dev_status, st) != cudaSuccess)
-        return SMX_ERR_CUDA;
-    return cuda_status(smx::launch_attn_merge(*s, w.part_o, w.part_m, w.part_l, out, true, st));
+    smx::StepIO io;
+    io.q_f32 = rs ? nullptr : q_f32;
+    io.q_bf16 = rs ? q_bf16 : nullptr;
+    io.qidx = qidx_bf16;
+    io.k_new = k_new; io.v_new = v_new; io.kidx_new = kidx_new;
+    io.page_table = page_table; io.ctx_len = ctx_len;
+    io.idx_pool = idx_pool; io.k_pool = k_pool; io.v_pool = v_pool;
+    io.topk_out = topk_pages; io.count_out = topk_count; io.out = out; io.status = dev_status;
+    io.counters = w.counters; io.scores = w.scores;
+    io.part_o = w.part_o; io.part_m = w.part_m; io.part_l = w.part_l;
+    return cuda_status(smx::launch_decode_step(*s, io, (cudaStream_t)stream));
 }
 
 int smx_decode_step_launches(const smx_shape_t* s) {
     if (check_shape(s) != SMX_OK) return 0;
-    return 3;
+    return 1;
 }
 
 int smx_suggest_num_splits(const smx_shape_t* s) {

@@ -305,6 +305,65 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // Order earlier generic-proxy accesses of shared memory before later async-proxy (bulk copy) ones.
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Order earlier generic-proxy accesses of global memory (including other threads' writes this
+// thread has acquired) before its later async-proxy (bulk copy) reads.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Hint: bring the 128-byte line holding p into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
+// ---- counters shared by the CTAs of one grid ---------------------------------------------------
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void spin_cycles(long long n) {
+    const long long t = clock64();
+    while (clock64() - t < n) {
+    }
+}
+
+// Release: this thread's earlier writes, and those of threads it synchronised with (a barrier
+// before the call), are visible before the increment is.
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// One thread waits until *p >= target, then orders its later reads after the writes released
+// before the update (a relaxed poll followed by an acquire fence). Between polls it sleeps
+// briefly (polling harder floods the counter's L2 slice and slows the updaters); it gives up
+// after about two seconds and 2^24 polls (false).
+__device__ __forceinline__ bool wait_geq_bounded(const uint32_t* p, uint32_t target) {
+    const uint64_t t0 = global_ns();
+    bool ok = false;
+    for (uint32_t i = 0; i < (1u << 24); ++i) {
+        if (ld_relaxed_u32(p) >= target) {
+            ok = true;
+            break;
+        }
+        if (global_ns() - t0 > 2000000000ull) break;
+        __nanosleep(i < 64 ? 32 : 128);
+    }
+    fence_acq_rel_gpu();
+    return ok;
+}
+
 // ---- shape helpers -----------------------------------------------------------------------------
 __device__ __forceinline__ int clamp_ctx(int ctx, int Q, int max_pages, int32_t* st) {
     const int cap = max_pages * kPage;

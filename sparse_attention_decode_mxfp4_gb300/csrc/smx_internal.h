@@ -32,34 +32,47 @@ cudaError_t launch_attn_split(const smx_shape_t& s, const void* q, const uint8_t
                               float* part_m, float* part_l, int32_t* status, cudaStream_t st);
 
 cudaError_t launch_attn_merge(const smx_shape_t& s, const float* part_o, const float* part_m,
-                              const float* part_l, float* out, bool pdl, cudaStream_t st);
-
-// The fused step's kernels: a1 + a2 + a3 + a4 in one launch (the scorer with the insert, the q
-// packing and, in the last CTA of each row, the selection), then a5 (split stage from the staged
-// selection); each may be launched as a programmatic dependent of the preceding kernel.
-// Workspace pieces through which the fused scorer hands the split stage the packed q and the
-// row's selection.
-struct FusedSelect {
-    const float* q_f32;   // MXFP4 K/V: q to pack (nullptr for the e4m3 row-scale format)
-    uint16_t* qbf;
-    int32_t* arrivals;
-    int32_t* sel_pages;
-    int32_t* sel_phys;
-    int32_t* sel_count;
-    int32_t* topk_out;
-    int32_t* count_out;
-};
-
-cudaError_t launch_index(const smx_shape_t& s, const uint16_t* qidx, uint8_t* idx_pool,
-                         const int32_t* page_table, const int32_t* ctx_len, float* scores, int32_t* status,
-                         const float* k_new, const float* v_new, const float* kidx_new, uint8_t* k_pool,
-                         uint8_t* v_pool, bool pdl, cudaStream_t st, const FusedSelect* fs);
+                              const float* part_l, float* out, cudaStream_t st);
 
 // Partition count that fills one wave of the device's SMs with split CTAs (0 on a CUDA error).
 int suggest_num_splits(const smx_shape_t& s);
-cudaError_t launch_attn_fused_split(const smx_shape_t& s, const uint16_t* qbf, const uint8_t* k_pool,
-                                    const uint8_t* v_pool, const int32_t* ctx_len, const int32_t* sel_pages,
-                                    const int32_t* sel_phys, const int32_t* sel_count, float* part_o,
-                                    float* part_m, float* part_l, int32_t* status, cudaStream_t st);
+
+// ---- the fused decode step (one cooperative kernel, smx_step.cu) ----
+struct StepGeom {
+    int row_warps;        // warps per token half of the attention (16 query rows each)
+    int rows_per_cta;     // 16 x row_warps
+    int n_rg;             // row groups per KV head
+    int page_bytes;       // bytes of one K or V page of one KV head
+    size_t smem;          // dynamic shared bytes of the kernel
+    size_t n_counters;    // u32 counters in the workspace: B rows, B x Hkv x n_rg groups, 1
+};
+StepGeom step_geom(const smx_shape_t& s);
+
+struct StepIO {
+    const float* q_f32;
+    const uint16_t* q_bf16;
+    const uint16_t* qidx;
+    const float* k_new;
+    const float* v_new;
+    const float* kidx_new;
+    const int32_t* page_table;
+    const int32_t* ctx_len;
+    uint8_t* idx_pool;
+    uint8_t* k_pool;
+    uint8_t* v_pool;
+    int32_t* topk_out;
+    int32_t* count_out;
+    float* out;
+    int32_t* status;
+    uint32_t* counters;   // n_counters, zero before the first step; every step leaves them zero
+    float* scores;        // [B][max_pages]
+    float* part_o;        // [B][S][Q][Hq][128]
+    float* part_m;        // [B][S][Q][Hq]
+    float* part_l;
+};
+cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStream_t st);
+
+// Bytes at the head of the decode-step workspace that must be zero before a step (the counters).
+size_t workspace_counter_bytes(const smx_shape_t& s);
 
 }  // namespace smx

@@ -1,9 +1,10 @@
 // smx_noalloc.cu -- smx_decode_step_noalloc: the decode step with its scratch held in a static
 // device array of SMX_NOALLOC_SCRATCH_BYTES, so that no call allocates device memory.
 //
-// The array is a module-scope device variable: the driver places it when the module is loaded
-// (zero-filled), and the first call on each device looks up its address once. Every later call
-// only launches the step's kernels into it. All calls on one device share the array.
+// The array is a module-scope device variable: the driver places it when the module is loaded,
+// and the first call on each device looks up its address once. Later calls launch the step into
+// it (plus a memset of the step counters when a shape needs more of them than the previous call
+// left zero). All calls on one device share the array.
 #include <mutex>
 
 #include "smx_internal.h"
@@ -15,10 +16,13 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
 void* g_scratch[kMaxDevices] = {};
+size_t g_zero_prefix[kMaxDevices] = {};   // leading bytes of the array known to be zero
 
-// Address of the scratch array on the current device. The first call on a device resolves it
-// (cudaGetSymbolAddress, which also loads the module there if it is not loaded yet) and clears
-// the per-row arrival counters at its head on `st`; the step's kernels leave them at zero again.
+// Address of the scratch array on the current device, with its first counter_bytes zero. The first
+// call on a device resolves it (cudaGetSymbolAddress, which also loads the module there if it is
+// not loaded yet) and clears the counters on `st`. The step leaves its counters zero but may write
+// its other data right after them, so a later call whose counters reach past the zero prefix the
+// previous call left clears them again (one memset on `st`).
 int scratch_on_current_device(void** out, size_t counter_bytes, cudaStream_t st) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SMX_ERR_CUDA;
@@ -30,9 +34,12 @@ int scratch_on_current_device(void** out, size_t counter_bytes, cudaStream_t st)
             (void)cudaGetLastError();
             return SMX_ERR_CUDA;
         }
-        if (cudaMemsetAsync(p, 0, counter_bytes, st) != cudaSuccess) return SMX_ERR_CUDA;
         g_scratch[dev] = p;
+        g_zero_prefix[dev] = 0;
     }
+    if (counter_bytes > g_zero_prefix[dev] && cudaMemsetAsync(g_scratch[dev], 0, counter_bytes, st) != cudaSuccess)
+        return SMX_ERR_CUDA;
+    g_zero_prefix[dev] = counter_bytes;
     *out = g_scratch[dev];
     return SMX_OK;
 }
@@ -53,8 +60,8 @@ extern "C" int smx_decode_step_noalloc(const smx_shape_t* s, const float* q_f32,
     }
     if (need > (size_t)SMX_NOALLOC_SCRATCH_BYTES) return SMX_ERR_WORKSPACE;
     void* scratch = nullptr;
-    // the arrival counters (one int per row) open the workspace layout
-    const int rc = scratch_on_current_device(&scratch, (size_t)s->B * sizeof(int32_t), (cudaStream_t)stream);
+    // the step's counters open the workspace layout
+    const int rc = scratch_on_current_device(&scratch, smx::workspace_counter_bytes(*s), (cudaStream_t)stream);
     if (rc != SMX_OK) return rc;
     return smx_decode_step(s, q_f32, q_bf16, qidx_bf16, k_new, v_new, kidx_new, page_table, ctx_len, k_pool, v_pool,
                            idx_pool, topk_pages, topk_count, out, scratch, (size_t)SMX_NOALLOC_SCRATCH_BYTES,

@@ -1,0 +1,487 @@
+// smx_step.cu -- the whole decode step (a1..a6) as one cooperative kernel.
+//
+// [ATOM-2812] "Mono decode over the MXFP4 KV and index caches": the new token rows are written
+// into the index, K and V pages before they are read ("--index-cache-dtype mxfp4", "MXFP4 main
+// KV"), q is packed to saturating e4m3 ("pack_q_e4m3"), every page of the row is scored, the
+// top-k pages are selected, the split stage runs over the selected pages only and the merge
+// combines the partitions.
+//
+// The grid holds at most one CTA per SM and is launched cooperatively, so all of its CTAs are
+// resident together and may wait for one another through counters in the workspace (never for a
+// CTA that could still be waiting to start). Phases of every CTA:
+//  A. Scoring. The B x max_pages page slots are cut into C chunks of P pages per row; chunk (b, j)
+//     is taken by CTA (b C + j) mod grid. The chunk's CTA writes the new index-K rows that land
+//     on its pages before it reads those pages (through L2), writes its share (j of C) of the
+//     row's new K/V rows, scores its pages and counts itself on the row's counter.
+//  B. Attention units (row b, KV head, row group, partition s), taken from the last CTA down. The
+//     unit's CTA first loads what does not depend on phase A (its q fragments, packed from f32 for
+//     MXFP4 K/V, and the row's page table), then waits for row b's C chunks, selects the row's
+//     top-k pages itself from the row's scores (every unit of the row computes the same
+//     selection, so no CTA waits for another to publish it), takes partition s of the ascending
+//     list and runs the split stage over it, writes its partials and counts itself on the (row,
+//     KV head, row group) counter.
+//  C. Merge. Each unit's CTA waits for the S partitions of its group and merges slice s of the
+//     group's query rows.
+//  D. The last CTA to finish resets every counter to zero for the next step.
+// Every wait is bounded (about two seconds); a wait that gives up sets SMX_DEV_TIMEOUT and the
+// CTA goes on without reading or writing out of bounds.
+#include <math.h>
+
+#include <mutex>
+
+#include "smx_attend.cuh"
+#include "smx_device.cuh"
+#include "smx_internal.h"
+#include "smx_score.cuh"
+#include "smx_select.cuh"
+
+namespace smx {
+
+struct StepArgs {
+    const float* q_f32;          // MXFP4 K/V: [B][Q][Hq][128], packed here
+    const uint16_t* q_bf16;      // FP8-KV: [B][Q][Hq][128] bf16 bits
+    const uint16_t* qidx;        // [B][Q][128] bf16 bits
+    const float* k_new;          // [B][Q][Hkv][128]
+    const float* v_new;
+    const float* kidx_new;       // [B][Q][128]
+    const int32_t* page_table;   // [B][max_pages]
+    const int32_t* ctx_len;      // [B]
+    uint8_t* idx_pool;
+    uint8_t* k_pool;
+    uint8_t* v_pool;
+    int32_t* topk_out;           // [B][topk]
+    int32_t* count_out;          // [B]
+    float* out;                  // [B][Q][Hq][128]
+    int32_t* status;
+    uint32_t* row_cnt;           // [B] chunks scored
+    uint32_t* grp_cnt;           // [B][Hkv][n_rg] partitions written
+    uint32_t* done_cnt;          // [1] CTAs past their last wait
+    float* scores;               // [B][max_pages]
+    float* part_o;               // [B][S][Q][Hq][128]
+    float* part_m;               // [B][S][Q][Hq]
+    float* part_l;
+    int64_t n_pool;
+    int B, Q, Hq, Hkv, G, max_pages, topk, S;
+    int row_warps, rows_per_cta, n_rg, page_bytes;
+    int chunk_pages, chunks_per_row;
+};
+
+constexpr int kStepWarps = 8;
+constexpr int kStepMaxChunk = 256;   // pages of one scoring chunk (page-table entries in smem)
+constexpr int kRedPages = 32;        // page maxima combined per flush
+constexpr int kPtCache = 2048;       // page-table entries of a unit's row kept in shared memory
+constexpr int kCounterStride = 32;   // u32 words between counters: each on its own 128-byte line
+
+template <bool RS, int NT>
+__global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(16) uint32_t qh[16][64];
+    __shared__ int sig[16];
+    __shared__ float red[kRedPages][kStepWarps];
+    __shared__ int64_t phys_s[kStepMaxChunk];
+    __shared__ SelectSmem selsm;
+    __shared__ __align__(8) uint64_t mbar[2];
+    __shared__ __align__(8) uint64_t mbar_q;   // the first unit's q rows
+    __shared__ int stage_page[2];
+    __shared__ int is_last;
+    __shared__ int32_t pt_s[kPtCache];   // the unit's row of the page table (rows up to kPtCache pages)
+
+    const AttendSmem sm = attend_smem(smem, a.page_bytes, mbar, stage_page);
+    uint32_t* keys = reinterpret_cast<uint32_t*>(smem);                  // selection keys (tile region)
+    int* sel_all = reinterpret_cast<int*>(sm.raw + 4 * a.page_bytes);    // the row's selection
+    int* sel = sel_all + a.topk;                                         // this partition's pages
+    int* selph = sel + a.topk;                                           // and their physical ids
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int nC = gridDim.x, c = blockIdx.x;
+    if (threadIdx.x == 0) {
+        mbar_init(&mbar[0], 1);
+        mbar_init(&mbar[1], 1);
+        mbar_init(&mbar_q, 1);
+        mbar_fence_init();
+    }
+
+    const int P = a.chunk_pages, C = a.chunks_per_row;
+    const int kv_rows = a.Q * 2 * a.Hkv;
+    const int M = a.G * a.Q;
+    const int n_units = a.B * a.Hkv * a.n_rg * a.S;
+
+    // This CTA's first attention unit: its q rows are staged into shared memory (bulk copies into
+    // the page-stage area, unused until the attention) and its row of the page table is loaded,
+    // before phase A, so that neither has to be fetched after it.
+    const int u0 = nC - 1 - c;
+    const int R = a.rows_per_cta;
+    const bool q_stageable = !RS || (reinterpret_cast<uintptr_t>(a.q_bf16) & 15u) == 0;
+    if (u0 < n_units) {
+        const int rg = (u0 / a.S) % a.n_rg, kvh = (u0 / (a.S * a.n_rg)) % a.Hkv, b = u0 / (a.S * a.n_rg * a.Hkv);
+        if (q_stageable && threadIdx.x == 0) {
+            const int m_lo = rg * R, m_hi = min(M, m_lo + R);
+            const uint32_t row_bytes = RS ? kD * 2 : kD * 4;
+            const uint8_t* q = RS ? reinterpret_cast<const uint8_t*>(a.q_bf16) : reinterpret_cast<const uint8_t*>(a.q_f32);
+            mbar_arrive_expect_tx(&mbar_q, (uint32_t)(m_hi - m_lo) * row_bytes);
+            // rows of one draft token are consecutive heads: one copy per token
+            for (int tq = m_lo / a.G; tq * a.G < m_hi; ++tq) {
+                const int r0 = max(m_lo, tq * a.G), r1 = min(m_hi, (tq + 1) * a.G);
+                const int64_t row = ((int64_t)b * a.Q + tq) * a.Hq + kvh * a.G + r0 % a.G;
+                bulk_g2s(sm.raw + (r0 - m_lo) * row_bytes, q + row * row_bytes, (uint32_t)(r1 - r0) * row_bytes, &mbar_q);
+            }
+        }
+    }
+    const int ctx_u0 = u0 < n_units ? a.ctx_len[u0 / (a.S * a.n_rg * a.Hkv)] : 0;   // the first unit's row length
+    // the first unit's row of the page table: loaded into registers now, stored to pt_s once the
+    // first chunk's loads are out (a store right here would hold the warp for the round trip)
+    constexpr int kPtPerThread = kPtCache / (kStepWarps * 32);
+    int32_t pt_r[kPtPerThread];
+    const int n_pt0 = u0 < n_units ? min(a.max_pages, kPtCache) : 0;
+    {
+        const int b = u0 < n_units ? u0 / (a.S * a.n_rg * a.Hkv) : 0;
+#pragma unroll
+        for (int k = 0; k < kPtPerThread; ++k) {
+            const int i = threadIdx.x + k * kStepWarps * 32;
+            pt_r[k] = i < n_pt0 ? a.page_table[(int64_t)b * a.max_pages + i] : 0;
+        }
+    }
+    bool pt_stored = false;
+    auto store_pt = [&]() {
+#pragma unroll
+        for (int k = 0; k < kPtPerThread; ++k) {
+            const int i = threadIdx.x + k * kStepWarps * 32;
+            if (i < n_pt0) pt_s[i] = pt_r[k];
+        }
+        pt_stored = true;
+    };
+    // ---------------- A. scoring chunks ----------------
+    for (int ci = c; ci < a.B * C; ci += nC) {
+        const int b = ci / C, j = ci % C;
+        const int p0 = j * P, np_max = max(0, min(P, a.max_pages - p0));
+        // independent loads first: the row's length, this chunk's page-table entries, the index
+        // query, and the first new K/V row of this warp's share (rows j + C w, j + C (w + 8), ...)
+        const int ctx_raw = a.ctx_len[b];
+        for (int i = threadIdx.x; i < np_max; i += blockDim.x) {
+            const int64_t ph = a.page_table[(int64_t)b * a.max_pages + p0 + i];
+            phys_s[i] = (ph < 0 || ph >= a.n_pool) ? -1 : ph;
+        }
+        const IndexQueryRaw qraw = load_index_query(a.qidx + (int64_t)b * a.Q * kD, a.Q);
+        // the row's new index-K rows, one per warp (written below if this chunk owns their page)
+        float4 kidx_x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (warp < a.Q) kidx_x = reinterpret_cast<const float4*>(a.kidx_new + ((int64_t)b * a.Q + warp) * kD)[lane];
+        const int kv_r0 = j + C * warp;
+        auto kv_row_src = [&](int r) {
+            const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);   // kind < Hkv: K head, else V head
+            const int64_t tok = (int64_t)b * a.Q + tq;
+            return reinterpret_cast<const float4*>((kind < a.Hkv ? a.k_new : a.v_new) + (tok * a.Hkv + kind % a.Hkv) * kD) + lane;
+        };
+        float4 kv_x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (kv_r0 < kv_rows) kv_x = *kv_row_src(kv_r0);
+        const int ctx = clamp_ctx(ctx_raw, a.Q, a.max_pages, (j == 0 && threadIdx.x == 0) ? a.status : nullptr);
+        const int n_pages = (ctx + kPage - 1) / kPage;
+        const int np = max(0, min(np_max, n_pages - p0));
+        const int first_new = ctx - a.Q;
+        // chunk pages [own_lo, own_hi) take new index-K rows (positions [lo_new, hi_new))
+        const int lo_new = max(max(first_new, 0), p0 * kPage), hi_new = min(ctx, (p0 + np) * kPage);
+        const bool owner = lo_new < hi_new;
+        const int own_lo = owner ? lo_new / kPage - p0 : np, own_hi = owner ? (hi_new - 1) / kPage - p0 + 1 : np;
+        __syncthreads();   // page-table entries staged (and the mbarriers initialised)
+
+        // pages go four at a time to the four warp pairs; warp 2q + h scores tiles 4h .. 4h + 3 of
+        // page i0 + q into a per-lane running maximum (one warp reduction per page). The next
+        // group's tiles are in flight while a group is scored; the pages that take no new rows go
+        // out before the inserts.
+        const int pq = warp >> 1, tile0 = (warp & 1) * 4;
+        TileFrag fa[4], fb[4];
+        auto load_page = [&](TileFrag (&f)[4], int i, bool skip_own) {
+            if (i < np && phys_s[i] >= 0 && !(skip_own && i >= own_lo && i < own_hi)) {
+                const uint8_t* page = a.idx_pool + phys_s[i] * kMxPageBytes;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) load_tile(f[k], page, tile0 + k, g, t);
+            }
+        };
+        load_page(fa, pq, true);
+        if (!pt_stored) store_pt();
+        int64_t kv_phys0 = -1;   // page of this warp's first K/V row (used after the scoring)
+        if (kv_r0 < kv_rows && first_new + kv_r0 / (2 * a.Hkv) >= 0)
+            kv_phys0 = a.page_table[(int64_t)b * a.max_pages + (first_new + kv_r0 / (2 * a.Hkv)) / kPage];
+        if (owner) {
+            // the new index-K rows on this chunk's pages (one warp per row), then those pages' tiles
+            for (int tq = warp; tq < a.Q; tq += kStepWarps) {
+                const int pos = first_new + tq;
+                if (pos < lo_new || pos >= hi_new) continue;
+                const int64_t phys = phys_s[pos / kPage - p0];
+                if (phys < 0) {
+                    if (lane == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                    continue;
+                }
+                const float4 x = tq == warp ? kidx_x : reinterpret_cast<const float4*>(a.kidx_new + ((int64_t)b * a.Q + tq) * kD)[lane];
+                uint8_t* page = a.idx_pool + phys * kMxPageBytes;
+                quant_row_mxfp4_warp(x, page + (pos % kPage) * 64, page + kMxScaleOff + (pos % kPage) * 4, lane);
+            }
+            __threadfence();
+            __syncthreads();
+            if (pq >= own_lo && pq < own_hi) load_page(fa, pq, false);
+        }
+
+        uint32_t qf[NT][16];
+        int sig_c[NT][2];
+        setup_index_query<NT>(qraw, a.Q, qh, sig, qf, sig_c);
+        const int lim = ctx - a.Q;   // token j counts for query n iff j <= lim + n
+#pragma unroll 1
+        for (int i0 = 0; i0 < np; i0 += 4) {
+            if (i0 + 4 < np) load_page(fb, i0 + 4 + pq, false);
+            const int i = i0 + pq;
+            if (i < np) {
+                float best = -INFINITY;
+                if (phys_s[i] >= 0) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        best = fmaxf(best, score_tile<NT>(fa[k], qf, sig_c, p0 + i, tile0 + k, g, t, lim, a.Q));
+                } else if ((warp & 1) == 0 && lane == 0) {
+                    flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
+                if (lane == 0) red[i % kRedPages][warp & 1] = best;
+            }
+            if ((i0 + 4) % kRedPages == 0 || i0 + 4 >= np) {   // page maxima of pages [base, i0 + 4)
+                __syncthreads();
+                const int base = (i0 / kRedPages) * kRedPages;
+                const int cnt = min(i0 + 4, np) - base;
+                if ((int)threadIdx.x < cnt)
+                    a.scores[(int64_t)b * a.max_pages + p0 + base + threadIdx.x] =
+                        fmaxf(red[threadIdx.x][0], red[threadIdx.x][1]);
+                __syncthreads();
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) fa[k] = fb[k];
+        }
+
+        // this warp's new K/V rows (read only by the attention phase, after the row's counter)
+        for (int r = kv_r0; r < kv_rows; r += C * kStepWarps) {
+            const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);
+            const int pos = first_new + tq;
+            if (pos < 0) continue;
+            const float4 x = r == kv_r0 ? kv_x : *kv_row_src(r);
+            const int64_t phys = r == kv_r0 ? kv_phys0 : (int64_t)a.page_table[(int64_t)b * a.max_pages + pos / kPage];
+            if (phys < 0 || phys >= a.n_pool) {
+                if (lane == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                continue;
+            }
+            const int h = kind % a.Hkv, slot = pos % kPage;
+            uint8_t* pool = kind < a.Hkv ? a.k_pool : a.v_pool;
+            if (RS) {
+                uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kRsPageBytes;
+                quant_row_e4m3rs_warp(x, page + slot * 128, reinterpret_cast<float*>(page + kRsScaleOff) + slot, lane);
+            } else {
+                uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kMxPageBytes;
+                quant_row_mxfp4_warp(x, page + slot * 64, page + kMxScaleOff + slot * 4, lane);
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) red_release_add(&a.row_cnt[kCounterStride * b], 1u);
+    }
+
+    // ---------------- B. attention units ----------------
+    if (!pt_stored) store_pt();
+    uint32_t gp = 0;          // pages staged by this CTA so far (sets the stages' phase parity)
+    bool copies_ok = true;    // false after a copy that did not land: stage nothing more
+    for (int u = u0; u < n_units; u += nC) {
+        const int s = u % a.S, rg = (u / a.S) % a.n_rg, kvh = (u / (a.S * a.n_rg)) % a.Hkv;
+        const int b = u / (a.S * a.n_rg * a.Hkv);
+        const bool first = u == u0;
+        const int ctx = clamp_ctx(first ? ctx_u0 : a.ctx_len[b], a.Q, a.max_pages, nullptr);
+        const int n_pages = (ctx + kPage - 1) / kPage;
+        const bool pt_cached = n_pages <= kPtCache;
+        const AttendLane L = attend_lane(rg, R, a.row_warps, M, a.G);
+        uint32_t qa[8][4];
+        if (!first || !q_stageable) {
+            // later units: q and the page table from global memory, before the wait
+            if (RS) load_qa_bf16<false>(qa, a.q_bf16, L, b, kvh, a.Q, a.Hq, a.G);
+            else load_qa_f32_e4m3(qa, a.q_f32, L, b, kvh, a.Q, a.Hq, a.G);
+        } else {
+            // the first unit's q rows were staged at the start: unpack them before the wait
+            if (!mbar_wait_bounded(&mbar_q, 0)) flag_status(a.status, SMX_DEV_TIMEOUT);
+            pack_staged_q<RS>(sm.raw, min(M - rg * R, R));
+            load_qa_packed(qa, sm.raw, rg * R, L);
+        }
+        if (!first && pt_cached) {
+            __syncthreads();   // the previous unit is done with pt_s
+            for (int base = 0; base < n_pages; base += kPtPerThread * kStepWarps * 32) {
+                int32_t v[kPtPerThread];
+#pragma unroll
+                for (int k = 0; k < kPtPerThread; ++k) {
+                    const int i = base + threadIdx.x + k * kStepWarps * 32;
+                    v[k] = i < n_pages ? a.page_table[(int64_t)b * a.max_pages + i] : 0;
+                }
+#pragma unroll
+                for (int k = 0; k < kPtPerThread; ++k) {
+                    const int i = base + threadIdx.x + k * kStepWarps * 32;
+                    if (i < n_pages) pt_s[i] = v[k];
+                }
+            }
+        }
+        if (threadIdx.x == 0 && !wait_geq_bounded(&a.row_cnt[kCounterStride * b], (uint32_t)C)) flag_status(a.status, SMX_DEV_TIMEOUT);
+        __syncthreads();
+        load_keys<true>(keys, a.scores + (int64_t)b * a.max_pages, n_pages);
+        __syncthreads();   // keys in place; the staged q rows read (the page stages are free)
+        const int k_eff = block_select(keys, n_pages, a.topk, sel_all, selsm);
+        const int lo = (int)(((int64_t)s * k_eff) / a.S), hi = (int)(((int64_t)(s + 1) * k_eff) / a.S);
+        auto resolve = [&](int i) {   // entry i of this partition: logical and physical page
+            const int p = sel_all[lo + i];
+            const int64_t v = pt_cached ? pt_s[p] : a.page_table[(int64_t)b * a.max_pages + p];
+            int ph = -1;
+            if (v >= 0 && v < a.n_pool) ph = (int)v;
+            else flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+            sel[i] = p;
+            selph[i] = ph;
+            return ph;
+        };
+        // the first two pages' copies go out first; the row's new K/V rows (other CTAs' writes,
+        // acquired above) are ordered before them
+        if (threadIdx.x == 0 && copies_ok) {
+            fence_proxy_async_global();
+            fence_proxy_async_smem();   // the staged q rows were read from the page stages
+            for (int i = 0; i < 2 && i < hi - lo; ++i)
+                attend_issue(sm, i, sel_all[lo + i], resolve(i), gp, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes);
+        }
+        for (int i = 2 + threadIdx.x; i < hi - lo; i += blockDim.x) resolve(i);
+        if (kvh == 0 && rg == 0 && s == 0) {
+            for (int i = threadIdx.x; i < a.topk; i += blockDim.x)
+                a.topk_out[(int64_t)b * a.topk + i] = i < k_eff ? sel_all[i] : -1;
+            if (threadIdx.x == 0) a.count_out[b] = k_eff;
+        }
+        __syncthreads();
+
+        float o[16][4];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+        float mrow0 = -INFINITY, mrow1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+        const int pos0 = ctx - a.Q + L.t0, pos1 = ctx - a.Q + L.t1;
+        if (copies_ok)
+            copies_ok = attend_pages<RS>(sm, sel, selph, hi - lo, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes, ctx,
+                                         qa, L, pos0, pos1, gp, o, mrow0, mrow1, l0, l1, a.status, true);
+        finish_partials(sm, L, o, mrow0, mrow1, l0, l1, a.part_o, a.part_m, a.part_l, b, s, kvh, a.S, a.Q, a.Hq, a.G);
+        __syncthreads();
+        if (threadIdx.x == 0) red_release_add(&a.grp_cnt[kCounterStride * ((b * a.Hkv + kvh) * a.n_rg + rg)], 1u);
+    }
+
+    // ---------------- C. merge: slice s of each unit's group ----------------
+    const int QH = a.Q * a.Hq;
+    for (int u = u0; u < n_units; u += nC) {
+        const int s = u % a.S, rg = (u / a.S) % a.n_rg, kvh = (u / (a.S * a.n_rg)) % a.Hkv;
+        const int b = u / (a.S * a.n_rg * a.Hkv);
+        if (threadIdx.x == 0 && !wait_geq_bounded(&a.grp_cnt[kCounterStride * ((b * a.Hkv + kvh) * a.n_rg + rg)], (uint32_t)a.S))
+            flag_status(a.status, SMX_DEV_TIMEOUT);
+        __syncthreads();
+        const int r_end = min((s + 1) * R / a.S, M - rg * R);
+        for (int lr = s * R / a.S + warp; lr < r_end; lr += kStepWarps) {
+            const int m = rg * R + lr;
+            const int r = (m / a.G) * a.Hq + kvh * a.G + m % a.G;   // draft token x Hq + head
+            merge_row<true>(a.part_o, a.part_m, a.part_l, (int64_t)b * a.S * QH + r, QH, a.S,
+                            a.out + ((int64_t)b * QH + r) * kD);
+        }
+    }
+
+    // ---------------- D. the last CTA out clears the counters ----------------
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        is_last = atomicAdd(a.done_cnt, 1u) == (uint32_t)nC - 1;
+    }
+    __syncthreads();
+    if (is_last) {
+        for (int i = threadIdx.x; i < a.B; i += blockDim.x) a.row_cnt[kCounterStride * i] = 0;
+        for (int i = threadIdx.x; i < a.B * a.Hkv * a.n_rg; i += blockDim.x) a.grp_cnt[kCounterStride * i] = 0;
+        if (threadIdx.x == 0) *a.done_cnt = 0;
+    }
+}
+
+// ---- host side -------------------------------------------------------------------------------------
+StepGeom step_geom(const smx_shape_t& s) {
+    StepGeom g;
+    const int M = (s.Hq / s.Hkv) * s.Q;
+    g.row_warps = min(kAttnMaxWarps / 2, (M + 15) / 16);
+    g.rows_per_cta = 16 * g.row_warps;
+    g.n_rg = (M + g.rows_per_cta - 1) / g.rows_per_cta;
+    g.page_bytes = s.kv_format == SMX_KV_E4M3_ROWSCALE ? kRsPageBytes : kMxPageBytes;
+    g.smem = attend_smem_bytes(g.page_bytes) + 12 * (size_t)s.topk;
+    g.n_counters = kCounterStride * ((size_t)s.B + (size_t)s.B * s.Hkv * g.n_rg + 1);
+    return g;
+}
+
+template <bool RS, int NT>
+static const void* step_fn() {
+    return reinterpret_cast<const void*>(decode_step_kernel<RS, NT>);
+}
+
+// Resident CTAs of the step kernel on the current device (cached per device, kernel and size).
+static int step_max_ctas(const void* fn, size_t smem) {
+    struct Entry { int dev; const void* fn; size_t smem; int n; };
+    static std::mutex mu;
+    static Entry seen[32];
+    static int n_seen = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_seen; ++i)
+        if (seen[i].dev == dev && seen[i].fn == fn && seen[i].smem == smem) return seen[i].n;
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kStepWarps * 32, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    const int n = sms * min(per_sm, 1);
+    if (n_seen < 32) seen[n_seen++] = Entry{dev, fn, smem, n};
+    return n;
+}
+
+cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStream_t st) {
+    const StepGeom geo = step_geom(s);
+    const bool rs = s.kv_format == SMX_KV_E4M3_ROWSCALE;
+    const bool nt2 = s.Q > 8;
+    const void* fn = rs ? (nt2 ? step_fn<true, 2>() : step_fn<true, 1>()) : (nt2 ? step_fn<false, 2>() : step_fn<false, 1>());
+    cudaError_t e = ensure_smem_attr(fn, (int)geo.smem);
+    if (e != cudaSuccess) return e;
+    const int max_ctas = step_max_ctas(fn, geo.smem);
+    if (max_ctas < 1) return cudaErrorCooperativeLaunchTooLarge;
+
+    StepArgs a = {};
+    a.q_f32 = io.q_f32; a.q_bf16 = io.q_bf16; a.qidx = io.qidx;
+    a.k_new = io.k_new; a.v_new = io.v_new; a.kidx_new = io.kidx_new;
+    a.page_table = io.page_table; a.ctx_len = io.ctx_len;
+    a.idx_pool = io.idx_pool; a.k_pool = io.k_pool; a.v_pool = io.v_pool;
+    a.topk_out = io.topk_out; a.count_out = io.count_out; a.out = io.out; a.status = io.status;
+    a.row_cnt = io.counters;
+    a.grp_cnt = io.counters + kCounterStride * s.B;
+    a.done_cnt = io.counters + kCounterStride * (s.B + (size_t)s.B * s.Hkv * geo.n_rg);
+    a.scores = io.scores; a.part_o = io.part_o; a.part_m = io.part_m; a.part_l = io.part_l;
+    a.n_pool = s.n_pool_pages;
+    a.B = s.B; a.Q = s.Q; a.Hq = s.Hq; a.Hkv = s.Hkv; a.G = s.Hq / s.Hkv; a.max_pages = s.max_pages_per_row;
+    a.topk = s.topk; a.S = s.num_splits;
+    a.row_warps = geo.row_warps; a.rows_per_cta = geo.rows_per_cta; a.n_rg = geo.n_rg; a.page_bytes = geo.page_bytes;
+
+    // grid: enough CTAs for every attention unit and for two pages each, at most one per SM
+    const int64_t n_units = (int64_t)s.B * s.Hkv * geo.n_rg * s.num_splits;
+    const int64_t slots = (int64_t)s.B * s.max_pages_per_row;
+    const int64_t want = n_units > (slots + 1) / 2 ? n_units : (slots + 1) / 2;
+    const int n_ctas = (int)(want < max_ctas ? want : max_ctas);
+    int64_t P = (slots + n_ctas - 1) / n_ctas;
+    if (P > kStepMaxChunk) P = kStepMaxChunk;
+    a.chunk_pages = (int)P;
+    a.chunks_per_row = (int)((s.max_pages_per_row + P - 1) / P);
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_ctas);
+    cfg.blockDim = dim3(kStepWarps * 32);
+    cfg.dynamicSmemBytes = geo.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (rs) return nt2 ? cudaLaunchKernelEx(&cfg, decode_step_kernel<true, 2>, a) : cudaLaunchKernelEx(&cfg, decode_step_kernel<true, 1>, a);
+    return nt2 ? cudaLaunchKernelEx(&cfg, decode_step_kernel<false, 2>, a) : cudaLaunchKernelEx(&cfg, decode_step_kernel<false, 1>, a);
+}
+
+}  // namespace smx
