@@ -78,15 +78,15 @@ def peaks():
 
 def kernel_sources_sha():
     h = hashlib.sha256()
-    for f in ("smx_index.cu", "smx_device.cuh"):
+    for f in ("smx_step.cu", "smx_attend.cuh", "smx_score.cuh", "smx_select.cuh", "smx_device.cuh"):
         h.update(open(os.path.join(ROOT, "sparse_attention_decode_mxfp4_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload_name):
-    """DRAM bytes per launch of the index scorer from a committed ncu summary, if it was taken
-    on the current kernel source and this workload; else None."""
-    p = os.path.join(ROOT, "profiles", "index_score_traffic.json")
+    """DRAM bytes per launch of the decode-step kernel from a committed ncu summary, if it was
+    taken on the current kernel source and this workload; else None."""
+    p = os.path.join(ROOT, "profiles", "decode_step_traffic.json")
     if not os.path.exists(p):
         return None
     try:
@@ -306,23 +306,12 @@ def main():
     us_step = ms * 1e3 / args.steps
     value = step_bytes * world * args.steps / (ms * 1e-3) / 1e9
 
-    # ---- dominant kernel (index scorer) alone, same rotation, CUDA events on its stream ----
-    scores = torch.empty((w.B, w.max_pages), dtype=torch.float32, device=dev)
-    g_idx = torch.cuda.CUDAGraph()
-    n_idx = args.steps
-    with torch.cuda.stream(s):
-        with torch.cuda.graph(g_idx, stream=s):
-            for i in range(n_idx):
-                ops.index_score(shape, inp["qidx_bf16"], copies[i % R][2], page_table, ctx_len, scores)
-    g_idx.replay()
-    torch.cuda.synchronize()
-    e0.record(cur)
-    g_idx.replay()
-    e1.record(cur)
-    e1.synchronize()
-    idx_us = e0.elapsed_time(e1) * 1e3 / n_idx
+    # ---- the dominant kernel: the step is one kernel (decode_step_kernel), timed above with CUDA
+    # events on the replay stream; its algorithmic bytes per launch are the step's bytes
     peak, peak_kind = peaks()
-    achieved = idx_b / (idx_us * 1e-6) / 1e9
+    launches_per_step = ops.decode_step_launches(shape)
+    kernel_us = us_step / launches_per_step
+    achieved = step_bytes / launches_per_step / (kernel_us * 1e-6) / 1e9
 
     # ---- end to end through the public API: pinned host inputs in, output back, every step ----
     host_in = {k: v.cpu().pin_memory() for k, v in inp.items() if v is not None}
@@ -363,11 +352,10 @@ def main():
                            index_bytes=idx_b, kv_bytes=kv_b, parallelism="replicas" if world > 1 else "single",
                            l2=f"rotating {R} pool copies ({R * pool_bytes / 1e6:.0f} MB, reads "
                               f"{R * step_bytes / 1e6:.0f} MB per rotation > 3x L2 {l2 / 1e6:.0f} MB)"),
-            "roofline": {"bound": "hbm", "kernel": "index_score_kernel", "achieved": achieved, "peak": peak,
+            "roofline": {"bound": "hbm", "kernel": "decode_step_kernel", "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": recorded_traffic(w.name), "us_per_launch": idx_us,
-                         "algorithmic_bytes_per_launch": idx_b},
-            "step_roofline_frac": value / world / peak,
+                         "traffic": recorded_traffic(w.name), "us_per_launch": kernel_us,
+                         "algorithmic_bytes_per_launch": step_bytes // launches_per_step},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "GB/s", "us_per_step": e2e_s * 1e6, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
