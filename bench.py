@@ -78,7 +78,8 @@ def peaks():
 
 def kernel_sources_sha():
     h = hashlib.sha256()
-    for f in ("smx_step.cu", "smx_attend.cuh", "smx_score.cuh", "smx_select.cuh", "smx_device.cuh"):
+    for f in ("smx_step.cu", "smx_attend.cuh", "smx_attend_tc.cuh", "smx_tc.cuh", "smx_score.cuh", "smx_select.cuh",
+              "smx_device.cuh"):
         h.update(open(os.path.join(ROOT, "sparse_attention_decode_mxfp4_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 

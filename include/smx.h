@@ -175,6 +175,13 @@ const char* smx_status_string(int status);
 /* Number of kernel launches smx_decode_step enqueues for this shape. */
 int smx_decode_step_launches(const smx_shape_t* shape);
 
+/* Whether smx_decode_step runs its attention on the fifth-generation tensor cores (tcgen05,
+ * 128-row tiles) for this shape on the CURRENT device: 1 yes, 0 no (mma.sync, up to 64-row
+ * tiles), SMX_ERR_INVALID_ARG / SMX_ERR_UNSUPPORTED for a bad shape. The tensor-core path is taken
+ * when the 64-row attention units (B x Hkv x row groups x S) would need more than one wave of the
+ * device's SMs. Reads device attributes; launches nothing. */
+int smx_decode_step_tensor_cores(const smx_shape_t* shape);
+
 /* A partition count S for this shape on the CURRENT device (the pages leave S to the
  * implementation: any S >= 1 gives the same attention up to rounding). It is the largest S
  * whose split CTAs (B x Hkv x row groups per partition) fill at most one wave of the device's

@@ -225,6 +225,12 @@ int smx_decode_step_launches(const smx_shape_t* s) {
     return 1;
 }
 
+int smx_decode_step_tensor_cores(const smx_shape_t* s) {
+    const int rc = check_shape(s);
+    if (rc) return rc;
+    return smx::decode_step_uses_tc(*s) ? 1 : 0;
+}
+
 int smx_suggest_num_splits(const smx_shape_t* s) {
     if (s == nullptr) return 0;
     smx_shape_t t = *s;

@@ -117,10 +117,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const floa
 }
 
 int suggest_num_splits(const smx_shape_t& s) {
+    // attention units of up to 64 query rows of one KV head each, one CTA per SM
     const int M = (s.Hq / s.Hkv) * s.Q;
     const int row_warps = min(kAttnMaxWarps / 2, (M + 15) / 16);
-    const int rows_per_cta = row_warps * 16;
-    const int ctas_per_split = s.B * s.Hkv * ((M + rows_per_cta - 1) / rows_per_cta);
+    const int ctas_per_split = s.B * s.Hkv * ((M + 16 * row_warps - 1) / (16 * row_warps));
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         (void)cudaGetLastError();

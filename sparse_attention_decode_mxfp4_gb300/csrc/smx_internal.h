@@ -46,7 +46,10 @@ struct StepGeom {
     size_t smem;          // dynamic shared bytes of the kernel
     size_t n_counters;    // u32 counters in the workspace: B rows, B x Hkv x n_rg groups, 1
 };
-StepGeom step_geom(const smx_shape_t& s);
+StepGeom step_geom(const smx_shape_t& s);                // the workspace's geometry (either path)
+StepGeom step_geom(const smx_shape_t& s, bool tc);       // tc: the tensor-core attention path
+// Whether the fused step runs its attention on the tensor-core path for this shape (current device).
+bool decode_step_uses_tc(const smx_shape_t& s);
 
 struct StepIO {
     const float* q_f32;

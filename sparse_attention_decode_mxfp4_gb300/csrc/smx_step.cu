@@ -30,6 +30,7 @@
 #include <mutex>
 
 #include "smx_attend.cuh"
+#include "smx_attend_tc.cuh"
 #include "smx_device.cuh"
 #include "smx_internal.h"
 #include "smx_score.cuh"
@@ -72,9 +73,9 @@ constexpr int kRedPages = 32;        // page maxima combined per flush
 constexpr int kPtCache = 2048;       // page-table entries of a unit's row kept in shared memory
 constexpr int kCounterStride = 32;   // u32 words between counters: each on its own 128-byte line
 
-template <bool RS, int NT>
+template <bool RS, int NT, bool TC>
 __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ __align__(16) uint32_t qh[16][64];
     __shared__ int sig[16];
     __shared__ float red[kRedPages][kStepWarps];
@@ -85,12 +86,33 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
     __shared__ int stage_page[2];
     __shared__ int is_last;
     __shared__ int32_t pt_s[kPtCache];   // the unit's row of the page table (rows up to kPtCache pages)
+    __shared__ __align__(8) uint64_t mbar_mma;   // tensor-core MMA completions
+    __shared__ uint32_t tmem_slot;
+    __shared__ float xch_tc[kStepWarps * 32];    // row maxima / sums exchanged between the two halves
 
-    const AttendSmem sm = attend_smem(smem, a.page_bytes, mbar, stage_page);
-    uint32_t* keys = reinterpret_cast<uint32_t*>(smem);                  // selection keys (tile region)
-    int* sel_all = reinterpret_cast<int*>(sm.raw + 4 * a.page_bytes);    // the row's selection
-    int* sel = sel_all + a.topk;                                         // this partition's pages
-    int* selph = sel + a.topk;                                           // and their physical ids
+    // dynamic shared memory. Tensor-core path: the tiles of smx_attend_tc.cuh, then the
+    // partition's lists; before the attention the K and V tiles hold the selection keys, the P
+    // tile the selection and the V / P tiles the staged q rows. mma.sync path: the bf16 tiles of
+    // smx_attend.cuh (also the keys), the page stages (also the staged q rows), then the lists.
+    AttendSmem sm;
+    uint32_t* keys;
+    int* sel_all;
+    uint8_t* q_stage;
+    if constexpr (TC) {
+        sm.raw = smem + kTcRaw;
+        sm.mbar = mbar;
+        sm.stage_page = stage_page;
+        keys = reinterpret_cast<uint32_t*>(smem + kTcK);
+        sel_all = reinterpret_cast<int*>(smem + kTcP);
+        q_stage = smem + kTcV;
+    } else {
+        sm = attend_smem(smem, a.page_bytes, mbar, stage_page);
+        keys = reinterpret_cast<uint32_t*>(smem);
+        sel_all = reinterpret_cast<int*>(sm.raw + 4 * a.page_bytes) + 2 * a.topk;
+        q_stage = sm.raw;
+    }
+    int* sel = reinterpret_cast<int*>(sm.raw + 4 * a.page_bytes);   // this partition's pages
+    int* selph = sel + a.topk;                                       // and their physical ids
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
@@ -99,6 +121,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
         mbar_init(&mbar[0], 1);
         mbar_init(&mbar[1], 1);
         mbar_init(&mbar_q, 1);
+        mbar_init(&mbar_mma, 1);
         mbar_fence_init();
     }
 
@@ -108,7 +131,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
     const int n_units = a.B * a.Hkv * a.n_rg * a.S;
 
     // This CTA's first attention unit: its q rows are staged into shared memory (bulk copies into
-    // the page-stage area, unused until the attention) and its row of the page table is loaded,
+    // the V and P tiles, unused until the attention) and its row of the page table is loaded,
     // before phase A, so that neither has to be fetched after it.
     const int u0 = nC - 1 - c;
     const int R = a.rows_per_cta;
@@ -124,7 +147,8 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
             for (int tq = m_lo / a.G; tq * a.G < m_hi; ++tq) {
                 const int r0 = max(m_lo, tq * a.G), r1 = min(m_hi, (tq + 1) * a.G);
                 const int64_t row = ((int64_t)b * a.Q + tq) * a.Hq + kvh * a.G + r0 % a.G;
-                bulk_g2s(sm.raw + (r0 - m_lo) * row_bytes, q + row * row_bytes, (uint32_t)(r1 - r0) * row_bytes, &mbar_q);
+                bulk_g2s(q_stage + (r0 - m_lo) * row_bytes, q + row * row_bytes, (uint32_t)(r1 - r0) * row_bytes,
+                         &mbar_q);
             }
         }
     }
@@ -281,87 +305,191 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
     }
 
     // ---------------- B. attention units ----------------
-    if (!pt_stored) store_pt();
-    uint32_t gp = 0;          // pages staged by this CTA so far (sets the stages' phase parity)
-    bool copies_ok = true;    // false after a copy that did not land: stage nothing more
-    for (int u = u0; u < n_units; u += nC) {
-        const int s = u % a.S, rg = (u / a.S) % a.n_rg, kvh = (u / (a.S * a.n_rg)) % a.Hkv;
-        const int b = u / (a.S * a.n_rg * a.Hkv);
-        const bool first = u == u0;
-        const int ctx = clamp_ctx(first ? ctx_u0 : a.ctx_len[b], a.Q, a.max_pages, nullptr);
-        const int n_pages = (ctx + kPage - 1) / kPage;
-        const bool pt_cached = n_pages <= kPtCache;
-        const AttendLane L = attend_lane(rg, R, a.row_warps, M, a.G);
-        uint32_t qa[8][4];
-        if (!first || !q_stageable) {
-            // later units: q and the page table from global memory, before the wait
-            if (RS) load_qa_bf16<false>(qa, a.q_bf16, L, b, kvh, a.Q, a.Hq, a.G);
-            else load_qa_f32_e4m3(qa, a.q_f32, L, b, kvh, a.Q, a.Hq, a.G);
-        } else {
-            // the first unit's q rows were staged at the start: unpack them before the wait
-            if (!mbar_wait_bounded(&mbar_q, 0)) flag_status(a.status, SMX_DEV_TIMEOUT);
-            pack_staged_q<RS>(sm.raw, min(M - rg * R, R));
-            load_qa_packed(qa, sm.raw, rg * R, L);
-        }
-        if (!first && pt_cached) {
-            __syncthreads();   // the previous unit is done with pt_s
-            for (int base = 0; base < n_pages; base += kPtPerThread * kStepWarps * 32) {
-                int32_t v[kPtPerThread];
-#pragma unroll
-                for (int k = 0; k < kPtPerThread; ++k) {
-                    const int i = base + threadIdx.x + k * kStepWarps * 32;
-                    v[k] = i < n_pages ? a.page_table[(int64_t)b * a.max_pages + i] : 0;
-                }
-#pragma unroll
-                for (int k = 0; k < kPtPerThread; ++k) {
-                    const int i = base + threadIdx.x + k * kStepWarps * 32;
-                    if (i < n_pages) pt_s[i] = v[k];
+    if constexpr (TC) {
+        if (!pt_stored) store_pt();
+        // tensor memory for this CTA's units (S at column 0, O at 128); the tiles need a
+        // 1024-byte-aligned base (checked; a CTA without it stages nothing and flags a timeout)
+        const bool has_units = u0 < n_units;
+        const bool smem_ok = (smem_u32(smem) & 1023u) == 0;
+        if (has_units && !smem_ok && threadIdx.x == 0) flag_status(a.status, SMX_DEV_TIMEOUT);
+        if (has_units && warp == 0) tmem_alloc(&tmem_slot, kTcCols);
+        tc_fence_before_sync();
+        __syncthreads();
+        tc_fence_after_sync();
+        const uint32_t tmem = tmem_slot;
+        uint32_t gp = 0;          // pages staged by this CTA so far (sets the stages' phase parity)
+        uint32_t mma_ph = 0;      // MMA completions seen so far
+        bool copies_ok = smem_ok; // false after a copy or MMA that did not finish: stage nothing more
+        for (int u = u0; u < n_units; u += nC) {
+            const int s = u % a.S, rg = (u / a.S) % a.n_rg, kvh = (u / (a.S * a.n_rg)) % a.Hkv;
+            const int b = u / (a.S * a.n_rg * a.Hkv);
+            const bool first = u == u0;
+            const int ctx = clamp_ctx(first ? ctx_u0 : a.ctx_len[b], a.Q, a.max_pages, nullptr);
+            const int n_pages = (ctx + kPage - 1) / kPage;
+            const bool pt_cached = n_pages <= kPtCache;
+            const int m_lo = rg * R, rows = min(M - m_lo, R);
+            TcLane L;
+            L.r = threadIdx.x & 127;
+            L.h = threadIdx.x >> 7;
+            L.valid = L.r < rows;
+            L.pos = ctx - a.Q + (L.valid ? (m_lo + L.r) / a.G : 0);
+            // the q tile, before the wait: the first unit's rows were staged at the start
+            if (first && q_stageable) {
+                if (!mbar_wait_bounded(&mbar_q, 0)) flag_status(a.status, SMX_DEV_TIMEOUT);
+                pack_q_tile_tc<RS>(smem + kTcV, rows, smem + kTcQ);
+            } else {
+                pack_q_tile_tc_global<RS>(RS ? (const void*)a.q_bf16 : (const void*)a.q_f32, b, kvh, m_lo, rows, a.Q, a.Hq,
+                                          a.G, smem + kTcQ);
+            }
+            if (!first && pt_cached) {
+                __syncthreads();   // the previous unit is done with pt_s
+                for (int base = 0; base < n_pages; base += kPtPerThread * kStepWarps * 32) {
+                    int32_t v[kPtPerThread];
+    #pragma unroll
+                    for (int k = 0; k < kPtPerThread; ++k) {
+                        const int i = base + threadIdx.x + k * kStepWarps * 32;
+                        v[k] = i < n_pages ? a.page_table[(int64_t)b * a.max_pages + i] : 0;
+                    }
+    #pragma unroll
+                    for (int k = 0; k < kPtPerThread; ++k) {
+                        const int i = base + threadIdx.x + k * kStepWarps * 32;
+                        if (i < n_pages) pt_s[i] = v[k];
+                    }
                 }
             }
-        }
-        if (threadIdx.x == 0 && !wait_geq_bounded(&a.row_cnt[kCounterStride * b], (uint32_t)C)) flag_status(a.status, SMX_DEV_TIMEOUT);
-        __syncthreads();
-        load_keys<true>(keys, a.scores + (int64_t)b * a.max_pages, n_pages);
-        __syncthreads();   // keys in place; the staged q rows read (the page stages are free)
-        const int k_eff = block_select(keys, n_pages, a.topk, sel_all, selsm);
-        const int lo = (int)(((int64_t)s * k_eff) / a.S), hi = (int)(((int64_t)(s + 1) * k_eff) / a.S);
-        auto resolve = [&](int i) {   // entry i of this partition: logical and physical page
-            const int p = sel_all[lo + i];
-            const int64_t v = pt_cached ? pt_s[p] : a.page_table[(int64_t)b * a.max_pages + p];
-            int ph = -1;
-            if (v >= 0 && v < a.n_pool) ph = (int)v;
-            else flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
-            sel[i] = p;
-            selph[i] = ph;
-            return ph;
-        };
-        // the first two pages' copies go out first; the row's new K/V rows (other CTAs' writes,
-        // acquired above) are ordered before them
-        if (threadIdx.x == 0 && copies_ok) {
-            fence_proxy_async_global();
-            fence_proxy_async_smem();   // the staged q rows were read from the page stages
-            for (int i = 0; i < 2 && i < hi - lo; ++i)
-                attend_issue(sm, i, sel_all[lo + i], resolve(i), gp, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes);
-        }
-        for (int i = 2 + threadIdx.x; i < hi - lo; i += blockDim.x) resolve(i);
-        if (kvh == 0 && rg == 0 && s == 0) {
-            for (int i = threadIdx.x; i < a.topk; i += blockDim.x)
-                a.topk_out[(int64_t)b * a.topk + i] = i < k_eff ? sel_all[i] : -1;
-            if (threadIdx.x == 0) a.count_out[b] = k_eff;
-        }
-        __syncthreads();
+            if (threadIdx.x == 0 && !wait_geq_bounded(&a.row_cnt[kCounterStride * b], (uint32_t)C)) flag_status(a.status, SMX_DEV_TIMEOUT);
+            __syncthreads();   // the row is scored; the staged q rows are packed (the V and P tiles are free)
+            load_keys<true>(keys, a.scores + (int64_t)b * a.max_pages, n_pages);
+            __syncthreads();
+            const int k_eff = block_select(keys, n_pages, a.topk, sel_all, selsm);
+            const int lo = (int)(((int64_t)s * k_eff) / a.S), hi = (int)(((int64_t)(s + 1) * k_eff) / a.S);
+            auto resolve = [&](int i) {   // entry i of this partition: logical and physical page
+                const int p = sel_all[lo + i];
+                const int64_t v = pt_cached ? pt_s[p] : a.page_table[(int64_t)b * a.max_pages + p];
+                int ph = -1;
+                if (v >= 0 && v < a.n_pool) ph = (int)v;
+                else flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                sel[i] = p;
+                selph[i] = ph;
+                return ph;
+            };
+            // the first two pages' copies go out first; the row's new K/V rows (other CTAs' writes,
+            // acquired above) are ordered before them
+            if (threadIdx.x == 0 && copies_ok) {
+                fence_proxy_async_global();
+                fence_proxy_async_smem();
+                for (int i = 0; i < 2 && i < hi - lo; ++i)
+                    attend_issue(sm, i, sel_all[lo + i], resolve(i), gp, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes);
+            }
+            for (int i = 2 + threadIdx.x; i < hi - lo; i += blockDim.x) resolve(i);
+            if (kvh == 0 && rg == 0 && s == 0) {
+                for (int i = threadIdx.x; i < a.topk; i += blockDim.x)
+                    a.topk_out[(int64_t)b * a.topk + i] = i < k_eff ? sel_all[i] : -1;
+                if (threadIdx.x == 0) a.count_out[b] = k_eff;
+            }
+            __syncthreads();
 
-        float o[16][4];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-        float mrow0 = -INFINITY, mrow1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-        const int pos0 = ctx - a.Q + L.t0, pos1 = ctx - a.Q + L.t1;
-        if (copies_ok)
-            copies_ok = attend_pages<RS>(sm, sel, selph, hi - lo, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes, ctx,
-                                         qa, L, pos0, pos1, gp, o, mrow0, mrow1, l0, l1, a.status, true);
-        finish_partials(sm, L, o, mrow0, mrow1, l0, l1, a.part_o, a.part_m, a.part_l, b, s, kvh, a.S, a.Q, a.Hq, a.G);
+            float m_run = -INFINITY, l = 0.0f;
+            const bool run = copies_ok && hi > lo;
+            if (run)
+                copies_ok = attend_pages_tc<RS>(smem, sm, sel, selph, hi - lo, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes,
+                                                ctx, tmem, &mbar_mma, mma_ph, L, xch_tc, gp, m_run, l, a.status);
+            finish_partials_tc(L, tmem, run, m_run, l, xch_tc, a.part_o, a.part_m, a.part_l, b, s, kvh, a.S, a.Q, a.Hq, a.G,
+                               m_lo);
+            __syncthreads();
+            if (threadIdx.x == 0) red_release_add(&a.grp_cnt[kCounterStride * ((b * a.Hkv + kvh) * a.n_rg + rg)], 1u);
+        }
+        tc_fence_before_sync();
         __syncthreads();
-        if (threadIdx.x == 0) red_release_add(&a.grp_cnt[kCounterStride * ((b * a.Hkv + kvh) * a.n_rg + rg)], 1u);
+        if (has_units && warp == 0) {
+            tc_fence_after_sync();
+            tmem_dealloc(tmem, kTcCols);
+        }
+
+    } else {
+        if (!pt_stored) store_pt();
+        uint32_t gp = 0;          // pages staged by this CTA so far (sets the stages' phase parity)
+        bool copies_ok = true;    // false after a copy that did not land: stage nothing more
+        for (int u = u0; u < n_units; u += nC) {
+            const int s = u % a.S, rg = (u / a.S) % a.n_rg, kvh = (u / (a.S * a.n_rg)) % a.Hkv;
+            const int b = u / (a.S * a.n_rg * a.Hkv);
+            const bool first = u == u0;
+            const int ctx = clamp_ctx(first ? ctx_u0 : a.ctx_len[b], a.Q, a.max_pages, nullptr);
+            const int n_pages = (ctx + kPage - 1) / kPage;
+            const bool pt_cached = n_pages <= kPtCache;
+            const AttendLane L = attend_lane(rg, R, a.row_warps, M, a.G);
+            uint32_t qa[8][4];
+            if (!first || !q_stageable) {
+                // later units: q and the page table from global memory, before the wait
+                if (RS) load_qa_bf16<false>(qa, a.q_bf16, L, b, kvh, a.Q, a.Hq, a.G);
+                else load_qa_f32_e4m3(qa, a.q_f32, L, b, kvh, a.Q, a.Hq, a.G);
+            } else {
+                // the first unit's q rows were staged at the start: unpack them before the wait
+                if (!mbar_wait_bounded(&mbar_q, 0)) flag_status(a.status, SMX_DEV_TIMEOUT);
+                pack_staged_q<RS>(q_stage, min(M - rg * R, R));
+                load_qa_packed(qa, q_stage, rg * R, L);
+            }
+            if (!first && pt_cached) {
+                __syncthreads();   // the previous unit is done with pt_s
+                for (int base = 0; base < n_pages; base += kPtPerThread * kStepWarps * 32) {
+                    int32_t v[kPtPerThread];
+    #pragma unroll
+                    for (int k = 0; k < kPtPerThread; ++k) {
+                        const int i = base + threadIdx.x + k * kStepWarps * 32;
+                        v[k] = i < n_pages ? a.page_table[(int64_t)b * a.max_pages + i] : 0;
+                    }
+    #pragma unroll
+                    for (int k = 0; k < kPtPerThread; ++k) {
+                        const int i = base + threadIdx.x + k * kStepWarps * 32;
+                        if (i < n_pages) pt_s[i] = v[k];
+                    }
+                }
+            }
+            if (threadIdx.x == 0 && !wait_geq_bounded(&a.row_cnt[kCounterStride * b], (uint32_t)C)) flag_status(a.status, SMX_DEV_TIMEOUT);
+            __syncthreads();
+            load_keys<true>(keys, a.scores + (int64_t)b * a.max_pages, n_pages);
+            __syncthreads();   // keys in place; the staged q rows read (the page stages are free)
+            const int k_eff = block_select(keys, n_pages, a.topk, sel_all, selsm);
+            const int lo = (int)(((int64_t)s * k_eff) / a.S), hi = (int)(((int64_t)(s + 1) * k_eff) / a.S);
+            auto resolve = [&](int i) {   // entry i of this partition: logical and physical page
+                const int p = sel_all[lo + i];
+                const int64_t v = pt_cached ? pt_s[p] : a.page_table[(int64_t)b * a.max_pages + p];
+                int ph = -1;
+                if (v >= 0 && v < a.n_pool) ph = (int)v;
+                else flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                sel[i] = p;
+                selph[i] = ph;
+                return ph;
+            };
+            // the first two pages' copies go out first; the row's new K/V rows (other CTAs' writes,
+            // acquired above) are ordered before them
+            if (threadIdx.x == 0 && copies_ok) {
+                fence_proxy_async_global();
+                fence_proxy_async_smem();   // the staged q rows were read from the page stages
+                for (int i = 0; i < 2 && i < hi - lo; ++i)
+                    attend_issue(sm, i, sel_all[lo + i], resolve(i), gp, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes);
+            }
+            for (int i = 2 + threadIdx.x; i < hi - lo; i += blockDim.x) resolve(i);
+            if (kvh == 0 && rg == 0 && s == 0) {
+                for (int i = threadIdx.x; i < a.topk; i += blockDim.x)
+                    a.topk_out[(int64_t)b * a.topk + i] = i < k_eff ? sel_all[i] : -1;
+                if (threadIdx.x == 0) a.count_out[b] = k_eff;
+            }
+            __syncthreads();
+
+            float o[16][4];
+    #pragma unroll
+            for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+            float mrow0 = -INFINITY, mrow1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+            const int pos0 = ctx - a.Q + L.t0, pos1 = ctx - a.Q + L.t1;
+            if (copies_ok)
+                copies_ok = attend_pages<RS>(sm, sel, selph, hi - lo, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes, ctx,
+                                             qa, L, pos0, pos1, gp, o, mrow0, mrow1, l0, l1, a.status, true);
+            finish_partials(sm, L, o, mrow0, mrow1, l0, l1, a.part_o, a.part_m, a.part_l, b, s, kvh, a.S, a.Q, a.Hq, a.G);
+            __syncthreads();
+            if (threadIdx.x == 0) red_release_add(&a.grp_cnt[kCounterStride * ((b * a.Hkv + kvh) * a.n_rg + rg)], 1u);
+        }
+
     }
 
     // ---------------- C. merge: slice s of each unit's group ----------------
@@ -396,21 +524,37 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
 }
 
 // ---- host side -------------------------------------------------------------------------------------
-StepGeom step_geom(const smx_shape_t& s) {
+// Attention rows per unit: 128 on the tensor-core path, 16 x row warps (<= 64) on mma.sync.
+static int unit_rows(const smx_shape_t& s, bool tc) {
+    const int M = (s.Hq / s.Hkv) * s.Q;
+    return tc ? kTcRows : 16 * min(kAttnMaxWarps / 2, (M + 15) / 16);
+}
+
+StepGeom step_geom(const smx_shape_t& s) { return step_geom(s, false); }
+
+StepGeom step_geom(const smx_shape_t& s, bool tc) {
     StepGeom g;
     const int M = (s.Hq / s.Hkv) * s.Q;
-    g.row_warps = min(kAttnMaxWarps / 2, (M + 15) / 16);
-    g.rows_per_cta = 16 * g.row_warps;
+    g.rows_per_cta = unit_rows(s, tc);
+    g.row_warps = g.rows_per_cta / 16;
     g.n_rg = (M + g.rows_per_cta - 1) / g.rows_per_cta;
     g.page_bytes = s.kv_format == SMX_KV_E4M3_ROWSCALE ? kRsPageBytes : kMxPageBytes;
-    g.smem = attend_smem_bytes(g.page_bytes) + 12 * (size_t)s.topk;
-    g.n_counters = kCounterStride * ((size_t)s.B + (size_t)s.B * s.Hkv * g.n_rg + 1);
+    g.smem = tc ? attend_tc_smem_bytes(g.page_bytes) + 8 * (size_t)s.topk
+                : attend_smem_bytes(g.page_bytes) + 16 * (size_t)s.topk;
+    // counters for the larger (mma.sync) group count, so the workspace does not depend on the path
+    const int rg64 = (M + unit_rows(s, false) - 1) / unit_rows(s, false);
+    g.n_counters = kCounterStride * ((size_t)s.B + (size_t)s.B * s.Hkv * rg64 + 1);
     return g;
 }
 
-template <bool RS, int NT>
+template <bool RS, int NT, bool TC>
 static const void* step_fn() {
-    return reinterpret_cast<const void*>(decode_step_kernel<RS, NT>);
+    return reinterpret_cast<const void*>(decode_step_kernel<RS, NT, TC>);
+}
+
+static const void* step_fn(bool rs, bool nt2, bool tc) {
+    if (tc) return rs ? (nt2 ? step_fn<true, 2, true>() : step_fn<true, 1, true>()) : (nt2 ? step_fn<false, 2, true>() : step_fn<false, 1, true>());
+    return rs ? (nt2 ? step_fn<true, 2, false>() : step_fn<true, 1, false>()) : (nt2 ? step_fn<false, 2, false>() : step_fn<false, 1, false>());
 }
 
 // Resident CTAs of the step kernel on the current device (cached per device, kernel and size).
@@ -435,11 +579,32 @@ static int step_max_ctas(const void* fn, size_t smem) {
     return n;
 }
 
+// The tensor-core attention when the 64-row mma.sync units would need more than one wave of
+// CTAs: per query row and page it does about 1.2x the work per SM of mma.sync (measured), but
+// with half as many units; with one wave, twice the CTAs in flight win (the step is latency-bound).
+static bool use_tc(const smx_shape_t& s, int max_ctas) {
+    const int M = (s.Hq / s.Hkv) * s.Q;
+    if (M <= 64 || max_ctas < 1) return false;
+    const int64_t units64 = (int64_t)s.B * s.Hkv * ((M + 63) / 64) * s.num_splits;
+    return units64 > max_ctas;
+}
+
+bool decode_step_uses_tc(const smx_shape_t& s) {
+    const StepGeom geo = step_geom(s, true);
+    const void* fn = step_fn(s.kv_format == SMX_KV_E4M3_ROWSCALE, s.Q > 8, true);
+    if (ensure_smem_attr(fn, (int)geo.smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return use_tc(s, step_max_ctas(fn, geo.smem));
+}
+
 cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStream_t st) {
-    const StepGeom geo = step_geom(s);
     const bool rs = s.kv_format == SMX_KV_E4M3_ROWSCALE;
     const bool nt2 = s.Q > 8;
-    const void* fn = rs ? (nt2 ? step_fn<true, 2>() : step_fn<true, 1>()) : (nt2 ? step_fn<false, 2>() : step_fn<false, 1>());
+    const bool tc = decode_step_uses_tc(s);
+    const StepGeom geo = step_geom(s, tc);
+    const void* fn = step_fn(rs, nt2, tc);
     cudaError_t e = ensure_smem_attr(fn, (int)geo.smem);
     if (e != cudaSuccess) return e;
     const int max_ctas = step_max_ctas(fn, geo.smem);
@@ -480,8 +645,12 @@ cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStrea
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (rs) return nt2 ? cudaLaunchKernelEx(&cfg, decode_step_kernel<true, 2>, a) : cudaLaunchKernelEx(&cfg, decode_step_kernel<true, 1>, a);
-    return nt2 ? cudaLaunchKernelEx(&cfg, decode_step_kernel<false, 2>, a) : cudaLaunchKernelEx(&cfg, decode_step_kernel<false, 1>, a);
+    if (tc) {
+        if (rs) return nt2 ? cudaLaunchKernelEx(&cfg, decode_step_kernel<true, 2, true>, a) : cudaLaunchKernelEx(&cfg, decode_step_kernel<true, 1, true>, a);
+        return nt2 ? cudaLaunchKernelEx(&cfg, decode_step_kernel<false, 2, true>, a) : cudaLaunchKernelEx(&cfg, decode_step_kernel<false, 1, true>, a);
+    }
+    if (rs) return nt2 ? cudaLaunchKernelEx(&cfg, decode_step_kernel<true, 2, false>, a) : cudaLaunchKernelEx(&cfg, decode_step_kernel<true, 1, false>, a);
+    return nt2 ? cudaLaunchKernelEx(&cfg, decode_step_kernel<false, 2, false>, a) : cudaLaunchKernelEx(&cfg, decode_step_kernel<false, 1, false>, a);
 }
 
 }  // namespace smx

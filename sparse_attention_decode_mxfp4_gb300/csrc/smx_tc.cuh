@@ -1,0 +1,122 @@
+// smx_tc.cuh -- fifth-generation tensor cores (tcgen05): tensor memory, shared-memory matrix
+// descriptors and the bf16 MMA the attention uses.
+//
+// Operand tiles are bf16 [rows][128] in shared memory, K-major with the 128-byte swizzle: two
+// K blocks of 64 elements, each rows x 128 B, in 8-row atoms of 1024 B; the 16-byte chunk c of
+// row r sits at chunk c ^ (r % 8). One MMA step (K = 16, 32 bytes of every row) starts 32 * (k % 4)
+// bytes into K block k / 4. The accumulator D (fp32, 128 rows x N columns) lives in tensor memory:
+// row i in lane i, column j in column j of the allocation.
+#pragma once
+
+#include <stdint.h>
+
+#include "smx_device.cuh"
+
+namespace smx {
+
+// Byte offset of element (r, k) of a bf16 [rows][128] tile in the layout above.
+__host__ __device__ __forceinline__ uint32_t sw128_off(int r, int k, int rows) {
+    const int kb = k >> 6, kk = k & 63;
+    return (uint32_t)(kb * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + ((((kk >> 3) ^ (r & 7)) & 7) << 4) + (kk & 7) * 2);
+}
+
+// Byte offset of the 16-byte chunk holding elements 8c .. 8c + 7 of row r.
+__host__ __device__ __forceinline__ uint32_t sw128_chunk(int r, int c, int rows) {
+    return (uint32_t)((c >> 3) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);   // start address
+    d |= (uint64_t)1 << 16;                     // leading byte offset (unused when swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;           // stride byte offset between 8-row atoms
+    d |= (uint64_t)1 << 46;                     // descriptor version
+    d |= (uint64_t)2 << 61;                     // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: dense kind::f16, bf16 A and B (both K-major), fp32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Allocate ncols (a power of two >= 32) tensor-memory columns; one whole warp calls it and the
+// base address lands in *slot (shared memory).
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+// Free the columns (one whole warp; no MMA or load may still be using them).
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[128 x N] (+)= A[128 x 128] . B[N x 128]^T over the 8 K steps of the tiles at a_s, b_s (one
+// thread), then arrive on bar when the MMAs are done.
+__device__ __forceinline__ void tc_mma_tile(uint32_t d_tmem, uint32_t a_s, uint32_t b_s, int a_rows, int b_rows,
+                                            uint32_t idesc, bool accumulate, uint64_t* bar) {
+    // bar == nullptr: no commit (a later tc_mma_tile's commit covers these MMAs too)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint64_t ad = sw128_desc(a_s + (k >> 2) * a_rows * 128 + (k & 3) * 32);
+        const uint64_t bd = sw128_desc(b_s + (k >> 2) * b_rows * 128 + (k & 3) * 32);
+        const uint32_t acc = (accumulate || k > 0) ? 1u : 0u;
+        asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+                     " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem), "l"(ad), "l"(bd),
+                     "r"(idesc), "r"(acc)
+                     : "memory");
+    }
+    if (bar != nullptr)
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                     : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's lane (the warp's 32 lanes) from taddr.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 consecutive fp32 columns of this thread's lane from taddr (waits for the load).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Store 16 fp32 columns of this thread's lane at taddr (waits for the store).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+        "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+        "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+}  // namespace smx

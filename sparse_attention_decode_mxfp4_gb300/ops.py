@@ -27,7 +27,7 @@ DEV_BAD_PAGE_ID, DEV_BAD_CTX, DEV_BAD_TOPK = 1, 2, 4
 SYMBOLS = ("smx_workspace_bytes", "smx_kv_insert", "smx_kv_prefill", "smx_pack_q_e4m3",
            "smx_index_score", "smx_index_score_topk", "smx_sparse_attn_split", "smx_sparse_attn_merge",
            "smx_decode_step", "smx_status_string", "smx_decode_step_launches",
-           "smx_suggest_num_splits", "smx_decode_step_noalloc")
+           "smx_suggest_num_splits", "smx_decode_step_noalloc", "smx_decode_step_tensor_cores")
 
 
 class SmxError(RuntimeError):
@@ -97,6 +97,7 @@ def lib() -> ctypes.CDLL:
             "smx_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "smx_decode_step_launches": (ctypes.c_int, [S]),
             "smx_suggest_num_splits": (ctypes.c_int, [S]),
+            "smx_decode_step_tensor_cores": (ctypes.c_int, [S]),
             "smx_decode_step_noalloc": (ctypes.c_int, [S] + [P] * 15 + [ST]),
         }
         for name, (res, args) in sigs.items():
@@ -142,6 +143,15 @@ def workspace_bytes(shape: Shape) -> int:
 def decode_step_launches(shape: Shape) -> int:
     cs = shape.c()
     return int(lib().smx_decode_step_launches(ctypes.byref(cs)))
+
+
+def decode_step_tensor_cores(shape: Shape) -> bool:
+    """Whether the fused step runs its attention on tcgen05 (128-row tiles) for `shape` here."""
+    cs = shape.c()
+    rc = int(lib().smx_decode_step_tensor_cores(ctypes.byref(cs)))
+    if rc < 0:
+        raise SmxError(f"smx_decode_step_tensor_cores: {lib().smx_status_string(rc).decode()} ({rc})")
+    return rc == 1
 
 
 def suggest_num_splits(shape: Shape) -> int:

@@ -86,7 +86,7 @@ def test_status_strings(L):
 
 
 def test_split_suggestion_refuses_bad_shapes(L):
-    bad = good_shape()
-    bad.Hq = 3   # not a multiple of Hkv
+    bad = good_shape(Hq=12, Hkv=5)   # Hq not a multiple of Hkv
     assert L.smx_suggest_num_splits(ctypes.byref(bad.c())) == 0
     assert L.smx_suggest_num_splits(None) == 0
+    assert L.smx_decode_step_tensor_cores(ctypes.byref(bad.c())) < 0

@@ -75,3 +75,27 @@ def test_fp8kv_ragged_small():
     w = wl.Workload("fp8kv_small", B=3, Q=8, Hq=16, Hkv=1, max_ctx=6000, topk=6, num_splits=4,
                     kv_format=wl.KV_E4M3_ROWSCALE, seed=99, ragged=True, big_row_frac=0.01)
     C.full_step_parity(w)
+
+
+def _uses_tc(w):
+    return ops.decode_step_tensor_cores(ops.Shape.of(w))
+
+
+@pytest.mark.parametrize("kv_format", [wl.KV_MXFP4, wl.KV_E4M3_ROWSCALE])
+def test_tensor_core_attention_path(kv_format):
+    # 8 rows x 2 groups of 64 query rows x 12 partitions = 192 mma.sync units: more than one wave,
+    # so the step runs its attention on the tensor cores (128-row units)
+    kw = dict(kv_format=kv_format)
+    if kv_format == wl.KV_E4M3_ROWSCALE:
+        kw["big_row_frac"] = 0.01
+    w = wl.Workload("tc_path", B=8, Q=8, Hq=16, Hkv=1, max_ctx=3000, topk=12, num_splits=12, seed=77, ragged=True, **kw)
+    assert _uses_tc(w)
+    C.full_step_parity(w)
+
+
+def test_configs_take_the_mma_path():
+    # the benchmark workloads at the suggested partition counts fit one wave of 64-row units
+    for c in (2, 3, 4):
+        w = wl.config(c)
+        shape = ops.Shape.of(w, ops.suggest_num_splits(ops.Shape.of(w, 1)))
+        assert not ops.decode_step_tensor_cores(shape)
