@@ -71,6 +71,13 @@ __device__ __forceinline__ int floor_log2_pos(float a) {
 // 2^k as fp32 for k in [-126, 127].
 __device__ __forceinline__ float exp2i_normal(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
 
+// x * 2^k for any k a float exponent difference can take (two exact power-of-two steps).
+__device__ __forceinline__ float mul_exp2(float x, int k) {
+    const int k1 = max(-126, min(127, k / 2));
+    const int k2 = max(-126, min(127, k - k1));
+    return x * exp2i_normal(k1) * exp2i_normal(k2);
+}
+
 // q packing rule: NaN -> 0x7F; otherwise clamp to [-448, 448], round to nearest even; the sign
 // bit is the input's sign.
 __device__ __forceinline__ uint32_t pack_q4(float4 x) {

@@ -25,13 +25,6 @@ constexpr int kIdxWarps = 8;
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h16) { return __uint_as_float(h16 << 16); }
 
-// x * 2^k for any k a float exponent difference can take (two exact power-of-two steps).
-__device__ __forceinline__ float mul_exp2(float x, int k) {
-    const int k1 = max(-126, min(127, k / 2));
-    const int k2 = max(-126, min(127, k - k1));
-    return x * exp2i_normal(k1) * exp2i_normal(k2);
-}
-
 // One lane's share of one 16-token tile: 16 B of nibbles of token rows g and g+8 and the rows'
 // scale words. Pages are read through L2 (a CTA that inserted rows must see its own writes).
 struct TileFrag {

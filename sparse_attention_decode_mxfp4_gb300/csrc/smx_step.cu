@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
         };
         load_page(fa, pq, true);
         if (!pt_stored) store_pt();
-        int64_t kv_phys0 = -1;   // page of this warp's first K/V row (used after the scoring)
+        int64_t kv_phys0 = -1;   // page of this warp's first K/V row
         if (kv_r0 < kv_rows && first_new + kv_r0 / (2 * a.Hkv) >= 0)
             kv_phys0 = a.page_table[(int64_t)b * a.max_pages + (first_new + kv_r0 / (2 * a.Hkv)) / kPage];
         if (owner) {
@@ -245,6 +245,28 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
             if (pq >= own_lo && pq < own_hi) load_page(fa, pq, false);
         }
 
+        // this warp's new K/V rows (read only by the attention phase, after the row's counter), while
+        // the index tiles are in flight
+        for (int r = kv_r0; r < kv_rows; r += C * kStepWarps) {
+            const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);
+            const int pos = first_new + tq;
+            if (pos < 0) continue;
+            const float4 x = r == kv_r0 ? kv_x : *kv_row_src(r);
+            const int64_t phys = r == kv_r0 ? kv_phys0 : (int64_t)a.page_table[(int64_t)b * a.max_pages + pos / kPage];
+            if (phys < 0 || phys >= a.n_pool) {
+                if (lane == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                continue;
+            }
+            const int h = kind % a.Hkv, slot = pos % kPage;
+            uint8_t* pool = kind < a.Hkv ? a.k_pool : a.v_pool;
+            if (RS) {
+                uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kRsPageBytes;
+                quant_row_e4m3rs_warp(x, page + slot * 128, reinterpret_cast<float*>(page + kRsScaleOff) + slot, lane);
+            } else {
+                uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kMxPageBytes;
+                quant_row_mxfp4_warp(x, page + slot * 64, page + kMxScaleOff + slot * 4, lane);
+            }
+        }
         uint32_t qf[NT][16];
         int sig_c[NT][2];
         setup_index_query<NT>(qraw, a.Q, qh, sig, qf, sig_c);
@@ -279,27 +301,6 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
             for (int k = 0; k < 4; ++k) fa[k] = fb[k];
         }
 
-        // this warp's new K/V rows (read only by the attention phase, after the row's counter)
-        for (int r = kv_r0; r < kv_rows; r += C * kStepWarps) {
-            const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);
-            const int pos = first_new + tq;
-            if (pos < 0) continue;
-            const float4 x = r == kv_r0 ? kv_x : *kv_row_src(r);
-            const int64_t phys = r == kv_r0 ? kv_phys0 : (int64_t)a.page_table[(int64_t)b * a.max_pages + pos / kPage];
-            if (phys < 0 || phys >= a.n_pool) {
-                if (lane == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
-                continue;
-            }
-            const int h = kind % a.Hkv, slot = pos % kPage;
-            uint8_t* pool = kind < a.Hkv ? a.k_pool : a.v_pool;
-            if (RS) {
-                uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kRsPageBytes;
-                quant_row_e4m3rs_warp(x, page + slot * 128, reinterpret_cast<float*>(page + kRsScaleOff) + slot, lane);
-            } else {
-                uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kMxPageBytes;
-                quant_row_mxfp4_warp(x, page + slot * 64, page + kMxScaleOff + slot * 4, lane);
-            }
-        }
         __syncthreads();
         if (threadIdx.x == 0) red_release_add(&a.row_cnt[kCounterStride * b], 1u);
     }

@@ -77,6 +77,12 @@ __device__ __forceinline__ void tc_mma_tile(uint32_t d_tmem, uint32_t a_s, uint3
                      : "memory");
 }
 
+// Arrive on bar once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
 // 32 consecutive fp32 columns of this thread's lane (the warp's 32 lanes) from taddr.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];

@@ -94,9 +94,13 @@ def test_insert_bit_exact(fmt, Hkv):
         assert np.array_equal(g[key].cpu().numpy(), r), key
 
 
-@pytest.mark.parametrize("Q,Hq,topk", [(1, 8, 4), (8, 16, 5), (16, 8, 7), (3, 4, 40)])
-def test_index_scores_and_topk(Q, Hq, topk):
-    w = small(Q=Q, Hq=Hq, topk=topk, max_ctx=5000)
+@pytest.mark.parametrize("Q,Hq,topk,B,max_ctx", [(1, 8, 4, 3, 5000), (8, 16, 5, 3, 5000), (16, 8, 7, 3, 5000),
+                                                (3, 4, 40, 3, 5000),
+                                                # rows long enough for the tensor-core scorer (>= 6 pages
+                                                # per CTA), with 8 and 16 query slots
+                                                (8, 16, 16, 3, 131072), (13, 16, 9, 2, 196608)])
+def test_index_scores_and_topk(Q, Hq, topk, B, max_ctx):
+    w = small(Q=Q, Hq=Hq, topk=topk, max_ctx=max_ctx, B=B)
     data = wl.generate(w)
     pools = H.oracle_pools(w, data, include_new=False)
     sh = oracle.shape_of(w)
