@@ -302,6 +302,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return false;
 }
 
+// Bounded wait for a pipeline hand-off: polls without sleeping (a sleep would add its wake-up
+// latency to every stage of a pipeline), giving up after about two seconds of global time.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 1023u) == 0) {
+            uint64_t t;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+            if (i == 0) t0 = t;
+            else if (t - t0 > 2000000000ull) return false;
+        }
+    }
+}
+
 // Copy `bytes` (multiple of 16, both addresses 16-byte aligned) global -> shared, completing on bar.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(

@@ -31,28 +31,40 @@ struct IndexArgs {
 
 constexpr int kIdxMaxPpc = 64;   // page-table entries of one CTA staged in shared memory
 constexpr int kIdxTcMinPages = 6;  // pages per CTA from which the tensor-core scorer is faster
-// dynamic shared memory: two page tiles and the query pieces, plus slack to align them to 1 KB
-constexpr int kIdxSmemBytes = 2 * kScTileBytes + kScQueryBytes + 1024;
+constexpr int kIdxRawStages = 4, kIdxTileStages = 3, kIdxAccStages = 3;
+// dynamic shared memory: the tile stages, the query pieces and the raw stages, plus slack to align
+// the tiles to 1 KB
+constexpr int kIdxSmemBytes = kIdxTileStages * kScTileBytes + kScQueryBytes + kIdxRawStages * kMxPageBytes + 1024;
 
-// Grid (CTAs per row, B), 256 threads. The CTA scores its range of the row's pages two at a time:
-// all threads repack the pair's nibbles into the two A tiles (the next two pairs' loads already in
-// flight) and warps 0-3 / 4-7 store the first / second page's scale factors, one thread issues the
-// MMAs, warps 0-3 and 4-7 take the epilogue of the first and the second page (one token per
-// thread), and a warp maximum per page goes through shared memory to threads 0 and 1, which write
-// the page scores after the next pair's barrier. One barrier per pair.
+// Grid (CTAs per row, B), 320 threads (ten warps), two CTAs per SM: the CTA scores its range of
+// the row's pages with the pipelined tensor-core scorer (sc_score_pages).
+constexpr int kIdxTcThreads = 320;
 template <int NQ>
-__global__ void __launch_bounds__(kIdxWarps * 32, 2) index_score_kernel(IndexArgs a) {
+__global__ void __launch_bounds__(kIdxTcThreads, 2) index_score_kernel(IndexArgs a) {
     extern __shared__ __align__(1024) uint8_t dsm[];
     __shared__ int64_t phys_s[kIdxMaxPpc];
     __shared__ float gmax[8][4];
-    __shared__ float red[2][kIdxWarps];
-    __shared__ __align__(8) uint64_t mbar;
+    __shared__ float red[4 * kScMaxAccStages];
+    __shared__ __align__(8) uint64_t bars[2 * kIdxRawStages + 2 * kScMaxTileStages + 2 * kScMaxAccStages];
     __shared__ uint32_t tmem_slot;
+    __shared__ int gave_up;
 
     uint8_t* tiles = dsm + ((1024u - (smem_u32(dsm) & 1023u)) & 1023u);
-    uint8_t* qt = tiles + 2 * kScTileBytes;
+    ScPipe pp;
+    pp.tiles = tiles;
+    pp.qt = tiles + kIdxTileStages * kScTileBytes;
+    pp.raw = pp.qt + kScQueryBytes;
+    pp.rfull = bars;
+    pp.rfree = bars + kIdxRawStages;
+    pp.full = bars + 2 * kIdxRawStages;
+    pp.tfree = pp.full + kIdxTileStages;
+    pp.afull = pp.full + 2 * kIdxTileStages;
+    pp.afree = pp.afull + kIdxAccStages;
+    pp.red = red;
+    pp.gave_up = &gave_up;
+    pp.seq = 0;
     const int b = blockIdx.y;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int warp = threadIdx.x >> 5;
     const int p_begin = blockIdx.x * a.pages_per_cta;
     const int p_end_all = min(p_begin + a.pages_per_cta, a.max_pages);
     // independent loads first: the row's length and this CTA's page-table entries
@@ -61,10 +73,7 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 2) index_score_kernel(IndexArg
         const int64_t ph = a.page_table[(int64_t)b * a.max_pages + p_begin + i];
         phys_s[i] = (ph < 0 || ph >= a.n_pool) ? -1 : ph;
     }
-    if (threadIdx.x == 0) {
-        mbar_init(&mbar, 1);
-        mbar_fence_init();
-    }
+    if (threadIdx.x == 0) sc_pipe_init<kIdxRawStages, kIdxTileStages, kIdxAccStages>(pp);
     if (warp == 0) tmem_alloc(&tmem_slot, kScTmemCols);
     tc_fence_before_sync();
     const int ctx = clamp_ctx(ctx_raw, a.Q, a.max_pages, (blockIdx.x == 0 && threadIdx.x == 0) ? a.status : nullptr);
@@ -72,87 +81,21 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 2) index_score_kernel(IndexArg
     const int p_end = min(p_end_all, n_pages);
     for (int p = max(p_begin, n_pages) + threadIdx.x; p < p_end_all; p += blockDim.x)
         a.scores[(int64_t)b * a.max_pages + p] = -INFINITY;
-    // the query pieces (its barriers also publish phys_s, the barrier and the allocation)
-    const ScQuery sq = sc_setup_query<NQ>(a.qidx + (int64_t)b * a.Q * kD, a.Q, qt, gmax);
+    // the query pieces (its barriers also publish phys_s, the barriers and the allocation)
+    const ScQuery sq = sc_setup_query<NQ>(a.qidx + (int64_t)b * a.Q * kD, a.Q, pp.qt, gmax);
     tc_fence_after_sync();
-    const uint32_t tmem = tmem_slot;
-    sc_init_sfb(tmem);
-
-    const int np = max(0, p_end - p_begin);
-    const int n_pairs = (np + 1) / 2;
-    const int h = warp >> 2;              // which page of a pair this warp takes
-    const int tok = threadIdx.x & 127;    // and which token
-    auto phys_of = [&](int i) -> int64_t { return i < np ? phys_s[i] : (int64_t)-1; };
-    ScPage c0, c1, n0, n1;                // pairs i and i + 1
-    uint32_t csw = 0, nsw = 0;            // this thread's token scale word of page h of each pair
-    auto load_pair = [&](ScPage& x0, ScPage& x1, uint32_t& sw, int pair) {
-        const int64_t ph0 = phys_of(2 * pair), ph1 = phys_of(2 * pair + 1);
-        if (ph0 >= 0) sc_load_page(x0, a.pool + ph0 * kMxPageBytes);
-        if (ph1 >= 0) sc_load_page(x1, a.pool + ph1 * kMxPageBytes);
-        const int64_t phh = h ? ph1 : ph0;
-        if (phh >= 0) sw = sc_load_scales(a.pool + phh * kMxPageBytes, tok);
-    };
-    if (n_pairs > 0) load_pair(c0, c1, csw, 0);
-    if (n_pairs > 1) load_pair(n0, n1, nsw, 1);
-    const int lim = ctx - a.Q;   // token j counts for query n iff j <= lim + n
-    bool failed = false;         // an MMA completion wait gave up
-    uint32_t fail_parity = 0;
-#pragma unroll 1
-    for (int i = 0; i <= n_pairs; ++i) {
-        if (i < n_pairs) {
-            sc_store_tile(c0, tiles);
-            sc_store_tile(c1, tiles + kScTileBytes);
-            sc_store_sfa(tmem, h, csw, sq);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        // tiles and scale factors of pair i ready; pair i - 1's maxima and tensor-memory reads done
-        if (__syncthreads_or(failed)) {
-            failed = true;
-            break;
-        }
-        tc_fence_after_sync();
-        if (i > 0 && threadIdx.x < 2) {
-            const int pp = 2 * (i - 1) + threadIdx.x;
-            if (pp < np) {
-                const float* r = red[(i - 1) & 1] + 4 * threadIdx.x;
-                a.scores[(int64_t)b * a.max_pages + p_begin + pp] =
-                    mul_exp2(fmaxf(fmaxf(r[0], r[1]), fmaxf(r[2], r[3])), -sq.sig_min);
-            }
-        }
-        if (i == n_pairs) break;
-        if (threadIdx.x == 0) {
-            sc_issue_page<NQ>(tmem, 0, smem_u32(tiles), smem_u32(qt));
-            sc_issue_page<NQ>(tmem, 1, smem_u32(tiles + kScTileBytes), smem_u32(qt));
-            tc_commit(&mbar);
-        }
-        c0 = n0;
-        c1 = n1;
-        csw = nsw;
-        if (i + 2 < n_pairs) load_pair(n0, n1, nsw, i + 2);
-        if (!mbar_wait_bounded(&mbar, (uint32_t)(i & 1))) {
-            failed = true;
-            fail_parity = (uint32_t)(i & 1);
-            flag_status(a.status, SMX_DEV_TIMEOUT);
-        }
-        tc_fence_after_sync();
-        const int pi = 2 * i + h;
-        float best = -INFINITY;
-        if (pi < np && phys_s[pi] >= 0)
-            best = sc_token_max<NQ>(tmem, h, (p_begin + pi) * kPage + tok, lim, a.Q);
-        else if (pi < np && tok == 0)
-            flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
-        if (lane == 0) red[i & 1][warp] = best;
-    }
-    // a wait that gave up: give the MMAs a second bounded wait before the columns are freed
-    if (failed) mbar_wait_bounded(&mbar, fail_parity);
+    pp.tmem = tmem_slot;
+    sc_init_sfb(pp.tmem);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    sc_score_pages<NQ, kIdxRawStages, kIdxTileStages, kIdxAccStages>(pp, a.pool, phys_s, max(0, p_end - p_begin), p_begin, ctx - a.Q,
+                                                        a.Q, sq, a.scores + (int64_t)b * a.max_pages, a.status);
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, kScTmemCols);
+        tmem_dealloc(pp.tmem, kScTmemCols);
     }
 }
 
@@ -291,8 +234,12 @@ cudaError_t launch_index_scores(const smx_shape_t& s, const uint16_t* qidx, cons
         if (s.Q <= 8) index_score_mma_kernel<1><<<grid, kIdxWarps * 32, 0, st>>>(a);
         else index_score_mma_kernel<2><<<grid, kIdxWarps * 32, 0, st>>>(a);
     } else {
-        if (s.Q <= 8) index_score_kernel<8><<<grid, kIdxWarps * 32, kIdxSmemBytes, st>>>(a);
-        else index_score_kernel<16><<<grid, kIdxWarps * 32, kIdxSmemBytes, st>>>(a);
+        const void* fn = s.Q <= 8 ? reinterpret_cast<const void*>(index_score_kernel<8>)
+                                  : reinterpret_cast<const void*>(index_score_kernel<16>);
+        const cudaError_t e = ensure_smem_attr(fn, kIdxSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (s.Q <= 8) index_score_kernel<8><<<grid, kIdxTcThreads, kIdxSmemBytes, st>>>(a);
+        else index_score_kernel<16><<<grid, kIdxTcThreads, kIdxSmemBytes, st>>>(a);
     }
     return cudaGetLastError();
 }
