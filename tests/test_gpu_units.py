@@ -98,7 +98,8 @@ def test_insert_bit_exact(fmt, Hkv):
                                                 (3, 4, 40, 3, 5000),
                                                 # rows long enough for the tensor-core scorer (>= 6 pages
                                                 # per CTA), with 8 and 16 query slots
-                                                (8, 16, 16, 3, 131072), (13, 16, 9, 2, 196608)])
+                                                (8, 16, 16, 3, 131072), (13, 16, 9, 2, 196608),
+                                                (1, 8, 8, 2, 131072)])
 def test_index_scores_and_topk(Q, Hq, topk, B, max_ctx):
     w = small(Q=Q, Hq=Hq, topk=topk, max_ctx=max_ctx, B=B)
     data = wl.generate(w)
@@ -143,6 +144,30 @@ def test_split_and_merge(fmt, S):
     assert ok, err
     ok, err = C.attn_close(out, res["out"])
     assert ok, err
+
+
+@pytest.mark.parametrize("max_ctx", [5000, 131072])   # the mma.sync scorer, the tensor-core scorer
+def test_index_scores_flag_bad_page_ids(max_ctx):
+    w = small(Q=8, Hq=16, topk=6, max_ctx=max_ctx, B=3)
+    data = wl.generate(w)
+    pools = H.oracle_pools(w, data, include_new=False)
+    sh = oracle.shape_of(w)
+    ref_s = oracle.index_scores(sh, data["qidx_bf16"], pools[2], data["page_table"], data["ctx_len"])
+    bad = dict(data)
+    bad["page_table"] = data["page_table"].copy()
+    bad["page_table"][0, 3] = w.n_pool_pages + 5
+    bad["page_table"][1, 10] = -1
+    g = C.gpu_inputs(w, bad, pools)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sc = ops.index_score(ops.Shape.of(w), g["qidx_bf16"], g["idx_pool"], g["page_table"], g["ctx_len"],
+                         dev_status=status).cpu().numpy().astype(np.float64)
+    assert int(status.item()) & ops.DEV_BAD_PAGE_ID
+    assert sc[0, 3] == -np.inf and sc[1, 10] == -np.inf
+    good = np.isfinite(ref_s)
+    good[0, 3] = good[1, 10] = False
+    rowmax = np.max(np.where(np.isfinite(ref_s), np.abs(ref_s), 0), axis=1, keepdims=True)
+    err = np.abs(sc - ref_s)[good]
+    assert np.all(err <= 2e-6 * np.broadcast_to(rowmax, ref_s.shape)[good] + 1e-6 * np.abs(ref_s[good])), err.max()
 
 
 def test_bad_page_ids_are_flagged_and_skipped():
