@@ -114,13 +114,14 @@ def _check(rc: int, what: str) -> None:
 
 
 def _p(t):
+    # a plain int: the entry points declare their pointer arguments c_void_p
     if t is None:
         return None
     if not t.is_cuda:
         raise SmxError("libsmx takes CUDA tensors only")
     if not t.is_contiguous():
         raise SmxError("libsmx takes contiguous tensors only")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def _st(stream):
