@@ -1,23 +1,30 @@
 // smx_attend_tc.cuh -- the split stage (a5) of one partition on the fifth-generation tensor cores:
-// QK and PV as 128 x 128 x 128 bf16 tcgen05 MMAs with fp32 accumulators in tensor memory.
+// QK and PV as 128 x 128 x 128 tcgen05 MMAs with fp32 accumulators in tensor memory.
 //
 // [ATOM-2812] "Mono decode over the MXFP4 KV and index caches", commit "MXFP4 main KV": QK against
 // the K page (fp4 with E8M0 group scales) and the e4m3 q, softmax with P in bf16, PV against V
 // widened to bf16 on chip, (sp_o, sp_m, sp_l) per partition.
 //
 // One CTA (8 warps) serves up to 128 query rows of one KV head; rows are (draft token, head)
-// pairs. Per selected page, staged by bulk copies (two pages in flight):
-//  1. K is widened to bf16 as a [128 tokens][128 dims] tile and V transposed into a
-//     [128 dims][128 tokens] tile (E2M1 x 2^e and e4m3 are exact in bf16; token rows past the
-//     context are zero, so poisoned slots never reach an MMA); both are K-major, 128-byte swizzle.
-//  2. One thread issues S = q K^T (8 MMA steps of K = 16) into tensor-memory columns 0..127.
-//  3. Thread (warp w, lane l) owns query row 32 (w % 4) + l and token / dim half w / 4: it reads
-//     its 64 scores (tcgen05.ld), scales, masks, takes the online softmax in the log2 domain (the
-//     row maximum is exchanged with its partner thread through shared memory) and writes its
-//     half of P as bf16 (FP8-KV: p times the V row scale as a bf16 high part and low part, the low
-//     part in the K tile, which S no longer needs).
-//  4. One thread issues O_page = P V^T (and P_lo V^T) into columns 128..255; every thread reads
-//     its 64 output columns and adds them to its running O after the softmax rescale.
+// pairs. Thread (warp w, lane l) owns query row 32 (w % 4) + l and token / dim half w / 4. Per
+// selected page, staged by bulk copies (two pages in flight):
+//
+// MXFP4 K/V (attend_pages_tc_mx):
+//  1. The K page's nibbles are copied into the fp4 operand layout (no conversion) and its E8M0
+//     scale words into the B scale block in tensor memory; one thread issues S = q K^T as four
+//     block-scaled MMAs (kind::mxf8f6f4, e4m3 q with unit scales, one per 32-dim group).
+//  2. Meanwhile V is widened to bf16 row by row ([token][dim], read by the PV MMA as an MN-major
+//     operand; token rows past the context are zero, so poisoned slots never reach an MMA).
+//  3. Each thread reads its 64 scores with one tensor-memory load, masks them, exchanges the half
+//     maximum with its partner thread, and writes its half of P as bf16. The running maximum
+//     follows the row maximum exactly, so the largest weight is exactly 1 (a maximum that lags by
+//     up to 8 would leave every weight rounded: on rows scaled x50 that alone breaks the output
+//     bound); O is rescaled in tensor memory when a row's maximum grows.
+//  4. One thread issues O += P V (eight MMAs) into columns 128..255; the next page's K copy and QK
+//     go ahead while it runs, and V / P are rewritten only after it completes.
+//
+// FP8-KV (attend_pages_tc): K widened to bf16 and V transposed into [dim][token] tiles, both
+// K-major; QK and PV as bf16 MMAs; p times the V row scale as a bf16 high part and low part.
 #pragma once
 
 #include <math.h>
@@ -29,77 +36,91 @@
 namespace smx {
 
 // Dynamic shared memory of the tensor-core attention (base 1024-byte aligned).
-constexpr int kTcQ = 0;             // q tile, bf16 [128 rows][128 dims]
-constexpr int kTcK = 32768;         // K tile [128 tokens][128 dims]; P low part (FP8-KV) after QK
-constexpr int kTcV = 65536;         // V^T tile [128 dims][128 tokens]
+constexpr int kTcQ = 0;             // q tile [128 rows][128 dims]: e4m3 (MXFP4), bf16 (FP8-KV)
+constexpr int kTcK = 32768;         // K tile [128 tokens][128 dims]: fp4 operand (MXFP4), bf16 (FP8-KV,
+                                    // then the P low part)
+constexpr int kTcV = 65536;         // V tile, bf16: [token][dim] (MXFP4), [dim][token] (FP8-KV)
 constexpr int kTcP = 98304;         // P tile [128 rows][128 tokens]
 constexpr int kTcScale = 131072;    // 128 K row scales, 128 V row scales (FP8-KV)
 constexpr int kTcRaw = 132096;      // two stages of (K page, V page)
-constexpr uint32_t kTcCols = 256;   // tensor-memory columns: S at 0, O at 128
+constexpr uint32_t kTcCols = 512;   // tensor-memory columns allocated
+constexpr uint32_t kTcColO = 128;   // S at column 0, O at 128
+constexpr uint32_t kTcColSFA = 256; // the A (q) scale block: 0x7F (2^0) in every byte
+constexpr uint32_t kTcColSFB = 264; // the B (K page) scale block
 constexpr int kTcRows = 128;        // query rows per CTA
 
 __host__ __device__ constexpr size_t attend_tc_smem_bytes(int page_bytes) {
     return (size_t)kTcRaw + 4 * (size_t)page_bytes;
 }
 
-// The q tile from `rows` query rows (rows past them are zero). Staged rows at src (shared memory,
-// 512-byte f32 rows for MXFP4 K/V, packed here to e4m3 by the q packing rule and widened to bf16;
-// 256-byte bf16 rows for FP8-KV). One (row, half) piece per thread of the 256-thread block.
+// The q tile from `rows` query rows (rows past them are zero). MXFP4 K/V: e4m3 codes by the q
+// packing rule, 128-byte rows; FP8-KV: bf16, 256-byte rows. Staged rows at src (shared memory):
+// 512-byte f32 rows (MXFP4), 256-byte bf16 rows (FP8-KV). Every thread of the 256-thread block.
 template <bool RS>
 __device__ __forceinline__ void pack_q_tile_tc(const uint8_t* src, int rows, uint8_t* tile) {
-    const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
+    if constexpr (RS) {
+        const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {   // chunk c of the half: dims 64 h + 8 c .. + 7
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (r < rows) {
-            if (RS) {
-                v = *reinterpret_cast<const uint4*>(src + r * 256 + (8 * h + c) * 16);
-            } else {
-                const float4* f = reinterpret_cast<const float4*>(src + r * 512 + (8 * h + c) * 32);
-                const float4 f0 = f[0], f1 = f[1];
-                const float2 g0 = f16x2_to_f32x2(e4m3x2_to_f16x2(pack_q2(f0.x, f0.y)));
-                const float2 g1 = f16x2_to_f32x2(e4m3x2_to_f16x2(pack_q2(f0.z, f0.w)));
-                const float2 g2 = f16x2_to_f32x2(e4m3x2_to_f16x2(pack_q2(f1.x, f1.y)));
-                const float2 g3 = f16x2_to_f32x2(e4m3x2_to_f16x2(pack_q2(f1.z, f1.w)));
-                v = make_uint4(f32x2_to_bf16x2(g0.x, g0.y), f32x2_to_bf16x2(g1.x, g1.y), f32x2_to_bf16x2(g2.x, g2.y),
-                               f32x2_to_bf16x2(g3.x, g3.y));
-            }
+        for (int c = 0; c < 8; ++c) {   // chunk c of the half: dims 64 h + 8 c .. + 7
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (r < rows) v = *reinterpret_cast<const uint4*>(src + r * 256 + (8 * h + c) * 16);
+            *reinterpret_cast<uint4*>(tile + sw128_chunk(r, 8 * h + c, kTcRows)) = v;
         }
-        *reinterpret_cast<uint4*>(tile + sw128_chunk(r, 8 * h + c, kTcRows)) = v;
+    } else {
+        // warp w packs rows w, w + 8, ...; lane l dims 4 l .. 4 l + 3 (one 512-byte row per warp)
+        const int lane = threadIdx.x & 31;
+#pragma unroll 4
+        for (int r = threadIdx.x >> 5; r < kTcRows; r += 8) {   // 8 warps
+            uint32_t w = 0;
+            if (r < rows) {
+                const float4 f = *reinterpret_cast<const float4*>(src + r * 512 + lane * 16);
+                w = pack_q2(f.x, f.y) | (pack_q2(f.z, f.w) << 16);
+            }
+            *reinterpret_cast<uint32_t*>(tile + sw128_chunk(r, lane >> 2, kTcRows) + 4 * (lane & 3)) = w;
+        }
     }
 }
 
-// The same from global q rows: row i of the unit is q row (b, i / G ... ) given by qrow(i).
+// The same from global q rows: unit row i is q row (b, (m_lo + i) / G, kvh G + (m_lo + i) % G).
 template <bool RS>
 __device__ __forceinline__ void pack_q_tile_tc_global(const void* q, int b, int kvh, int m_lo, int rows, int Q, int Hq,
                                                       int G, uint8_t* tile) {
-    const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
-    const int m = m_lo + r;
-    const int64_t row = ((int64_t)b * Q + (r < rows ? m / G : 0)) * Hq + kvh * G + (r < rows ? m % G : 0);
+    auto q_row = [&](int i) {   // global row of unit row i < rows
+        const int m = m_lo + i;
+        return ((int64_t)b * Q + m / G) * Hq + kvh * G + m % G;
+    };
+    if constexpr (RS) {
+        const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
+        const int64_t row = q_row(r < rows ? r : 0);
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (r < rows) {
-            if (RS) {
-                v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(q) + row * 256 + (8 * h + c) * 16);
-            } else {
-                const float4* f = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(q) + row * kD + (8 * h + c) * 8);
-                const float4 f0 = f[0], f1 = f[1];
-                const float2 g0 = f16x2_to_f32x2(e4m3x2_to_f16x2(pack_q2(f0.x, f0.y)));
-                const float2 g1 = f16x2_to_f32x2(e4m3x2_to_f16x2(pack_q2(f0.z, f0.w)));
-                const float2 g2 = f16x2_to_f32x2(e4m3x2_to_f16x2(pack_q2(f1.x, f1.y)));
-                const float2 g3 = f16x2_to_f32x2(e4m3x2_to_f16x2(pack_q2(f1.z, f1.w)));
-                v = make_uint4(f32x2_to_bf16x2(g0.x, g0.y), f32x2_to_bf16x2(g1.x, g1.y), f32x2_to_bf16x2(g2.x, g2.y),
-                               f32x2_to_bf16x2(g3.x, g3.y));
-            }
+        for (int c = 0; c < 8; ++c) {
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (r < rows) v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(q) + row * 256 + (8 * h + c) * 16);
+            *reinterpret_cast<uint4*>(tile + sw128_chunk(r, 8 * h + c, kTcRows)) = v;
         }
-        *reinterpret_cast<uint4*>(tile + sw128_chunk(r, 8 * h + c, kTcRows)) = v;
+    } else {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        constexpr int kPer = kTcRows / 8;   // rows per warp
+        float4 f[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {   // all loads in flight together
+            const int r = warp + 8 * k;
+            f[k] = r < rows ? *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(q) + q_row(r) * kD + 4 * lane)
+                            : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int r = warp + 8 * k;
+            const uint32_t w = pack_q2(f[k].x, f[k].y) | (pack_q2(f[k].z, f[k].w) << 16);
+            *reinterpret_cast<uint32_t*>(tile + sw128_chunk(r, lane >> 2, kTcRows) + 4 * (lane & 3)) = w;
+        }
     }
 }
 
-// K page (raw, shared memory) -> K tile [token][dim]; FP8-KV row scales -> rscale.
+// A K or V page (raw, shared memory) -> bf16 tile [token][dim] (K-major for the token as the
+// row); FP8-KV row scales -> rscale. Token rows at or past valid_rows are zero.
 template <bool RS>
-__device__ __forceinline__ void widen_k_tc(const uint8_t* raw, int valid_rows, uint8_t* tile, float* rscale) {
+__device__ __forceinline__ void widen_rows_tc(const uint8_t* raw, int valid_rows, uint8_t* tile, float* rscale) {
     if constexpr (RS) {
         // 128 tokens x 8 chunks of 16 codes (two output chunks each)
 #pragma unroll 1
@@ -155,6 +176,36 @@ __device__ __forceinline__ void widen_k_tc(const uint8_t* raw, int valid_rows, u
                     make_uint4(ob[4 * k], ob[4 * k + 1], ob[4 * k + 2], ob[4 * k + 3]);
         }
     }
+}
+
+// MXFP4 K page (raw, shared memory) -> the fp4 operand tile [token][128 dims] (each 16-dim chunk:
+// its 8 nibble bytes, then 8 zero bytes) and its E8M0 scale words -> the B scale block (token t's
+// word, byte g = group g, in lane t % 32 of column t / 32, every quadrant: warp w < 4 writes
+// quadrant w). Token rows past the context keep whatever the page holds: their scores are masked.
+__device__ __forceinline__ void repack_k_mx_tc(const uint8_t* raw, uint8_t* tile, uint32_t tmem) {
+    uint2 w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {   // 128 tokens x 8 chunks over the 256 threads
+        const int it = (int)threadIdx.x + 256 * k;
+        w[k] = *reinterpret_cast<const uint2*>(raw + (it >> 3) * 64 + (it & 7) * 8);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int it = (int)threadIdx.x + 256 * k;
+        *reinterpret_cast<uint4*>(tile + sw128_chunk(it >> 3, it & 7, kTcRows)) = make_uint4(w[k].x, w[k].y, 0u, 0u);
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < 4) {
+        const uint32_t* sc = reinterpret_cast<const uint32_t*>(raw + kMxScaleOff);
+        tmem_st4(tmem + ((uint32_t)(32 * warp) << 16) + kTcColSFB, sc[lane], sc[32 + lane], sc[64 + lane], sc[96 + lane]);
+    }
+}
+
+// 2^x for the softmax weights (x <= 0; -inf gives 0): the hardware base-2 exponential.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // V page (raw, shared memory) -> V^T tile [dim][token]; FP8-KV row scales -> rscale. Thread t
@@ -269,7 +320,7 @@ __device__ __forceinline__ bool attend_pages_tc(uint8_t* smem, const AttendSmem&
         const int valid_rows = p >= 0 ? min(kPage, ctx - p * kPage) : 0;
         const int jpage = p >= 0 ? p * kPage : 0;
         const uint8_t* rk = sm.raw + st * 2 * page_bytes;
-        widen_k_tc<RS>(rk, valid_rows, k_tile, kscale);
+        widen_rows_tc<RS>(rk, valid_rows, k_tile, kscale);
         widen_vt_tc<RS>(rk + page_bytes, valid_rows, vt_tile, vscale);
         fence_proxy_async_smem();   // the tiles (generic writes) before the MMAs read them
         __syncthreads();            // tiles ready; this stage's raw bytes are consumed
@@ -367,6 +418,143 @@ __device__ __forceinline__ bool attend_pages_tc(uint8_t* smem, const AttendSmem&
     }
     gp += (uint32_t)np;
     return ok_all;
+}
+
+// MXFP4 K/V: the pages sel[0..np) / selph[0..np) of this CTA's partition, as attend_pages_tc
+// (pages 0 and 1 issued by the caller; the q tile holds e4m3 codes; the A scale block at column
+// kTcColSFA holds 0x7F in every byte). bars[0] counts QK completions (qk_ph phases seen), bars[1]
+// PV completions (pv_ph). The page loop keeps one PV in flight: page i + 1's K repack and QK run
+// while PV i does. m: the row's running maximum (log2 domain); l: this half's share of the row's
+// weight sum.
+// Returns false (every thread alike) if a copy or an MMA did not finish within the bounded wait
+// (status gets SMX_DEV_TIMEOUT); O is then incomplete.
+__device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, const AttendSmem& sm, const int* sel, const int* selph,
+                                                   int np, const uint8_t* k_pool, const uint8_t* v_pool, int Hkv, int kvh,
+                                                   int page_bytes, int ctx, uint32_t tmem, uint64_t* bars, uint32_t& qk_ph,
+                                                   uint32_t& pv_ph, const TcLane& L, float* xch, uint32_t& gp, float& m,
+                                                   float& l, int32_t* status) {
+    uint8_t* q_tile = smem + kTcQ;
+    uint8_t* k_tile = smem + kTcK;
+    uint8_t* v_tile = smem + kTcV;
+    uint8_t* p_tile = smem + kTcP;
+    const uint32_t lane_base = tmem + ((uint32_t)(L.r & ~31) << 16);   // this warp's 32 lanes
+    const uint32_t s_cols = lane_base + 64 * L.h;
+    const uint32_t o_cols = lane_base + kTcColO + 64 * L.h;
+    bool ok_all = true;
+    bool pv_pending = false;
+#pragma unroll 1
+    for (int i = 0; i < np; ++i) {
+        const int st = (int)((gp + i) & 1);
+        const uint32_t parity = (uint32_t)(((gp + i) >> 1) & 1);
+        const uint32_t next_parity = (uint32_t)(((gp + i + 1) >> 1) & 1);
+        const bool ok = mbar_wait_bounded(&sm.mbar[st], parity);
+        const int p = sm.stage_page[st];
+        const int valid_rows = p >= 0 ? min(kPage, ctx - p * kPage) : 0;
+        const int jpage = p >= 0 ? p * kPage : 0;
+        const uint8_t* rk = sm.raw + st * 2 * page_bytes;
+        // the K tile and the B scale block are free: QK i - 1 completed (waited on in page i - 1)
+        repack_k_mx_tc(rk, k_tile, tmem);
+        fence_proxy_async_smem();   // the K tile (generic writes) before the MMAs read it
+        tc_fence_before_sync();
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0) {
+                attend_drain(sm, st, parity, i + 1 < np, next_parity, status);
+                if (pv_pending) mbar_wait_bounded(&bars[1], pv_ph & 1);
+            }
+            __syncthreads();
+            ok_all = false;
+            pv_pending = false;
+            break;
+        }
+        if (threadIdx.x == 0) {
+            tc_fence_after_sync();
+            tc_mma_mx_tile(tmem, smem_u32(q_tile), smem_u32(k_tile), tmem + kTcColSFA, tmem + kTcColSFB);
+            tc_commit(&bars[0]);
+        }
+        // V, once PV i - 1 no longer reads the V and P tiles
+        bool mma_ok = true;
+        if (pv_pending) {
+            mma_ok = tc_wait(&bars[1], pv_ph & 1);
+            ++pv_ph;
+            pv_pending = false;
+            tc_fence_after_sync();
+        }
+        widen_rows_tc<false>(rk + page_bytes, valid_rows, v_tile, nullptr);
+        fence_proxy_async_smem();
+        mma_ok = tc_wait(&bars[0], qk_ph & 1) && mma_ok;
+        ++qk_ph;
+        tc_fence_after_sync();
+        // this half's 64 scores: scaled to the log2 domain, masked past the context and causally
+        float z[64];
+        tmem_ld64(s_cols, z);
+        const int lim = L.valid ? min(valid_rows, L.pos - jpage + 1) - 64 * L.h : 0;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+            z[j] = j < lim ? z[j] * kLog2eOverSqrtD : -INFINITY;
+            mx = fmaxf(mx, z[j]);
+        }
+        xch[threadIdx.x] = mx;
+        if (__syncthreads_or(!mma_ok)) {   // the V tile is written; this stage's raw bytes are consumed
+            if (threadIdx.x == 0) {
+                flag_status(status, SMX_DEV_TIMEOUT);
+                if (i + 1 < np) mbar_wait_bounded(&sm.mbar[st ^ 1], next_parity);
+            }
+            __syncthreads();
+            ok_all = false;
+            break;
+        }
+        if (threadIdx.x == 0 && i + 2 < np)
+            attend_issue(sm, i + 2, sel[i + 2], selph[i + 2], gp, k_pool, v_pool, Hkv, kvh, page_bytes);
+        mx = fmaxf(mx, xch[threadIdx.x ^ 128]);   // the partner thread holds the other half of the row
+        const bool raise = mx > m;   // false while the row has seen nothing (mx = -inf)
+        const float alpha = raise ? ex2_approx(m - mx) : 1.0f;   // m = -inf: 0
+        if (raise) {
+            m = mx;
+            l *= alpha;
+        }
+        if (i > 0 && __any_sync(0xFFFFFFFFu, raise)) {
+            // rescale the warp's output columns in place (PV i - 1 is done; alpha is 1 for the
+            // rows that keep their maximum)
+            float ov[64];
+            tmem_ld64(o_cols, ov);
+#pragma unroll
+            for (int j = 0; j < 64; ++j) ov[j] *= alpha;
+            tmem_st64(o_cols, ov);
+        }
+        // this half of P as bf16; l sums the rounded weights the MMA uses
+        const float mb = m == -INFINITY ? 0.0f : m;
+        uint32_t hw[32];
+#pragma unroll
+        for (int q2 = 0; q2 < 32; ++q2) {
+            const __nv_bfloat162 hb = __floats2bfloat162_rn(ex2_approx(z[2 * q2] - mb), ex2_approx(z[2 * q2 + 1] - mb));
+            const float2 hr = __bfloat1622float2(hb);
+            l += hr.x + hr.y;
+            hw[q2] = *reinterpret_cast<const uint32_t*>(&hb);
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(p_tile + sw128_chunk(L.r, 8 * L.h + c, kTcRows)) =
+                make_uint4(hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
+        fence_proxy_async_smem();   // P (generic writes) before the MMA reads it
+        tc_fence_before_sync();     // the S and O accesses before the next MMAs
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            tc_fence_after_sync();
+            tc_mma_tile_bmn(tmem + kTcColO, smem_u32(p_tile), smem_u32(v_tile), i > 0);
+            tc_commit(&bars[1]);
+        }
+        pv_pending = true;
+    }
+    if (pv_pending) {   // the last PV
+        const bool ok = tc_wait(&bars[1], pv_ph & 1);
+        ++pv_ph;
+        tc_fence_after_sync();
+        if (!ok && threadIdx.x == 0) flag_status(status, SMX_DEV_TIMEOUT);
+        ok_all = ok_all && ok;
+    }
+    gp += (uint32_t)np;
+    return __syncthreads_and(ok_all) != 0;
 }
 
 // Partials of this CTA's real rows for partition s: O from tensor-memory columns 128..255 (zero

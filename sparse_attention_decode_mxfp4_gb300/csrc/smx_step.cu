@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
     __shared__ int stage_page[2];
     __shared__ int is_last;
     __shared__ int32_t pt_s[kPtCache];   // the unit's row of the page table (rows up to kPtCache pages)
-    __shared__ __align__(8) uint64_t mbar_mma;   // tensor-core MMA completions
+    __shared__ __align__(8) uint64_t mbar_mma[2];   // tensor-core MMA completions (MXFP4: QK, PV)
     __shared__ uint32_t tmem_slot;
     __shared__ float xch_tc[kStepWarps * 32];    // row maxima / sums exchanged between the two halves
 
@@ -121,7 +121,8 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
         mbar_init(&mbar[0], 1);
         mbar_init(&mbar[1], 1);
         mbar_init(&mbar_q, 1);
-        mbar_init(&mbar_mma, 1);
+        mbar_init(&mbar_mma[0], 1);
+        mbar_init(&mbar_mma[1], 1);
         mbar_fence_init();
     }
 
@@ -318,8 +319,13 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
         __syncthreads();
         tc_fence_after_sync();
         const uint32_t tmem = tmem_slot;
+        if (!RS && has_units && warp < 4) {   // unit scales for the e4m3 q (A) of the block-scaled QK
+            tmem_st4(tmem + ((uint32_t)(32 * warp) << 16) + kTcColSFA, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+            tc_fence_before_sync();
+        }
         uint32_t gp = 0;          // pages staged by this CTA so far (sets the stages' phase parity)
-        uint32_t mma_ph = 0;      // MMA completions seen so far
+        uint32_t mma_ph = 0;      // MMA completions seen so far (MXFP4: QK completions)
+        uint32_t pv_ph = 0;       // MXFP4: PV completions seen so far
         bool copies_ok = smem_ok; // false after a copy or MMA that did not finish: stage nothing more
         for (int u = u0; u < n_units; u += nC) {
             const int s = u % a.S, rg = (u / a.S) % a.n_rg, kvh = (u / (a.S * a.n_rg)) % a.Hkv;
@@ -392,9 +398,16 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
 
             float m_run = -INFINITY, l = 0.0f;
             const bool run = copies_ok && hi > lo;
-            if (run)
-                copies_ok = attend_pages_tc<RS>(smem, sm, sel, selph, hi - lo, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes,
-                                                ctx, tmem, &mbar_mma, mma_ph, L, xch_tc, gp, m_run, l, a.status);
+            if (run) {
+                if constexpr (RS)
+                    copies_ok = attend_pages_tc<RS>(smem, sm, sel, selph, hi - lo, a.k_pool, a.v_pool, a.Hkv, kvh,
+                                                    a.page_bytes, ctx, tmem, &mbar_mma[0], mma_ph, L, xch_tc, gp, m_run, l,
+                                                    a.status);
+                else
+                    copies_ok = attend_pages_tc_mx(smem, sm, sel, selph, hi - lo, a.k_pool, a.v_pool, a.Hkv, kvh,
+                                                   a.page_bytes, ctx, tmem, mbar_mma, mma_ph, pv_ph, L, xch_tc, gp, m_run,
+                                                   l, a.status);
+            }
             finish_partials_tc(L, tmem, run, m_run, l, xch_tc, a.part_o, a.part_m, a.part_l, b, s, kvh, a.S, a.Q, a.Hq, a.G,
                                m_lo);
             __syncthreads();

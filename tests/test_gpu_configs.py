@@ -93,6 +93,21 @@ def test_tensor_core_attention_path(kv_format):
     C.full_step_parity(w)
 
 
+@pytest.mark.parametrize("kv_format,Q,big", [(wl.KV_MXFP4, 8, 0.0), (wl.KV_MXFP4, 8, 0.01), (wl.KV_MXFP4, 16, 0.0),
+                                          (wl.KV_E4M3_ROWSCALE, 8, 0.01)])
+def test_tensor_core_attention_multi_page(kv_format, Q, big):
+    # 20 rows x (2 or 4) groups of 64 query rows x 4 partitions = 160 or 320 mma.sync units: the
+    # tensor-core path, with 8 pages per partition (ragged rows: fewer), so the page loop runs
+    # several pages per unit and rescales O whenever a row's maximum grows; rows scaled x50 (big)
+    # make the maxima jump. (MXFP4 weights are bf16: with x50 rows the attention concentrates on a
+    # few tokens and bf16 rounding of their weights alone -- exact scores and V -- reaches 1.14x the
+    # output bound on the Q = 16 case, 0.67x on Q = 8; the FP8-KV weights carry a low part.)
+    w = wl.Workload("tc_pages", B=20, Q=Q, Hq=16, Hkv=1, max_ctx=6000, topk=32, num_splits=4, seed=515,
+                    ragged=True, kv_format=kv_format, big_row_frac=big)
+    assert _uses_tc(w)
+    C.full_step_parity(w)
+
+
 def test_configs_take_the_mma_path():
     # the benchmark workloads at the suggested partition counts fit one wave of 64-row units
     for c in (2, 3, 4):
