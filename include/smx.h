@@ -184,10 +184,14 @@ int smx_decode_step_tensor_cores(const smx_shape_t* shape);
 
 /* A partition count S for this shape on the CURRENT device (the pages leave S to the
  * implementation: any S >= 1 gives the same attention up to rounding). It is the largest S
- * whose split CTAs (B x Hkv x row groups per partition) fill at most one wave of the device's
- * SMs at the split kernel's occupancy, lowered so every partition holds the same number of
- * selected pages. shape->num_splits is ignored. Returns S >= 1, or 0 when the other fields of
- * the shape are invalid or a CUDA query fails. Reads device attributes; launches nothing. */
+ * whose split CTAs (B x Hkv x row groups of up to 64 query rows per partition) fill at most one
+ * wave of the device's SMs, lowered so every partition holds the same number of selected pages.
+ * For MXFP4 K/V with more than 64 query rows per KV head, when that leaves 3 or more selected
+ * pages per partition, it is instead the same count for row groups of 128 rows: the fused step
+ * then runs its attention on the tensor cores (smx_decode_step_tensor_cores), the standalone
+ * split stage in two waves. shape->num_splits is ignored. Returns S >= 1, or 0 when the other
+ * fields of the shape are invalid or a CUDA query fails. Reads device attributes; launches
+ * nothing. */
 int smx_suggest_num_splits(const smx_shape_t* shape);
 
 /* Bytes of the static device scratch smx_decode_step_noalloc works in (16 MiB). */

@@ -420,19 +420,72 @@ __device__ __forceinline__ bool attend_pages_tc(uint8_t* smem, const AttendSmem&
     return ok_all;
 }
 
-// MXFP4 K/V: the pages sel[0..np) / selph[0..np) of this CTA's partition, as attend_pages_tc
-// (pages 0 and 1 issued by the caller; the q tile holds e4m3 codes; the A scale block at column
-// kTcColSFA holds 0x7F in every byte). bars[0] counts QK completions (qk_ph phases seen), bars[1]
-// PV completions (pv_ph). The page loop keeps one PV in flight: page i + 1's K repack and QK run
-// while PV i does. m: the row's running maximum (log2 domain); l: this half's share of the row's
-// weight sum.
+// MXFP4 K/V copies: the K or V page of entry i into slot (gp + i) % 2 of the stage area
+// (slot s: K page at raw + 2 s page_bytes, V page right after it), completing on cbar[slot] (K)
+// or cbar[2 + slot] (V). phys < 0: no copy, the barrier's phase completes at once. One thread.
+__device__ __forceinline__ void mx_issue(uint8_t* raw, uint64_t* cbar, int i, bool v, int64_t phys, uint32_t gp,
+                                         const uint8_t* pool, int Hkv, int kvh, int page_bytes) {
+    const int st = (int)((gp + i) & 1);
+    uint64_t* bar = &cbar[(v ? 2 : 0) + st];
+    if (phys < 0) {
+        mbar_arrive(bar);
+        return;
+    }
+    mbar_arrive_expect_tx(bar, (uint32_t)page_bytes);
+    bulk_g2s(raw + st * 2 * page_bytes + (v ? page_bytes : 0), pool + (phys * Hkv + kvh) * (int64_t)page_bytes,
+             (uint32_t)page_bytes, bar);
+}
+
+// bf16x2 product (round to nearest even; exact here: powers of two times codes).
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// The two bf16x2 factors whose product is 2^(b - 15) for an E8M0 byte b (each a power of two in
+// bf16's normal range for every b < 255; b = 255 gives NaN, as the E8M0 NaN code).
+__device__ __forceinline__ void v_scale_factors(uint32_t b, uint32_t& s1, uint32_t& s2) {
+    const int k = (int)b - 15, k1 = k >> 1, k2 = k - k1;
+    const uint32_t e1 = (uint32_t)(k1 + 127) << 7, e2 = (uint32_t)(k2 + 127) << 7;
+    s1 = b == 0xFFu ? 0x7FC07FC0u : (e1 | (e1 << 16));
+    s2 = e2 | (e2 << 16);
+}
+
+// One 16-byte chunk of the V tile: 8 E2M1 codes (w) times 2^(b - 127) as bf16 (exact). Each code's
+// f16 (exact) with its exponent and mantissa bits shifted down by 3 is a bf16 holding the code
+// times 2^-112 (zero stays zero); two power-of-two multiplies (s1 s2 = 2^(b - 15)) finish it.
+// No conversion-pipe work past the E2M1 -> f16 conversion.
+__device__ __forceinline__ uint4 widen_v_chunk(uint32_t w, uint32_t s1, uint32_t s2) {
+    uint32_t h[4], o[4];
+    e2m1x8_to_f16x2(w, h[0], h[1], h[2], h[3]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t t = ((h[q] & 0x7FFF7FFFu) >> 3) | (h[q] & 0x80008000u);
+        o[q] = bf16x2_mul(bf16x2_mul(t, s1), s2);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// MXFP4 K/V: the pages sel[0..np) / selph[0..np) of this CTA's partition. The caller issued the
+// K and V copies of entries 0 and 1 (mx_issue, in that order: K 0, V 0, K 1, V 1); the q tile
+// holds e4m3 codes; the A scale block (column kTcColSFA) holds 0x7F in every byte. cbar: copy
+// barriers [K slot 0, K slot 1, V slot 0, V slot 1]; bars[0] counts QK completions (qk_ph phases
+// seen), bars[1] PV completions (pv_ph). Per page i, with two CTA barriers:
+//   (QK i was issued during page i - 1) S i is read and masked; K i + 1 is repacked (QK i is
+//   done, so the K tile and B scale block are free); barrier B; thread 0 issues QK i + 1 and the
+//   K copy of page i + 3; the row maxima are combined, PV i - 1 is waited for, O is rescaled,
+//   and P i (ex2) is written interleaved with the widening of V i (ALU and conversion pipes);
+//   barrier C; thread 224 issues PV i, thread 32 the V copy of page i + 2.
+// m: the row's running maximum (log2 domain); l: this half's share of the row's weight sum.
 // Returns false (every thread alike) if a copy or an MMA did not finish within the bounded wait
 // (status gets SMX_DEV_TIMEOUT); O is then incomplete.
-__device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, const AttendSmem& sm, const int* sel, const int* selph,
-                                                   int np, const uint8_t* k_pool, const uint8_t* v_pool, int Hkv, int kvh,
-                                                   int page_bytes, int ctx, uint32_t tmem, uint64_t* bars, uint32_t& qk_ph,
-                                                   uint32_t& pv_ph, const TcLane& L, float* xch, uint32_t& gp, float& m,
-                                                   float& l, int32_t* status) {
+__device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, uint8_t* raw, uint64_t* cbar, const int* sel,
+                                                   const int* selph, int np, const uint8_t* k_pool,
+                                                   const uint8_t* v_pool, int Hkv, int kvh, int page_bytes, int ctx,
+                                                   uint32_t tmem, uint64_t* bars, uint32_t& qk_ph, uint32_t& pv_ph,
+                                                   const TcLane& L, float* xch, uint32_t& gp, float& m, float& l,
+                                                   int32_t* status) {
     uint8_t* q_tile = smem + kTcQ;
     uint8_t* k_tile = smem + kTcK;
     uint8_t* v_tile = smem + kTcV;
@@ -440,51 +493,42 @@ __device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, const AttendSm
     const uint32_t lane_base = tmem + ((uint32_t)(L.r & ~31) << 16);   // this warp's 32 lanes
     const uint32_t s_cols = lane_base + 64 * L.h;
     const uint32_t o_cols = lane_base + kTcColO + 64 * L.h;
+    auto slot = [&](int i) { return (int)((gp + i) & 1); };
+    auto par = [&](int i) { return (uint32_t)(((gp + i) >> 1) & 1); };
+    auto k_raw = [&](int i) { return raw + slot(i) * 2 * page_bytes; };
+    // copies issued / waited for (pages), MMA commits issued: the same in every thread
+    int k_iss = min(np, 2), v_iss = min(np, 2), k_done = 0, v_done = 0;
+    uint32_t qk_iss = qk_ph, pv_iss = pv_ph;
     bool ok_all = true;
-    bool pv_pending = false;
-#pragma unroll 1
-    for (int i = 0; i < np; ++i) {
-        const int st = (int)((gp + i) & 1);
-        const uint32_t parity = (uint32_t)(((gp + i) >> 1) & 1);
-        const uint32_t next_parity = (uint32_t)(((gp + i + 1) >> 1) & 1);
-        const bool ok = mbar_wait_bounded(&sm.mbar[st], parity);
-        const int p = sm.stage_page[st];
-        const int valid_rows = p >= 0 ? min(kPage, ctx - p * kPage) : 0;
-        const int jpage = p >= 0 ? p * kPage : 0;
-        const uint8_t* rk = sm.raw + st * 2 * page_bytes;
-        // the K tile and the B scale block are free: QK i - 1 completed (waited on in page i - 1)
-        repack_k_mx_tc(rk, k_tile, tmem);
-        fence_proxy_async_smem();   // the K tile (generic writes) before the MMAs read it
-        tc_fence_before_sync();
-        if (__syncthreads_or(!ok)) {
-            if (threadIdx.x == 0) {
-                attend_drain(sm, st, parity, i + 1 < np, next_parity, status);
-                if (pv_pending) mbar_wait_bounded(&bars[1], pv_ph & 1);
-            }
-            __syncthreads();
-            ok_all = false;
-            pv_pending = false;
-            break;
-        }
+
+    // K 0 and QK 0
+    bool ok = mbar_wait_bounded(&cbar[slot(0)], par(0));
+    if (ok) k_done = 1;
+    repack_k_mx_tc(k_raw(0), k_tile, tmem);
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    if (__syncthreads_or(!ok)) {
+        ok_all = false;
+    } else {
         if (threadIdx.x == 0) {
             tc_fence_after_sync();
             tc_mma_mx_tile(tmem, smem_u32(q_tile), smem_u32(k_tile), tmem + kTcColSFA, tmem + kTcColSFB);
             tc_commit(&bars[0]);
+            if (np > 2) mx_issue(raw, cbar, 2, false, selph[2], gp, k_pool, Hkv, kvh, page_bytes);
         }
-        // V, once PV i - 1 no longer reads the V and P tiles
-        bool mma_ok = true;
-        if (pv_pending) {
-            mma_ok = tc_wait(&bars[1], pv_ph & 1);
-            ++pv_ph;
-            pv_pending = false;
-            tc_fence_after_sync();
-        }
-        widen_rows_tc<false>(rk + page_bytes, valid_rows, v_tile, nullptr);
-        fence_proxy_async_smem();
-        mma_ok = tc_wait(&bars[0], qk_ph & 1) && mma_ok;
+        ++qk_iss;
+        if (np > 2) ++k_iss;
+    }
+
+#pragma unroll 1
+    for (int i = 0; ok_all && i < np; ++i) {
+        const int p = selph[i] >= 0 ? sel[i] : -1;
+        const int valid_rows = p >= 0 ? min(kPage, ctx - p * kPage) : 0;
+        const int jpage = p >= 0 ? p * kPage : 0;
+        // S i: scaled to the log2 domain, masked past the context and causally
+        ok = tc_wait(&bars[0], qk_ph & 1);
         ++qk_ph;
         tc_fence_after_sync();
-        // this half's 64 scores: scaled to the log2 domain, masked past the context and causally
         float z[64];
         tmem_ld64(s_cols, z);
         const int lim = L.valid ? min(valid_rows, L.pos - jpage + 1) - 64 * L.h : 0;
@@ -494,18 +538,30 @@ __device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, const AttendSm
             z[j] = j < lim ? z[j] * kLog2eOverSqrtD : -INFINITY;
             mx = fmaxf(mx, z[j]);
         }
+        // K i + 1 (QK i is done: the K tile and the B scale block are free)
+        if (i + 1 < np) {
+            if (mbar_wait_bounded(&cbar[slot(i + 1)], par(i + 1))) k_done = i + 2;
+            else ok = false;
+            repack_k_mx_tc(k_raw(i + 1), k_tile, tmem);
+        }
         xch[threadIdx.x] = mx;
-        if (__syncthreads_or(!mma_ok)) {   // the V tile is written; this stage's raw bytes are consumed
-            if (threadIdx.x == 0) {
-                flag_status(status, SMX_DEV_TIMEOUT);
-                if (i + 1 < np) mbar_wait_bounded(&sm.mbar[st ^ 1], next_parity);
-            }
-            __syncthreads();
+        fence_proxy_async_smem();
+        tc_fence_before_sync();   // S i read; the B scale block written
+        if (__syncthreads_or(!ok)) {
             ok_all = false;
             break;
         }
-        if (threadIdx.x == 0 && i + 2 < np)
-            attend_issue(sm, i + 2, sel[i + 2], selph[i + 2], gp, k_pool, v_pool, Hkv, kvh, page_bytes);
+        if (threadIdx.x == 0) {
+            if (i + 1 < np) {
+                tc_fence_after_sync();
+                tc_mma_mx_tile(tmem, smem_u32(q_tile), smem_u32(k_tile), tmem + kTcColSFA, tmem + kTcColSFB);
+                tc_commit(&bars[0]);
+            }
+            if (i + 3 < np) mx_issue(raw, cbar, i + 3, false, selph[i + 3], gp, k_pool, Hkv, kvh, page_bytes);
+        }
+        if (i + 1 < np) ++qk_iss;
+        if (i + 3 < np) ++k_iss;
+
         mx = fmaxf(mx, xch[threadIdx.x ^ 128]);   // the partner thread holds the other half of the row
         const bool raise = mx > m;   // false while the row has seen nothing (mx = -inf)
         const float alpha = raise ? ex2_approx(m - mx) : 1.0f;   // m = -inf: 0
@@ -513,48 +569,91 @@ __device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, const AttendSm
             m = mx;
             l *= alpha;
         }
+        // PV i - 1 done: O, the P tile and the V tile are free
+        bool ok2 = true;
+        if (pv_iss != pv_ph) {
+            ok2 = tc_wait(&bars[1], pv_ph & 1);
+            ++pv_ph;
+            tc_fence_after_sync();
+        }
         if (i > 0 && __any_sync(0xFFFFFFFFu, raise)) {
-            // rescale the warp's output columns in place (PV i - 1 is done; alpha is 1 for the
-            // rows that keep their maximum)
             float ov[64];
             tmem_ld64(o_cols, ov);
 #pragma unroll
             for (int j = 0; j < 64; ++j) ov[j] *= alpha;
             tmem_st64(o_cols, ov);
         }
-        // this half of P as bf16; l sums the rounded weights the MMA uses
-        const float mb = m == -INFINITY ? 0.0f : m;
-        uint32_t hw[32];
+        if (mbar_wait_bounded(&cbar[2 + slot(i)], par(i))) v_done = i + 1;
+        else ok2 = false;
+        // this half of P as bf16 (l sums the rounded weights the MMA uses), interleaved with this
+        // thread's two (token, 32-dim group) items of V: item t + 256 k is token (t + 256 k) / 4,
+        // group t % 4; chunk q of an item is dims 32 g + 8 q .. + 7
+        const uint8_t* vr = k_raw(i) + page_bytes;
+        uint4 vw[2];
+        uint32_t vs1[2], vs2[2];
+        int vrow[2];
 #pragma unroll
-        for (int q2 = 0; q2 < 32; ++q2) {
-            const __nv_bfloat162 hb = __floats2bfloat162_rn(ex2_approx(z[2 * q2] - mb), ex2_approx(z[2 * q2 + 1] - mb));
-            const float2 hr = __bfloat1622float2(hb);
-            l += hr.x + hr.y;
-            hw[q2] = *reinterpret_cast<const uint32_t*>(&hb);
+        for (int k = 0; k < 2; ++k) {
+            const int it = (int)threadIdx.x + 256 * k;
+            vrow[k] = it >> 2;
+            vw[k] = *reinterpret_cast<const uint4*>(vr + vrow[k] * 64 + (it & 3) * 16);
+            v_scale_factors(vr[kMxScaleOff + it], vs1[k], vs2[k]);
         }
+        const float mb = m == -INFINITY ? 0.0f : m;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(p_tile + sw128_chunk(L.r, 8 * L.h + c, kTcRows)) =
-                make_uint4(hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
-        fence_proxy_async_smem();   // P (generic writes) before the MMA reads it
-        tc_fence_before_sync();     // the S and O accesses before the next MMAs
-        __syncthreads();
-        if (threadIdx.x == 0) {
+        for (int c = 0; c < 8; ++c) {
+            uint32_t hw[4];
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2) {
+                const __nv_bfloat162 hb =
+                    __floats2bfloat162_rn(ex2_approx(z[8 * c + 2 * q2] - mb), ex2_approx(z[8 * c + 2 * q2 + 1] - mb));
+                const float2 hr = __bfloat1622float2(hb);
+                l += hr.x + hr.y;
+                hw[q2] = *reinterpret_cast<const uint32_t*>(&hb);
+            }
+            *reinterpret_cast<uint4*>(p_tile + sw128_chunk(L.r, 8 * L.h + c, kTcRows)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            const int k = c >> 2, q = c & 3;
+            const int g = ((int)threadIdx.x + 256 * k) & 3;
+            const uint32_t w = q == 0 ? vw[k].x : q == 1 ? vw[k].y : q == 2 ? vw[k].z : vw[k].w;
+            const uint4 o = vrow[k] < valid_rows ? widen_v_chunk(w, vs1[k], vs2[k]) : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(v_tile + sw128_chunk(vrow[k], 4 * g + q, kTcRows)) = o;
+        }
+        fence_proxy_async_smem();   // P and V (generic writes) before the MMA reads them
+        tc_fence_before_sync();     // the O accesses before the next MMAs
+        if (__syncthreads_or(!ok2)) {
+            ok_all = false;
+            break;
+        }
+        if (threadIdx.x == 224) {
             tc_fence_after_sync();
             tc_mma_tile_bmn(tmem + kTcColO, smem_u32(p_tile), smem_u32(v_tile), i > 0);
             tc_commit(&bars[1]);
         }
-        pv_pending = true;
+        if (threadIdx.x == 32 && i + 2 < np)
+            mx_issue(raw, cbar, i + 2, true, selph[i + 2], gp, v_pool, Hkv, kvh, page_bytes);
+        ++pv_iss;
+        if (i + 2 < np) ++v_iss;
     }
-    if (pv_pending) {   // the last PV
-        const bool ok = tc_wait(&bars[1], pv_ph & 1);
+
+    // drain: every MMA committed and every copy issued completes before the tiles, the stage area
+    // or tensor memory are used again (bounded waits; a timeout is flagged)
+    bool ok3 = true;
+    while (pv_ph != pv_iss) {
+        ok3 = tc_wait(&bars[1], pv_ph & 1) && ok3;
         ++pv_ph;
-        tc_fence_after_sync();
-        if (!ok && threadIdx.x == 0) flag_status(status, SMX_DEV_TIMEOUT);
-        ok_all = ok_all && ok;
     }
+    while (qk_ph != qk_iss) {
+        ok3 = tc_wait(&bars[0], qk_ph & 1) && ok3;
+        ++qk_ph;
+    }
+    tc_fence_after_sync();
+    if (!ok_all && threadIdx.x == 0) {
+        for (int j = k_done; j < k_iss; ++j) mbar_wait_bounded(&cbar[slot(j)], par(j));
+        for (int j = v_done; j < v_iss; ++j) mbar_wait_bounded(&cbar[2 + slot(j)], par(j));
+    }
+    if ((!ok_all || !ok3) && threadIdx.x == 0) flag_status(status, SMX_DEV_TIMEOUT);
     gp += (uint32_t)np;
-    return __syncthreads_and(ok_all) != 0;
+    return __syncthreads_and(ok_all && ok3) != 0;
 }
 
 // Partials of this CTA's real rows for partition s: O from tensor-memory columns 128..255 (zero

@@ -116,20 +116,32 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(const floa
     merge_row<false>(part_o, part_m, part_l, (int64_t)b * S * QH + r, QH, S, out + (int64_t)row * kD);
 }
 
-int suggest_num_splits(const smx_shape_t& s) {
-    // attention units of up to 64 query rows of one KV head each, one CTA per SM
+// The largest S whose units of up to `rows` query rows (B x Hkv x row groups per partition) fill at
+// most one wave of `sms` CTAs, lowered so every partition holds the same number of selected pages.
+static int one_wave_splits(const smx_shape_t& s, int rows, int sms) {
     const int M = (s.Hq / s.Hkv) * s.Q;
-    const int row_warps = min(kAttnMaxWarps / 2, (M + 15) / 16);
-    const int ctas_per_split = s.B * s.Hkv * ((M + 16 * row_warps - 1) / (16 * row_warps));
+    const int per_split = s.B * s.Hkv * ((M + rows - 1) / rows);
+    const int s_max = max(1, sms / max(1, per_split));
+    const int pages_per_split = (s.topk + s_max - 1) / s_max;
+    return max(1, (s.topk + pages_per_split - 1) / pages_per_split);
+}
+
+int suggest_num_splits(const smx_shape_t& s) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
-    // one CTA per SM: one wave of split CTAs, then equal page counts per partition
-    const int s_max = max(1, sms / max(1, ctas_per_split));
-    const int pages_per_split = (s.topk + s_max - 1) / s_max;
-    return max(1, (s.topk + pages_per_split - 1) / pages_per_split);
+    // one CTA per SM: one wave of 64-row (mma.sync) units
+    const int M = (s.Hq / s.Hkv) * s.Q;
+    const int rows64 = 16 * min(kAttnMaxWarps / 2, (M + 15) / 16);
+    const int s_mma = one_wave_splits(s, rows64, sms);
+    // MXFP4 K/V with more than 64 query rows per KV head: when that wave leaves 3 or more selected
+    // pages per partition, one wave of 128-row tensor-core units (which the fused step then takes,
+    // the 64-row units needing more than one wave) is faster. Measured on GB300, whole step: 4 to 8
+    // pages per 64-row unit 10 to 26 % faster; at 2 pages about even, at 1 page mma.sync ahead.
+    if (s.kv_format == SMX_KV_MXFP4 && M > 64 && (s.topk + s_mma - 1) / s_mma >= 3) return one_wave_splits(s, 128, sms);
+    return s_mma;
 }
 
 cudaError_t launch_attn_split(const smx_shape_t& s, const void* q, const uint8_t* k_pool,

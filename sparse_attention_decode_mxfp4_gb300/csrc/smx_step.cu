@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
     __shared__ float red[kRedPages][kStepWarps];
     __shared__ int64_t phys_s[kStepMaxChunk];
     __shared__ SelectSmem selsm;
-    __shared__ __align__(8) uint64_t mbar[2];
+    __shared__ __align__(8) uint64_t mbar[4];   // page copies (tensor-core MXFP4: K slot 0, 1, V slot 0, 1)
     __shared__ __align__(8) uint64_t mbar_q;   // the first unit's q rows
     __shared__ int stage_page[2];
     __shared__ int is_last;
@@ -120,6 +120,8 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
     if (threadIdx.x == 0) {
         mbar_init(&mbar[0], 1);
         mbar_init(&mbar[1], 1);
+        mbar_init(&mbar[2], 1);
+        mbar_init(&mbar[3], 1);
         mbar_init(&mbar_q, 1);
         mbar_init(&mbar_mma[0], 1);
         mbar_init(&mbar_mma[1], 1);
@@ -385,8 +387,15 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
             if (threadIdx.x == 0 && copies_ok) {
                 fence_proxy_async_global();
                 fence_proxy_async_smem();
-                for (int i = 0; i < 2 && i < hi - lo; ++i)
-                    attend_issue(sm, i, sel_all[lo + i], resolve(i), gp, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes);
+                for (int i = 0; i < 2 && i < hi - lo; ++i) {
+                    if constexpr (RS) {
+                        attend_issue(sm, i, sel_all[lo + i], resolve(i), gp, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes);
+                    } else {
+                        const int ph = resolve(i);
+                        mx_issue(sm.raw, mbar, i, false, ph, gp, a.k_pool, a.Hkv, kvh, a.page_bytes);
+                        mx_issue(sm.raw, mbar, i, true, ph, gp, a.v_pool, a.Hkv, kvh, a.page_bytes);
+                    }
+                }
             }
             for (int i = 2 + threadIdx.x; i < hi - lo; i += blockDim.x) resolve(i);
             if (kvh == 0 && rg == 0 && s == 0) {
@@ -404,9 +413,9 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
                                                     a.page_bytes, ctx, tmem, &mbar_mma[0], mma_ph, L, xch_tc, gp, m_run, l,
                                                     a.status);
                 else
-                    copies_ok = attend_pages_tc_mx(smem, sm, sel, selph, hi - lo, a.k_pool, a.v_pool, a.Hkv, kvh,
-                                                   a.page_bytes, ctx, tmem, mbar_mma, mma_ph, pv_ph, L, xch_tc, gp, m_run,
-                                                   l, a.status);
+                    copies_ok = attend_pages_tc_mx(smem, sm.raw, mbar, sel, selph, hi - lo, a.k_pool, a.v_pool, a.Hkv,
+                                                   kvh, a.page_bytes, ctx, tmem, mbar_mma, mma_ph, pv_ph, L, xch_tc, gp,
+                                                   m_run, l, a.status);
             }
             finish_partials_tc(L, tmem, run, m_run, l, xch_tc, a.part_o, a.part_m, a.part_l, b, s, kvh, a.S, a.Q, a.Hq, a.G,
                                m_lo);

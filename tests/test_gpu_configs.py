@@ -108,6 +108,19 @@ def test_tensor_core_attention_multi_page(kv_format, Q, big):
     C.full_step_parity(w)
 
 
+def test_suggestion_takes_the_tensor_cores_for_many_pages():
+    # 8 rows x 128 query rows, k = 64: one wave of 64-row units leaves 8 pages per partition, so
+    # the suggested S is one wave of 128-row units (4 pages each), on the tensor cores
+    w = wl.Workload("many_pages", B=8, Q=8, Hq=16, Hkv=1, max_ctx=16384, topk=64, num_splits=1, seed=616,
+                    ragged=True)
+    S = ops.suggest_num_splits(ops.Shape.of(w, 1))
+    shape = ops.Shape.of(w, S)
+    assert ops.decode_step_tensor_cores(shape)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert w.B * w.Hkv * S <= sms
+    C.full_step_parity(w, num_splits=S)
+
+
 def test_configs_take_the_mma_path():
     # the benchmark workloads at the suggested partition counts fit one wave of 64-row units
     for c in (2, 3, 4):
