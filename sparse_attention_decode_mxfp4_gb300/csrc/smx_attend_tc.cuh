@@ -16,7 +16,8 @@
 //  2. Meanwhile V is widened to bf16 row by row ([token][dim], read by the PV MMA as an MN-major
 //     operand; token rows past the context are zero, so poisoned slots never reach an MMA).
 //  3. Each thread reads its 64 scores with one tensor-memory load, masks them, exchanges the half
-//     maximum with its partner thread, and writes its half of P as bf16. The running maximum
+//     maximum with its partner thread, and writes its half of P as bf16 (the PV MMA sums the
+//     weights it uses, against a column of ones appended to V: N = 144). The running maximum
 //     follows the row maximum exactly, so the largest weight is exactly 1 (a maximum that lags by
 //     up to 8 would leave every weight rounded: on rows scaled x50 that alone breaks the output
 //     bound); O is rescaled in tensor memory when a row's maximum grows.
@@ -40,13 +41,17 @@ constexpr int kTcQ = 0;             // q tile [128 rows][128 dims]: e4m3 (MXFP4)
 constexpr int kTcK = 32768;         // K tile [128 tokens][128 dims]: fp4 operand (MXFP4), bf16 (FP8-KV,
                                     // then the P low part)
 constexpr int kTcV = 65536;         // V tile, bf16: [token][dim] (MXFP4), [dim][token] (FP8-KV)
-constexpr int kTcP = 98304;         // P tile [128 rows][128 tokens]
+constexpr int kTcP = 98304;         // P tile [128 rows][128 tokens] (FP8-KV); MXFP4: V's third block
+constexpr int kTcMxP0 = 16384;      // MXFP4 P tile, tokens 0..63 [128 rows][64] (after the e4m3 q tile)
+constexpr int kTcMxP1 = 49152;      // MXFP4 P tile, tokens 64..127 (after the fp4 K tile)
 constexpr int kTcScale = 131072;    // 128 K row scales, 128 V row scales (FP8-KV)
 constexpr int kTcRaw = 132096;      // two stages of (K page, V page)
 constexpr uint32_t kTcCols = 512;   // tensor-memory columns allocated
-constexpr uint32_t kTcColO = 128;   // S at column 0, O at 128
-constexpr uint32_t kTcColSFA = 256; // the A (q) scale block: 0x7F (2^0) in every byte
-constexpr uint32_t kTcColSFB = 264; // the B (K page) scale block
+constexpr uint32_t kTcColO = 128;   // S at column 0, O at 128 (MXFP4: 144 columns, the last 16 from
+                                    // V's column of ones: column 256 is the row's weight sum l)
+constexpr uint32_t kTcColSFA = 288; // the A (q) scale block: 0x7F (2^0) in every byte
+constexpr uint32_t kTcColSFB = 296; // the B (K page) scale block
+constexpr int kTcMxN = 144;         // MXFP4 PV: 128 V dims + 16 (a column of ones, then zeros)
 constexpr int kTcRows = 128;        // query rows per CTA
 
 __host__ __device__ constexpr size_t attend_tc_smem_bytes(int page_bytes) {
@@ -472,13 +477,15 @@ __device__ __forceinline__ uint4 widen_v_chunk(uint32_t w, uint32_t s1, uint32_t
 // holds e4m3 codes; the A scale block (column kTcColSFA) holds 0x7F in every byte. cbar: copy
 // barriers [K slot 0, K slot 1, V slot 0, V slot 1]; bars[0] counts QK completions (qk_ph phases
 // seen), bars[1] PV completions (pv_ph). Per page i, with two CTA barriers:
-//   (QK i was issued during page i - 1) S i is read and masked; K i + 1 is repacked (QK i is
-//   done, so the K tile and B scale block are free); barrier B; thread 0 issues QK i + 1 and the
+//   (QK i was issued during page i - 1) K i + 1 is repacked (QK i is done, so the K tile and B
+//   scale block are free; PV i - 1 may still run) and S i is read and masked; barrier B; thread 0 issues QK i + 1 and the
 //   K copy of page i + 3; the row maxima are combined, PV i - 1 is waited for, O is rescaled,
 //   and P i (ex2) is written interleaved with the widening of V i (ALU and conversion pipes);
+//   the PV MMA (N = 144) also sums the bf16 weights, against V's column of ones;
 //   barrier C; thread 224 issues PV i, thread 32 the V copy of page i + 2.
-// m: the row's running maximum (log2 domain); l: this half's share of the row's weight sum.
-// Returns false (every thread alike) if a copy or an MMA did not finish within the bounded wait
+// m: the row's running maximum (log2 domain). l: on return, the row's weight sum relative to 2^m
+// (column 128 of O, from V's column of ones) in the h = 0 thread, 0 in the other (as the FP8-KV
+// loop's halves, which the partials add). Returns false (every thread alike) if a copy or an MMA did not finish within the bounded wait
 // (status gets SMX_DEV_TIMEOUT); O is then incomplete.
 __device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, uint8_t* raw, uint64_t* cbar, const int* sel,
                                                    const int* selph, int np, const uint8_t* k_pool,
@@ -489,10 +496,18 @@ __device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, uint8_t* raw, 
     uint8_t* q_tile = smem + kTcQ;
     uint8_t* k_tile = smem + kTcK;
     uint8_t* v_tile = smem + kTcV;
-    uint8_t* p_tile = smem + kTcP;
+    uint8_t* p_half = smem + (L.h ? kTcMxP1 : kTcMxP0);   // this thread's half of the P tile
     const uint32_t lane_base = tmem + ((uint32_t)(L.r & ~31) << 16);   // this warp's 32 lanes
     const uint32_t s_cols = lane_base + 64 * L.h;
     const uint32_t o_cols = lane_base + kTcColO + 64 * L.h;
+    const uint32_t l_col = lane_base + kTcColO + 128;   // O's column 128: the row's weight sum
+    // V's third 64-dim block: dim 128 is 1 for every token, dims 129..143 are 0 (read by the PV
+    // MMA as N = 144, so the MMA sums the bf16 weights it multiplies)
+    {
+        const int t = threadIdx.x >> 1, j = threadIdx.x & 1;
+        *reinterpret_cast<uint4*>(v_tile + sw128_chunk(t, 16 + j, kTcRows)) =
+            make_uint4(j == 0 ? 0x3F80u : 0u, 0u, 0u, 0u);
+    }
     auto slot = [&](int i) { return (int)((gp + i) & 1); };
     auto par = [&](int i) { return (uint32_t)(((gp + i) >> 1) & 1); };
     auto k_raw = [&](int i) { return raw + slot(i) * 2 * page_bytes; };
@@ -525,25 +540,27 @@ __device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, uint8_t* raw, 
         const int p = selph[i] >= 0 ? sel[i] : -1;
         const int valid_rows = p >= 0 ? min(kPage, ctx - p * kPage) : 0;
         const int jpage = p >= 0 ? p * kPage : 0;
-        // S i: scaled to the log2 domain, masked past the context and causally
-        ok = tc_wait(&bars[0], qk_ph & 1);
+        ok = tc_wait(&bars[0], qk_ph & 1);   // QK i
         ++qk_ph;
         tc_fence_after_sync();
-        float z[64];
-        tmem_ld64(s_cols, z);
-        const int lim = L.valid ? min(valid_rows, L.pos - jpage + 1) - 64 * L.h : 0;
-        float mx = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-            z[j] = j < lim ? z[j] * kLog2eOverSqrtD : -INFINITY;
-            mx = fmaxf(mx, z[j]);
-        }
-        // K i + 1 (QK i is done: the K tile and the B scale block are free)
+        // K i + 1 first (QK i is done: the K tile and the B scale block are free): it needs no
+        // tensor-memory read, so it runs while PV i - 1 still occupies tensor memory
         if (i + 1 < np) {
             if (mbar_wait_bounded(&cbar[slot(i + 1)], par(i + 1))) k_done = i + 2;
             else ok = false;
             repack_k_mx_tc(k_raw(i + 1), k_tile, tmem);
         }
+        // S i: scaled to the log2 domain, masked past the context and causally
+        float z[64];   // raw q.k; the log2-domain scale is applied with the maximum below
+        tmem_ld64(s_cols, z);
+        const int lim = L.valid ? min(valid_rows, L.pos - jpage + 1) - 64 * L.h : 0;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+            z[j] = j < lim ? z[j] : -INFINITY;
+            mx = fmaxf(mx, z[j]);
+        }
+        mx *= kLog2eOverSqrtD;
         xch[threadIdx.x] = mx;
         fence_proxy_async_smem();
         tc_fence_before_sync();   // S i read; the B scale block written
@@ -565,10 +582,7 @@ __device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, uint8_t* raw, 
         mx = fmaxf(mx, xch[threadIdx.x ^ 128]);   // the partner thread holds the other half of the row
         const bool raise = mx > m;   // false while the row has seen nothing (mx = -inf)
         const float alpha = raise ? ex2_approx(m - mx) : 1.0f;   // m = -inf: 0
-        if (raise) {
-            m = mx;
-            l *= alpha;
-        }
+        if (raise) m = mx;
         // PV i - 1 done: O, the P tile and the V tile are free
         bool ok2 = true;
         if (pv_iss != pv_ph) {
@@ -582,6 +596,7 @@ __device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, uint8_t* raw, 
 #pragma unroll
             for (int j = 0; j < 64; ++j) ov[j] *= alpha;
             tmem_st64(o_cols, ov);
+            if (L.h) tmem_st1(l_col, tmem_ld1(l_col) * alpha);   // warp-uniform: h is the warp's half
         }
         if (mbar_wait_bounded(&cbar[2 + slot(i)], par(i))) v_done = i + 1;
         else ok2 = false;
@@ -599,19 +614,17 @@ __device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, uint8_t* raw, 
             vw[k] = *reinterpret_cast<const uint4*>(vr + vrow[k] * 64 + (it & 3) * 16);
             v_scale_factors(vr[kMxScaleOff + it], vs1[k], vs2[k]);
         }
-        const float mb = m == -INFINITY ? 0.0f : m;
+        const float nmb = m == -INFINITY ? 0.0f : -m;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             uint32_t hw[4];
 #pragma unroll
             for (int q2 = 0; q2 < 4; ++q2) {
-                const __nv_bfloat162 hb =
-                    __floats2bfloat162_rn(ex2_approx(z[8 * c + 2 * q2] - mb), ex2_approx(z[8 * c + 2 * q2 + 1] - mb));
-                const float2 hr = __bfloat1622float2(hb);
-                l += hr.x + hr.y;
-                hw[q2] = *reinterpret_cast<const uint32_t*>(&hb);
+                const float e0 = ex2_approx(fmaf(z[8 * c + 2 * q2], kLog2eOverSqrtD, nmb));
+                const float e1 = ex2_approx(fmaf(z[8 * c + 2 * q2 + 1], kLog2eOverSqrtD, nmb));
+                hw[q2] = f32x2_to_bf16x2(e0, e1);
             }
-            *reinterpret_cast<uint4*>(p_tile + sw128_chunk(L.r, 8 * L.h + c, kTcRows)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(p_half + sw128_chunk(L.r, c, kTcRows)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             const int k = c >> 2, q = c & 3;
             const int g = ((int)threadIdx.x + 256 * k) & 3;
             const uint32_t w = q == 0 ? vw[k].x : q == 1 ? vw[k].y : q == 2 ? vw[k].z : vw[k].w;
@@ -626,7 +639,8 @@ __device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, uint8_t* raw, 
         }
         if (threadIdx.x == 224) {
             tc_fence_after_sync();
-            tc_mma_tile_bmn(tmem + kTcColO, smem_u32(p_tile), smem_u32(v_tile), i > 0);
+            tc_mma_tile_bmn(tmem + kTcColO, smem_u32(smem + kTcMxP0), smem_u32(smem + kTcMxP1), smem_u32(v_tile), kTcMxN,
+                            i > 0);
             tc_commit(&bars[1]);
         }
         if (threadIdx.x == 32 && i + 2 < np)
@@ -652,6 +666,9 @@ __device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, uint8_t* raw, 
         for (int j = v_done; j < v_iss; ++j) mbar_wait_bounded(&cbar[2 + slot(j)], par(j));
     }
     if ((!ok_all || !ok3) && threadIdx.x == 0) flag_status(status, SMX_DEV_TIMEOUT);
+    // the row's weight sum, from the MMA: held by the h = 0 thread (the partner's share is 0)
+    const float l_row = tmem_ld1(l_col);
+    l = L.h ? 0.0f : l_row;
     gp += (uint32_t)np;
     return __syncthreads_and(ok_all && ok3) != 0;
 }

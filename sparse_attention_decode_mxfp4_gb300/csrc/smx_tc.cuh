@@ -224,13 +224,15 @@ __device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr) {
     return d;
 }
 
-// D[128 x 128] (+)= A[128 x 128] . B[128 x 128]: A K-major (the tile at a_s, as tc_mma_tile), B
-// MN-major [k][n] at b_s (each 16-row K step is two atoms, 2048 B). One thread; no commit.
-__device__ __forceinline__ void tc_mma_tile_bmn(uint32_t d_tmem, uint32_t a_s, uint32_t b_s, bool accumulate) {
-    constexpr uint32_t idesc = idesc_bf16(128, 128) | (1u << 16);   // B MN-major
+// D[128 x N] (+)= A[128 x 128] . B[128 x N]: A K-major, its two 64-element K blocks at a_lo and
+// a_hi (each [128 rows][64], 8-row atoms 1024 B apart), B MN-major [k][n] at b_s (sw128_desc_mn;
+// each 16-row K step is two atoms, 2048 B). N a multiple of 16, at most 192. One thread; no commit.
+__device__ __forceinline__ void tc_mma_tile_bmn(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_s, int N,
+                                                bool accumulate) {
+    const uint32_t idesc = idesc_bf16(128, N) | (1u << 16);   // B MN-major
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const uint64_t ad = sw128_desc(a_s + (k >> 2) * 128 * 128 + (k & 3) * 32);
+        const uint64_t ad = sw128_desc((k < 4 ? a_lo : a_hi) + (k & 3) * 32);
         const uint64_t bd = sw128_desc_mn(b_s + 2048 * k);
         const uint32_t acc = (accumulate || k > 0) ? 1u : 0u;
         asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
@@ -238,6 +240,21 @@ __device__ __forceinline__ void tc_mma_tile_bmn(uint32_t d_tmem, uint32_t a_s, u
                      "r"(idesc), "r"(acc)
                      : "memory");
     }
+}
+
+// One fp32 column of this thread's lane (waits for the load).
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n tcgen05.wait::ld.sync.aligned;" : "=r"(r) : "r"(taddr)
+                 : "memory");
+    return __uint_as_float(r);
+}
+
+// Store one fp32 column of this thread's lane (waits for the store).
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+                 "r"(__float_as_uint(v))
+                 : "memory");
 }
 
 }  // namespace smx

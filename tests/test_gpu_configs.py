@@ -121,6 +121,20 @@ def test_suggestion_takes_the_tensor_cores_for_many_pages():
     C.full_step_parity(w, num_splits=S)
 
 
+SUGGESTED = [c for c in wl.sweep_cases() if c.Q == 8 and c.Hq == 16 and c.topk == 128]
+
+
+@pytest.mark.parametrize("case", SUGGESTED, ids=[c.name for c in SUGGESTED])
+def test_sweep_at_suggested_splits(case):
+    # the sweep's largest cases (128 query rows, k = 128) at the partition count the library
+    # suggests: with B >= 2 one wave of 64-row units would hold 4 or more pages each, so these run
+    # the tensor-core attention
+    S = ops.suggest_num_splits(ops.Shape.of(case, 1))
+    if case.B >= 2:
+        assert ops.decode_step_tensor_cores(ops.Shape.of(case, S))
+    C.full_step_parity(case, num_splits=S)
+
+
 def test_configs_take_the_mma_path():
     # the benchmark workloads at the suggested partition counts fit one wave of 64-row units
     for c in (2, 3, 4):
