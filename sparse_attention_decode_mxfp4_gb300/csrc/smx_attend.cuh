@@ -13,10 +13,12 @@
 // the context so poisoned slots never reach an MMA, with a 16-byte XOR swizzle that keeps
 // ldmatrix conflict-free. Warp (half h, group w) owns 16 rows and 64 tokens of every page, in
 // 16-token units: QK (fp32), mask, online softmax in the log2 domain (rescale only when a row's
-// maximum grows), then the weights -- bf16 for MXFP4; for the FP8-KV format p times the V row
-// scale as a bf16 high part plus a bf16 low part, so the weights keep ~16 significant bits --
-// multiplied into V (the accumulator layout of QK is the A layout of PV). The two token halves
-// are combined in shared memory at the end.
+// maximum grows), then the weights -- p (FP8-KV: p times the V row scale) as a bf16 high part
+// plus a bf16 low part, so they keep ~16 significant bits -- multiplied into V (the accumulator
+// layout of QK is the A layout of PV). The pages keep P in bf16 alone; that is the reading kept
+// here only for the high part: when a few tokens share a row's mass, one bf16 rounding of their
+// weights moves outputs near zero by ~2^-9 |v_i - v_j|, the size of the output bound. The two
+// token halves are combined in shared memory at the end.
 #pragma once
 
 #include <math.h>
@@ -401,7 +403,9 @@ __device__ __forceinline__ bool attend_pages(const AttendSmem& sm, const int* se
                 mrow0 = mn0;
                 mrow1 = mn1;
             }
-            // weights; l (per lane, reduced at the end) sums the weights the PV product uses
+            // weights as a bf16 high part plus a bf16 low part (~16 significant bits: bf16 alone
+            // moves outputs near zero by up to ~2^-9 |v_i - v_j| when a few tokens share the
+            // mass, the size of the output bound); l (per lane, reduced at the end) sums them
             uint32_t ph[2][2], pl[2][2];
 #pragma unroll
             for (int nb = 0; nb < 2; ++nb) {
@@ -411,27 +415,21 @@ __device__ __forceinline__ bool attend_pages(const AttendSmem& sm, const int* se
                     const float mn = (c < 2) ? mrow0 : mrow1;
                     e[c] = (mn == -INFINITY) ? 0.0f : exp2f(sc[nb][c] - mn);
                 }
+                l0 += e[0] + e[1];
+                l1 += e[2] + e[3];
                 if (RS) {
-                    l0 += e[0] + e[1];
-                    l1 += e[2] + e[3];
                     const int tok = tok0 + nb * 8 + 2 * t;
                     const float s0 = sm.vscale[tok], s1 = sm.vscale[tok + 1];
                     e[0] *= s0; e[1] *= s1; e[2] *= s0; e[3] *= s1;
                 }
                 const __nv_bfloat162 h01 = __floats2bfloat162_rn(e[0], e[1]), h23 = __floats2bfloat162_rn(e[2], e[3]);
                 const float2 r01 = __bfloat1622float2(h01), r23 = __bfloat1622float2(h23);
-                if (!RS) {
-                    l0 += r01.x + r01.y;
-                    l1 += r23.x + r23.y;
-                }
                 ph[nb][0] = *reinterpret_cast<const uint32_t*>(&h01);
                 ph[nb][1] = *reinterpret_cast<const uint32_t*>(&h23);
-                if (RS) {
-                    const __nv_bfloat162 l01 = __floats2bfloat162_rn(e[0] - r01.x, e[1] - r01.y);
-                    const __nv_bfloat162 l23 = __floats2bfloat162_rn(e[2] - r23.x, e[3] - r23.y);
-                    pl[nb][0] = *reinterpret_cast<const uint32_t*>(&l01);
-                    pl[nb][1] = *reinterpret_cast<const uint32_t*>(&l23);
-                }
+                const __nv_bfloat162 l01 = __floats2bfloat162_rn(e[0] - r01.x, e[1] - r01.y);
+                const __nv_bfloat162 l23 = __floats2bfloat162_rn(e[2] - r23.x, e[3] - r23.y);
+                pl[nb][0] = *reinterpret_cast<const uint32_t*>(&l01);
+                pl[nb][1] = *reinterpret_cast<const uint32_t*>(&l23);
             }
             // O += P V for these 16 tokens
 #pragma unroll
@@ -440,10 +438,8 @@ __device__ __forceinline__ bool attend_pages(const AttendSmem& sm, const int* se
                 ldmatrix_x4_trans(b0, b1, b2, b3, sm.Vs + swz(tok0 + ((lane >> 3) & 1) * 8 + (lane & 7), db + (lane >> 4)));
                 mma_bf16_16816(o[db], ph[0][0], ph[0][1], ph[1][0], ph[1][1], b0, b1);
                 mma_bf16_16816(o[db + 1], ph[0][0], ph[0][1], ph[1][0], ph[1][1], b2, b3);
-                if (RS) {
-                    mma_bf16_16816(o[db], pl[0][0], pl[0][1], pl[1][0], pl[1][1], b0, b1);
-                    mma_bf16_16816(o[db + 1], pl[0][0], pl[0][1], pl[1][0], pl[1][1], b2, b3);
-                }
+                mma_bf16_16816(o[db], pl[0][0], pl[0][1], pl[1][0], pl[1][1], b0, b1);
+                mma_bf16_16816(o[db + 1], pl[0][0], pl[0][1], pl[1][0], pl[1][1], b2, b3);
             }
         }
         __syncthreads();   // before the next page overwrites the tiles

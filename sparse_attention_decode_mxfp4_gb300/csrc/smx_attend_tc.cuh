@@ -16,13 +16,15 @@
 //  2. Meanwhile V is widened to bf16 row by row ([token][dim], read by the PV MMA as an MN-major
 //     operand; token rows past the context are zero, so poisoned slots never reach an MMA).
 //  3. Each thread reads its 64 scores with one tensor-memory load, masks them, exchanges the half
-//     maximum with its partner thread, and writes its half of P as bf16 (the PV MMA sums the
-//     weights it uses, against a column of ones appended to V: N = 144). The running maximum
+//     maximum with its partner thread, and writes its half of P as a bf16 high part and a bf16
+//     low part (~16 significant bits; two PV passes; the PV MMAs also sum the weights they use,
+//     against a column of ones appended to V: N = 144). The running maximum
 //     follows the row maximum exactly, so the largest weight is exactly 1 (a maximum that lags by
 //     up to 8 would leave every weight rounded: on rows scaled x50 that alone breaks the output
 //     bound); O is rescaled in tensor memory when a row's maximum grows.
-//  4. One thread issues O += P V (eight MMAs) into columns 128..255; the next page's K copy and QK
-//     go ahead while it runs, and V / P are rewritten only after it completes.
+//  4. One thread issues O += P_hi V + P_lo V (sixteen MMAs) into columns 128..271; the next
+//     page's K copy and QK go ahead while it runs, and V / P are rewritten only after it
+//     completes.
 //
 // FP8-KV (attend_pages_tc): K widened to bf16 and V transposed into [dim][token] tiles, both
 // K-major; QK and PV as bf16 MMAs; p times the V row scale as a bf16 high part and low part.
@@ -45,7 +47,10 @@ constexpr int kTcP = 98304;         // P tile [128 rows][128 tokens] (FP8-KV); M
 constexpr int kTcMxP0 = 16384;      // MXFP4 P tile, tokens 0..63 [128 rows][64] (after the e4m3 q tile)
 constexpr int kTcMxP1 = 49152;      // MXFP4 P tile, tokens 64..127 (after the fp4 K tile)
 constexpr int kTcScale = 131072;    // 128 K row scales, 128 V row scales (FP8-KV)
-constexpr int kTcRaw = 132096;      // two stages of (K page, V page)
+constexpr int kTcRaw = 132096;      // two stages of (K page, V page) (FP8-KV)
+constexpr int kTcMxPL0 = 114688;    // MXFP4 P low part, tokens 0..63 (after V's third block)
+constexpr int kTcMxPL1 = 131072;    // MXFP4 P low part, tokens 64..127
+constexpr int kTcMxRaw = 147456;    // MXFP4: two stages of (K page, V page)
 constexpr uint32_t kTcCols = 512;   // tensor-memory columns allocated
 constexpr uint32_t kTcColO = 128;   // S at column 0, O at 128 (MXFP4: 144 columns, the last 16 from
                                     // V's column of ones: column 256 is the row's weight sum l)
@@ -55,7 +60,7 @@ constexpr int kTcMxN = 144;         // MXFP4 PV: 128 V dims + 16 (a column of on
 constexpr int kTcRows = 128;        // query rows per CTA
 
 __host__ __device__ constexpr size_t attend_tc_smem_bytes(int page_bytes) {
-    return (size_t)kTcRaw + 4 * (size_t)page_bytes;
+    return (size_t)(page_bytes == kMxPageBytes ? kTcMxRaw : kTcRaw) + 4 * (size_t)page_bytes;
 }
 
 // The q tile from `rows` query rows (rows past them are zero). MXFP4 K/V: e4m3 codes by the q
@@ -496,7 +501,8 @@ __device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, uint8_t* raw, 
     uint8_t* q_tile = smem + kTcQ;
     uint8_t* k_tile = smem + kTcK;
     uint8_t* v_tile = smem + kTcV;
-    uint8_t* p_half = smem + (L.h ? kTcMxP1 : kTcMxP0);   // this thread's half of the P tile
+    uint8_t* p_half = smem + (L.h ? kTcMxP1 : kTcMxP0);    // this thread's half of the P tile
+    uint8_t* pl_half = smem + (L.h ? kTcMxPL1 : kTcMxPL0); // and of its low part
     const uint32_t lane_base = tmem + ((uint32_t)(L.r & ~31) << 16);   // this warp's 32 lanes
     const uint32_t s_cols = lane_base + 64 * L.h;
     const uint32_t o_cols = lane_base + kTcColO + 64 * L.h;
@@ -617,14 +623,16 @@ __device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, uint8_t* raw, 
         const float nmb = m == -INFINITY ? 0.0f : -m;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            uint32_t hw[4];
+            uint32_t hw[4], lw[4];
 #pragma unroll
             for (int q2 = 0; q2 < 4; ++q2) {
                 const float e0 = ex2_approx(fmaf(z[8 * c + 2 * q2], kLog2eOverSqrtD, nmb));
                 const float e1 = ex2_approx(fmaf(z[8 * c + 2 * q2 + 1], kLog2eOverSqrtD, nmb));
                 hw[q2] = f32x2_to_bf16x2(e0, e1);
+                lw[q2] = f32x2_to_bf16x2(e0 - __uint_as_float(hw[q2] << 16), e1 - __uint_as_float(hw[q2] & 0xFFFF0000u));
             }
             *reinterpret_cast<uint4*>(p_half + sw128_chunk(L.r, c, kTcRows)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(pl_half + sw128_chunk(L.r, c, kTcRows)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             const int k = c >> 2, q = c & 3;
             const int g = ((int)threadIdx.x + 256 * k) & 3;
             const uint32_t w = q == 0 ? vw[k].x : q == 1 ? vw[k].y : q == 2 ? vw[k].z : vw[k].w;
@@ -641,6 +649,8 @@ __device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, uint8_t* raw, 
             tc_fence_after_sync();
             tc_mma_tile_bmn(tmem + kTcColO, smem_u32(smem + kTcMxP0), smem_u32(smem + kTcMxP1), smem_u32(v_tile), kTcMxN,
                             i > 0);
+            tc_mma_tile_bmn(tmem + kTcColO, smem_u32(smem + kTcMxPL0), smem_u32(smem + kTcMxPL1), smem_u32(v_tile), kTcMxN,
+                            true);
             tc_commit(&bars[1]);
         }
         if (threadIdx.x == 32 && i + 2 < np)

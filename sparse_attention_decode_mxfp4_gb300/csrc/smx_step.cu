@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
     int* sel_all;
     uint8_t* q_stage;
     if constexpr (TC) {
-        sm.raw = smem + kTcRaw;
+        sm.raw = smem + (RS ? kTcRaw : kTcMxRaw);
         sm.mbar = mbar;
         sm.stage_page = stage_page;
         keys = reinterpret_cast<uint32_t*>(smem + kTcK);

@@ -8,6 +8,7 @@ import torch
 from sparse_attention_decode_mxfp4_gb300 import ops
 from sparse_attention_decode_mxfp4_gb300 import workloads as wl
 from tests import gpu_common as C
+from tests import helpers as H
 
 pytestmark = pytest.mark.gpu
 
@@ -94,14 +95,14 @@ def test_tensor_core_attention_path(kv_format):
 
 
 @pytest.mark.parametrize("kv_format,Q,big", [(wl.KV_MXFP4, 8, 0.0), (wl.KV_MXFP4, 8, 0.01), (wl.KV_MXFP4, 16, 0.0),
-                                          (wl.KV_E4M3_ROWSCALE, 8, 0.01)])
+                                          (wl.KV_MXFP4, 16, 0.01), (wl.KV_E4M3_ROWSCALE, 8, 0.01)])
 def test_tensor_core_attention_multi_page(kv_format, Q, big):
     # 20 rows x (2 or 4) groups of 64 query rows x 4 partitions = 160 or 320 mma.sync units: the
     # tensor-core path, with 8 pages per partition (ragged rows: fewer), so the page loop runs
     # several pages per unit and rescales O whenever a row's maximum grows; rows scaled x50 (big)
-    # make the maxima jump. (MXFP4 weights are bf16: with x50 rows the attention concentrates on a
-    # few tokens and bf16 rounding of their weights alone -- exact scores and V -- reaches 1.14x the
-    # output bound on the Q = 16 case, 0.67x on Q = 8; the FP8-KV weights carry a low part.)
+    # make the maxima jump and concentrate the attention on a few tokens (with bf16 weights alone,
+    # exact scores and V, the Q = 16 case reaches 1.14x the output bound: the weights carry a
+    # bf16 low part)
     w = wl.Workload("tc_pages", B=20, Q=Q, Hq=16, Hkv=1, max_ctx=6000, topk=32, num_splits=4, seed=515,
                     ragged=True, kv_format=kv_format, big_row_frac=big)
     assert _uses_tc(w)
@@ -133,6 +134,38 @@ def test_sweep_at_suggested_splits(case):
     if case.B >= 2:
         assert ops.decode_step_tensor_cores(ops.Shape.of(case, S))
     C.full_step_parity(case, num_splits=S)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(Q=5, Hq=16, max_ctx=3000, topk=8, num_splits=12),                     # 80 rows: a partial 128-row unit
+    dict(Q=8, Hq=32, Hkv=2, max_ctx=3000, topk=8, num_splits=12, B=4),         # GQA: two KV heads of 128 rows
+    dict(Q=8, Hq=16, max_ctx=3000, topk=4, num_splits=24),                     # more partitions than pages
+    dict(Q=8, Hq=16, max_ctx=8, ctx_lens=(8,) * 8, topk=2, num_splits=12),     # ctx == Q: one partial page
+    dict(Q=8, Hq=16, max_ctx=136, ctx_lens=(136,) * 8, topk=2, num_splits=12),  # the new tokens on page 2
+])
+def test_tensor_core_edge_cases(kw):
+    # shapes whose 64-row units exceed one wave, so the step runs the tensor-core attention
+    base = dict(name="tc_edge", B=8, Hkv=1, seed=5151, ragged=True)
+    base.update(kw)
+    if "ctx_lens" in base:
+        base["ragged"] = False
+    w = wl.Workload(**base)
+    assert _uses_tc(w)
+    C.full_step_parity(w)
+
+
+def test_tensor_core_bad_page_ids_are_flagged_and_skipped():
+    w = wl.Workload("tc_bad_ids", B=8, Q=8, Hq=16, Hkv=1, max_ctx=3000, topk=8, num_splits=12, seed=77, ragged=True)
+    assert _uses_tc(w)
+    data = wl.generate(w)
+    pools = H.oracle_pools(w, data)
+    bad = dict(data)
+    bad["page_table"] = data["page_table"].copy()
+    bad["page_table"][0, 0] = w.n_pool_pages + 5
+    bad["page_table"][1, 1] = -1
+    got = C.gpu_step(w, bad, pools)
+    assert got["status"] & ops.DEV_BAD_PAGE_ID
+    assert np.all(np.isfinite(got["out"]))
 
 
 def test_configs_take_the_mma_path():
