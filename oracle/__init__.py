@@ -104,6 +104,7 @@ def lib():
             "orc_sparse_attn_split": (None, [S, P, P, P, P, P, P, P, P, P, P]),
             "orc_sparse_attn_merge": (None, [S, P, P, P, P]),
             "orc_decode_step": (None, [S] + [P] * 19),
+            "orc_decode_step_reuse": (None, [S] + [P] * 15),
             "orc_set_threads": (None, [ctypes.c_int]),
             "orc_max_threads": (ctypes.c_int, []),
         }
@@ -293,6 +294,41 @@ def decode_step(sh: Shape, *, q_f32=None, q_bf16=None, qidx_bf16, k_new, v_new, 
                           _p(v_pool), _p(idx_pool), _p(scores), _p(pages), _p(count), _p(q8),
                           _p(po), _p(pm), _p(pl), _p(out))
     res = dict(scores=scores, topk_pages=pages, topk_count=count, out=out)
+    if sh.kv_format != KV_E4M3_ROWSCALE:
+        res["q_e4m3"] = q8
+    if want_partials:
+        res.update(part_o=po, part_m=pm, part_l=pl)
+    return res
+
+
+
+def decode_step_reuse(sh: Shape, *, q_f32=None, q_bf16=None, k_new, v_new, page_table, ctx_len,
+                      k_pool, v_pool, topk_pages, topk_count, want_partials=False):
+    """The step of a layer reusing an earlier layer's selection: K/V insert (the K and V pools
+    updated in place; no index cache), q packing, split over (topk_pages, topk_count) as given,
+    merge. Returns a dict with q_e4m3 (MXFP4 K/V only), out and, if asked, the partials."""
+    q_f32 = None if q_f32 is None else _c(q_f32, np.float32)
+    q_bf16 = None if q_bf16 is None else _c(q_bf16, np.uint16)
+    k_new, v_new = (_c(a, np.float32) for a in (k_new, v_new))
+    page_table, ctx_len = _c(page_table, np.int32), _c(ctx_len, np.int32)
+    topk_pages, topk_count = _c(topk_pages, np.int32), _c(topk_count, np.int32)
+    if sh.kv_format == KV_E4M3_ROWSCALE:
+        assert q_bf16 is not None
+    else:
+        assert q_f32 is not None
+    B, Q, Hq, S = sh.B, sh.Q, sh.Hq, sh.num_splits
+    q8 = np.zeros((B, Q, Hq, 128), np.uint8)
+    out = np.zeros((B, Q, Hq, 128), np.float64)
+    po = pm = pl = None
+    if want_partials:
+        po = np.zeros((B, S, Q, Hq, 128), np.float64)
+        pm = np.zeros((B, S, Q, Hq), np.float64)
+        pl = np.zeros((B, S, Q, Hq), np.float64)
+    cs = sh.c()
+    lib().orc_decode_step_reuse(ctypes.byref(cs), _p(q_f32), _p(q_bf16), _p(k_new), _p(v_new),
+                                _p(page_table), _p(ctx_len), _p(k_pool), _p(v_pool), _p(topk_pages),
+                                _p(topk_count), _p(q8), _p(po), _p(pm), _p(pl), _p(out))
+    res = dict(out=out)
     if sh.kv_format != KV_E4M3_ROWSCALE:
         res["q_e4m3"] = q8
     if want_partials:

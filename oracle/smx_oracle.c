@@ -264,7 +264,7 @@ static void insert_token(const orc_shape* sh, int b, int64_t pos, const float* k
     if (pos < 0 || p >= sh->max_pages) return;
     phys = page_table[(size_t)b * sh->max_pages + p];
     if (phys < 0 || phys >= sh->n_pool_pages) return;
-    {
+    if (kidx_row && idx_pool) {   /* a layer without an index cache writes K and V only */
         uint8_t nib[64], sc[4];
         orc_mxfp4_quant_row(kidx_row, nib, sc);
         orc_mxfp4_store_row(idx_pool + (size_t)phys * ORC_MXFP4_PAGE_BYTES, slot, nib, sc);
@@ -277,7 +277,8 @@ static void insert_token(const orc_shape* sh, int b, int64_t pos, const float* k
 
 /* a1: the Q new tokens of row b sit at positions ctx_len[b] - Q + t, t in [0, Q)
  * ([ATOM-2812] K1 index-K insert and K/V insert; ctx_len counts the new tokens).
- * k_new, v_new: [B][Q][Hkv][128]; kidx_new: [B][Q][128]. */
+ * k_new, v_new: [B][Q][Hkv][128]; kidx_new: [B][Q][128], or NULL (with idx_pool NULL) for a
+ * layer without an index cache: K and V rows only. */
 void orc_kv_insert(const orc_shape* sh, const float* k_new, const float* v_new,
                    const float* kidx_new, const int32_t* page_table, const int32_t* ctx_len,
                    uint8_t* k_pool, uint8_t* v_pool, uint8_t* idx_pool) {
@@ -286,7 +287,7 @@ void orc_kv_insert(const orc_shape* sh, const float* k_new, const float* v_new,
             size_t r = (size_t)b * sh->Q + t;
             insert_token(sh, b, (int64_t)ctx_len[b] - sh->Q + t,
                          k_new + r * sh->Hkv * ORC_D, v_new + r * sh->Hkv * ORC_D,
-                         kidx_new + r * ORC_D, page_table, k_pool, v_pool, idx_pool);
+                         kidx_new ? kidx_new + r * ORC_D : NULL, page_table, k_pool, v_pool, idx_pool);
         }
 }
 
@@ -531,6 +532,40 @@ void orc_decode_step(const orc_shape* sh, const float* q_f32, const uint16_t* q_
     }
     orc_index_scores(sh, qidx_bf16, idx_pool, page_table, ctx_len, scores);
     orc_topk(sh, scores, ctx_len, topk_pages, topk_count);
+    if (!po) po = (double*)malloc(np * ORC_D * sizeof(double));
+    if (!pm) pm = (double*)malloc(np * sizeof(double));
+    if (!pl) pl = (double*)malloc(np * sizeof(double));
+    orc_sparse_attn_split(sh, qa, k_pool, v_pool, page_table, ctx_len, topk_pages, topk_count,
+                          po, pm, pl);
+    orc_sparse_attn_merge(sh, po, pm, pl, out);
+    if (po != part_o) free(po);
+    if (pm != part_m) free(pm);
+    if (pl != part_l) free(pl);
+}
+
+/* The step of a layer that reuses an earlier layer's selection ([MiniMax-M3.1] "Enable Mono
+ * decode with fixed DSpark verify", the dense_prefix_mono note: an index_topk_freq schedule gives
+ * layers that run no indexer and attend over the sparse blocks a previous layer selected).
+ * Readings: such a layer has no index cache, so only its K and V rows are inserted (a1 without
+ * the index-K row); the selection arrives as the earlier layer's (topk_pages, topk_count): logical
+ * page ids of the same rows, ascending, which this layer's page table maps to its own K/V pages;
+ * q packing (a2), the split (a5) and the merge (a6) are those of the full step. */
+void orc_decode_step_reuse(const orc_shape* sh, const float* q_f32, const uint16_t* q_bf16,
+                           const float* k_new, const float* v_new, const int32_t* page_table,
+                           const int32_t* ctx_len, uint8_t* k_pool, uint8_t* v_pool,
+                           const int32_t* topk_pages, const int32_t* topk_count, uint8_t* q_e4m3,
+                           double* part_o, double* part_m, double* part_l, double* out) {
+    size_t nq = (size_t)sh->B * sh->Q * sh->Hq * ORC_D;
+    size_t np = (size_t)sh->B * sh->num_splits * sh->Q * sh->Hq;
+    double *po = part_o, *pm = part_m, *pl = part_l;
+    const void* qa;
+    orc_kv_insert(sh, k_new, v_new, NULL, page_table, ctx_len, k_pool, v_pool, NULL);
+    if (sh->kv_format == ORC_KV_E4M3_ROWSCALE) {
+        qa = q_bf16;
+    } else {
+        orc_pack_q_e4m3(q_f32, q_e4m3, (int64_t)nq);
+        qa = q_e4m3;
+    }
     if (!po) po = (double*)malloc(np * ORC_D * sizeof(double));
     if (!pm) pm = (double*)malloc(np * sizeof(double));
     if (!pl) pl = (double*)malloc(np * sizeof(double));

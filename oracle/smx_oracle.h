@@ -93,6 +93,13 @@ void orc_decode_step(const orc_shape* sh, const float* q_f32, const uint16_t* q_
                      int32_t* topk_pages, int32_t* topk_count, uint8_t* q_e4m3,
                      double* part_o, double* part_m, double* part_l, double* out);
 
+/* The step of a layer that reuses an earlier layer's selection: K/V insert (no index-K), q
+ * packing, split over (topk_pages, topk_count) as given, merge. Same buffers as orc_decode_step. */
+void orc_decode_step_reuse(const orc_shape* sh, const float* q_f32, const uint16_t* q_bf16,
+                           const float* k_new, const float* v_new, const int32_t* page_table,
+                           const int32_t* ctx_len, uint8_t* k_pool, uint8_t* v_pool,
+                           const int32_t* topk_pages, const int32_t* topk_count, uint8_t* q_e4m3,
+                           double* part_o, double* part_m, double* part_l, double* out);
 void orc_set_threads(int n);
 int orc_max_threads(void);
 

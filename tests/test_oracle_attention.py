@@ -2,8 +2,8 @@
 dense attention over exactly the selected tokens (torch float64), full causal attention via
 torch's scaled_dot_product_attention when every page is selected, any split count merging to
 the single pass, NaN-poisoned tails that do not leak, a wrong page table that changes the
-output, a consistent physical permutation that does not, GQA as independent heads, and a
-hand-derived merge."""
+output, a consistent physical permutation that does not, GQA as independent heads, a
+hand-derived merge, and the step of a layer that reuses an earlier layer's selection."""
 import os
 
 import numpy as np
@@ -202,3 +202,50 @@ def test_insert_writes_exactly_the_new_rows(fmt):
                         changed[pi][phys, h, 8192 + 4 * slot:8196 + 4 * slot] = True
     for p0, p1, ch in zip(before, after, changed):
         assert np.array_equal(p0[~ch], p1[~ch])
+
+
+def _reuse(w, data, pools, pages, count):
+    kp, vp, ip = (p.copy() for p in pools)
+    rr = oracle.decode_step_reuse(oracle.shape_of(w), q_f32=data["q"], q_bf16=data["q_bf16"],
+                                  k_new=data["k_new"], v_new=data["v_new"], page_table=data["page_table"],
+                                  ctx_len=data["ctx_len"], k_pool=kp, v_pool=vp, topk_pages=pages,
+                                  topk_count=count)
+    return rr, (kp, vp, ip)
+
+
+@pytest.mark.parametrize("fmt", [wl.KV_MXFP4, wl.KV_E4M3_ROWSCALE])
+def test_reuse_with_the_steps_own_selection_reproduces_the_step(fmt):
+    # a reusing layer handed the selection the full step made computes the full step's attention
+    # with the same operations, writes the same K/V bytes and leaves the index cache alone
+    w = small(fmt)
+    data, pools = _case(w)
+    res, new_pools = H.oracle_step(w, data, pools)
+    rr, (kp, vp, ip) = _reuse(w, data, pools, res["topk_pages"], res["topk_count"])
+    assert np.array_equal(rr["out"], res["out"])
+    assert np.array_equal(kp, new_pools[0]) and np.array_equal(vp, new_pools[1])
+    assert np.array_equal(ip, pools[2])
+    if fmt == wl.KV_MXFP4:
+        assert np.array_equal(rr["q_e4m3"], res["q_e4m3"])
+
+
+@pytest.mark.parametrize("fmt", [wl.KV_MXFP4, wl.KV_E4M3_ROWSCALE])
+def test_reuse_attends_over_exactly_the_given_pages(fmt):
+    # another layer's selection (seeded random pages of each row, not this layer's scores): dense
+    # attention over exactly those pages' visible tokens, and not the step's own output
+    w = small(fmt, topk=3, max_ctx=1400)
+    data, pools = _case(w)
+    rng = np.random.default_rng(123)
+    n_pages = (data["ctx_len"] + 127) // 128
+    pages = -np.ones((w.B, w.topk), np.int32)
+    count = np.zeros(w.B, np.int32)
+    for b in range(w.B):
+        k = min(w.topk, int(n_pages[b]))
+        pages[b, :k] = np.sort(rng.choice(int(n_pages[b]), size=k, replace=False))
+        count[b] = k
+    rr, (kp, vp, _) = _reuse(w, data, pools, pages, count)
+    ref = H.dense_selected_attention(w, data, H.q_values(w, data, rr), kp, vp, pages, count)
+    assert np.all(np.isfinite(rr["out"]))
+    assert _close(rr["out"], ref)
+    res, _ = H.oracle_step(w, data, pools)
+    if not np.array_equal(np.sort(res["topk_pages"], axis=1), np.sort(pages, axis=1)):
+        assert not np.allclose(rr["out"], res["out"])
