@@ -38,6 +38,8 @@ import torch  # noqa: E402
 from sparse_attention_decode_mxfp4_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "sparse MXFP4 decode step: µs/step and achieved HBM GB/s vs GB300 peak"
+METRIC_REUSE = ("sparse MXFP4 decode step of a layer reusing an earlier layer's selection: µs/step and "
+                "achieved HBM GB/s vs GB300 peak")
 
 
 def parse():
@@ -51,6 +53,9 @@ def parse():
                     help="partitions of the split stage (0 = about two CTAs per SM, at most one page each)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--reuse", action="store_true",
+                    help="time the step of a layer that reuses one full step's selection (K/V insert, "
+                         "split and merge; no index scoring or selection); bytes = the selected K/V pages")
     return ap.parse_args()
 
 
@@ -193,25 +198,38 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(w, data, step_bytes):
-    """Oracle on this host's cores: whole steps of the same workload, repeated for ~10 s."""
+def cpu_baseline(w, data, step_bytes, reuse=False):
+    """Oracle on this host's cores: whole steps of the same workload, repeated for ~10 s (reuse:
+    the reusing layer's step over the oracle's own selection)."""
     import oracle
     from oracle import shape_of
     pools = wl.empty_pools(w)
     sh = shape_of(w)
     oracle.kv_fill(sh, data["k"], data["v"], data["kidx"], data["page_table"], data["n_hist"], *pools)
+
+    def full():
+        return oracle.decode_step(sh, q_f32=data["q"], q_bf16=data["q_bf16"], qidx_bf16=data["qidx_bf16"],
+                                  k_new=data["k_new"], v_new=data["v_new"], kidx_new=data["kidx_new"],
+                                  page_table=data["page_table"], ctx_len=data["ctx_len"], k_pool=pools[0],
+                                  v_pool=pools[1], idx_pool=pools[2])
+
+    sel = full() if reuse else None
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.decode_step(sh, q_f32=data["q"], q_bf16=data["q_bf16"], qidx_bf16=data["qidx_bf16"],
-                           k_new=data["k_new"], v_new=data["v_new"], kidx_new=data["kidx_new"],
-                           page_table=data["page_table"], ctx_len=data["ctx_len"], k_pool=pools[0],
-                           v_pool=pools[1], idx_pool=pools[2])
+        if reuse:
+            oracle.decode_step_reuse(sh, q_f32=data["q"], q_bf16=data["q_bf16"], k_new=data["k_new"],
+                                     v_new=data["v_new"], page_table=data["page_table"], ctx_len=data["ctx_len"],
+                                     k_pool=pools[0], v_pool=pools[1], topk_pages=sel["topk_pages"],
+                                     topk_count=sel["topk_count"])
+        else:
+            full()
         reps += 1
         dt = time.perf_counter() - t0
         if dt > 10.0:
             break
     return {"value": step_bytes * reps / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
-            "kind": "oracle", "sample": f"{reps} whole steps of the workload ({dt:.1f} s)",
+            "kind": "oracle", "sample": f"{reps} whole {'reusing-layer ' if reuse else ''}steps of the workload "
+                                       f"({dt:.1f} s)",
             "us_per_step": dt / reps * 1e6}
 
 
@@ -237,6 +255,8 @@ def main():
     shape = ops.Shape.of(w, args.splits or default_splits(w))
     data = wl.generate(w)
     idx_b, kv_b = algorithmic_bytes(w, data["ctx_len"])
+    if args.reuse:
+        idx_b = 0   # a reusing layer reads no index page
     step_bytes = idx_b + kv_b
 
     def T(a):
@@ -266,6 +286,18 @@ def main():
         ops.decode_step(shape, **io, page_table=pt, ctx_len=cl, k_pool=kp, v_pool=vp, idx_pool=ip,
                         topk_pages=topk_pages, topk_count=topk_count, out=o, workspace=workspace,
                         dev_status=status)
+
+    if args.reuse:
+        # an earlier layer's selection: one full step's output, then the reusing layer's step
+        step(0)
+        sel_pages, sel_count = topk_pages.clone(), topk_count.clone()
+        del inp["qidx_bf16"], inp["kidx_new"]
+
+        def step(i, pt=page_table, cl=ctx_len, io=inp, o=out):   # noqa: F811
+            kp, vp, _ = copies[i % R]
+            ops.decode_step_reuse(shape, **io, page_table=pt, ctx_len=cl, k_pool=kp, v_pool=vp,
+                                  topk_pages=sel_pages, topk_count=sel_count, out=o, workspace=workspace,
+                                  dev_status=status)
 
     step(0)
     torch.cuda.synchronize()
@@ -355,21 +387,23 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, data, step_bytes)
+        cpu = cpu_baseline(w, data, step_bytes, reuse=args.reuse)
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "metric": METRIC_REUSE if args.reuse else METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": us_step / 1e3, "us_per_step": us_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded N(0,1) rows quantised on the GPU; BASELINE workload shapes)",
-            "config": dict(w.describe(), num_splits=shape.num_splits, bytes_per_step=step_bytes,
+            "config": dict(w.describe(), step="reusing layer" if args.reuse else "full",
+                           num_splits=shape.num_splits, bytes_per_step=step_bytes,
                            index_bytes=idx_b, kv_bytes=kv_b, parallelism="replicas" if world > 1 else "single",
                            l2=f"rotating {R} pool copies ({R * pool_bytes / 1e6:.0f} MB, reads "
                               f"{R * step_bytes / 1e6:.0f} MB per rotation > 3x L2 {l2 / 1e6:.0f} MB)"),
             "roofline": {"bound": "hbm", "kernel": "decode_step_kernel", "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": recorded_traffic(w.name), "us_per_launch": kernel_us,
+                         "traffic": None if args.reuse else recorded_traffic(w.name), "us_per_launch": kernel_us,
                          "algorithmic_bytes_per_launch": step_bytes // launches_per_step},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "GB/s", "us_per_step": e2e_s * 1e6, "h2d_bytes_per_step": h2d,

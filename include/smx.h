@@ -169,6 +169,26 @@ int smx_decode_step(const smx_shape_t* shape, const float* q_f32, const uint16_t
                     int32_t* topk_count, float* out, void* workspace, size_t ws_bytes,
                     int32_t* dev_status, smx_stream_t stream);
 
+/* The step of a layer that reuses an earlier layer's selection ([MiniMax-M3.1] "Enable Mono
+ * decode with fixed DSpark verify": an index_topk_freq schedule gives layers that run no indexer
+ * and attend over the sparse blocks a previous layer selected). On `stream`: the Q new K and V
+ * rows of every row are inserted (no index cache: nothing is scored and no index row is
+ * written), q is packed (MXFP4 K/V), and the split stage and the merge run over the given
+ * selection: topk_count[b] in [0, min(topk, ceil(ctx_len[b] / 128))] and topk_pages[b][0 ..
+ * count) the logical page ids, ascending, of row b ([B][topk] int32, device; e.g. an earlier
+ * smx_decode_step's outputs), which this layer's page_table maps to its own K/V pages. Arguments
+ * as smx_decode_step (same workspace size; q_f32 or q_bf16 by format; k_new/v_new/k_pool/v_pool
+ * 16-byte aligned). A count outside that range is clamped and an id outside the row's pages
+ * skipped (an empty page), both flagged SMX_DEV_BAD_PAGE_ID in dev_status. One cooperative
+ * kernel, as smx_decode_step without its scoring and selection. Returns SMX_OK,
+ * SMX_ERR_INVALID_ARG (a NULL or misaligned pointer), SMX_ERR_UNSUPPORTED (shape),
+ * SMX_ERR_WORKSPACE or SMX_ERR_CUDA. */
+int smx_decode_step_reuse(const smx_shape_t* shape, const float* q_f32, const uint16_t* q_bf16,
+                          const float* k_new, const float* v_new, const int32_t* page_table,
+                          const int32_t* ctx_len, uint8_t* k_pool, uint8_t* v_pool,
+                          const int32_t* topk_pages, const int32_t* topk_count, float* out,
+                          void* workspace, size_t ws_bytes, int32_t* dev_status, smx_stream_t stream);
+
 /* Static text for a status code. */
 const char* smx_status_string(int status);
 

@@ -207,7 +207,7 @@ int smx_decode_step(const smx_shape_t* s, const float* q_f32, const uint16_t* q_
     if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
         return SMX_ERR_WORKSPACE;
     const Workspace w = layout(s, workspace);
-    smx::StepIO io;
+    smx::StepIO io = {};
     io.q_f32 = rs ? nullptr : q_f32;
     io.q_bf16 = rs ? q_bf16 : nullptr;
     io.qidx = qidx_bf16;
@@ -218,6 +218,35 @@ int smx_decode_step(const smx_shape_t* s, const float* q_f32, const uint16_t* q_
     io.counters = w.counters; io.scores = w.scores;
     io.part_o = w.part_o; io.part_m = w.part_m; io.part_l = w.part_l;
     return cuda_status(smx::launch_decode_step(*s, io, (cudaStream_t)stream));
+}
+
+int smx_decode_step_reuse(const smx_shape_t* s, const float* q_f32, const uint16_t* q_bf16, const float* k_new,
+                          const float* v_new, const int32_t* page_table, const int32_t* ctx_len, uint8_t* k_pool,
+                          uint8_t* v_pool, const int32_t* topk_pages, const int32_t* topk_count, float* out,
+                          void* workspace, size_t ws_bytes, int32_t* dev_status, smx_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    const bool rs = s->kv_format == SMX_KV_E4M3_ROWSCALE;
+    if ((rs ? (const void*)q_bf16 : (const void*)q_f32) == nullptr) return SMX_ERR_INVALID_ARG;
+    if (!k_new || !v_new || !page_table || !ctx_len || !k_pool || !v_pool || !topk_pages || !topk_count || !out)
+        return SMX_ERR_INVALID_ARG;
+    if (!rs && !aligned16(q_f32)) return SMX_ERR_INVALID_ARG;
+    if (rs && (reinterpret_cast<uintptr_t>(q_bf16) & 3u)) return SMX_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool)) return SMX_ERR_INVALID_ARG;
+    const size_t need = layout(s, nullptr).bytes;
+    if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+        return SMX_ERR_WORKSPACE;
+    const Workspace w = layout(s, workspace);
+    smx::StepIO io = {};
+    io.q_f32 = rs ? nullptr : q_f32;
+    io.q_bf16 = rs ? q_bf16 : nullptr;
+    io.k_new = k_new; io.v_new = v_new;
+    io.page_table = page_table; io.ctx_len = ctx_len;
+    io.k_pool = k_pool; io.v_pool = v_pool;
+    io.topk_in = topk_pages; io.count_in = topk_count; io.out = out; io.status = dev_status;
+    io.counters = w.counters; io.scores = w.scores;
+    io.part_o = w.part_o; io.part_m = w.part_m; io.part_l = w.part_l;
+    return cuda_status(smx::launch_decode_step(*s, io, (cudaStream_t)stream, true));
 }
 
 int smx_decode_step_launches(const smx_shape_t* s) {

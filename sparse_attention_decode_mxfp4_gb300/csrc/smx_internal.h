@@ -65,6 +65,8 @@ struct StepIO {
     uint8_t* v_pool;
     int32_t* topk_out;
     int32_t* count_out;
+    const int32_t* topk_in;    // a reused selection (launch_decode_step with reuse), else null
+    const int32_t* count_in;
     float* out;
     int32_t* status;
     uint32_t* counters;   // n_counters, zero before the first step; every step leaves them zero
@@ -73,7 +75,7 @@ struct StepIO {
     float* part_m;        // [B][S][Q][Hq]
     float* part_l;
 };
-cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStream_t st);
+cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStream_t st, bool reuse = false);
 
 // Bytes at the head of the decode-step workspace that must be zero before a step (the counters).
 size_t workspace_counter_bytes(const smx_shape_t& s);

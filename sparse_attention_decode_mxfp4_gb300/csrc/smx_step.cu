@@ -65,6 +65,8 @@ struct StepArgs {
     int B, Q, Hq, Hkv, G, max_pages, topk, S;
     int row_warps, rows_per_cta, n_rg, page_bytes;
     int chunk_pages, chunks_per_row;
+    const int32_t* topk_in;      // REUSE: the given selection [B][topk], and its counts [B]
+    const int32_t* count_in;
 };
 
 constexpr int kStepWarps = 8;
@@ -73,7 +75,26 @@ constexpr int kRedPages = 32;        // page maxima combined per flush
 constexpr int kPtCache = 2048;       // page-table entries of a unit's row kept in shared memory
 constexpr int kCounterStride = 32;   // u32 words between counters: each on its own 128-byte line
 
-template <bool RS, int NT, bool TC>
+// A reusing layer's selection for row b (entries [0, k_eff) of sel_all): the given count clamped
+// to [0, min(topk, n_pages)], each id checked against the row's pages (an id outside them is
+// flagged and becomes -1: an empty page). Every thread; ends with a barrier.
+__device__ __forceinline__ int given_selection(const StepArgs& a, int b, int n_pages, int* sel_all) {
+    const int raw = a.count_in[b];
+    const int k_eff = max(0, min(raw, min(a.topk, n_pages)));
+    if (threadIdx.x == 0 && raw != k_eff) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+    for (int i = threadIdx.x; i < k_eff; i += blockDim.x) {
+        int p = a.topk_in[(int64_t)b * a.topk + i];
+        if (p < 0 || p >= n_pages) {
+            flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+            p = -1;
+        }
+        sel_all[i] = p;
+    }
+    __syncthreads();
+    return k_eff;
+}
+
+template <bool RS, int NT, bool TC, bool REUSE>
 __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ __align__(16) uint32_t qh[16][64];
@@ -127,6 +148,8 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
         mbar_init(&mbar_mma[1], 1);
         mbar_fence_init();
     }
+    __syncthreads();   // the barriers are initialised before any thread polls one (a CTA with no
+                       // scoring chunk reaches its attention unit's q wait without another barrier)
 
     const int P = a.chunk_pages, C = a.chunks_per_row;
     const int kv_rows = a.Q * 2 * a.Hkv;
@@ -179,133 +202,170 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
         pt_stored = true;
     };
     // ---------------- A. scoring chunks ----------------
-    for (int ci = c; ci < a.B * C; ci += nC) {
-        const int b = ci / C, j = ci % C;
-        const int p0 = j * P, np_max = max(0, min(P, a.max_pages - p0));
-        // independent loads first: the row's length, this chunk's page-table entries, the index
-        // query, and the first new K/V row of this warp's share (rows j + C w, j + C (w + 8), ...)
-        const int ctx_raw = a.ctx_len[b];
-        for (int i = threadIdx.x; i < np_max; i += blockDim.x) {
-            const int64_t ph = a.page_table[(int64_t)b * a.max_pages + p0 + i];
-            phys_s[i] = (ph < 0 || ph >= a.n_pool) ? -1 : ph;
-        }
-        const IndexQueryRaw qraw = load_index_query(a.qidx + (int64_t)b * a.Q * kD, a.Q);
-        // the row's new index-K rows, one per warp (written below if this chunk owns their page)
-        float4 kidx_x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (warp < a.Q) kidx_x = reinterpret_cast<const float4*>(a.kidx_new + ((int64_t)b * a.Q + warp) * kD)[lane];
-        const int kv_r0 = j + C * warp;
-        auto kv_row_src = [&](int r) {
-            const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);   // kind < Hkv: K head, else V head
-            const int64_t tok = (int64_t)b * a.Q + tq;
-            return reinterpret_cast<const float4*>((kind < a.Hkv ? a.k_new : a.v_new) + (tok * a.Hkv + kind % a.Hkv) * kD) + lane;
-        };
-        float4 kv_x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (kv_r0 < kv_rows) kv_x = *kv_row_src(kv_r0);
-        const int ctx = clamp_ctx(ctx_raw, a.Q, a.max_pages, (j == 0 && threadIdx.x == 0) ? a.status : nullptr);
-        const int n_pages = (ctx + kPage - 1) / kPage;
-        const int np = max(0, min(np_max, n_pages - p0));
-        const int first_new = ctx - a.Q;
-        // chunk pages [own_lo, own_hi) take new index-K rows (positions [lo_new, hi_new))
-        const int lo_new = max(max(first_new, 0), p0 * kPage), hi_new = min(ctx, (p0 + np) * kPage);
-        const bool owner = lo_new < hi_new;
-        const int own_lo = owner ? lo_new / kPage - p0 : np, own_hi = owner ? (hi_new - 1) / kPage - p0 + 1 : np;
-        __syncthreads();   // page-table entries staged (and the mbarriers initialised)
-
-        // pages go four at a time to the four warp pairs; warp 2q + h scores tiles 4h .. 4h + 3 of
-        // page i0 + q into a per-lane running maximum (one warp reduction per page). The next
-        // group's tiles are in flight while a group is scored; the pages that take no new rows go
-        // out before the inserts.
-        const int pq = warp >> 1, tile0 = (warp & 1) * 4;
-        TileFrag fa[4], fb[4];
-        auto load_page = [&](TileFrag (&f)[4], int i, bool skip_own) {
-            if (i < np && phys_s[i] >= 0 && !(skip_own && i >= own_lo && i < own_hi)) {
-                const uint8_t* page = a.idx_pool + phys_s[i] * kMxPageBytes;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) load_tile(f[k], page, tile0 + k, g, t);
-            }
-        };
-        load_page(fa, pq, true);
-        if (!pt_stored) store_pt();
-        int64_t kv_phys0 = -1;   // page of this warp's first K/V row
-        if (kv_r0 < kv_rows && first_new + kv_r0 / (2 * a.Hkv) >= 0)
-            kv_phys0 = a.page_table[(int64_t)b * a.max_pages + (first_new + kv_r0 / (2 * a.Hkv)) / kPage];
-        if (owner) {
-            // the new index-K rows on this chunk's pages (one warp per row), then those pages' tiles
-            for (int tq = warp; tq < a.Q; tq += kStepWarps) {
+    if constexpr (REUSE) {
+        // a layer reusing an earlier layer's selection has no index cache: each chunk (b, j) writes
+        // its warps' share of row b's new K/V rows (rows j + C w, j + C (w + 8), ...), then releases
+        // the row counter
+        for (int ci = c; ci < a.B * C; ci += nC) {
+            const int b = ci / C, j = ci % C;
+            const int ctx = clamp_ctx(a.ctx_len[b], a.Q, a.max_pages, (j == 0 && threadIdx.x == 0) ? a.status : nullptr);
+            const int first_new = ctx - a.Q;
+            for (int r = j + C * warp; r < kv_rows; r += C * kStepWarps) {
+                const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);   // kind < Hkv: K head, else V head
                 const int pos = first_new + tq;
-                if (pos < lo_new || pos >= hi_new) continue;
-                const int64_t phys = phys_s[pos / kPage - p0];
-                if (phys < 0) {
+                if (pos < 0) continue;
+                const int64_t tok = (int64_t)b * a.Q + tq;
+                const float4 x = reinterpret_cast<const float4*>((kind < a.Hkv ? a.k_new : a.v_new) +
+                                                                 (tok * a.Hkv + kind % a.Hkv) * kD)[lane];
+                const int64_t phys = a.page_table[(int64_t)b * a.max_pages + pos / kPage];
+                if (phys < 0 || phys >= a.n_pool) {
                     if (lane == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
                     continue;
                 }
-                const float4 x = tq == warp ? kidx_x : reinterpret_cast<const float4*>(a.kidx_new + ((int64_t)b * a.Q + tq) * kD)[lane];
-                uint8_t* page = a.idx_pool + phys * kMxPageBytes;
-                quant_row_mxfp4_warp(x, page + (pos % kPage) * 64, page + kMxScaleOff + (pos % kPage) * 4, lane);
-            }
-            __threadfence();
-            __syncthreads();
-            if (pq >= own_lo && pq < own_hi) load_page(fa, pq, false);
-        }
-
-        // this warp's new K/V rows (read only by the attention phase, after the row's counter), while
-        // the index tiles are in flight
-        for (int r = kv_r0; r < kv_rows; r += C * kStepWarps) {
-            const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);
-            const int pos = first_new + tq;
-            if (pos < 0) continue;
-            const float4 x = r == kv_r0 ? kv_x : *kv_row_src(r);
-            const int64_t phys = r == kv_r0 ? kv_phys0 : (int64_t)a.page_table[(int64_t)b * a.max_pages + pos / kPage];
-            if (phys < 0 || phys >= a.n_pool) {
-                if (lane == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
-                continue;
-            }
-            const int h = kind % a.Hkv, slot = pos % kPage;
-            uint8_t* pool = kind < a.Hkv ? a.k_pool : a.v_pool;
-            if (RS) {
-                uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kRsPageBytes;
-                quant_row_e4m3rs_warp(x, page + slot * 128, reinterpret_cast<float*>(page + kRsScaleOff) + slot, lane);
-            } else {
-                uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kMxPageBytes;
-                quant_row_mxfp4_warp(x, page + slot * 64, page + kMxScaleOff + slot * 4, lane);
-            }
-        }
-        uint32_t qf[NT][16];
-        int sig_c[NT][2];
-        setup_index_query<NT>(qraw, a.Q, qh, sig, qf, sig_c);
-        const int lim = ctx - a.Q;   // token j counts for query n iff j <= lim + n
-#pragma unroll 1
-        for (int i0 = 0; i0 < np; i0 += 4) {
-            if (i0 + 4 < np) load_page(fb, i0 + 4 + pq, false);
-            const int i = i0 + pq;
-            if (i < np) {
-                float best = -INFINITY;
-                if (phys_s[i] >= 0) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        best = fmaxf(best, score_tile<NT>(fa[k], qf, sig_c, p0 + i, tile0 + k, g, t, lim, a.Q));
-                } else if ((warp & 1) == 0 && lane == 0) {
-                    flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                const int h = kind % a.Hkv, slot = pos % kPage;
+                uint8_t* pool = kind < a.Hkv ? a.k_pool : a.v_pool;
+                if (RS) {
+                    uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kRsPageBytes;
+                    quant_row_e4m3rs_warp(x, page + slot * 128, reinterpret_cast<float*>(page + kRsScaleOff) + slot, lane);
+                } else {
+                    uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kMxPageBytes;
+                    quant_row_mxfp4_warp(x, page + slot * 64, page + kMxScaleOff + slot * 4, lane);
                 }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
-                if (lane == 0) red[i % kRedPages][warp & 1] = best;
             }
-            if ((i0 + 4) % kRedPages == 0 || i0 + 4 >= np) {   // page maxima of pages [base, i0 + 4)
-                __syncthreads();
-                const int base = (i0 / kRedPages) * kRedPages;
-                const int cnt = min(i0 + 4, np) - base;
-                if ((int)threadIdx.x < cnt)
-                    a.scores[(int64_t)b * a.max_pages + p0 + base + threadIdx.x] =
-                        fmaxf(red[threadIdx.x][0], red[threadIdx.x][1]);
-                __syncthreads();
+            if (!pt_stored) store_pt();
+            __syncthreads();
+            if (threadIdx.x == 0) red_release_add(&a.row_cnt[kCounterStride * b], 1u);
+        }
+    } else {
+        for (int ci = c; ci < a.B * C; ci += nC) {
+            const int b = ci / C, j = ci % C;
+            const int p0 = j * P, np_max = max(0, min(P, a.max_pages - p0));
+            // independent loads first: the row's length, this chunk's page-table entries, the index
+            // query, and the first new K/V row of this warp's share (rows j + C w, j + C (w + 8), ...)
+            const int ctx_raw = a.ctx_len[b];
+            for (int i = threadIdx.x; i < np_max; i += blockDim.x) {
+                const int64_t ph = a.page_table[(int64_t)b * a.max_pages + p0 + i];
+                phys_s[i] = (ph < 0 || ph >= a.n_pool) ? -1 : ph;
             }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) fa[k] = fb[k];
+            const IndexQueryRaw qraw = load_index_query(a.qidx + (int64_t)b * a.Q * kD, a.Q);
+            // the row's new index-K rows, one per warp (written below if this chunk owns their page)
+            float4 kidx_x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (warp < a.Q) kidx_x = reinterpret_cast<const float4*>(a.kidx_new + ((int64_t)b * a.Q + warp) * kD)[lane];
+            const int kv_r0 = j + C * warp;
+            auto kv_row_src = [&](int r) {
+                const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);   // kind < Hkv: K head, else V head
+                const int64_t tok = (int64_t)b * a.Q + tq;
+                return reinterpret_cast<const float4*>((kind < a.Hkv ? a.k_new : a.v_new) + (tok * a.Hkv + kind % a.Hkv) * kD) + lane;
+            };
+            float4 kv_x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (kv_r0 < kv_rows) kv_x = *kv_row_src(kv_r0);
+            const int ctx = clamp_ctx(ctx_raw, a.Q, a.max_pages, (j == 0 && threadIdx.x == 0) ? a.status : nullptr);
+            const int n_pages = (ctx + kPage - 1) / kPage;
+            const int np = max(0, min(np_max, n_pages - p0));
+            const int first_new = ctx - a.Q;
+            // chunk pages [own_lo, own_hi) take new index-K rows (positions [lo_new, hi_new))
+            const int lo_new = max(max(first_new, 0), p0 * kPage), hi_new = min(ctx, (p0 + np) * kPage);
+            const bool owner = lo_new < hi_new;
+            const int own_lo = owner ? lo_new / kPage - p0 : np, own_hi = owner ? (hi_new - 1) / kPage - p0 + 1 : np;
+            __syncthreads();   // page-table entries staged (and the mbarriers initialised)
+
+            // pages go four at a time to the four warp pairs; warp 2q + h scores tiles 4h .. 4h + 3 of
+            // page i0 + q into a per-lane running maximum (one warp reduction per page). The next
+            // group's tiles are in flight while a group is scored; the pages that take no new rows go
+            // out before the inserts.
+            const int pq = warp >> 1, tile0 = (warp & 1) * 4;
+            TileFrag fa[4], fb[4];
+            auto load_page = [&](TileFrag (&f)[4], int i, bool skip_own) {
+                if (i < np && phys_s[i] >= 0 && !(skip_own && i >= own_lo && i < own_hi)) {
+                    const uint8_t* page = a.idx_pool + phys_s[i] * kMxPageBytes;
+    #pragma unroll
+                    for (int k = 0; k < 4; ++k) load_tile(f[k], page, tile0 + k, g, t);
+                }
+            };
+            load_page(fa, pq, true);
+            if (!pt_stored) store_pt();
+            int64_t kv_phys0 = -1;   // page of this warp's first K/V row
+            if (kv_r0 < kv_rows && first_new + kv_r0 / (2 * a.Hkv) >= 0)
+                kv_phys0 = a.page_table[(int64_t)b * a.max_pages + (first_new + kv_r0 / (2 * a.Hkv)) / kPage];
+            if (owner) {
+                // the new index-K rows on this chunk's pages (one warp per row), then those pages' tiles
+                for (int tq = warp; tq < a.Q; tq += kStepWarps) {
+                    const int pos = first_new + tq;
+                    if (pos < lo_new || pos >= hi_new) continue;
+                    const int64_t phys = phys_s[pos / kPage - p0];
+                    if (phys < 0) {
+                        if (lane == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                        continue;
+                    }
+                    const float4 x = tq == warp ? kidx_x : reinterpret_cast<const float4*>(a.kidx_new + ((int64_t)b * a.Q + tq) * kD)[lane];
+                    uint8_t* page = a.idx_pool + phys * kMxPageBytes;
+                    quant_row_mxfp4_warp(x, page + (pos % kPage) * 64, page + kMxScaleOff + (pos % kPage) * 4, lane);
+                }
+                __threadfence();
+                __syncthreads();
+                if (pq >= own_lo && pq < own_hi) load_page(fa, pq, false);
+            }
+
+            // this warp's new K/V rows (read only by the attention phase, after the row's counter), while
+            // the index tiles are in flight
+            for (int r = kv_r0; r < kv_rows; r += C * kStepWarps) {
+                const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);
+                const int pos = first_new + tq;
+                if (pos < 0) continue;
+                const float4 x = r == kv_r0 ? kv_x : *kv_row_src(r);
+                const int64_t phys = r == kv_r0 ? kv_phys0 : (int64_t)a.page_table[(int64_t)b * a.max_pages + pos / kPage];
+                if (phys < 0 || phys >= a.n_pool) {
+                    if (lane == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                    continue;
+                }
+                const int h = kind % a.Hkv, slot = pos % kPage;
+                uint8_t* pool = kind < a.Hkv ? a.k_pool : a.v_pool;
+                if (RS) {
+                    uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kRsPageBytes;
+                    quant_row_e4m3rs_warp(x, page + slot * 128, reinterpret_cast<float*>(page + kRsScaleOff) + slot, lane);
+                } else {
+                    uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kMxPageBytes;
+                    quant_row_mxfp4_warp(x, page + slot * 64, page + kMxScaleOff + slot * 4, lane);
+                }
+            }
+            uint32_t qf[NT][16];
+            int sig_c[NT][2];
+            setup_index_query<NT>(qraw, a.Q, qh, sig, qf, sig_c);
+            const int lim = ctx - a.Q;   // token j counts for query n iff j <= lim + n
+    #pragma unroll 1
+            for (int i0 = 0; i0 < np; i0 += 4) {
+                if (i0 + 4 < np) load_page(fb, i0 + 4 + pq, false);
+                const int i = i0 + pq;
+                if (i < np) {
+                    float best = -INFINITY;
+                    if (phys_s[i] >= 0) {
+    #pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            best = fmaxf(best, score_tile<NT>(fa[k], qf, sig_c, p0 + i, tile0 + k, g, t, lim, a.Q));
+                    } else if ((warp & 1) == 0 && lane == 0) {
+                        flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                    }
+    #pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
+                    if (lane == 0) red[i % kRedPages][warp & 1] = best;
+                }
+                if ((i0 + 4) % kRedPages == 0 || i0 + 4 >= np) {   // page maxima of pages [base, i0 + 4)
+                    __syncthreads();
+                    const int base = (i0 / kRedPages) * kRedPages;
+                    const int cnt = min(i0 + 4, np) - base;
+                    if ((int)threadIdx.x < cnt)
+                        a.scores[(int64_t)b * a.max_pages + p0 + base + threadIdx.x] =
+                            fmaxf(red[threadIdx.x][0], red[threadIdx.x][1]);
+                    __syncthreads();
+                }
+    #pragma unroll
+                for (int k = 0; k < 4; ++k) fa[k] = fb[k];
+            }
+
+            __syncthreads();
+            if (threadIdx.x == 0) red_release_add(&a.row_cnt[kCounterStride * b], 1u);
         }
 
-        __syncthreads();
-        if (threadIdx.x == 0) red_release_add(&a.row_cnt[kCounterStride * b], 1u);
     }
 
     // ---------------- B. attention units ----------------
@@ -368,17 +428,24 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
             }
             if (threadIdx.x == 0 && !wait_geq_bounded(&a.row_cnt[kCounterStride * b], (uint32_t)C)) flag_status(a.status, SMX_DEV_TIMEOUT);
             __syncthreads();   // the row is scored; the staged q rows are packed (the V and P tiles are free)
-            load_keys<true>(keys, a.scores + (int64_t)b * a.max_pages, n_pages);
-            __syncthreads();
-            const int k_eff = block_select(keys, n_pages, a.topk, sel_all, selsm);
+            int k_eff;
+            if constexpr (REUSE) {
+                k_eff = given_selection(a, b, n_pages, sel_all);
+            } else {
+                load_keys<true>(keys, a.scores + (int64_t)b * a.max_pages, n_pages);
+                __syncthreads();
+                k_eff = block_select(keys, n_pages, a.topk, sel_all, selsm);
+            }
             const int lo = (int)(((int64_t)s * k_eff) / a.S), hi = (int)(((int64_t)(s + 1) * k_eff) / a.S);
             auto resolve = [&](int i) {   // entry i of this partition: logical and physical page
                 const int p = sel_all[lo + i];
-                const int64_t v = pt_cached ? pt_s[p] : a.page_table[(int64_t)b * a.max_pages + p];
                 int ph = -1;
-                if (v >= 0 && v < a.n_pool) ph = (int)v;
-                else flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
-                sel[i] = p;
+                if (p >= 0) {   // (a reused selection's bad id is -1: an empty page)
+                    const int64_t v = pt_cached ? pt_s[p] : a.page_table[(int64_t)b * a.max_pages + p];
+                    if (v >= 0 && v < a.n_pool) ph = (int)v;
+                    else flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                }
+                sel[i] = max(p, 0);
                 selph[i] = ph;
                 return ph;
             };
@@ -398,7 +465,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
                 }
             }
             for (int i = 2 + threadIdx.x; i < hi - lo; i += blockDim.x) resolve(i);
-            if (kvh == 0 && rg == 0 && s == 0) {
+            if (!REUSE && kvh == 0 && rg == 0 && s == 0) {
                 for (int i = threadIdx.x; i < a.topk; i += blockDim.x)
                     a.topk_out[(int64_t)b * a.topk + i] = i < k_eff ? sel_all[i] : -1;
                 if (threadIdx.x == 0) a.count_out[b] = k_eff;
@@ -470,17 +537,25 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
             }
             if (threadIdx.x == 0 && !wait_geq_bounded(&a.row_cnt[kCounterStride * b], (uint32_t)C)) flag_status(a.status, SMX_DEV_TIMEOUT);
             __syncthreads();
-            load_keys<true>(keys, a.scores + (int64_t)b * a.max_pages, n_pages);
-            __syncthreads();   // keys in place; the staged q rows read (the page stages are free)
-            const int k_eff = block_select(keys, n_pages, a.topk, sel_all, selsm);
+            int k_eff;
+            if constexpr (REUSE) {
+                __syncthreads();   // the staged q rows read (the page stages are free)
+                k_eff = given_selection(a, b, n_pages, sel_all);
+            } else {
+                load_keys<true>(keys, a.scores + (int64_t)b * a.max_pages, n_pages);
+                __syncthreads();   // keys in place; the staged q rows read (the page stages are free)
+                k_eff = block_select(keys, n_pages, a.topk, sel_all, selsm);
+            }
             const int lo = (int)(((int64_t)s * k_eff) / a.S), hi = (int)(((int64_t)(s + 1) * k_eff) / a.S);
             auto resolve = [&](int i) {   // entry i of this partition: logical and physical page
                 const int p = sel_all[lo + i];
-                const int64_t v = pt_cached ? pt_s[p] : a.page_table[(int64_t)b * a.max_pages + p];
                 int ph = -1;
-                if (v >= 0 && v < a.n_pool) ph = (int)v;
-                else flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
-                sel[i] = p;
+                if (p >= 0) {   // (a reused selection's bad id is -1: an empty page)
+                    const int64_t v = pt_cached ? pt_s[p] : a.page_table[(int64_t)b * a.max_pages + p];
+                    if (v >= 0 && v < a.n_pool) ph = (int)v;
+                    else flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                }
+                sel[i] = max(p, 0);
                 selph[i] = ph;
                 return ph;
             };
@@ -493,7 +568,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
                     attend_issue(sm, i, sel_all[lo + i], resolve(i), gp, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes);
             }
             for (int i = 2 + threadIdx.x; i < hi - lo; i += blockDim.x) resolve(i);
-            if (kvh == 0 && rg == 0 && s == 0) {
+            if (!REUSE && kvh == 0 && rg == 0 && s == 0) {
                 for (int i = threadIdx.x; i < a.topk; i += blockDim.x)
                     a.topk_out[(int64_t)b * a.topk + i] = i < k_eff ? sel_all[i] : -1;
                 if (threadIdx.x == 0) a.count_out[b] = k_eff;
@@ -570,14 +645,22 @@ StepGeom step_geom(const smx_shape_t& s, bool tc) {
     return g;
 }
 
-template <bool RS, int NT, bool TC>
+template <bool RS, int NT, bool TC, bool REUSE>
 static const void* step_fn() {
-    return reinterpret_cast<const void*>(decode_step_kernel<RS, NT, TC>);
+    return reinterpret_cast<const void*>(decode_step_kernel<RS, NT, TC, REUSE>);
 }
 
-static const void* step_fn(bool rs, bool nt2, bool tc) {
-    if (tc) return rs ? (nt2 ? step_fn<true, 2, true>() : step_fn<true, 1, true>()) : (nt2 ? step_fn<false, 2, true>() : step_fn<false, 1, true>());
-    return rs ? (nt2 ? step_fn<true, 2, false>() : step_fn<true, 1, false>()) : (nt2 ? step_fn<false, 2, false>() : step_fn<false, 1, false>());
+// The step kernel variant: FP8-KV pages (rs), 9..16 query tokens (nt2: two n-tiles in the
+// scorer), tensor-core attention (tc), a reused selection (reuse: no scorer, so one n-tile form).
+static const void* step_fn(bool rs, bool nt2, bool tc, bool reuse = false) {
+    if (reuse) {
+        if (tc) return rs ? step_fn<true, 1, true, true>() : step_fn<false, 1, true, true>();
+        return rs ? step_fn<true, 1, false, true>() : step_fn<false, 1, false, true>();
+    }
+    if (tc) return rs ? (nt2 ? step_fn<true, 2, true, false>() : step_fn<true, 1, true, false>())
+                      : (nt2 ? step_fn<false, 2, true, false>() : step_fn<false, 1, true, false>());
+    return rs ? (nt2 ? step_fn<true, 2, false, false>() : step_fn<true, 1, false, false>())
+              : (nt2 ? step_fn<false, 2, false, false>() : step_fn<false, 1, false, false>());
 }
 
 // Resident CTAs of the step kernel on the current device (cached per device, kernel and size).
@@ -622,12 +705,27 @@ bool decode_step_uses_tc(const smx_shape_t& s) {
     return use_tc(s, step_max_ctas(fn, geo.smem));
 }
 
-cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStream_t st) {
+// One cooperative launch of a step kernel variant (every CTA resident, at most one per SM).
+static cudaError_t launch_step_kernel(const void* fn, int n_ctas, size_t smem, cudaStream_t st, StepArgs a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_ctas);
+    cfg.blockDim = dim3(kStepWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, reinterpret_cast<void (*)(StepArgs)>(const_cast<void*>(fn)), a);
+}
+
+cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStream_t st, bool reuse) {
     const bool rs = s.kv_format == SMX_KV_E4M3_ROWSCALE;
     const bool nt2 = s.Q > 8;
     const bool tc = decode_step_uses_tc(s);
     const StepGeom geo = step_geom(s, tc);
-    const void* fn = step_fn(rs, nt2, tc);
+    const void* fn = step_fn(rs, nt2, tc, reuse);
     cudaError_t e = ensure_smem_attr(fn, (int)geo.smem);
     if (e != cudaSuccess) return e;
     const int max_ctas = step_max_ctas(fn, geo.smem);
@@ -647,33 +745,28 @@ cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStrea
     a.B = s.B; a.Q = s.Q; a.Hq = s.Hq; a.Hkv = s.Hkv; a.G = s.Hq / s.Hkv; a.max_pages = s.max_pages_per_row;
     a.topk = s.topk; a.S = s.num_splits;
     a.row_warps = geo.row_warps; a.rows_per_cta = geo.rows_per_cta; a.n_rg = geo.n_rg; a.page_bytes = geo.page_bytes;
+    a.topk_in = io.topk_in; a.count_in = io.count_in;
 
     // grid: enough CTAs for every attention unit and for two pages each, at most one per SM
     const int64_t n_units = (int64_t)s.B * s.Hkv * geo.n_rg * s.num_splits;
     const int64_t slots = (int64_t)s.B * s.max_pages_per_row;
+    if (reuse) {
+        // no scoring: chunks of a row only write its new K/V rows, one row per warp
+        const int kv_rows = s.Q * 2 * s.Hkv;
+        const int C = (kv_rows + kStepWarps - 1) / kStepWarps;
+        const int64_t want = n_units > (int64_t)s.B * C ? n_units : (int64_t)s.B * C;
+        a.chunk_pages = 0;
+        a.chunks_per_row = C;
+        const int n_ctas = (int)(want < max_ctas ? want : max_ctas);
+        return launch_step_kernel(fn, n_ctas, geo.smem, st, a);
+    }
     const int64_t want = n_units > (slots + 1) / 2 ? n_units : (slots + 1) / 2;
     const int n_ctas = (int)(want < max_ctas ? want : max_ctas);
     int64_t P = (slots + n_ctas - 1) / n_ctas;
     if (P > kStepMaxChunk) P = kStepMaxChunk;
     a.chunk_pages = (int)P;
     a.chunks_per_row = (int)((s.max_pages_per_row + P - 1) / P);
-
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(n_ctas);
-    cfg.blockDim = dim3(kStepWarps * 32);
-    cfg.dynamicSmemBytes = geo.smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (tc) {
-        if (rs) return nt2 ? cudaLaunchKernelEx(&cfg, decode_step_kernel<true, 2, true>, a) : cudaLaunchKernelEx(&cfg, decode_step_kernel<true, 1, true>, a);
-        return nt2 ? cudaLaunchKernelEx(&cfg, decode_step_kernel<false, 2, true>, a) : cudaLaunchKernelEx(&cfg, decode_step_kernel<false, 1, true>, a);
-    }
-    if (rs) return nt2 ? cudaLaunchKernelEx(&cfg, decode_step_kernel<true, 2, false>, a) : cudaLaunchKernelEx(&cfg, decode_step_kernel<true, 1, false>, a);
-    return nt2 ? cudaLaunchKernelEx(&cfg, decode_step_kernel<false, 2, false>, a) : cudaLaunchKernelEx(&cfg, decode_step_kernel<false, 1, false>, a);
+    return launch_step_kernel(fn, n_ctas, geo.smem, st, a);
 }
 
 }  // namespace smx

@@ -27,7 +27,8 @@ DEV_BAD_PAGE_ID, DEV_BAD_CTX, DEV_BAD_TOPK = 1, 2, 4
 SYMBOLS = ("smx_workspace_bytes", "smx_kv_insert", "smx_kv_prefill", "smx_pack_q_e4m3",
            "smx_index_score", "smx_index_score_topk", "smx_sparse_attn_split", "smx_sparse_attn_merge",
            "smx_decode_step", "smx_status_string", "smx_decode_step_launches",
-           "smx_suggest_num_splits", "smx_decode_step_noalloc", "smx_decode_step_tensor_cores")
+           "smx_suggest_num_splits", "smx_decode_step_noalloc", "smx_decode_step_tensor_cores",
+           "smx_decode_step_reuse")
 
 
 class SmxError(RuntimeError):
@@ -94,6 +95,7 @@ def lib() -> ctypes.CDLL:
             "smx_sparse_attn_split": (ctypes.c_int, [S] + [P] * 11 + [ST]),
             "smx_sparse_attn_merge": (ctypes.c_int, [S, P, P, P, P, ST]),
             "smx_decode_step": (ctypes.c_int, [S] + [P] * 15 + [ctypes.c_size_t, P, ST]),
+            "smx_decode_step_reuse": (ctypes.c_int, [S] + [P] * 12 + [ctypes.c_size_t, P, ST]),
             "smx_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "smx_decode_step_launches": (ctypes.c_int, [S]),
             "smx_suggest_num_splits": (ctypes.c_int, [S]),
@@ -267,6 +269,24 @@ def decode_step(shape, *, q_f32=None, q_bf16=None, qidx_bf16, k_new, v_new, kidx
                                  _p(workspace), workspace.numel(), _p(dev_status), _st(stream)),
            "smx_decode_step")
     return out, topk_pages, topk_count
+
+
+def decode_step_reuse(shape, *, q_f32=None, q_bf16=None, k_new, v_new, page_table, ctx_len, k_pool, v_pool,
+                      topk_pages, topk_count, out=None, workspace=None, dev_status=None, stream=None):
+    """The step of a layer reusing an earlier layer's selection (topk_pages [B][topk] and
+    topk_count [B] int32, inputs): K/V insert, q packing, split and merge."""
+    dev = _dev(k_pool)
+    if out is None:
+        out = torch.empty((shape.B, shape.Q, shape.Hq, 128), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(shape, dev)
+    cs = shape.c()
+    _check(lib().smx_decode_step_reuse(ctypes.byref(cs), _p(q_f32), _p(q_bf16), _p(k_new), _p(v_new),
+                                       _p(page_table), _p(ctx_len), _p(k_pool), _p(v_pool), _p(topk_pages),
+                                       _p(topk_count), _p(out), _p(workspace), workspace.numel(), _p(dev_status),
+                                       _st(stream)),
+           "smx_decode_step_reuse")
+    return out
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20

@@ -44,6 +44,55 @@ def gpu_step(w, data, pools, num_splits=None):
                 status=int(status.item()))
 
 
+def gpu_step_reuse(w, data, pools, topk_pages, topk_count, num_splits=None):
+    """The reusing layer's step through the C ABI on device copies of the inputs."""
+    shape = ops.Shape.of(w, num_splits)
+    g = gpu_inputs(w, data, pools)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = ops.decode_step_reuse(
+        shape, q_f32=g["q_f32"] if w.kv_format == wl.KV_MXFP4 else None,
+        q_bf16=g["q_bf16"] if w.kv_format == wl.KV_E4M3_ROWSCALE else None,
+        k_new=g["k_new"], v_new=g["v_new"], page_table=g["page_table"], ctx_len=g["ctx_len"],
+        k_pool=g["k_pool"], v_pool=g["v_pool"], topk_pages=dev_t(np.asarray(topk_pages, np.int32)),
+        topk_count=dev_t(np.asarray(topk_count, np.int32)), dev_status=status)
+    torch.cuda.synchronize()
+    return dict(out=out.cpu().numpy(), pools=tuple(g[k].cpu().numpy() for k in ("k_pool", "v_pool", "idx_pool")),
+                status=int(status.item()))
+
+
+def random_selection(w, data, seed):
+    """Another layer's selection: seeded distinct pages of each row, ascending, padded with -1."""
+    rng = np.random.default_rng(seed)
+    n_pages = (data["ctx_len"] + 127) // 128
+    pages = -np.ones((w.B, w.topk), np.int32)
+    count = np.zeros(w.B, np.int32)
+    for b in range(w.B):
+        k = min(w.topk, int(n_pages[b]))
+        pages[b, :k] = np.sort(rng.choice(int(n_pages[b]), size=k, replace=False))
+        count[b] = k
+    return pages, count
+
+
+def reuse_parity(w, pages, count, data=None, num_splits=None):
+    """The reusing layer's step against the oracle: K/V pool bytes bit-exact, the index pool
+    untouched, the attention within the bound."""
+    data = data if data is not None else wl.generate(w)
+    pools = H.oracle_pools(w, data)
+    kp, vp = pools[0].copy(), pools[1].copy()
+    ref = oracle.decode_step_reuse(oracle.shape_of(w, num_splits), q_f32=data["q"], q_bf16=data["q_bf16"],
+                                   k_new=data["k_new"], v_new=data["v_new"], page_table=data["page_table"],
+                                   ctx_len=data["ctx_len"], k_pool=kp, v_pool=vp, topk_pages=pages,
+                                   topk_count=count)
+    got = gpu_step_reuse(w, data, pools, pages, count, num_splits)
+    assert got["status"] == 0
+    assert np.array_equal(got["pools"][0], kp) and np.array_equal(got["pools"][1], vp), "inserted K/V bytes differ"
+    assert np.array_equal(got["pools"][2], pools[2]), "the index pool was written"
+    assert np.all(np.isfinite(got["out"]))
+    ok, err = attn_close(got["out"], ref["out"])
+    assert ok, f"max err {err}"
+    return err
+
+
 def check_topk_sets(ref_scores, ref_pages, ref_count, gpu_pages, gpu_count):
     """Sets must be equal except for swaps between pages whose oracle scores differ by less
     than 1e-5 relative. Returns the number of swapped pages."""

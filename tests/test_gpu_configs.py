@@ -168,6 +168,37 @@ def test_tensor_core_bad_page_ids_are_flagged_and_skipped():
     assert np.all(np.isfinite(got["out"]))
 
 
+@pytest.mark.parametrize("fmt", [wl.KV_MXFP4, wl.KV_E4M3_ROWSCALE])
+@pytest.mark.parametrize("tc", [False, True])
+@pytest.mark.parametrize("sel", ["scored", "random"])
+def test_reuse_step(fmt, tc, sel):
+    # a layer reusing an earlier layer's selection: the full step's own selection (the scorer's)
+    # or a seeded random one, on the mma.sync path (B 4, S 4) and the tensor-core path (B 8, S 12)
+    kw = dict(big_row_frac=0.01) if fmt == wl.KV_E4M3_ROWSCALE else {}
+    w = wl.Workload("reuse", B=8 if tc else 4, Q=8, Hq=16, Hkv=1, max_ctx=6000, topk=8, num_splits=12 if tc else 4,
+                    kv_format=fmt, seed=818, ragged=True, **kw)
+    assert _uses_tc(w) == tc
+    data = wl.generate(w)
+    if sel == "scored":
+        res, _ = H.oracle_step(w, data, H.oracle_pools(w, data))
+        pages, count = res["topk_pages"], res["topk_count"]
+    else:
+        pages, count = C.random_selection(w, data, 19)
+    C.reuse_parity(w, pages, count, data=data)
+
+
+def test_reuse_step_flags_bad_selections():
+    w = wl.Workload("reuse_bad", B=4, Q=8, Hq=16, Hkv=1, max_ctx=3000, topk=8, num_splits=4, seed=9, ragged=True)
+    data = wl.generate(w)
+    pools = H.oracle_pools(w, data)
+    pages, count = C.random_selection(w, data, 3)
+    pages[0, 1] = 10000          # past the row's pages
+    count[1] = w.topk + 5        # more than topk
+    got = C.gpu_step_reuse(w, data, pools, pages, count)
+    assert got["status"] & ops.DEV_BAD_PAGE_ID
+    assert np.all(np.isfinite(got["out"]))
+
+
 def test_configs_take_the_mma_path():
     # the benchmark workloads at the suggested partition counts fit one wave of 64-row units
     for c in (2, 3, 4):
