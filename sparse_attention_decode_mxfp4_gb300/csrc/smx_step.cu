@@ -148,8 +148,9 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
         mbar_init(&mbar_mma[1], 1);
         mbar_fence_init();
     }
-    __syncthreads();   // the barriers are initialised before any thread polls one (a CTA with no
-                       // scoring chunk reaches its attention unit's q wait without another barrier)
+    // the barriers are initialised before any thread polls one: a CTA with no chunk in phase A
+    // reaches its attention unit's q wait without another barrier
+    if (blockIdx.x >= a.B * a.chunks_per_row) __syncthreads();
 
     const int P = a.chunk_pages, C = a.chunks_per_row;
     const int kv_rows = a.Q * 2 * a.Hkv;
