@@ -89,10 +89,10 @@ def kernel_sources_sha():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_name):
-    """DRAM bytes per launch of the decode-step kernel from a committed ncu summary, if it was
-    taken on the current kernel source and this workload; else None."""
-    p = os.path.join(ROOT, "profiles", "decode_step_traffic.json")
+def recorded_traffic(workload_name, reuse=False):
+    """DRAM bytes per launch of the decode-step kernel (reuse: its reusing-layer variant) from a
+    committed ncu summary, if it was taken on the current kernel source and this workload; else None."""
+    p = os.path.join(ROOT, "profiles", "decode_step_reuse_traffic.json" if reuse else "decode_step_traffic.json")
     if not os.path.exists(p):
         return None
     try:
@@ -403,7 +403,7 @@ def main():
                               f"{R * step_bytes / 1e6:.0f} MB per rotation > 3x L2 {l2 / 1e6:.0f} MB)"),
             "roofline": {"bound": "hbm", "kernel": "decode_step_kernel", "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": None if args.reuse else recorded_traffic(w.name), "us_per_launch": kernel_us,
+                         "traffic": recorded_traffic(w.name, args.reuse), "us_per_launch": kernel_us,
                          "algorithmic_bytes_per_launch": step_bytes // launches_per_step},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "GB/s", "us_per_step": e2e_s * 1e6, "h2d_bytes_per_step": h2d,
