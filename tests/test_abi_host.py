@@ -58,6 +58,8 @@ def test_bad_shapes_are_refused(L, kw, code):
     assert rc == code
     rc = L.smx_sparse_attn_merge(ctypes.byref(cs), fake, fake, fake, fake, None)
     assert rc == code
+    rc = L.smx_decode_step_reuse(ctypes.byref(cs), *([fake] * 12), 1 << 30, None, None)
+    assert rc == code
 
 
 def test_null_and_misaligned_pointers_are_refused(L):
@@ -77,6 +79,29 @@ def test_null_and_misaligned_pointers_are_refused(L):
     # MXFP4 K/V needs q_f32
     args2 = [None] + [a] * 13
     assert L.smx_decode_step(ctypes.byref(cs), *args2, a, ws, None, None) == -1
+
+
+def test_reuse_step_refuses_null_misaligned_and_workspace(L):
+    cs = good_shape().c()
+    a = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 4)
+    ws = L.smx_workspace_bytes(ctypes.byref(cs))
+    # q_f32, q_bf16, k_new, v_new, page_table, ctx_len, k_pool, v_pool, topk_pages, topk_count, out
+    ok = [a] * 11
+    assert L.smx_decode_step_reuse(ctypes.byref(cs), *ok, a, ws - 256, None, None) == -4
+    assert L.smx_decode_step_reuse(ctypes.byref(cs), *ok, None, ws, None, None) == -4
+    for i in (0, 2, 3, 4, 5, 6, 7, 8, 9, 10):   # q_f32 (MXFP4 K/V) and every other required pointer
+        args = list(ok)
+        args[i] = None
+        assert L.smx_decode_step_reuse(ctypes.byref(cs), *args, a, ws, None, None) == -1, i
+    for i in (0, 2, 3, 6, 7):   # 16-byte aligned: q_f32, k_new, v_new, k_pool, v_pool
+        args = list(ok)
+        args[i] = mis
+        assert L.smx_decode_step_reuse(ctypes.byref(cs), *args, a, ws, None, None) == -1, i
+    # q_bf16 may be NULL with MXFP4 K/V (q_f32 is the one used)
+    args = list(ok)
+    args[1] = None
+    assert L.smx_decode_step_reuse(ctypes.byref(cs), *args, a, ws - 256, None, None) == -4
 
 
 def test_status_strings(L):
