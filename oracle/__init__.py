@@ -47,7 +47,8 @@ class _Shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("Q", ctypes.c_int32), ("Hq", ctypes.c_int32),
                 ("Hkv", ctypes.c_int32), ("max_pages", ctypes.c_int32),
                 ("n_pool_pages", ctypes.c_int64), ("topk", ctypes.c_int32),
-                ("num_splits", ctypes.c_int32), ("kv_format", ctypes.c_int32)]
+                ("num_splits", ctypes.c_int32), ("kv_format", ctypes.c_int32),
+                ("pages_per_block", ctypes.c_int32)]
 
 
 @dataclass
@@ -61,10 +62,11 @@ class Shape:
     topk: int
     num_splits: int
     kv_format: int = KV_MXFP4
+    pages_per_block: int = 1
 
     def c(self) -> _Shape:
         return _Shape(self.B, self.Q, self.Hq, self.Hkv, self.max_pages, self.n_pool_pages,
-                      self.topk, self.num_splits, self.kv_format)
+                      self.topk, self.num_splits, self.kv_format, self.pages_per_block)
 
     @property
     def kv_page_bytes(self) -> int:
@@ -74,7 +76,8 @@ class Shape:
 def shape_of(w, num_splits=None) -> Shape:
     """Oracle shape of a workload object (anything with B, Q, Hq, Hkv, max_pages, ...)."""
     return Shape(w.B, w.Q, w.Hq, w.Hkv, w.max_pages, w.n_pool_pages, w.topk,
-                 w.num_splits if num_splits is None else num_splits, w.kv_format)
+                 w.num_splits if num_splits is None else num_splits, w.kv_format,
+                 getattr(w, "pages_per_block", 1))
 
 
 def lib():

@@ -375,20 +375,37 @@ static int beats(double sa, int64_t a, double sb, int64_t b) {
     return a < b;
 }
 
+/* Pages per selected block ([ATOM-2812] commit "MXFP4 main KV": a selected block is one page of
+ * the sparse table, PAGES_PER_BLOCK a build parameter). Reading for blocks of several pages: a
+ * block's score is the max of its pages' scores (NaN left out, as for tokens), the top-k ranks
+ * blocks with the same rule as pages, and the split stage takes every page of a selected block
+ * that lies in the row. */
+static int ppb_of(const orc_shape* sh) { return sh->pages_per_block > 1 ? sh->pages_per_block : 1; }
+
 void orc_topk(const orc_shape* sh, const double* scores, const int32_t* ctx_len,
               int32_t* topk_pages, int32_t* topk_count) {
+    const int ppb = ppb_of(sh);
     for (int b = 0; b < sh->B; ++b) {
         int64_t n = n_pages_of(sh, ctx_len[b]);
-        int64_t k_eff = sh->topk < n ? sh->topk : n;
+        int64_t nb = (n + ppb - 1) / ppb;
+        int64_t k_eff = sh->topk < nb ? sh->topk : nb;
         const double* s = scores + (size_t)b * sh->max_pages;
         int32_t* out = topk_pages + (size_t)b * sh->topk;
+        double* bs = (double*)malloc((size_t)(nb > 0 ? nb : 1) * sizeof(double));
+        for (int64_t blk = 0; blk < nb; ++blk) {
+            double m = NAN;
+            for (int64_t p = blk * ppb; p < (blk + 1) * ppb && p < n; ++p)
+                if (!isnan(s[p]) && (isnan(m) || s[p] > m)) m = s[p];
+            bs[blk] = m;
+        }
         int c = 0;
-        for (int64_t p = 0; p < n; ++p) {
+        for (int64_t p = 0; p < nb; ++p) {
             int64_t rank = 0;
-            for (int64_t o = 0; o < n; ++o)
-                if (o != p && beats(s[o], o, s[p], p)) ++rank;
+            for (int64_t o = 0; o < nb; ++o)
+                if (o != p && beats(bs[o], o, bs[p], p)) ++rank;
             if (rank < k_eff) out[c++] = (int32_t)p;
         }
+        free(bs);
         for (int i = c; i < sh->topk; ++i) out[i] = -1;
         topk_count[b] = c;
     }
@@ -401,7 +418,8 @@ void orc_topk(const orc_shape* sh, const double* scores, const int32_t* ctx_len,
  *   T = { j : page(j) selected, j < ctx_len, j <= pos_t };
  *   z_j = (sum_d q[d] K_j[d]) / sqrt(128), fp64.
  * Readings: partition s of S takes positions [floor(s k_eff / S), floor((s+1) k_eff / S)) of
- * the ascending list (S > k_eff gives empty partitions); m is kept in the log2 domain,
+ * the ascending list (S > k_eff gives empty partitions); with blocks of several pages an entry is
+ * a block id and stands for the block's pages in the row; m is kept in the log2 domain,
  *   m_s = max_j z_j log2(e),  l_s = sum_j 2^(z_j log2(e) - m_s),
  *   o_s = sum_j 2^(z_j log2(e) - m_s) V_j      (unnormalised);
  * a partition with no token stores m = -inf, l = 0, o = 0.
@@ -419,7 +437,7 @@ void orc_sparse_attn_split(const orc_shape* sh, const void* q, const uint8_t* k_
                            const int32_t* ctx_len, const int32_t* topk_pages,
                            const int32_t* topk_count, double* part_o, double* part_m,
                            double* part_l) {
-    const int S = sh->num_splits, G = sh->Hq / sh->Hkv;
+    const int S = sh->num_splits, G = sh->Hq / sh->Hkv, ppb = ppb_of(sh);
     const double inv_sqrt_d = 1.0 / sqrt((double)ORC_D);
     int64_t total = (int64_t)sh->B * sh->Q * sh->Hq;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -429,6 +447,7 @@ void orc_sparse_attn_split(const orc_shape* sh, const void* q, const uint8_t* k_
         int h = (int)(bth % sh->Hq);
         int kvh = h / G;
         int64_t ctx = ctx_len[b], pos_t = ctx - sh->Q + t;
+        int64_t n_row = n_pages_of(sh, ctx_len[b]);
         int k_eff = topk_count[b];
         double qv[ORC_D], krow[ORC_D], vrow[ORC_D];
         size_t qbase = (((size_t)b * sh->Q + t) * sh->Hq + h) * ORC_D;
@@ -439,8 +458,9 @@ void orc_sparse_attn_split(const orc_shape* sh, const void* q, const uint8_t* k_
             double* o = part_o + pi * ORC_D;
             double m = -INFINITY, l = 0.0;
             /* pass 1: the maximum */
-            for (int i = lo; i < hi; ++i) {
-                int64_t p = topk_pages[(size_t)b * sh->topk + i];
+            for (int64_t e = (int64_t)lo * ppb; e < (int64_t)hi * ppb; ++e) {
+                int64_t p = (int64_t)topk_pages[(size_t)b * sh->topk + e / ppb] * ppb + e % ppb;
+                if (p >= n_row) continue;   /* the row's last block may end past its pages */
                 int64_t phys = page_table[(size_t)b * sh->max_pages + p];
                 const uint8_t* kp = kv_page(sh, (uint8_t*)k_pool, phys, kvh);
                 for (int slot = 0; slot < ORC_PAGE; ++slot) {
@@ -456,8 +476,9 @@ void orc_sparse_attn_split(const orc_shape* sh, const void* q, const uint8_t* k_
             for (int d = 0; d < ORC_D; ++d) o[d] = 0.0;
             /* pass 2: weights and the weighted sum */
             if (m != -INFINITY) {
-                for (int i = lo; i < hi; ++i) {
-                    int64_t p = topk_pages[(size_t)b * sh->topk + i];
+                for (int64_t e = (int64_t)lo * ppb; e < (int64_t)hi * ppb; ++e) {
+                    int64_t p = (int64_t)topk_pages[(size_t)b * sh->topk + e / ppb] * ppb + e % ppb;
+                    if (p >= n_row) continue;
                     int64_t phys = page_table[(size_t)b * sh->max_pages + p];
                     const uint8_t* kp = kv_page(sh, (uint8_t*)k_pool, phys, kvh);
                     const uint8_t* vp = kv_page(sh, (uint8_t*)v_pool, phys, kvh);

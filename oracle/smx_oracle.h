@@ -40,6 +40,7 @@ typedef struct {
     int32_t topk;           /* k (pages) */
     int32_t num_splits;     /* S partitions of the selected list */
     int32_t kv_format;      /* ORC_KV_* for the K/V pools; the index pool is always MXFP4 */
+    int32_t pages_per_block; /* pages per selected block (0 or 1: one page) */
 } orc_shape;
 
 /* ---- element formats ---- */

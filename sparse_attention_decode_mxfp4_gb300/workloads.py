@@ -51,6 +51,7 @@ class Workload:
     big_row_factor: float = 50.0
     shift_page_frac: float = 0.0
     shift_value: float = 3.0
+    pages_per_block: int = 1        # pages per selected block of the sparse table
 
     @property
     def max_pages(self) -> int:

@@ -249,3 +249,52 @@ def test_reuse_attends_over_exactly_the_given_pages(fmt):
     res, _ = H.oracle_step(w, data, pools)
     if not np.array_equal(np.sort(res["topk_pages"], axis=1), np.sort(pages, axis=1)):
         assert not np.allclose(rr["out"], res["out"])
+
+
+def _expand_blocks(w, data, pages, count, ppb):
+    """Page lists of selected blocks: every page of each block that lies in the row."""
+    n_pages = (data["ctx_len"] + 127) // 128
+    out = -np.ones((w.B, w.topk * ppb), np.int32)
+    cnt = np.zeros(w.B, np.int32)
+    for b in range(w.B):
+        pl = [blk * ppb + q for blk in pages[b, :count[b]] for q in range(ppb) if blk * ppb + q < n_pages[b]]
+        out[b, :len(pl)] = pl
+        cnt[b] = len(pl)
+    return out, cnt
+
+
+@pytest.mark.parametrize("ppb", [2, 4])
+def test_block_selection_ranks_block_maxima(ppb):
+    # with blocks of several pages the top-k ranks each block by its best page (ties to the lower
+    # block id), against a brute-force ranking of the oracle's own page scores
+    w = small(topk=3, max_ctx=2600, pages_per_block=ppb, B=3)
+    data, pools = _case(w)
+    res, _ = H.oracle_step(w, data, pools)
+    for b in range(w.B):
+        n = (int(data["ctx_len"][b]) + 127) // 128
+        nb = (n + ppb - 1) // ppb
+        bs = [np.nanmax(res["scores"][b, k * ppb:min(n, (k + 1) * ppb)]) for k in range(nb)]
+        order = sorted(range(nb), key=lambda k: (-bs[k], k))[:min(w.topk, nb)]
+        assert res["topk_count"][b] == len(order)
+        assert list(res["topk_pages"][b, :len(order)]) == sorted(order)
+
+
+@pytest.mark.parametrize("fmt", [wl.KV_MXFP4, wl.KV_E4M3_ROWSCALE])
+@pytest.mark.parametrize("ppb", [2, 4])
+def test_blocks_attend_over_their_pages(fmt, ppb):
+    # the step's attention over selected blocks = dense attention over exactly their pages' tokens,
+    # and = the page-granular split handed the expanded page list
+    w = small(fmt, topk=2, max_ctx=2600, pages_per_block=ppb, B=3, num_splits=3)
+    data, pools = _case(w)
+    res, new_pools = H.oracle_step(w, data, pools)
+    q = H.q_values(w, data, res)
+    pages, cnt = _expand_blocks(w, data, res["topk_pages"], res["topk_count"], ppb)
+    ref = H.dense_selected_attention(w, data, q, new_pools[0], new_pools[1], pages, cnt)
+    assert np.all(np.isfinite(res["out"]))
+    assert _close(res["out"], ref)
+    w1 = wl.shrink(w, pages_per_block=1, topk=w.topk * ppb)
+    sh1 = oracle.shape_of(w1)
+    qsrc = data["q_bf16"] if fmt == wl.KV_E4M3_ROWSCALE else res["q_e4m3"]
+    po, pm, pl = oracle.sparse_attn_split(sh1, qsrc, new_pools[0], new_pools[1], data["page_table"], data["ctx_len"],
+                                          pages, cnt)
+    assert _close(res["out"], oracle.sparse_attn_merge(sh1, po, pm, pl))
