@@ -89,6 +89,13 @@ typedef struct {
     int32_t topk;               /* k pages selected per row */
     int32_t num_splits;         /* S partitions of the selected list for the split stage */
     int32_t kv_format;          /* SMX_KV_*: K/V page format; the index pool is always MXFP4 */
+    int32_t pages_per_block;    /* pages per selected block: 0 or 1 (one page), 2 or 4 ([ATOM-2812]
+                                 * commit "MXFP4 main KV": PAGES_PER_BLOCK is a build parameter).
+                                 * With 2 or 4, topk counts blocks: a block's score is its best page's,
+                                 * topk_pages hold block ids (ascending), and the split stage takes
+                                 * every page of a selected block inside the row. Only the fused
+                                 * steps take 2 or 4; the standalone top-k and split stage refuse
+                                 * them (SMX_ERR_UNSUPPORTED). topk * pages_per_block <= 4096. */
 } smx_shape_t;
 
 /* Bytes of device workspace smx_decode_step needs for this shape (step counters, page scores,
@@ -179,7 +186,7 @@ int smx_decode_step(const smx_shape_t* shape, const float* q_f32, const uint16_t
  * smx_decode_step's outputs), which this layer's page_table maps to its own K/V pages. Arguments
  * as smx_decode_step (same workspace size; q_f32 or q_bf16 by format; k_new/v_new/k_pool/v_pool
  * 16-byte aligned). A count outside that range is clamped and an id outside the row's pages
- * skipped (an empty page), both flagged SMX_DEV_BAD_PAGE_ID in dev_status. One cooperative
+ * skipped (an empty page), both flagged SMX_DEV_BAD_TOPK in dev_status. One cooperative
  * kernel, as smx_decode_step without its scoring and selection. Returns SMX_OK,
  * SMX_ERR_INVALID_ARG (a NULL or misaligned pointer), SMX_ERR_UNSUPPORTED (shape),
  * SMX_ERR_WORKSPACE or SMX_ERR_CUDA. */

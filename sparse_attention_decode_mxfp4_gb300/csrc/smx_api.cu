@@ -59,8 +59,14 @@ int check_shape(const smx_shape_t* s) {
     if (s->n_pool_pages > 0x7FFFFFFF) return SMX_ERR_UNSUPPORTED;
     if (s->B > 65535 || s->num_splits > 65535 || (int64_t)s->Hkv * s->Hq * s->Q > 65535)
         return SMX_ERR_UNSUPPORTED;
+    const int ppb = s->pages_per_block;
+    if (ppb != 0 && ppb != 1 && ppb != 2 && ppb != 4) return SMX_ERR_UNSUPPORTED;
+    if ((int64_t)s->topk * (ppb > 1 ? ppb : 1) > SMX_MAX_TOPK) return SMX_ERR_UNSUPPORTED;
     return SMX_OK;
 }
+
+// The standalone top-k and split stage take one page per selected block only.
+static int check_page_blocks(const smx_shape_t* s) { return s->pages_per_block > 1 ? SMX_ERR_UNSUPPORTED : SMX_OK; }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? SMX_OK : SMX_ERR_CUDA; }
 
@@ -152,6 +158,7 @@ int smx_index_score_topk(const smx_shape_t* s, const uint16_t* qidx_bf16, const 
                          int32_t* topk_pages, int32_t* topk_count, int32_t* dev_status, smx_stream_t stream) {
     int rc = check_shape(s);
     if (rc) return rc;
+    if ((rc = check_page_blocks(s))) return rc;
     if (!qidx_bf16 || !idx_pool || !page_table || !ctx_len || !page_scores || !topk_pages || !topk_count)
         return SMX_ERR_INVALID_ARG;
     if (!aligned16(qidx_bf16) || !aligned16(idx_pool)) return SMX_ERR_INVALID_ARG;
@@ -168,6 +175,7 @@ int smx_sparse_attn_split(const smx_shape_t* s, const void* q, const uint8_t* k_
                           int32_t* dev_status, smx_stream_t stream) {
     int rc = check_shape(s);
     if (rc) return rc;
+    if ((rc = check_page_blocks(s))) return rc;
     if (!q || !k_pool || !v_pool || !page_table || !ctx_len || !topk_pages || !topk_count || !part_o ||
         !part_m || !part_l)
         return SMX_ERR_INVALID_ARG;

@@ -140,7 +140,8 @@ int suggest_num_splits(const smx_shape_t& s) {
     // pages per partition, one wave of 128-row tensor-core units (which the fused step then takes,
     // the 64-row units needing more than one wave) is faster. Measured on GB300, whole step: 4 to 8
     // pages per 64-row unit 10 to 26 % faster; at 2 pages about even, at 1 page mma.sync ahead.
-    if (s.kv_format == SMX_KV_MXFP4 && M > 64 && (s.topk + s_mma - 1) / s_mma >= 3) return one_wave_splits(s, 128, sms);
+    const int ppb = s.pages_per_block > 1 ? s.pages_per_block : 1;   // pages per selected block
+    if (s.kv_format == SMX_KV_MXFP4 && M > 64 && (s.topk + s_mma - 1) / s_mma * ppb >= 3) return one_wave_splits(s, 128, sms);
     return s_mma;
 }
 

@@ -67,6 +67,7 @@ struct StepArgs {
     int chunk_pages, chunks_per_row;
     const int32_t* topk_in;      // REUSE: the given selection [B][topk], and its counts [B]
     const int32_t* count_in;
+    int ppb_log2;                // log2 of the pages per selected block (0: one page)
 };
 
 constexpr int kStepWarps = 8;
@@ -75,17 +76,38 @@ constexpr int kRedPages = 32;        // page maxima combined per flush
 constexpr int kPtCache = 2048;       // page-table entries of a unit's row kept in shared memory
 constexpr int kCounterStride = 32;   // u32 words between counters: each on its own 128-byte line
 
+// Selection over blocks of 2^log2 pages: keys[0 .. n_pages) (page keys, shared memory) become
+// keys[0 .. n_blocks), each block's best page key (score_key is order-preserving; NaN pages, key 0,
+// lose to any number). In rounds of one block per thread: every read of a round comes before its
+// writes (a barrier), and a round's writes land below the next rounds' reads. Every thread.
+__device__ __forceinline__ int block_max_keys(uint32_t* keys, int n_pages, int log2) {
+    const int ppb = 1 << log2, nb = (n_pages + ppb - 1) >> log2;
+    for (int r0 = 0; r0 < nb; r0 += blockDim.x) {
+        const int blk = r0 + (int)threadIdx.x;
+        uint32_t m = 0u;
+        if (blk < nb)
+            for (int q = 0; q < ppb; ++q) {
+                const int p = (blk << log2) + q;
+                if (p < n_pages) m = max(m, keys[p]);
+            }
+        __syncthreads();
+        if (blk < nb) keys[blk] = m;
+    }
+    __syncthreads();
+    return nb;
+}
+
 // A reusing layer's selection for row b (entries [0, k_eff) of sel_all): the given count clamped
 // to [0, min(topk, n_pages)], each id checked against the row's pages (an id outside them is
 // flagged and becomes -1: an empty page). Every thread; ends with a barrier.
 __device__ __forceinline__ int given_selection(const StepArgs& a, int b, int n_pages, int* sel_all) {
     const int raw = a.count_in[b];
     const int k_eff = max(0, min(raw, min(a.topk, n_pages)));
-    if (threadIdx.x == 0 && raw != k_eff) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+    if (threadIdx.x == 0 && raw != k_eff) flag_status(a.status, SMX_DEV_BAD_TOPK);
     for (int i = threadIdx.x; i < k_eff; i += blockDim.x) {
         int p = a.topk_in[(int64_t)b * a.topk + i];
         if (p < 0 || p >= n_pages) {
-            flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+            flag_status(a.status, SMX_DEV_BAD_TOPK);
             p = -1;
         }
         sel_all[i] = p;
@@ -129,11 +151,11 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
     } else {
         sm = attend_smem(smem, a.page_bytes, mbar, stage_page);
         keys = reinterpret_cast<uint32_t*>(smem);
-        sel_all = reinterpret_cast<int*>(sm.raw + 4 * a.page_bytes) + 2 * a.topk;
+        sel_all = reinterpret_cast<int*>(sm.raw + 4 * a.page_bytes) + 2 * (a.topk << a.ppb_log2);
         q_stage = sm.raw;
     }
     int* sel = reinterpret_cast<int*>(sm.raw + 4 * a.page_bytes);   // this partition's pages
-    int* selph = sel + a.topk;                                       // and their physical ids
+    int* selph = sel + (a.topk << a.ppb_log2);                       // and their physical ids
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
@@ -429,19 +451,24 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
             }
             if (threadIdx.x == 0 && !wait_geq_bounded(&a.row_cnt[kCounterStride * b], (uint32_t)C)) flag_status(a.status, SMX_DEV_TIMEOUT);
             __syncthreads();   // the row is scored; the staged q rows are packed (the V and P tiles are free)
+            const int n_blocks = (n_pages + (1 << a.ppb_log2) - 1) >> a.ppb_log2;
             int k_eff;
             if constexpr (REUSE) {
-                k_eff = given_selection(a, b, n_pages, sel_all);
+                k_eff = given_selection(a, b, n_blocks, sel_all);
             } else {
                 load_keys<true>(keys, a.scores + (int64_t)b * a.max_pages, n_pages);
                 __syncthreads();
-                k_eff = block_select(keys, n_pages, a.topk, sel_all, selsm);
+                if (a.ppb_log2) block_max_keys(keys, n_pages, a.ppb_log2);
+                k_eff = block_select(keys, n_blocks, a.topk, sel_all, selsm);
             }
             const int lo = (int)(((int64_t)s * k_eff) / a.S), hi = (int)(((int64_t)(s + 1) * k_eff) / a.S);
+            const int npg = (hi - lo) << a.ppb_log2;   // the partition's blocks as pages (one block: one page)
             auto resolve = [&](int i) {   // entry i of this partition: logical and physical page
-                const int p = sel_all[lo + i];
+                const int blk = sel_all[lo + (i >> a.ppb_log2)];
+                int p = blk < 0 ? -1 : (blk << a.ppb_log2) + (i & ((1 << a.ppb_log2) - 1));
+                if (p >= n_pages) p = -1;   // past the row in its last block: an empty page
                 int ph = -1;
-                if (p >= 0) {   // (a reused selection's bad id is -1: an empty page)
+                if (p >= 0) {   // (a reused selection's bad id is -1: an empty page, flagged)
                     const int64_t v = pt_cached ? pt_s[p] : a.page_table[(int64_t)b * a.max_pages + p];
                     if (v >= 0 && v < a.n_pool) ph = (int)v;
                     else flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
@@ -455,9 +482,9 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
             if (threadIdx.x == 0 && copies_ok) {
                 fence_proxy_async_global();
                 fence_proxy_async_smem();
-                for (int i = 0; i < 2 && i < hi - lo; ++i) {
+                for (int i = 0; i < 2 && i < npg; ++i) {
                     if constexpr (RS) {
-                        attend_issue(sm, i, sel_all[lo + i], resolve(i), gp, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes);
+                        { const int ph = resolve(i); attend_issue(sm, i, sel[i], ph, gp, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes); }
                     } else {
                         const int ph = resolve(i);
                         mx_issue(sm.raw, mbar, i, false, ph, gp, a.k_pool, a.Hkv, kvh, a.page_bytes);
@@ -465,7 +492,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
                     }
                 }
             }
-            for (int i = 2 + threadIdx.x; i < hi - lo; i += blockDim.x) resolve(i);
+            for (int i = 2 + threadIdx.x; i < npg; i += blockDim.x) resolve(i);
             if (!REUSE && kvh == 0 && rg == 0 && s == 0) {
                 for (int i = threadIdx.x; i < a.topk; i += blockDim.x)
                     a.topk_out[(int64_t)b * a.topk + i] = i < k_eff ? sel_all[i] : -1;
@@ -474,14 +501,14 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
             __syncthreads();
 
             float m_run = -INFINITY, l = 0.0f;
-            const bool run = copies_ok && hi > lo;
+            const bool run = copies_ok && npg > 0;
             if (run) {
                 if constexpr (RS)
-                    copies_ok = attend_pages_tc<RS>(smem, sm, sel, selph, hi - lo, a.k_pool, a.v_pool, a.Hkv, kvh,
+                    copies_ok = attend_pages_tc<RS>(smem, sm, sel, selph, npg, a.k_pool, a.v_pool, a.Hkv, kvh,
                                                     a.page_bytes, ctx, tmem, &mbar_mma[0], mma_ph, L, xch_tc, gp, m_run, l,
                                                     a.status);
                 else
-                    copies_ok = attend_pages_tc_mx(smem, sm.raw, mbar, sel, selph, hi - lo, a.k_pool, a.v_pool, a.Hkv,
+                    copies_ok = attend_pages_tc_mx(smem, sm.raw, mbar, sel, selph, npg, a.k_pool, a.v_pool, a.Hkv,
                                                    kvh, a.page_bytes, ctx, tmem, mbar_mma, mma_ph, pv_ph, L, xch_tc, gp,
                                                    m_run, l, a.status);
             }
@@ -538,20 +565,25 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
             }
             if (threadIdx.x == 0 && !wait_geq_bounded(&a.row_cnt[kCounterStride * b], (uint32_t)C)) flag_status(a.status, SMX_DEV_TIMEOUT);
             __syncthreads();
+            const int n_blocks = (n_pages + (1 << a.ppb_log2) - 1) >> a.ppb_log2;
             int k_eff;
             if constexpr (REUSE) {
                 __syncthreads();   // the staged q rows read (the page stages are free)
-                k_eff = given_selection(a, b, n_pages, sel_all);
+                k_eff = given_selection(a, b, n_blocks, sel_all);
             } else {
                 load_keys<true>(keys, a.scores + (int64_t)b * a.max_pages, n_pages);
                 __syncthreads();   // keys in place; the staged q rows read (the page stages are free)
-                k_eff = block_select(keys, n_pages, a.topk, sel_all, selsm);
+                if (a.ppb_log2) block_max_keys(keys, n_pages, a.ppb_log2);
+                k_eff = block_select(keys, n_blocks, a.topk, sel_all, selsm);
             }
             const int lo = (int)(((int64_t)s * k_eff) / a.S), hi = (int)(((int64_t)(s + 1) * k_eff) / a.S);
+            const int npg = (hi - lo) << a.ppb_log2;   // the partition's blocks as pages (one block: one page)
             auto resolve = [&](int i) {   // entry i of this partition: logical and physical page
-                const int p = sel_all[lo + i];
+                const int blk = sel_all[lo + (i >> a.ppb_log2)];
+                int p = blk < 0 ? -1 : (blk << a.ppb_log2) + (i & ((1 << a.ppb_log2) - 1));
+                if (p >= n_pages) p = -1;   // past the row in its last block: an empty page
                 int ph = -1;
-                if (p >= 0) {   // (a reused selection's bad id is -1: an empty page)
+                if (p >= 0) {   // (a reused selection's bad id is -1: an empty page, flagged)
                     const int64_t v = pt_cached ? pt_s[p] : a.page_table[(int64_t)b * a.max_pages + p];
                     if (v >= 0 && v < a.n_pool) ph = (int)v;
                     else flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
@@ -565,10 +597,10 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
             if (threadIdx.x == 0 && copies_ok) {
                 fence_proxy_async_global();
                 fence_proxy_async_smem();   // the staged q rows were read from the page stages
-                for (int i = 0; i < 2 && i < hi - lo; ++i)
-                    attend_issue(sm, i, sel_all[lo + i], resolve(i), gp, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes);
+                for (int i = 0; i < 2 && i < npg; ++i)
+                    { const int ph = resolve(i); attend_issue(sm, i, sel[i], ph, gp, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes); }
             }
-            for (int i = 2 + threadIdx.x; i < hi - lo; i += blockDim.x) resolve(i);
+            for (int i = 2 + threadIdx.x; i < npg; i += blockDim.x) resolve(i);
             if (!REUSE && kvh == 0 && rg == 0 && s == 0) {
                 for (int i = threadIdx.x; i < a.topk; i += blockDim.x)
                     a.topk_out[(int64_t)b * a.topk + i] = i < k_eff ? sel_all[i] : -1;
@@ -582,7 +614,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
             float mrow0 = -INFINITY, mrow1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
             const int pos0 = ctx - a.Q + L.t0, pos1 = ctx - a.Q + L.t1;
             if (copies_ok)
-                copies_ok = attend_pages<RS>(sm, sel, selph, hi - lo, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes, ctx,
+                copies_ok = attend_pages<RS>(sm, sel, selph, npg, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes, ctx,
                                              qa, L, pos0, pos1, gp, o, mrow0, mrow1, l0, l1, a.status, true);
             finish_partials(sm, L, o, mrow0, mrow1, l0, l1, a.part_o, a.part_m, a.part_l, b, s, kvh, a.S, a.Q, a.Hq, a.G);
             __syncthreads();
@@ -638,8 +670,9 @@ StepGeom step_geom(const smx_shape_t& s, bool tc) {
     g.row_warps = g.rows_per_cta / 16;
     g.n_rg = (M + g.rows_per_cta - 1) / g.rows_per_cta;
     g.page_bytes = s.kv_format == SMX_KV_E4M3_ROWSCALE ? kRsPageBytes : kMxPageBytes;
-    g.smem = tc ? attend_tc_smem_bytes(g.page_bytes) + 8 * (size_t)s.topk
-                : attend_smem_bytes(g.page_bytes) + 16 * (size_t)s.topk;
+    const size_t ppb = s.pages_per_block > 1 ? (size_t)s.pages_per_block : 1;
+    g.smem = tc ? attend_tc_smem_bytes(g.page_bytes) + 8 * ppb * (size_t)s.topk
+                : attend_smem_bytes(g.page_bytes) + (8 * ppb + 4) * (size_t)s.topk;
     // counters for the larger (mma.sync) group count, so the workspace does not depend on the path
     const int rg64 = (M + unit_rows(s, false) - 1) / unit_rows(s, false);
     g.n_counters = kCounterStride * ((size_t)s.B + (size_t)s.B * s.Hkv * rg64 + 1);
@@ -747,6 +780,7 @@ cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStrea
     a.topk = s.topk; a.S = s.num_splits;
     a.row_warps = geo.row_warps; a.rows_per_cta = geo.rows_per_cta; a.n_rg = geo.n_rg; a.page_bytes = geo.page_bytes;
     a.topk_in = io.topk_in; a.count_in = io.count_in;
+    a.ppb_log2 = s.pages_per_block == 4 ? 2 : s.pages_per_block == 2 ? 1 : 0;
 
     // grid: enough CTAs for every attention unit and for two pages each, at most one per SM
     const int64_t n_units = (int64_t)s.B * s.Hkv * geo.n_rg * s.num_splits;

@@ -40,7 +40,8 @@ class _CShape(ctypes.Structure):
                 ("Hkv", ctypes.c_int32), ("D", ctypes.c_int32), ("Di", ctypes.c_int32),
                 ("page_tokens", ctypes.c_int32), ("max_pages_per_row", ctypes.c_int32),
                 ("n_pool_pages", ctypes.c_int64), ("topk", ctypes.c_int32),
-                ("num_splits", ctypes.c_int32), ("kv_format", ctypes.c_int32)]
+                ("num_splits", ctypes.c_int32), ("kv_format", ctypes.c_int32),
+                ("pages_per_block", ctypes.c_int32)]
 
 
 @dataclass
@@ -57,17 +58,19 @@ class Shape:
     D: int = 128
     Di: int = 128
     page_tokens: int = 128
+    pages_per_block: int = 1
 
     @classmethod
     def of(cls, w, num_splits=None) -> "Shape":
         """Shape of a workload object (B, Q, Hq, Hkv, max_pages, n_pool_pages, topk, ...)."""
         return cls(w.B, w.Q, w.Hq, w.Hkv, w.max_pages, w.n_pool_pages, w.topk,
-                   w.num_splits if num_splits is None else num_splits, w.kv_format)
+                   w.num_splits if num_splits is None else num_splits, w.kv_format,
+                   pages_per_block=getattr(w, "pages_per_block", 1))
 
     def c(self) -> _CShape:
         return _CShape(self.B, self.Q, self.Hq, self.Hkv, self.D, self.Di, self.page_tokens,
                        self.max_pages_per_row, self.n_pool_pages, self.topk, self.num_splits,
-                       self.kv_format)
+                       self.kv_format, self.pages_per_block)
 
     @property
     def kv_page_bytes(self) -> int:

@@ -61,9 +61,11 @@ def gpu_step_reuse(w, data, pools, topk_pages, topk_count, num_splits=None):
 
 
 def random_selection(w, data, seed):
-    """Another layer's selection: seeded distinct pages of each row, ascending, padded with -1."""
+    """Another layer's selection: seeded distinct pages (blocks) of each row, ascending, padded
+    with -1."""
     rng = np.random.default_rng(seed)
-    n_pages = (data["ctx_len"] + 127) // 128
+    ppb = getattr(w, "pages_per_block", 1)
+    n_pages = ((data["ctx_len"] + 127) // 128 + ppb - 1) // ppb
     pages = -np.ones((w.B, w.topk), np.int32)
     count = np.zeros(w.B, np.int32)
     for b in range(w.B):
@@ -91,6 +93,21 @@ def reuse_parity(w, pages, count, data=None, num_splits=None):
     ok, err = attn_close(got["out"], ref["out"])
     assert ok, f"max err {err}"
     return err
+
+
+def block_scores(w, scores):
+    """Scores of the selection's units: pages, or with blocks of several pages each block's best
+    page (NaN pages left out), [B][n_blocks] padded with -inf."""
+    ppb = getattr(w, "pages_per_block", 1)
+    if ppb <= 1:
+        return scores
+    nb = (scores.shape[1] + ppb - 1) // ppb
+    out = np.full((scores.shape[0], nb), -np.inf)
+    for k in range(nb):
+        blk = scores[:, k * ppb:(k + 1) * ppb]
+        with np.errstate(invalid="ignore"):
+            out[:, k] = np.where(np.all(np.isnan(blk), axis=1), np.nan, np.nanmax(np.where(np.isnan(blk), -np.inf, blk), axis=1))
+    return out
 
 
 def check_topk_sets(ref_scores, ref_pages, ref_count, gpu_pages, gpu_count):
@@ -138,7 +155,7 @@ def full_step_parity(w, num_splits=None, data=None):
     assert got["status"] == 0
     for a, b in zip(got["pools"], ref_pools):
         assert np.array_equal(a, b), "inserted page bytes differ"
-    swaps = check_topk_sets(ref["scores"], ref["topk_pages"], ref["topk_count"], got["topk_pages"],
+    swaps = check_topk_sets(block_scores(w, ref["scores"]), ref["topk_pages"], ref["topk_count"], got["topk_pages"],
                             got["topk_count"])
     ref_out = ref["out"]
     if swaps:

@@ -47,7 +47,8 @@ def good_shape(**kw):
     (dict(topk=0), -1), (dict(num_splits=0), -1), (dict(n_pool_pages=0), -1),
     (dict(max_pages_per_row=0), -1),
     (dict(D=64), -2), (dict(Di=256), -2), (dict(page_tokens=64), -2), (dict(Q=17), -2),
-    (dict(kv_format=7), -2), (dict(topk=5000), -2),
+    (dict(kv_format=7), -2), (dict(topk=5000), -2), (dict(pages_per_block=3), -2),
+    (dict(pages_per_block=4, topk=2000), -2),
 ])
 def test_bad_shapes_are_refused(L, kw, code):
     s = good_shape(**kw)
@@ -102,6 +103,14 @@ def test_reuse_step_refuses_null_misaligned_and_workspace(L):
     args = list(ok)
     args[1] = None
     assert L.smx_decode_step_reuse(ctypes.byref(cs), *args, a, ws - 256, None, None) == -4
+
+
+def test_standalone_topk_and_split_refuse_blocks_of_pages(L):
+    cs = good_shape(pages_per_block=2).c()
+    fake = ctypes.c_void_p(1 << 20)
+    assert L.smx_index_score_topk(ctypes.byref(cs), fake, fake, fake, fake, fake, fake, fake, None, None) == -2
+    assert L.smx_sparse_attn_split(ctypes.byref(cs), *([fake] * 10), None, None) == -2
+    assert L.smx_workspace_bytes(ctypes.byref(cs)) > 0   # the fused steps take it
 
 
 def test_status_strings(L):

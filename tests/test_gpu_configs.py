@@ -195,8 +195,32 @@ def test_reuse_step_flags_bad_selections():
     pages[0, 1] = 10000          # past the row's pages
     count[1] = w.topk + 5        # more than topk
     got = C.gpu_step_reuse(w, data, pools, pages, count)
-    assert got["status"] & ops.DEV_BAD_PAGE_ID
+    assert got["status"] & ops.DEV_BAD_TOPK
     assert np.all(np.isfinite(got["out"]))
+
+
+@pytest.mark.parametrize("fmt,tc,ppb", [(wl.KV_MXFP4, False, 2), (wl.KV_MXFP4, False, 4), (wl.KV_MXFP4, True, 2),
+                                         (wl.KV_MXFP4, True, 4), (wl.KV_E4M3_ROWSCALE, False, 2),
+                                         (wl.KV_E4M3_ROWSCALE, True, 2)])
+def test_pages_per_block(fmt, tc, ppb):
+    # selection blocks of 2 or 4 pages: block maxima ranked, each selected block's pages attended
+    # (the row's last block may end past it); mma.sync units (B 4, S 4) or tensor-core units (B 8,
+    # S 12: more partitions than blocks)
+    kw = dict(big_row_frac=0.01) if fmt == wl.KV_E4M3_ROWSCALE else {}
+    w = wl.Workload("ppb", B=8 if tc else 4, Q=8, Hq=16, Hkv=1, max_ctx=6000, topk=6 if not tc else 4,
+                    num_splits=12 if tc else 4, kv_format=fmt, seed=929, ragged=True, pages_per_block=ppb, **kw)
+    assert _uses_tc(w) == tc
+    C.full_step_parity(w)
+
+
+@pytest.mark.parametrize("tc", [False, True])
+def test_reuse_step_pages_per_block(tc):
+    w = wl.Workload("reuse_ppb", B=8 if tc else 4, Q=8, Hq=16, Hkv=1, max_ctx=6000, topk=4,
+                    num_splits=12 if tc else 4, seed=31, ragged=True, pages_per_block=2)
+    assert _uses_tc(w) == tc
+    data = wl.generate(w)
+    pages, count = C.random_selection(w, data, 5)
+    C.reuse_parity(w, pages, count, data=data)
 
 
 def test_configs_take_the_mma_path():
