@@ -104,6 +104,22 @@ def recorded_traffic(workload_name, reuse=False):
     return d.get("dram_bytes_per_launch")
 
 
+def slowest_rank(x, device):
+    """The largest x over the ranks of the process group (the slowest rank's time), x itself with
+    no group or one rank. Any backend (NCCL on the GPUs, gloo in the host tests)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(step_bytes, world, steps, seconds):
+    """Every rank's step bytes over the slowest rank's time, GB/s (the replicas' aggregate)."""
+    return step_bytes * world * steps / seconds / 1e9
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -330,14 +346,12 @@ def main():
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     clk = clocks.stop()
+    ms = slowest_rank(ms, dev)
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
     assert status.item() == 0, f"device status {status.item()}"
     us_step = ms * 1e3 / args.steps
-    value = step_bytes * world * args.steps / (ms * 1e-3) / 1e9
+    value = whole_job_gbs(step_bytes, world, args.steps, ms * 1e-3)
 
     # ---- the dominant kernel: the step is one kernel (decode_step_kernel), timed above with CUDA
     # events on the replay stream; its algorithmic bytes per launch are the step's bytes
@@ -419,7 +433,8 @@ def main():
         g_e2e.replay()
     torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / (reps * n_e2e)
-    e2e_val = step_bytes * world / e2e_s / 1e9
+    e2e_s = slowest_rank(e2e_s, dev)
+    e2e_val = whole_job_gbs(step_bytes, world, 1, e2e_s)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
