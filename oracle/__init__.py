@@ -27,18 +27,22 @@ MXFP4_PAGE_BYTES = 8704
 E4M3RS_PAGE_BYTES = 16896
 
 
+def compile_library(src: str, out: str, quiet: bool = False) -> None:
+    """gcc, -O2, no fast-math, no FMA contraction (so x86-64 and aarch64 give the same bits)."""
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-Wall", "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True, capture_output=quiet)
+
+
 def build(force: bool = False) -> str:
-    """Compile smx_oracle.c into oracle/_build/liboracle.so (gcc, -O2, no fast-math,
-    no FMA contraction so x86-64 and aarch64 give the same bits)."""
+    """Compile smx_oracle.c into oracle/_build/liboracle.so."""
     os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
     hdr = os.path.join(_HERE, "smx_oracle.h")
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(_SRC), os.path.getmtime(hdr))):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
-           "-fPIC", "-shared", "-Wall", "-o", tmp, _SRC, "-lm"]
-    subprocess.run(cmd, check=True)
+    compile_library(_SRC, tmp)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -81,10 +85,12 @@ def shape_of(w, num_splits=None) -> Shape:
 
 
 def lib():
+    """The oracle library, built on first use. SMX_ORACLE_LIB names a prebuilt copy to load
+    instead (the pins' own test runs them against copies with planted mistakes)."""
     global _lib
     if _lib is None:
-        build()
-        L = ctypes.CDLL(_LIB_PATH)
+        path = os.environ.get("SMX_ORACLE_LIB") or build()
+        L = ctypes.CDLL(path)
         P = ctypes.c_void_p
         S = ctypes.POINTER(_Shape)
         sigs = {

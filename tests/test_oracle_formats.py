@@ -231,3 +231,36 @@ def test_e4m3_rowscale_row():
                               .to(torch.float64).numpy() * float(s))
     codes, s = oracle.e4m3rs_quant_row(np.zeros(128, np.float32))
     assert s == 1.0 and np.all(codes == 0)
+
+
+def _e4m3_cast(y):
+    return torch.from_numpy(np.clip(y, -448, 448).astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_rowscale_divides_by_the_scale():
+    """Codes are the e4m3 cast of fl32(x / s), a true fp32 division: elements placed within a few
+    ulps of e4m3 rounding midpoints, where x * fl32(1 / s) would land on another code."""
+    rng = np.random.default_rng(41)
+    grid = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mids = (grid[1:] + grid[:-1]) / 2                               # e4m3 rounding boundaries
+    n_disc = 0
+    for _ in range(24):
+        amax = np.float32(rng.uniform(0.5, 8.0) * 2.0 ** rng.integers(-8, 8))
+        s = np.float32(amax) / np.float32(448.0)
+        x = np.empty(128, np.float32)
+        x[0] = amax
+        m = rng.choice(mids[mids > 1.0], size=127)
+        base = (m * np.float64(s)).astype(np.float32)
+        steps = rng.integers(-2, 3, size=127)
+        for i in range(127):
+            v = base[i]
+            for _ in range(abs(int(steps[i]))):
+                v = np.nextafter(v, np.float32(np.inf if steps[i] > 0 else -np.inf), dtype=np.float32)
+            x[i + 1] = -v if rng.random() < 0.5 else v
+        x = np.clip(x, -amax, amax)
+        codes, s_o = oracle.e4m3rs_quant_row(x)
+        assert np.float32(s_o) == s
+        want = _e4m3_cast((x / s).astype(np.float32))
+        assert np.array_equal(codes, want)
+        n_disc += int(np.sum(_e4m3_cast((x * (np.float32(1.0) / s)).astype(np.float32)) != want))
+    assert n_disc > 0, "no element separates division from the reciprocal product"
