@@ -170,7 +170,8 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------------------------
 def run_reference(args):
-    """The CPU oracle as it stands, one batch row of the workload per step, all host cores."""
+    """The CPU oracle as it stands, one batch row of the workload per step, all host cores (with
+    --reuse, the reusing layer's step over the oracle's own selection of that row)."""
     import oracle
     w = wl.config(args.config)
     data = wl.generate(w)
@@ -183,15 +184,30 @@ def run_reference(args):
         pools = wl.empty_pools(wb)
         sh = oracle.shape_of(wb)
         oracle.kv_fill(sh, db["k"], db["v"], db["kidx"], db["page_table"], db["n_hist"], *pools)
-        samples.append((wb, sh, db, pools))
+        samples.append([wb, sh, db, pools, None])
     idx_b, kv_b = algorithmic_bytes(w, data["ctx_len"])
+    if args.reuse:
+        idx_b = 0   # a reusing layer reads no index page
     per_row = (idx_b + kv_b) / w.B
 
+    def full(sh, db, pools):
+        return oracle.decode_step(sh, q_f32=db["q"], q_bf16=db["q_bf16"], qidx_bf16=db["qidx_bf16"],
+                                  k_new=db["k_new"], v_new=db["v_new"], kidx_new=db["kidx_new"],
+                                  page_table=db["page_table"], ctx_len=db["ctx_len"], k_pool=pools[0],
+                                  v_pool=pools[1], idx_pool=pools[2])
+
+    if args.reuse:
+        for smp in samples:
+            smp[4] = full(*smp[1:4])
+
     def one(i):
-        wb, sh, db, pools = samples[i % len(samples)]
-        oracle.decode_step(sh, q_f32=db["q"], q_bf16=db["q_bf16"], qidx_bf16=db["qidx_bf16"], k_new=db["k_new"],
-                           v_new=db["v_new"], kidx_new=db["kidx_new"], page_table=db["page_table"],
-                           ctx_len=db["ctx_len"], k_pool=pools[0], v_pool=pools[1], idx_pool=pools[2])
+        wb, sh, db, pools, sel = samples[i % len(samples)]
+        if sel is None:
+            full(sh, db, pools)
+        else:
+            oracle.decode_step_reuse(sh, q_f32=db["q"], q_bf16=db["q_bf16"], k_new=db["k_new"], v_new=db["v_new"],
+                                     page_table=db["page_table"], ctx_len=db["ctx_len"], k_pool=pools[0],
+                                     v_pool=pools[1], topk_pages=sel["topk_pages"], topk_count=sel["topk_count"])
 
     for i in range(args.warmup):
         one(i)
@@ -202,11 +218,13 @@ def run_reference(args):
     value = per_row * args.steps / dt / 1e9
     cores = oracle.max_threads()
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC_REUSE if args.reuse else METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": dict(w.describe(), sample="one batch row per step (rows cycled)", parallelism="replicas"),
+        "config": dict(w.describe(), step="reusing layer" if args.reuse else "full",
+                       sample="one batch row per step (rows cycled)",
+                       parallelism="replicas" if args.gpus > 1 else "single"),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": "one batch row of the workload per step, rows cycled"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -446,7 +464,7 @@ def main():
             "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": us_step / 1e3, "us_per_step": us_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic (seeded N(0,1) rows quantised on the GPU; BASELINE workload shapes)",
+            "data": "synthetic (seeded N(0,1) rows quantised on the GPU; the benchmark workload's shapes)",
             "config": dict(w.describe(), step="reusing layer" if args.reuse else "full",
                            num_splits=shape.num_splits, bytes_per_step=step_bytes,
                            index_bytes=idx_b, kv_bytes=kv_b, parallelism="replicas" if world > 1 else "single",

@@ -67,7 +67,7 @@ class Workload:
 
     def describe(self) -> dict:
         return dict(workload=self.name, B=self.B, Q=self.Q, Hq=self.Hq, Hkv=self.Hkv,
-                    max_ctx=self.max_ctx, topk=self.topk, num_splits=self.num_splits,
+                    max_ctx=self.max_ctx, topk=self.topk,
                     kv="e4m3_rowscale" if self.kv_format == KV_E4M3_ROWSCALE else "mxfp4",
                     seed=self.seed)
 

@@ -27,6 +27,25 @@ def test_fixed_workload(n):
     C.full_step_parity(w)
 
 
+def bench_splits(w):
+    """The benchmark's launch configuration: the library's suggested partition count."""
+    return ops.suggest_num_splits(ops.Shape.of(w, 1))
+
+
+@pytest.mark.parametrize("n", [2, 3, 4])
+def test_fixed_workload_at_bench_splits(n):
+    w = wl.config(n)
+    C.full_step_parity(w, num_splits=bench_splits(w))
+
+
+@pytest.mark.parametrize("n", [2, 4])
+def test_reuse_step_at_bench_size(n):
+    w = wl.config(n)
+    data = wl.generate(w)
+    pages, count = C.random_selection(w, data, 11)
+    C.reuse_parity(w, pages, count, data=data, num_splits=bench_splits(w))
+
+
 def sweep_subset():
     """Every 7th case plus the largest one: covers each value of every axis, ragged lengths and
     cases with more partitions than selected pages."""
