@@ -3,7 +3,9 @@
 Argument marshalling only: every step of the decode path runs in the CUDA kernels of
 libsmx.so. Tensors must be CUDA tensors (torch is used for device memory and streams); outputs
 that are not passed in are allocated with torch. Every call enqueues on the current torch
-stream unless `stream` (a torch.cuda.Stream) is given. A non-zero status raises SmxError.
+stream unless `stream` (a torch.cuda.Stream) is given. A non-zero status raises SmxError, and so
+does a buffer smaller than the shape needs (checked here, before the call: the C ABI sees only
+pointers).
 There is no CPU fallback: if libsmx.so is missing, the first call raises.
 """
 from __future__ import annotations
@@ -22,6 +24,7 @@ KV_E4M3_ROWSCALE = 1
 MXFP4_PAGE_BYTES = 8704
 E4M3RS_PAGE_BYTES = 16896
 DEV_BAD_PAGE_ID, DEV_BAD_CTX, DEV_BAD_TOPK = 1, 2, 4
+SMX_ERR_WORKSPACE = -4
 
 # every symbol include/smx.h declares
 SYMBOLS = ("smx_workspace_bytes", "smx_kv_insert", "smx_kv_prefill", "smx_pack_q_e4m3",
@@ -141,6 +144,27 @@ def _dev(*ts):
     return torch.device("cuda")
 
 
+def _need(what, **bufs):
+    """Refuse a buffer smaller than the shape needs before anything is enqueued: the C ABI takes
+    plain pointers and cannot see sizes. bufs: name -> (tensor or None, bytes the shape needs)."""
+    for name, (t, nbytes) in bufs.items():
+        if t is None:
+            continue
+        have = t.numel() * t.element_size()
+        if have < nbytes:
+            raise SmxError(f"{what}: {name} holds {have} bytes, the shape needs {nbytes}")
+
+
+def _step_bufs(shape, q_f32, q_bf16, k_new, v_new, page_table, ctx_len, k_pool, v_pool, dev_status):
+    """Sizes of the arguments every form of the step shares."""
+    B, Q, Hq, Hkv = shape.B, shape.Q, shape.Hq, shape.Hkv
+    return dict(q_f32=(q_f32, B * Q * Hq * 128 * 4), q_bf16=(q_bf16, B * Q * Hq * 128 * 2),
+                k_new=(k_new, B * Q * Hkv * 128 * 4), v_new=(v_new, B * Q * Hkv * 128 * 4),
+                page_table=(page_table, B * shape.max_pages_per_row * 4), ctx_len=(ctx_len, B * 4),
+                k_pool=(k_pool, shape.n_pool_pages * Hkv * shape.kv_page_bytes),
+                v_pool=(v_pool, shape.n_pool_pages * Hkv * shape.kv_page_bytes), dev_status=(dev_status, 4))
+
+
 def workspace_bytes(shape: Shape) -> int:
     cs = shape.c()
     return int(lib().smx_workspace_bytes(ctypes.byref(cs)))
@@ -171,6 +195,10 @@ def suggest_num_splits(shape: Shape) -> int:
 
 def kv_insert(shape, k_new, v_new, kidx_new, page_table, ctx_len, k_pool, v_pool, idx_pool,
               dev_status=None, stream=None):
+    B, Q = shape.B, shape.Q
+    _need("smx_kv_insert", **_step_bufs(shape, None, None, k_new, v_new, page_table, ctx_len, k_pool, v_pool,
+                                        dev_status),
+          kidx_new=(kidx_new, B * Q * 128 * 4), idx_pool=(idx_pool, shape.n_pool_pages * MXFP4_PAGE_BYTES))
     cs = shape.c()
     _check(lib().smx_kv_insert(ctypes.byref(cs), _p(k_new), _p(v_new), _p(kidx_new), _p(page_table),
                                _p(ctx_len), _p(k_pool), _p(v_pool), _p(idx_pool), _p(dev_status),
@@ -179,8 +207,12 @@ def kv_insert(shape, k_new, v_new, kidx_new, page_table, ctx_len, k_pool, v_pool
 
 def kv_prefill(shape, k, v, kidx, page_table, n_fill, k_pool, v_pool, idx_pool, dev_status=None,
                stream=None):
-    cs = shape.c()
     T = kidx.shape[1]
+    B, Hkv = shape.B, shape.Hkv
+    _need("smx_kv_prefill", k=(k, B * T * Hkv * 128 * 4), v=(v, B * T * Hkv * 128 * 4), kidx=(kidx, B * T * 128 * 4),
+          **_step_bufs(shape, None, None, None, None, page_table, None, k_pool, v_pool, dev_status),
+          n_fill=(n_fill, B * 4), idx_pool=(idx_pool, shape.n_pool_pages * MXFP4_PAGE_BYTES))
+    cs = shape.c()
     _check(lib().smx_kv_prefill(ctypes.byref(cs), _p(k), _p(v), _p(kidx), T, _p(page_table),
                                 _p(n_fill), _p(k_pool), _p(v_pool), _p(idx_pool), _p(dev_status),
                                 _st(stream)), "smx_kv_prefill")
@@ -189,8 +221,16 @@ def kv_prefill(shape, k, v, kidx, page_table, n_fill, k_pool, v_pool, idx_pool, 
 def pack_q_e4m3(q, out=None, stream=None):
     if out is None:
         out = torch.empty(q.shape, dtype=torch.uint8, device=q.device)
+    _need("smx_pack_q_e4m3", out=(out, q.numel()))
     _check(lib().smx_pack_q_e4m3(_p(q), _p(out), q.numel(), _st(stream)), "smx_pack_q_e4m3")
     return out
+
+
+def _index_bufs(shape, qidx_bf16, idx_pool, page_table, ctx_len, page_scores, dev_status):
+    B = shape.B
+    return dict(qidx_bf16=(qidx_bf16, B * shape.Q * 128 * 2), idx_pool=(idx_pool, shape.n_pool_pages * MXFP4_PAGE_BYTES),
+                page_table=(page_table, B * shape.max_pages_per_row * 4), ctx_len=(ctx_len, B * 4),
+                page_scores=(page_scores, B * shape.max_pages_per_row * 4), dev_status=(dev_status, 4))
 
 
 def index_score(shape, qidx_bf16, idx_pool, page_table, ctx_len, page_scores=None, dev_status=None,
@@ -198,6 +238,7 @@ def index_score(shape, qidx_bf16, idx_pool, page_table, ctx_len, page_scores=Non
     if page_scores is None:
         page_scores = torch.empty((shape.B, shape.max_pages_per_row), dtype=torch.float32,
                                   device=idx_pool.device)
+    _need("smx_index_score", **_index_bufs(shape, qidx_bf16, idx_pool, page_table, ctx_len, page_scores, dev_status))
     cs = shape.c()
     _check(lib().smx_index_score(ctypes.byref(cs), _p(qidx_bf16), _p(idx_pool), _p(page_table),
                                  _p(ctx_len), _p(page_scores), _p(dev_status), _st(stream)),
@@ -214,6 +255,9 @@ def index_score_topk(shape, qidx_bf16, idx_pool, page_table, ctx_len, page_score
         topk_pages = torch.empty((shape.B, shape.topk), dtype=torch.int32, device=dev)
     if topk_count is None:
         topk_count = torch.empty((shape.B,), dtype=torch.int32, device=dev)
+    _need("smx_index_score_topk", **_index_bufs(shape, qidx_bf16, idx_pool, page_table, ctx_len, page_scores,
+                                                dev_status),
+          topk_pages=(topk_pages, shape.B * shape.topk * 4), topk_count=(topk_count, shape.B * 4))
     cs = shape.c()
     _check(lib().smx_index_score_topk(ctypes.byref(cs), _p(qidx_bf16), _p(idx_pool), _p(page_table),
                                       _p(ctx_len), _p(page_scores), _p(topk_pages), _p(topk_count),
@@ -231,6 +275,12 @@ def sparse_attn_split(shape, q, k_pool, v_pool, page_table, ctx_len, topk_pages,
         part_m = torch.empty(rows, dtype=torch.float32, device=dev)
     if part_l is None:
         part_l = torch.empty(rows, dtype=torch.float32, device=dev)
+    n_rows = shape.B * shape.num_splits * shape.Q * shape.Hq
+    q_bytes = shape.B * shape.Q * shape.Hq * 128 * (2 if shape.kv_format == KV_E4M3_ROWSCALE else 1)
+    _need("smx_sparse_attn_split", q=(q, q_bytes),
+          **_step_bufs(shape, None, None, None, None, page_table, ctx_len, k_pool, v_pool, dev_status),
+          topk_pages=(topk_pages, shape.B * shape.topk * 4), topk_count=(topk_count, shape.B * 4),
+          part_o=(part_o, n_rows * 128 * 4), part_m=(part_m, n_rows * 4), part_l=(part_l, n_rows * 4))
     cs = shape.c()
     _check(lib().smx_sparse_attn_split(ctypes.byref(cs), _p(q), _p(k_pool), _p(v_pool), _p(page_table),
                                        _p(ctx_len), _p(topk_pages), _p(topk_count), _p(part_o),
@@ -242,6 +292,9 @@ def sparse_attn_split(shape, q, k_pool, v_pool, page_table, ctx_len, topk_pages,
 def sparse_attn_merge(shape, part_o, part_m, part_l, out=None, stream=None):
     if out is None:
         out = torch.empty((shape.B, shape.Q, shape.Hq, 128), dtype=torch.float32, device=part_o.device)
+    n_rows = shape.B * shape.num_splits * shape.Q * shape.Hq
+    _need("smx_sparse_attn_merge", part_o=(part_o, n_rows * 128 * 4), part_m=(part_m, n_rows * 4),
+          part_l=(part_l, n_rows * 4), out=(out, shape.B * shape.Q * shape.Hq * 128 * 4))
     cs = shape.c()
     _check(lib().smx_sparse_attn_merge(ctypes.byref(cs), _p(part_o), _p(part_m), _p(part_l), _p(out),
                                        _st(stream)), "smx_sparse_attn_merge")
@@ -251,6 +304,16 @@ def sparse_attn_merge(shape, part_o, part_m, part_l, out=None, stream=None):
 def alloc_workspace(shape, device=None) -> torch.Tensor:
     """Zeroed workspace for decode_step (its per-row counters must start at zero)."""
     return torch.zeros(max(256, workspace_bytes(shape)), dtype=torch.uint8, device=device or "cuda")
+
+
+def _full_step_bufs(shape, q_f32, q_bf16, qidx_bf16, k_new, v_new, kidx_new, page_table, ctx_len, k_pool, v_pool,
+                    idx_pool, topk_pages, topk_count, out, dev_status):
+    B, Q = shape.B, shape.Q
+    return dict(**_step_bufs(shape, q_f32, q_bf16, k_new, v_new, page_table, ctx_len, k_pool, v_pool, dev_status),
+                qidx_bf16=(qidx_bf16, B * Q * 128 * 2), kidx_new=(kidx_new, B * Q * 128 * 4),
+                idx_pool=(idx_pool, shape.n_pool_pages * MXFP4_PAGE_BYTES),
+                topk_pages=(topk_pages, B * shape.topk * 4), topk_count=(topk_count, B * 4),
+                out=(out, B * Q * shape.Hq * 128 * 4))
 
 
 def decode_step(shape, *, q_f32=None, q_bf16=None, qidx_bf16, k_new, v_new, kidx_new, page_table,
@@ -265,6 +328,9 @@ def decode_step(shape, *, q_f32=None, q_bf16=None, qidx_bf16, k_new, v_new, kidx
         out = torch.empty((shape.B, shape.Q, shape.Hq, 128), dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = alloc_workspace(shape, dev)
+    _need("smx_decode_step", **_full_step_bufs(shape, q_f32, q_bf16, qidx_bf16, k_new, v_new, kidx_new, page_table,
+                                               ctx_len, k_pool, v_pool, idx_pool, topk_pages, topk_count, out,
+                                               dev_status))
     cs = shape.c()
     _check(lib().smx_decode_step(ctypes.byref(cs), _p(q_f32), _p(q_bf16), _p(qidx_bf16), _p(k_new),
                                  _p(v_new), _p(kidx_new), _p(page_table), _p(ctx_len), _p(k_pool),
@@ -283,6 +349,10 @@ def decode_step_reuse(shape, *, q_f32=None, q_bf16=None, k_new, v_new, page_tabl
         out = torch.empty((shape.B, shape.Q, shape.Hq, 128), dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = alloc_workspace(shape, dev)
+    _need("smx_decode_step_reuse", **_step_bufs(shape, q_f32, q_bf16, k_new, v_new, page_table, ctx_len, k_pool,
+                                                v_pool, dev_status),
+          topk_pages=(topk_pages, shape.B * shape.topk * 4), topk_count=(topk_count, shape.B * 4),
+          out=(out, shape.B * shape.Q * shape.Hq * 128 * 4))
     cs = shape.c()
     _check(lib().smx_decode_step_reuse(ctypes.byref(cs), _p(q_f32), _p(q_bf16), _p(k_new), _p(v_new),
                                        _p(page_table), _p(ctx_len), _p(k_pool), _p(v_pool), _p(topk_pages),
@@ -301,6 +371,11 @@ def decode_step_noalloc(shape, *, q_f32=None, q_bf16=None, qidx_bf16, k_new, v_n
     """smx_decode_step_noalloc: the whole step in the library's static device scratch. Every
     output buffer is the caller's; the call allocates nothing (first call per device: before any
     stream capture). Calls that overlap on one device race on the shared scratch."""
+    if workspace_bytes(shape) > NOALLOC_SCRATCH_BYTES:
+        _check(SMX_ERR_WORKSPACE, "smx_decode_step_noalloc")
+    _need("smx_decode_step_noalloc", **_full_step_bufs(shape, q_f32, q_bf16, qidx_bf16, k_new, v_new, kidx_new,
+                                                       page_table, ctx_len, k_pool, v_pool, idx_pool, topk_pages,
+                                                       topk_count, out, dev_status))
     cs = shape.c()
     _check(lib().smx_decode_step_noalloc(ctypes.byref(cs), _p(q_f32), _p(q_bf16), _p(qidx_bf16), _p(k_new),
                                          _p(v_new), _p(kidx_new), _p(page_table), _p(ctx_len), _p(k_pool),
