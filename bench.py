@@ -248,8 +248,8 @@ def cpu_baseline(w, data, step_bytes, reuse=False):
                                   v_pool=pools[1], idx_pool=pools[2])
 
     sel = full() if reuse else None
-    reps, t0 = 0, time.perf_counter()
-    while True:
+
+    def one():
         if reuse:
             oracle.decode_step_reuse(sh, q_f32=data["q"], q_bf16=data["q_bf16"], k_new=data["k_new"],
                                      v_new=data["v_new"], page_table=data["page_table"], ctx_len=data["ctx_len"],
@@ -257,14 +257,27 @@ def cpu_baseline(w, data, step_bytes, reuse=False):
                                      topk_count=sel["topk_count"])
         else:
             full()
-        reps += 1
-        dt = time.perf_counter() - t0
-        if dt > 10.0:
-            break
-    return {"value": step_bytes * reps / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
+
+    def timed(seconds, min_reps):
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            one()
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt > seconds and reps >= min_reps:
+                return reps, dt
+
+    cores = oracle.max_threads()
+    reps, dt = timed(10.0, 1)
+    oracle.set_threads(1)        # the same steps on one core, a shorter sample
+    try:
+        reps1, dt1 = timed(4.0, 2)
+    finally:
+        oracle.set_threads(cores)
+    return {"value": step_bytes * reps / dt / 1e9, "unit": "GB/s", "cores": cores,
             "kind": "oracle", "sample": f"{reps} whole {'reusing-layer ' if reuse else ''}steps of the workload "
-                                       f"({dt:.1f} s)",
-            "us_per_step": dt / reps * 1e6}
+                                       f"({dt:.1f} s) on {cores} threads; {reps1} more on one thread ({dt1:.1f} s)",
+            "us_per_step": dt / reps * 1e6, "single_thread_us_per_step": dt1 / reps1 * 1e6}
 
 
 def main():
