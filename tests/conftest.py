@@ -16,8 +16,15 @@ def pytest_configure(config):
 def pytest_addoption(parser):
     parser.addoption("--full-sweep", action="store_true", default=False,
                      help="run all 216 sweep cases instead of the default stratified subset")
+    parser.addoption("--max-size", action="store_true", default=False,
+                     help="run the parity cases at the ABI's maximum sizes (2M-token rows; minutes of oracle time)")
 
 
 @pytest.fixture(scope="session")
 def full_sweep(request):
     return request.config.getoption("--full-sweep")
+
+
+@pytest.fixture(scope="session")
+def max_size(request):
+    return request.config.getoption("--max-size")

@@ -74,6 +74,25 @@ def test_sweep_full(case, full_sweep):
     C.full_step_parity(case)
 
 
+MAX_SIZE = [
+    # 16384 pages per row (2M tokens), 4096 selected pages, 16 query tokens
+    wl.Workload("max_pages_b1_q16_h8_ctx2097152_k4096", B=1, Q=16, Hq=8, Hkv=1, max_ctx=2097152, topk=4096,
+                num_splits=1, seed=919),
+    # the same row in blocks of 4 pages: 1024 blocks = 4096 pages
+    wl.Workload("max_blocks_b1_q8_h16_ctx2097152_k1024x4", B=1, Q=8, Hq=16, Hkv=1, max_ctx=2097152, topk=1024,
+                num_splits=1, seed=920, pages_per_block=4),
+]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("w", MAX_SIZE, ids=[w.name for w in MAX_SIZE])
+def test_maximum_sizes(w, max_size):
+    if not max_size:
+        pytest.skip("run with --max-size")
+    assert w.max_pages == 16384 and w.topk * w.pages_per_block == 4096
+    C.full_step_parity(w, num_splits=bench_splits(w))
+
+
 @pytest.mark.parametrize("kw", [
     dict(Q=16, Hq=8, max_ctx=3000, topk=6, num_splits=4),          # two n-tiles in the scorer
     dict(Q=2, Hq=8, Hkv=2, max_ctx=1500, topk=3, num_splits=2),    # GQA
