@@ -60,7 +60,12 @@ enum {
     SMX_ERR_WORKSPACE = -4     /* workspace pointer null or smaller than smx_workspace_bytes */
 };
 
-enum { SMX_KV_MXFP4 = 0, SMX_KV_E4M3_ROWSCALE = 1 };
+enum {
+    SMX_KV_MXFP4 = 0,
+    SMX_KV_E4M3_ROWSCALE = 1,
+    SMX_KV_NVFP4 = 2   /* named for callers that probe it; refused (SMX_ERR_UNSUPPORTED), as [ATOM-2812]
+                        * refuses NVFP4 main KV ("MXFP4 main KV": NVFP4 stays refused) */
+};
 
 /* device status bits */
 enum {

@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libsmx.so")
 
 KV_MXFP4 = 0
 KV_E4M3_ROWSCALE = 1
+KV_NVFP4 = 2   # refused by the library (SMX_ERR_UNSUPPORTED)
 MXFP4_PAGE_BYTES = 8704
 E4M3RS_PAGE_BYTES = 16896
 DEV_BAD_PAGE_ID, DEV_BAD_CTX, DEV_BAD_TOPK = 1, 2, 4

@@ -47,7 +47,8 @@ def good_shape(**kw):
     (dict(topk=0), -1), (dict(num_splits=0), -1), (dict(n_pool_pages=0), -1),
     (dict(max_pages_per_row=0), -1),
     (dict(D=64), -2), (dict(Di=256), -2), (dict(page_tokens=64), -2), (dict(Q=17), -2),
-    (dict(kv_format=7), -2), (dict(topk=5000), -2), (dict(pages_per_block=3), -2),
+    (dict(kv_format=7), -2), (dict(kv_format=2), -2),   # 2 = SMX_KV_NVFP4, refused as on the pages
+    (dict(topk=5000), -2), (dict(pages_per_block=3), -2),
     (dict(pages_per_block=4, topk=2000), -2),
 ])
 def test_bad_shapes_are_refused(L, kw, code):
