@@ -1,12 +1,14 @@
 """Benchmark of the sparse MXFP4 decode step on GB300.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--impl smx|reference] [--config 2]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl smx|reference] [--config 5]
 
 One step = the whole hot path (insert, q pack, index score of every page, top-k, split-K
-attention, merge) on the fixed 7-draft verify workload (B=4 rows x Q=8 query tokens, 16 query
-heads on 1 KV head, 16384-token contexts = 128 pages, top-k 16) by default. The metric is
-achieved HBM GB/s of the algorithmic bytes (every index page of each row + the K and V pages
-of the selected set) per step; microseconds per step are reported too.
+attention, merge). The headline workload (--config, default 5) is the largest case of the sweep:
+B = 4 rows x Q = 8 query tokens, 16 query heads on 1 KV head, ragged contexts up to 262144 tokens
+(1158 to 1695 pages), top-k 128 pages. The metric is achieved HBM GB/s of the algorithmic bytes
+(every index page of each row + the K and V pages of the selected set) per step; microseconds per
+step are reported too. The same line carries `per_config`: the fixed 7-draft verify (2), FP8-KV
+(3) and long-context (4) workloads, each timed the same way.
 
 The timed K steps are replayed from one CUDA graph; every step reads a different copy of the
 three page pools, with enough copies that their bytes exceed 3x the L2 cache, so each step reads
@@ -48,7 +50,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="smx", choices=["smx", "reference"])
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--config", type=int, default=5)
+    ap.add_argument("--per-config", default="2,3,4",
+                    help="other workloads timed in the same run, reported under per_config ('' for none)")
     ap.add_argument("--splits", type=int, default=0,
                     help="partitions of the split stage (0 = about two CTAs per SM, at most one page each)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -83,8 +87,8 @@ def peaks():
 
 def kernel_sources_sha():
     h = hashlib.sha256()
-    for f in ("smx_step.cu", "smx_attend.cuh", "smx_attend_tc.cuh", "smx_tc.cuh", "smx_score.cuh", "smx_select.cuh",
-              "smx_device.cuh"):
+    for f in ("smx_step.cu", "smx_attend.cuh", "smx_attend_tc.cuh", "smx_tc.cuh", "smx_scan.cuh", "smx_score_tc.cuh",
+              "smx_select.cuh", "smx_device.cuh"):
         h.update(open(os.path.join(ROOT, "sparse_attention_decode_mxfp4_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -280,6 +284,111 @@ def cpu_baseline(w, data, step_bytes, reuse=False):
             "us_per_step": dt / reps * 1e6, "single_thread_us_per_step": dt1 / reps1 * 1e6}
 
 
+class Prepared:
+    """One workload on the device: pools prefilled by the library, R rotating copies (more than 3x
+    L2 of bytes read per rotation), the step's inputs and outputs, and step(i) (one decode step over
+    copy i mod R, through the binding of the C ABI)."""
+
+    def __init__(self, w, args, dev, reuse=False):
+        from sparse_attention_decode_mxfp4_gb300 import ops
+        self.w = w
+        self.shape = ops.Shape.of(w, args.splits or default_splits(w))
+        self.data = data = wl.generate(w)
+        idx_b, kv_b = algorithmic_bytes(w, data["ctx_len"])
+        if reuse:
+            idx_b = 0   # a reusing layer reads no index page
+        self.idx_b, self.kv_b, self.step_bytes = idx_b, kv_b, idx_b + kv_b
+
+        def T(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+        self.page_table, self.ctx_len = T(data["page_table"]), T(data["ctx_len"])
+        base = tuple(torch.zeros(p.shape, dtype=torch.uint8, device=dev) for p in wl.empty_pools(w))
+        ops.kv_prefill(self.shape, T(data["k"]), T(data["v"]), T(data["kidx"]), self.page_table, T(data["n_hist"]),
+                       *base)
+        torch.cuda.synchronize()
+        self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.pool_bytes = sum(p.numel() for p in base)
+        self.R = R = max(2, math.ceil(3 * self.l2 / self.step_bytes))
+        self.copies = [tuple(p.clone() for p in base) for _ in range(R)]
+        del base
+        self.inp = dict(q_f32=T(data["q"]) if w.kv_format == wl.KV_MXFP4 else None,
+                        q_bf16=T(data["q_bf16"].view(np.int16)) if w.kv_format == wl.KV_E4M3_ROWSCALE else None,
+                        qidx_bf16=T(data["qidx_bf16"].view(np.int16)), k_new=T(data["k_new"]),
+                        v_new=T(data["v_new"]), kidx_new=T(data["kidx_new"]))
+        self.out = torch.empty((w.B, w.Q, w.Hq, 128), dtype=torch.float32, device=dev)
+        self.topk_pages = torch.empty((w.B, w.topk), dtype=torch.int32, device=dev)
+        self.topk_count = torch.empty((w.B,), dtype=torch.int32, device=dev)
+        self.workspace = ops.alloc_workspace(self.shape, dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.reuse = reuse
+        if reuse:
+            # an earlier layer's selection: one full step's output, then the reusing layer's step
+            self.step(0)
+            self.sel_pages, self.sel_count = self.topk_pages.clone(), self.topk_count.clone()
+            del self.inp["qidx_bf16"], self.inp["kidx_new"]
+
+    def step(self, i, pt=None, cl=None, io=None, o=None):
+        from sparse_attention_decode_mxfp4_gb300 import ops
+        pt = self.page_table if pt is None else pt
+        cl = self.ctx_len if cl is None else cl
+        io = self.inp if io is None else io
+        o = self.out if o is None else o
+        kp, vp, ip = self.copies[i % self.R]
+        if self.reuse:
+            ops.decode_step_reuse(self.shape, **io, page_table=pt, ctx_len=cl, k_pool=kp, v_pool=vp,
+                                  topk_pages=self.sel_pages, topk_count=self.sel_count, out=o,
+                                  workspace=self.workspace, dev_status=self.status)
+        else:
+            ops.decode_step(self.shape, **io, page_table=pt, ctx_len=cl, k_pool=kp, v_pool=vp, idx_pool=ip,
+                            topk_pages=self.topk_pages, topk_count=self.topk_count, out=o,
+                            workspace=self.workspace, dev_status=self.status)
+
+    def l2_note(self):
+        return (f"rotating {self.R} pool copies ({self.R * self.pool_bytes / 1e6:.0f} MB, reads "
+                f"{self.R * self.step_bytes / 1e6:.0f} MB per rotation > 3x L2 {self.l2 / 1e6:.0f} MB)")
+
+
+def time_steps(prep, steps, warmup, world, dev, clocks=None):
+    """Milliseconds of `steps` decode steps replayed from one CUDA graph (after a replayed graph of
+    `warmup` steps), CUDA events on the replay stream, the slowest rank's; clocks sampled inside."""
+    import torch.distributed as dist
+    prep.step(0)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    g_warm, g_timed = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g_warm, stream=s):
+            for i in range(max(3, warmup)):
+                prep.step(i)
+        with torch.cuda.graph(g_timed, stream=s):
+            for i in range(steps):
+                prep.step(i)
+    torch.cuda.synchronize()
+    g_warm.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    g_timed.replay()
+    e1.record(cur)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop() if clocks is not None else None
+    ms = slowest_rank(ms, dev)
+    if world > 1:
+        dist.barrier()
+    assert prep.status.item() == 0, f"device status {prep.status.item()}"
+    return ms, clk
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -298,95 +407,34 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     smx_build.build()
-    w = wl.config(args.config)
-    shape = ops.Shape.of(w, args.splits or default_splits(w))
-    data = wl.generate(w)
-    idx_b, kv_b = algorithmic_bytes(w, data["ctx_len"])
-    if args.reuse:
-        idx_b = 0   # a reusing layer reads no index page
-    step_bytes = idx_b + kv_b
+    peak, peak_kind = peaks()
 
-    def T(a):
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    # ---- the other workloads first (their memory is freed before the headline one) ----
+    per_config = {}
+    for n in [int(x) for x in args.per_config.split(",") if x.strip()]:
+        if n == args.config:
+            continue
+        p = Prepared(wl.config(n), args, dev, reuse=args.reuse)
+        k = min(args.steps, 100)
+        ms_n, _ = time_steps(p, k, max(3, args.warmup), world, dev)
+        us_n = ms_n * 1e3 / k
+        gbs = whole_job_gbs(p.step_bytes, world, k, ms_n * 1e-3)
+        per_config[str(n)] = {"workload": p.w.name, "us_per_step": us_n, "value": gbs, "unit": "GB/s",
+                              "roofline_frac": gbs / world / peak, "bytes_per_step": p.step_bytes,
+                              "index_bytes": p.idx_b, "kv_bytes": p.kv_b, "num_splits": p.shape.num_splits,
+                              "steps": k, "l2": p.l2_note(), "traffic": recorded_traffic(p.w.name, args.reuse)}
+        del p
+        torch.cuda.empty_cache()
 
-    page_table, ctx_len = T(data["page_table"]), T(data["ctx_len"])
-    base = tuple(torch.zeros(p.shape, dtype=torch.uint8, device=dev) for p in wl.empty_pools(w))
-    ops.kv_prefill(shape, T(data["k"]), T(data["v"]), T(data["kidx"]), page_table, T(data["n_hist"]), *base)
-    torch.cuda.synchronize()
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    pool_bytes = sum(p.numel() for p in base)
-    R = max(2, math.ceil(3 * l2 / step_bytes))
-    copies = [tuple(p.clone() for p in base) for _ in range(R)]
-    del base
-    inp = dict(q_f32=T(data["q"]) if w.kv_format == wl.KV_MXFP4 else None,
-               q_bf16=T(data["q_bf16"].view(np.int16)) if w.kv_format == wl.KV_E4M3_ROWSCALE else None,
-               qidx_bf16=T(data["qidx_bf16"].view(np.int16)), k_new=T(data["k_new"]), v_new=T(data["v_new"]),
-               kidx_new=T(data["kidx_new"]))
-    out = torch.empty((w.B, w.Q, w.Hq, 128), dtype=torch.float32, device=dev)
-    topk_pages = torch.empty((w.B, w.topk), dtype=torch.int32, device=dev)
-    topk_count = torch.empty((w.B,), dtype=torch.int32, device=dev)
-    workspace = ops.alloc_workspace(shape, dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-
-    def step(i, pt=page_table, cl=ctx_len, io=inp, o=out):
-        kp, vp, ip = copies[i % R]
-        ops.decode_step(shape, **io, page_table=pt, ctx_len=cl, k_pool=kp, v_pool=vp, idx_pool=ip,
-                        topk_pages=topk_pages, topk_count=topk_count, out=o, workspace=workspace,
-                        dev_status=status)
-
-    if args.reuse:
-        # an earlier layer's selection: one full step's output, then the reusing layer's step
-        step(0)
-        sel_pages, sel_count = topk_pages.clone(), topk_count.clone()
-        del inp["qidx_bf16"], inp["kidx_new"]
-
-        def step(i, pt=page_table, cl=ctx_len, io=inp, o=out):   # noqa: F811
-            kp, vp, _ = copies[i % R]
-            ops.decode_step_reuse(shape, **io, page_table=pt, ctx_len=cl, k_pool=kp, v_pool=vp,
-                                  topk_pages=sel_pages, topk_count=sel_count, out=o, workspace=workspace,
-                                  dev_status=status)
-
-    step(0)
-    torch.cuda.synchronize()
-    s = torch.cuda.Stream(device=dev)
-    s.wait_stream(torch.cuda.current_stream())
-    g_warm, g_timed = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    with torch.cuda.stream(s):
-        with torch.cuda.graph(g_warm, stream=s):
-            for i in range(max(3, args.warmup)):
-                step(i)
-        with torch.cuda.graph(g_timed, stream=s):
-            for i in range(args.steps):
-                step(i)
-    torch.cuda.synchronize()
-
-    # ---- timed region: K steps from one graph replay ----
-    g_warm.replay()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
+    prep = Prepared(wl.config(args.config), args, dev, reuse=args.reuse)
+    w, shape, step_bytes = prep.w, prep.shape, prep.step_bytes
     clocks = ClockSampler(local)
-    clocks.start()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    cur = torch.cuda.current_stream()
-    e0.record(cur)
-    g_timed.replay()
-    e1.record(cur)
-    e1.synchronize()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    clk = clocks.stop()
-    ms = slowest_rank(ms, dev)
-    if world > 1:
-        dist.barrier()
-    assert status.item() == 0, f"device status {status.item()}"
+    ms, clk = time_steps(prep, args.steps, args.warmup, world, dev, clocks)
     us_step = ms * 1e3 / args.steps
     value = whole_job_gbs(step_bytes, world, args.steps, ms * 1e-3)
 
     # ---- the dominant kernel: the step is one kernel (decode_step_kernel), timed above with CUDA
     # events on the replay stream; its algorithmic bytes per launch are the step's bytes
-    peak, peak_kind = peaks()
     launches_per_step = ops.decode_step_launches(shape)
     kernel_us = us_step / launches_per_step
     achieved = step_bytes / launches_per_step / (kernel_us * 1e-6) / 1e9
@@ -394,8 +442,9 @@ def main():
     # ---- end to end through the public API: pinned host inputs in, output back, every step ----
     # every input of a step in one pinned host buffer (256-byte aligned slices) with a device twin
     # of the same layout: one host->device copy per step, then one device->host copy of the output
+    inp, out = prep.inp, prep.out
     srcs = {k: v for k, v in inp.items() if v is not None}
-    srcs["page_table"], srcs["ctx_len"] = page_table, ctx_len
+    srcs["page_table"], srcs["ctx_len"] = prep.page_table, prep.ctx_len
     offs, total = {}, 0
     for k, v in srcs.items():
         offs[k] = total
@@ -419,6 +468,7 @@ def main():
     h2d = sum(v.numel() * v.element_size() for v in srcs.values())
     d2h = host_outs[0].numel() * host_outs[0].element_size()
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    s = torch.cuda.Stream(device=dev)
 
     def e2e_cycle(n):
         main = torch.cuda.current_stream()
@@ -437,7 +487,7 @@ def main():
             main.wait_event(ev_in[i])
             if i >= 2:
                 main.wait_event(ev_out[i - 2])        # step i - 2's output has been read back
-            step(i, pt=dev_ins[b]["page_table"], cl=dev_ins[b]["ctx_len"], io=io_e2es[b], o=outs[b])
+            prep.step(i, pt=dev_ins[b]["page_table"], cl=dev_ins[b]["ctx_len"], io=io_e2es[b], o=outs[b])
             ev_done[i].record(main)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_done[i])
@@ -448,7 +498,7 @@ def main():
 
     # captured once and replayed, as a serving loop would; pool copies rotate as in the timed
     # region; wall clock over whole replays
-    n_e2e = max(R, 2)
+    n_e2e = max(prep.R, 2)
     with torch.cuda.stream(s):
         e2e_cycle(4)
     torch.cuda.synchronize()
@@ -469,7 +519,7 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, data, step_bytes, reuse=args.reuse)
+        cpu = cpu_baseline(w, prep.data, step_bytes, reuse=args.reuse)
 
     if rank == 0:
         line = {
@@ -480,13 +530,14 @@ def main():
             "data": "synthetic (seeded N(0,1) rows quantised on the GPU; the benchmark workload's shapes)",
             "config": dict(w.describe(), step="reusing layer" if args.reuse else "full",
                            num_splits=shape.num_splits, bytes_per_step=step_bytes,
-                           index_bytes=idx_b, kv_bytes=kv_b, parallelism="replicas" if world > 1 else "single",
-                           l2=f"rotating {R} pool copies ({R * pool_bytes / 1e6:.0f} MB, reads "
-                              f"{R * step_bytes / 1e6:.0f} MB per rotation > 3x L2 {l2 / 1e6:.0f} MB)"),
+                           index_bytes=prep.idx_b, kv_bytes=prep.kv_b,
+                           ctx_len=[int(x) for x in prep.data["ctx_len"]],
+                           parallelism="replicas" if world > 1 else "single", l2=prep.l2_note()),
             "roofline": {"bound": "hbm", "kernel": "decode_step_kernel", "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": recorded_traffic(w.name, args.reuse), "us_per_launch": kernel_us,
                          "algorithmic_bytes_per_launch": step_bytes // launches_per_step},
+            "per_config": per_config,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "GB/s", "us_per_step": e2e_s * 1e6, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

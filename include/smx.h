@@ -22,6 +22,9 @@
  *    page scores -inf, an attention page contributes nothing), so a bad table can never make
  *    a kernel read or write outside the pools. The caller clears it.
  *  - D (head dim) = Di (index dim) = 128 and page_tokens = 128 are the only supported values.
+ *  - Alignment: float and pool arrays 16-byte aligned; idx_pool 32-byte aligned for the calls that
+ *    score it (it is read by tensor-map copies of a packed 4-bit type); otherwise
+ *    SMX_ERR_INVALID_ARG.
  *
  * Shapes and layouts (row-major, C order):
  *   q_f32     [B][Q][Hq][128] float        q_bf16   [B][Q][Hq][128] bf16 bits (uint16)
@@ -72,7 +75,8 @@ enum {
     SMX_DEV_BAD_PAGE_ID = 1,   /* a page-table entry outside [0, n_pool_pages) was met */
     SMX_DEV_BAD_CTX = 2,       /* ctx_len outside [Q, max_pages_per_row * 128] (row clamped) */
     SMX_DEV_BAD_TOPK = 4,      /* a selected page id outside [0, ceil(ctx_len/128)) */
-    SMX_DEV_TIMEOUT = 8        /* a bounded wait for a page copy gave up (the CTA stopped early) */
+    SMX_DEV_TIMEOUT = 8        /* a bounded wait gave up: for another CTA (smx_set_wait_limit_ns), or for
+                                * a page copy (the CTA stopped staging pages) */
 };
 
 #define SMX_MXFP4_PAGE_BYTES 8704
@@ -115,6 +119,12 @@ size_t smx_workspace_bytes(const smx_shape_t* shape);
  * the same row store). With kv_format == SMX_KV_E4M3_ROWSCALE, K and V rows are written as
  * e4m3 codes of x / s with s = fl32(amax / 448) (s = 1 when amax = 0) and the index row stays
  * MXFP4. Writes the Q new tokens of every row at positions ctx_len - Q + t. */
+int smx_kv_insert_mxfp4(const smx_shape_t* shape, const float* k_new, const float* v_new,
+                        const float* kidx_new, const int32_t* page_table, const int32_t* ctx_len,
+                        uint8_t* k_pool, uint8_t* v_pool, uint8_t* idx_pool, int32_t* dev_status,
+                        smx_stream_t stream);
+
+/* The same call under its shorter name (kept for existing callers). */
 int smx_kv_insert(const smx_shape_t* shape, const float* k_new, const float* v_new,
                   const float* kidx_new, const int32_t* page_table, const int32_t* ctx_len,
                   uint8_t* k_pool, uint8_t* v_pool, uint8_t* idx_pool, int32_t* dev_status,
@@ -133,7 +143,13 @@ int smx_kv_prefill(const smx_shape_t* shape, const float* k, const float* v, con
  * +-448, NaN gives 0x7F. */
 int smx_pack_q_e4m3(const float* q, uint8_t* q_e4m3, int64_t n, smx_stream_t stream);
 
-/* a3 alone -- the page scores of smx_index_score_topk without the selection. */
+/* a3 alone -- [ATOM-2812] "--index-cache-dtype mxfp4": the page scorer reads every MXFP4 index
+ * page of the row (16 B key loads plus a dword of E8M0 scales per tile) against the bf16 index
+ * query; the score of a page is the best dot product over its tokens and the row's query tokens
+ * (page-score rule of the benchmark workloads: max over the page's tokens of q_idx . k_idx).
+ * page_scores [B][max_pages_per_row] float as in smx_index_score_topk, without the selection.
+ * Returns SMX_OK, SMX_ERR_INVALID_ARG (NULL or misaligned pointer), SMX_ERR_UNSUPPORTED (shape)
+ * or SMX_ERR_CUDA. */
 int smx_index_score(const smx_shape_t* shape, const uint16_t* qidx_bf16, const uint8_t* idx_pool,
                     const int32_t* page_table, const int32_t* ctx_len, float* page_scores,
                     int32_t* dev_status, smx_stream_t stream);
@@ -166,7 +182,11 @@ int smx_sparse_attn_split(const smx_shape_t* shape, const void* q, const uint8_t
 int smx_sparse_attn_merge(const smx_shape_t* shape, const float* part_o, const float* part_m,
                           const float* part_l, float* out, smx_stream_t stream);
 
-/* The whole step (a1..a6) on `stream`. q_f32 is required for MXFP4 K/V, q_bf16 for E4M3
+/* The whole step (a1..a6) on `stream`: [ATOM-2812] "--index-cache-dtype mxfp4" (index-K rows are
+ * written, then every index page is scored and the top-k pages kept) and "MXFP4 main KV" (K/V rows
+ * written, split stage over the selected pages, merge), in the fused single-launch form of
+ * [ATOM-2686] Summary (the Mono decode path: one step per layer for the fixed 7-draft verify,
+ * 8 query tokens per row). q_f32 is required for MXFP4 K/V, q_bf16 for E4M3
  * row-scale K/V (the other may be NULL). Pools are updated in place (the Q new rows).
  * topk_pages/topk_count are outputs; workspace holds ws_bytes >= smx_workspace_bytes(shape)
  * bytes of scratch (256-byte aligned, zeroed before its first use). One cooperative kernel of at
@@ -200,6 +220,17 @@ int smx_decode_step_reuse(const smx_shape_t* shape, const float* q_f32, const ui
                           const int32_t* ctx_len, uint8_t* k_pool, uint8_t* v_pool,
                           const int32_t* topk_pages, const int32_t* topk_count, float* out,
                           void* workspace, size_t ws_bytes, int32_t* dev_status, smx_stream_t stream);
+
+/* Bound, in nanoseconds of GPU global time, of every wait of the fused steps for other CTAs of
+ * the same launch (a row's page scores, a group's partitions: the co-residency the pages' persistent
+ * kernel assumed, [vLLM-60528] "Merge Danger"). A wait that runs out sets SMX_DEV_TIMEOUT in
+ * dev_status and the CTA goes on with whatever it finds, reading and writing only inside the
+ * caller's buffers: that step's outputs are then undefined but finite, and the step still leaves the
+ * workspace counters at zero, so the next step is sound. ns = 0 restores the default (200 ms,
+ * far above the longest step of the largest shapes). Process-wide; applies to launches enqueued
+ * after the call. Returns the bound in force before the call. Meant for tests that make a wait give
+ * up; waits for a CTA's own copies and MMAs are not affected. */
+uint64_t smx_set_wait_limit_ns(uint64_t ns);
 
 /* Static text for a status code. */
 const char* smx_status_string(int status);
@@ -241,15 +272,16 @@ int smx_suggest_num_splits(const smx_shape_t* shape);
  * synchronise the whole device; and plain C callers that have no device allocator of their own.
  *
  * The first call on each device (with that device current) looks up the array's address with
- * cudaGetSymbolAddress, which may load the module on that device, and clears the step counters at
- * its head on `stream`. Make that first call before any stream capture. Later calls launch the
- * step; the step leaves its counters at zero, and a call whose shape needs more counter bytes than
- * the previous call's also clears them first (one memset on `stream`).
+ * cudaGetSymbolAddress, which may load the module on that device: make that first call before any
+ * stream capture. Every call clears the step counters at the head of the array (one memset of
+ * smx_workspace_bytes' counter prefix, a few hundred bytes, on `stream`) and then launches the
+ * step; the array keeps the rest of the last call's contents.
  *
- * Returns SMX_ERR_WORKSPACE, before touching the device, when smx_workspace_bytes(shape) exceeds
- * SMX_NOALLOC_SCRATCH_BYTES; SMX_ERR_CUDA if the address lookup fails. All calls on one device
- * share the one array: calls that overlap on the GPU (other streams, other host threads) race
- * on it and give undefined results. */
+ * Argument checks are smx_decode_step's and run first, before the device is touched; then
+ * SMX_ERR_WORKSPACE when smx_workspace_bytes(shape) exceeds SMX_NOALLOC_SCRATCH_BYTES, and
+ * SMX_ERR_CUDA if the address lookup or the memset fails. All calls on one device share the one
+ * array: calls that overlap on the GPU (other streams, other host threads) race on it and give
+ * undefined results. */
 int smx_decode_step_noalloc(const smx_shape_t* shape, const float* q_f32, const uint16_t* q_bf16,
                             const uint16_t* qidx_bf16, const float* k_new, const float* v_new,
                             const float* kidx_new, const int32_t* page_table, const int32_t* ctx_len,

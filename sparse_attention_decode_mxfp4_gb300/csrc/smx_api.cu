@@ -5,6 +5,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "smx_device.cuh"
 #include "smx_internal.h"
 
 namespace smx {
@@ -36,6 +37,13 @@ cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
 
 size_t workspace_counter_bytes(const smx_shape_t& s) { return step_geom(s).n_counters * sizeof(uint32_t); }
 
+static std::atomic<uint64_t> g_wait_limit_ns{0};   // 0: the default bound
+
+uint64_t wait_limit_ns() {
+    const uint64_t v = g_wait_limit_ns.load(std::memory_order_relaxed);
+    return v ? v : kDefaultWaitNs;
+}
+
 }  // namespace smx
 
 namespace {
@@ -45,6 +53,9 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The index pool is read by tensor-map copies of a packed 4-bit type: 32-byte aligned.
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 int check_shape(const smx_shape_t* s) {
     if (!s) return SMX_ERR_INVALID_ARG;
@@ -101,6 +112,29 @@ Workspace layout(const smx_shape_t* s, void* base) {
 
 }  // namespace
 
+namespace smx {
+
+int check_step_args(const smx_shape_t* s, const float* q_f32, const uint16_t* q_bf16, const uint16_t* qidx_bf16,
+                    const float* k_new, const float* v_new, const float* kidx_new, const int32_t* page_table,
+                    const int32_t* ctx_len, const uint8_t* k_pool, const uint8_t* v_pool, const uint8_t* idx_pool,
+                    const int32_t* topk_pages, const int32_t* topk_count, const float* out) {
+    const int rc = check_shape(s);
+    if (rc) return rc;
+    const bool rs = s->kv_format == SMX_KV_E4M3_ROWSCALE;
+    if ((rs ? (const void*)q_bf16 : (const void*)q_f32) == nullptr) return SMX_ERR_INVALID_ARG;
+    if (!qidx_bf16 || !k_new || !v_new || !kidx_new || !page_table || !ctx_len || !k_pool || !v_pool ||
+        !idx_pool || !topk_pages || !topk_count || !out)
+        return SMX_ERR_INVALID_ARG;
+    if (!rs && !aligned16(q_f32)) return SMX_ERR_INVALID_ARG;
+    if (rs && (reinterpret_cast<uintptr_t>(q_bf16) & 3u)) return SMX_ERR_INVALID_ARG;
+    if (!aligned16(qidx_bf16) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(kidx_new) ||
+        !aligned16(k_pool) || !aligned16(v_pool) || !aligned32(idx_pool))
+        return SMX_ERR_INVALID_ARG;
+    return SMX_OK;
+}
+
+}  // namespace smx
+
 extern "C" {
 
 size_t smx_workspace_bytes(const smx_shape_t* shape) {
@@ -108,9 +142,9 @@ size_t smx_workspace_bytes(const smx_shape_t* shape) {
     return layout(shape, nullptr).bytes;
 }
 
-int smx_kv_insert(const smx_shape_t* s, const float* k_new, const float* v_new, const float* kidx_new,
-                  const int32_t* page_table, const int32_t* ctx_len, uint8_t* k_pool, uint8_t* v_pool,
-                  uint8_t* idx_pool, int32_t* dev_status, smx_stream_t stream) {
+int smx_kv_insert_mxfp4(const smx_shape_t* s, const float* k_new, const float* v_new, const float* kidx_new,
+                        const int32_t* page_table, const int32_t* ctx_len, uint8_t* k_pool, uint8_t* v_pool,
+                        uint8_t* idx_pool, int32_t* dev_status, smx_stream_t stream) {
     int rc = check_shape(s);
     if (rc) return rc;
     if (!k_new || !v_new || !kidx_new || !page_table || !ctx_len || !k_pool || !v_pool || !idx_pool)
@@ -120,6 +154,13 @@ int smx_kv_insert(const smx_shape_t* s, const float* k_new, const float* v_new, 
         return SMX_ERR_INVALID_ARG;
     return cuda_status(smx::launch_kv_insert(*s, k_new, v_new, kidx_new, s->Q, page_table, ctx_len, nullptr,
                                              k_pool, v_pool, idx_pool, dev_status, false, (cudaStream_t)stream));
+}
+
+int smx_kv_insert(const smx_shape_t* s, const float* k_new, const float* v_new, const float* kidx_new,
+                  const int32_t* page_table, const int32_t* ctx_len, uint8_t* k_pool, uint8_t* v_pool,
+                  uint8_t* idx_pool, int32_t* dev_status, smx_stream_t stream) {
+    return smx_kv_insert_mxfp4(s, k_new, v_new, kidx_new, page_table, ctx_len, k_pool, v_pool, idx_pool, dev_status,
+                               stream);
 }
 
 int smx_kv_prefill(const smx_shape_t* s, const float* k, const float* v, const float* kidx, int64_t T,
@@ -148,7 +189,7 @@ int smx_index_score(const smx_shape_t* s, const uint16_t* qidx_bf16, const uint8
     int rc = check_shape(s);
     if (rc) return rc;
     if (!qidx_bf16 || !idx_pool || !page_table || !ctx_len || !page_scores) return SMX_ERR_INVALID_ARG;
-    if (!aligned16(qidx_bf16) || !aligned16(idx_pool)) return SMX_ERR_INVALID_ARG;
+    if (!aligned16(qidx_bf16) || !aligned32(idx_pool)) return SMX_ERR_INVALID_ARG;
     return cuda_status(smx::launch_index_scores(*s, qidx_bf16, idx_pool, page_table, ctx_len, page_scores,
                                                 dev_status, (cudaStream_t)stream));
 }
@@ -161,7 +202,7 @@ int smx_index_score_topk(const smx_shape_t* s, const uint16_t* qidx_bf16, const 
     if ((rc = check_page_blocks(s))) return rc;
     if (!qidx_bf16 || !idx_pool || !page_table || !ctx_len || !page_scores || !topk_pages || !topk_count)
         return SMX_ERR_INVALID_ARG;
-    if (!aligned16(qidx_bf16) || !aligned16(idx_pool)) return SMX_ERR_INVALID_ARG;
+    if (!aligned16(qidx_bf16) || !aligned32(idx_pool)) return SMX_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = smx::launch_index_scores(*s, qidx_bf16, idx_pool, page_table, ctx_len, page_scores,
                                              dev_status, st);
@@ -199,18 +240,10 @@ int smx_decode_step(const smx_shape_t* s, const float* q_f32, const uint16_t* q_
                     const int32_t* ctx_len, uint8_t* k_pool, uint8_t* v_pool, uint8_t* idx_pool,
                     int32_t* topk_pages, int32_t* topk_count, float* out, void* workspace, size_t ws_bytes,
                     int32_t* dev_status, smx_stream_t stream) {
-    int rc = check_shape(s);
+    const int rc = smx::check_step_args(s, q_f32, q_bf16, qidx_bf16, k_new, v_new, kidx_new, page_table, ctx_len,
+                                        k_pool, v_pool, idx_pool, topk_pages, topk_count, out);
     if (rc) return rc;
     const bool rs = s->kv_format == SMX_KV_E4M3_ROWSCALE;
-    if ((rs ? (const void*)q_bf16 : (const void*)q_f32) == nullptr) return SMX_ERR_INVALID_ARG;
-    if (!qidx_bf16 || !k_new || !v_new || !kidx_new || !page_table || !ctx_len || !k_pool || !v_pool ||
-        !idx_pool || !topk_pages || !topk_count || !out)
-        return SMX_ERR_INVALID_ARG;
-    if (!rs && !aligned16(q_f32)) return SMX_ERR_INVALID_ARG;
-    if (rs && (reinterpret_cast<uintptr_t>(q_bf16) & 3u)) return SMX_ERR_INVALID_ARG;
-    if (!aligned16(qidx_bf16) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(kidx_new) ||
-        !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(idx_pool))
-        return SMX_ERR_INVALID_ARG;
     const size_t need = layout(s, nullptr).bytes;
     if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
         return SMX_ERR_WORKSPACE;
@@ -274,6 +307,12 @@ int smx_suggest_num_splits(const smx_shape_t* s) {
     t.num_splits = 1;
     if (check_shape(&t) != SMX_OK) return 0;
     return smx::suggest_num_splits(t);
+}
+
+uint64_t smx_set_wait_limit_ns(uint64_t ns) {
+    const uint64_t before = smx::wait_limit_ns();
+    smx::g_wait_limit_ns.store(ns, std::memory_order_relaxed);
+    return before;
 }
 
 const char* smx_status_string(int status) {

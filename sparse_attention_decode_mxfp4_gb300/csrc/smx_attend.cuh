@@ -560,7 +560,13 @@ __device__ __forceinline__ void merge_row(const float* part_o, const float* part
         }
     }
     if (M != -INFINITY) {
-        acc.x /= L; acc.y /= L; acc.z /= L; acc.w /= L;
+        if (L == 0.0f) {
+            // a partition with a maximum but no weight is never written by a completed split stage
+            // (its largest weight is 1); it can be read only after a wait gave up: write zeros
+            acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            acc.x /= L; acc.y /= L; acc.z /= L; acc.w /= L;
+        }
     }
     reinterpret_cast<float4*>(out_row)[lane] = acc;
 }

@@ -78,27 +78,20 @@ __device__ __forceinline__ float mul_exp2(float x, int k) {
     return x * exp2i_normal(k1) * exp2i_normal(k2);
 }
 
-// q packing rule: NaN -> 0x7F; otherwise clamp to [-448, 448], round to nearest even; the sign
-// bit is the input's sign.
-__device__ __forceinline__ uint32_t pack_q4(float4 x) {
-    float v[4] = {x.x, x.y, x.z, x.w};
-    uint32_t code[4];
-#pragma unroll
-    for (int i = 0; i < 4; i += 2) {
-        float a0 = fminf(fabsf(v[i]), 448.0f), a1 = fminf(fabsf(v[i + 1]), 448.0f);
-        uint32_t c = e4m3x2_rn_sat(a0, a1);
-        code[i] = c & 0xFF;
-        code[i + 1] = c >> 8;
-    }
-    uint32_t out = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint32_t c = code[i] | ((__float_as_uint(v[i]) >> 24) & 0x80u);
-        if (v[i] != v[i]) c = 0x7Fu;
-        out |= c << (8 * i);
-    }
-    return out;
+// q packing rule for two floats: NaN -> 0x7F; otherwise clamp to [-448, 448] and round to nearest
+// even; the sign bit is the input's sign. Returns the two e4m3 bytes (lo in bits 0..7).
+__device__ __forceinline__ uint32_t pack_q2(float x0, float x1) {
+    const uint32_t c = e4m3x2_rn_sat(fminf(fabsf(x0), 448.0f), fminf(fabsf(x1), 448.0f));
+    uint32_t b0 = (c & 0xFF) | ((__float_as_uint(x0) >> 24) & 0x80u);
+    uint32_t b1 = (c >> 8) | ((__float_as_uint(x1) >> 24) & 0x80u);
+    if (x0 != x0) b0 = 0x7F;
+    if (x1 != x1) b1 = 0x7F;
+    return b0 | (b1 << 8);
 }
+
+// Four floats by the same rule (one call of pack_q2 per pair: the standalone packing kernel and
+// the fused step share this code).
+__device__ __forceinline__ uint32_t pack_q4(float4 x) { return pack_q2(x.x, x.y) | (pack_q2(x.z, x.w) << 16); }
 
 // One 128-element row to MXFP4, warp-cooperative: lane l holds elements 4l..4l+3 (group
 // l / 8). Writes 64 nibble bytes at `nib` and 4 scale bytes at `sc`.
@@ -258,16 +251,6 @@ __device__ __forceinline__ float ldg_cg_f32(const float* p) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
 
-// The q packing rule for two floats: returns the two e4m3 bytes (lo in bits 0..7).
-__device__ __forceinline__ uint32_t pack_q2(float x0, float x1) {
-    const uint32_t c = e4m3x2_rn_sat(fminf(fabsf(x0), 448.0f), fminf(fabsf(x1), 448.0f));
-    uint32_t b0 = (c & 0xFF) | ((__float_as_uint(x0) >> 24) & 0x80u);
-    uint32_t b1 = (c >> 8) | ((__float_as_uint(x1) >> 24) & 0x80u);
-    if (x0 != x0) b0 = 0x7F;
-    if (x1 != x1) b1 = 0x7F;
-    return b0 | (b1 << 8);
-}
-
 // ---- bulk copies (TMA, 1-D) with mbarrier completion -----------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -367,11 +350,16 @@ __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
 
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// Default bound of a wait for other CTAs of the step (ns of global time): far above the longest
+// step the ABI's largest shapes run (tens of milliseconds), short enough that a stuck step frees
+// a shared GPU quickly.
+constexpr uint64_t kDefaultWaitNs = 200000000ull;
+
 // One thread waits until *p >= target, then orders its later reads after the writes released
 // before the update (a relaxed poll followed by an acquire fence). Between polls it sleeps
 // briefly (polling harder floods the counter's L2 slice and slows the updaters); it gives up
-// after about two seconds and 2^24 polls (false).
-__device__ __forceinline__ bool wait_geq_bounded(const uint32_t* p, uint32_t target) {
+// (false) once limit_ns of global time have passed since its first poll, or after 2^24 polls.
+__device__ __forceinline__ bool wait_geq_bounded(const uint32_t* p, uint32_t target, uint64_t limit_ns) {
     const uint64_t t0 = global_ns();
     bool ok = false;
     for (uint32_t i = 0; i < (1u << 24); ++i) {
@@ -379,7 +367,7 @@ __device__ __forceinline__ bool wait_geq_bounded(const uint32_t* p, uint32_t tar
             ok = true;
             break;
         }
-        if (global_ns() - t0 > 2000000000ull) break;
+        if (global_ns() - t0 >= limit_ns) break;
         __nanosleep(i < 64 ? 32 : 128);
     }
     fence_acq_rel_gpu();

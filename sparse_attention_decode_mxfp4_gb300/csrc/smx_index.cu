@@ -6,13 +6,16 @@
 // mxfp4": every page of the row is scored against the index query; commit "MXFP4 main KV": the
 // selected blocks (one 128-token page each) fill the row's sparse table.
 //
-// Scorer: tcgen05 kind::f8f6f4 MMAs of each page's E2M1 codes against the row's index queries
-// (smx_score_tc.cuh), grid (CTAs per row, B), two CTAs of 8 warps per SM.
+// Scorer: the tensor-map-fed block-scaled tcgen05 scan of smx_scan.cuh, grid (CTAs per row, B), one
+// CTA of 8 warps per SM; rows cut into very few pages per CTA take the mma.sync scorer.
 #include <math.h>
+
+#include <mutex>
 
 #include "smx_device.cuh"
 #include "smx_internal.h"
 #include "smx_score.cuh"
+#include "smx_scan.cuh"
 #include "smx_score_tc.cuh"
 #include "smx_select.cuh"
 
@@ -30,39 +33,34 @@ struct IndexArgs {
 };
 
 constexpr int kIdxMaxPpc = 64;   // page-table entries of one CTA staged in shared memory
-constexpr int kIdxTcMinPages = 6;  // pages per CTA from which the tensor-core scorer is faster
-constexpr int kIdxRawStages = 4, kIdxTileStages = 3, kIdxAccStages = 3;
-// dynamic shared memory: the tile stages, the query pieces and the raw stages, plus slack to align
-// the tiles to 1 KB
-constexpr int kIdxSmemBytes = kIdxTileStages * kScTileBytes + kScQueryBytes + kIdxRawStages * kMxPageBytes + 1024;
+constexpr int kIdxScanMinPages = 3;   // pages per CTA from which the tensor-core scan is faster
+constexpr int kIdxStages = 12;        // page stages of a scanning CTA (one CTA per SM: 214 KB)
+// dynamic shared memory: the scan's stages and query pieces, plus slack to align them to 1 KB
+constexpr int kIdxSmemBytes = scan_smem_bytes(kIdxStages, scan_acc_stages(8)) + 1024;
 
-// Grid (CTAs per row, B), 320 threads (ten warps), two CTAs per SM: the CTA scores its range of
-// the row's pages with the pipelined tensor-core scorer (sc_score_pages).
-constexpr int kIdxTcThreads = 320;
-template <int NQ>
-__global__ void __launch_bounds__(kIdxTcThreads, 2) index_score_kernel(IndexArgs a) {
+// Grid (CTAs per row, B), 256 threads, one CTA per SM: the CTA scans its range of the row's pages
+// with the tensor-map-fed tensor-core pipeline of smx_scan.cuh (SA accumulator stages; 256 columns
+// of tensor memory).
+template <int NQ, int SA>
+__global__ void __launch_bounds__(256, 1) index_scan_kernel(const IndexArgs a, const __grid_constant__ CUtensorMap map) {
     extern __shared__ __align__(1024) uint8_t dsm[];
     __shared__ int64_t phys_s[kIdxMaxPpc];
     __shared__ float gmax[8][4];
-    __shared__ float red[4 * kScMaxAccStages];
-    __shared__ __align__(8) uint64_t bars[2 * kIdxRawStages + 2 * kScMaxTileStages + 2 * kScMaxAccStages];
+    __shared__ float red[kScanRedPages * 4];
+    __shared__ __align__(8) uint64_t bars[scan_barriers(kIdxStages, SA)];
     __shared__ uint32_t tmem_slot;
     __shared__ int gave_up;
 
-    uint8_t* tiles = dsm + ((1024u - (smem_u32(dsm) & 1023u)) & 1023u);
-    ScPipe pp;
-    pp.tiles = tiles;
-    pp.qt = tiles + kIdxTileStages * kScTileBytes;
-    pp.raw = pp.qt + kScQueryBytes;
-    pp.rfull = bars;
-    pp.rfree = bars + kIdxRawStages;
-    pp.full = bars + 2 * kIdxRawStages;
-    pp.tfree = pp.full + kIdxTileStages;
-    pp.afull = pp.full + 2 * kIdxTileStages;
-    pp.afree = pp.afull + kIdxAccStages;
-    pp.red = red;
-    pp.gave_up = &gave_up;
-    pp.seq = 0;
+    uint8_t* base = dsm + ((1024u - (smem_u32(dsm) & 1023u)) & 1023u);
+    ScanPipe sp;
+    sp.tiles = base;
+    sp.qt = base + kIdxStages * kScanTileBytes;
+    sp.ring = sp.qt + kScQueryBytes;
+    scan_bind<kIdxStages, SA>(sp, bars);
+    sp.red = red;
+    sp.gave_up = &gave_up;
+    sp.seq = 0;
+    sp.ins_seq = 0;
     const int b = blockIdx.y;
     const int warp = threadIdx.x >> 5;
     const int p_begin = blockIdx.x * a.pages_per_cta;
@@ -73,8 +71,8 @@ __global__ void __launch_bounds__(kIdxTcThreads, 2) index_score_kernel(IndexArgs
         const int64_t ph = a.page_table[(int64_t)b * a.max_pages + p_begin + i];
         phys_s[i] = (ph < 0 || ph >= a.n_pool) ? -1 : ph;
     }
-    if (threadIdx.x == 0) sc_pipe_init<kIdxRawStages, kIdxTileStages, kIdxAccStages>(pp);
-    if (warp == 0) tmem_alloc(&tmem_slot, kScTmemCols);
+    if (threadIdx.x == 0) scan_init<kIdxStages, SA>(sp, 1);
+    if (warp == 0) tmem_alloc(&tmem_slot, kScanTmemCols);
     tc_fence_before_sync();
     const int ctx = clamp_ctx(ctx_raw, a.Q, a.max_pages, (blockIdx.x == 0 && threadIdx.x == 0) ? a.status : nullptr);
     const int n_pages = (ctx + kPage - 1) / kPage;
@@ -82,20 +80,19 @@ __global__ void __launch_bounds__(kIdxTcThreads, 2) index_score_kernel(IndexArgs
     for (int p = max(p_begin, n_pages) + threadIdx.x; p < p_end_all; p += blockDim.x)
         a.scores[(int64_t)b * a.max_pages + p] = -INFINITY;
     // the query pieces (its barriers also publish phys_s, the barriers and the allocation)
-    const ScQuery sq = sc_setup_query<NQ>(a.qidx + (int64_t)b * a.Q * kD, a.Q, pp.qt, gmax);
+    const ScQuery sq = sc_setup_query<NQ>(a.qidx + (int64_t)b * a.Q * kD, a.Q, sp.qt, gmax);
     tc_fence_after_sync();
-    pp.tmem = tmem_slot;
-    sc_init_sfb(pp.tmem);
-    tc_fence_before_sync();
+    sp.tmem = tmem_slot;
+    const int np = max(0, p_end - p_begin);
+    scan_pages<NQ, kIdxStages, SA>(sp, &map, phys_s, np, p_begin, np, ctx - a.Q, a.Q, sq,
+                                   a.scores + (int64_t)b * a.max_pages, a.status, [] {});
     __syncthreads();
-    tc_fence_after_sync();
-    sc_score_pages<NQ, kIdxRawStages, kIdxTileStages, kIdxAccStages>(pp, a.pool, phys_s, max(0, p_end - p_begin), p_begin, ctx - a.Q,
-                                                        a.Q, sq, a.scores + (int64_t)b * a.max_pages, a.status);
+    scan_finish<kIdxStages>(sp, a.status);
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after_sync();
-        tmem_dealloc(pp.tmem, kScTmemCols);
+        tmem_dealloc(sp.tmem, kScanTmemCols);
     }
 }
 
@@ -201,6 +198,43 @@ __global__ void __launch_bounds__(kSelThreads) topk_kernel(const float* __restri
     if (threadIdx.x == 0) topk_count[b] = k_eff;
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link against the driver
+// library), looked up once.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+cudaError_t encode_index_map(CUtensorMap* map, const uint8_t* idx_pool, int64_t n_pool) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return cudaErrorNotSupported;
+    // [page][row][element]: a page is 136 rows of 128 fp4 elements (64 B): 128 token rows of
+    // nibbles, then the 512 bytes of scale words as 8 more rows; pages 8704 B apart. One box = one
+    // whole page, each 16-element chunk unpacked to 16 bytes, 128-byte swizzle.
+    const cuuint64_t dims[3] = {128, (cuuint64_t)kScanRows, (cuuint64_t)n_pool};
+    const cuuint64_t strides[2] = {64, (cuuint64_t)kMxPageBytes};
+    const cuuint32_t box[3] = {128, (cuuint32_t)kScanRows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<uint8_t*>(idx_pool), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 static int sm_count() {
     static int cached[64] = {0};
     int dev = 0;
@@ -212,12 +246,13 @@ static int sm_count() {
     return cached[dev];
 }
 
-static int index_pages_per_cta(const smx_shape_t& s) {
-    // one wave: two CTAs of 8 warps per SM over all rows, an even number of pages each
-    const int64_t slots = 2 * (int64_t)sm_count();
+// Pages per CTA for one wave of `per_sm` CTAs per SM over all rows (even for the mma.sync scorer,
+// which walks pages in pairs), at most kIdxMaxPpc (longer rows take more waves).
+static int index_pages_per_cta(const smx_shape_t& s, int per_sm, bool even) {
+    const int64_t slots = per_sm * (int64_t)sm_count();
     const int64_t total = (int64_t)s.B * s.max_pages_per_row;
     int64_t ppc = (total + slots - 1) / slots;
-    ppc = (ppc + 1) & ~(int64_t)1;
+    if (even) ppc = (ppc + 1) & ~(int64_t)1;
     if (ppc > kIdxMaxPpc) ppc = kIdxMaxPpc;
     return (int)(ppc < 2 ? 2 : ppc);
 }
@@ -228,18 +263,24 @@ cudaError_t launch_index_scores(const smx_shape_t& s, const uint16_t* qidx, cons
     IndexArgs a = {};
     a.qidx = qidx; a.pool = idx_pool; a.page_table = page_table; a.ctx_len = ctx_len; a.scores = scores;
     a.status = status; a.n_pool = s.n_pool_pages; a.Q = s.Q; a.max_pages = s.max_pages_per_row;
-    a.pages_per_cta = index_pages_per_cta(s);
+    // the mma.sync scorer (two CTAs per SM) for rows cut into very few pages per CTA, else the scan
+    a.pages_per_cta = index_pages_per_cta(s, 2, true);
+    const bool mma = a.pages_per_cta < kIdxScanMinPages;
+    if (!mma) a.pages_per_cta = index_pages_per_cta(s, 1, false);
     const dim3 grid((s.max_pages_per_row + a.pages_per_cta - 1) / a.pages_per_cta, s.B);
-    if (a.pages_per_cta < kIdxTcMinPages) {
+    if (mma) {
         if (s.Q <= 8) index_score_mma_kernel<1><<<grid, kIdxWarps * 32, 0, st>>>(a);
         else index_score_mma_kernel<2><<<grid, kIdxWarps * 32, 0, st>>>(a);
     } else {
-        const void* fn = s.Q <= 8 ? reinterpret_cast<const void*>(index_score_kernel<8>)
-                                  : reinterpret_cast<const void*>(index_score_kernel<16>);
-        const cudaError_t e = ensure_smem_attr(fn, kIdxSmemBytes);
+        CUtensorMap map;
+        cudaError_t e = encode_index_map(&map, idx_pool, s.n_pool_pages);
         if (e != cudaSuccess) return e;
-        if (s.Q <= 8) index_score_kernel<8><<<grid, kIdxTcThreads, kIdxSmemBytes, st>>>(a);
-        else index_score_kernel<16><<<grid, kIdxTcThreads, kIdxSmemBytes, st>>>(a);
+        const void* fn = s.Q <= 8 ? reinterpret_cast<const void*>(index_scan_kernel<8, scan_acc_stages(8)>)
+                                  : reinterpret_cast<const void*>(index_scan_kernel<16, scan_acc_stages(16)>);
+        e = ensure_smem_attr(fn, kIdxSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (s.Q <= 8) index_scan_kernel<8, scan_acc_stages(8)><<<grid, 256, kIdxSmemBytes, st>>>(a, map);
+        else index_scan_kernel<16, scan_acc_stages(16)><<<grid, 256, kIdxSmemBytes, st>>>(a, map);
     }
     return cudaGetLastError();
 }

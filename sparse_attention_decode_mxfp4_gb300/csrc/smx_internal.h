@@ -1,6 +1,7 @@
 // smx_internal.h -- launchers shared between the kernel translation units and the C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -22,6 +23,11 @@ cudaError_t launch_pack_q(const float* q, uint8_t* out, int64_t n, cudaStream_t 
 cudaError_t launch_index_scores(const smx_shape_t& s, const uint16_t* qidx, const uint8_t* idx_pool,
                                 const int32_t* page_table, const int32_t* ctx_len, float* scores,
                                 int32_t* status, cudaStream_t st);
+
+// Tensor map of an MXFP4 index pool ([n_pool][8704] bytes, 32-byte aligned) for the scan: one box
+// = one whole page (128 token rows of nibbles, then its scale words), unpacked for the fp4 MMA
+// operand, 128-byte swizzle.
+cudaError_t encode_index_map(CUtensorMap* map, const uint8_t* idx_pool, int64_t n_pool);
 
 cudaError_t launch_topk(const smx_shape_t& s, const float* scores, const int32_t* ctx_len,
                         int32_t* topk_pages, int32_t* topk_count, cudaStream_t st);
@@ -76,6 +82,16 @@ struct StepIO {
     float* part_l;
 };
 cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStream_t st, bool reuse = false);
+
+// The argument checks of smx_decode_step (shape, pointers, alignment; not the workspace): SMX_OK
+// or the status smx_decode_step returns for them. Reads no device memory.
+int check_step_args(const smx_shape_t* s, const float* q_f32, const uint16_t* q_bf16, const uint16_t* qidx_bf16,
+                    const float* k_new, const float* v_new, const float* kidx_new, const int32_t* page_table,
+                    const int32_t* ctx_len, const uint8_t* k_pool, const uint8_t* v_pool, const uint8_t* idx_pool,
+                    const int32_t* topk_pages, const int32_t* topk_count, const float* out);
+
+// Bound of the step kernels' waits for other CTAs (ns), as set by smx_set_wait_limit_ns.
+uint64_t wait_limit_ns();
 
 // Bytes at the head of the decode-step workspace that must be zero before a step (the counters).
 size_t workspace_counter_bytes(const smx_shape_t& s);

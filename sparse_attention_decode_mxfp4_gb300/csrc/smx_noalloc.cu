@@ -2,9 +2,9 @@
 // device array of SMX_NOALLOC_SCRATCH_BYTES, so that no call allocates device memory.
 //
 // The array is a module-scope device variable: the driver places it when the module is loaded,
-// and the first call on each device looks up its address once. Later calls launch the step into
-// it (plus a memset of the step counters when a shape needs more of them than the previous call
-// left zero). All calls on one device share the array.
+// and the first call on each device looks up its address once. Every call then clears the step
+// counters at the head of the array (one memset of a few hundred bytes on the caller's stream)
+// and launches the step into it. All calls on one device share the array.
 #include <mutex>
 
 #include "smx_internal.h"
@@ -16,14 +16,11 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
 void* g_scratch[kMaxDevices] = {};
-size_t g_zero_prefix[kMaxDevices] = {};   // leading bytes of the array known to be zero
 
-// Address of the scratch array on the current device, with its first counter_bytes zero. The first
-// call on a device resolves it (cudaGetSymbolAddress, which also loads the module there if it is
-// not loaded yet) and clears the counters on `st`. The step leaves its counters zero but may write
-// its other data right after them, so a later call whose counters reach past the zero prefix the
-// previous call left clears them again (one memset on `st`).
-int scratch_on_current_device(void** out, size_t counter_bytes, cudaStream_t st) {
+// Address of the scratch array on the current device. The first call on a device resolves it
+// (cudaGetSymbolAddress, which also loads the module there if it is not loaded yet); host code
+// only ever passes this address to kernels, never the array's host-side name.
+int scratch_on_current_device(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SMX_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return SMX_ERR_UNSUPPORTED;
@@ -35,11 +32,7 @@ int scratch_on_current_device(void** out, size_t counter_bytes, cudaStream_t st)
             return SMX_ERR_CUDA;
         }
         g_scratch[dev] = p;
-        g_zero_prefix[dev] = 0;
     }
-    if (counter_bytes > g_zero_prefix[dev] && cudaMemsetAsync(g_scratch[dev], 0, counter_bytes, st) != cudaSuccess)
-        return SMX_ERR_CUDA;
-    g_zero_prefix[dev] = counter_bytes;
     *out = g_scratch[dev];
     return SMX_OK;
 }
@@ -51,18 +44,20 @@ extern "C" int smx_decode_step_noalloc(const smx_shape_t* s, const float* q_f32,
                                        const float* kidx_new, const int32_t* page_table, const int32_t* ctx_len,
                                        uint8_t* k_pool, uint8_t* v_pool, uint8_t* idx_pool, int32_t* topk_pages,
                                        int32_t* topk_count, float* out, int32_t* dev_status, smx_stream_t stream) {
-    const size_t need = smx_workspace_bytes(s);
-    if (need == 0) {
-        // an invalid shape: smx_decode_step checks the shape before anything else and returns
-        // its status without touching the device
-        return smx_decode_step(s, q_f32, q_bf16, qidx_bf16, k_new, v_new, kidx_new, page_table, ctx_len, k_pool,
-                               v_pool, idx_pool, topk_pages, topk_count, out, nullptr, 0, dev_status, stream);
-    }
-    if (need > (size_t)SMX_NOALLOC_SCRATCH_BYTES) return SMX_ERR_WORKSPACE;
-    void* scratch = nullptr;
-    // the step's counters open the workspace layout
-    const int rc = scratch_on_current_device(&scratch, smx::workspace_counter_bytes(*s), (cudaStream_t)stream);
+    // the same argument checks as smx_decode_step, before the device is touched
+    int rc = smx::check_step_args(s, q_f32, q_bf16, qidx_bf16, k_new, v_new, kidx_new, page_table, ctx_len, k_pool,
+                                  v_pool, idx_pool, topk_pages, topk_count, out);
     if (rc != SMX_OK) return rc;
+    if (smx_workspace_bytes(s) > (size_t)SMX_NOALLOC_SCRATCH_BYTES) return SMX_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    if ((rc = scratch_on_current_device(&scratch)) != SMX_OK) return rc;
+    // The step's counters open the workspace layout and must be zero when it starts. A step leaves
+    // them zero, but a call of another shape may have written other data over that range since,
+    // so every call clears them, on the same stream, just before the launch.
+    if (cudaMemsetAsync(scratch, 0, smx::workspace_counter_bytes(*s), (cudaStream_t)stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SMX_ERR_CUDA;
+    }
     return smx_decode_step(s, q_f32, q_bf16, qidx_bf16, k_new, v_new, kidx_new, page_table, ctx_len, k_pool, v_pool,
                            idx_pool, topk_pages, topk_count, out, scratch, (size_t)SMX_NOALLOC_SCRATCH_BYTES,
                            dev_status, stream);

@@ -1,0 +1,366 @@
+// smx_scan.cuh -- the index scan (a3) as a tensor-map-fed pipeline on the fifth-generation tensor
+// cores: every page of the MXFP4 index cache against the row's index queries, with no SIMT work
+// on the fp4 keys.
+//
+// [ATOM-2812] "Mono decode over the MXFP4 KV and index caches", commit "--index-cache-dtype
+// mxfp4": every page of the row is scored; S_p = max over its tokens j and the draft queries t
+// (j <= pos_t) of q_idx[t] . k_idx[j], the keys being E2M1 codes times the E8M0 scale of their
+// 32-element group; the scorer reads a 16 B key load plus a dword of scales per tile.
+//
+// Per page:
+//  * ONE tensor-map copy (cp.async.bulk.tensor, data type 16U4_ALIGN16B, 128-byte swizzle) takes
+//    the whole 8704-byte page as 136 rows of 64 bytes: rows 0..127 are the tokens' packed nibbles,
+//    rows 128..135 the tokens' E8M0 scale words (16 tokens a row). Shared memory receives each
+//    16-element chunk as its 8 bytes followed by an 8-byte gap: rows 0..127 form the K-major
+//    [128 tokens][128] fp4 operand the MMA reads, and token t's scale word sits in row 128 + t/16.
+//    The copy counts the 8704 bytes it reads.
+//  * An MMA-issuing warp copies the page's 128 scale words into a small ring (the tile is then the
+//    MMA's alone) and its lane 0 issues four tcgen05.mma kind::f8f6f4 (A = the page's E2M1 codes,
+//    M = 128 tokens; B = the query pieces in e4m3, N = 2 NQ; K = 32 = one scale group each) into
+//    four fp32 accumulators in tensor memory, unscaled.
+//  * The epilogue (thread = token) weighs group g's accumulator by 2^(e_g - 127 - sigma_g), adds
+//    the two query pieces, masks by the causal rule and takes the max over queries, then over the
+//    page's tokens. A NaN group scale (0xFF) makes the token's score NaN, which the max leaves out.
+// The queries come from sc_setup_query: each bf16 element times 2^sigma_g (the group's largest
+// magnitude in (224, 448]) split exactly into two e4m3 pieces (rows n and NQ + n). The products
+// are exact; only the MMA's and the epilogue's fp32 additions round.
+// Roles (8 warps): lane 0 of warps 0 and 3 issue the copies of the even and the odd pages (one
+// thread issues at most one copy per ~600 cycles: two issuers reach the copy engines' rate);
+// warps 1 and 2 take the MMAs of the even and the odd pages (the scale copy by the whole warp, the
+// MMA issue by lane 0, which an issue holds about a hundred cycles); warps 4-7 first run the
+// caller's work (the fused step writes the new rows there: they would idle until the first
+// accumulator anyway), then take the epilogue (warp 4 + q reaches tensor-memory lanes 32 q ..), two
+// pages an iteration. Nothing waits on the epilogue but the reuse of an accumulator stage, so the
+// copies and the MMAs run as the data lands. Every wait is bounded; once one gives up the CTA's
+// later waits return at once and SMX_DEV_TIMEOUT is set.
+#pragma once
+
+#include <cuda.h>
+
+#include "smx_device.cuh"
+#include "smx_score_tc.cuh"
+#include "smx_tc.cuh"
+
+namespace smx {
+
+constexpr int kScanRows = 136;                    // one page as rows of 64 bytes
+constexpr int kScanTileBytes = kScanRows * 128;   // unpacked: 128 bytes a row (17 x 1 KB)
+constexpr uint32_t kScanTxBytes = kMxPageBytes;   // completion bytes of one page's copy
+constexpr int kScanRedPages = 32;                 // page maxima combined per flush
+constexpr int kScanScaleBytes = 512;              // one page's scale words in the ring
+constexpr int kScanTmemCols = 512;                // tensor-memory columns a scanning CTA allocates
+
+// Accumulator stages of a scan with NQ query slots: four groups x 2 NQ columns each, 384 columns.
+__host__ __device__ constexpr int scan_acc_stages(int nq) { return 384 / (8 * nq); }
+
+// Shared-memory bytes of a scan with `stages` page stages (then the query pieces and the scale
+// ring of `sa` pages), from a 1024-byte-aligned base.
+__host__ __device__ constexpr int scan_smem_bytes(int stages, int sa) {
+    return stages * kScanTileBytes + kScQueryBytes + sa * kScanScaleBytes;
+}
+
+struct ScanPipe {
+    uint8_t* tiles;       // [ST][kScanTileBytes], 1024-byte aligned
+    uint8_t* qt;          // the query pieces (sc_setup_query), 1024-byte aligned
+    uint8_t* ring;        // [SA][kScanScaleBytes]: the scale words of the page in accumulator stage a
+    uint64_t* full;       // [ST] page copy landed (1 arrival + transaction bytes)
+    uint64_t* empty;      // [ST] stage free: the page's MMAs are done (commit)
+    uint64_t* afull;      // [SA] accumulators written (commit) and the ring slot filled (1 arrival)
+    uint64_t* aempty;     // [SA] accumulators and ring slot read (4 epilogue warps)
+    uint64_t* ins;        // the caller's new index rows are written (insert_arrivals arrivals)
+    float* red;           // [kScanRedPages][4] warp maxima (as order-preserving keys)
+    int* gave_up;         // shared flag
+    uint32_t tmem;        // base column of the scan's tensor memory
+    uint32_t seq;         // pages this CTA has scanned so far (sets every barrier's phase)
+    uint32_t ins_seq;     // insert hand-offs so far (the parity of `ins`)
+};
+
+// Barriers a ScanPipe needs: 2 ST + 2 SA + 1.
+__host__ __device__ constexpr int scan_barriers(int st, int sa) { return 2 * st + 2 * sa + 1; }
+
+// Points the pipe's barriers into bars[scan_barriers(ST, SA)].
+template <int ST, int SA>
+__device__ __forceinline__ void scan_bind(ScanPipe& sp, uint64_t* bars) {
+    sp.full = bars;
+    sp.empty = bars + ST;
+    sp.afull = bars + 2 * ST;
+    sp.aempty = sp.afull + SA;
+    sp.ins = sp.aempty + SA;
+}
+
+// One thread: the barriers (before the first use, behind a block barrier).
+template <int ST, int SA>
+__device__ __forceinline__ void scan_init(ScanPipe& sp, uint32_t insert_arrivals) {
+#pragma unroll
+    for (int s = 0; s < ST; ++s) {
+        mbar_init(&sp.full[s], 1);
+        mbar_init(&sp.empty[s], 1);
+    }
+#pragma unroll
+    for (int s = 0; s < SA; ++s) {
+        mbar_init(&sp.afull[s], 2);
+        mbar_init(&sp.aempty[s], 4);
+    }
+    mbar_init(sp.ins, insert_arrivals);
+    *sp.gave_up = 0;
+    mbar_fence_init();
+}
+
+__device__ __forceinline__ bool scan_wait(const ScanPipe& sp, uint64_t* bar, uint32_t parity, int32_t* status) {
+    if (*(volatile int*)sp.gave_up) return false;
+    if (mbar_wait_spin(bar, parity)) return true;
+    *(volatile int*)sp.gave_up = 1;
+    flag_status(status, SMX_DEV_TIMEOUT);
+    return false;
+}
+
+// The whole page `phys` (tensor map over the index pool: [pages][136 rows][128 fp4]) into `dst`,
+// completing on bar.
+__device__ __forceinline__ void scan_tma_page(void* dst, const CUtensorMap* map, int phys, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(smem_u32(dst)), "l"(map), "r"(0), "r"(0), "r"(phys), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// kind::f8f6f4 instruction descriptor: fp32 D, A E2M1, B E4M3 (both K-major), M = 128, N.
+__host__ __device__ constexpr uint32_t idesc_scan(int N) {
+    return (1u << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+// 2 NQ consecutive fp32 columns of this thread's lane (no wait).
+template <int NQ>
+__device__ __forceinline__ void scan_ld(uint32_t taddr, uint32_t (&r)[2 * NQ]) {
+    if constexpr (NQ == 8) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(taddr)
+            : "memory");
+    } else {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+              "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+              "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+            : "r"(taddr)
+            : "memory");
+    }
+}
+
+// A token's score for one page from its scale word and its four group accumulators (group g at
+// columns taddr + 2 NQ g: piece 0 in column n, piece 1 in NQ + n): with x_g = e_g - sigma_g and
+// X = max_g x_g, t_n = sum_g 2^(x_g - X) (D_g[n] + D_g[NQ + n]) (weights exact powers of two, at
+// most 1; a group more than 2^126 below the largest is dropped) and the score is the max over
+// queries n < Q with j <= lim + n of t_n, times 2^(X - 127): -inf if no query counts, NaN if a
+// group scale is NaN. Loads the accumulators in rounds of 32 columns and waits for them.
+template <int NQ>
+__device__ __forceinline__ float scan_token_score(uint32_t taddr, uint32_t sw, const int (&sig)[4], int j, int lim,
+                                                  int Q) {
+    int x[4];
+    int X = -1000;
+    bool nan = false;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const int e = (int)((sw >> (8 * g)) & 0xFFu);
+        nan |= e == 0xFF;
+        x[g] = e - sig[g];
+        X = max(X, x[g]);
+    }
+    float f[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const int d = x[g] - X;   // <= 0
+        f[g] = d >= -126 ? __uint_as_float((uint32_t)(d + 127) << 23) : 0.0f;
+    }
+    float t[NQ];
+    constexpr int GPR = NQ == 8 ? 2 : 1;   // groups per load round (32 columns)
+#pragma unroll
+    for (int h = 0; h < 4; h += GPR) {
+        uint32_t r[GPR][2 * NQ];
+#pragma unroll
+        for (int k = 0; k < GPR; ++k) scan_ld<NQ>(taddr + (uint32_t)((h + k) * 2 * NQ), r[k]);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int k = 0; k < GPR; ++k)
+#pragma unroll
+            for (int n = 0; n < NQ; ++n) {
+                const float a = __uint_as_float(r[k][n]) + __uint_as_float(r[k][NQ + n]);
+                t[n] = (h + k == 0) ? f[0] * a : fmaf(f[h + k], a, t[n]);
+            }
+    }
+    float best = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < NQ; ++n) {
+        const bool ok = n < Q && j <= lim + n;
+        best = ok ? fmaxf(best, t[n]) : best;
+    }
+    if (nan) return __uint_as_float(0x7FC00000u);
+    return best == -INFINITY ? best : mul_exp2(best, X - 127);
+}
+
+// Order-preserving u32 key of a float (NaN lowest) and back, for one-instruction warp maxima.
+__device__ __forceinline__ uint32_t scan_key(float v) {
+    if (v != v) return 0u;
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float scan_unkey(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+    uint32_t r;
+    asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+    return r;
+}
+
+// Scores pages phys[0 .. np) (physical ids in shared memory; -1 = a bad id: flagged, scored -inf)
+// of one row, logical pages p_first .., into score_row[p_first + i]. Warps 4-7 call pre() first;
+// the new index rows of pages [wait_from, np) are written there: pre() arrives on sp.ins (one arrival
+// per warp, after a proxy fence) and the copiers wait for those arrivals before copying those pages
+// (wait_from >= np: no wait). Every thread of the 8-warp block calls it. Every thread must reach a
+// block barrier after the call before the next one (or before reusing the query pieces);
+// scan_finish then retires the last stages.
+template <int NQ, int ST, int SA, class Pre>
+__device__ __forceinline__ void scan_pages(ScanPipe& sp, const CUtensorMap* map, const int64_t* phys, int np,
+                                           int p_first, int wait_from, int lim, int Q, const ScQuery& sq,
+                                           float* score_row, int32_t* status, Pre pre) {
+    static_assert(SA * 8 * NQ <= 384, "accumulators");
+    constexpr int N = 2 * NQ;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t seq = sp.seq;
+    if (warp == 0 || warp == 3) {
+        // ---- page copies: warp 0 the even pages, warp 3 the odd ones ----
+        if (lane == 0) {
+            bool waited = false;
+#pragma unroll 1
+            for (int i = warp == 0 ? 0 : 1; i < np; i += 2) {
+                const uint32_t g = seq + (uint32_t)i, st = g % ST, use = g / ST;
+                if (use > 0) scan_wait(sp, &sp.empty[st], (use - 1) & 1u, status);
+                if (i >= wait_from && !waited) {
+                    scan_wait(sp, sp.ins, sp.ins_seq & 1u, status);
+                    fence_proxy_async_global();
+                    waited = true;
+                }
+                const int64_t ph = phys[i];
+                if (ph >= 0 && !*(volatile int*)sp.gave_up) {
+                    mbar_arrive_expect_tx(&sp.full[st], kScanTxBytes);
+                    scan_tma_page(sp.tiles + st * kScanTileBytes, map, (int)ph, &sp.full[st]);
+                } else {
+                    mbar_arrive(&sp.full[st]);   // a bad page id: nothing to copy (scored -inf)
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1 || warp == 2) {
+        // ---- scale copy and MMA issue: warp 1 the even pages, warp 2 the odd ones ----
+        constexpr uint32_t idesc = idesc_scan(N);
+        const uint32_t qt_s = smem_u32(sp.qt);
+#pragma unroll 1
+        for (int i = warp - 1; i < np; i += 2) {
+            const uint32_t g = seq + (uint32_t)i, st = g % ST, as = g % SA;
+            // the accumulator stage and its ring slot are free (the epilogue read page g - SA)
+            if (g >= (uint32_t)SA) scan_wait(sp, &sp.aempty[as], ((g / SA) - 1) & 1u, status);
+            const bool ok = scan_wait(sp, &sp.full[st], (g / ST) & 1u, status);
+            // tokens 4 lane .. 4 lane + 3: two 8-byte halves of the scale rows, one 16-byte store
+            const uint8_t* srow = sp.tiles + st * kScanTileBytes + 128 * 128;
+            {
+                const int t0 = 4 * lane, r = t0 >> 4, c0 = (t0 & 15) >> 1;
+                const uint2 w01 = *reinterpret_cast<const uint2*>(srow + r * 128 + (((c0 ^ r) & 7) << 4));
+                const uint2 w23 = *reinterpret_cast<const uint2*>(srow + r * 128 + ((((c0 + 1) ^ r) & 7) << 4));
+                *reinterpret_cast<uint4*>(sp.ring + as * kScanScaleBytes + 16 * lane) = make_uint4(w01.x, w01.y, w23.x, w23.y);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                tc_fence_after_sync();
+                if (ok && phys[i] >= 0 && !*(volatile int*)sp.gave_up) {
+                    const uint32_t tile_s = smem_u32(sp.tiles + st * kScanTileBytes);
+                    const uint32_t d = sp.tmem + as * 4 * N;
+#pragma unroll
+                    for (int gg = 0; gg < 4; ++gg) {
+                        const uint64_t ad = sw128_desc(tile_s + 32 * gg);
+                        const uint64_t bd = sw128_desc(qt_s + 32 * gg);
+                        asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+                                     " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d + gg * N),
+                                     "l"(ad), "l"(bd), "r"(idesc), "r"(0u)
+                                     : "memory");
+                    }
+                }
+                tc_commit(&sp.afull[as]);
+                tc_commit(&sp.empty[st]);
+                mbar_arrive(&sp.afull[as]);   // the ring slot is written (release)
+            }
+            __syncwarp();
+        }
+    } else if (warp >= 4) {
+        pre();
+        // ---- epilogue: thread = token, two pages an iteration ----
+        const int qd = warp - 4, tok = 32 * qd + lane;
+        const uint32_t lane_base = sp.tmem + ((uint32_t)(32 * qd) << 16);
+        const int sig[4] = {sq.sig_min + sq.rel[0], sq.sig_min + sq.rel[1], sq.sig_min + sq.rel[2], sq.sig_min + sq.rel[3]};
+#pragma unroll 1
+        for (int i = 0; i < np; i += 2) {
+            const bool two = i + 1 < np;
+            const uint32_t g0 = seq + (uint32_t)i, g1 = g0 + 1u;
+            scan_wait(sp, &sp.afull[g0 % SA], (g0 / SA) & 1u, status);
+            if (two) scan_wait(sp, &sp.afull[g1 % SA], (g1 / SA) & 1u, status);
+            tc_fence_after_sync();
+            // warp-uniform (the tensor-memory loads are warp-collective)
+            const bool gave = *(volatile int*)sp.gave_up != 0;
+            const bool good0 = __all_sync(0xFFFFFFFFu, phys[i] >= 0 && !gave);
+            const bool good1 = two && __all_sync(0xFFFFFFFFu, phys[i + 1] >= 0 && !gave);
+            const uint32_t sw0 = reinterpret_cast<const uint32_t*>(sp.ring + (g0 % SA) * kScanScaleBytes)[tok];
+            const uint32_t sw1 = two ? reinterpret_cast<const uint32_t*>(sp.ring + (g1 % SA) * kScanScaleBytes)[tok] : 0u;
+            const int j0 = (p_first + i) * kPage + tok;
+            const float s0 = good0 ? scan_token_score<NQ>(lane_base + (g0 % SA) * 4 * N, sw0, sig, j0, lim, Q) : -INFINITY;
+            const float s1 = good1 ? scan_token_score<NQ>(lane_base + (g1 % SA) * 4 * N, sw1, sig, j0 + kPage, lim, Q)
+                                   : -INFINITY;
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&sp.aempty[g0 % SA]);
+                if (two) mbar_arrive(&sp.aempty[g1 % SA]);
+            }
+            // NaN tokens rank lowest
+            const uint32_t k0 = warp_max_u32(scan_key(s0)), k1 = warp_max_u32(scan_key(s1));
+            if (lane == 0) {
+                reinterpret_cast<uint32_t*>(sp.red)[(i % kScanRedPages) * 4 + qd] = k0;
+                if (two) reinterpret_cast<uint32_t*>(sp.red)[((i + 1) % kScanRedPages) * 4 + qd] = k1;
+            }
+            const int last = two ? i + 1 : i;
+            if ((last + 1) % kScanRedPages == 0 || last + 1 == np) {
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                const int base = (last / kScanRedPages) * kScanRedPages, cnt = last + 1 - base;
+                const int t = threadIdx.x - 128;
+                if (t < cnt) {
+                    const uint32_t* m = reinterpret_cast<const uint32_t*>(sp.red) + 4 * t;
+                    const bool ok_page = phys[base + t] >= 0;
+                    const uint32_t k = max(max(m[0], m[1]), max(m[2], m[3]));
+                    // a page whose every token is NaN or masked scores -inf
+                    score_row[p_first + base + t] = (ok_page && k != 0u) ? scan_unkey(k) : -INFINITY;
+                    if (!ok_page) flag_status(status, SMX_DEV_BAD_PAGE_ID);
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+            }
+        }
+    }
+    sp.seq = seq + (uint32_t)np;
+    if (wait_from < np) sp.ins_seq += 1;
+}
+
+// After the block barrier that follows the last scan_pages of a CTA (or before its barriers or
+// columns are used for anything else): thread 0 waits until the last stages' MMA commits have
+// arrived.
+template <int ST>
+__device__ __forceinline__ void scan_finish(ScanPipe& sp, int32_t* status) {
+    if (threadIdx.x == 0) {
+        const uint32_t end = sp.seq;
+        for (uint32_t g = end > (uint32_t)ST ? end - ST : 0u; g < end; ++g)
+            scan_wait(sp, &sp.empty[g % ST], (g / ST) & 1u, status);
+    }
+}
+
+}  // namespace smx

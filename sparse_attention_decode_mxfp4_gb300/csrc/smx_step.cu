@@ -23,9 +23,11 @@
 //  C. Merge. Each unit's CTA waits for the S partitions of its group and merges slice s of the
 //     group's query rows.
 //  D. The last CTA to finish resets every counter to zero for the next step.
-// Every wait is bounded (about two seconds); a wait that gives up sets SMX_DEV_TIMEOUT and the
-// CTA goes on without reading or writing out of bounds.
+// Every wait is bounded (waits for other CTAs: 200 ms of global time by default, see
+// smx_set_wait_limit_ns; waits for this CTA's own copies and MMAs: about a second); a wait that
+// gives up sets SMX_DEV_TIMEOUT and the CTA goes on without reading or writing out of bounds.
 #include <math.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -33,7 +35,7 @@
 #include "smx_attend_tc.cuh"
 #include "smx_device.cuh"
 #include "smx_internal.h"
-#include "smx_score.cuh"
+#include "smx_scan.cuh"
 #include "smx_select.cuh"
 
 namespace smx {
@@ -68,13 +70,16 @@ struct StepArgs {
     const int32_t* topk_in;      // REUSE: the given selection [B][topk], and its counts [B]
     const int32_t* count_in;
     int ppb_log2;                // log2 of the pages per selected block (0: one page)
+    uint64_t wait_ns;            // bound of every wait for other CTAs (global-timer ns)
 };
 
 constexpr int kStepWarps = 8;
 constexpr int kStepMaxChunk = 256;   // pages of one scoring chunk (page-table entries in smem)
-constexpr int kRedPages = 32;        // page maxima combined per flush
 constexpr int kPtCache = 2048;       // page-table entries of a unit's row kept in shared memory
 constexpr int kCounterStride = 32;   // u32 words between counters: each on its own 128-byte line
+constexpr int kStepScanStages = 10;  // page stages of the index scan (pages in flight per SM)
+constexpr int kPlanRows = 256;       // rows up to which the scan's chunks follow the rows' real lengths
+
 
 // Selection over blocks of 2^log2 pages: keys[0 .. n_pages) (page keys, shared memory) become
 // keys[0 .. n_blocks), each block's best page key (score_key is order-preserving; NaN pages, key 0,
@@ -117,12 +122,20 @@ __device__ __forceinline__ int given_selection(const StepArgs& a, int b, int n_p
 }
 
 template <bool RS, int NT, bool TC, bool REUSE>
-__global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArgs a) {
+__global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const StepArgs a,
+                                                                       const __grid_constant__ CUtensorMap idx_map) {
+    constexpr int NQ = 8 * NT;                   // query slots of the index scan
+    constexpr int kStepScanAcc = scan_acc_stages(NQ);   // its accumulator stages
+    constexpr bool kScan = !REUSE;               // phase A scans the index cache
+    constexpr bool kTmem = kScan || TC;          // tensor memory: the scan's accumulators, the attention's
     extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ __align__(16) uint32_t qh[16][64];
-    __shared__ int sig[16];
-    __shared__ float red[kRedPages][kStepWarps];
     __shared__ int64_t phys_s[kStepMaxChunk];
+    __shared__ float gmax[8][4];                 // the scan's query set-up
+    __shared__ float scan_red[kScanRedPages * 4];
+    __shared__ __align__(8) uint64_t scan_bars[scan_barriers(kStepScanStages, kStepScanAcc)];
+    __shared__ int scan_gave_up;
+    __shared__ int plan_c0[kPlanRows], plan_cn[kPlanRows];   // balanced chunk plan: row b's first chunk, count
+    __shared__ int plan_total, plan_mine;
     __shared__ SelectSmem selsm;
     __shared__ __align__(8) uint64_t mbar[4];   // page copies (tensor-core MXFP4: K slot 0, 1, V slot 0, 1)
     __shared__ __align__(8) uint64_t mbar_q;   // the first unit's q rows
@@ -160,6 +173,20 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int nC = gridDim.x, c = blockIdx.x;
+    // the index scan's stages from the (1024-byte aligned) start of dynamic shared memory; they are
+    // free again once phase A is done (the attention's tiles overlap them)
+    ScanPipe sp;
+    {
+        uint8_t* base = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
+        sp.tiles = base;
+        sp.qt = base + kStepScanStages * kScanTileBytes;
+        sp.ring = sp.qt + kScQueryBytes;
+        scan_bind<kStepScanStages, kStepScanAcc>(sp, scan_bars);
+        sp.red = scan_red;
+        sp.gave_up = &scan_gave_up;
+        sp.seq = 0;
+        sp.ins_seq = 0;
+    }
     if (threadIdx.x == 0) {
         mbar_init(&mbar[0], 1);
         mbar_init(&mbar[1], 1);
@@ -168,13 +195,48 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
         mbar_init(&mbar_q, 1);
         mbar_init(&mbar_mma[0], 1);
         mbar_init(&mbar_mma[1], 1);
+        if constexpr (kScan) scan_init<kStepScanStages, kStepScanAcc>(sp, 4);   // insert hand-off: warps 4-7
         mbar_fence_init();
     }
-    // the barriers are initialised before any thread polls one: a CTA with no chunk in phase A
-    // reaches its attention unit's q wait without another barrier
-    if (blockIdx.x >= a.B * a.chunks_per_row) __syncthreads();
-
-    const int P = a.chunk_pages, C = a.chunks_per_row;
+    // one allocation of tensor memory for the whole kernel (one CTA per SM holds all 512 columns)
+    if (kTmem && warp == 0) tmem_alloc(&tmem_slot, kTcCols);
+    tc_fence_before_sync();
+    // Scoring chunks. Balanced plan (up to kPlanRows rows and at least two CTAs per row): from the
+    // rows' real page counts n_b (T in all), chunks of P = ceil(T / (grid - B)) pages, ceil(n_b / P)
+    // of them (at least one) for row b -- at most one chunk per CTA, CTA c taking chunk c in row
+    // order. Every CTA computes the same plan; plan_c0[b] / plan_cn[b] hold row b's first chunk and
+    // chunk count (also the count its attention units wait for). Otherwise the host's plan: chunks of
+    // a.chunk_pages over the page table's width, a.chunks_per_row per row, chunk ci on CTA ci mod grid.
+    // (The plan's block barriers also publish the barriers' initialisation.)
+    const bool balanced = kScan && a.B <= kPlanRows && nC >= 2 * a.B;
+    int P = a.chunk_pages, C = a.chunks_per_row;
+    if (balanced) {
+        int nb = 0;
+        if ((int)threadIdx.x < a.B) {
+            const int ctx_t = clamp_ctx(a.ctx_len[threadIdx.x], a.Q, a.max_pages, nullptr);
+            nb = (ctx_t + kPage - 1) / kPage;
+        }
+        const uint32_t tot = sel_block_incl_scan((uint32_t)nb, selsm, 0);
+        if (threadIdx.x == blockDim.x - 1) plan_total = (int)tot;
+        __syncthreads();
+        P = max(1, (plan_total + (nC - a.B) - 1) / (nC - a.B));
+        const int cb = (int)threadIdx.x < a.B ? max(1, (nb + P - 1) / P) : 0;
+        if (threadIdx.x == 0) plan_mine = -1;
+        const uint32_t incl = sel_block_incl_scan((uint32_t)cb, selsm, 1);
+        if ((int)threadIdx.x < a.B) {
+            const int c0 = (int)incl - cb;
+            plan_c0[threadIdx.x] = c0;
+            plan_cn[threadIdx.x] = cb;
+            if (c >= c0 && c < c0 + cb) plan_mine = threadIdx.x;   // the row of this CTA's chunk
+        }
+        __syncthreads();
+    } else {
+        // the barriers are initialised before any thread polls one: a CTA with no chunk in phase A
+        // reaches its attention unit's q wait without another barrier
+        if (blockIdx.x >= a.B * a.chunks_per_row) __syncthreads();
+    }
+    // chunks per row b (the count of its row counter)
+    auto row_chunks = [&](int b) { return balanced ? plan_cn[b] : C; };
     const int kv_rows = a.Q * 2 * a.Hkv;
     const int M = a.G * a.Q;
     const int n_units = a.B * a.Hkv * a.n_rg * a.S;
@@ -184,7 +246,8 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
     // before phase A, so that neither has to be fetched after it.
     const int u0 = nC - 1 - c;
     const int R = a.rows_per_cta;
-    const bool q_stageable = !RS || (reinterpret_cast<uintptr_t>(a.q_bf16) & 15u) == 0;
+    // (only when nothing is scanned: the scan's stages overlap the staging area)
+    const bool q_stageable = !kScan && (!RS || (reinterpret_cast<uintptr_t>(a.q_bf16) & 15u) == 0);
     if (u0 < n_units) {
         const int rg = (u0 / a.S) % a.n_rg, kvh = (u0 / (a.S * a.n_rg)) % a.Hkv, b = u0 / (a.S * a.n_rg * a.Hkv);
         if (q_stageable && threadIdx.x == 0) {
@@ -260,135 +323,101 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
             if (threadIdx.x == 0) red_release_add(&a.row_cnt[kCounterStride * b], 1u);
         }
     } else {
-        for (int ci = c; ci < a.B * C; ci += nC) {
-            const int b = ci / C, j = ci % C;
+        // this CTA's chunks: balanced, chunk c (if any); else ci = c, c + grid, ...
+        const int b_bal = balanced ? plan_mine : -1;
+        const int n_chunks = balanced ? (b_bal >= 0 ? 1 : 0) : max(0, (a.B * C - c + nC - 1) / nC);
+#pragma unroll 1
+        for (int k = 0; k < n_chunks; ++k) {
+            const int ci = c + k * nC;
+            const int b = balanced ? b_bal : ci / C;
+            const int j = balanced ? c - plan_c0[b_bal] : ci % C;
+            const int Cb = row_chunks(b);
             const int p0 = j * P, np_max = max(0, min(P, a.max_pages - p0));
-            // independent loads first: the row's length, this chunk's page-table entries, the index
-            // query, and the first new K/V row of this warp's share (rows j + C w, j + C (w + 8), ...)
+            // independent loads first: the row's length, this chunk's page-table entries and, on the
+            // writing warps (4-7), their first new rows
             const int ctx_raw = a.ctx_len[b];
             for (int i = threadIdx.x; i < np_max; i += blockDim.x) {
                 const int64_t ph = a.page_table[(int64_t)b * a.max_pages + p0 + i];
                 phys_s[i] = (ph < 0 || ph >= a.n_pool) ? -1 : ph;
             }
-            const IndexQueryRaw qraw = load_index_query(a.qidx + (int64_t)b * a.Q * kD, a.Q);
-            // the row's new index-K rows, one per warp (written below if this chunk owns their page)
-            float4 kidx_x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (warp < a.Q) kidx_x = reinterpret_cast<const float4*>(a.kidx_new + ((int64_t)b * a.Q + warp) * kD)[lane];
-            const int kv_r0 = j + C * warp;
+            // the new rows are written by warps 4-7 (w = warp - 4) before they take the scan's epilogue
+            const bool writer = warp >= 4;
+            const int w4 = warp - 4;
+            const int kv_r0 = j + Cb * w4;   // this writing warp's K/V rows: kv_r0, kv_r0 + 4 Cb, ...
             auto kv_row_src = [&](int r) {
                 const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);   // kind < Hkv: K head, else V head
                 const int64_t tok = (int64_t)b * a.Q + tq;
                 return reinterpret_cast<const float4*>((kind < a.Hkv ? a.k_new : a.v_new) + (tok * a.Hkv + kind % a.Hkv) * kD) + lane;
             };
-            float4 kv_x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (kv_r0 < kv_rows) kv_x = *kv_row_src(kv_r0);
+            float4 kidx_x = make_float4(0.f, 0.f, 0.f, 0.f), kv_x = kidx_x;
+            if (writer) {
+                if (w4 < a.Q) kidx_x = reinterpret_cast<const float4*>(a.kidx_new + ((int64_t)b * a.Q + w4) * kD)[lane];
+                if (kv_r0 < kv_rows) kv_x = *kv_row_src(kv_r0);
+            }
             const int ctx = clamp_ctx(ctx_raw, a.Q, a.max_pages, (j == 0 && threadIdx.x == 0) ? a.status : nullptr);
             const int n_pages = (ctx + kPage - 1) / kPage;
             const int np = max(0, min(np_max, n_pages - p0));
             const int first_new = ctx - a.Q;
-            // chunk pages [own_lo, own_hi) take new index-K rows (positions [lo_new, hi_new))
+            // chunk pages [own_lo, ..) take new index-K rows (positions [lo_new, hi_new))
             const int lo_new = max(max(first_new, 0), p0 * kPage), hi_new = min(ctx, (p0 + np) * kPage);
             const bool owner = lo_new < hi_new;
-            const int own_lo = owner ? lo_new / kPage - p0 : np, own_hi = owner ? (hi_new - 1) / kPage - p0 + 1 : np;
-            __syncthreads();   // page-table entries staged (and the mbarriers initialised)
-
-            // pages go four at a time to the four warp pairs; warp 2q + h scores tiles 4h .. 4h + 3 of
-            // page i0 + q into a per-lane running maximum (one warp reduction per page). The next
-            // group's tiles are in flight while a group is scored; the pages that take no new rows go
-            // out before the inserts.
-            const int pq = warp >> 1, tile0 = (warp & 1) * 4;
-            TileFrag fa[4], fb[4];
-            auto load_page = [&](TileFrag (&f)[4], int i, bool skip_own) {
-                if (i < np && phys_s[i] >= 0 && !(skip_own && i >= own_lo && i < own_hi)) {
-                    const uint8_t* page = a.idx_pool + phys_s[i] * kMxPageBytes;
-    #pragma unroll
-                    for (int k = 0; k < 4; ++k) load_tile(f[k], page, tile0 + k, g, t);
-                }
-            };
-            load_page(fa, pq, true);
+            const int own_lo = owner ? lo_new / kPage - p0 : np;
+            // the row's query pieces (its block barriers also publish phys_s)
+            const ScQuery sq = sc_setup_query<NQ>(a.qidx + (int64_t)b * a.Q * kD, a.Q, sp.qt, gmax);
             if (!pt_stored) store_pt();
-            int64_t kv_phys0 = -1;   // page of this warp's first K/V row
-            if (kv_r0 < kv_rows && first_new + kv_r0 / (2 * a.Hkv) >= 0)
-                kv_phys0 = a.page_table[(int64_t)b * a.max_pages + (first_new + kv_r0 / (2 * a.Hkv)) / kPage];
-            if (owner) {
-                // the new index-K rows on this chunk's pages (one warp per row), then those pages' tiles
-                for (int tq = warp; tq < a.Q; tq += kStepWarps) {
+            auto write_rows = [&]() {   // warps 4-7, before the scan's epilogue
+                if (owner) {
+                    // the new index-K rows on this chunk's pages (one warp per row), before the copiers
+                    // read those pages (they wait for the four writing warps)
+                    for (int tq = w4; tq < a.Q; tq += 4) {
+                        const int pos = first_new + tq;
+                        if (pos < lo_new || pos >= hi_new) continue;
+                        const int64_t phys = phys_s[pos / kPage - p0];
+                        if (phys < 0) {
+                            if (lane == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                            continue;
+                        }
+                        const float4 x = tq == w4 ? kidx_x : reinterpret_cast<const float4*>(a.kidx_new + ((int64_t)b * a.Q + tq) * kD)[lane];
+                        uint8_t* page = a.idx_pool + phys * kMxPageBytes;
+                        quant_row_mxfp4_warp(x, page + (pos % kPage) * 64, page + kMxScaleOff + (pos % kPage) * 4, lane);
+                    }
+                    fence_proxy_async_global();
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sp.ins);
+                }
+                // this warp's share of the row's new K/V rows (read only by the attention phase, after
+                // the row's counter)
+                for (int r = kv_r0; r < kv_rows; r += 4 * Cb) {
+                    const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);
                     const int pos = first_new + tq;
-                    if (pos < lo_new || pos >= hi_new) continue;
-                    const int64_t phys = phys_s[pos / kPage - p0];
-                    if (phys < 0) {
+                    if (pos < 0) continue;
+                    const float4 x = r == kv_r0 ? kv_x : *kv_row_src(r);
+                    const int64_t phys = a.page_table[(int64_t)b * a.max_pages + pos / kPage];
+                    if (phys < 0 || phys >= a.n_pool) {
                         if (lane == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
                         continue;
                     }
-                    const float4 x = tq == warp ? kidx_x : reinterpret_cast<const float4*>(a.kidx_new + ((int64_t)b * a.Q + tq) * kD)[lane];
-                    uint8_t* page = a.idx_pool + phys * kMxPageBytes;
-                    quant_row_mxfp4_warp(x, page + (pos % kPage) * 64, page + kMxScaleOff + (pos % kPage) * 4, lane);
-                }
-                __threadfence();
-                __syncthreads();
-                if (pq >= own_lo && pq < own_hi) load_page(fa, pq, false);
-            }
-
-            // this warp's new K/V rows (read only by the attention phase, after the row's counter), while
-            // the index tiles are in flight
-            for (int r = kv_r0; r < kv_rows; r += C * kStepWarps) {
-                const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);
-                const int pos = first_new + tq;
-                if (pos < 0) continue;
-                const float4 x = r == kv_r0 ? kv_x : *kv_row_src(r);
-                const int64_t phys = r == kv_r0 ? kv_phys0 : (int64_t)a.page_table[(int64_t)b * a.max_pages + pos / kPage];
-                if (phys < 0 || phys >= a.n_pool) {
-                    if (lane == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
-                    continue;
-                }
-                const int h = kind % a.Hkv, slot = pos % kPage;
-                uint8_t* pool = kind < a.Hkv ? a.k_pool : a.v_pool;
-                if (RS) {
-                    uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kRsPageBytes;
-                    quant_row_e4m3rs_warp(x, page + slot * 128, reinterpret_cast<float*>(page + kRsScaleOff) + slot, lane);
-                } else {
-                    uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kMxPageBytes;
-                    quant_row_mxfp4_warp(x, page + slot * 64, page + kMxScaleOff + slot * 4, lane);
-                }
-            }
-            uint32_t qf[NT][16];
-            int sig_c[NT][2];
-            setup_index_query<NT>(qraw, a.Q, qh, sig, qf, sig_c);
-            const int lim = ctx - a.Q;   // token j counts for query n iff j <= lim + n
-    #pragma unroll 1
-            for (int i0 = 0; i0 < np; i0 += 4) {
-                if (i0 + 4 < np) load_page(fb, i0 + 4 + pq, false);
-                const int i = i0 + pq;
-                if (i < np) {
-                    float best = -INFINITY;
-                    if (phys_s[i] >= 0) {
-    #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            best = fmaxf(best, score_tile<NT>(fa[k], qf, sig_c, p0 + i, tile0 + k, g, t, lim, a.Q));
-                    } else if ((warp & 1) == 0 && lane == 0) {
-                        flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                    const int h = kind % a.Hkv, slot = pos % kPage;
+                    uint8_t* pool = kind < a.Hkv ? a.k_pool : a.v_pool;
+                    if (RS) {
+                        uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kRsPageBytes;
+                        quant_row_e4m3rs_warp(x, page + slot * 128, reinterpret_cast<float*>(page + kRsScaleOff) + slot, lane);
+                    } else {
+                        uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kMxPageBytes;
+                        quant_row_mxfp4_warp(x, page + slot * 64, page + kMxScaleOff + slot * 4, lane);
                     }
-    #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
-                    if (lane == 0) red[i % kRedPages][warp & 1] = best;
                 }
-                if ((i0 + 4) % kRedPages == 0 || i0 + 4 >= np) {   // page maxima of pages [base, i0 + 4)
-                    __syncthreads();
-                    const int base = (i0 / kRedPages) * kRedPages;
-                    const int cnt = min(i0 + 4, np) - base;
-                    if ((int)threadIdx.x < cnt)
-                        a.scores[(int64_t)b * a.max_pages + p0 + base + threadIdx.x] =
-                            fmaxf(red[threadIdx.x][0], red[threadIdx.x][1]);
-                    __syncthreads();
-                }
-    #pragma unroll
-                for (int k = 0; k < 4; ++k) fa[k] = fb[k];
-            }
-
+            };
+            if (kTmem) sp.tmem = tmem_slot;
+            scan_pages<NQ, kStepScanStages, kStepScanAcc>(sp, &idx_map, phys_s, np, p0, owner ? own_lo : np,
+                                                         ctx - a.Q, a.Q, sq, a.scores + (int64_t)b * a.max_pages,
+                                                         a.status, write_rows);
             __syncthreads();
             if (threadIdx.x == 0) red_release_add(&a.row_cnt[kCounterStride * b], 1u);
         }
-
+        __syncthreads();
+        scan_finish<kStepScanStages>(sp, a.status);
     }
 
     // ---------------- B. attention units ----------------
@@ -399,7 +428,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
         const bool has_units = u0 < n_units;
         const bool smem_ok = (smem_u32(smem) & 1023u) == 0;
         if (has_units && !smem_ok && threadIdx.x == 0) flag_status(a.status, SMX_DEV_TIMEOUT);
-        if (has_units && warp == 0) tmem_alloc(&tmem_slot, kTcCols);
+        // (tensor memory was allocated at the start; the scan's accumulators are all read)
         tc_fence_before_sync();
         __syncthreads();
         tc_fence_after_sync();
@@ -449,7 +478,8 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
                     }
                 }
             }
-            if (threadIdx.x == 0 && !wait_geq_bounded(&a.row_cnt[kCounterStride * b], (uint32_t)C)) flag_status(a.status, SMX_DEV_TIMEOUT);
+            if (threadIdx.x == 0 && !wait_geq_bounded(&a.row_cnt[kCounterStride * b], (uint32_t)row_chunks(b), a.wait_ns))
+                flag_status(a.status, SMX_DEV_TIMEOUT);
             __syncthreads();   // the row is scored; the staged q rows are packed (the V and P tiles are free)
             const int n_blocks = (n_pages + (1 << a.ppb_log2) - 1) >> a.ppb_log2;
             int k_eff;
@@ -519,13 +549,21 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
         }
         tc_fence_before_sync();
         __syncthreads();
-        if (has_units && warp == 0) {
+        if (warp == 0) {
             tc_fence_after_sync();
             tmem_dealloc(tmem, kTcCols);
         }
 
     } else {
         if (!pt_stored) store_pt();
+        if constexpr (kTmem) {   // the scan's tensor memory: every accumulator has been read
+            tc_fence_before_sync();
+            __syncthreads();
+            if (warp == 0) {
+                tc_fence_after_sync();
+                tmem_dealloc(tmem_slot, kTcCols);
+            }
+        }
         uint32_t gp = 0;          // pages staged by this CTA so far (sets the stages' phase parity)
         bool copies_ok = true;    // false after a copy that did not land: stage nothing more
         for (int u = u0; u < n_units; u += nC) {
@@ -563,7 +601,8 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
                     }
                 }
             }
-            if (threadIdx.x == 0 && !wait_geq_bounded(&a.row_cnt[kCounterStride * b], (uint32_t)C)) flag_status(a.status, SMX_DEV_TIMEOUT);
+            if (threadIdx.x == 0 && !wait_geq_bounded(&a.row_cnt[kCounterStride * b], (uint32_t)row_chunks(b), a.wait_ns))
+                flag_status(a.status, SMX_DEV_TIMEOUT);
             __syncthreads();
             const int n_blocks = (n_pages + (1 << a.ppb_log2) - 1) >> a.ppb_log2;
             int k_eff;
@@ -628,7 +667,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
     for (int u = u0; u < n_units; u += nC) {
         const int s = u % a.S, rg = (u / a.S) % a.n_rg, kvh = (u / (a.S * a.n_rg)) % a.Hkv;
         const int b = u / (a.S * a.n_rg * a.Hkv);
-        if (threadIdx.x == 0 && !wait_geq_bounded(&a.grp_cnt[kCounterStride * ((b * a.Hkv + kvh) * a.n_rg + rg)], (uint32_t)a.S))
+        if (threadIdx.x == 0 && !wait_geq_bounded(&a.grp_cnt[kCounterStride * ((b * a.Hkv + kvh) * a.n_rg + rg)], (uint32_t)a.S, a.wait_ns))
             flag_status(a.status, SMX_DEV_TIMEOUT);
         __syncthreads();
         const int r_end = min((s + 1) * R / a.S, M - rg * R);
@@ -645,6 +684,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(StepArg
     if (threadIdx.x == 0) {
         __threadfence();
         is_last = atomicAdd(a.done_cnt, 1u) == (uint32_t)nC - 1;
+        if (is_last) __threadfence();   // every other CTA's counter updates come before the reset
     }
     __syncthreads();
     if (is_last) {
@@ -673,6 +713,9 @@ StepGeom step_geom(const smx_shape_t& s, bool tc) {
     const size_t ppb = s.pages_per_block > 1 ? (size_t)s.pages_per_block : 1;
     g.smem = tc ? attend_tc_smem_bytes(g.page_bytes) + 8 * ppb * (size_t)s.topk
                 : attend_smem_bytes(g.page_bytes) + (8 * ppb + 4) * (size_t)s.topk;
+    // the index scan's stages share the space (plus slack to align them to 1 KB)
+    const size_t scan = (size_t)scan_smem_bytes(kStepScanStages, scan_acc_stages(8)) + 1024;
+    if (g.smem < scan) g.smem = scan;
     // counters for the larger (mma.sync) group count, so the workspace does not depend on the path
     const int rg64 = (M + unit_rows(s, false) - 1) / unit_rows(s, false);
     g.n_counters = kCounterStride * ((size_t)s.B + (size_t)s.B * s.Hkv * rg64 + 1);
@@ -740,7 +783,8 @@ bool decode_step_uses_tc(const smx_shape_t& s) {
 }
 
 // One cooperative launch of a step kernel variant (every CTA resident, at most one per SM).
-static cudaError_t launch_step_kernel(const void* fn, int n_ctas, size_t smem, cudaStream_t st, StepArgs a) {
+static cudaError_t launch_step_kernel(const void* fn, int n_ctas, size_t smem, cudaStream_t st, StepArgs a,
+                                      const CUtensorMap& map) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(n_ctas);
     cfg.blockDim = dim3(kStepWarps * 32);
@@ -751,7 +795,7 @@ static cudaError_t launch_step_kernel(const void* fn, int n_ctas, size_t smem, c
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, reinterpret_cast<void (*)(StepArgs)>(const_cast<void*>(fn)), a);
+    return cudaLaunchKernelEx(&cfg, reinterpret_cast<void (*)(StepArgs, CUtensorMap)>(const_cast<void*>(fn)), a, map);
 }
 
 cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStream_t st, bool reuse) {
@@ -781,10 +825,17 @@ cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStrea
     a.row_warps = geo.row_warps; a.rows_per_cta = geo.rows_per_cta; a.n_rg = geo.n_rg; a.page_bytes = geo.page_bytes;
     a.topk_in = io.topk_in; a.count_in = io.count_in;
     a.ppb_log2 = s.pages_per_block == 4 ? 2 : s.pages_per_block == 2 ? 1 : 0;
+    a.wait_ns = wait_limit_ns();
 
     // grid: enough CTAs for every attention unit and for two pages each, at most one per SM
     const int64_t n_units = (int64_t)s.B * s.Hkv * geo.n_rg * s.num_splits;
     const int64_t slots = (int64_t)s.B * s.max_pages_per_row;
+    CUtensorMap map;   // the index pool for the scan (unused by a reusing layer)
+    memset(&map, 0, sizeof(map));
+    if (!reuse) {
+        e = encode_index_map(&map, io.idx_pool, s.n_pool_pages);
+        if (e != cudaSuccess) return e;
+    }
     if (reuse) {
         // no scoring: chunks of a row only write its new K/V rows, one row per warp
         const int kv_rows = s.Q * 2 * s.Hkv;
@@ -793,7 +844,7 @@ cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStrea
         a.chunk_pages = 0;
         a.chunks_per_row = C;
         const int n_ctas = (int)(want < max_ctas ? want : max_ctas);
-        return launch_step_kernel(fn, n_ctas, geo.smem, st, a);
+        return launch_step_kernel(fn, n_ctas, geo.smem, st, a, map);
     }
     const int64_t want = n_units > (slots + 1) / 2 ? n_units : (slots + 1) / 2;
     const int n_ctas = (int)(want < max_ctas ? want : max_ctas);
@@ -801,7 +852,7 @@ cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStrea
     if (P > kStepMaxChunk) P = kStepMaxChunk;
     a.chunk_pages = (int)P;
     a.chunks_per_row = (int)((s.max_pages_per_row + P - 1) / P);
-    return launch_step_kernel(fn, n_ctas, geo.smem, st, a);
+    return launch_step_kernel(fn, n_ctas, geo.smem, st, a, map);
 }
 
 }  // namespace smx

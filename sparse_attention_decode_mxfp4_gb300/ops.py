@@ -24,15 +24,15 @@ KV_E4M3_ROWSCALE = 1
 KV_NVFP4 = 2   # refused by the library (SMX_ERR_UNSUPPORTED)
 MXFP4_PAGE_BYTES = 8704
 E4M3RS_PAGE_BYTES = 16896
-DEV_BAD_PAGE_ID, DEV_BAD_CTX, DEV_BAD_TOPK = 1, 2, 4
+DEV_BAD_PAGE_ID, DEV_BAD_CTX, DEV_BAD_TOPK, DEV_TIMEOUT = 1, 2, 4, 8
 SMX_ERR_WORKSPACE = -4
 
 # every symbol include/smx.h declares
-SYMBOLS = ("smx_workspace_bytes", "smx_kv_insert", "smx_kv_prefill", "smx_pack_q_e4m3",
+SYMBOLS = ("smx_workspace_bytes", "smx_kv_insert_mxfp4", "smx_kv_insert", "smx_kv_prefill", "smx_pack_q_e4m3",
            "smx_index_score", "smx_index_score_topk", "smx_sparse_attn_split", "smx_sparse_attn_merge",
            "smx_decode_step", "smx_status_string", "smx_decode_step_launches",
            "smx_suggest_num_splits", "smx_decode_step_noalloc", "smx_decode_step_tensor_cores",
-           "smx_decode_step_reuse")
+           "smx_decode_step_reuse", "smx_set_wait_limit_ns")
 
 
 class SmxError(RuntimeError):
@@ -94,6 +94,7 @@ def lib() -> ctypes.CDLL:
         P, S, I64, ST = ctypes.c_void_p, ctypes.POINTER(_CShape), ctypes.c_int64, ctypes.c_void_p
         sigs = {
             "smx_workspace_bytes": (ctypes.c_size_t, [S]),
+            "smx_kv_insert_mxfp4": (ctypes.c_int, [S] + [P] * 9 + [ST]),
             "smx_kv_insert": (ctypes.c_int, [S] + [P] * 9 + [ST]),
             "smx_kv_prefill": (ctypes.c_int, [S, P, P, P, I64] + [P] * 6 + [ST]),
             "smx_pack_q_e4m3": (ctypes.c_int, [P, P, I64, ST]),
@@ -108,6 +109,7 @@ def lib() -> ctypes.CDLL:
             "smx_suggest_num_splits": (ctypes.c_int, [S]),
             "smx_decode_step_tensor_cores": (ctypes.c_int, [S]),
             "smx_decode_step_noalloc": (ctypes.c_int, [S] + [P] * 15 + [ST]),
+            "smx_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
         }
         for name, (res, args) in sigs.items():
             f = getattr(L, name)
@@ -197,13 +199,13 @@ def suggest_num_splits(shape: Shape) -> int:
 def kv_insert(shape, k_new, v_new, kidx_new, page_table, ctx_len, k_pool, v_pool, idx_pool,
               dev_status=None, stream=None):
     B, Q = shape.B, shape.Q
-    _need("smx_kv_insert", **_step_bufs(shape, None, None, k_new, v_new, page_table, ctx_len, k_pool, v_pool,
+    _need("smx_kv_insert_mxfp4", **_step_bufs(shape, None, None, k_new, v_new, page_table, ctx_len, k_pool, v_pool,
                                         dev_status),
           kidx_new=(kidx_new, B * Q * 128 * 4), idx_pool=(idx_pool, shape.n_pool_pages * MXFP4_PAGE_BYTES))
     cs = shape.c()
-    _check(lib().smx_kv_insert(ctypes.byref(cs), _p(k_new), _p(v_new), _p(kidx_new), _p(page_table),
-                               _p(ctx_len), _p(k_pool), _p(v_pool), _p(idx_pool), _p(dev_status),
-                               _st(stream)), "smx_kv_insert")
+    _check(lib().smx_kv_insert_mxfp4(ctypes.byref(cs), _p(k_new), _p(v_new), _p(kidx_new), _p(page_table),
+                                     _p(ctx_len), _p(k_pool), _p(v_pool), _p(idx_pool), _p(dev_status),
+                                     _st(stream)), "smx_kv_insert_mxfp4")
 
 
 def kv_prefill(shape, k, v, kidx, page_table, n_fill, k_pool, v_pool, idx_pool, dev_status=None,
@@ -300,6 +302,11 @@ def sparse_attn_merge(shape, part_o, part_m, part_l, out=None, stream=None):
     _check(lib().smx_sparse_attn_merge(ctypes.byref(cs), _p(part_o), _p(part_m), _p(part_l), _p(out),
                                        _st(stream)), "smx_sparse_attn_merge")
     return out
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Bound of the fused steps' waits for other CTAs (0 = the default); returns the previous one."""
+    return int(lib().smx_set_wait_limit_ns(int(ns)))
 
 
 def alloc_workspace(shape, device=None) -> torch.Tensor:

@@ -73,7 +73,10 @@ class Workload:
 
 
 def config(n: int) -> Workload:
-    """The four fixed workloads (1 = tiny, 2 = fixed 7-draft verify, 3 = FP8 KV, 4 = long)."""
+    """The fixed workloads (1 = tiny, 2 = fixed 7-draft verify, 3 = FP8 KV, 4 = long) and, as 5, the
+    largest case of the sweep (B 4, Q 8, 16 heads, contexts up to 262144 tokens, top-k 128)."""
+    if n == 5:
+        return sweep_cases()[-1]
     if n == 1:
         return Workload("tiny_b1_q1_h8_ctx1024_k4", B=1, Q=1, Hq=8, Hkv=1, max_ctx=1024,
                         topk=4, num_splits=2, seed=1001)

@@ -28,16 +28,24 @@ def gpu_inputs(w, data, pools):
     return d
 
 
-def gpu_step(w, data, pools, num_splits=None):
+def gpu_step(w, data, pools, num_splits=None, noalloc=False, workspace=None):
+    """The whole step through the C ABI on device copies of the inputs (noalloc: the entry point
+    that works in the library's static scratch)."""
     shape = ops.Shape.of(w, num_splits)
     g = gpu_inputs(w, data, pools)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out, pages, count = ops.decode_step(
-        shape, q_f32=g["q_f32"] if w.kv_format == wl.KV_MXFP4 else None,
-        q_bf16=g["q_bf16"] if w.kv_format == wl.KV_E4M3_ROWSCALE else None,
-        qidx_bf16=g["qidx_bf16"], k_new=g["k_new"], v_new=g["v_new"], kidx_new=g["kidx_new"],
-        page_table=g["page_table"], ctx_len=g["ctx_len"], k_pool=g["k_pool"], v_pool=g["v_pool"],
-        idx_pool=g["idx_pool"], dev_status=status)
+    kw = dict(q_f32=g["q_f32"] if w.kv_format == wl.KV_MXFP4 else None,
+              q_bf16=g["q_bf16"] if w.kv_format == wl.KV_E4M3_ROWSCALE else None,
+              qidx_bf16=g["qidx_bf16"], k_new=g["k_new"], v_new=g["v_new"], kidx_new=g["kidx_new"],
+              page_table=g["page_table"], ctx_len=g["ctx_len"], k_pool=g["k_pool"], v_pool=g["v_pool"],
+              idx_pool=g["idx_pool"], dev_status=status)
+    if noalloc:
+        out, pages, count = ops.decode_step_noalloc(
+            shape, topk_pages=torch.full((w.B, w.topk), -7, dtype=torch.int32, device="cuda"),
+            topk_count=torch.full((w.B,), -7, dtype=torch.int32, device="cuda"),
+            out=torch.full((w.B, w.Q, w.Hq, 128), float("nan"), dtype=torch.float32, device="cuda"), **kw)
+    else:
+        out, pages, count = ops.decode_step(shape, workspace=workspace, **kw)
     torch.cuda.synchronize()
     return dict(out=out.cpu().numpy(), topk_pages=pages.cpu().numpy(), topk_count=count.cpu().numpy(),
                 pools=tuple(g[k].cpu().numpy() for k in ("k_pool", "v_pool", "idx_pool")),
@@ -146,12 +154,12 @@ def oracle_out_for_set(w, data, res, pools_after, pages, count, num_splits=None)
     return oracle.sparse_attn_merge(sh, po, pm, pl)
 
 
-def full_step_parity(w, num_splits=None, data=None):
+def full_step_parity(w, num_splits=None, data=None, noalloc=False, workspace=None):
     """Whole-step parity on one workload: pool bytes, top-k sets, attention output."""
     data = data if data is not None else wl.generate(w)
     pools = H.oracle_pools(w, data)
     ref, ref_pools = H.oracle_step(w, data, pools, num_splits=num_splits)
-    got = gpu_step(w, data, pools, num_splits=num_splits)
+    got = gpu_step(w, data, pools, num_splits=num_splits, noalloc=noalloc, workspace=workspace)
     assert got["status"] == 0
     for a, b in zip(got["pools"], ref_pools):
         assert np.array_equal(a, b), "inserted page bytes differ"

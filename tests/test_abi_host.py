@@ -68,8 +68,9 @@ def test_null_and_misaligned_pointers_are_refused(L):
     cs = good_shape().c()
     a = ctypes.c_void_p(1 << 20)
     mis = ctypes.c_void_p((1 << 20) + 4)
-    assert L.smx_kv_insert(ctypes.byref(cs), None, a, a, a, a, a, a, a, None, None) == -1
-    assert L.smx_kv_insert(ctypes.byref(cs), mis, a, a, a, a, a, a, a, None, None) == -1
+    for insert in (L.smx_kv_insert_mxfp4, L.smx_kv_insert):   # the call and its shorter alias
+        assert insert(ctypes.byref(cs), None, a, a, a, a, a, a, a, None, None) == -1
+        assert insert(ctypes.byref(cs), mis, a, a, a, a, a, a, a, None, None) == -1
     assert L.smx_pack_q_e4m3(a, a, 0, None) == -1
     assert L.smx_pack_q_e4m3(mis, a, 16, None) == -1
     ws = L.smx_workspace_bytes(ctypes.byref(cs))
