@@ -317,6 +317,11 @@ __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence
 // Hint: bring the 128-byte line holding p into L2.
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
+// The same, with the evict-last priority (kept while streams marked evict-first pass through L2).
+__device__ __forceinline__ void prefetch_l2_keep(const void* p) {
+    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
+}
+
 // ---- counters shared by the CTAs of one grid ---------------------------------------------------
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;

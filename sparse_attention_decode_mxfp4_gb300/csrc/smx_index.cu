@@ -6,8 +6,8 @@
 // mxfp4": every page of the row is scored against the index query; commit "MXFP4 main KV": the
 // selected blocks (one 128-token page each) fill the row's sparse table.
 //
-// Scorer: the tensor-map-fed block-scaled tcgen05 scan of smx_scan.cuh, grid (CTAs per row, B), one
-// CTA of 8 warps per SM; rows cut into very few pages per CTA take the mma.sync scorer.
+// Scorer: the tensor-map-fed tcgen05 scan of smx_scan.cuh, grid (CTAs per row, B), two CTAs of 8
+// warps per SM; rows cut into very few pages per CTA take the mma.sync scorer.
 #include <math.h>
 
 #include <mutex>
@@ -34,15 +34,26 @@ struct IndexArgs {
 
 constexpr int kIdxMaxPpc = 64;   // page-table entries of one CTA staged in shared memory
 constexpr int kIdxScanMinPages = 3;   // pages per CTA from which the tensor-core scan is faster
-constexpr int kIdxStages = 12;        // page stages of a scanning CTA (one CTA per SM: 214 KB)
-// dynamic shared memory: the scan's stages and query pieces, plus slack to align them to 1 KB
-constexpr int kIdxSmemBytes = scan_smem_bytes(kIdxStages, scan_acc_stages(8)) + 1024;
+// Shape of a scanning CTA with NQ query slots: with 8 slots two CTAs share an SM (6 page stages and
+// 256 tensor-memory columns each); with 16 the epilogue needs all 255 registers a thread can hold,
+// so one CTA takes the SM (12 stages, 512 columns).
+template <int NQ>
+struct IdxScanShape {
+    static constexpr int kCtasPerSm = NQ <= 8 ? 2 : 1;
+    static constexpr int kStages = 12 / kCtasPerSm;
+    static constexpr int kTmemCols = 512 / kCtasPerSm;
+    static constexpr int kAcc = scan_acc_stages(NQ, kTmemCols);
+    // dynamic shared memory: the stages and query pieces, plus slack to align them to 1 KB
+    static constexpr int kSmemBytes = scan_smem_bytes(kStages, kAcc) + 1024;
+};
 
-// Grid (CTAs per row, B), 256 threads, one CTA per SM: the CTA scans its range of the row's pages
-// with the tensor-map-fed tensor-core pipeline of smx_scan.cuh (SA accumulator stages; 256 columns
-// of tensor memory).
-template <int NQ, int SA>
-__global__ void __launch_bounds__(256, 1) index_scan_kernel(const IndexArgs a, const __grid_constant__ CUtensorMap map) {
+// Grid (CTAs per row, B), 256 threads: the CTA scans its range of the row's pages with the
+// tensor-map-fed tensor-core pipeline of smx_scan.cuh.
+template <int NQ>
+__global__ void __launch_bounds__(256, IdxScanShape<NQ>::kCtasPerSm)
+    index_scan_kernel(const IndexArgs a, const __grid_constant__ CUtensorMap map) {
+    using Sh = IdxScanShape<NQ>;
+    constexpr int kIdxStages = Sh::kStages, SA = Sh::kAcc;
     extern __shared__ __align__(1024) uint8_t dsm[];
     __shared__ int64_t phys_s[kIdxMaxPpc];
     __shared__ float gmax[8][4];
@@ -72,7 +83,7 @@ __global__ void __launch_bounds__(256, 1) index_scan_kernel(const IndexArgs a, c
         phys_s[i] = (ph < 0 || ph >= a.n_pool) ? -1 : ph;
     }
     if (threadIdx.x == 0) scan_init<kIdxStages, SA>(sp, 1);
-    if (warp == 0) tmem_alloc(&tmem_slot, kScanTmemCols);
+    if (warp == 0) tmem_alloc(&tmem_slot, Sh::kTmemCols);
     tc_fence_before_sync();
     const int ctx = clamp_ctx(ctx_raw, a.Q, a.max_pages, (blockIdx.x == 0 && threadIdx.x == 0) ? a.status : nullptr);
     const int n_pages = (ctx + kPage - 1) / kPage;
@@ -92,7 +103,7 @@ __global__ void __launch_bounds__(256, 1) index_scan_kernel(const IndexArgs a, c
     __syncthreads();
     if (warp == 0) {
         tc_fence_after_sync();
-        tmem_dealloc(sp.tmem, kScanTmemCols);
+        tmem_dealloc(sp.tmem, Sh::kTmemCols);
     }
 }
 
@@ -266,22 +277,26 @@ cudaError_t launch_index_scores(const smx_shape_t& s, const uint16_t* qidx, cons
     // the mma.sync scorer (two CTAs per SM) for rows cut into very few pages per CTA, else the scan
     a.pages_per_cta = index_pages_per_cta(s, 2, true);
     const bool mma = a.pages_per_cta < kIdxScanMinPages;
-    if (!mma) a.pages_per_cta = index_pages_per_cta(s, 1, false);
-    const dim3 grid((s.max_pages_per_row + a.pages_per_cta - 1) / a.pages_per_cta, s.B);
     if (mma) {
+        const dim3 grid((s.max_pages_per_row + a.pages_per_cta - 1) / a.pages_per_cta, s.B);
         if (s.Q <= 8) index_score_mma_kernel<1><<<grid, kIdxWarps * 32, 0, st>>>(a);
         else index_score_mma_kernel<2><<<grid, kIdxWarps * 32, 0, st>>>(a);
-    } else {
-        CUtensorMap map;
-        cudaError_t e = encode_index_map(&map, idx_pool, s.n_pool_pages);
-        if (e != cudaSuccess) return e;
-        const void* fn = s.Q <= 8 ? reinterpret_cast<const void*>(index_scan_kernel<8, scan_acc_stages(8)>)
-                                  : reinterpret_cast<const void*>(index_scan_kernel<16, scan_acc_stages(16)>);
-        e = ensure_smem_attr(fn, kIdxSmemBytes);
-        if (e != cudaSuccess) return e;
-        if (s.Q <= 8) index_scan_kernel<8, scan_acc_stages(8)><<<grid, 256, kIdxSmemBytes, st>>>(a, map);
-        else index_scan_kernel<16, scan_acc_stages(16)><<<grid, 256, kIdxSmemBytes, st>>>(a, map);
+        return cudaGetLastError();
     }
+    CUtensorMap map;
+    cudaError_t e = encode_index_map(&map, idx_pool, s.n_pool_pages);
+    if (e != cudaSuccess) return e;
+    auto scan = [&](auto kern, int per_sm, int smem) -> cudaError_t {
+        a.pages_per_cta = index_pages_per_cta(s, per_sm, false);
+        const dim3 grid((s.max_pages_per_row + a.pages_per_cta - 1) / a.pages_per_cta, s.B);
+        const cudaError_t r = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem);
+        if (r != cudaSuccess) return r;
+        kern<<<grid, 256, smem, st>>>(a, map);
+        return cudaSuccess;
+    };
+    e = s.Q <= 8 ? scan(index_scan_kernel<8>, IdxScanShape<8>::kCtasPerSm, IdxScanShape<8>::kSmemBytes)
+                 : scan(index_scan_kernel<16>, IdxScanShape<16>::kCtasPerSm, IdxScanShape<16>::kSmemBytes);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

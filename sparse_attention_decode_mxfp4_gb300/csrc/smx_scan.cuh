@@ -48,10 +48,9 @@ constexpr int kScanTileBytes = kScanRows * 128;   // unpacked: 128 bytes a row (
 constexpr uint32_t kScanTxBytes = kMxPageBytes;   // completion bytes of one page's copy
 constexpr int kScanRedPages = 32;                 // page maxima combined per flush
 constexpr int kScanScaleBytes = 512;              // one page's scale words in the ring
-constexpr int kScanTmemCols = 512;                // tensor-memory columns a scanning CTA allocates
-
-// Accumulator stages of a scan with NQ query slots: four groups x 2 NQ columns each, 384 columns.
-__host__ __device__ constexpr int scan_acc_stages(int nq) { return 384 / (8 * nq); }
+// Accumulator stages of a scan with NQ query slots in `cols` tensor-memory columns (four groups x
+// 2 NQ columns a stage).
+__host__ __device__ constexpr int scan_acc_stages(int nq, int cols) { return cols / (8 * nq); }
 
 // Shared-memory bytes of a scan with `stages` page stages (then the query pieces and the scale
 // ring of `sa` pages), from a 1024-byte-aligned base.
@@ -114,12 +113,19 @@ __device__ __forceinline__ bool scan_wait(const ScanPipe& sp, uint64_t* bar, uin
     return false;
 }
 
+// L2 policy for the index pages: each is read once a step, so evict it first.
+__device__ __forceinline__ uint64_t scan_l2_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // The whole page `phys` (tensor map over the index pool: [pages][136 rows][128 fp4]) into `dst`,
-// completing on bar.
-__device__ __forceinline__ void scan_tma_page(void* dst, const CUtensorMap* map, int phys, uint64_t* bar) {
+// completing on bar, with L2 policy pol.
+__device__ __forceinline__ void scan_tma_page(void* dst, const CUtensorMap* map, int phys, uint64_t* bar, uint64_t pol) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-        ::"r"(smem_u32(dst)), "l"(map), "r"(0), "r"(0), "r"(phys), "r"(smem_u32(bar))
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;"
+        ::"r"(smem_u32(dst)), "l"(map), "r"(0), "r"(0), "r"(phys), "r"(smem_u32(bar)), "l"(pol)
         : "memory");
 }
 
@@ -228,7 +234,6 @@ template <int NQ, int ST, int SA, class Pre>
 __device__ __forceinline__ void scan_pages(ScanPipe& sp, const CUtensorMap* map, const int64_t* phys, int np,
                                            int p_first, int wait_from, int lim, int Q, const ScQuery& sq,
                                            float* score_row, int32_t* status, Pre pre) {
-    static_assert(SA * 8 * NQ <= 384, "accumulators");
     constexpr int N = 2 * NQ;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t seq = sp.seq;
@@ -236,6 +241,7 @@ __device__ __forceinline__ void scan_pages(ScanPipe& sp, const CUtensorMap* map,
         // ---- page copies: warp 0 the even pages, warp 3 the odd ones ----
         if (lane == 0) {
             bool waited = false;
+            const uint64_t pol = scan_l2_policy();
 #pragma unroll 1
             for (int i = warp == 0 ? 0 : 1; i < np; i += 2) {
                 const uint32_t g = seq + (uint32_t)i, st = g % ST, use = g / ST;
@@ -248,7 +254,7 @@ __device__ __forceinline__ void scan_pages(ScanPipe& sp, const CUtensorMap* map,
                 const int64_t ph = phys[i];
                 if (ph >= 0 && !*(volatile int*)sp.gave_up) {
                     mbar_arrive_expect_tx(&sp.full[st], kScanTxBytes);
-                    scan_tma_page(sp.tiles + st * kScanTileBytes, map, (int)ph, &sp.full[st]);
+                    scan_tma_page(sp.tiles + st * kScanTileBytes, map, (int)ph, &sp.full[st], pol);
                 } else {
                     mbar_arrive(&sp.full[st]);   // a bad page id: nothing to copy (scored -inf)
                 }

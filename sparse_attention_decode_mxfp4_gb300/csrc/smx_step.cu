@@ -77,7 +77,8 @@ constexpr int kStepWarps = 8;
 constexpr int kStepMaxChunk = 256;   // pages of one scoring chunk (page-table entries in smem)
 constexpr int kPtCache = 2048;       // page-table entries of a unit's row kept in shared memory
 constexpr int kCounterStride = 32;   // u32 words between counters: each on its own 128-byte line
-constexpr int kStepScanStages = 10;  // page stages of the index scan (pages in flight per SM)
+constexpr int kStepScanStages = 9;   // page stages of the index scan (pages in flight per SM)
+constexpr int kStepQFront = 32768;   // bytes ahead of the scan's stages: the first unit's q (staged or packed)
 constexpr int kPlanRows = 256;       // rows up to which the scan's chunks follow the rows' real lengths
 
 
@@ -125,7 +126,7 @@ template <bool RS, int NT, bool TC, bool REUSE>
 __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const StepArgs a,
                                                                        const __grid_constant__ CUtensorMap idx_map) {
     constexpr int NQ = 8 * NT;                   // query slots of the index scan
-    constexpr int kStepScanAcc = scan_acc_stages(NQ);   // its accumulator stages
+    constexpr int kStepScanAcc = scan_acc_stages(NQ, 384);   // its accumulator stages (of the 512 columns)
     constexpr bool kScan = !REUSE;               // phase A scans the index cache
     constexpr bool kTmem = kScan || TC;          // tensor memory: the scan's accumulators, the attention's
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
         sm = attend_smem(smem, a.page_bytes, mbar, stage_page);
         keys = reinterpret_cast<uint32_t*>(smem);
         sel_all = reinterpret_cast<int*>(sm.raw + 4 * a.page_bytes) + 2 * (a.topk << a.ppb_log2);
-        q_stage = sm.raw;
+        q_stage = kScan ? smem : sm.raw;   // scanning: the front, ahead of the scan's stages
     }
     int* sel = reinterpret_cast<int*>(sm.raw + 4 * a.page_bytes);   // this partition's pages
     int* selph = sel + (a.topk << a.ppb_log2);                       // and their physical ids
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
     // free again once phase A is done (the attention's tiles overlap them)
     ScanPipe sp;
     {
-        uint8_t* base = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
+        uint8_t* base = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u) + kStepQFront;
         sp.tiles = base;
         sp.qt = base + kStepScanStages * kScanTileBytes;
         sp.ring = sp.qt + kScQueryBytes;
@@ -246,8 +247,21 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
     // before phase A, so that neither has to be fetched after it.
     const int u0 = nC - 1 - c;
     const int R = a.rows_per_cta;
-    // (only when nothing is scanned: the scan's stages overlap the staging area)
-    const bool q_stageable = !kScan && (!RS || (reinterpret_cast<uintptr_t>(a.q_bf16) & 15u) == 0);
+    // (the tensor-core path's staging area is taken by the scan's stages: there, the first unit's q
+    // rows are brought into L2 with the evict-last priority instead, so that the index pages streaming
+    // through L2 during the scan, copied with the evict-first one, leave them there)
+    const bool q_stageable = !(TC && kScan) && (!RS || (reinterpret_cast<uintptr_t>(a.q_bf16) & 15u) == 0);
+    if (TC && kScan && u0 < n_units) {
+        const int rg = (u0 / a.S) % a.n_rg, kvh = (u0 / (a.S * a.n_rg)) % a.Hkv, b = u0 / (a.S * a.n_rg * a.Hkv);
+        const int m_lo = rg * R, rows = min(M, m_lo + R) - m_lo;
+        const int lines = RS ? 2 : 4;   // 128-byte lines of a q row (bf16 or f32)
+        const uint8_t* q = RS ? reinterpret_cast<const uint8_t*>(a.q_bf16) : reinterpret_cast<const uint8_t*>(a.q_f32);
+        for (int li = threadIdx.x; li < rows * lines; li += blockDim.x) {
+            const int m = m_lo + li / lines;
+            const int64_t row = ((int64_t)b * a.Q + m / a.G) * a.Hq + kvh * a.G + m % a.G;
+            prefetch_l2_keep(q + row * (lines * 128) + (li % lines) * 128);
+        }
+    }
     if (u0 < n_units) {
         const int rg = (u0 / a.S) % a.n_rg, kvh = (u0 / (a.S * a.n_rg)) % a.Hkv, b = u0 / (a.S * a.n_rg * a.Hkv);
         if (q_stageable && threadIdx.x == 0) {
@@ -416,8 +430,6 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
             __syncthreads();
             if (threadIdx.x == 0) red_release_add(&a.row_cnt[kCounterStride * b], 1u);
         }
-        __syncthreads();
-        scan_finish<kStepScanStages>(sp, a.status);
     }
 
     // ---------------- B. attention units ----------------
@@ -454,7 +466,8 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
             L.h = threadIdx.x >> 7;
             L.valid = L.r < rows;
             L.pos = ctx - a.Q + (L.valid ? (m_lo + L.r) / a.G : 0);
-            // the q tile, before the wait: the first unit's rows were staged at the start
+            // the q tile, before the wait: the first unit's rows were staged at the start (or, when the
+            // scan took the staging area, brought into L2 at the start)
             if (first && q_stageable) {
                 if (!mbar_wait_bounded(&mbar_q, 0)) flag_status(a.status, SMX_DEV_TIMEOUT);
                 pack_q_tile_tc<RS>(smem + kTcV, rows, smem + kTcQ);
@@ -556,14 +569,6 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
 
     } else {
         if (!pt_stored) store_pt();
-        if constexpr (kTmem) {   // the scan's tensor memory: every accumulator has been read
-            tc_fence_before_sync();
-            __syncthreads();
-            if (warp == 0) {
-                tc_fence_after_sync();
-                tmem_dealloc(tmem_slot, kTcCols);
-            }
-        }
         uint32_t gp = 0;          // pages staged by this CTA so far (sets the stages' phase parity)
         bool copies_ok = true;    // false after a copy that did not land: stage nothing more
         for (int u = u0; u < n_units; u += nC) {
@@ -679,6 +684,16 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
         }
     }
 
+    // the scan's tensor memory (the tensor-core path freed its allocation after the attention)
+    if constexpr (kTmem && !TC) {
+        tc_fence_before_sync();
+        __syncthreads();
+        if (warp == 0) {
+            tc_fence_after_sync();
+            tmem_dealloc(tmem_slot, kTcCols);
+        }
+    }
+
     // ---------------- D. the last CTA out clears the counters ----------------
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -714,7 +729,7 @@ StepGeom step_geom(const smx_shape_t& s, bool tc) {
     g.smem = tc ? attend_tc_smem_bytes(g.page_bytes) + 8 * ppb * (size_t)s.topk
                 : attend_smem_bytes(g.page_bytes) + (8 * ppb + 4) * (size_t)s.topk;
     // the index scan's stages share the space (plus slack to align them to 1 KB)
-    const size_t scan = (size_t)scan_smem_bytes(kStepScanStages, scan_acc_stages(8)) + 1024;
+    const size_t scan = (size_t)kStepQFront + scan_smem_bytes(kStepScanStages, scan_acc_stages(8, 384)) + 1024;
     if (g.smem < scan) g.smem = scan;
     // counters for the larger (mma.sync) group count, so the workspace does not depend on the path
     const int rg64 = (M + unit_rows(s, false) - 1) / unit_rows(s, false);

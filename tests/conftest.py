@@ -10,21 +10,13 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
-    config.addinivalue_line("markers", "slow: long-running GPU parity case")
 
 
 def pytest_addoption(parser):
-    parser.addoption("--full-sweep", action="store_true", default=False,
-                     help="run all 216 sweep cases instead of the default stratified subset")
-    parser.addoption("--max-size", action="store_true", default=False,
-                     help="run the parity cases at the ABI's maximum sizes (2M-token rows; minutes of oracle time)")
+    parser.addoption("--quick", action="store_true", default=False,
+                     help="GPU parity: a stratified subset of the 216 sweep cases and no maximum-size rows")
 
 
 @pytest.fixture(scope="session")
-def full_sweep(request):
-    return request.config.getoption("--full-sweep")
-
-
-@pytest.fixture(scope="session")
-def max_size(request):
-    return request.config.getoption("--max-size")
+def quick(request):
+    return request.config.getoption("--quick")

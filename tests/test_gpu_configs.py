@@ -1,6 +1,7 @@
 """Whole-step GPU parity (pool bytes bit-exact, top-k sets under the swap rule, attention within
-max|err| <= 2e-3 + 1e-2 |ref|) on the four fixed workloads at full size, a stratified subset
-of the 216-case sweep (all of it with --full-sweep), and edge cases."""
+max|err| <= 2e-3 + 1e-2 |ref|) on the four fixed workloads at full size, all 216 cases of the sweep,
+rows at the ABI's maximum sizes, and edge cases. --quick runs a stratified subset of the sweep
+and leaves out the maximum sizes."""
 import numpy as np
 import pytest
 import torch
@@ -48,7 +49,7 @@ def test_reuse_step_at_bench_size(n):
 
 def sweep_subset():
     """Every 7th case plus the largest one: covers each value of every axis, ragged lengths and
-    cases with more partitions than selected pages."""
+    cases with more partitions than selected pages (the --quick run)."""
     cases = wl.sweep_cases()
     sub = [c for i, c in enumerate(cases) if i % 7 == 0] + [cases[-1]]
     for axis, vals in (("B", wl.SWEEP_B), ("Q", wl.SWEEP_Q), ("max_ctx", wl.SWEEP_CTX),
@@ -58,19 +59,14 @@ def sweep_subset():
     return sub
 
 
-SUB = sweep_subset()
+SUB = {c.name for c in sweep_subset()}
 
 
-@pytest.mark.parametrize("case", SUB, ids=[c.name for c in SUB])
-def test_sweep_subset(case):
-    C.full_step_parity(case)
-
-
-@pytest.mark.slow
 @pytest.mark.parametrize("case", wl.sweep_cases(), ids=[c.name for c in wl.sweep_cases()])
-def test_sweep_full(case, full_sweep):
-    if not full_sweep:
-        pytest.skip("run with --full-sweep")
+def test_sweep(case, quick):
+    """All 216 sweep cases (--quick: the stratified subset only)."""
+    if quick and case.name not in SUB:
+        pytest.skip("--quick runs the stratified subset")
     C.full_step_parity(case)
 
 
@@ -84,11 +80,10 @@ MAX_SIZE = [
 ]
 
 
-@pytest.mark.slow
 @pytest.mark.parametrize("w", MAX_SIZE, ids=[w.name for w in MAX_SIZE])
-def test_maximum_sizes(w, max_size):
-    if not max_size:
-        pytest.skip("run with --max-size")
+def test_maximum_sizes(w, quick):
+    if quick:
+        pytest.skip("--quick leaves out the 2M-token rows")
     assert w.max_pages == 16384 and w.topk * w.pages_per_block == 4096
     C.full_step_parity(w, num_splits=bench_splits(w))
 
