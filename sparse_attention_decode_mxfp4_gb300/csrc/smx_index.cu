@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(256, IdxScanShape<NQ>::kCtasPerSm)
     constexpr int kIdxStages = Sh::kStages, SA = Sh::kAcc;
     extern __shared__ __align__(1024) uint8_t dsm[];
     __shared__ int64_t phys_s[kIdxMaxPpc];
-    __shared__ float gmax[8][4];
+    __shared__ float gmax[16];
     __shared__ float red[kScanRedPages * 4];
     __shared__ __align__(8) uint64_t bars[scan_barriers(kIdxStages, SA)];
     __shared__ uint32_t tmem_slot;
@@ -69,9 +69,11 @@ __global__ void __launch_bounds__(256, IdxScanShape<NQ>::kCtasPerSm)
     sp.ring = sp.qt + kScQueryBytes;
     scan_bind<kIdxStages, SA>(sp, bars);
     sp.red = red;
+    sp.gmax = gmax;
     sp.gave_up = &gave_up;
     sp.seq = 0;
     sp.ins_seq = 0;
+    sp.q_seq = 0;
     const int b = blockIdx.y;
     const int warp = threadIdx.x >> 5;
     const int p_begin = blockIdx.x * a.pages_per_cta;
@@ -90,12 +92,13 @@ __global__ void __launch_bounds__(256, IdxScanShape<NQ>::kCtasPerSm)
     const int p_end = min(p_end_all, n_pages);
     for (int p = max(p_begin, n_pages) + threadIdx.x; p < p_end_all; p += blockDim.x)
         a.scores[(int64_t)b * a.max_pages + p] = -INFINITY;
-    // the query pieces (its barriers also publish phys_s, the barriers and the allocation)
-    const ScQuery sq = sc_setup_query<NQ>(a.qidx + (int64_t)b * a.Q * kD, a.Q, sp.qt, gmax);
+    // phys_s, the barriers and the allocation published (the epilogue warps build the query pieces
+    // inside the scan, while the first pages are in flight)
+    __syncthreads();
     tc_fence_after_sync();
     sp.tmem = tmem_slot;
     const int np = max(0, p_end - p_begin);
-    scan_pages<NQ, kIdxStages, SA>(sp, &map, phys_s, np, p_begin, np, ctx - a.Q, a.Q, sq,
+    scan_pages<NQ, kIdxStages, SA>(sp, &map, phys_s, np, p_begin, np, ctx - a.Q, a.Q, a.qidx + (int64_t)b * a.Q * kD,
                                    a.scores + (int64_t)b * a.max_pages, a.status, [] {});
     __syncthreads();
     scan_finish<kIdxStages>(sp, a.status);

@@ -67,15 +67,18 @@ struct ScanPipe {
     uint64_t* afull;      // [SA] accumulators written (commit) and the ring slot filled (1 arrival)
     uint64_t* aempty;     // [SA] accumulators and ring slot read (4 epilogue warps)
     uint64_t* ins;        // the caller's new index rows are written (insert_arrivals arrivals)
+    uint64_t* qready;     // the query pieces are in qt (4 arrivals: the epilogue warps)
     float* red;           // [kScanRedPages][4] warp maxima (as order-preserving keys)
+    float* gmax;          // [4][4] per-warp group maxima of the query set-up (shared)
     int* gave_up;         // shared flag
     uint32_t tmem;        // base column of the scan's tensor memory
     uint32_t seq;         // pages this CTA has scanned so far (sets every barrier's phase)
     uint32_t ins_seq;     // insert hand-offs so far (the parity of `ins`)
+    uint32_t q_seq;       // query set-ups so far (the parity of `qready`)
 };
 
-// Barriers a ScanPipe needs: 2 ST + 2 SA + 1.
-__host__ __device__ constexpr int scan_barriers(int st, int sa) { return 2 * st + 2 * sa + 1; }
+// Barriers a ScanPipe needs: 2 ST + 2 SA + 2.
+__host__ __device__ constexpr int scan_barriers(int st, int sa) { return 2 * st + 2 * sa + 2; }
 
 // Points the pipe's barriers into bars[scan_barriers(ST, SA)].
 template <int ST, int SA>
@@ -85,6 +88,7 @@ __device__ __forceinline__ void scan_bind(ScanPipe& sp, uint64_t* bars) {
     sp.afull = bars + 2 * ST;
     sp.aempty = sp.afull + SA;
     sp.ins = sp.aempty + SA;
+    sp.qready = sp.ins + 1;
 }
 
 // One thread: the barriers (before the first use, behind a block barrier).
@@ -101,6 +105,7 @@ __device__ __forceinline__ void scan_init(ScanPipe& sp, uint32_t insert_arrivals
         mbar_init(&sp.aempty[s], 4);
     }
     mbar_init(sp.ins, insert_arrivals);
+    mbar_init(sp.qready, 4);
     *sp.gave_up = 0;
     mbar_fence_init();
 }
@@ -230,9 +235,80 @@ __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
 // (wait_from >= np: no wait). Every thread of the 8-warp block calls it. Every thread must reach a
 // block barrier after the call before the next one (or before reusing the query pieces);
 // scan_finish then retires the last stages.
+// The query pieces of one row (bf16 bits [Q][128], Q <= NQ) built by the 128 threads of warps 4-7
+// while the first pages are in flight: the same arithmetic as sc_setup_query (per 32-dim group g a
+// power-of-two scale 2^sig[g] that brings the group's largest |q| into (224, 448] where it fits;
+// each scaled value as an e4m3 high piece plus an e4m3 low piece of the remainder), item
+// it = t, t + 128 being query slot it / 16 and 8-dim slice it % 16. Writes the pieces to qt, makes
+// them visible to the tensor cores, arrives on qready (one arrival per warp) and returns sig.
+template <int NQ>
+__device__ __forceinline__ void scan_setup_query(const ScanPipe& sp, const uint16_t* qrow, int Q, int (&sig)[4]) {
+    const int t = (int)threadIdx.x - 128, lane = t & 31, qd = t >> 5;
+    constexpr int kItems = NQ / 8;   // 16 slices per query slot over 128 threads
+    float x[kItems][8];
+    float m = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+        const int it = t + 128 * k, n = it >> 4, c8 = it & 15;
+        uint2 r0 = make_uint2(0, 0), r1 = r0;
+        if (n < Q) {
+            const uint2* src = reinterpret_cast<const uint2*>(qrow + (int64_t)n * kD + 8 * c8);
+            r0 = src[0];
+            r1 = src[1];
+        }
+        const uint32_t w[4] = {r0.x, r0.y, r1.x, r1.y};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[k][2 * i] = __uint_as_float(w[i] << 16);
+            x[k][2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[k][i]));   // (NaN ignored, as the scorer's)
+    }
+    // lanes of one group within the warp differ in lane bits 0, 1 (slice) and 4 (query); item k's
+    // group is the same as item 0's (it differs by 128)
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+    if ((lane & 3) == 0 && lane < 16) sp.gmax[qd * 4 + (lane >> 2)] = m;
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+#pragma unroll
+    for (int gg = 0; gg < 4; ++gg) {
+        const float mx = fmaxf(fmaxf(sp.gmax[gg], sp.gmax[4 + gg]), fmaxf(sp.gmax[8 + gg], sp.gmax[12 + gg]));
+        int s = 0;
+        if (mx > 0.0f && mx == mx) {
+            const int E = floor_log2_pos(mx);            // mx in [2^E, 2^(E+1))
+            s = 7 - E;                                    // scaled max in [128, 256)
+            if (mul_exp2(mx, s + 1) <= 448.0f) s += 1;   // in (224, 448] where it fits
+        }
+        sig[gg] = s;
+    }
+    const int g = (lane & 15) >> 2;
+    const int s_mine = g == 0 ? sig[0] : g == 1 ? sig[1] : g == 2 ? sig[2] : sig[3];
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+        const int it = t + 128 * k, n = it >> 4, c8 = it & 15;
+        uint32_t b0[2] = {0, 0}, b1[2] = {0, 0};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float y0 = mul_exp2(x[k][2 * i], s_mine), y1 = mul_exp2(x[k][2 * i + 1], s_mine);
+            const uint32_t q0 = e4m3x2_rn_sat(y0, y1);
+            const float2 f0 = e4m3x2_to_f32x2(q0);
+            const uint32_t q1 = e4m3x2_rn_sat(y0 - f0.x, y1 - f0.y);
+            b0[i >> 1] |= q0 << (16 * (i & 1));
+            b1[i >> 1] |= q1 << (16 * (i & 1));
+        }
+        *reinterpret_cast<uint2*>(sp.qt + sc_chunk(n, c8 >> 1) + 8 * (c8 & 1)) = make_uint2(b0[0], b0[1]);
+        *reinterpret_cast<uint2*>(sp.qt + sc_chunk(NQ + n, c8 >> 1) + 8 * (c8 & 1)) = make_uint2(b1[0], b1[1]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sp.qready);
+}
+
 template <int NQ, int ST, int SA, class Pre>
 __device__ __forceinline__ void scan_pages(ScanPipe& sp, const CUtensorMap* map, const int64_t* phys, int np,
-                                           int p_first, int wait_from, int lim, int Q, const ScQuery& sq,
+                                           int p_first, int wait_from, int lim, int Q, const uint16_t* qrow,
                                            float* score_row, int32_t* status, Pre pre) {
     constexpr int N = 2 * NQ;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -265,6 +341,8 @@ __device__ __forceinline__ void scan_pages(ScanPipe& sp, const CUtensorMap* map,
         // ---- scale copy and MMA issue: warp 1 the even pages, warp 2 the odd ones ----
         constexpr uint32_t idesc = idesc_scan(N);
         const uint32_t qt_s = smem_u32(sp.qt);
+        // the query pieces (written by the epilogue warps while the first pages are in flight)
+        if (np > warp - 1) scan_wait(sp, sp.qready, sp.q_seq & 1u, status);
 #pragma unroll 1
         for (int i = warp - 1; i < np; i += 2) {
             const uint32_t g = seq + (uint32_t)i, st = g % ST, as = g % SA;
@@ -302,11 +380,12 @@ __device__ __forceinline__ void scan_pages(ScanPipe& sp, const CUtensorMap* map,
             __syncwarp();
         }
     } else if (warp >= 4) {
+        int sig[4];
+        scan_setup_query<NQ>(sp, qrow, Q, sig);
         pre();
         // ---- epilogue: thread = token, two pages an iteration ----
         const int qd = warp - 4, tok = 32 * qd + lane;
         const uint32_t lane_base = sp.tmem + ((uint32_t)(32 * qd) << 16);
-        const int sig[4] = {sq.sig_min + sq.rel[0], sq.sig_min + sq.rel[1], sq.sig_min + sq.rel[2], sq.sig_min + sq.rel[3]};
 #pragma unroll 1
         for (int i = 0; i < np; i += 2) {
             const bool two = i + 1 < np;
@@ -355,6 +434,7 @@ __device__ __forceinline__ void scan_pages(ScanPipe& sp, const CUtensorMap* map,
     }
     sp.seq = seq + (uint32_t)np;
     if (wait_from < np) sp.ins_seq += 1;
+    sp.q_seq += 1;
 }
 
 // After the block barrier that follows the last scan_pages of a CTA (or before its barriers or

@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
     constexpr bool kTmem = kScan || TC;          // tensor memory: the scan's accumulators, the attention's
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ int64_t phys_s[kStepMaxChunk];
-    __shared__ float gmax[8][4];                 // the scan's query set-up
+    __shared__ float gmax[16];                   // the scan's query set-up
     __shared__ float scan_red[kScanRedPages * 4];
     __shared__ __align__(8) uint64_t scan_bars[scan_barriers(kStepScanStages, kStepScanAcc)];
     __shared__ int scan_gave_up;
@@ -184,6 +184,8 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
         sp.ring = sp.qt + kScQueryBytes;
         scan_bind<kStepScanStages, kStepScanAcc>(sp, scan_bars);
         sp.red = scan_red;
+        sp.gmax = gmax;
+        sp.q_seq = 0;
         sp.gave_up = &scan_gave_up;
         sp.seq = 0;
         sp.ins_seq = 0;
@@ -376,8 +378,9 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
             const int lo_new = max(max(first_new, 0), p0 * kPage), hi_new = min(ctx, (p0 + np) * kPage);
             const bool owner = lo_new < hi_new;
             const int own_lo = owner ? lo_new / kPage - p0 : np;
-            // the row's query pieces (its block barriers also publish phys_s)
-            const ScQuery sq = sc_setup_query<NQ>(a.qidx + (int64_t)b * a.Q * kD, a.Q, sp.qt, gmax);
+            // phys_s published (the epilogue warps build the row's query pieces inside the scan, while
+            // the first pages are in flight)
+            __syncthreads();
             if (!pt_stored) store_pt();
             auto write_rows = [&]() {   // warps 4-7, before the scan's epilogue
                 if (owner) {
@@ -425,7 +428,8 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
             };
             if (kTmem) sp.tmem = tmem_slot;
             scan_pages<NQ, kStepScanStages, kStepScanAcc>(sp, &idx_map, phys_s, np, p0, owner ? own_lo : np,
-                                                         ctx - a.Q, a.Q, sq, a.scores + (int64_t)b * a.max_pages,
+                                                         ctx - a.Q, a.Q, a.qidx + (int64_t)b * a.Q * kD,
+                                                         a.scores + (int64_t)b * a.max_pages,
                                                          a.status, write_rows);
             __syncthreads();
             if (threadIdx.x == 0) red_release_add(&a.row_cnt[kCounterStride * b], 1u);
