@@ -108,9 +108,13 @@ typedef struct {
 } smx_shape_t;
 
 /* Bytes of device workspace smx_decode_step needs for this shape (step counters, page scores,
- * packed q, split partials, alignment padding). Zero the workspace once before its first use: the
+ * split partials, packed q, alignment padding). Zero the workspace once before its first use: the
  * counters it holds must start at zero, and every call leaves them at zero again. One workspace
- * serves one shape; calls that share a workspace must not overlap on the GPU. */
+ * serves one shape; calls that share a workspace must not overlap on the GPU. Its last
+ * B * Hkv * ceil(Q * Hq / Hkv / 128) * 16384 bytes are the packed q tiles of the tensor-core
+ * attention units (e4m3 codes by smx_pack_q_e4m3's rule, 128 rows of 128 bytes per tile, the
+ * 16-byte chunks of row i at ((chunk ^ i) & 7) * 16 within its 128 bytes, rows in 8-row atoms of
+ * 1024 bytes), written by a step that takes that path; a caller may read them after the step. */
 size_t smx_workspace_bytes(const smx_shape_t* shape);
 
 /* a1 -- [ATOM-2812] "--index-cache-dtype mxfp4" (index-K row store: E8M0 group scale =

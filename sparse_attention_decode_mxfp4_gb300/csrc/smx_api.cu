@@ -87,6 +87,7 @@ struct Workspace {
     float* part_o;
     float* part_m;
     float* part_l;
+    uint8_t* q_img;
     size_t bytes;
 };
 
@@ -106,6 +107,7 @@ Workspace layout(const smx_shape_t* s, void* base) {
     w.part_o = reinterpret_cast<float*>(take(rows * 128 * sizeof(float)));
     w.part_m = reinterpret_cast<float*>(take(rows * sizeof(float)));
     w.part_l = reinterpret_cast<float*>(take(rows * sizeof(float)));
+    w.q_img = reinterpret_cast<uint8_t*>(take(smx::step_q_image_bytes(*s)));
     w.bytes = off;
     return w;
 }
@@ -257,7 +259,7 @@ int smx_decode_step(const smx_shape_t* s, const float* q_f32, const uint16_t* q_
     io.idx_pool = idx_pool; io.k_pool = k_pool; io.v_pool = v_pool;
     io.topk_out = topk_pages; io.count_out = topk_count; io.out = out; io.status = dev_status;
     io.counters = w.counters; io.scores = w.scores;
-    io.part_o = w.part_o; io.part_m = w.part_m; io.part_l = w.part_l;
+    io.part_o = w.part_o; io.part_m = w.part_m; io.part_l = w.part_l; io.q_img = w.q_img;
     return cuda_status(smx::launch_decode_step(*s, io, (cudaStream_t)stream));
 }
 
@@ -286,7 +288,7 @@ int smx_decode_step_reuse(const smx_shape_t* s, const float* q_f32, const uint16
     io.k_pool = k_pool; io.v_pool = v_pool;
     io.topk_in = topk_pages; io.count_in = topk_count; io.out = out; io.status = dev_status;
     io.counters = w.counters; io.scores = w.scores;
-    io.part_o = w.part_o; io.part_m = w.part_m; io.part_l = w.part_l;
+    io.part_o = w.part_o; io.part_m = w.part_m; io.part_l = w.part_l; io.q_img = w.q_img;
     return cuda_status(smx::launch_decode_step(*s, io, (cudaStream_t)stream, true));
 }
 

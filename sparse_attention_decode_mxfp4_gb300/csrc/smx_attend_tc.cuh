@@ -685,19 +685,19 @@ __device__ __forceinline__ bool attend_pages_tc_mx(uint8_t* smem, uint8_t* raw, 
 
 // Partials of this CTA's real rows for partition s: O from tensor-memory columns 128..255 (zero
 // if the partition had no page), the row's l this half's plus the partner's (exchanged through
-// xch); half h writes dims 64 h .. 64 h + 63. part_o [B][S][Q][Hq][128], part_m / part_l
-// [B][S][Q][Hq]; unit row i is query row m_lo + i. Every thread calls it.
+// xch). part_o [B][S][Q][Hq][128], part_m / part_l [B][S][Q][Hq]; unit row i is query row
+// m_lo + i. O goes through `stage` (64 KB of free shared memory, 16-byte aligned: 128 rows of
+// 512 bytes, the 16-byte chunk q of row i at chunk q ^ (i % 32)), so that each warp writes whole
+// 512-byte rows of part_o (a thread's own half row would scatter 16-byte pieces over 32 rows).
+// Every thread calls it, after the page loop drained (the tiles are free).
 __device__ __forceinline__ void finish_partials_tc(const TcLane& L, uint32_t tmem, bool have_o, float m, float l,
-                                                   float* xch, float* part_o, float* part_m, float* part_l, int b, int s,
-                                                   int kvh, int S, int Q, int Hq, int G, int m_lo) {
-    __syncthreads();   // xch free (its last readers passed the page loop's final barrier)
+                                                   float* xch, uint8_t* stage, float* part_o, float* part_m,
+                                                   float* part_l, int b, int s, int kvh, int S, int Q, int Hq, int G,
+                                                   int m_lo, int rows) {
+    __syncthreads();   // xch and the stage free (their last readers passed the page loop's final barrier)
     xch[threadIdx.x] = l;
-    __syncthreads();
-    const float l_row = l + xch[threadIdx.x ^ 128];
-    const int mq = m_lo + L.r;
-    const int64_t row = (((int64_t)b * S + s) * Q + (L.valid ? mq / G : 0)) * Hq + kvh * G + (L.valid ? mq % G : 0);
-    float4* dst = reinterpret_cast<float4*>(part_o + row * kD + 64 * L.h);
     const uint32_t o_cols = tmem + ((uint32_t)(L.r & ~31) << 16) + 128 + 64 * L.h;
+    uint4* srow = reinterpret_cast<uint4*>(stage) + L.r * 32;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
         float ov[16];
@@ -707,14 +707,28 @@ __device__ __forceinline__ void finish_partials_tc(const TcLane& L, uint32_t tme
 #pragma unroll
             for (int j = 0; j < 16; ++j) ov[j] = 0.0f;
         }
-        if (L.valid) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) dst[4 * c + j] = make_float4(ov[4 * j], ov[4 * j + 1], ov[4 * j + 2], ov[4 * j + 3]);
+        for (int k = 0; k < 4; ++k) {
+            const int q = 16 * L.h + 4 * c + k;   // logical chunk: dims 4 q .. 4 q + 3
+            srow[q ^ (L.r & 31)] = make_uint4(__float_as_uint(ov[4 * k]), __float_as_uint(ov[4 * k + 1]),
+                                              __float_as_uint(ov[4 * k + 2]), __float_as_uint(ov[4 * k + 3]));
         }
     }
+    __syncthreads();
+    const int mq = m_lo + L.r;
     if (L.valid && L.h == 0) {
+        const int64_t row = (((int64_t)b * S + s) * Q + mq / G) * Hq + kvh * G + mq % G;
         part_m[row] = m;
-        part_l[row] = l_row;
+        part_l[row] = l + xch[threadIdx.x ^ 128];
+    }
+    // whole rows: warp w writes unit rows w, w + 8, ..., lane j the dims 4 j .. 4 j + 3
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint4* st4 = reinterpret_cast<const uint4*>(stage);
+#pragma unroll 4
+    for (int i = warp; i < rows; i += 8) {
+        const int mi = m_lo + i;
+        const int64_t row = (((int64_t)b * S + s) * Q + mi / G) * Hq + kvh * G + mi % G;
+        reinterpret_cast<uint4*>(part_o + row * kD)[lane] = st4[i * 32 + (lane ^ (i & 31))];
     }
 }
 

@@ -80,7 +80,10 @@ struct StepIO {
     float* part_o;        // [B][S][Q][Hq][128]
     float* part_m;        // [B][S][Q][Hq]
     float* part_l;
+    uint8_t* q_img;       // [B][Hkv][tc row groups][16384]: the tensor-core units' packed q tiles
 };
+// Bytes of the packed q tile images of the fused step's tensor-core units (either path reserves them).
+size_t step_q_image_bytes(const smx_shape_t& s);
 cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStream_t st, bool reuse = false);
 
 // The argument checks of smx_decode_step (shape, pointers, alignment; not the workspace): SMX_OK

@@ -63,6 +63,7 @@ struct StepArgs {
     float* part_o;               // [B][S][Q][Hq][128]
     float* part_m;               // [B][S][Q][Hq]
     float* part_l;
+    uint8_t* q_img;              // [B][Hkv][n_rg][kQImgBytes]: tensor-core units' packed q tiles
     int64_t n_pool;
     int B, Q, Hq, Hkv, G, max_pages, topk, S;
     int row_warps, rows_per_cta, n_rg, page_bytes;
@@ -80,6 +81,7 @@ constexpr int kCounterStride = 32;   // u32 words between counters: each on its 
 constexpr int kStepScanStages = 9;   // page stages of the index scan (pages in flight per SM)
 constexpr int kStepQFront = 32768;   // bytes ahead of the scan's stages: the first unit's q (staged or packed)
 constexpr int kPlanRows = 256;       // rows up to which the scan's chunks follow the rows' real lengths
+constexpr int kQImgBytes = kTcRows * kD;   // one unit's e4m3 q tile image (the shared-memory operand layout)
 
 
 // Selection over blocks of 2^log2 pages: keys[0 .. n_pages) (page keys, shared memory) become
@@ -129,6 +131,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
     constexpr int kStepScanAcc = scan_acc_stages(NQ, 384);   // its accumulator stages (of the 512 columns)
     constexpr bool kScan = !REUSE;               // phase A scans the index cache
     constexpr bool kTmem = kScan || TC;          // tensor memory: the scan's accumulators, the attention's
+    constexpr bool kQImg = TC && !RS && kScan;   // q tiles packed by the scanning CTAs into the workspace
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ int64_t phys_s[kStepMaxChunk];
     __shared__ float gmax[16];                   // the scan's query set-up
@@ -172,7 +175,6 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
     int* selph = sel + (a.topk << a.ppb_log2);                       // and their physical ids
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = lane >> 2, t = lane & 3;
     const int nC = gridDim.x, c = blockIdx.x;
     // the index scan's stages from the (1024-byte aligned) start of dynamic shared memory; they are
     // free again once phase A is done (the attention's tiles overlap them)
@@ -253,7 +255,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
     // rows are brought into L2 with the evict-last priority instead, so that the index pages streaming
     // through L2 during the scan, copied with the evict-first one, leave them there)
     const bool q_stageable = !(TC && kScan) && (!RS || (reinterpret_cast<uintptr_t>(a.q_bf16) & 15u) == 0);
-    if (TC && kScan && u0 < n_units) {
+    if (TC && kScan && !kQImg && u0 < n_units) {
         const int rg = (u0 / a.S) % a.n_rg, kvh = (u0 / (a.S * a.n_rg)) % a.Hkv, b = u0 / (a.S * a.n_rg * a.Hkv);
         const int m_lo = rg * R, rows = min(M, m_lo + R) - m_lo;
         const int lines = RS ? 2 : 4;   // 128-byte lines of a q row (bf16 or f32)
@@ -425,6 +427,20 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
                         quant_row_mxfp4_warp(x, page + slot * 64, page + kMxScaleOff + slot * 4, lane);
                     }
                 }
+                if constexpr (kQImg) {
+                    // this chunk's share of the row's q rows (r = draft token x Hq + head, rows
+                    // j + Cb w4 + 4 Cb k), by the q packing rule into the tensor-core units' q tile
+                    // images: unit row m = token x G + head % G of KV head head / G, row group m / 128,
+                    // in the operand layout the QK MMA reads (published by the row's counter)
+                    const int QH = a.Q * a.Hq;
+                    for (int r = j + Cb * w4; r < QH; r += 4 * Cb) {
+                        const int tq = r / a.Hq, h = r % a.Hq, kvh = h / a.G, m = tq * a.G + h % a.G;
+                        const float4 x = reinterpret_cast<const float4*>(a.q_f32 + ((int64_t)b * QH + r) * kD)[lane];
+                        uint8_t* img = a.q_img + (((int64_t)b * a.Hkv + kvh) * a.n_rg + m / kTcRows) * kQImgBytes;
+                        *reinterpret_cast<uint32_t*>(img + sw128_chunk(m % kTcRows, lane >> 2, kTcRows) + 4 * (lane & 3)) =
+                            pack_q4(x);
+                    }
+                }
             };
             if (kTmem) sp.tmem = tmem_slot;
             scan_pages<NQ, kStepScanStages, kStepScanAcc>(sp, &idx_map, phys_s, np, p0, owner ? own_lo : np,
@@ -456,6 +472,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
         uint32_t gp = 0;          // pages staged by this CTA so far (sets the stages' phase parity)
         uint32_t mma_ph = 0;      // MMA completions seen so far (MXFP4: QK completions)
         uint32_t pv_ph = 0;       // MXFP4: PV completions seen so far
+        uint32_t q_img_ph = 0;    // q tile image copies waited for (the parity of mbar_q)
         bool copies_ok = smem_ok; // false after a copy or MMA that did not finish: stage nothing more
         for (int u = u0; u < n_units; u += nC) {
             const int s = u % a.S, rg = (u / a.S) % a.n_rg, kvh = (u / (a.S * a.n_rg)) % a.Hkv;
@@ -472,12 +489,14 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
             L.pos = ctx - a.Q + (L.valid ? (m_lo + L.r) / a.G : 0);
             // the q tile, before the wait: the first unit's rows were staged at the start (or, when the
             // scan took the staging area, brought into L2 at the start)
-            if (first && q_stageable) {
-                if (!mbar_wait_bounded(&mbar_q, 0)) flag_status(a.status, SMX_DEV_TIMEOUT);
-                pack_q_tile_tc<RS>(smem + kTcV, rows, smem + kTcQ);
-            } else {
-                pack_q_tile_tc_global<RS>(RS ? (const void*)a.q_bf16 : (const void*)a.q_f32, b, kvh, m_lo, rows, a.Q, a.Hq,
-                                          a.G, smem + kTcQ);
+            if constexpr (!kQImg) {
+                if (first && q_stageable) {
+                    if (!mbar_wait_bounded(&mbar_q, 0)) flag_status(a.status, SMX_DEV_TIMEOUT);
+                    pack_q_tile_tc<RS>(smem + kTcV, rows, smem + kTcQ);
+                } else {
+                    pack_q_tile_tc_global<RS>(RS ? (const void*)a.q_bf16 : (const void*)a.q_f32, b, kvh, m_lo, rows, a.Q,
+                                              a.Hq, a.G, smem + kTcQ);
+                }
             }
             if (!first && pt_cached) {
                 __syncthreads();   // the previous unit is done with pt_s
@@ -498,6 +517,15 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
             if (threadIdx.x == 0 && !wait_geq_bounded(&a.row_cnt[kCounterStride * b], (uint32_t)row_chunks(b), a.wait_ns))
                 flag_status(a.status, SMX_DEV_TIMEOUT);
             __syncthreads();   // the row is scored; the staged q rows are packed (the V and P tiles are free)
+            // the unit's q tile: one copy of its image (written by the row's scanning CTAs, acquired
+            // with the row's counter), in flight during the selection
+            const bool q_img_issued = kQImg && copies_ok;
+            if (q_img_issued && threadIdx.x == 0) {
+                fence_proxy_async_global();
+                mbar_arrive_expect_tx(&mbar_q, (uint32_t)kQImgBytes);
+                bulk_g2s(smem + kTcQ, a.q_img + (((int64_t)b * a.Hkv + kvh) * a.n_rg + rg) * kQImgBytes,
+                         (uint32_t)kQImgBytes, &mbar_q);
+            }
             const int n_blocks = (n_pages + (1 << a.ppb_log2) - 1) >> a.ppb_log2;
             int k_eff;
             if constexpr (REUSE) {
@@ -545,7 +573,13 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
                     a.topk_out[(int64_t)b * a.topk + i] = i < k_eff ? sel_all[i] : -1;
                 if (threadIdx.x == 0) a.count_out[b] = k_eff;
             }
-            __syncthreads();
+            bool q_ok = true;   // the q tile landed (thread 0; issued before the selection)
+            if (q_img_issued && threadIdx.x == 0) {
+                q_ok = mbar_wait_bounded(&mbar_q, q_img_ph & 1u);
+                if (!q_ok) flag_status(a.status, SMX_DEV_TIMEOUT);
+            }
+            if (q_img_issued) ++q_img_ph;
+            if (__syncthreads_or(!q_ok)) copies_ok = false;   // stage nothing more
 
             float m_run = -INFINITY, l = 0.0f;
             const bool run = copies_ok && npg > 0;
@@ -559,8 +593,8 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
                                                    kvh, a.page_bytes, ctx, tmem, mbar_mma, mma_ph, pv_ph, L, xch_tc, gp,
                                                    m_run, l, a.status);
             }
-            finish_partials_tc(L, tmem, run, m_run, l, xch_tc, a.part_o, a.part_m, a.part_l, b, s, kvh, a.S, a.Q, a.Hq, a.G,
-                               m_lo);
+            finish_partials_tc(L, tmem, run, m_run, l, xch_tc, smem, a.part_o, a.part_m, a.part_l, b, s, kvh, a.S, a.Q,
+                               a.Hq, a.G, m_lo, rows);
             __syncthreads();
             if (threadIdx.x == 0) red_release_add(&a.grp_cnt[kCounterStride * ((b * a.Hkv + kvh) * a.n_rg + rg)], 1u);
         }
@@ -722,6 +756,11 @@ static int unit_rows(const smx_shape_t& s, bool tc) {
 
 StepGeom step_geom(const smx_shape_t& s) { return step_geom(s, false); }
 
+size_t step_q_image_bytes(const smx_shape_t& s) {
+    const int M = (s.Hq / s.Hkv) * s.Q;
+    return (size_t)s.B * s.Hkv * ((M + kTcRows - 1) / kTcRows) * kQImgBytes;
+}
+
 StepGeom step_geom(const smx_shape_t& s, bool tc) {
     StepGeom g;
     const int M = (s.Hq / s.Hkv) * s.Q;
@@ -837,7 +876,7 @@ cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStrea
     a.row_cnt = io.counters;
     a.grp_cnt = io.counters + kCounterStride * s.B;
     a.done_cnt = io.counters + kCounterStride * (s.B + (size_t)s.B * s.Hkv * geo.n_rg);
-    a.scores = io.scores; a.part_o = io.part_o; a.part_m = io.part_m; a.part_l = io.part_l;
+    a.scores = io.scores; a.part_o = io.part_o; a.part_m = io.part_m; a.part_l = io.part_l; a.q_img = io.q_img;
     a.n_pool = s.n_pool_pages;
     a.B = s.B; a.Q = s.Q; a.Hq = s.Hq; a.Hkv = s.Hkv; a.G = s.Hq / s.Hkv; a.max_pages = s.max_pages_per_row;
     a.topk = s.topk; a.S = s.num_splits;
