@@ -23,8 +23,10 @@ _lib = None
 
 KV_MXFP4 = 0
 KV_E4M3_ROWSCALE = 1
+KV_NVFP4 = 2
 MXFP4_PAGE_BYTES = 8704
 E4M3RS_PAGE_BYTES = 16896
+NVFP4_PAGE_BYTES = 9216
 
 
 def compile_library(src: str, out: str, quiet: bool = False) -> None:
@@ -52,7 +54,9 @@ class _Shape(ctypes.Structure):
                 ("Hkv", ctypes.c_int32), ("max_pages", ctypes.c_int32),
                 ("n_pool_pages", ctypes.c_int64), ("topk", ctypes.c_int32),
                 ("num_splits", ctypes.c_int32), ("kv_format", ctypes.c_int32),
-                ("pages_per_block", ctypes.c_int32)]
+                ("pages_per_block", ctypes.c_int32), ("idx_format", ctypes.c_int32),
+                ("nv_scale_k", ctypes.c_float), ("nv_scale_v", ctypes.c_float),
+                ("nv_scale_idx", ctypes.c_float)]
 
 
 @dataclass
@@ -67,21 +71,32 @@ class Shape:
     num_splits: int
     kv_format: int = KV_MXFP4
     pages_per_block: int = 1
+    idx_format: int = KV_MXFP4
+    nv_scale_k: float = 1.0
+    nv_scale_v: float = 1.0
+    nv_scale_idx: float = 1.0
 
     def c(self) -> _Shape:
         return _Shape(self.B, self.Q, self.Hq, self.Hkv, self.max_pages, self.n_pool_pages,
-                      self.topk, self.num_splits, self.kv_format, self.pages_per_block)
+                      self.topk, self.num_splits, self.kv_format, self.pages_per_block,
+                      self.idx_format, self.nv_scale_k, self.nv_scale_v, self.nv_scale_idx)
 
     @property
     def kv_page_bytes(self) -> int:
-        return E4M3RS_PAGE_BYTES if self.kv_format == KV_E4M3_ROWSCALE else MXFP4_PAGE_BYTES
+        return {KV_E4M3_ROWSCALE: E4M3RS_PAGE_BYTES, KV_NVFP4: NVFP4_PAGE_BYTES}.get(self.kv_format, MXFP4_PAGE_BYTES)
+
+    @property
+    def idx_page_bytes(self) -> int:
+        return NVFP4_PAGE_BYTES if self.idx_format == KV_NVFP4 else MXFP4_PAGE_BYTES
 
 
 def shape_of(w, num_splits=None) -> Shape:
     """Oracle shape of a workload object (anything with B, Q, Hq, Hkv, max_pages, ...)."""
     return Shape(w.B, w.Q, w.Hq, w.Hkv, w.max_pages, w.n_pool_pages, w.topk,
                  w.num_splits if num_splits is None else num_splits, w.kv_format,
-                 getattr(w, "pages_per_block", 1))
+                 getattr(w, "pages_per_block", 1), getattr(w, "idx_format", KV_MXFP4),
+                 getattr(w, "nv_scale_k", 1.0), getattr(w, "nv_scale_v", 1.0),
+                 getattr(w, "nv_scale_idx", 1.0))
 
 
 def lib():
@@ -102,6 +117,8 @@ def lib():
             "orc_e4m3_encode": (ctypes.c_uint8, [ctypes.c_double]),
             "orc_mxfp4_quant_row": (None, [P, P, P]),
             "orc_e4m3rs_quant_row": (None, [P, P, P]),
+            "orc_nvfp4_quant_row": (None, [P, ctypes.c_float, P, P]),
+            "orc_nvfp4_load_row": (None, [P, ctypes.c_int, ctypes.c_float, P]),
             "orc_pack_q_one": (ctypes.c_uint8, [ctypes.c_float]),
             "orc_pack_q_e4m3": (None, [P, P, ctypes.c_int64]),
             "orc_mxfp4_load_row": (None, [P, ctypes.c_int, P]),
@@ -184,6 +201,23 @@ def e4m3rs_quant_row(x):
     s = np.zeros(1, np.float32)
     lib().orc_e4m3rs_quant_row(_p(x), _p(codes), _p(s))
     return codes, s[0]
+
+
+def nvfp4_quant_row(x, g: float):
+    """One row to NVFP4 with the per-tensor decode scale g: (64 nibble bytes, 8 E4M3 scale bytes)."""
+    x = _c(x, np.float32).reshape(128)
+    nib = np.zeros(64, np.uint8)
+    sc = np.zeros(8, np.uint8)
+    lib().orc_nvfp4_quant_row(_p(x), float(g), _p(nib), _p(sc))
+    return nib, sc
+
+
+def nvfp4_load_row(page, slot: int, g: float):
+    page = _c(page, np.uint8).reshape(-1)
+    assert page.size >= NVFP4_PAGE_BYTES
+    out = np.zeros(128, np.float64)
+    lib().orc_nvfp4_load_row(_p(page), int(slot), float(g), _p(out))
+    return out
 
 
 def pack_q_e4m3(q):

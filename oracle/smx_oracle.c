@@ -175,6 +175,52 @@ void orc_e4m3rs_quant_row(const float* x, uint8_t* codes128, float* scale) {
     *scale = s;
 }
 
+/* One 128-element row to NVFP4 with the per-tensor decode scale g ([NVFP4]): eight blocks of
+ * 16 elements, each with an E4M3 scale byte; a value decodes as E2M1(code) x E4M3(byte) x g.
+ * Readings (the pages name the format only):
+ *   s = amax / (6 g), with 6 g and the quotient each rounded to fp32 (round to nearest even);
+ *   byte = E4M3 nearest to min(s, 448), ties to even (0 when s rounds to zero);
+ *   S = E4M3(byte) x g rounded to fp32; y_i = x_i / S rounded to fp32;
+ *   code_i = E2M1 nearest to y_i (orc_e2m1_encode: ties to even, saturating at 6, sign kept).
+ * The arithmetic is fp32 because the codes are decided by it: the quantiser of the kernel
+ * computes in fp32 and the pages fix no other precision. A block whose scale byte is 0 (amax
+ * 0, or below half the smallest E4M3 subnormal times 6 g) stores codes 0; a block holding a NaN
+ * or an infinity stores byte 0x7F (E4M3 NaN) and codes 0. Nibble packing as MXFP4. */
+void orc_nvfp4_quant_row(const float* x, float g, uint8_t* nib64, uint8_t* scale8) {
+    uint8_t codes[ORC_D];
+    volatile float six_g = 6.0f * g;   /* volatile: one fp32 rounding, no contraction */
+    for (int blk = 0; blk < ORC_D / ORC_NV_BLOCK; ++blk) {
+        const float* xb = x + blk * ORC_NV_BLOCK;
+        int nonfinite = 0;
+        float amax = 0.0f;
+        for (int i = 0; i < ORC_NV_BLOCK; ++i) {
+            if (!isfinite(xb[i])) nonfinite = 1;
+            else if (fabsf(xb[i]) > amax) amax = fabsf(xb[i]);
+        }
+        if (nonfinite) {
+            scale8[blk] = 0x7F;
+            for (int i = 0; i < ORC_NV_BLOCK; ++i) codes[blk * ORC_NV_BLOCK + i] = 0;
+            continue;
+        }
+        volatile float s = amax / six_g;
+        double sc = (double)s;
+        if (sc > 448.0) sc = 448.0;
+        uint8_t byte = orc_e4m3_encode(sc);
+        scale8[blk] = byte;
+        volatile float S = (float)orc_e4m3_value(byte) * g;
+        for (int i = 0; i < ORC_NV_BLOCK; ++i) {
+            if (S == 0.0f) {
+                codes[blk * ORC_NV_BLOCK + i] = 0;
+                continue;
+            }
+            volatile float y = xb[i] / S;
+            codes[blk * ORC_NV_BLOCK + i] = orc_e2m1_encode((double)y);
+        }
+    }
+    for (int i = 0; i < ORC_D / 2; ++i)
+        nib64[i] = (uint8_t)(codes[2 * i] | (codes[2 * i + 1] << 4));
+}
+
 /* q packing. [ATOM-2812] commit "e4m3 q_out convention": q is written as e4m3 at unit
  * scale, saturating, from the f32 elements; commit "pack_q_e4m3": in-range values are
  * torch's e4m3 cast, beyond +-448 (infinities too) saturate to +-448, NaN stays NaN.
@@ -227,8 +273,31 @@ void orc_e4m3rs_load_row(const uint8_t* page, int slot, double* out128) {
     for (int d = 0; d < ORC_D; ++d) out128[d] = orc_e4m3_value(page[(size_t)slot * 128 + d]) * (double)s;
 }
 
+/* NVFP4 page (9216 B; reading, the pages give none): bytes [0, 8192) the 128 token rows x 64 B
+ * of nibbles as MXFP4; bytes [8192, 9216) the 128 token rows x 8 E4M3 block scales, block j of
+ * slot s at 8192 + 8 s + j. The per-tensor scale g lives with the pool, not in its pages. */
+void orc_nvfp4_store_row(uint8_t* page, int slot, const uint8_t* nib64, const uint8_t* scale8) {
+    memcpy(page + (size_t)slot * 64, nib64, 64);
+    memcpy(page + 8192 + (size_t)slot * 8, scale8, 8);
+}
+
+void orc_nvfp4_load_row(const uint8_t* page, int slot, float g, double* out128) {
+    const uint8_t* nib = page + (size_t)slot * 64;
+    const uint8_t* sc = page + 8192 + (size_t)slot * 8;
+    for (int d = 0; d < ORC_D; ++d) {
+        int byte = nib[d / 2];
+        int code = (d % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+        out128[d] = orc_e2m1_value(code) * orc_e4m3_value(sc[d / ORC_NV_BLOCK]) * (double)g;
+    }
+}
+
 static size_t kv_page_bytes(const orc_shape* sh) {
+    if (sh->kv_format == ORC_KV_NVFP4) return ORC_NVFP4_PAGE_BYTES;
     return sh->kv_format == ORC_KV_E4M3_ROWSCALE ? ORC_E4M3RS_PAGE_BYTES : ORC_MXFP4_PAGE_BYTES;
+}
+
+static size_t idx_page_bytes(const orc_shape* sh) {
+    return sh->idx_format == ORC_KV_NVFP4 ? ORC_NVFP4_PAGE_BYTES : ORC_MXFP4_PAGE_BYTES;
 }
 
 /* K/V pools hold [n_pool_pages][Hkv][page]; the index pool holds [n_pool_pages][page]. */
@@ -236,12 +305,17 @@ static uint8_t* kv_page(const orc_shape* sh, uint8_t* pool, int64_t phys, int kv
     return pool + ((size_t)phys * sh->Hkv + kvh) * kv_page_bytes(sh);
 }
 
-static void store_kv_row(const orc_shape* sh, uint8_t* page, int slot, const float* x) {
+/* g: the pool's NVFP4 scale (K or V). */
+static void store_kv_row(const orc_shape* sh, uint8_t* page, int slot, const float* x, float g) {
     if (sh->kv_format == ORC_KV_E4M3_ROWSCALE) {
         uint8_t codes[ORC_D];
         float s;
         orc_e4m3rs_quant_row(x, codes, &s);
         orc_e4m3rs_store_row(page, slot, codes, s);
+    } else if (sh->kv_format == ORC_KV_NVFP4) {
+        uint8_t nib[64], sc[8];
+        orc_nvfp4_quant_row(x, g, nib, sc);
+        orc_nvfp4_store_row(page, slot, nib, sc);
     } else {
         uint8_t nib[64], sc[4];
         orc_mxfp4_quant_row(x, nib, sc);
@@ -249,9 +323,23 @@ static void store_kv_row(const orc_shape* sh, uint8_t* page, int slot, const flo
     }
 }
 
-static void load_kv_row(const orc_shape* sh, const uint8_t* page, int slot, double* out) {
+static void load_kv_row(const orc_shape* sh, const uint8_t* page, int slot, float g, double* out) {
     if (sh->kv_format == ORC_KV_E4M3_ROWSCALE) orc_e4m3rs_load_row(page, slot, out);
+    else if (sh->kv_format == ORC_KV_NVFP4) orc_nvfp4_load_row(page, slot, g, out);
     else orc_mxfp4_load_row(page, slot, out);
+}
+
+/* The index pool's rows: MXFP4, or NVFP4 with the index scale. */
+static void store_idx_row(const orc_shape* sh, uint8_t* idx_pool, int64_t phys, int slot, const float* x) {
+    if (sh->idx_format == ORC_KV_NVFP4) {
+        uint8_t nib[64], sc[8];
+        orc_nvfp4_quant_row(x, sh->nv_scale_idx, nib, sc);
+        orc_nvfp4_store_row(idx_pool + (size_t)phys * ORC_NVFP4_PAGE_BYTES, slot, nib, sc);
+    } else {
+        uint8_t nib[64], sc[4];
+        orc_mxfp4_quant_row(x, nib, sc);
+        orc_mxfp4_store_row(idx_pool + (size_t)phys * ORC_MXFP4_PAGE_BYTES, slot, nib, sc);
+    }
 }
 
 /* Insert of token position pos of row b: index-K row, and K and V rows of every KV head. */
@@ -264,14 +352,11 @@ static void insert_token(const orc_shape* sh, int b, int64_t pos, const float* k
     if (pos < 0 || p >= sh->max_pages) return;
     phys = page_table[(size_t)b * sh->max_pages + p];
     if (phys < 0 || phys >= sh->n_pool_pages) return;
-    if (kidx_row && idx_pool) {   /* a layer without an index cache writes K and V only */
-        uint8_t nib[64], sc[4];
-        orc_mxfp4_quant_row(kidx_row, nib, sc);
-        orc_mxfp4_store_row(idx_pool + (size_t)phys * ORC_MXFP4_PAGE_BYTES, slot, nib, sc);
-    }
+    if (kidx_row && idx_pool)   /* a layer without an index cache writes K and V only */
+        store_idx_row(sh, idx_pool, phys, slot, kidx_row);
     for (int h = 0; h < sh->Hkv; ++h) {
-        store_kv_row(sh, kv_page(sh, k_pool, phys, h), slot, k_row + (size_t)h * ORC_D);
-        store_kv_row(sh, kv_page(sh, v_pool, phys, h), slot, v_row + (size_t)h * ORC_D);
+        store_kv_row(sh, kv_page(sh, k_pool, phys, h), slot, k_row + (size_t)h * ORC_D, sh->nv_scale_k);
+        store_kv_row(sh, kv_page(sh, v_pool, phys, h), slot, v_row + (size_t)h * ORC_D, sh->nv_scale_v);
     }
 }
 
@@ -340,11 +425,12 @@ void orc_index_scores(const orc_shape* sh, const uint16_t* qidx_bf16, const uint
             continue;
         }
         int64_t phys = page_table[bp];
-        const uint8_t* page = idx_pool + (size_t)phys * ORC_MXFP4_PAGE_BYTES;
+        const uint8_t* page = idx_pool + (size_t)phys * idx_page_bytes(sh);
         for (int slot = 0; slot < ORC_PAGE; ++slot) {
             int64_t j = p * ORC_PAGE + slot;
             if (j >= ctx) break;
-            orc_mxfp4_load_row(page, slot, krow);
+            if (sh->idx_format == ORC_KV_NVFP4) orc_nvfp4_load_row(page, slot, sh->nv_scale_idx, krow);
+            else orc_mxfp4_load_row(page, slot, krow);
             for (int t = 0; t < sh->Q; ++t) {
                 int64_t pos_t = ctx - sh->Q + t;
                 if (j > pos_t) continue;
@@ -466,7 +552,7 @@ void orc_sparse_attn_split(const orc_shape* sh, const void* q, const uint8_t* k_
                 for (int slot = 0; slot < ORC_PAGE; ++slot) {
                     int64_t j = p * ORC_PAGE + slot;
                     if (j >= ctx || j > pos_t) continue;
-                    load_kv_row(sh, kp, slot, krow);
+                    load_kv_row(sh, kp, slot, sh->nv_scale_k, krow);
                     double dot = 0.0;
                     for (int d = 0; d < ORC_D; ++d) dot += qv[d] * krow[d];
                     double y = dot * inv_sqrt_d * M_LOG2E;
@@ -485,8 +571,8 @@ void orc_sparse_attn_split(const orc_shape* sh, const void* q, const uint8_t* k_
                     for (int slot = 0; slot < ORC_PAGE; ++slot) {
                         int64_t j = p * ORC_PAGE + slot;
                         if (j >= ctx || j > pos_t) continue;
-                        load_kv_row(sh, kp, slot, krow);
-                        load_kv_row(sh, vp, slot, vrow);
+                        load_kv_row(sh, kp, slot, sh->nv_scale_k, krow);
+                        load_kv_row(sh, vp, slot, sh->nv_scale_v, vrow);
                         double dot = 0.0;
                         for (int d = 0; d < ORC_D; ++d) dot += qv[d] * krow[d];
                         double w = exp2(dot * inv_sqrt_d * M_LOG2E - m);

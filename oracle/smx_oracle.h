@@ -19,6 +19,11 @@
  *                Summary (fixed 7-draft verify: 8 query tokens per row; FP8 KV cache).
  *   [OCP-MX]     OCP Microscaling Formats (MX) v1.0 (E2M1 element, E8M0 scale).
  *   [OCP-FP8]    OCP 8-bit Floating Point (OFP8) v1.0 (E4M3: bias 7, max 448, no inf).
+ *   [NVFP4]      NVIDIA's 4-bit format as the pages name it ([ATOM-2812] PR title "FP4 index
+ *                cache and NVFP4 sparse KV cache"; commit "--index-cache-dtype mxfp4": "MXFP4 /
+ *                NVFP4 main KV, NVFP4 index ... stay refused"): E2M1 elements, one E4M3 scale
+ *                per 16 elements, one fp32 scale per tensor. The pages give no page layout or
+ *                rounding rule; the readings are at orc_nvfp4_quant_row.
  * Readings the pages leave open are listed next to each function.
  */
 #ifndef SMX_ORACLE_H
@@ -30,8 +35,10 @@
 #define ORC_GROUP 32         /* MX block size */
 #define ORC_MXFP4_PAGE_BYTES 8704   /* 128 x 64 B nibbles + 128 x 4 B E8M0 scales */
 #define ORC_E4M3RS_PAGE_BYTES 16896 /* 128 x 128 B e4m3 codes + 128 x 4 B fp32 scales */
+#define ORC_NV_BLOCK 16             /* NVFP4 block size */
+#define ORC_NVFP4_PAGE_BYTES 9216   /* 128 x 64 B nibbles + 128 x 8 B E4M3 block scales */
 
-enum { ORC_KV_MXFP4 = 0, ORC_KV_E4M3_ROWSCALE = 1 };
+enum { ORC_KV_MXFP4 = 0, ORC_KV_E4M3_ROWSCALE = 1, ORC_KV_NVFP4 = 2 };
 
 typedef struct {
     int32_t B, Q, Hq, Hkv;
@@ -39,8 +46,12 @@ typedef struct {
     int64_t n_pool_pages;   /* physical pages in each pool */
     int32_t topk;           /* k (pages) */
     int32_t num_splits;     /* S partitions of the selected list */
-    int32_t kv_format;      /* ORC_KV_* for the K/V pools; the index pool is always MXFP4 */
+    int32_t kv_format;      /* ORC_KV_* for the K/V pools */
     int32_t pages_per_block; /* pages per selected block (0 or 1: one page) */
+    int32_t idx_format;     /* ORC_KV_MXFP4 or ORC_KV_NVFP4 for the index pool */
+    float nv_scale_k;       /* NVFP4 per-tensor decode scales (fp32, > 0) of the K, V and */
+    float nv_scale_v;       /* index pools; unused by the other formats */
+    float nv_scale_idx;
 } orc_shape;
 
 /* ---- element formats ---- */
@@ -54,6 +65,7 @@ uint8_t orc_e4m3_encode(double v);          /* nearest E4M3 for finite |v| <= 44
 /* ---- quantisers ---- */
 void orc_mxfp4_quant_row(const float* x, uint8_t* nib64, uint8_t* scale4);
 void orc_e4m3rs_quant_row(const float* x, uint8_t* codes128, float* scale);
+void orc_nvfp4_quant_row(const float* x, float g, uint8_t* nib64, uint8_t* scale8);
 uint8_t orc_pack_q_one(float x);
 void orc_pack_q_e4m3(const float* q, uint8_t* out, int64_t n);
 
@@ -62,6 +74,8 @@ void orc_mxfp4_store_row(uint8_t* page, int slot, const uint8_t* nib64, const ui
 void orc_mxfp4_load_row(const uint8_t* page, int slot, double* out128);
 void orc_e4m3rs_store_row(uint8_t* page, int slot, const uint8_t* codes128, float scale);
 void orc_e4m3rs_load_row(const uint8_t* page, int slot, double* out128);
+void orc_nvfp4_store_row(uint8_t* page, int slot, const uint8_t* nib64, const uint8_t* scale8);
+void orc_nvfp4_load_row(const uint8_t* page, int slot, float g, double* out128);
 
 /* ---- insert ---- */
 void orc_kv_insert(const orc_shape* sh, const float* k_new, const float* v_new,

@@ -16,8 +16,13 @@ Recipe (per workload, numpy PCG64 ``default_rng(seed)``; draws in this order):
   5. index-K page shift (long-context workload): per row round(0.05 * n_pages) distinct pages
      get +3.0 on every element of index-K;
   6. the page table: a random permutation of the physical page ids, row-major;
-  7. poison bytes for tail slots (random nibble bytes; scales 0xFF / NaN).
+  7. poison bytes for tail slots (random nibble bytes; scales 0xFF / NaN; NVFP4 scales 0x7F /
+     NaN).
 q_idx and, for the FP8-KV workload, q are rounded to bf16 (round to nearest even).
+NVFP4 variants (K/V and index pages NVFP4) draw the same inputs; their per-tensor decode scales
+are fixed calibration inputs of the workload (NV_SCALE: with N(0, 1) rows a 16-element block's
+largest |x| of about 1 to 4 maps to E4M3 block scales of about 10 to 40, rows scaled x50 to
+about 500 before saturation at 448), not something this module computes.
 """
 from __future__ import annotations
 
@@ -29,8 +34,11 @@ PAGE = 128
 D = 128
 KV_MXFP4 = 0
 KV_E4M3_ROWSCALE = 1
+KV_NVFP4 = 2
 MXFP4_PAGE_BYTES = 8704
 E4M3RS_PAGE_BYTES = 16896
+NVFP4_PAGE_BYTES = 9216
+NV_SCALE = 0.0173   # per-tensor NVFP4 decode scale of the synthetic K, V and index pools
 
 
 @dataclass(frozen=True)
@@ -52,6 +60,10 @@ class Workload:
     shift_page_frac: float = 0.0
     shift_value: float = 3.0
     pages_per_block: int = 1        # pages per selected block of the sparse table
+    idx_format: int = KV_MXFP4      # index pool: MXFP4 or NVFP4
+    nv_scale_k: float = NV_SCALE    # NVFP4 per-tensor decode scales (used by NVFP4 pools only)
+    nv_scale_v: float = NV_SCALE
+    nv_scale_idx: float = NV_SCALE
 
     @property
     def max_pages(self) -> int:
@@ -63,13 +75,19 @@ class Workload:
 
     @property
     def kv_page_bytes(self) -> int:
-        return E4M3RS_PAGE_BYTES if self.kv_format == KV_E4M3_ROWSCALE else MXFP4_PAGE_BYTES
+        return {KV_E4M3_ROWSCALE: E4M3RS_PAGE_BYTES, KV_NVFP4: NVFP4_PAGE_BYTES}.get(self.kv_format, MXFP4_PAGE_BYTES)
+
+    @property
+    def idx_page_bytes(self) -> int:
+        return NVFP4_PAGE_BYTES if self.idx_format == KV_NVFP4 else MXFP4_PAGE_BYTES
 
     def describe(self) -> dict:
-        return dict(workload=self.name, B=self.B, Q=self.Q, Hq=self.Hq, Hkv=self.Hkv,
-                    max_ctx=self.max_ctx, topk=self.topk,
-                    kv="e4m3_rowscale" if self.kv_format == KV_E4M3_ROWSCALE else "mxfp4",
-                    seed=self.seed)
+        names = {KV_MXFP4: "mxfp4", KV_E4M3_ROWSCALE: "e4m3_rowscale", KV_NVFP4: "nvfp4"}
+        d = dict(workload=self.name, B=self.B, Q=self.Q, Hq=self.Hq, Hkv=self.Hkv,
+                 max_ctx=self.max_ctx, topk=self.topk, kv=names[self.kv_format], seed=self.seed)
+        if self.idx_format != KV_MXFP4:
+            d["index"] = names[self.idx_format]
+        return d
 
 
 def config(n: int) -> Workload:
@@ -100,6 +118,12 @@ SWEEP_Q = (1, 4, 8)
 SWEEP_CTX = (4096, 32768, 131072, 262144)
 SWEEP_K = (8, 32, 128)
 SWEEP_HQ = (8, 16)
+
+
+def nvfp4_variant(w: Workload) -> Workload:
+    """The same workload with NVFP4 K/V and index pages (E2M1 + E4M3 scale per 16 + the
+    per-tensor scales NV_SCALE)."""
+    return replace(w, name="nvfp4_" + w.name, kv_format=KV_NVFP4, idx_format=KV_NVFP4)
 
 
 def sweep_cases() -> list:
@@ -213,13 +237,16 @@ def poison_pools(w: Workload, data: dict, k_pool: np.ndarray, v_pool: np.ndarray
     (NaN); e4m3 row-scale slots get codes 0x7F (NaN) and a NaN fp32 scale."""
     rng = np.random.default_rng(data["poison_seed"])
     nan_f32 = np.frombuffer(np.array([np.nan], np.float32).tobytes(), np.uint8)
-    idx = idx_pool.reshape(w.n_pool_pages, MXFP4_PAGE_BYTES)
+    idx = idx_pool.reshape(w.n_pool_pages, w.idx_page_bytes)
     kk = k_pool.reshape(w.n_pool_pages, w.Hkv, w.kv_page_bytes)
     vv = v_pool.reshape(w.n_pool_pages, w.Hkv, w.kv_page_bytes)
     for phys, lo in poison_slots(w, data, include_new):
         n = PAGE - lo
         idx[phys, lo * 64:PAGE * 64] = rng.integers(0, 256, n * 64, dtype=np.uint8)
-        idx[phys, 8192 + lo * 4:8192 + PAGE * 4] = 0xFF
+        if w.idx_format == KV_NVFP4:
+            idx[phys, 8192 + lo * 8:8192 + PAGE * 8] = 0x7F
+        else:
+            idx[phys, 8192 + lo * 4:8192 + PAGE * 4] = 0xFF
         for pool in (kk, vv):
             if w.kv_format == KV_E4M3_ROWSCALE:
                 pool[phys, :, lo * 128:PAGE * 128] = 0x7F
@@ -227,13 +254,16 @@ def poison_pools(w: Workload, data: dict, k_pool: np.ndarray, v_pool: np.ndarray
             else:
                 pool[phys, :, lo * 64:PAGE * 64] = rng.integers(0, 256, (w.Hkv, n * 64),
                                                                 dtype=np.uint8)
-                pool[phys, :, 8192 + lo * 4:8192 + PAGE * 4] = 0xFF
+                if w.kv_format == KV_NVFP4:
+                    pool[phys, :, 8192 + lo * 8:8192 + PAGE * 8] = 0x7F
+                else:
+                    pool[phys, :, 8192 + lo * 4:8192 + PAGE * 4] = 0xFF
 
 
 def empty_pools(w: Workload):
     return (np.zeros((w.n_pool_pages, w.Hkv, w.kv_page_bytes), np.uint8),
             np.zeros((w.n_pool_pages, w.Hkv, w.kv_page_bytes), np.uint8),
-            np.zeros((w.n_pool_pages, MXFP4_PAGE_BYTES), np.uint8))
+            np.zeros((w.n_pool_pages, w.idx_page_bytes), np.uint8))
 
 
 def shrink(w: Workload, **kw) -> Workload:

@@ -30,10 +30,13 @@ def oracle_step(w, data, pools, num_splits=None, want_partials=False):
     return res, (k_pool, v_pool, idx_pool)
 
 
-def load_kv_row(w, pool, phys, kvh, slot):
+def load_kv_row(w, pool, phys, kvh, slot, pool_is_k=True):
     page = pool.reshape(w.n_pool_pages, w.Hkv, w.kv_page_bytes)[phys, kvh]
     if w.kv_format == wl.KV_E4M3_ROWSCALE:
         return oracle.e4m3rs_load_row(page, slot)
+    if w.kv_format == wl.KV_NVFP4:
+        g = w.nv_scale_k if pool_is_k else w.nv_scale_v
+        return oracle.nvfp4_load_row(page, slot, g)
     return oracle.mxfp4_load_row(page, slot)
 
 
@@ -61,7 +64,7 @@ def dense_selected_attention(w, data, q, k_pool, v_pool, topk_pages, topk_count)
                     if j < ctx:
                         toks.append(j)
                         K.append(load_kv_row(w, k_pool, phys, kvh, slot))
-                        V.append(load_kv_row(w, v_pool, phys, kvh, slot))
+                        V.append(load_kv_row(w, v_pool, phys, kvh, slot, pool_is_k=False))
             if not toks:
                 continue
             toks = torch.tensor(toks)

@@ -56,7 +56,7 @@ def test_full_selection_is_causal_attention():
     assert res["topk_count"][0] == (ctx + 127) // 128
     pt = data["page_table"][0]
     K = torch.tensor(np.array([H.load_kv_row(w, kp, pt[j // 128], 0, j % 128) for j in range(ctx)]))
-    V = torch.tensor(np.array([H.load_kv_row(w, vp, pt[j // 128], 0, j % 128) for j in range(ctx)]))
+    V = torch.tensor(np.array([H.load_kv_row(w, vp, pt[j // 128], 0, j % 128, pool_is_k=False) for j in range(ctx)]))
     q = torch.tensor(H.q_values(w, data, res)[0])                     # [Q][Hq][128]
     pos = torch.arange(ctx - w.Q, ctx)
     mask = torch.arange(ctx)[None, :] <= pos[:, None]                 # [Q][ctx]

@@ -13,7 +13,8 @@ from concurrent.futures import ThreadPoolExecutor
 import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-PIN_FILES = ["tests/test_oracle_formats.py", "tests/test_oracle_index.py", "tests/test_oracle_attention.py"]
+PIN_FILES = ["tests/test_oracle_formats.py", "tests/test_oracle_index.py", "tests/test_oracle_attention.py",
+             "tests/test_oracle_nvfp4.py"]
 
 # (name, text in smx_oracle.c, replacement, occurrences replaced)
 MISTAKES = [
@@ -35,7 +36,7 @@ MISTAKES = [
     ("mxfp4_zero_group_scale", "        int se = 0;\n        if (amax > 0.0) {", "        int se = -127;\n        if (amax > 0.0) {", 1),
     ("mxfp4_nonfinite_kept", "if (!isfinite(xg[i])) nonfinite = 1;", "if (isnan(xg[i])) nonfinite = 1;", 1),
     ("nibble_order", "nib64[i] = (uint8_t)(codes[2 * i] | (codes[2 * i + 1] << 4));",
-     "nib64[i] = (uint8_t)(codes[2 * i + 1] | (codes[2 * i] << 4));", 1),
+     "nib64[i] = (uint8_t)(codes[2 * i + 1] | (codes[2 * i] << 4));", 2),
     ("scale_byte_slot", "memcpy(page + 8192 + (size_t)slot * 4, scale4, 4);",
      "memcpy(page + 8192 + (size_t)(slot ^ 1) * 4, scale4, 4);", 1),
     ("load_group_index", "orc_e8m0_value(sc[d / ORC_GROUP])", "orc_e8m0_value(sc[d % 4])", 1),
@@ -47,8 +48,8 @@ MISTAKES = [
     # insert
     ("insert_position", "insert_token(sh, b, (int64_t)ctx_len[b] - sh->Q + t,",
      "insert_token(sh, b, (int64_t)ctx_len[b] - sh->Q + t - 1,", 1),
-    ("insert_v_from_k", "store_kv_row(sh, kv_page(sh, v_pool, phys, h), slot, v_row + (size_t)h * ORC_D);",
-     "store_kv_row(sh, kv_page(sh, v_pool, phys, h), slot, k_row + (size_t)h * ORC_D);", 1),
+    ("insert_v_from_k", "store_kv_row(sh, kv_page(sh, v_pool, phys, h), slot, v_row + (size_t)h * ORC_D, sh->nv_scale_v);",
+     "store_kv_row(sh, kv_page(sh, v_pool, phys, h), slot, k_row + (size_t)h * ORC_D, sh->nv_scale_v);", 1),
     # index score and top-k
     ("score_causal_off_by_one", "if (j > pos_t) continue;", "if (j >= pos_t) continue;", 1),
     ("score_no_causal_mask", "if (j > pos_t) continue;", "(void)pos_t;", 1),
@@ -66,13 +67,30 @@ MISTAKES = [
     ("attn_q_transposed", "size_t qbase = (((size_t)b * sh->Q + t) * sh->Hq + h) * ORC_D;",
      "size_t qbase = (((size_t)b * sh->Hq + h) * sh->Q + t) * ORC_D;", 1),
     ("attn_causal_mask", "if (j >= ctx || j > pos_t) continue;", "if (j >= ctx) continue;", 2),
-    ("attn_v_is_k", "load_kv_row(sh, vp, slot, vrow);", "load_kv_row(sh, kp, slot, vrow);", 1),
+    ("attn_v_is_k", "load_kv_row(sh, vp, slot, sh->nv_scale_v, vrow);", "load_kv_row(sh, kp, slot, sh->nv_scale_v, vrow);", 1),
     ("attn_natural_exp", "double w = exp2(dot * inv_sqrt_d * M_LOG2E - m);", "double w = exp(dot * inv_sqrt_d - m);", 1),
     ("split_partitions_overlap", "hi = (int)(((int64_t)(s + 1) * k_eff) / S);",
      "hi = (int)(((int64_t)(s + 1) * k_eff + S - 1) / S);", 1),
     ("block_first_page_only", "* ppb + e % ppb;", "* ppb;", 2),
     ("merge_natural_exp", "double w = exp2(part_m[pi] - M);", "double w = exp(part_m[pi] - M);", 1),
     ("merge_unnormalised", "for (int d = 0; d < ORC_D; ++d) o[d] /= L;", "(void)L;", 1),
+    # NVFP4 pages
+    ("nvfp4_scale_divisor", "volatile float six_g = 6.0f * g;", "volatile float six_g = 4.0f * g;", 1),
+    ("nvfp4_scale_without_g", "volatile float s = amax / six_g;", "volatile float s = amax / 6.0f;", 1),
+    ("nvfp4_no_saturation", "if (sc > 448.0) sc = 448.0;", "(void)0;", 1),
+    ("nvfp4_element_scale_without_g", "volatile float S = (float)orc_e4m3_value(byte) * g;",
+     "volatile float S = (float)orc_e4m3_value(byte);", 1),
+    ("nvfp4_nonfinite_byte", "scale8[blk] = 0x7F;", "scale8[blk] = 0xFF;", 1),
+    ("nvfp4_zero_scale_divides", "            if (S == 0.0f) {", "            if (0) {", 1),
+    ("nvfp4_load_block_size", "orc_e4m3_value(sc[d / ORC_NV_BLOCK])", "orc_e4m3_value(sc[d / ORC_GROUP])", 1),
+    ("nvfp4_load_without_g", "orc_e4m3_value(sc[d / ORC_NV_BLOCK]) * (double)g;", "orc_e4m3_value(sc[d / ORC_NV_BLOCK]);", 1),
+    ("nvfp4_scale_slot", "memcpy(page + 8192 + (size_t)slot * 8, scale8, 8);",
+     "memcpy(page + 8192 + (size_t)slot * 4, scale8, 8);", 1),
+    ("nvfp4_index_takes_k_scale", "orc_nvfp4_quant_row(x, sh->nv_scale_idx, nib, sc);",
+     "orc_nvfp4_quant_row(x, sh->nv_scale_k, nib, sc);", 1),
+    ("nvfp4_score_takes_k_scale", "orc_nvfp4_load_row(page, slot, sh->nv_scale_idx, krow);",
+     "orc_nvfp4_load_row(page, slot, sh->nv_scale_k, krow);", 1),
+    ("nvfp4_v_takes_k_scale", "load_kv_row(sh, vp, slot, sh->nv_scale_v, vrow);", "load_kv_row(sh, vp, slot, sh->nv_scale_k, vrow);", 1),
     # the reusing layer's step
     ("reuse_skips_insert", "    orc_kv_insert(sh, k_new, v_new, NULL, page_table, ctx_len, k_pool, v_pool, NULL);\n",
      "", 1),

@@ -31,7 +31,7 @@ def worst_ratio(weights):
         ctx = int(data["ctx_len"][b])
         phys = int(data["page_table"][b][0])
         K = np.array([H.load_kv_row(w, kp, phys, 0, j) for j in range(ctx)])
-        V = np.array([H.load_kv_row(w, vp, phys, 0, j) for j in range(ctx)])
+        V = np.array([H.load_kv_row(w, vp, phys, 0, j, pool_is_k=False) for j in range(ctx)])
         for t in range(w.Q):
             n = ctx - w.Q + t + 1                                   # tokens 0 .. pos_t
             z = (q[b, t] @ K[:n].T).astype(np.float32).astype(np.float64) * (LOG2E / np.sqrt(128.0))
