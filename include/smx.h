@@ -66,8 +66,19 @@ enum {
 enum {
     SMX_KV_MXFP4 = 0,
     SMX_KV_E4M3_ROWSCALE = 1,
-    SMX_KV_NVFP4 = 2   /* named for callers that probe it; refused (SMX_ERR_UNSUPPORTED), as [ATOM-2812]
-                        * refuses NVFP4 main KV ("MXFP4 main KV": NVFP4 stays refused) */
+    SMX_KV_NVFP4 = 2   /* NVFP4 pages: the format [ATOM-2812] names (PR title "FP4 index cache and
+                        * NVFP4 sparse KV cache") and its Mono path refuses ("--index-cache-dtype
+                        * mxfp4": "MXFP4 / NVFP4 main KV, NVFP4 index ... stay refused"); built here
+                        * from its plain reading: E2M1 codes packed as in an MXFP4 page, one E4M3
+                        * scale byte per 16 elements, one fp32 per-tensor decode scale per pool
+                        * (smx_shape_t.nv_scale_*). Page (9216 B): bytes [0, 8192) 128 token rows x
+                        * 64 nibble bytes, bytes [8192, 9216) 128 token rows x 8 block scales. Row
+                        * store: s = amax / (6 g) in fp32, byte = E4M3 nearest to min(s, 448),
+                        * codes = nearest E2M1 to x / (E4M3(byte) g) in fp32 (ties to even,
+                        * saturating, sign kept); a zero scale stores codes 0, a block holding
+                        * NaN / Inf stores byte 0x7F and codes 0. Value = E2M1 x E4M3 x g. Valid as
+                        * kv_format and as idx_format; steps with an NVFP4 pool run the standalone
+                        * kernels in sequence (smx_decode_step_launches). */
 };
 
 /* device status bits */
@@ -81,6 +92,7 @@ enum {
 
 #define SMX_MXFP4_PAGE_BYTES 8704
 #define SMX_E4M3RS_PAGE_BYTES 16896
+#define SMX_NVFP4_PAGE_BYTES 9216
 #define SMX_MAX_Q 16
 #define SMX_MAX_TOPK 4096
 #define SMX_MAX_PAGES_PER_ROW 16384  /* 2M tokens per row */
@@ -97,7 +109,7 @@ typedef struct {
     int64_t n_pool_pages;       /* physical pages in each pool */
     int32_t topk;               /* k pages selected per row */
     int32_t num_splits;         /* S partitions of the selected list for the split stage */
-    int32_t kv_format;          /* SMX_KV_*: K/V page format; the index pool is always MXFP4 */
+    int32_t kv_format;          /* SMX_KV_*: K/V page format */
     int32_t pages_per_block;    /* pages per selected block: 0 or 1 (one page), 2 or 4 ([ATOM-2812]
                                  * commit "MXFP4 main KV": PAGES_PER_BLOCK is a build parameter).
                                  * With 2 or 4, topk counts blocks: a block's score is its best page's,
@@ -105,6 +117,11 @@ typedef struct {
                                  * every page of a selected block inside the row. Only the fused
                                  * steps take 2 or 4; the standalone top-k and split stage refuse
                                  * them (SMX_ERR_UNSUPPORTED). topk * pages_per_block <= 4096. */
+    int32_t idx_format;         /* index page format: SMX_KV_MXFP4 (0, [ATOM-2812] "--index-cache-dtype
+                                 * mxfp4") or SMX_KV_NVFP4 */
+    float nv_scale_k;           /* NVFP4 per-tensor decode scales of the K, V and index pools: finite */
+    float nv_scale_v;           /* and > 0 where that pool is NVFP4, ignored otherwise (SMX_ERR_INVALID_ARG */
+    float nv_scale_idx;         /* if not); with NVFP4, pages_per_block must be 0 or 1 */
 } smx_shape_t;
 
 /* Bytes of device workspace smx_decode_step needs for this shape (step counters, page scores,

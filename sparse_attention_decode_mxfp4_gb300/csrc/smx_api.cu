@@ -65,7 +65,13 @@ int check_shape(const smx_shape_t* s) {
     if (s->Hq % s->Hkv != 0) return SMX_ERR_INVALID_ARG;
     if (s->D != 128 || s->Di != 128 || s->page_tokens != 128) return SMX_ERR_UNSUPPORTED;
     if (s->Q > SMX_MAX_Q) return SMX_ERR_UNSUPPORTED;
-    if (s->kv_format != SMX_KV_MXFP4 && s->kv_format != SMX_KV_E4M3_ROWSCALE) return SMX_ERR_UNSUPPORTED;
+    if (s->kv_format != SMX_KV_MXFP4 && s->kv_format != SMX_KV_E4M3_ROWSCALE && s->kv_format != SMX_KV_NVFP4)
+        return SMX_ERR_UNSUPPORTED;
+    if (s->idx_format != SMX_KV_MXFP4 && s->idx_format != SMX_KV_NVFP4) return SMX_ERR_UNSUPPORTED;
+    auto scale_ok = [](float g) { return g > 0.0f && g <= 3.0e38f; };   // finite, positive (NaN fails)
+    if (s->kv_format == SMX_KV_NVFP4 && !(scale_ok(s->nv_scale_k) && scale_ok(s->nv_scale_v))) return SMX_ERR_INVALID_ARG;
+    if (s->idx_format == SMX_KV_NVFP4 && !scale_ok(s->nv_scale_idx)) return SMX_ERR_INVALID_ARG;
+    if (smx::nvfp4_chain(*s) && s->pages_per_block > 1) return SMX_ERR_UNSUPPORTED;
     if (s->topk > SMX_MAX_TOPK || s->max_pages_per_row > SMX_MAX_PAGES_PER_ROW) return SMX_ERR_UNSUPPORTED;
     if (s->n_pool_pages > 0x7FFFFFFF) return SMX_ERR_UNSUPPORTED;
     if (s->B > 65535 || s->num_splits > 65535 || (int64_t)s->Hkv * s->Hq * s->Q > 65535)
@@ -250,6 +256,22 @@ int smx_decode_step(const smx_shape_t* s, const float* q_f32, const uint16_t* q_
     if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
         return SMX_ERR_WORKSPACE;
     const Workspace w = layout(s, workspace);
+    if (smx::nvfp4_chain(*s)) {
+        // NVFP4 pages: the standalone kernels in the step's order (the packed q goes to the
+        // workspace's q tile region, which holds B x Q x Hq x 128 bytes)
+        const cudaStream_t st = (cudaStream_t)stream;
+        cudaError_t e = smx::launch_kv_insert(*s, k_new, v_new, kidx_new, s->Q, page_table, ctx_len, nullptr, k_pool,
+                                              v_pool, idx_pool, dev_status, false, st);
+        if (e == cudaSuccess && !rs) e = smx::launch_pack_q(q_f32, w.q_img, (int64_t)s->B * s->Q * s->Hq * 128, st);
+        if (e == cudaSuccess)
+            e = smx::launch_index_scores(*s, qidx_bf16, idx_pool, page_table, ctx_len, w.scores, dev_status, st);
+        if (e == cudaSuccess) e = smx::launch_topk(*s, w.scores, ctx_len, topk_pages, topk_count, st);
+        if (e == cudaSuccess)
+            e = smx::launch_attn_split(*s, rs ? (const void*)q_bf16 : (const void*)w.q_img, k_pool, v_pool, page_table,
+                                       ctx_len, topk_pages, topk_count, w.part_o, w.part_m, w.part_l, dev_status, st);
+        if (e == cudaSuccess) e = smx::launch_attn_merge(*s, w.part_o, w.part_m, w.part_l, out, st);
+        return cuda_status(e);
+    }
     smx::StepIO io = {};
     io.q_f32 = rs ? nullptr : q_f32;
     io.q_bf16 = rs ? q_bf16 : nullptr;
@@ -280,6 +302,18 @@ int smx_decode_step_reuse(const smx_shape_t* s, const float* q_f32, const uint16
     if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
         return SMX_ERR_WORKSPACE;
     const Workspace w = layout(s, workspace);
+    if (smx::nvfp4_chain(*s)) {
+        // NVFP4 K/V: insert (K and V rows only), pack q, the split over the given selection, merge
+        const cudaStream_t st = (cudaStream_t)stream;
+        cudaError_t e = smx::launch_kv_insert(*s, k_new, v_new, nullptr, s->Q, page_table, ctx_len, nullptr, k_pool,
+                                              v_pool, nullptr, dev_status, false, st);
+        if (e == cudaSuccess && !rs) e = smx::launch_pack_q(q_f32, w.q_img, (int64_t)s->B * s->Q * s->Hq * 128, st);
+        if (e == cudaSuccess)
+            e = smx::launch_attn_split(*s, rs ? (const void*)q_bf16 : (const void*)w.q_img, k_pool, v_pool, page_table,
+                                       ctx_len, topk_pages, topk_count, w.part_o, w.part_m, w.part_l, dev_status, st);
+        if (e == cudaSuccess) e = smx::launch_attn_merge(*s, w.part_o, w.part_m, w.part_l, out, st);
+        return cuda_status(e);
+    }
     smx::StepIO io = {};
     io.q_f32 = rs ? nullptr : q_f32;
     io.q_bf16 = rs ? q_bf16 : nullptr;
@@ -294,12 +328,14 @@ int smx_decode_step_reuse(const smx_shape_t* s, const float* q_f32, const uint16
 
 int smx_decode_step_launches(const smx_shape_t* s) {
     if (check_shape(s) != SMX_OK) return 0;
+    if (smx::nvfp4_chain(*s)) return s->kv_format == SMX_KV_E4M3_ROWSCALE ? 5 : 6;
     return 1;
 }
 
 int smx_decode_step_tensor_cores(const smx_shape_t* s) {
     const int rc = check_shape(s);
     if (rc) return rc;
+    if (smx::nvfp4_chain(*s)) return 0;
     return smx::decode_step_uses_tc(*s) ? 1 : 0;
 }
 

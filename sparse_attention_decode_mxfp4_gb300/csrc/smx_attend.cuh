@@ -39,7 +39,8 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) { return row * 256 +
 // unscaled and the row scales go to rscale[]: K's scale multiplies the scores, V's multiplies
 // the softmax weights. Token rows at or past valid_rows are zero.
 template <bool RS>
-__device__ __forceinline__ void widen_page(const uint8_t* raw, int valid_rows, uint8_t* tile, float* rscale) {
+__device__ __forceinline__ void widen_page(const uint8_t* raw, int valid_rows, uint8_t* tile, float* rscale,
+                                           bool nv = false) {
     if constexpr (RS) {
         // 128 rows x 8 chunks of 16 codes
         for (int it = threadIdx.x; it < 128 * 8; it += blockDim.x) {
@@ -64,16 +65,28 @@ __device__ __forceinline__ void widen_page(const uint8_t* raw, int valid_rows, u
             *reinterpret_cast<uint4*>(tile + swz(r, 2 * c + 1)) = o1;
         }
     } else {
-        // MXFP4: 128 rows x 4 chunks of 16 nibble bytes (32 elements = one scale group)
+        // MXFP4: 128 rows x 4 chunks of 16 nibble bytes (32 elements = one scale group). NVFP4 (nv):
+        // the chunk is blocks 2c (words 0, 1) and 2c + 1 (words 2, 3), each with an E4M3 scale; the
+        // product E2M1 x E4M3 (at most 6 significant bits) is exact in bf16, and the pool's
+        // per-tensor scale is applied by the caller (to the scores and to O)
         for (int it = threadIdx.x; it < 128 * 4; it += blockDim.x) {
             const int r = it >> 2, c = it & 3;
             uint32_t ob[16];
             if (r < valid_rows) {
                 const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 64 + c * 16);
-                const float sc = e8m0_to_f32(raw[kMxScaleOff + r * 4 + c]);
+                float sc_lo, sc_hi;
+                if (nv) {
+                    const uint32_t b2 = *reinterpret_cast<const uint16_t*>(raw + kNvScaleOff + r * 8 + 2 * c);
+                    const float2 f = f16x2_to_f32x2(e4m3x2_to_f16x2(b2));
+                    sc_lo = f.x;
+                    sc_hi = f.y;
+                } else {
+                    sc_lo = sc_hi = e8m0_to_f32(raw[kMxScaleOff + r * 4 + c]);
+                }
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
+                    const float sc = i < 2 ? sc_lo : sc_hi;
                     uint32_t h0, h1, h2, h3;
                     e2m1x8_to_f16x2(ws[i], h0, h1, h2, h3);
                     const float2 f0 = f16x2_to_f32x2(h0), f1 = f16x2_to_f32x2(h1);
@@ -314,7 +327,8 @@ __device__ __forceinline__ bool attend_pages(const AttendSmem& sm, const int* se
                                              const uint8_t* k_pool, const uint8_t* v_pool, int Hkv, int kvh,
                                              int page_bytes, int ctx, const uint32_t (&qa)[8][4], const AttendLane& L,
                                              int pos0, int pos1, uint32_t& gp, float (&o)[16][4], float& mrow0,
-                                             float& mrow1, float& l0, float& l1, int32_t* status, bool first_issued) {
+                                             float& mrow1, float& l0, float& l1, int32_t* status, bool first_issued,
+                                             float qk_scale = kLog2eOverSqrtD, bool nv = false) {
     const int lane = L.lane, t = L.t, th = L.th;
     auto issue = [&](int i) { attend_issue(sm, i, sel[i], selph[i], gp, k_pool, v_pool, Hkv, kvh, page_bytes); };
     if (threadIdx.x == 0 && !first_issued)
@@ -341,8 +355,8 @@ __device__ __forceinline__ bool attend_pages(const AttendSmem& sm, const int* se
         const int valid_rows = p >= 0 ? min(kPage, ctx - p * kPage) : 0;
         if (p >= 0) {
             const uint8_t* rk = sm.raw + st * 2 * page_bytes;
-            widen_page<RS>(rk, valid_rows, sm.Ks, sm.kscale);
-            widen_page<RS>(rk + page_bytes, valid_rows, sm.Vs, sm.vscale);
+            widen_page<RS>(rk, valid_rows, sm.Ks, sm.kscale, nv);
+            widen_page<RS>(rk + page_bytes, valid_rows, sm.Vs, sm.vscale, nv);
         }
         __syncthreads();   // tiles ready; this stage's raw bytes are consumed
         if (threadIdx.x == 0 && i + 2 < np) {
@@ -376,7 +390,7 @@ __device__ __forceinline__ bool attend_pages(const AttendSmem& sm, const int* se
                 for (int c = 0; c < 4; ++c) {
                     const int tok = tok0 + nb * 8 + 2 * t + (c & 1);
                     const int j = jpage + tok;
-                    float z = sc[nb][c] * kLog2eOverSqrtD;
+                    float z = sc[nb][c] * qk_scale;
                     if (RS) z *= sm.kscale[tok];
                     const bool ok2 = (c < 2) ? (L.v0 && j <= pos0) : (L.v1 && j <= pos1);
                     z = ok2 ? z : -INFINITY;
@@ -453,7 +467,8 @@ __device__ __forceinline__ bool attend_pages(const AttendSmem& sm, const int* se
 // part_o [B][S][Q][Hq][128], part_m / part_l [B][S][Q][Hq]. Every thread calls it (barriers).
 __device__ __forceinline__ void finish_partials(const AttendSmem& sm, const AttendLane& L, float (&o)[16][4], float mrow0,
                                                 float mrow1, float l0, float l1, float* part_o, float* part_m,
-                                                float* part_l, int b, int s, int kvh, int S, int Q, int Hq, int G) {
+                                                float* part_l, int b, int s, int kvh, int S, int Q, int Hq, int G,
+                                                float o_scale = 1.0f) {
     const int lane = L.lane, t = L.t;
     l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
     l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
@@ -493,8 +508,8 @@ __device__ __forceinline__ void finish_partials(const AttendSmem& sm, const Atte
 #pragma unroll
             for (int db = 0; db < 16; ++db) {
                 const int d = db * 8 + 2 * t;
-                if (L.v0) *reinterpret_cast<float2*>(part_o + r0 * kD + d) = make_float2(o[db][0], o[db][1]);
-                if (L.v1) *reinterpret_cast<float2*>(part_o + r1 * kD + d) = make_float2(o[db][2], o[db][3]);
+                if (L.v0) *reinterpret_cast<float2*>(part_o + r0 * kD + d) = make_float2(o[db][0] * o_scale, o[db][1] * o_scale);
+                if (L.v1) *reinterpret_cast<float2*>(part_o + r1 * kD + d) = make_float2(o[db][2] * o_scale, o[db][3] * o_scale);
             }
             if (t == 0) {
                 if (L.v0) { part_m[r0] = mrow0; part_l[r0] = l0; }

@@ -26,6 +26,9 @@ struct AttnArgs {
     int32_t* status;
     int64_t n_pool;
     int B, Q, Hq, Hkv, G, max_pages, topk, S, rows_per_cta, n_row_groups, page_bytes;
+    int nv;            // NVFP4 K/V pages
+    float qk_scale;    // log2(e) / sqrt(128), times the K pool's NVFP4 scale
+    float o_scale;     // 1, or the V pool's NVFP4 scale
 };
 
 // grid (S, B, Hkv x row groups), 2 x row_warps warps
@@ -98,8 +101,9 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1) attn_split_kernel(AttnA
     float mrow0 = -INFINITY, mrow1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
     uint32_t gp = 0;
     attend_pages<RS>(sm, sel, selph, hi - lo, a.k_pool, a.v_pool, a.Hkv, kvh, a.page_bytes, ctx, qa, L, pos0, pos1,
-                     gp, o, mrow0, mrow1, l0, l1, a.status, false);
-    finish_partials(sm, L, o, mrow0, mrow1, l0, l1, a.part_o, a.part_m, a.part_l, b, s, kvh, a.S, a.Q, a.Hq, a.G);
+                     gp, o, mrow0, mrow1, l0, l1, a.status, false, a.qk_scale, a.nv != 0);
+    finish_partials(sm, L, o, mrow0, mrow1, l0, l1, a.part_o, a.part_m, a.part_l, b, s, kvh, a.S, a.Q, a.Hq, a.G,
+                    a.o_scale);
 }
 
 // a6: one warp per (b, t, h) row
@@ -161,7 +165,11 @@ cudaError_t launch_attn_split(const smx_shape_t& s, const void* q, const uint8_t
     a.rows_per_cta = row_warps * 16;
     a.n_row_groups = (M + a.rows_per_cta - 1) / a.rows_per_cta;
     const bool rs = s.kv_format == SMX_KV_E4M3_ROWSCALE;
-    a.page_bytes = rs ? kRsPageBytes : kMxPageBytes;
+    a.page_bytes = kv_page_bytes(s);
+    a.nv = s.kv_format == SMX_KV_NVFP4;
+    // NVFP4: the pool's per-tensor scales, on the scores (folded into the softmax scale) and on O
+    a.qk_scale = a.nv ? kLog2eOverSqrtD * s.nv_scale_k : kLog2eOverSqrtD;
+    a.o_scale = a.nv ? s.nv_scale_v : 1.0f;
     const size_t smem = attend_smem_bytes(a.page_bytes) + 8 * (size_t)s.topk;
     const void* kfn = rs ? reinterpret_cast<const void*>(attn_split_kernel<true>)
                          : reinterpret_cast<const void*>(attn_split_kernel<false>);

@@ -21,6 +21,8 @@ constexpr int kMxPageBytes = SMX_MXFP4_PAGE_BYTES;   // 8704
 constexpr int kMxScaleOff = 8192;
 constexpr int kRsPageBytes = SMX_E4M3RS_PAGE_BYTES;  // 16896
 constexpr int kRsScaleOff = 16384;
+constexpr int kNvPageBytes = SMX_NVFP4_PAGE_BYTES;   // 9216: 128 x 64 B nibbles, 128 x 8 E4M3 block scales
+constexpr int kNvScaleOff = 8192;
 
 __device__ __forceinline__ void flag_status(int32_t* st, int bit) {
     if (st) atomicOr(st, bit);
@@ -185,6 +187,51 @@ __device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h) {
     __half2 v = *reinterpret_cast<__half2*>(&h);
     return __half22float2(v);
 }
+
+// One 128-element row to NVFP4 with the per-tensor decode scale g, warp-cooperative: lane l
+// holds elements 4l..4l+3 (block l / 4 of 16). Per block: s = fl32(amax / fl32(6 g)); the E4M3
+// scale byte is s rounded to nearest even, saturating at 448; S = fl32(E4M3(byte) x g); each
+// code is x / S (fp32, rounded to nearest) rounded to the nearest E2M1 value (ties to even,
+// saturating at 6, the sign of x kept). S == 0 gives codes 0; a block holding NaN or an infinity
+// gets byte 0x7F (E4M3 NaN) and codes 0. Writes 64 nibble bytes at `nib` and the 8 block scale
+// bytes at `sc` (8-byte aligned).
+__device__ __forceinline__ void quant_row_nvfp4_warp(float4 x, float g, uint8_t* nib, uint8_t* sc, int lane) {
+    const float v[4] = {x.x, x.y, x.z, x.w};
+    bool nonfinite = false;
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (!isfinite(v[i])) nonfinite = true;
+        else amax = fmaxf(amax, fabsf(v[i]));
+    }
+    const unsigned blk_mask = 0xFu << (lane & ~3);
+    const bool blk_nonfinite = (__ballot_sync(0xFFFFFFFFu, nonfinite) & blk_mask) != 0;
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    const float s = fminf(__fdiv_rn(amax, __fmul_rn(6.0f, g)), 448.0f);
+    const uint32_t sbyte = blk_nonfinite ? 0x7Fu : (e4m3x2_rn_sat(s, 0.0f) & 0xFFu);
+    const float S = __fmul_rn(f16x2_to_f32x2(e4m3x2_to_f16x2(sbyte)).x, g);
+    uint32_t codes = 0;
+    if (!blk_nonfinite && S != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 4; i += 2) {
+            const float y0 = __fdiv_rn(v[i], S), y1 = __fdiv_rn(v[i + 1], S);
+            uint32_t c = e2m1x2_rn_sat(fabsf(y0), fabsf(y1));
+            c |= ((__float_as_uint(y0) >> 28) & 0x8u) | ((__float_as_uint(y1) >> 24) & 0x80u);
+            codes |= c << (4 * i);
+        }
+    }
+    reinterpret_cast<uint16_t*>(nib)[lane] = (uint16_t)codes;
+    // lanes 0, 4, ..., 28 hold the eight block bytes; lane 0 gathers them
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        lo |= __shfl_sync(0xFFFFFFFFu, sbyte, 4 * k) << (8 * k);
+        hi |= __shfl_sync(0xFFFFFFFFu, sbyte, 16 + 4 * k) << (8 * k);
+    }
+    if (lane == 0) *reinterpret_cast<uint2*>(sc) = make_uint2(lo, hi);
+}
+
 
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
     __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));

@@ -30,6 +30,7 @@ struct IndexArgs {
     int32_t* status;
     int64_t n_pool;
     int Q, max_pages, pages_per_cta;
+    float nv_scale;   // NVFP4 index pages: the pool's per-tensor decode scale
 };
 
 constexpr int kIdxMaxPpc = 64;   // page-table entries of one CTA staged in shared memory
@@ -114,8 +115,9 @@ __global__ void __launch_bounds__(256, IdxScanShape<NQ>::kCtasPerSm)
 // pages two at a time, a warp scoring two 16-token tiles of a page, the next tile's loads in flight
 // while the current one is scored): one pass over a handful of pages finishes sooner than the
 // tensor-core pipeline fills.
-template <int NT>
+template <int NT, bool NV>
 __global__ void __launch_bounds__(kIdxWarps * 32, 2) index_score_mma_kernel(IndexArgs a) {
+    constexpr int kPageBytes = NV ? kNvPageBytes : kMxPageBytes;
     __shared__ __align__(16) uint32_t qh[16][64];  // f16x2 of q' per query, natural dim order
     __shared__ int sig[16];
     __shared__ float red[2][kIdxWarps];
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 2) index_score_mma_kernel(Inde
     TileFrag cur;
     if (n_tasks > 0) {
         const int64_t ph = task_phys(0);
-        if (ph >= 0) load_tile(cur, a.pool + ph * kMxPageBytes, tile0, g, t);
+        if (ph >= 0) load_tile<NV>(cur, a.pool + ph * kPageBytes, tile0, g, t);
     }
     uint32_t qf[NT][16];
     int sig_c[NT][2];
@@ -168,9 +170,12 @@ __global__ void __launch_bounds__(kIdxWarps * 32, 2) index_score_mma_kernel(Inde
         TileFrag nxt;
         if (q + 1 < n_tasks) {
             const int64_t phn = task_phys(q + 1);
-            if (phn >= 0) load_tile(nxt, a.pool + phn * kMxPageBytes, tile0 + ((q + 1) & 1), g, t);
+            if (phn >= 0) load_tile<NV>(nxt, a.pool + phn * kPageBytes, tile0 + ((q + 1) & 1), g, t);
         }
-        if (ph >= 0) best = fmaxf(best, score_tile<NT>(cur, qf, sig_c, p, tile0 + (q & 1), g, t, lim, a.Q));
+        if (ph >= 0) {
+            if constexpr (NV) best = fmaxf(best, score_tile_nv<NT>(cur, qf, sig_c, p, tile0 + (q & 1), g, t, lim, a.Q, a.nv_scale));
+            else best = fmaxf(best, score_tile<NT>(cur, qf, sig_c, p, tile0 + (q & 1), g, t, lim, a.Q));
+        }
         else if (p < p_end && (q & 1) == 0 && lane == 0 && (warp & 3) == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
         cur = nxt;
         if (q & 1) {   // both tiles of this iteration's page scored: combine the page's 4 warps
@@ -277,13 +282,21 @@ cudaError_t launch_index_scores(const smx_shape_t& s, const uint16_t* qidx, cons
     IndexArgs a = {};
     a.qidx = qidx; a.pool = idx_pool; a.page_table = page_table; a.ctx_len = ctx_len; a.scores = scores;
     a.status = status; a.n_pool = s.n_pool_pages; a.Q = s.Q; a.max_pages = s.max_pages_per_row;
+    a.nv_scale = s.nv_scale_idx;
     // the mma.sync scorer (two CTAs per SM) for rows cut into very few pages per CTA, else the scan
     a.pages_per_cta = index_pages_per_cta(s, 2, true);
-    const bool mma = a.pages_per_cta < kIdxScanMinPages;
+    // NVFP4 index pages: always the mma.sync scorer
+    const bool nv = s.idx_format == SMX_KV_NVFP4;
+    const bool mma = nv || a.pages_per_cta < kIdxScanMinPages;
     if (mma) {
         const dim3 grid((s.max_pages_per_row + a.pages_per_cta - 1) / a.pages_per_cta, s.B);
-        if (s.Q <= 8) index_score_mma_kernel<1><<<grid, kIdxWarps * 32, 0, st>>>(a);
-        else index_score_mma_kernel<2><<<grid, kIdxWarps * 32, 0, st>>>(a);
+        if (nv) {
+            if (s.Q <= 8) index_score_mma_kernel<1, true><<<grid, kIdxWarps * 32, 0, st>>>(a);
+            else index_score_mma_kernel<2, true><<<grid, kIdxWarps * 32, 0, st>>>(a);
+        } else {
+            if (s.Q <= 8) index_score_mma_kernel<1, false><<<grid, kIdxWarps * 32, 0, st>>>(a);
+            else index_score_mma_kernel<2, false><<<grid, kIdxWarps * 32, 0, st>>>(a);
+        }
         return cudaGetLastError();
     }
     CUtensorMap map;

@@ -5,7 +5,9 @@
 // + packed fp4 conversion); commit "MXFP4 main KV": K and V rows use the same row store;
 // commits "e4m3 q_out convention" / "pack_q_e4m3": q as saturating e4m3 at unit scale.
 // One warp quantises one 128-element row: lane l owns elements 4l..4l+3 (one float4 load,
-// coalesced 512 B per warp) and writes 2 nibble bytes; lane 0 writes the 4 scale bytes.
+// coalesced 512 B per warp) and writes 2 nibble bytes; lane 0 writes the 4 scale bytes (MXFP4)
+// or the 8 block scale bytes (NVFP4, the format the pages name: E2M1 with an E4M3 scale per 16
+// elements and the pool's per-tensor fp32 scale).
 #include "smx_device.cuh"
 #include "smx_internal.h"
 
@@ -24,7 +26,8 @@ struct InsertArgs {
     int32_t* status;
     int64_t T;             // token stride of the dense inputs
     int64_t n_pool;
-    int B, Q, Hkv, max_pages, kv_format;
+    int B, Q, Hkv, max_pages, kv_format, idx_format;
+    float nv_k, nv_v, nv_idx;  // NVFP4 per-tensor decode scales
     int prefill;
 };
 
@@ -32,13 +35,21 @@ __device__ __forceinline__ void store_row(const InsertArgs& a, int kind, int64_t
                                           const float* src, int lane) {
     const float4 x = reinterpret_cast<const float4*>(src)[lane];
     if (kind == 0) {
-        uint8_t* page = a.idx_pool + phys * kMxPageBytes;
-        quant_row_mxfp4_warp(x, page + slot * 64, page + kMxScaleOff + slot * 4, lane);
+        if (a.idx_format == SMX_KV_NVFP4) {
+            uint8_t* page = a.idx_pool + phys * kNvPageBytes;
+            quant_row_nvfp4_warp(x, a.nv_idx, page + slot * 64, page + kNvScaleOff + slot * 8, lane);
+        } else {
+            uint8_t* page = a.idx_pool + phys * kMxPageBytes;
+            quant_row_mxfp4_warp(x, page + slot * 64, page + kMxScaleOff + slot * 4, lane);
+        }
         return;
     }
     const int h = (kind - 1) % a.Hkv;
     uint8_t* pool = (kind <= a.Hkv) ? a.k_pool : a.v_pool;
-    if (a.kv_format == SMX_KV_E4M3_ROWSCALE) {
+    if (a.kv_format == SMX_KV_NVFP4) {
+        uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kNvPageBytes;
+        quant_row_nvfp4_warp(x, kind <= a.Hkv ? a.nv_k : a.nv_v, page + slot * 64, page + kNvScaleOff + slot * 8, lane);
+    } else if (a.kv_format == SMX_KV_E4M3_ROWSCALE) {
         uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kRsPageBytes;
         quant_row_e4m3rs_warp(x, page + slot * 128, reinterpret_cast<float*>(page + kRsScaleOff) + slot, lane);
     } else {
@@ -47,7 +58,8 @@ __device__ __forceinline__ void store_row(const InsertArgs& a, int kind, int64_t
     }
 }
 
-// One warp per (row b, token, kind) with kind 0 = index-K, 1..Hkv = K heads, Hkv+1..2Hkv = V.
+// One warp per (row b, token, kind) with kind 0 = index-K (skipped without an index input),
+// 1..Hkv = K heads, Hkv+1..2Hkv = V.
 __global__ void __launch_bounds__(256) kv_insert_kernel(InsertArgs a) {
     const int lane = threadIdx.x & 31;
     const int kinds = 1 + 2 * a.Hkv;
@@ -56,6 +68,7 @@ __global__ void __launch_bounds__(256) kv_insert_kernel(InsertArgs a) {
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
     for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total; w += nwarps) {
         const int kind = (int)(w % kinds);
+        if (kind == 0 && a.kidx == nullptr) continue;
         const int64_t tok = w / kinds;
         const int b = (int)(tok / per_row);
         const int64_t i = tok % per_row;
@@ -72,7 +85,7 @@ __global__ void __launch_bounds__(256) kv_insert_kernel(InsertArgs a) {
         } else {
             const int ctx = a.ctx_len[b];
             if (ctx < a.Q || ctx > a.max_pages * kPage) {
-                if (lane == 0 && kind == 0) flag_status(a.status, SMX_DEV_BAD_CTX);
+                if (lane == 0 && kind == 1) flag_status(a.status, SMX_DEV_BAD_CTX);
                 continue;
             }
             pos = (int64_t)ctx - a.Q + i;
@@ -80,7 +93,7 @@ __global__ void __launch_bounds__(256) kv_insert_kernel(InsertArgs a) {
         }
         const int64_t phys = a.page_table[(int64_t)b * a.max_pages + pos / kPage];
         if (phys < 0 || phys >= a.n_pool) {
-            if (lane == 0 && kind == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+            if (lane == 0 && kind == 1) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
             continue;
         }
         const int slot = (int)(pos % kPage);
@@ -113,7 +126,8 @@ cudaError_t launch_kv_insert(const smx_shape_t& s, const float* k, const float* 
     a.k = k; a.v = v; a.kidx = kidx; a.page_table = page_table; a.ctx_len = ctx_len; a.n_fill = n_fill;
     a.k_pool = k_pool; a.v_pool = v_pool; a.idx_pool = idx_pool; a.status = status;
     a.T = T; a.n_pool = s.n_pool_pages; a.B = s.B; a.Q = s.Q; a.Hkv = s.Hkv;
-    a.max_pages = s.max_pages_per_row; a.kv_format = s.kv_format; a.prefill = prefill ? 1 : 0;
+    a.max_pages = s.max_pages_per_row; a.kv_format = s.kv_format; a.idx_format = s.idx_format;
+    a.nv_k = s.nv_scale_k; a.nv_v = s.nv_scale_v; a.nv_idx = s.nv_scale_idx; a.prefill = prefill ? 1 : 0;
     const int64_t rows = (int64_t)s.B * (prefill ? T : s.Q) * (1 + 2 * s.Hkv);
     int64_t blocks = (rows + 7) / 8;
     if (blocks > 152 * 32) blocks = 152 * 32;

@@ -43,6 +43,17 @@ cudaError_t launch_attn_merge(const smx_shape_t& s, const float* part_o, const f
 // Partition count that fills one wave of the device's SMs with split CTAs (0 on a CUDA error).
 int suggest_num_splits(const smx_shape_t& s);
 
+// Steps with an NVFP4 pool run the standalone kernels in sequence instead of the fused kernel.
+inline bool nvfp4_chain(const smx_shape_t& s) { return s.kv_format == SMX_KV_NVFP4 || s.idx_format == SMX_KV_NVFP4; }
+// Bytes of one K or V page of one KV head, and of one index page.
+inline int kv_page_bytes(const smx_shape_t& s) {
+    return s.kv_format == SMX_KV_E4M3_ROWSCALE ? SMX_E4M3RS_PAGE_BYTES
+         : s.kv_format == SMX_KV_NVFP4 ? SMX_NVFP4_PAGE_BYTES : SMX_MXFP4_PAGE_BYTES;
+}
+inline int idx_page_bytes(const smx_shape_t& s) {
+    return s.idx_format == SMX_KV_NVFP4 ? SMX_NVFP4_PAGE_BYTES : SMX_MXFP4_PAGE_BYTES;
+}
+
 // ---- the fused decode step (one cooperative kernel, smx_step.cu) ----
 struct StepGeom {
     int row_warps;        // warps per token half of the attention (16 query rows each)

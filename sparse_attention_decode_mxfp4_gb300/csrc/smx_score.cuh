@@ -27,17 +27,82 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h16) { return __uint_
 
 // One lane's share of one 16-token tile: 16 B of nibbles of token rows g and g+8 and the rows'
 // scale words. Pages are read through L2 (a CTA that inserted rows must see its own writes).
+// NVFP4 pages (NV): the lane's 32 elements are blocks 2t and 2t + 1, whose two E4M3 scale bytes
+// are the low (t even) or high (t odd) half of the row's scale word 4 (t / 2).
 struct TileFrag {
     uint4 c0, c1;
     uint32_t sw0, sw1;
 };
 
+template <bool NV = false>
 __device__ __forceinline__ void load_tile(TileFrag& f, const uint8_t* page, int tile, int g, int t) {
     const int r0 = tile * 16 + g, r1 = r0 + 8;
     f.c0 = ldg_cg_v4(page + r0 * 64 + 16 * t);
     f.c1 = ldg_cg_v4(page + r1 * 64 + 16 * t);
-    f.sw0 = ldg_cg_u32(page + kMxScaleOff + 4 * r0);
-    f.sw1 = ldg_cg_u32(page + kMxScaleOff + 4 * r1);
+    if constexpr (NV) {
+        const int sh = 16 * (t & 1);
+        f.sw0 = (ldg_cg_u32(page + kNvScaleOff + 8 * r0 + 4 * (t >> 1)) >> sh) & 0xFFFFu;
+        f.sw1 = (ldg_cg_u32(page + kNvScaleOff + 8 * r1 + 4 * (t >> 1)) >> sh) & 0xFFFFu;
+    } else {
+        f.sw0 = ldg_cg_u32(page + kMxScaleOff + 4 * r0);
+        f.sw1 = ldg_cg_u32(page + kMxScaleOff + 4 * r1);
+    }
+}
+
+// NVFP4: the max over this lane's scores of one tile. Each E2M1 pair is widened to f16x2 and
+// multiplied by its block's E4M3 scale (as f16; the product, at most 6 significant bits between
+// 2^-10 and 2688, is exact), so one fp32 accumulator per row serves the whole row; the query's
+// power-of-two factor and the per-tensor scale g are applied to the fp32 result. A NaN scale
+// makes the token's score NaN, which the maximum leaves out.
+template <int NT>
+__device__ __forceinline__ float score_tile_nv(const TileFrag& f, const uint32_t (&qf)[NT][16], const int (&sig_c)[NT][2],
+                                               int p, int tile, int g, int t, int lim, int Q, float g_idx) {
+    const int r0 = tile * 16 + g, r1 = r0 + 8;
+    // f16x2 splats of the scales of blocks 2t (words 0, 1) and 2t + 1 (words 2, 3), rows r0, r1
+    uint32_t fa[2], fb[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const uint32_t b0 = (f.sw0 >> (8 * k)) & 0xFFu, b1 = (f.sw1 >> (8 * k)) & 0xFFu;
+        fa[k] = e4m3x2_to_f16x2(b0 | (b0 << 8));
+        fb[k] = e4m3x2_to_f16x2(b1 | (b1 << 8));
+    }
+    float acc[NT][2][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) acc[nt][h][0] = acc[nt][h][1] = acc[nt][h][2] = acc[nt][h][3] = 0.0f;
+    const uint32_t w0[4] = {f.c0.x, f.c0.y, f.c0.z, f.c0.w};
+    const uint32_t w1[4] = {f.c1.x, f.c1.y, f.c1.z, f.c1.w};
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+        uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+        e2m1x8_to_f16x2(w0[wi], x0, x1, x2, x3);
+        e2m1x8_to_f16x2(w1[wi], y0, y1, y2, y3);
+        const uint32_t s0 = fa[wi >> 1], s1 = fb[wi >> 1];
+        x0 = hmul2_u32(x0, s0); x1 = hmul2_u32(x1, s0); x2 = hmul2_u32(x2, s0); x3 = hmul2_u32(x3, s0);
+        y0 = hmul2_u32(y0, s1); y1 = hmul2_u32(y1, s1); y2 = hmul2_u32(y2, s1); y3 = hmul2_u32(y3, s1);
+        const int k0 = 2 * wi, k1 = 2 * wi + 1;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            mma_f16_16816(acc[nt][0], x0, y0, x1, y1, qf[nt][2 * k0], qf[nt][2 * k0 + 1]);
+            mma_f16_16816(acc[nt][1], x2, y2, x3, y3, qf[nt][2 * k1], qf[nt][2 * k1 + 1]);
+        }
+    }
+    const int j0 = p * kPage + r0, j1 = p * kPage + r1;
+    float best = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int col = c & 1;
+            const int n = nt * 8 + 2 * t + col;
+            const int j = (c < 2) ? j0 : j1;
+            const bool valid = (n < Q) && (j <= lim + n);
+            const float v = __fmul_rn(mul_exp2(acc[nt][0][c] + acc[nt][1][c], -sig_c[nt][col]), g_idx);
+            best = valid ? fmaxf(best, v) : best;
+        }
+    }
+    return best;
 }
 
 // Max over this lane's scores of one tile (two token rows x its query columns).

@@ -21,9 +21,10 @@ LIB_PATH = os.path.join(_HERE, "_build", "libsmx.so")
 
 KV_MXFP4 = 0
 KV_E4M3_ROWSCALE = 1
-KV_NVFP4 = 2   # refused by the library (SMX_ERR_UNSUPPORTED)
+KV_NVFP4 = 2   # E2M1 + an E4M3 scale per 16 elements + the pool's fp32 scale (K/V and index pools)
 MXFP4_PAGE_BYTES = 8704
 E4M3RS_PAGE_BYTES = 16896
+NVFP4_PAGE_BYTES = 9216
 DEV_BAD_PAGE_ID, DEV_BAD_CTX, DEV_BAD_TOPK, DEV_TIMEOUT = 1, 2, 4, 8
 SMX_ERR_WORKSPACE = -4
 
@@ -45,7 +46,9 @@ class _CShape(ctypes.Structure):
                 ("page_tokens", ctypes.c_int32), ("max_pages_per_row", ctypes.c_int32),
                 ("n_pool_pages", ctypes.c_int64), ("topk", ctypes.c_int32),
                 ("num_splits", ctypes.c_int32), ("kv_format", ctypes.c_int32),
-                ("pages_per_block", ctypes.c_int32)]
+                ("pages_per_block", ctypes.c_int32), ("idx_format", ctypes.c_int32),
+                ("nv_scale_k", ctypes.c_float), ("nv_scale_v", ctypes.c_float),
+                ("nv_scale_idx", ctypes.c_float)]
 
 
 @dataclass
@@ -63,22 +66,33 @@ class Shape:
     Di: int = 128
     page_tokens: int = 128
     pages_per_block: int = 1
+    idx_format: int = KV_MXFP4
+    nv_scale_k: float = 0.0    # NVFP4 per-tensor decode scales (> 0 where that pool is NVFP4)
+    nv_scale_v: float = 0.0
+    nv_scale_idx: float = 0.0
 
     @classmethod
     def of(cls, w, num_splits=None) -> "Shape":
         """Shape of a workload object (B, Q, Hq, Hkv, max_pages, n_pool_pages, topk, ...)."""
         return cls(w.B, w.Q, w.Hq, w.Hkv, w.max_pages, w.n_pool_pages, w.topk,
                    w.num_splits if num_splits is None else num_splits, w.kv_format,
-                   pages_per_block=getattr(w, "pages_per_block", 1))
+                   pages_per_block=getattr(w, "pages_per_block", 1),
+                   idx_format=getattr(w, "idx_format", KV_MXFP4), nv_scale_k=getattr(w, "nv_scale_k", 0.0),
+                   nv_scale_v=getattr(w, "nv_scale_v", 0.0), nv_scale_idx=getattr(w, "nv_scale_idx", 0.0))
 
     def c(self) -> _CShape:
         return _CShape(self.B, self.Q, self.Hq, self.Hkv, self.D, self.Di, self.page_tokens,
                        self.max_pages_per_row, self.n_pool_pages, self.topk, self.num_splits,
-                       self.kv_format, self.pages_per_block)
+                       self.kv_format, self.pages_per_block, self.idx_format, self.nv_scale_k,
+                       self.nv_scale_v, self.nv_scale_idx)
 
     @property
     def kv_page_bytes(self) -> int:
-        return E4M3RS_PAGE_BYTES if self.kv_format == KV_E4M3_ROWSCALE else MXFP4_PAGE_BYTES
+        return {KV_E4M3_ROWSCALE: E4M3RS_PAGE_BYTES, KV_NVFP4: NVFP4_PAGE_BYTES}.get(self.kv_format, MXFP4_PAGE_BYTES)
+
+    @property
+    def idx_page_bytes(self) -> int:
+        return NVFP4_PAGE_BYTES if self.idx_format == KV_NVFP4 else MXFP4_PAGE_BYTES
 
 
 _lib = None
@@ -201,7 +215,7 @@ def kv_insert(shape, k_new, v_new, kidx_new, page_table, ctx_len, k_pool, v_pool
     B, Q = shape.B, shape.Q
     _need("smx_kv_insert_mxfp4", **_step_bufs(shape, None, None, k_new, v_new, page_table, ctx_len, k_pool, v_pool,
                                         dev_status),
-          kidx_new=(kidx_new, B * Q * 128 * 4), idx_pool=(idx_pool, shape.n_pool_pages * MXFP4_PAGE_BYTES))
+          kidx_new=(kidx_new, B * Q * 128 * 4), idx_pool=(idx_pool, shape.n_pool_pages * shape.idx_page_bytes))
     cs = shape.c()
     _check(lib().smx_kv_insert_mxfp4(ctypes.byref(cs), _p(k_new), _p(v_new), _p(kidx_new), _p(page_table),
                                      _p(ctx_len), _p(k_pool), _p(v_pool), _p(idx_pool), _p(dev_status),
@@ -214,7 +228,7 @@ def kv_prefill(shape, k, v, kidx, page_table, n_fill, k_pool, v_pool, idx_pool, 
     B, Hkv = shape.B, shape.Hkv
     _need("smx_kv_prefill", k=(k, B * T * Hkv * 128 * 4), v=(v, B * T * Hkv * 128 * 4), kidx=(kidx, B * T * 128 * 4),
           **_step_bufs(shape, None, None, None, None, page_table, None, k_pool, v_pool, dev_status),
-          n_fill=(n_fill, B * 4), idx_pool=(idx_pool, shape.n_pool_pages * MXFP4_PAGE_BYTES))
+          n_fill=(n_fill, B * 4), idx_pool=(idx_pool, shape.n_pool_pages * shape.idx_page_bytes))
     cs = shape.c()
     _check(lib().smx_kv_prefill(ctypes.byref(cs), _p(k), _p(v), _p(kidx), T, _p(page_table),
                                 _p(n_fill), _p(k_pool), _p(v_pool), _p(idx_pool), _p(dev_status),
@@ -231,7 +245,7 @@ def pack_q_e4m3(q, out=None, stream=None):
 
 def _index_bufs(shape, qidx_bf16, idx_pool, page_table, ctx_len, page_scores, dev_status):
     B = shape.B
-    return dict(qidx_bf16=(qidx_bf16, B * shape.Q * 128 * 2), idx_pool=(idx_pool, shape.n_pool_pages * MXFP4_PAGE_BYTES),
+    return dict(qidx_bf16=(qidx_bf16, B * shape.Q * 128 * 2), idx_pool=(idx_pool, shape.n_pool_pages * shape.idx_page_bytes),
                 page_table=(page_table, B * shape.max_pages_per_row * 4), ctx_len=(ctx_len, B * 4),
                 page_scores=(page_scores, B * shape.max_pages_per_row * 4), dev_status=(dev_status, 4))
 
@@ -319,7 +333,7 @@ def _full_step_bufs(shape, q_f32, q_bf16, qidx_bf16, k_new, v_new, kidx_new, pag
     B, Q = shape.B, shape.Q
     return dict(**_step_bufs(shape, q_f32, q_bf16, k_new, v_new, page_table, ctx_len, k_pool, v_pool, dev_status),
                 qidx_bf16=(qidx_bf16, B * Q * 128 * 2), kidx_new=(kidx_new, B * Q * 128 * 4),
-                idx_pool=(idx_pool, shape.n_pool_pages * MXFP4_PAGE_BYTES),
+                idx_pool=(idx_pool, shape.n_pool_pages * shape.idx_page_bytes),
                 topk_pages=(topk_pages, B * shape.topk * 4), topk_count=(topk_count, B * 4),
                 out=(out, B * Q * shape.Hq * 128 * 4))
 

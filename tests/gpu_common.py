@@ -34,7 +34,7 @@ def gpu_step(w, data, pools, num_splits=None, noalloc=False, workspace=None):
     shape = ops.Shape.of(w, num_splits)
     g = gpu_inputs(w, data, pools)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    kw = dict(q_f32=g["q_f32"] if w.kv_format == wl.KV_MXFP4 else None,
+    kw = dict(q_f32=g["q_f32"] if w.kv_format != wl.KV_E4M3_ROWSCALE else None,
               q_bf16=g["q_bf16"] if w.kv_format == wl.KV_E4M3_ROWSCALE else None,
               qidx_bf16=g["qidx_bf16"], k_new=g["k_new"], v_new=g["v_new"], kidx_new=g["kidx_new"],
               page_table=g["page_table"], ctx_len=g["ctx_len"], k_pool=g["k_pool"], v_pool=g["v_pool"],
@@ -58,7 +58,7 @@ def gpu_step_reuse(w, data, pools, topk_pages, topk_count, num_splits=None):
     g = gpu_inputs(w, data, pools)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = ops.decode_step_reuse(
-        shape, q_f32=g["q_f32"] if w.kv_format == wl.KV_MXFP4 else None,
+        shape, q_f32=g["q_f32"] if w.kv_format != wl.KV_E4M3_ROWSCALE else None,
         q_bf16=g["q_bf16"] if w.kv_format == wl.KV_E4M3_ROWSCALE else None,
         k_new=g["k_new"], v_new=g["v_new"], page_table=g["page_table"], ctx_len=g["ctx_len"],
         k_pool=g["k_pool"], v_pool=g["v_pool"], topk_pages=dev_t(np.asarray(topk_pages, np.int32)),

@@ -47,7 +47,13 @@ def good_shape(**kw):
     (dict(topk=0), -1), (dict(num_splits=0), -1), (dict(n_pool_pages=0), -1),
     (dict(max_pages_per_row=0), -1),
     (dict(D=64), -2), (dict(Di=256), -2), (dict(page_tokens=64), -2), (dict(Q=17), -2),
-    (dict(kv_format=7), -2), (dict(kv_format=2), -2),   # 2 = SMX_KV_NVFP4, refused as on the pages
+    (dict(kv_format=7), -2), (dict(idx_format=1), -2), (dict(idx_format=3), -2),
+    # NVFP4 pools need a finite positive per-tensor scale, and one page per selected block
+    (dict(kv_format=2), -1), (dict(kv_format=2, nv_scale_k=0.5), -1),
+    (dict(kv_format=2, nv_scale_k=0.5, nv_scale_v=float("nan")), -1),
+    (dict(kv_format=2, nv_scale_k=0.5, nv_scale_v=float("inf")), -1), (dict(idx_format=2), -1),
+    (dict(idx_format=2, nv_scale_idx=-1.0), -1),
+    (dict(kv_format=2, nv_scale_k=0.5, nv_scale_v=0.5, pages_per_block=2), -2),
     (dict(topk=5000), -2), (dict(pages_per_block=3), -2),
     (dict(pages_per_block=4, topk=2000), -2),
 ])
@@ -62,6 +68,21 @@ def test_bad_shapes_are_refused(L, kw, code):
     assert rc == code
     rc = L.smx_decode_step_reuse(ctypes.byref(cs), *([fake] * 12), 1 << 30, None, None)
     assert rc == code
+
+
+@pytest.mark.parametrize("kw,launches", [
+    (dict(kv_format=2, nv_scale_k=0.5, nv_scale_v=0.25), 6),
+    (dict(idx_format=2, nv_scale_idx=0.125), 6),
+    (dict(kv_format=2, idx_format=2, nv_scale_k=0.5, nv_scale_v=0.25, nv_scale_idx=0.125), 6),
+    (dict(kv_format=1, idx_format=2, nv_scale_idx=0.125), 5),
+    (dict(), 1),
+])
+def test_nvfp4_shapes_are_taken(L, kw, launches):
+    # a step with an NVFP4 pool runs the standalone kernels in sequence (no q packing with FP8-KV)
+    cs = good_shape(**kw).c()
+    assert L.smx_workspace_bytes(ctypes.byref(cs)) > 0
+    assert L.smx_decode_step_launches(ctypes.byref(cs)) == launches
+    assert L.smx_decode_step_tensor_cores(ctypes.byref(cs)) == (0 if launches > 1 else L.smx_decode_step_tensor_cores(ctypes.byref(cs)))
 
 
 def test_null_and_misaligned_pointers_are_refused(L):
