@@ -60,6 +60,9 @@ def parse():
     ap.add_argument("--reuse", action="store_true",
                     help="time the step of a layer that reuses one full step's selection (K/V insert, "
                          "split and merge; no index scoring or selection); bytes = the selected K/V pages")
+    ap.add_argument("--stage", default="step", choices=["step", "index"],
+                    help="index: time the index scorer alone (smx_index_score over the workload's index "
+                         "pages, rotating copies of the index pool); bytes = the index pages read")
     return ap.parse_args()
 
 
@@ -87,15 +90,16 @@ def peaks():
 
 def kernel_sources_sha():
     h = hashlib.sha256()
-    for f in ("smx_step.cu", "smx_attend.cuh", "smx_attend_tc.cuh", "smx_tc.cuh", "smx_scan.cuh", "smx_score_tc.cuh",
+    for f in ("smx_step.cu", "smx_attend.cuh", "smx_attend_tc.cuh", "smx_tc.cuh", "smx_scan.cuh",
               "smx_select.cuh", "smx_device.cuh"):
         h.update(open(os.path.join(ROOT, "sparse_attention_decode_mxfp4_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload_name, reuse=False):
-    """DRAM bytes per launch of the decode-step kernel (reuse: its reusing-layer variant) from a
-    committed ncu summary, if it was taken on the current kernel source and this workload; else None."""
+    """DRAM bytes per launch of the decode-step kernel (reuse: its reusing-layer variant) on this
+    workload from a committed ncu summary (one record per workload), if it was taken on the current
+    kernel source; else None."""
     p = os.path.join(ROOT, "profiles", "decode_step_reuse_traffic.json" if reuse else "decode_step_traffic.json")
     if not os.path.exists(p):
         return None
@@ -103,9 +107,12 @@ def recorded_traffic(workload_name, reuse=False):
         d = json.load(open(p))
     except Exception:
         return None
-    if d.get("kernel_sources_sha") != kernel_sources_sha() or d.get("workload") != workload_name:
+    if d.get("kernel_sources_sha") != kernel_sources_sha():
         return None
-    return d.get("dram_bytes_per_launch")
+    for r in d.get("records", [d]):
+        if r.get("workload") == workload_name:
+            return r.get("dram_bytes_per_launch")
+    return None
 
 
 def slowest_rank(x, device):
@@ -312,7 +319,7 @@ class Prepared:
         self.R = R = max(2, math.ceil(3 * self.l2 / self.step_bytes))
         self.copies = [tuple(p.clone() for p in base) for _ in range(R)]
         del base
-        self.inp = dict(q_f32=T(data["q"]) if w.kv_format == wl.KV_MXFP4 else None,
+        self.inp = dict(q_f32=T(data["q"]) if w.kv_format != wl.KV_E4M3_ROWSCALE else None,
                         q_bf16=T(data["q_bf16"].view(np.int16)) if w.kv_format == wl.KV_E4M3_ROWSCALE else None,
                         qidx_bf16=T(data["qidx_bf16"].view(np.int16)), k_new=T(data["k_new"]),
                         v_new=T(data["v_new"]), kidx_new=T(data["kidx_new"]))
@@ -389,6 +396,63 @@ def time_steps(prep, steps, warmup, world, dev, clocks=None):
     return ms, clk
 
 
+def run_index_stage(args, world, dev, peak, peak_kind):
+    """The index scorer (a3) alone on one workload: every index page of every row scored once per
+    call, over rotating copies of the index pool (more than 3x L2 read per rotation), replayed from
+    a CUDA graph and timed with CUDA events."""
+    from sparse_attention_decode_mxfp4_gb300 import ops
+    w = wl.config(args.config)
+    shape = ops.Shape.of(w, 1)
+    data = wl.generate(w)
+    idx_b, _ = algorithmic_bytes(w, data["ctx_len"])
+
+    def T(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    base = tuple(torch.zeros(p.shape, dtype=torch.uint8, device=dev) for p in wl.empty_pools(w))
+    pt, cl = T(data["page_table"]), T(data["ctx_len"])
+    ops.kv_prefill(shape, T(data["k"]), T(data["v"]), T(data["kidx"]), pt, T(data["n_hist"]), *base)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    R = max(2, math.ceil(3 * l2 / idx_b))
+    pools = [base[2].clone() for _ in range(R)]
+    del base
+    qidx = T(data["qidx_bf16"].view(np.int16))
+    scores = torch.empty((w.B, w.max_pages), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    steps, warm = args.steps, max(3, args.warmup)
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    g_warm, g = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g_warm, stream=s):
+            for i in range(warm):
+                ops.index_score(shape, qidx, pools[i % R], pt, cl, page_scores=scores, dev_status=status)
+        with torch.cuda.graph(g, stream=s):
+            for i in range(steps):
+                ops.index_score(shape, qidx, pools[i % R], pt, cl, page_scores=scores, dev_status=status)
+    torch.cuda.synchronize()
+    g_warm.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1)
+    assert status.item() == 0, f"device status {status.item()}"
+    us = ms * 1e3 / steps
+    gbs = idx_b / (us * 1e-6) / 1e9
+    print(json.dumps({
+        "metric": "index scorer (a3) alone: us per call and achieved HBM GB/s vs GB300 peak", "value": gbs,
+        "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": warm, "us_per_call": us, "higher_is_better": True,
+        "dtype": "f32", "data": "synthetic (seeded N(0,1) index-K rows quantised on the GPU)",
+        "config": {"workload": w.name, "B": w.B, "Q": w.Q, "max_ctx": w.max_ctx, "index_bytes": idx_b,
+                   "pages": int(idx_b // wl.MXFP4_PAGE_BYTES),
+                   "l2": f"rotating {R} index pool copies ({R * idx_b / 1e6:.0f} MB read per rotation)"},
+        "roofline": {"bound": "hbm", "kernel": "index_scan_kernel / index_score_mma_kernel", "achieved": gbs,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": gbs / peak}}))
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -408,6 +472,10 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     smx_build.build()
     peak, peak_kind = peaks()
+    if args.stage == "index":
+        if rank == 0:
+            run_index_stage(args, world, dev, peak, peak_kind)
+        return
 
     # ---- the other workloads first (their memory is freed before the headline one) ----
     per_config = {}

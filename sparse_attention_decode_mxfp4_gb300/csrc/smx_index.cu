@@ -16,7 +16,6 @@
 #include "smx_internal.h"
 #include "smx_score.cuh"
 #include "smx_scan.cuh"
-#include "smx_score_tc.cuh"
 #include "smx_select.cuh"
 
 namespace smx {

@@ -21,15 +21,17 @@
 //  * The epilogue (thread = token) weighs group g's accumulator by 2^(e_g - 127 - sigma_g), adds
 //    the two query pieces, masks by the causal rule and takes the max over queries, then over the
 //    page's tokens. A NaN group scale (0xFF) makes the token's score NaN, which the max leaves out.
-// The queries come from sc_setup_query: each bf16 element times 2^sigma_g (the group's largest
-// magnitude in (224, 448]) split exactly into two e4m3 pieces (rows n and NQ + n). The products
-// are exact; only the MMA's and the epilogue's fp32 additions round.
+// The queries (scan_setup_query): each bf16 element times 2^sigma_g (the group's largest
+// magnitude in (224, 448]) split exactly into two e4m3 pieces (rows n and NQ + n): exact for every
+// element within 2^9.8 of its group's maximum (e4m3 keeps 4 significant bits per piece), a
+// smaller one off by at most half the e4m3 subnormal step, 2^-17.8 of the group maximum. The
+// products are exact; only the MMA's and the epilogue's fp32 additions round.
 // Roles (8 warps): lane 0 of warps 0 and 3 issue the copies of the even and the odd pages (one
 // thread issues at most one copy per ~600 cycles: two issuers reach the copy engines' rate);
 // warps 1 and 2 take the MMAs of the even and the odd pages (the scale copy by the whole warp, the
 // MMA issue by lane 0, which an issue holds about a hundred cycles); warps 4-7 first run the
-// caller's work (the fused step writes the new rows there: they would idle until the first
-// accumulator anyway), then take the epilogue (warp 4 + q reaches tensor-memory lanes 32 q ..), two
+// query set-up and the caller's work (the fused step writes the new rows there: they would idle
+// until the first accumulator anyway), then take the epilogue (warp 4 + q reaches tensor-memory lanes 32 q ..), two
 // pages an iteration. Nothing waits on the epilogue but the reuse of an accumulator stage, so the
 // copies and the MMAs run as the data lands. Every wait is bounded; once one gives up the CTA's
 // later waits return at once and SMX_DEV_TIMEOUT is set.
@@ -38,10 +40,19 @@
 #include <cuda.h>
 
 #include "smx_device.cuh"
-#include "smx_score_tc.cuh"
 #include "smx_tc.cuh"
 
 namespace smx {
+
+constexpr int kScQueryBytes = 32 * 128;   // the query pieces: up to 32 rows (two pieces x 16 query slots)
+
+// Byte offset of 16-byte chunk c of row r of a K-major tile with the 128-byte swizzle (8-row atoms
+// of 1024 bytes).
+__host__ __device__ __forceinline__ uint32_t sc_chunk(int r, int c) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + (((c ^ r) & 7) << 4));
+}
+
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t w16) { return f16x2_to_f32x2(e4m3x2_to_f16x2(w16)); }
 
 constexpr int kScanRows = 136;                    // one page as rows of 64 bytes
 constexpr int kScanTileBytes = kScanRows * 128;   // unpacked: 128 bytes a row (17 x 1 KB)
@@ -60,7 +71,7 @@ __host__ __device__ constexpr int scan_smem_bytes(int stages, int sa) {
 
 struct ScanPipe {
     uint8_t* tiles;       // [ST][kScanTileBytes], 1024-byte aligned
-    uint8_t* qt;          // the query pieces (sc_setup_query), 1024-byte aligned
+    uint8_t* qt;          // the query pieces (scan_setup_query), 1024-byte aligned
     uint8_t* ring;        // [SA][kScanScaleBytes]: the scale words of the page in accumulator stage a
     uint64_t* full;       // [ST] page copy landed (1 arrival + transaction bytes)
     uint64_t* empty;      // [ST] stage free: the page's MMAs are done (commit)
@@ -236,7 +247,7 @@ __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
 // block barrier after the call before the next one (or before reusing the query pieces);
 // scan_finish then retires the last stages.
 // The query pieces of one row (bf16 bits [Q][128], Q <= NQ) built by the 128 threads of warps 4-7
-// while the first pages are in flight: the same arithmetic as sc_setup_query (per 32-dim group g a
+// while the first pages are in flight (per 32-dim group g a
 // power-of-two scale 2^sig[g] that brings the group's largest |q| into (224, 448] where it fits;
 // each scaled value as an e4m3 high piece plus an e4m3 low piece of the remainder), item
 // it = t, t + 128 being query slot it / 16 and 8-dim slice it % 16. Writes the pieces to qt, makes
