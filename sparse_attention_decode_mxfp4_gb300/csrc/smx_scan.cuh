@@ -102,6 +102,22 @@ __device__ __forceinline__ void scan_bind(ScanPipe& sp, uint64_t* bars) {
     sp.qready = sp.ins + 1;
 }
 
+// One warp: the barriers, one per lane (before the first use, behind a block barrier).
+template <int ST, int SA>
+__device__ __forceinline__ void scan_init_warp(ScanPipe& sp, uint32_t insert_arrivals, int lane) {
+    constexpr int kN = 2 * ST + 2 * SA + 2;
+    for (int j = lane; j < kN; j += 32) {
+        if (j < ST) mbar_init(&sp.full[j], 1);
+        else if (j < 2 * ST) mbar_init(&sp.empty[j - ST], 1);
+        else if (j < 2 * ST + SA) mbar_init(&sp.afull[j - 2 * ST], 2);
+        else if (j < 2 * ST + 2 * SA) mbar_init(&sp.aempty[j - 2 * ST - SA], 4);
+        else if (j == 2 * ST + 2 * SA) mbar_init(sp.ins, insert_arrivals);
+        else mbar_init(sp.qready, 4);
+    }
+    if (lane == 0) *sp.gave_up = 0;
+    mbar_fence_init();
+}
+
 // One thread: the barriers (before the first use, behind a block barrier).
 template <int ST, int SA>
 __device__ __forceinline__ void scan_init(ScanPipe& sp, uint32_t insert_arrivals) {

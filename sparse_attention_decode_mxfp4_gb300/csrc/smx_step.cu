@@ -192,19 +192,20 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
         sp.seq = 0;
         sp.ins_seq = 0;
     }
-    if (threadIdx.x == 0) {
-        mbar_init(&mbar[0], 1);
-        mbar_init(&mbar[1], 1);
-        mbar_init(&mbar[2], 1);
-        mbar_init(&mbar[3], 1);
-        mbar_init(&mbar_q, 1);
-        mbar_init(&mbar_mma[0], 1);
-        mbar_init(&mbar_mma[1], 1);
-        if constexpr (kScan) scan_init<kStepScanStages, kStepScanAcc>(sp, 4);   // insert hand-off: warps 4-7
+    // the set-up's first global loads go out before anything else: the rows' lengths for the
+    // balanced plan (below)
+    const bool balanced = kScan && a.B <= kPlanRows && nC >= 2 * a.B;
+    const int ctx_pre = (balanced && (int)threadIdx.x < a.B) ? a.ctx_len[threadIdx.x] : 0;
+    // one allocation of tensor memory for the whole kernel (one CTA per SM holds all 512 columns),
+    // while warps 1 and 2 initialise the barriers
+    if (kTmem && warp == 0) tmem_alloc(&tmem_slot, kTcCols);
+    if (warp == 1 && lane < 7) {
+        mbar_init(lane < 4 ? &mbar[lane] : lane == 4 ? &mbar_q : &mbar_mma[lane - 5], 1);
         mbar_fence_init();
     }
-    // one allocation of tensor memory for the whole kernel (one CTA per SM holds all 512 columns)
-    if (kTmem && warp == 0) tmem_alloc(&tmem_slot, kTcCols);
+    if constexpr (kScan) {
+        if (warp == 2) scan_init_warp<kStepScanStages, kStepScanAcc>(sp, 4, lane);   // insert hand-off: warps 4-7
+    }
     tc_fence_before_sync();
     // Scoring chunks. Balanced plan (up to kPlanRows rows and at least two CTAs per row): from the
     // rows' real page counts n_b (T in all), chunks of P = ceil(T / (grid - B)) pages, ceil(n_b / P)
@@ -213,12 +214,11 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
     // chunk count (also the count its attention units wait for). Otherwise the host's plan: chunks of
     // a.chunk_pages over the page table's width, a.chunks_per_row per row, chunk ci on CTA ci mod grid.
     // (The plan's block barriers also publish the barriers' initialisation.)
-    const bool balanced = kScan && a.B <= kPlanRows && nC >= 2 * a.B;
     int P = a.chunk_pages, C = a.chunks_per_row;
     if (balanced) {
         int nb = 0;
         if ((int)threadIdx.x < a.B) {
-            const int ctx_t = clamp_ctx(a.ctx_len[threadIdx.x], a.Q, a.max_pages, nullptr);
+            const int ctx_t = clamp_ctx(ctx_pre, a.Q, a.max_pages, nullptr);
             nb = (ctx_t + kPage - 1) / kPage;
         }
         const uint32_t tot = sel_block_incl_scan((uint32_t)nb, selsm, 0);
