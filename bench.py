@@ -8,7 +8,9 @@ B = 4 rows x Q = 8 query tokens, 16 query heads on 1 KV head, ragged contexts up
 (1158 to 1695 pages), top-k 128 pages. The metric is achieved HBM GB/s of the algorithmic bytes
 (every index page of each row + the K and V pages of the selected set) per step; microseconds per
 step are reported too. The same line carries `per_config`: the fixed 7-draft verify (2), FP8-KV
-(3) and long-context (4) workloads, each timed the same way.
+(3) and long-context (4) workloads and the verify workload with NVFP4 K/V and index pages (nv2,
+six launches a step), each timed the same way. `--stage index` times the index scorer alone,
+`--reuse` the step of a layer that reuses a selection.
 
 The timed K steps are replayed from one CUDA graph; every step reads a different copy of the
 three page pools, with enough copies that their bytes exceed 3x the L2 cache, so each step reads
@@ -51,8 +53,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="smx", choices=["smx", "reference"])
     ap.add_argument("--config", type=int, default=5)
-    ap.add_argument("--per-config", default="2,3,4",
-                    help="other workloads timed in the same run, reported under per_config ('' for none)")
+    ap.add_argument("--per-config", default="2,3,4,nv2",
+                    help="other workloads timed in the same run, reported under per_config ('' for none; "
+                         "nvN: config N with NVFP4 K/V and index pages)")
     ap.add_argument("--splits", type=int, default=0,
                     help="partitions of the split stage (0 = about two CTAs per SM, at most one page each)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -68,7 +71,7 @@ def parse():
 
 def algorithmic_bytes(w, ctx_len):
     n_pages = [(int(c) + 127) // 128 for c in ctx_len]
-    idx = sum(n * wl.MXFP4_PAGE_BYTES for n in n_pages)
+    idx = sum(n * w.idx_page_bytes for n in n_pages)
     kv = sum(min(w.topk, n) * 2 * w.Hkv * w.kv_page_bytes for n in n_pages)
     return idx, kv
 
@@ -479,18 +482,22 @@ def main():
 
     # ---- the other workloads first (their memory is freed before the headline one) ----
     per_config = {}
-    for n in [int(x) for x in args.per_config.split(",") if x.strip()]:
-        if n == args.config:
+    for tok in [x.strip() for x in args.per_config.split(",") if x.strip()]:
+        nv = tok.startswith("nv")
+        n = int(tok[2:] if nv else tok)
+        if n == args.config and not nv:
             continue
-        p = Prepared(wl.config(n), args, dev, reuse=args.reuse)
+        w_n = wl.nvfp4_variant(wl.config(n)) if nv else wl.config(n)
+        p = Prepared(w_n, args, dev, reuse=args.reuse)
         k = min(args.steps, 100)
         ms_n, _ = time_steps(p, k, max(3, args.warmup), world, dev)
         us_n = ms_n * 1e3 / k
         gbs = whole_job_gbs(p.step_bytes, world, k, ms_n * 1e-3)
-        per_config[str(n)] = {"workload": p.w.name, "us_per_step": us_n, "value": gbs, "unit": "GB/s",
+        per_config[tok] = {"workload": p.w.name, "us_per_step": us_n, "value": gbs, "unit": "GB/s",
                               "roofline_frac": gbs / world / peak, "bytes_per_step": p.step_bytes,
                               "index_bytes": p.idx_b, "kv_bytes": p.kv_b, "num_splits": p.shape.num_splits,
-                              "steps": k, "l2": p.l2_note(), "traffic": recorded_traffic(p.w.name, args.reuse)}
+                              "steps": k, "l2": p.l2_note(), "traffic": recorded_traffic(p.w.name, args.reuse),
+                              "launches_per_step": ops.decode_step_launches(p.shape)}
         del p
         torch.cuda.empty_cache()
 
