@@ -331,12 +331,13 @@ class Prepared:
         self.topk_count = torch.empty((w.B,), dtype=torch.int32, device=dev)
         self.workspace = ops.alloc_workspace(self.shape, dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.reuse = reuse
+        self.reuse = False
         if reuse:
             # an earlier layer's selection: one full step's output, then the reusing layer's step
             self.step(0)
             self.sel_pages, self.sel_count = self.topk_pages.clone(), self.topk_count.clone()
             del self.inp["qidx_bf16"], self.inp["kidx_new"]
+            self.reuse = True
 
     def step(self, i, pt=None, cl=None, io=None, o=None):
         from sparse_attention_decode_mxfp4_gb300 import ops
