@@ -36,6 +36,7 @@
 #include "smx_device.cuh"
 #include "smx_internal.h"
 #include "smx_scan.cuh"
+#include "smx_score.cuh"
 #include "smx_select.cuh"
 
 namespace smx {
@@ -130,7 +131,13 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
     constexpr int NQ = 8 * NT;                   // query slots of the index scan
     constexpr int kStepScanAcc = scan_acc_stages(NQ, 384);   // its accumulator stages (of the 512 columns)
     constexpr bool kScan = !REUSE;               // phase A scans the index cache
-    constexpr bool kTmem = kScan || TC;          // tensor memory: the scan's accumulators, the attention's
+    // the scanner: with the tensor-core attention (long rows, many pages per unit) the tensor-map
+    // scan (smx_scan.cuh), which streams long chunks fastest; with the mma.sync attention the mma.sync
+    // scorer (smx_score.cuh), which starts sooner on the short chunks those shapes give. One scanner
+    // per kernel variant: two in one kernel measured slower on every workload.
+    constexpr bool kScanTma = kScan && TC;
+    constexpr bool kScanMma = kScan && !TC;
+    constexpr bool kTmem = TC;                   // tensor memory: the scan's accumulators, the attention's
     constexpr bool kQImg = TC && !RS && kScan;   // q tiles packed by the scanning CTAs into the workspace
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ int64_t phys_s[kStepMaxChunk];
@@ -169,7 +176,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
         sm = attend_smem(smem, a.page_bytes, mbar, stage_page);
         keys = reinterpret_cast<uint32_t*>(smem);
         sel_all = reinterpret_cast<int*>(sm.raw + 4 * a.page_bytes) + 2 * (a.topk << a.ppb_log2);
-        q_stage = kScan ? smem : sm.raw;   // scanning: the front, ahead of the scan's stages
+        q_stage = sm.raw;   // the page stages (no copy lands there before the attention)
     }
     int* sel = reinterpret_cast<int*>(sm.raw + 4 * a.page_bytes);   // this partition's pages
     int* selph = sel + (a.topk << a.ppb_log2);                       // and their physical ids
@@ -192,10 +199,31 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
         sp.seq = 0;
         sp.ins_seq = 0;
     }
-    // the set-up's first global loads go out before anything else: the rows' lengths for the
-    // balanced plan (below)
-    const bool balanced = kScan && a.B <= kPlanRows && nC >= 2 * a.B;
+    // the set-up's global loads go out before anything waits: the rows' lengths for the balanced
+    // plan (below), then the first attention unit's row length and row of the page table. The
+    // balanced plan is the tensor-map scan's: its long chunks shrink by the rows' raggedness; the
+    // mma.sync scan's short chunks gain less than the plan's round trip costs on rows of equal length.
+    bool balanced = kScanTma && a.B <= kPlanRows && nC >= 2 * a.B;
     const int ctx_pre = (balanced && (int)threadIdx.x < a.B) ? a.ctx_len[threadIdx.x] : 0;
+    const int kv_rows = a.Q * 2 * a.Hkv;
+    const int M = a.G * a.Q;
+    const int n_units = a.B * a.Hkv * a.n_rg * a.S;
+    const int u0 = nC - 1 - c;   // this CTA's first attention unit
+    const int R = a.rows_per_cta;
+    const int ctx_u0 = u0 < n_units ? a.ctx_len[u0 / (a.S * a.n_rg * a.Hkv)] : 0;   // its row length
+    // its row of the page table: loaded into registers now, stored to pt_s once the first chunk's
+    // loads are out (a store right here would hold the warp for the round trip)
+    constexpr int kPtPerThread = kPtCache / (kStepWarps * 32);
+    int32_t pt_r[kPtPerThread];
+    const int n_pt0 = u0 < n_units ? min(a.max_pages, kPtCache) : 0;
+    {
+        const int b = u0 < n_units ? u0 / (a.S * a.n_rg * a.Hkv) : 0;
+#pragma unroll
+        for (int k = 0; k < kPtPerThread; ++k) {
+            const int i = threadIdx.x + k * kStepWarps * 32;
+            pt_r[k] = i < n_pt0 ? a.page_table[(int64_t)b * a.max_pages + i] : 0;
+        }
+    }
     // one allocation of tensor memory for the whole kernel (one CTA per SM holds all 512 columns),
     // while warps 1 and 2 initialise the barriers
     if (kTmem && warp == 0) tmem_alloc(&tmem_slot, kTcCols);
@@ -204,10 +232,42 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
         mbar_fence_init();
     }
     if constexpr (kScan) {
-        if (warp == 2) scan_init_warp<kStepScanStages, kStepScanAcc>(sp, 4, lane);   // insert hand-off: warps 4-7
+        if (kScanTma && warp == 2) scan_init_warp<kStepScanStages, kStepScanAcc>(sp, 4, lane);   // insert hand-off: warps 4-7
+    }
+    // The first unit's q rows: staged into shared memory by bulk copies (the mma.sync path: into the
+    // page stages; a reusing layer on the tensor-core path: into the V and P tiles; both unused until
+    // the attention), issued by the thread that initialised their barrier. The tensor-core path with
+    // a scan packs the q tile images instead (MXFP4), or brings the FP8-KV q rows into L2 with the
+    // evict-last priority, so that the index pages streaming through L2 during the scan, copied
+    // with the evict-first one, leave them there.
+    const bool q_stageable = !(TC && kScan) && (!RS || (reinterpret_cast<uintptr_t>(a.q_bf16) & 15u) == 0);
+    if (TC && kScan && !kQImg && u0 < n_units) {
+        const int rg = (u0 / a.S) % a.n_rg, kvh = (u0 / (a.S * a.n_rg)) % a.Hkv, b = u0 / (a.S * a.n_rg * a.Hkv);
+        const int m_lo = rg * R, rows = min(M, m_lo + R) - m_lo;
+        const int lines = RS ? 2 : 4;   // 128-byte lines of a q row (bf16 or f32)
+        const uint8_t* q = RS ? reinterpret_cast<const uint8_t*>(a.q_bf16) : reinterpret_cast<const uint8_t*>(a.q_f32);
+        for (int li = threadIdx.x; li < rows * lines; li += blockDim.x) {
+            const int m = m_lo + li / lines;
+            const int64_t row = ((int64_t)b * a.Q + m / a.G) * a.Hq + kvh * a.G + m % a.G;
+            prefetch_l2_keep(q + row * (lines * 128) + (li % lines) * 128);
+        }
+    }
+    if (q_stageable && u0 < n_units && warp == 1 && lane == 4) {
+        const int rg = (u0 / a.S) % a.n_rg, kvh = (u0 / (a.S * a.n_rg)) % a.Hkv, b = u0 / (a.S * a.n_rg * a.Hkv);
+        const int m_lo = rg * R, m_hi = min(M, m_lo + R);
+        const uint32_t row_bytes = RS ? kD * 2 : kD * 4;
+        const uint8_t* q = RS ? reinterpret_cast<const uint8_t*>(a.q_bf16) : reinterpret_cast<const uint8_t*>(a.q_f32);
+        mbar_arrive_expect_tx(&mbar_q, (uint32_t)(m_hi - m_lo) * row_bytes);
+        // rows of one draft token are consecutive heads: one copy per token
+        for (int tq = m_lo / a.G; tq * a.G < m_hi; ++tq) {
+            const int r0 = max(m_lo, tq * a.G), r1 = min(m_hi, (tq + 1) * a.G);
+            const int64_t row = ((int64_t)b * a.Q + tq) * a.Hq + kvh * a.G + r0 % a.G;
+            bulk_g2s(q_stage + (r0 - m_lo) * row_bytes, q + row * row_bytes, (uint32_t)(r1 - r0) * row_bytes, &mbar_q);
+        }
     }
     tc_fence_before_sync();
-    // Scoring chunks. Balanced plan (up to kPlanRows rows and at least two CTAs per row): from the
+    // Scoring chunks. Balanced plan (tensor-map scan, up to kPlanRows rows, at least two CTAs per row
+    // and chunks of at most kStepMaxChunk pages): from the
     // rows' real page counts n_b (T in all), chunks of P = ceil(T / (grid - B)) pages, ceil(n_b / P)
     // of them (at least one) for row b -- at most one chunk per CTA, CTA c taking chunk c in row
     // order. Every CTA computes the same plan; plan_c0[b] / plan_cn[b] hold row b's first chunk and
@@ -225,16 +285,22 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
         if (threadIdx.x == blockDim.x - 1) plan_total = (int)tot;
         __syncthreads();
         P = max(1, (plan_total + (nC - a.B) - 1) / (nC - a.B));
-        const int cb = (int)threadIdx.x < a.B ? max(1, (nb + P - 1) / P) : 0;
-        if (threadIdx.x == 0) plan_mine = -1;
-        const uint32_t incl = sel_block_incl_scan((uint32_t)cb, selsm, 1);
-        if ((int)threadIdx.x < a.B) {
-            const int c0 = (int)incl - cb;
-            plan_c0[threadIdx.x] = c0;
-            plan_cn[threadIdx.x] = cb;
-            if (c >= c0 && c < c0 + cb) plan_mine = threadIdx.x;   // the row of this CTA's chunk
+        if (P > kStepMaxChunk) {
+            // chunks longer than the page-table stage: the host's plan (every CTA sees the same total)
+            balanced = false;
+            P = a.chunk_pages;
+        } else {
+            const int cb = (int)threadIdx.x < a.B ? max(1, (nb + P - 1) / P) : 0;
+            if (threadIdx.x == 0) plan_mine = -1;
+            const uint32_t incl = sel_block_incl_scan((uint32_t)cb, selsm, 1);
+            if ((int)threadIdx.x < a.B) {
+                const int c0 = (int)incl - cb;
+                plan_c0[threadIdx.x] = c0;
+                plan_cn[threadIdx.x] = cb;
+                if (c >= c0 && c < c0 + cb) plan_mine = threadIdx.x;   // the row of this CTA's chunk
+            }
+            __syncthreads();
         }
-        __syncthreads();
     } else {
         // the barriers are initialised before any thread polls one: a CTA with no chunk in phase A
         // reaches its attention unit's q wait without another barrier
@@ -242,60 +308,6 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
     }
     // chunks per row b (the count of its row counter)
     auto row_chunks = [&](int b) { return balanced ? plan_cn[b] : C; };
-    const int kv_rows = a.Q * 2 * a.Hkv;
-    const int M = a.G * a.Q;
-    const int n_units = a.B * a.Hkv * a.n_rg * a.S;
-
-    // This CTA's first attention unit: its q rows are staged into shared memory (bulk copies into
-    // the V and P tiles, unused until the attention) and its row of the page table is loaded,
-    // before phase A, so that neither has to be fetched after it.
-    const int u0 = nC - 1 - c;
-    const int R = a.rows_per_cta;
-    // (the tensor-core path's staging area is taken by the scan's stages: there, the first unit's q
-    // rows are brought into L2 with the evict-last priority instead, so that the index pages streaming
-    // through L2 during the scan, copied with the evict-first one, leave them there)
-    const bool q_stageable = !(TC && kScan) && (!RS || (reinterpret_cast<uintptr_t>(a.q_bf16) & 15u) == 0);
-    if (TC && kScan && !kQImg && u0 < n_units) {
-        const int rg = (u0 / a.S) % a.n_rg, kvh = (u0 / (a.S * a.n_rg)) % a.Hkv, b = u0 / (a.S * a.n_rg * a.Hkv);
-        const int m_lo = rg * R, rows = min(M, m_lo + R) - m_lo;
-        const int lines = RS ? 2 : 4;   // 128-byte lines of a q row (bf16 or f32)
-        const uint8_t* q = RS ? reinterpret_cast<const uint8_t*>(a.q_bf16) : reinterpret_cast<const uint8_t*>(a.q_f32);
-        for (int li = threadIdx.x; li < rows * lines; li += blockDim.x) {
-            const int m = m_lo + li / lines;
-            const int64_t row = ((int64_t)b * a.Q + m / a.G) * a.Hq + kvh * a.G + m % a.G;
-            prefetch_l2_keep(q + row * (lines * 128) + (li % lines) * 128);
-        }
-    }
-    if (u0 < n_units) {
-        const int rg = (u0 / a.S) % a.n_rg, kvh = (u0 / (a.S * a.n_rg)) % a.Hkv, b = u0 / (a.S * a.n_rg * a.Hkv);
-        if (q_stageable && threadIdx.x == 0) {
-            const int m_lo = rg * R, m_hi = min(M, m_lo + R);
-            const uint32_t row_bytes = RS ? kD * 2 : kD * 4;
-            const uint8_t* q = RS ? reinterpret_cast<const uint8_t*>(a.q_bf16) : reinterpret_cast<const uint8_t*>(a.q_f32);
-            mbar_arrive_expect_tx(&mbar_q, (uint32_t)(m_hi - m_lo) * row_bytes);
-            // rows of one draft token are consecutive heads: one copy per token
-            for (int tq = m_lo / a.G; tq * a.G < m_hi; ++tq) {
-                const int r0 = max(m_lo, tq * a.G), r1 = min(m_hi, (tq + 1) * a.G);
-                const int64_t row = ((int64_t)b * a.Q + tq) * a.Hq + kvh * a.G + r0 % a.G;
-                bulk_g2s(q_stage + (r0 - m_lo) * row_bytes, q + row * row_bytes, (uint32_t)(r1 - r0) * row_bytes,
-                         &mbar_q);
-            }
-        }
-    }
-    const int ctx_u0 = u0 < n_units ? a.ctx_len[u0 / (a.S * a.n_rg * a.Hkv)] : 0;   // the first unit's row length
-    // the first unit's row of the page table: loaded into registers now, stored to pt_s once the
-    // first chunk's loads are out (a store right here would hold the warp for the round trip)
-    constexpr int kPtPerThread = kPtCache / (kStepWarps * 32);
-    int32_t pt_r[kPtPerThread];
-    const int n_pt0 = u0 < n_units ? min(a.max_pages, kPtCache) : 0;
-    {
-        const int b = u0 < n_units ? u0 / (a.S * a.n_rg * a.Hkv) : 0;
-#pragma unroll
-        for (int k = 0; k < kPtPerThread; ++k) {
-            const int i = threadIdx.x + k * kStepWarps * 32;
-            pt_r[k] = i < n_pt0 ? a.page_table[(int64_t)b * a.max_pages + i] : 0;
-        }
-    }
     bool pt_stored = false;
     auto store_pt = [&]() {
 #pragma unroll
@@ -351,44 +363,56 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
             const int j = balanced ? c - plan_c0[b_bal] : ci % C;
             const int Cb = row_chunks(b);
             const int p0 = j * P, np_max = max(0, min(P, a.max_pages - p0));
-            // independent loads first: the row's length, this chunk's page-table entries and, on the
-            // writing warps (4-7), their first new rows
+            // independent loads first: the row's length, this chunk's page-table entries
             const int ctx_raw = a.ctx_len[b];
             for (int i = threadIdx.x; i < np_max; i += blockDim.x) {
                 const int64_t ph = a.page_table[(int64_t)b * a.max_pages + p0 + i];
                 phys_s[i] = (ph < 0 || ph >= a.n_pool) ? -1 : ph;
             }
-            // the new rows are written by warps 4-7 (w = warp - 4) before they take the scan's epilogue
-            const bool writer = warp >= 4;
-            const int w4 = warp - 4;
-            const int kv_r0 = j + Cb * w4;   // this writing warp's K/V rows: kv_r0, kv_r0 + 4 Cb, ...
-            auto kv_row_src = [&](int r) {
-                const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);   // kind < Hkv: K head, else V head
-                const int64_t tok = (int64_t)b * a.Q + tq;
-                return reinterpret_cast<const float4*>((kind < a.Hkv ? a.k_new : a.v_new) + (tok * a.Hkv + kind % a.Hkv) * kD) + lane;
-            };
-            float4 kidx_x = make_float4(0.f, 0.f, 0.f, 0.f), kv_x = kidx_x;
-            if (writer) {
-                if (w4 < a.Q) kidx_x = reinterpret_cast<const float4*>(a.kidx_new + ((int64_t)b * a.Q + w4) * kD)[lane];
+            if constexpr (kScanMma) {
+                // the mma.sync scorer: all eight warps write the chunk's share of the new rows
+                // (index-K rows on its pages, K/V rows), then score its pages four at a time: warp
+                // 2q + h scores tiles 4h .. 4h + 3 of page i0 + q, the next group's tiles in flight;
+                // the pages that take no new rows are loaded before the inserts. Scratch: the start
+                // of the attention's K tile (free until the attention).
+                const int g = lane >> 2, t = lane & 3;
+                uint32_t(&qh)[16][64] = *reinterpret_cast<uint32_t(*)[16][64]>(smem);
+                int* sig = reinterpret_cast<int*>(smem + 16 * 64 * 4);
+                float(*red)[kStepWarps] = reinterpret_cast<float(*)[kStepWarps]>(smem + 16 * 64 * 4 + 64);
+                const IndexQueryRaw qraw = load_index_query(a.qidx + (int64_t)b * a.Q * kD, a.Q);
+                float4 kidx_x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (warp < a.Q) kidx_x = reinterpret_cast<const float4*>(a.kidx_new + ((int64_t)b * a.Q + warp) * kD)[lane];
+                const int kv_r0 = j + Cb * warp;   // this warp's K/V rows: kv_r0, kv_r0 + 8 Cb, ...
+                auto kv_row_src = [&](int r) {
+                    const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);   // kind < Hkv: K head, else V head
+                    const int64_t tok = (int64_t)b * a.Q + tq;
+                    return reinterpret_cast<const float4*>((kind < a.Hkv ? a.k_new : a.v_new) + (tok * a.Hkv + kind % a.Hkv) * kD) + lane;
+                };
+                float4 kv_x = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (kv_r0 < kv_rows) kv_x = *kv_row_src(kv_r0);
-            }
-            const int ctx = clamp_ctx(ctx_raw, a.Q, a.max_pages, (j == 0 && threadIdx.x == 0) ? a.status : nullptr);
-            const int n_pages = (ctx + kPage - 1) / kPage;
-            const int np = max(0, min(np_max, n_pages - p0));
-            const int first_new = ctx - a.Q;
-            // chunk pages [own_lo, ..) take new index-K rows (positions [lo_new, hi_new))
-            const int lo_new = max(max(first_new, 0), p0 * kPage), hi_new = min(ctx, (p0 + np) * kPage);
-            const bool owner = lo_new < hi_new;
-            const int own_lo = owner ? lo_new / kPage - p0 : np;
-            // phys_s published (the epilogue warps build the row's query pieces inside the scan, while
-            // the first pages are in flight)
-            __syncthreads();
-            if (!pt_stored) store_pt();
-            auto write_rows = [&]() {   // warps 4-7, before the scan's epilogue
+                const int ctx = clamp_ctx(ctx_raw, a.Q, a.max_pages, (j == 0 && threadIdx.x == 0) ? a.status : nullptr);
+                const int n_pages = (ctx + kPage - 1) / kPage;
+                const int np = max(0, min(np_max, n_pages - p0));
+                const int first_new = ctx - a.Q;
+                // chunk pages [own_lo, own_hi) take new index-K rows (positions [lo_new, hi_new))
+                const int lo_new = max(max(first_new, 0), p0 * kPage), hi_new = min(ctx, (p0 + np) * kPage);
+                const bool owner = lo_new < hi_new;
+                const int own_lo = owner ? lo_new / kPage - p0 : np, own_hi = owner ? (hi_new - 1) / kPage - p0 + 1 : np;
+                __syncthreads();   // page-table entries staged (and the barriers initialised)
+                const int pq = warp >> 1, tile0 = (warp & 1) * 4;
+                TileFrag fa[4], fb[4];
+                auto load_page = [&](TileFrag(&f)[4], int i, bool skip_own) {
+                    if (i < np && phys_s[i] >= 0 && !(skip_own && i >= own_lo && i < own_hi)) {
+                        const uint8_t* page = a.idx_pool + phys_s[i] * kMxPageBytes;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) load_tile(f[kk], page, tile0 + kk, g, t);
+                    }
+                };
+                load_page(fa, pq, true);
+                if (!pt_stored) store_pt();
                 if (owner) {
-                    // the new index-K rows on this chunk's pages (one warp per row), before the copiers
-                    // read those pages (they wait for the four writing warps)
-                    for (int tq = w4; tq < a.Q; tq += 4) {
+                    // the new index-K rows on this chunk's pages (one warp per row), then those pages' tiles
+                    for (int tq = warp; tq < a.Q; tq += kStepWarps) {
                         const int pos = first_new + tq;
                         if (pos < lo_new || pos >= hi_new) continue;
                         const int64_t phys = phys_s[pos / kPage - p0];
@@ -396,18 +420,17 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
                             if (lane == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
                             continue;
                         }
-                        const float4 x = tq == w4 ? kidx_x : reinterpret_cast<const float4*>(a.kidx_new + ((int64_t)b * a.Q + tq) * kD)[lane];
+                        const float4 x = tq == warp ? kidx_x : reinterpret_cast<const float4*>(a.kidx_new + ((int64_t)b * a.Q + tq) * kD)[lane];
                         uint8_t* page = a.idx_pool + phys * kMxPageBytes;
                         quant_row_mxfp4_warp(x, page + (pos % kPage) * 64, page + kMxScaleOff + (pos % kPage) * 4, lane);
                     }
-                    fence_proxy_async_global();
                     __threadfence();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(sp.ins);
+                    __syncthreads();
+                    if (pq >= own_lo && pq < own_hi) load_page(fa, pq, false);
                 }
-                // this warp's share of the row's new K/V rows (read only by the attention phase, after
-                // the row's counter)
-                for (int r = kv_r0; r < kv_rows; r += 4 * Cb) {
+                // this warp's new K/V rows (read only by the attention phase, after the row's counter),
+                // while the index tiles are in flight
+                for (int r = kv_r0; r < kv_rows; r += Cb * kStepWarps) {
                     const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);
                     const int pos = first_new + tq;
                     if (pos < 0) continue;
@@ -427,26 +450,130 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
                         quant_row_mxfp4_warp(x, page + slot * 64, page + kMxScaleOff + slot * 4, lane);
                     }
                 }
-                if constexpr (kQImg) {
-                    // this chunk's share of the row's q rows (r = draft token x Hq + head, rows
-                    // j + Cb w4 + 4 Cb k), by the q packing rule into the tensor-core units' q tile
-                    // images: unit row m = token x G + head % G of KV head head / G, row group m / 128,
-                    // in the operand layout the QK MMA reads (published by the row's counter)
-                    const int QH = a.Q * a.Hq;
-                    for (int r = j + Cb * w4; r < QH; r += 4 * Cb) {
-                        const int tq = r / a.Hq, h = r % a.Hq, kvh = h / a.G, m = tq * a.G + h % a.G;
-                        const float4 x = reinterpret_cast<const float4*>(a.q_f32 + ((int64_t)b * QH + r) * kD)[lane];
-                        uint8_t* img = a.q_img + (((int64_t)b * a.Hkv + kvh) * a.n_rg + m / kTcRows) * kQImgBytes;
-                        *reinterpret_cast<uint32_t*>(img + sw128_chunk(m % kTcRows, lane >> 2, kTcRows) + 4 * (lane & 3)) =
-                            pack_q4(x);
+                uint32_t qf[NT][16];
+                int sig_c[NT][2];
+                setup_index_query<NT>(qraw, a.Q, qh, sig, qf, sig_c);
+                const int lim = ctx - a.Q;   // token j counts for query n iff j <= lim + n
+#pragma unroll 1
+                for (int i0 = 0; i0 < np; i0 += 4) {
+                    if (i0 + 4 < np) load_page(fb, i0 + 4 + pq, false);
+                    const int i = i0 + pq;
+                    if (i < np) {
+                        float best = -INFINITY;
+                        if (phys_s[i] >= 0) {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                best = fmaxf(best, score_tile<NT>(fa[kk], qf, sig_c, p0 + i, tile0 + kk, g, t, lim, a.Q));
+                        } else if ((warp & 1) == 0 && lane == 0) {
+                            flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                        }
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
+                        if (lane == 0) red[i % kScanRedPages][warp & 1] = best;
                     }
+                    if ((i0 + 4) % kScanRedPages == 0 || i0 + 4 >= np) {   // page maxima of pages [base, i0 + 4)
+                        __syncthreads();
+                        const int base = (i0 / kScanRedPages) * kScanRedPages;
+                        const int cnt = min(i0 + 4, np) - base;
+                        if ((int)threadIdx.x < cnt)
+                            a.scores[(int64_t)b * a.max_pages + p0 + base + threadIdx.x] =
+                                fmaxf(red[threadIdx.x][0], red[threadIdx.x][1]);
+                        __syncthreads();
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) fa[kk] = fb[kk];
                 }
-            };
-            if (kTmem) sp.tmem = tmem_slot;
-            scan_pages<NQ, kStepScanStages, kStepScanAcc>(sp, &idx_map, phys_s, np, p0, owner ? own_lo : np,
-                                                         ctx - a.Q, a.Q, a.qidx + (int64_t)b * a.Q * kD,
-                                                         a.scores + (int64_t)b * a.max_pages,
-                                                         a.status, write_rows);
+            } else {
+                // the new rows are written by warps 4-7 (w = warp - 4) before they take the scan's epilogue
+                const bool writer = warp >= 4;
+                const int w4 = warp - 4;
+                const int kv_r0 = j + Cb * w4;   // this writing warp's K/V rows: kv_r0, kv_r0 + 4 Cb, ...
+                auto kv_row_src = [&](int r) {
+                    const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);   // kind < Hkv: K head, else V head
+                    const int64_t tok = (int64_t)b * a.Q + tq;
+                    return reinterpret_cast<const float4*>((kind < a.Hkv ? a.k_new : a.v_new) + (tok * a.Hkv + kind % a.Hkv) * kD) + lane;
+                };
+                float4 kidx_x = make_float4(0.f, 0.f, 0.f, 0.f), kv_x = kidx_x;
+                if (writer) {
+                    if (w4 < a.Q) kidx_x = reinterpret_cast<const float4*>(a.kidx_new + ((int64_t)b * a.Q + w4) * kD)[lane];
+                    if (kv_r0 < kv_rows) kv_x = *kv_row_src(kv_r0);
+                }
+                const int ctx = clamp_ctx(ctx_raw, a.Q, a.max_pages, (j == 0 && threadIdx.x == 0) ? a.status : nullptr);
+                const int n_pages = (ctx + kPage - 1) / kPage;
+                const int np = max(0, min(np_max, n_pages - p0));
+                const int first_new = ctx - a.Q;
+                // chunk pages [own_lo, ..) take new index-K rows (positions [lo_new, hi_new))
+                const int lo_new = max(max(first_new, 0), p0 * kPage), hi_new = min(ctx, (p0 + np) * kPage);
+                const bool owner = lo_new < hi_new;
+                const int own_lo = owner ? lo_new / kPage - p0 : np;
+                // phys_s published (the epilogue warps build the row's query pieces inside the scan, while
+                // the first pages are in flight)
+                __syncthreads();
+                if (!pt_stored) store_pt();
+                auto write_rows = [&]() {   // warps 4-7, before the scan's epilogue
+                    if (owner) {
+                        // the new index-K rows on this chunk's pages (one warp per row), before the copiers
+                        // read those pages (they wait for the four writing warps)
+                        for (int tq = w4; tq < a.Q; tq += 4) {
+                            const int pos = first_new + tq;
+                            if (pos < lo_new || pos >= hi_new) continue;
+                            const int64_t phys = phys_s[pos / kPage - p0];
+                            if (phys < 0) {
+                                if (lane == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                                continue;
+                            }
+                            const float4 x = tq == w4 ? kidx_x : reinterpret_cast<const float4*>(a.kidx_new + ((int64_t)b * a.Q + tq) * kD)[lane];
+                            uint8_t* page = a.idx_pool + phys * kMxPageBytes;
+                            quant_row_mxfp4_warp(x, page + (pos % kPage) * 64, page + kMxScaleOff + (pos % kPage) * 4, lane);
+                        }
+                        fence_proxy_async_global();
+                        __threadfence();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(sp.ins);
+                    }
+                    // this warp's share of the row's new K/V rows (read only by the attention phase, after
+                    // the row's counter)
+                    for (int r = kv_r0; r < kv_rows; r += 4 * Cb) {
+                        const int tq = r / (2 * a.Hkv), kind = r % (2 * a.Hkv);
+                        const int pos = first_new + tq;
+                        if (pos < 0) continue;
+                        const float4 x = r == kv_r0 ? kv_x : *kv_row_src(r);
+                        const int64_t phys = a.page_table[(int64_t)b * a.max_pages + pos / kPage];
+                        if (phys < 0 || phys >= a.n_pool) {
+                            if (lane == 0) flag_status(a.status, SMX_DEV_BAD_PAGE_ID);
+                            continue;
+                        }
+                        const int h = kind % a.Hkv, slot = pos % kPage;
+                        uint8_t* pool = kind < a.Hkv ? a.k_pool : a.v_pool;
+                        if (RS) {
+                            uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kRsPageBytes;
+                            quant_row_e4m3rs_warp(x, page + slot * 128, reinterpret_cast<float*>(page + kRsScaleOff) + slot, lane);
+                        } else {
+                            uint8_t* page = pool + (phys * a.Hkv + h) * (int64_t)kMxPageBytes;
+                            quant_row_mxfp4_warp(x, page + slot * 64, page + kMxScaleOff + slot * 4, lane);
+                        }
+                    }
+                    if constexpr (kQImg) {
+                        // this chunk's share of the row's q rows (r = draft token x Hq + head, rows
+                        // j + Cb w4 + 4 Cb k), by the q packing rule into the tensor-core units' q tile
+                        // images: unit row m = token x G + head % G of KV head head / G, row group m / 128,
+                        // in the operand layout the QK MMA reads (published by the row's counter)
+                        const int QH = a.Q * a.Hq;
+                        for (int r = j + Cb * w4; r < QH; r += 4 * Cb) {
+                            const int tq = r / a.Hq, h = r % a.Hq, kvh = h / a.G, m = tq * a.G + h % a.G;
+                            const float4 x = reinterpret_cast<const float4*>(a.q_f32 + ((int64_t)b * QH + r) * kD)[lane];
+                            uint8_t* img = a.q_img + (((int64_t)b * a.Hkv + kvh) * a.n_rg + m / kTcRows) * kQImgBytes;
+                            *reinterpret_cast<uint32_t*>(img + sw128_chunk(m % kTcRows, lane >> 2, kTcRows) + 4 * (lane & 3)) =
+                                pack_q4(x);
+                        }
+                    }
+                };
+                if (kTmem) sp.tmem = tmem_slot;
+                scan_pages<NQ, kStepScanStages, kStepScanAcc>(sp, &idx_map, phys_s, np, p0, owner ? own_lo : np,
+                                                             ctx - a.Q, a.Q, a.qidx + (int64_t)b * a.Q * kD,
+                                                             a.scores + (int64_t)b * a.max_pages,
+                                                             a.status, write_rows);
+            }
             __syncthreads();
             if (threadIdx.x == 0) red_release_add(&a.row_cnt[kCounterStride * b], 1u);
         }
@@ -722,16 +849,6 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
         }
     }
 
-    // the scan's tensor memory (the tensor-core path freed its allocation after the attention)
-    if constexpr (kTmem && !TC) {
-        tc_fence_before_sync();
-        __syncthreads();
-        if (warp == 0) {
-            tc_fence_after_sync();
-            tmem_dealloc(tmem_slot, kTcCols);
-        }
-    }
-
     // ---------------- D. the last CTA out clears the counters ----------------
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -771,9 +888,9 @@ StepGeom step_geom(const smx_shape_t& s, bool tc) {
     const size_t ppb = s.pages_per_block > 1 ? (size_t)s.pages_per_block : 1;
     g.smem = tc ? attend_tc_smem_bytes(g.page_bytes) + 8 * ppb * (size_t)s.topk
                 : attend_smem_bytes(g.page_bytes) + (8 * ppb + 4) * (size_t)s.topk;
-    // the index scan's stages share the space (plus slack to align them to 1 KB)
+    // the tensor-core path's index scan shares the space (plus slack to align it to 1 KB)
     const size_t scan = (size_t)kStepQFront + scan_smem_bytes(kStepScanStages, scan_acc_stages(8, 384)) + 1024;
-    if (g.smem < scan) g.smem = scan;
+    if (tc && g.smem < scan) g.smem = scan;
     // counters for the larger (mma.sync) group count, so the workspace does not depend on the path
     const int rg64 = (M + unit_rows(s, false) - 1) / unit_rows(s, false);
     g.n_counters = kCounterStride * ((size_t)s.B + (size_t)s.B * s.Hkv * rg64 + 1);

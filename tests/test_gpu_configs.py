@@ -77,6 +77,11 @@ MAX_SIZE = [
     # the same row in blocks of 4 pages: 1024 blocks = 4096 pages
     wl.Workload("max_blocks_b1_q8_h16_ctx2097152_k1024x4", B=1, Q=8, Hq=16, Hkv=1, max_ctx=2097152, topk=1024,
                 num_splits=1, seed=920, pages_per_block=4),
+    # four rows of 9728 pages: spread over the grid's scoring CTAs a chunk would be 263 pages, more
+    # than a chunk's page-table stage holds (256), so the step takes the fixed plan of 256-page
+    # chunks, several per CTA
+    wl.Workload("long_rows_b4_q8_h16_ctx1245184_k64", B=4, Q=8, Hq=16, Hkv=1, max_ctx=1245184, topk=64,
+                num_splits=1, seed=921),
 ]
 
 
@@ -84,7 +89,10 @@ MAX_SIZE = [
 def test_maximum_sizes(w, quick):
     if quick:
         pytest.skip("--quick leaves out the 2M-token rows")
-    assert w.max_pages == 16384 and w.topk * w.pages_per_block == 4096
+    if w.B == 1:
+        assert w.max_pages == 16384 and w.topk * w.pages_per_block == 4096
+    else:
+        assert w.B * w.max_pages > 256 * (152 - w.B)
     C.full_step_parity(w, num_splits=bench_splits(w))
 
 
