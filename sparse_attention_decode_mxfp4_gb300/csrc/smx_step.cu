@@ -199,6 +199,20 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
         sp.seq = 0;
         sp.ins_seq = 0;
     }
+    // one allocation of tensor memory for the whole kernel (one CTA per SM holds all 512 columns),
+    // while warps 1 and 2 initialise the barriers: on-chip set-up that may run while the stream's
+    // previous kernel finishes (the launch allows it to start early, programmatic dependent
+    // launch); every global access comes after the wait for that kernel's completion
+    if (kTmem && warp == 0) tmem_alloc(&tmem_slot, kTcCols);
+    if (warp == 1 && lane < 7) {
+        mbar_init(lane < 4 ? &mbar[lane] : lane == 4 ? &mbar_q : &mbar_mma[lane - 5], 1);
+        mbar_fence_init();
+    }
+    if constexpr (kScan) {
+        if (kScanTma && warp == 2) scan_init_warp<kStepScanStages, kStepScanAcc>(sp, 4, lane);   // insert hand-off: warps 4-7
+    }
+    pdl_wait();
+    pdl_trigger();   // the next step may begin its own set-up once SMs free up
     // the set-up's global loads go out before anything waits: the rows' lengths for the balanced
     // plan (below), then the first attention unit's row length and row of the page table. The
     // balanced plan is the tensor-map scan's: its long chunks shrink by the rows' raggedness; the
@@ -223,16 +237,6 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
             const int i = threadIdx.x + k * kStepWarps * 32;
             pt_r[k] = i < n_pt0 ? a.page_table[(int64_t)b * a.max_pages + i] : 0;
         }
-    }
-    // one allocation of tensor memory for the whole kernel (one CTA per SM holds all 512 columns),
-    // while warps 1 and 2 initialise the barriers
-    if (kTmem && warp == 0) tmem_alloc(&tmem_slot, kTcCols);
-    if (warp == 1 && lane < 7) {
-        mbar_init(lane < 4 ? &mbar[lane] : lane == 4 ? &mbar_q : &mbar_mma[lane - 5], 1);
-        mbar_fence_init();
-    }
-    if constexpr (kScan) {
-        if (kScanTma && warp == 2) scan_init_warp<kStepScanStages, kStepScanAcc>(sp, 4, lane);   // insert hand-off: warps 4-7
     }
     // The first unit's q rows: staged into shared memory by bulk copies (the mma.sync path: into the
     // page stages; a reusing layer on the tensor-core path: into the V and P tiles; both unused until
@@ -965,12 +969,25 @@ static cudaError_t launch_step_kernel(const void* fn, int n_ctas, size_t smem, c
     cfg.blockDim = dim3(kStepWarps * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    // programmatic dependent launch: the kernel's on-chip set-up may overlap the previous kernel's
+    // tail; it waits for that kernel's completion before its first global access
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, reinterpret_cast<void (*)(StepArgs, CUtensorMap)>(const_cast<void*>(fn)), a, map);
+    static bool pdl_ok = true;   // cleared if the runtime refuses the pair of attributes
+    cfg.numAttrs = pdl_ok ? 2 : 1;
+    auto kernel = reinterpret_cast<void (*)(StepArgs, CUtensorMap)>(const_cast<void*>(fn));
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, map);
+    if (e != cudaSuccess && pdl_ok && e != cudaErrorStreamCaptureInvalidated && e != cudaErrorStreamCaptureUnsupported) {
+        (void)cudaGetLastError();
+        pdl_ok = false;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kernel, a, map);
+    }
+    return e;
 }
 
 cudaError_t launch_decode_step(const smx_shape_t& s, const StepIO& io, cudaStream_t st, bool reuse) {
