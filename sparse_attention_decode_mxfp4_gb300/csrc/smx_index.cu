@@ -44,7 +44,7 @@ struct IdxScanShape {
     static constexpr int kTmemCols = 512 / kCtasPerSm;
     static constexpr int kAcc = scan_acc_stages(NQ, kTmemCols);
     // dynamic shared memory: the stages and query pieces, plus slack to align them to 1 KB
-    static constexpr int kSmemBytes = scan_smem_bytes(kStages, kAcc) + 1024;
+    static constexpr int kSmemBytes = scan_smem_bytes(kStages, kAcc, NQ) + 1024;
 };
 
 // Grid (CTAs per row, B), 256 threads: the CTA scans its range of the row's pages with the
@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(256, IdxScanShape<NQ>::kCtasPerSm)
     ScanPipe sp;
     sp.tiles = base;
     sp.qt = base + kIdxStages * kScanTileBytes;
-    sp.ring = sp.qt + kScQueryBytes;
+    sp.ring = sp.qt + scan_query_bytes(NQ);
     scan_bind<kIdxStages, SA>(sp, bars);
     sp.red = red;
     sp.gmax = gmax;

@@ -44,7 +44,10 @@
 
 namespace smx {
 
-constexpr int kScQueryBytes = 32 * 128;   // the query pieces: up to 32 rows (two pieces x 16 query slots)
+// The query pieces of NQ query slots: rows [0, NQ) the high pieces, [NQ, 2 NQ) the low pieces,
+// [2 NQ, 3 NQ) zero (so that rows [NQ, 3 NQ) are a second N = 2 NQ operand whose first NQ rows are
+// the low pieces); at least 32 rows.
+__host__ __device__ constexpr int scan_query_bytes(int nq) { return (3 * nq > 32 ? 3 * nq : 32) * 128; }
 
 // Byte offset of 16-byte chunk c of row r of a K-major tile with the 128-byte swizzle (8-row atoms
 // of 1024 bytes).
@@ -63,10 +66,10 @@ constexpr int kScanScaleBytes = 512;              // one page's scale words in t
 // 2 NQ columns a stage).
 __host__ __device__ constexpr int scan_acc_stages(int nq, int cols) { return cols / (8 * nq); }
 
-// Shared-memory bytes of a scan with `stages` page stages (then the query pieces and the scale
-// ring of `sa` pages), from a 1024-byte-aligned base.
-__host__ __device__ constexpr int scan_smem_bytes(int stages, int sa) {
-    return stages * kScanTileBytes + kScQueryBytes + sa * kScanScaleBytes;
+// Shared-memory bytes of a scan of NQ query slots with `stages` page stages (then the query
+// pieces and the scale ring of `sa` pages), from a 1024-byte-aligned base.
+__host__ __device__ constexpr int scan_smem_bytes(int stages, int sa, int nq) {
+    return stages * kScanTileBytes + scan_query_bytes(nq) + sa * kScanScaleBytes;
 }
 
 struct ScanPipe {
@@ -166,38 +169,37 @@ __host__ __device__ constexpr uint32_t idesc_scan(int N) {
     return (1u << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
 
-// 2 NQ consecutive fp32 columns of this thread's lane (no wait).
+// NQ consecutive fp32 columns of this thread's lane (no wait).
 template <int NQ>
-__device__ __forceinline__ void scan_ld(uint32_t taddr, uint32_t (&r)[2 * NQ]) {
+__device__ __forceinline__ void scan_ld(uint32_t taddr, uint32_t (&r)[NQ]) {
     if constexpr (NQ == 8) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                     : "r"(taddr)
+                     : "memory");
+    } else {
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
             : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
               "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
             : "r"(taddr)
             : "memory");
-    } else {
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-              "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-              "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-            : "r"(taddr)
-            : "memory");
     }
 }
 
 // A token's score for one page from its scale word and its four group accumulators (group g at
-// columns taddr + 2 NQ g: piece 0 in column n, piece 1 in NQ + n): with x_g = e_g - sigma_g and
-// X = max_g x_g, t_n = sum_g 2^(x_g - X) (D_g[n] + D_g[NQ + n]) (weights exact powers of two, at
-// most 1; a group more than 2^126 below the largest is dropped) and the score is the max over
-// queries n < Q with j <= lim + n of t_n, times 2^(X - 127): -inf if no query counts, NaN if a
-// group scale is NaN. Loads the accumulators in rounds of 32 columns and waits for them.
+// columns taddr + 2 NQ g; column n holds D_g[n], the high and the low query piece of query n
+// summed by the two MMAs): with x_g = e_g - sigma_g and X = max_g x_g,
+// t_n = sum_g 2^(x_g - X) D_g[n] (weights exact powers of two, at most 1; a group more than 2^126
+// below the largest is dropped) and the score is the max over queries n < Q with j <= lim + n of
+// t_n, times 2^(X - 127): -inf if no query counts, NaN if a group scale is NaN. One wait for the
+// four groups' loads.
 template <int NQ>
 __device__ __forceinline__ float scan_token_score(uint32_t taddr, uint32_t sw, const int (&sig)[4], int j, int lim,
                                                   int Q) {
+    uint32_t r[4][NQ];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) scan_ld<NQ>(taddr + (uint32_t)(g * 2 * NQ), r[g]);
     int x[4];
     int X = -1000;
     bool nan = false;
@@ -214,21 +216,13 @@ __device__ __forceinline__ float scan_token_score(uint32_t taddr, uint32_t sw, c
         const int d = x[g] - X;   // <= 0
         f[g] = d >= -126 ? __uint_as_float((uint32_t)(d + 127) << 23) : 0.0f;
     }
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
     float t[NQ];
-    constexpr int GPR = NQ == 8 ? 2 : 1;   // groups per load round (32 columns)
 #pragma unroll
-    for (int h = 0; h < 4; h += GPR) {
-        uint32_t r[GPR][2 * NQ];
+    for (int n = 0; n < NQ; ++n) {
+        t[n] = f[0] * __uint_as_float(r[0][n]);
 #pragma unroll
-        for (int k = 0; k < GPR; ++k) scan_ld<NQ>(taddr + (uint32_t)((h + k) * 2 * NQ), r[k]);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-        for (int k = 0; k < GPR; ++k)
-#pragma unroll
-            for (int n = 0; n < NQ; ++n) {
-                const float a = __uint_as_float(r[k][n]) + __uint_as_float(r[k][NQ + n]);
-                t[n] = (h + k == 0) ? f[0] * a : fmaf(f[h + k], a, t[n]);
-            }
+        for (int g = 1; g < 4; ++g) t[n] = fmaf(f[g], __uint_as_float(r[g][n]), t[n]);
     }
     float best = -INFINITY;
 #pragma unroll
@@ -327,6 +321,7 @@ __device__ __forceinline__ void scan_setup_query(const ScanPipe& sp, const uint1
         }
         *reinterpret_cast<uint2*>(sp.qt + sc_chunk(n, c8 >> 1) + 8 * (c8 & 1)) = make_uint2(b0[0], b0[1]);
         *reinterpret_cast<uint2*>(sp.qt + sc_chunk(NQ + n, c8 >> 1) + 8 * (c8 & 1)) = make_uint2(b1[0], b1[1]);
+        *reinterpret_cast<uint2*>(sp.qt + sc_chunk(2 * NQ + n, c8 >> 1) + 8 * (c8 & 1)) = make_uint2(0u, 0u);
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -390,14 +385,20 @@ __device__ __forceinline__ void scan_pages(ScanPipe& sp, const CUtensorMap* map,
                 if (ok && phys[i] >= 0 && !*(volatile int*)sp.gave_up) {
                     const uint32_t tile_s = smem_u32(sp.tiles + st * kScanTileBytes);
                     const uint32_t d = sp.tmem + as * 4 * N;
+                    // per group two MMAs into one accumulator: B = query rows [0, N) (high pieces,
+                    // then low), then rows [NQ, NQ + N) (low pieces, then zeros), so that column n <
+                    // NQ sums both pieces of query n (columns NQ.. are not read)
 #pragma unroll
                     for (int gg = 0; gg < 4; ++gg) {
                         const uint64_t ad = sw128_desc(tile_s + 32 * gg);
-                        const uint64_t bd = sw128_desc(qt_s + 32 * gg);
-                        asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
-                                     " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d + gg * N),
-                                     "l"(ad), "l"(bd), "r"(idesc), "r"(0u)
-                                     : "memory");
+#pragma unroll
+                        for (int pc = 0; pc < 2; ++pc) {
+                            const uint64_t bd = sw128_desc(qt_s + pc * NQ * 128 + 32 * gg);
+                            asm volatile("{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+                                         " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d + gg * N),
+                                         "l"(ad), "l"(bd), "r"(idesc), "r"((uint32_t)pc)
+                                         : "memory");
+                        }
                     }
                 }
                 tc_commit(&sp.afull[as]);

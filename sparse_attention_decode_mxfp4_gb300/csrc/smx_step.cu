@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kStepWarps * 32, 1) decode_step_kernel(const S
         uint8_t* base = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u) + kStepQFront;
         sp.tiles = base;
         sp.qt = base + kStepScanStages * kScanTileBytes;
-        sp.ring = sp.qt + kScQueryBytes;
+        sp.ring = sp.qt + scan_query_bytes(NQ);
         scan_bind<kStepScanStages, kStepScanAcc>(sp, scan_bars);
         sp.red = scan_red;
         sp.gmax = gmax;
@@ -893,7 +893,8 @@ StepGeom step_geom(const smx_shape_t& s, bool tc) {
     g.smem = tc ? attend_tc_smem_bytes(g.page_bytes) + 8 * ppb * (size_t)s.topk
                 : attend_smem_bytes(g.page_bytes) + (8 * ppb + 4) * (size_t)s.topk;
     // the tensor-core path's index scan shares the space (plus slack to align it to 1 KB)
-    const size_t scan = (size_t)kStepQFront + scan_smem_bytes(kStepScanStages, scan_acc_stages(8, 384)) + 1024;
+    const int nq = s.Q > 8 ? 16 : 8;
+    const size_t scan = (size_t)kStepQFront + scan_smem_bytes(kStepScanStages, scan_acc_stages(nq, 384), nq) + 1024;
     if (tc && g.smem < scan) g.smem = scan;
     // counters for the larger (mma.sync) group count, so the workspace does not depend on the path
     const int rg64 = (M + unit_rows(s, false) - 1) / unit_rows(s, false);
