@@ -214,7 +214,10 @@ int smx_sparse_attn_merge(const smx_shape_t* shape, const float* part_o, const f
  * most one CTA per SM: inserts, q packing and page scores; then per attention unit the row's
  * selection, the split stage over one partition and the merge of a slice of rows, the phases
  * ordered by counters in the workspace (bounded waits: SMX_DEV_TIMEOUT in dev_status if one gives
- * up). Calls that share a workspace must not overlap on the GPU. */
+ * up). Calls that share a workspace must not overlap on the GPU. The kernel is launched with
+ * programmatic dependent launch: its CTAs may start their on-chip set-up while the previous kernel
+ * on `stream` finishes, and wait for that kernel's completion before their first global access,
+ * so stream order holds for every input and output. */
 int smx_decode_step(const smx_shape_t* shape, const float* q_f32, const uint16_t* q_bf16,
                     const uint16_t* qidx_bf16, const float* k_new, const float* v_new,
                     const float* kidx_new, const int32_t* page_table, const int32_t* ctx_len,
